@@ -1,0 +1,189 @@
+"""Seeded synthetic inputs: model weights, log-mel streams, start offsets, resets.
+
+This module is the only code shared by the oracle's tests and the CUDA path's
+tests; it holds none of the encoder's arithmetic.  Every value comes from one
+counter-based generator so that any tensor element can be regenerated alone:
+
+    splitmix64(z):  z += 0x9E3779B97F4A7C15
+                    z  = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9
+                    z  = (z ^ (z >> 27)) * 0x94D049BB133111EB
+                    return z ^ (z >> 31)                       (all mod 2^64)
+    key(seed, tid)  = splitmix64(splitmix64(seed) ^ tid)
+    bits(key, i)    = splitmix64(key + i)
+    uniform(key, i) = (bits(key, i) >> 11) * 2^-53             in [0, 1)
+    normal(key, i)  = sqrt(-2 ln(1 - uniform(key, 2i))) * cos(2 pi uniform(key, 2i + 1))
+
+Weights (seed 0 by default) follow the synthetic init of the workloads:
+Xavier-normal linears and convolutions (std = sqrt(2 / (fan_in + fan_out)),
+fan = channels x taps for convolutions, 9 / 9 for the depthwise kernel), LayerNorm
+and folded-BatchNorm gains uniform on [0.9, 1.1], every bias, LayerNorm/BatchNorm
+shift and the positional biases pos_bias_u / pos_bias_v ~ N(0, 0.02^2).  In bf16
+configurations every parameter is rounded to the nearest bf16 value (ties to
+even) here, so the device copy is exact and the oracle sees the same numbers.
+
+Log-mel (seed 1000 + stream id) is N(0, 1) with near-silence spans N(-4, 0.3^2);
+span lengths are uniform on 30..200 mel frames and spans are placed until they
+cover the requested fraction of frames.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .config import ModelConfig, DTYPE_BF16
+
+_M64 = np.uint64(0xFFFFFFFFFFFFFFFF)
+_GOLD = np.uint64(0x9E3779B97F4A7C15)
+_C1 = np.uint64(0xBF58476D1CE4E5B9)
+_C2 = np.uint64(0x94D049BB133111EB)
+
+TID_MEL = 1 << 20
+TID_SPANS = (1 << 20) + 1
+TID_OFFSETS = (1 << 20) + 2
+TID_RESETS = (1 << 20) + 3
+
+
+def splitmix64(z):
+    z = np.asarray(z, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = z + _GOLD
+        z = (z ^ (z >> np.uint64(30))) * _C1
+        z = (z ^ (z >> np.uint64(27))) * _C2
+    return z ^ (z >> np.uint64(31))
+
+
+def key(seed: int, tid: int) -> np.uint64:
+    return splitmix64(splitmix64(np.uint64(seed)) ^ np.uint64(tid))
+
+
+def uniform(k: np.uint64, idx: np.ndarray) -> np.ndarray:
+    with np.errstate(over="ignore"):
+        b = splitmix64(np.uint64(k) + np.asarray(idx, dtype=np.uint64))
+    return (b >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+
+def normal(k: np.uint64, n: int, start: int = 0) -> np.ndarray:
+    i = np.arange(start, start + n, dtype=np.uint64)
+    u1 = uniform(k, 2 * i)
+    u2 = uniform(k, 2 * i + np.uint64(1))
+    return np.sqrt(-2.0 * np.log1p(-u1)) * np.cos(2.0 * np.pi * u2)
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bf16 (ties to even), kept as float32."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return (b << np.uint64(16)).astype(np.uint32).view(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# Weight layout.  All linears are stored [out, in]; the subsampling
+# convolutions [out, tap, in]; the depthwise kernel [channel, tap].
+# ---------------------------------------------------------------------------
+
+def weight_layout(cfg: ModelConfig):
+    """Ordered (name, shape, kind) list; the flat blob is their concatenation.
+
+    kind: ("xavier", fan_in, fan_out) | "gain" | "bias".
+    """
+    D, F, M, J, K, H = cfg.d_model, cfg.ff_dim, cfg.mel_bins, cfg.joint_dim, cfg.dw_kernel, cfg.n_heads
+    HD = D // H
+    L = []
+    L += [("sub.w1", (D, 3, M), ("xavier", 3 * M, 3 * D)), ("sub.b1", (D,), "bias"),
+          ("sub.w2", (D, 3, D), ("xavier", 3 * D, 3 * D)), ("sub.b2", (D,), "bias"),
+          ("sub.w3", (D, 3, D), ("xavier", 3 * D, 3 * D)), ("sub.b3", (D,), "bias"),
+          ("sub.wo", (D, D), ("xavier", D, D)), ("sub.bo", (D,), "bias")]
+    for l in range(cfg.n_layers):
+        p = f"l{l}."
+        L += [(p + "ff1.ln_g", (D,), "gain"), (p + "ff1.ln_b", (D,), "bias"),
+              (p + "ff1.w1", (F, D), ("xavier", D, F)), (p + "ff1.b1", (F,), "bias"),
+              (p + "ff1.w2", (D, F), ("xavier", F, D)), (p + "ff1.b2", (D,), "bias")]
+        L += [(p + "att.ln_g", (D,), "gain"), (p + "att.ln_b", (D,), "bias"),
+              (p + "att.wq", (D, D), ("xavier", D, D)), (p + "att.bq", (D,), "bias"),
+              (p + "att.wk", (D, D), ("xavier", D, D)), (p + "att.bk", (D,), "bias"),
+              (p + "att.wv", (D, D), ("xavier", D, D)), (p + "att.bv", (D,), "bias"),
+              (p + "att.wo", (D, D), ("xavier", D, D)), (p + "att.bo", (D,), "bias"),
+              (p + "att.wpos", (D, D), ("xavier", D, D)),
+              (p + "att.pbu", (H, HD), "bias"), (p + "att.pbv", (H, HD), "bias")]
+        L += [(p + "conv.ln_g", (D,), "gain"), (p + "conv.ln_b", (D,), "bias"),
+              (p + "conv.w_pw1", (2 * D, D), ("xavier", D, 2 * D)), (p + "conv.b_pw1", (2 * D,), "bias"),
+              (p + "conv.w_dw", (D, K), ("xavier", K, K)), (p + "conv.b_dw", (D,), "bias"),
+              (p + "conv.bn_g", (D,), "gain"), (p + "conv.bn_b", (D,), "bias"),
+              (p + "conv.w_pw2", (D, D), ("xavier", D, D)), (p + "conv.b_pw2", (D,), "bias")]
+        L += [(p + "ff2.ln_g", (D,), "gain"), (p + "ff2.ln_b", (D,), "bias"),
+              (p + "ff2.w1", (F, D), ("xavier", D, F)), (p + "ff2.b1", (F,), "bias"),
+              (p + "ff2.w2", (D, F), ("xavier", F, D)), (p + "ff2.b2", (D,), "bias")]
+        L += [(p + "out.ln_g", (D,), "gain"), (p + "out.ln_b", (D,), "bias")]
+    L += [("joint.w", (J, D), ("xavier", D, J)), ("joint.b", (J,), "bias")]
+    return L
+
+
+def weights_size(cfg: ModelConfig) -> int:
+    return int(sum(np.prod(s) for _, s, _ in weight_layout(cfg)))
+
+
+def make_weights(cfg: ModelConfig, seed: int = 0) -> dict:
+    """Named float32 parameter arrays (bf16-representable in bf16 configurations)."""
+    out = {}
+    for tid, (name, shape, kind) in enumerate(weight_layout(cfg)):
+        n = int(np.prod(shape))
+        k = key(seed, tid)
+        if kind == "gain":
+            v = 0.9 + 0.2 * uniform(k, np.arange(n, dtype=np.uint64))
+        elif kind == "bias":
+            v = 0.02 * normal(k, n)
+        else:
+            _, fi, fo = kind
+            v = np.sqrt(2.0 / (fi + fo)) * normal(k, n)
+        v = v.astype(np.float32).reshape(shape)
+        if cfg.dtype == DTYPE_BF16:
+            v = round_bf16(v).reshape(shape)
+        out[name] = v
+    return out
+
+
+def pack_weights(cfg: ModelConfig, w: dict) -> np.ndarray:
+    """Flat float32 blob in weight_layout order (the C library's input format)."""
+    parts = []
+    for name, shape, _ in weight_layout(cfg):
+        a = np.asarray(w[name], dtype=np.float32)
+        assert a.shape == tuple(shape), (name, a.shape, shape)
+        parts.append(a.reshape(-1))
+    return np.ascontiguousarray(np.concatenate(parts))
+
+
+def make_mel(n_frames: int, stream_id: int, mel_bins: int = 128, silence_frac: float = 0.2,
+             seed_base: int = 1000) -> np.ndarray:
+    """[n_frames, mel_bins] float32 synthetic log-mel with near-silence spans."""
+    seed = seed_base + stream_id
+    x = normal(key(seed, TID_MEL), n_frames * mel_bins).reshape(n_frames, mel_bins)
+    silent = np.zeros(n_frames, dtype=bool)
+    target = int(round(silence_frac * n_frames))
+    ks = key(seed, TID_SPANS)
+    draw = 0
+    while silent.sum() < target and draw < 4 * n_frames + 8:
+        u = uniform(ks, np.array([draw, draw + 1], dtype=np.uint64))
+        draw += 2
+        length = 30 + int(u[0] * 171)
+        start = int(u[1] * max(1, n_frames - length + 1))
+        silent[start:start + length] = True
+    ksil = key(seed, TID_MEL + 7)
+    quiet = -4.0 + 0.3 * normal(ksil, n_frames * mel_bins).reshape(n_frames, mel_bins)
+    x = np.where(silent[:, None], quiet, x)
+    return x.astype(np.float32)
+
+
+def start_offsets(n_streams: int, max_offset: int, seed: int = 7) -> np.ndarray:
+    """Even start offsets in subsampled frames: 2 * floor(u / 2), u uniform on 0..max_offset-1."""
+    if max_offset <= 0:
+        return np.zeros(n_streams, dtype=np.int64)
+    u = uniform(key(seed, TID_OFFSETS), np.arange(n_streams, dtype=np.uint64))
+    raw = np.floor(u * max_offset).astype(np.int64)
+    return 2 * (raw // 2)
+
+
+def reset_mask(n_streams: int, step: int, prob: float, seed: int = 11) -> np.ndarray:
+    """Streams that reset before push `step` (independent Bernoulli(prob) per stream and step)."""
+    if prob <= 0:
+        return np.zeros(n_streams, dtype=bool)
+    idx = np.arange(n_streams, dtype=np.uint64) * np.uint64(1 << 32) + np.uint64(step)
+    return uniform(key(seed, TID_RESETS), idx) < prob
