@@ -1,0 +1,1234 @@
+// Host engine of the cache-aware Conformer library: weight upload, per-stream
+// GPU-resident state pools, the step planner that turns one push of many
+// streams into a fixed sequence of kernel launches (optionally replayed from a
+// CUDA graph), flush, the offline chunked-causal encode, state export/import,
+// and the extern "C" entry points declared in include/cac.h.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <new>
+#include <tuple>
+#include <vector>
+
+#include "gemm.cuh"
+#include "kernels.cuh"
+
+using namespace cac;
+
+namespace {
+
+constexpr int MEL = 128;
+constexpr int TAIL = 14;
+constexpr int CONV_CACHE = 8;
+constexpr int N_TAPS = 7;  // per-layer trace taps; tap 7 = subsampled input
+
+uint16_t f2bf(float f) {
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0;
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+float bf2f(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    std::memcpy(&f, &u, 4);
+    return f;
+}
+
+#define CK(call)                                                                          \
+    do {                                                                                  \
+        cudaError_t e_ = (call);                                                          \
+        if (e_ != cudaSuccess) {                                                          \
+            std::fprintf(stderr, "cac: %s failed: %s\n", #call, cudaGetErrorString(e_)); \
+            return CAC_E_CUDA;                                                            \
+        }                                                                                 \
+    } while (0)
+
+#define RET(call)                    \
+    do {                             \
+        int r_ = (call);             \
+        if (r_ != CAC_OK) return r_; \
+    } while (0)
+
+struct Lin {
+    void* w = nullptr;   // [N][K] bf16 or fp32
+    float* b = nullptr;  // [N] or null
+    int N = 0, K = 0;
+    int BN = 128;
+    CUtensorMap tm;      // bf16 weights on the tcgen05 path
+};
+
+struct LayerW {
+    float *ff1_g = nullptr, *ff1_b = nullptr, *att_g = nullptr, *att_b = nullptr, *conv_g = nullptr,
+          *conv_b = nullptr, *ff2_g = nullptr, *ff2_b = nullptr, *out_g = nullptr, *out_b = nullptr;
+    Lin ff1_w1, ff1_w2, qkv, wo, pw1, pw2, ff2_w1, ff2_w2;
+    float *pbu = nullptr, *pbv = nullptr, *P = nullptr, *dwT = nullptr, *bdw = nullptr, *bng = nullptr,
+          *bnb = nullptr;
+};
+
+struct OfflineWs {
+    size_t bytes = 0;
+    void* base = nullptr;
+};
+
+}  // namespace
+
+struct cac_model {
+    cac_config cfg{};
+    int bf16 = 1, tc = 1;
+    int D = 0, H = 0, HD = 0, F = 0, L = 0, J = 0;
+    int rmin = 0, NR = 0;
+    std::vector<void*> allocs;
+    Lin sub1, sub2, sub3, subo, joint;
+    std::vector<LayerW> layers;
+    int* status = nullptr;
+    OfflineWs ws;
+    long long launches = 0;
+};
+
+namespace {
+
+int dalloc(cac_model* m, size_t bytes, void** out) {
+    void* p = nullptr;
+    if (cudaMalloc(&p, std::max<size_t>(bytes, 16)) != cudaSuccess) return CAC_E_NOMEM;
+    m->allocs.push_back(p);
+    *out = p;
+    return CAC_OK;
+}
+
+int upload_f32(cac_model* m, const float* src, size_t n, float** out) {
+    void* p;
+    RET(dalloc(m, n * sizeof(float), &p));
+    CK(cudaMemcpy(p, src, n * sizeof(float), cudaMemcpyHostToDevice));
+    *out = static_cast<float*>(p);
+    return CAC_OK;
+}
+
+// Upload a [N][K] weight (rows optionally gathered through `perm`) and its bias.
+int upload_lin(cac_model* m, const float* w, const float* b, int N, int K, Lin* lin, const std::vector<int>* perm) {
+    lin->N = N;
+    lin->K = K;
+    const size_t n = (size_t)N * K;
+    void* p;
+    if (m->bf16) {
+        std::vector<uint16_t> h(n);
+        for (int r = 0; r < N; ++r) {
+            const int src = perm ? (*perm)[r] : r;
+            for (int k = 0; k < K; ++k) h[(size_t)r * K + k] = f2bf(w[(size_t)src * K + k]);
+        }
+        RET(dalloc(m, n * 2, &p));
+        CK(cudaMemcpy(p, h.data(), n * 2, cudaMemcpyHostToDevice));
+    } else {
+        std::vector<float> h(n);
+        for (int r = 0; r < N; ++r) {
+            const int src = perm ? (*perm)[r] : r;
+            std::memcpy(&h[(size_t)r * K], &w[(size_t)src * K], sizeof(float) * K);
+        }
+        RET(dalloc(m, n * 4, &p));
+        CK(cudaMemcpy(p, h.data(), n * 4, cudaMemcpyHostToDevice));
+    }
+    lin->w = p;
+    if (b) {
+        std::vector<float> hb(N);
+        for (int r = 0; r < N; ++r) hb[r] = b[perm ? (*perm)[r] : r];
+        RET(upload_f32(m, hb.data(), N, &lin->b));
+    }
+    if (m->tc) {
+        lin->BN = (N % 128 == 0) ? 128 : 64;
+        if (N % lin->BN || K % 64) return CAC_E_UNSUPPORTED;
+        if (!make_tmap_bf16(&lin->tm, p, K, N, (uint64_t)K * 2, lin->BN)) return CAC_E_CUDA;
+    }
+    return CAC_OK;
+}
+
+struct Cursor {
+    const float* p;
+    size_t left;
+    const float* take(size_t n) {
+        if (n > left) return nullptr;
+        const float* r = p;
+        p += n;
+        left -= n;
+        return r;
+    }
+};
+
+int validate(const cac_config* c) {
+    if (!c) return CAC_E_INVAL;
+    if (c->n_layers <= 0 || c->d_model <= 0 || c->n_heads <= 0 || c->ff_dim <= 0) return CAC_E_INVAL;
+    if (c->d_model % c->n_heads) return CAC_E_INVAL;
+    const int hd = c->d_model / c->n_heads;
+    if (hd != 64 && hd != 16) return CAC_E_UNSUPPORTED;
+    if (c->dw_kernel != 9 || c->mel_bins != MEL) return CAC_E_UNSUPPORTED;
+    if (c->d_model % 64 || c->ff_dim % 64 || c->joint_dim % 64 || c->d_model > 1024) return CAC_E_UNSUPPORTED;
+    if (c->att_left < 0 || c->att_chunk <= 0 || c->att_chunk > 8) return CAC_E_INVAL;
+    if (c->dtype != CAC_DTYPE_F32 && c->dtype != CAC_DTYPE_BF16) return CAC_E_INVAL;
+    if (c->right_context < 0 || c->right_context > 8) return CAC_E_UNSUPPORTED;
+    if (c->right_context > 0 && (c->emit_frames <= 0 || c->lookahead_frames < 0 ||
+                                 c->emit_frames + c->lookahead_frames > 24 ||
+                                 c->att_left + c->emit_frames + c->lookahead_frames > 96))
+        return CAC_E_UNSUPPORTED;
+    if (c->right_context == 0 && c->att_left + 8 > 80) return CAC_E_UNSUPPORTED;
+    return CAC_OK;
+}
+
+// GEMM dispatch: tcgen05 for bf16 models (unless the SIMT debugging twin is
+// requested), SIMT for fp32 models.  conv_C > 0: A is a stride-2 convolution
+// window read through the im2col view (M output rows = window row pairs).
+int gemm(cac_model* m, const void* A, long long lda, int M, int K, const Lin& W, int conv_C, EpiParams ep,
+         cudaStream_t s, long long* launches) {
+    if (M <= 0) return CAC_OK;
+    ep.act_bf16 = m->bf16;
+    if (m->tc) {
+        CUtensorMap tmA;
+        const bool ok = conv_C ? make_tmap_bf16_conv(&tmA, A, conv_C, (uint64_t)M + 1, 128)
+                               : make_tmap_bf16(&tmA, A, K, M, (uint64_t)lda * 2, 128);
+        if (!ok) return CAC_E_CUDA;
+        CK(launch_gemm_tc(&tmA, &W.tm, M, W.N, K, W.BN, conv_C, ep, m->status, s));
+    } else {
+        CK(launch_gemm_simt(m->bf16, A, lda, W.w, K, M, W.N, K, ep, s));
+    }
+    ++*launches;
+    return CAC_OK;
+}
+
+size_t act_bytes(const cac_model* m) { return m->bf16 ? 2 : 4; }
+
+}  // namespace
+
+// ===========================================================================
+// model
+// ===========================================================================
+extern "C" size_t cac_weights_size(const cac_config* c) {
+    const int v = validate(c);
+    if (v != CAC_OK && v != CAC_E_UNSUPPORTED) return 0;
+    const size_t D = c->d_model, F = c->ff_dim, M = c->mel_bins, J = c->joint_dim, K = c->dw_kernel;
+    size_t n = D * 3 * M + D + 2 * (D * 3 * D + D) + D * D + D;
+    const size_t ff = 2 * D + F * D + F + D * F + D;
+    const size_t att = 2 * D + 4 * (D * D + D) + D * D + 2 * D;
+    const size_t conv = 2 * D + 2 * D * D + 2 * D + D * K + D + 2 * D + D * D + D;
+    n += (size_t)c->n_layers * (2 * ff + att + conv + 2 * D);
+    n += J * D + J;
+    return n;
+}
+
+extern "C" int cac_model_create(const cac_config* cfg, const float* weights, size_t n_floats, cac_model** out) {
+    if (!out || !weights) return CAC_E_INVAL;
+    *out = nullptr;
+    RET(validate(cfg));
+    if (n_floats != cac_weights_size(cfg)) return CAC_E_INVAL;
+    cac_model* m = new (std::nothrow) cac_model();
+    if (!m) return CAC_E_NOMEM;
+    m->cfg = *cfg;
+    m->bf16 = cfg->dtype == CAC_DTYPE_BF16;
+    m->tc = m->bf16 && !cfg->gemm_simt;
+    m->D = cfg->d_model;
+    m->H = cfg->n_heads;
+    m->HD = m->D / m->H;
+    m->F = cfg->ff_dim;
+    m->L = cfg->n_layers;
+    m->J = cfg->joint_dim;
+    const int back = std::max(cfg->att_chunk - 1, cfg->right_context);
+    m->rmin = -back;
+    m->NR = cfg->att_left + std::max(cfg->att_chunk - 1, 0) - m->rmin + 1;
+    const int D = m->D, F = m->F, H = m->H, HD = m->HD;
+
+    auto fail = [&](int code) {
+        cac_model_destroy(m);
+        return code;
+    };
+    Cursor c{weights, n_floats};
+    int r;
+    void* st;
+    if ((r = dalloc(m, sizeof(int), &st)) != CAC_OK) return fail(r);
+    m->status = static_cast<int*>(st);
+    if (cudaMemset(m->status, 0, sizeof(int)) != cudaSuccess) return fail(CAC_E_CUDA);
+
+    const float *w, *b;
+    w = c.take((size_t)D * 3 * MEL); b = c.take(D);
+    if ((r = upload_lin(m, w, b, D, 3 * MEL, &m->sub1, nullptr)) != CAC_OK) return fail(r);
+    w = c.take((size_t)D * 3 * D); b = c.take(D);
+    if ((r = upload_lin(m, w, b, D, 3 * D, &m->sub2, nullptr)) != CAC_OK) return fail(r);
+    w = c.take((size_t)D * 3 * D); b = c.take(D);
+    if ((r = upload_lin(m, w, b, D, 3 * D, &m->sub3, nullptr)) != CAC_OK) return fail(r);
+    w = c.take((size_t)D * D); b = c.take(D);
+    if ((r = upload_lin(m, w, b, D, D, &m->subo, nullptr)) != CAC_OK) return fail(r);
+
+    // GLU interleave: every 32 output columns of pw1 = 16 value rows then their 16 gate rows
+    std::vector<int> glu_perm(2 * D);
+    for (int j = 0; j < 2 * D; ++j) {
+        const int s = j / 32, q = j % 32;
+        glu_perm[j] = q < 16 ? 16 * s + q : D + 16 * s + (q - 16);
+    }
+
+    // position table pe(r) for r = rmin .. rmin + NR - 1 (shared by all layers)
+    float* pe = nullptr;
+    {
+        void* p;
+        if ((r = dalloc(m, sizeof(float) * m->NR * D, &p)) != CAC_OK) return fail(r);
+        pe = static_cast<float*>(p);
+        if (launch_sinusoid(pe, m->NR, m->rmin, D, 0) != cudaSuccess) return fail(CAC_E_CUDA);
+    }
+
+    m->layers.resize(m->L);
+    std::vector<float> tmp;
+    for (int l = 0; l < m->L; ++l) {
+        LayerW& Lw = m->layers[l];
+        auto vec = [&](float** dst, size_t n) {
+            const float* s = c.take(n);
+            return s ? upload_f32(m, s, n, dst) : CAC_E_INVAL;
+        };
+        auto lin = [&](Lin* dst, int N, int K, const std::vector<int>* perm) {
+            const float* ww = c.take((size_t)N * K);
+            const float* bb = c.take(N);
+            return (ww && bb) ? upload_lin(m, ww, bb, N, K, dst, perm) : CAC_E_INVAL;
+        };
+        if ((r = vec(&Lw.ff1_g, D)) || (r = vec(&Lw.ff1_b, D)) || (r = lin(&Lw.ff1_w1, F, D, nullptr)) ||
+            (r = lin(&Lw.ff1_w2, D, F, nullptr)))
+            return fail(r);
+        if ((r = vec(&Lw.att_g, D)) || (r = vec(&Lw.att_b, D))) return fail(r);
+        {   // q, k, v concatenated into one [3D][D] projection
+            const float *wq = c.take((size_t)D * D), *bq = c.take(D), *wk = c.take((size_t)D * D), *bk = c.take(D),
+                        *wv = c.take((size_t)D * D), *bv = c.take(D);
+            if (!wv || !bv) return fail(CAC_E_INVAL);
+            std::vector<float> wqkv((size_t)3 * D * D), bqkv(3 * D);
+            std::memcpy(&wqkv[0], wq, sizeof(float) * D * D);
+            std::memcpy(&wqkv[(size_t)D * D], wk, sizeof(float) * D * D);
+            std::memcpy(&wqkv[(size_t)2 * D * D], wv, sizeof(float) * D * D);
+            std::memcpy(&bqkv[0], bq, sizeof(float) * D);
+            std::memcpy(&bqkv[D], bk, sizeof(float) * D);
+            std::memcpy(&bqkv[2 * D], bv, sizeof(float) * D);
+            if ((r = upload_lin(m, wqkv.data(), bqkv.data(), 3 * D, D, &Lw.qkv, nullptr)) != CAC_OK) return fail(r);
+        }
+        if ((r = lin(&Lw.wo, D, D, nullptr))) return fail(r);
+        {   // P = pe @ wpos^T, computed once per layer in fp32
+            const float* wpos = c.take((size_t)D * D);
+            if (!wpos) return fail(CAC_E_INVAL);
+            float* wpos_d;
+            if ((r = upload_f32(m, wpos, (size_t)D * D, &wpos_d)) != CAC_OK) return fail(r);
+            void* p;
+            if ((r = dalloc(m, sizeof(float) * m->NR * D, &p)) != CAC_OK) return fail(r);
+            Lw.P = static_cast<float*>(p);
+            EpiParams ep;
+            ep.kind = EPI_STORE;
+            ep.act_bf16 = 0;
+            ep.out_f32 = Lw.P;
+            ep.ldo = D;
+            if (launch_gemm_simt(0, pe, D, wpos_d, D, m->NR, D, D, ep, 0) != cudaSuccess) return fail(CAC_E_CUDA);
+        }
+        if ((r = vec(&Lw.pbu, (size_t)H * HD)) || (r = vec(&Lw.pbv, (size_t)H * HD))) return fail(r);
+        if ((r = vec(&Lw.conv_g, D)) || (r = vec(&Lw.conv_b, D)) || (r = lin(&Lw.pw1, 2 * D, D, &glu_perm)))
+            return fail(r);
+        {   // depthwise [D][9] -> [9][D]
+            const float* wdw = c.take((size_t)D * 9);
+            if (!wdw) return fail(CAC_E_INVAL);
+            tmp.assign((size_t)9 * D, 0.f);
+            for (int ch = 0; ch < D; ++ch)
+                for (int k = 0; k < 9; ++k) tmp[(size_t)k * D + ch] = wdw[(size_t)ch * 9 + k];
+            if ((r = upload_f32(m, tmp.data(), tmp.size(), &Lw.dwT)) != CAC_OK) return fail(r);
+        }
+        if ((r = vec(&Lw.bdw, D)) || (r = vec(&Lw.bng, D)) || (r = vec(&Lw.bnb, D)) ||
+            (r = lin(&Lw.pw2, D, D, nullptr)))
+            return fail(r);
+        if ((r = vec(&Lw.ff2_g, D)) || (r = vec(&Lw.ff2_b, D)) || (r = lin(&Lw.ff2_w1, F, D, nullptr)) ||
+            (r = lin(&Lw.ff2_w2, D, F, nullptr)))
+            return fail(r);
+        if ((r = vec(&Lw.out_g, D)) || (r = vec(&Lw.out_b, D))) return fail(r);
+    }
+    {
+        const float* wj = c.take((size_t)m->J * D);
+        const float* bj = c.take(m->J);
+        if (!wj || !bj) return fail(CAC_E_INVAL);
+        if ((r = upload_lin(m, wj, bj, m->J, D, &m->joint, nullptr)) != CAC_OK) return fail(r);
+    }
+    if (c.left != 0) return fail(CAC_E_INVAL);
+    if (cudaDeviceSynchronize() != cudaSuccess) return fail(CAC_E_CUDA);
+    *out = m;
+    return CAC_OK;
+}
+
+extern "C" void cac_model_destroy(cac_model* m) {
+    if (!m) return;
+    cudaDeviceSynchronize();
+    for (void* p : m->allocs) cudaFree(p);
+    if (m->ws.base) cudaFree(m->ws.base);
+    delete m;
+}
+
+extern "C" int cac_model_check(cac_model* m) {
+    if (!m) return CAC_E_INVAL;
+    CK(cudaDeviceSynchronize());
+    int st = 0;
+    CK(cudaMemcpy(&st, m->status, sizeof(int), cudaMemcpyDeviceToHost));
+    CK(cudaMemset(m->status, 0, sizeof(int)));
+    return st;
+}
+
+// ===========================================================================
+// pool
+// ===========================================================================
+namespace {
+constexpr int ID_SLOTS = 8;
+
+struct GraphKey {
+    int nb, n, nvalid;
+    const void *mel, *enc, *joint;
+    long long mel_bstride;
+    int out_bstride, out_off;
+    bool operator<(const GraphKey& o) const {
+        return std::tie(nb, n, nvalid, mel, enc, joint, mel_bstride, out_bstride, out_off) <
+               std::tie(o.nb, o.n, o.nvalid, o.mel, o.enc, o.joint, o.mel_bstride, o.out_bstride, o.out_off);
+    }
+};
+struct GraphEntry {
+    int seen = 0;
+    cudaGraphExec_t exec = nullptr;
+    long long kernels = 0;
+};
+}  // namespace
+
+struct cac_pool {
+    cac_model* m = nullptr;
+    int S = 0, nmax = 0, R = 0;
+    std::vector<void*> allocs;
+    // per-stream device state
+    int* pos = nullptr;        // subsampled frames consumed
+    void* tail = nullptr;      // [S][14][128]
+    void* kring = nullptr;     // [S][L][H][R][HD]
+    void* vring = nullptr;
+    void* conv = nullptr;      // [S][L][8][D]
+    // step scratch
+    void *win1 = nullptr, *win2 = nullptr, *win3 = nullptr, *y3 = nullptr;
+    float* x = nullptr;
+    void *xln = nullptr, *h = nullptr, *o = nullptr, *glu = nullptr, *yc = nullptr;
+    float* q = nullptr;
+    int* ids_dev = nullptr;     // batch slot -> stream id for the current push
+    int* rids_dev = nullptr;    // ids of the current reset
+    int* nvalid_dev = nullptr;  // flush: valid mel frames per batch slot
+    int* status = nullptr;
+    // host mirrors
+    std::vector<uint8_t> alive, finished;
+    std::vector<int> pos_host;
+    // pinned id staging ring
+    int* pinned = nullptr;
+    cudaEvent_t slot_ev[ID_SLOTS] = {};
+    int slot = 0;
+    // staging for cac_stream_push_host
+    float* h_mel = nullptr;
+    float* d_mel = nullptr;
+    float* h_out = nullptr;
+    float* d_out = nullptr;
+    size_t h_mel_cap = 0, h_out_cap = 0;
+    // graphs, tracing, counters
+    bool graphs = false;
+    std::map<GraphKey, GraphEntry> gcache;
+    bool trace = false;
+    float* trace_buf = nullptr;  // [L][7][rows][D] + [rows][D]
+    int trace_rows = 0;
+    long long launches = 0;
+    long long ring_sstride = 0, conv_sstride = 0;
+    size_t tail_elems = 0;
+};
+
+namespace {
+
+int palloc(cac_pool* p, size_t bytes, void** out, bool zero = true) {
+    void* d = nullptr;
+    if (cudaMalloc(&d, std::max<size_t>(bytes, 16)) != cudaSuccess) return CAC_E_NOMEM;
+    p->allocs.push_back(d);
+    if (zero && cudaMemset(d, 0, std::max<size_t>(bytes, 16)) != cudaSuccess) return CAC_E_CUDA;
+    *out = d;
+    return CAC_OK;
+}
+
+// Copy `n` ids into the next pinned slot and queue their upload to `dst`.
+int upload_ids(cac_pool* p, const int* ids, int n, int* dst, cudaStream_t s) {
+    const int k = p->slot;
+    p->slot = (p->slot + 1) % ID_SLOTS;
+    CK(cudaEventSynchronize(p->slot_ev[k]));
+    int* h = p->pinned + (size_t)k * p->S;
+    std::memcpy(h, ids, sizeof(int) * n);
+    CK(cudaMemcpyAsync(dst, h, sizeof(int) * n, cudaMemcpyHostToDevice, s));
+    CK(cudaEventRecord(p->slot_ev[k], s));
+    return CAC_OK;
+}
+
+int check_ids(cac_pool* p, int n, const int* ids, bool need_unfinished) {
+    if (n <= 0 || n > p->S || !ids) return CAC_E_INVAL;
+    std::vector<uint8_t> seen(p->S, 0);
+    for (int i = 0; i < n; ++i) {
+        const int id = ids[i];
+        if (id < 0 || id >= p->S || seen[id]) return CAC_E_INVAL;
+        seen[id] = 1;
+        if (!p->alive[id]) return CAC_E_STATE;
+        if (need_unfinished && p->finished[id]) return CAC_E_STATE;
+    }
+    return CAC_OK;
+}
+
+int trace_tap(cac_pool* p, int layer, int tap, const void* src, bool src_act, int rows, cudaStream_t s) {
+    if (!p->trace) return CAC_OK;
+    cac_model* m = p->m;
+    const long long per = (long long)p->trace_rows * m->D;
+    float* dst = tap == N_TAPS ? p->trace_buf + (long long)m->L * N_TAPS * per
+                               : p->trace_buf + ((long long)layer * N_TAPS + tap) * per;
+    CK(launch_to_f32(src, dst, (long long)rows * m->D, src_act && m->bf16, s));
+    ++p->launches;
+    return CAC_OK;
+}
+
+// One step: nb batch slots (ids already in p->ids_dev), n new frames each.
+//   mel: stream b's first mel row at mel + b * mel_bstride (8n rows; with
+//        nvalid, rows >= nvalid[b] read as zero)
+//   enc/joint: frame i of slot b goes to row b * out_bstride + out_off + i
+int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride, const int* nvalid, float* enc,
+             float* joint, int out_bstride, int out_off, cudaStream_t s) {
+    cac_model* m = p->m;
+    const int D = m->D, F = m->F, L = m->L;
+    const int M = nb * n;
+    long long* lc = &p->launches;
+    const size_t ab = act_bytes(m);
+    const int bf = m->bf16;
+
+    // 1. mel staging: [melTail | mel] windows, tail update
+    CK(launch_stage_mel(mel, mel_bstride, nvalid, p->win1, p->tail, p->ids_dev, p->pos, n, nb, bf, p->status, s));
+    ++*lc;
+    // 2. three stride-2 convolutions (implicit GEMMs over the windows) + out linear
+    const int W1 = TAIL + 8 * n, W2 = 4 * n + 6, W3 = 2 * n + 2;
+    {
+        EpiParams ep;
+        ep.kind = EPI_SUB;
+        ep.bias = m->sub1.b;
+        ep.out_act = p->win2;
+        ep.ldo = D;
+        ep.ids = p->ids_dev;
+        ep.pos = p->pos;
+        ep.P = W1 / 2; ep.T_out = W2; ep.dst_rows = W2; ep.dst_off = 0; ep.tmult = 4; ep.toff = 6;
+        RET(gemm(m, p->win1, 2 * MEL, nb * (W1 / 2), 3 * MEL, m->sub1, MEL, ep, s, lc));
+        ep.bias = m->sub2.b;
+        ep.out_act = p->win3;
+        ep.P = W2 / 2; ep.T_out = W3; ep.dst_rows = W3; ep.tmult = 2; ep.toff = 2;
+        RET(gemm(m, p->win2, 2 * D, nb * (W2 / 2), 3 * D, m->sub2, D, ep, s, lc));
+        ep.bias = m->sub3.b;
+        ep.out_act = p->y3;
+        ep.P = W3 / 2; ep.T_out = n; ep.dst_rows = n; ep.tmult = 1; ep.toff = 0;
+        RET(gemm(m, p->win3, 2 * D, nb * (W3 / 2), 3 * D, m->sub3, D, ep, s, lc));
+    }
+    {
+        EpiParams ep;
+        ep.kind = EPI_STORE;
+        ep.bias = m->subo.b;
+        ep.out_f32 = p->x;
+        ep.ldo = D;
+        RET(gemm(m, p->y3, D, M, D, m->subo, 0, ep, s, lc));
+    }
+    RET(trace_tap(p, 0, N_TAPS, p->x, false, M, s));
+    CK(launch_layernorm(p->x, M, D, m->layers[0].ff1_g, m->layers[0].ff1_b, nullptr, p->xln, nullptr, nullptr,
+                        nullptr, bf, 1 << 30, 0, 0, s));
+    ++*lc;
+
+    for (int l = 0; l < L; ++l) {
+        const LayerW& Lw = m->layers[l];
+        EpiParams ep;
+        // FF1: x += 1/2 * (W2 SiLU(W1 LN(x) + b1) + b2)   (LN(x) already in xln)
+        ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff1_w1.b; ep.out_act = p->h; ep.ldo = F;
+        RET(gemm(m, p->xln, D, M, D, Lw.ff1_w1, 0, ep, s, lc));
+        ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.ff1_w2.b; ep.x = p->x; ep.ldx = D; ep.scale = 0.5f;
+        RET(gemm(m, p->h, F, M, F, Lw.ff1_w2, 0, ep, s, lc));
+        RET(trace_tap(p, l, 0, p->x, false, M, s));
+        // attention: xln = LN(x); Q and K/V into the rings
+        CK(launch_layernorm(p->x, M, D, Lw.att_g, Lw.att_b, nullptr, p->xln, nullptr, nullptr, nullptr, bf,
+                            1 << 30, 0, 0, s));
+        ++*lc;
+        ep = EpiParams(); ep.kind = EPI_QKV; ep.bias = Lw.qkv.b; ep.D = D; ep.HD = m->HD; ep.R = p->R;
+        ep.ring_sstride = p->ring_sstride;
+        ep.kring = static_cast<char*>(p->kring) + (long long)l * m->H * p->R * m->HD * ab;
+        ep.vring = static_cast<char*>(p->vring) + (long long)l * m->H * p->R * m->HD * ab;
+        ep.q = p->q; ep.ldq = D; ep.ids = p->ids_dev; ep.pos = p->pos; ep.nq = n;
+        RET(gemm(m, p->xln, D, M, D, Lw.qkv, 0, ep, s, lc));
+        {
+            AttnParams a;
+            a.q = p->q; a.ldq = D;
+            a.k = ep.kring; a.v = ep.vring; a.sstride = p->ring_sstride; a.R = p->R;
+            a.ids = p->ids_dev; a.pos = p->pos; a.nq = n;
+            a.P = Lw.P; a.rmin = m->rmin; a.NR = m->NR; a.pbu = Lw.pbu; a.pbv = Lw.pbv;
+            a.out = p->o; a.ldo = D;
+            a.H = m->H; a.D = D; a.HD = m->HD;
+            a.left = m->cfg.att_left; a.chunk = m->cfg.att_chunk; a.rc = 0;
+            a.nb = nb;
+            a.scale = 1.f / std::sqrt((float)m->HD);
+            CK(launch_attention_stream(a, bf, s));
+            ++*lc;
+        }
+        RET(trace_tap(p, l, 1, p->o, true, M, s));
+        ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.wo.b; ep.x = p->x; ep.ldx = D; ep.scale = 1.f;
+        RET(gemm(m, p->o, D, M, D, Lw.wo, 0, ep, s, lc));
+        RET(trace_tap(p, l, 2, p->x, false, M, s));
+        // conv module
+        CK(launch_layernorm(p->x, M, D, Lw.conv_g, Lw.conv_b, nullptr, p->xln, nullptr, nullptr, nullptr, bf,
+                            1 << 30, 0, 0, s));
+        ++*lc;
+        ep = EpiParams(); ep.kind = EPI_GLU; ep.bias = Lw.pw1.b; ep.out_act = p->glu; ep.ldo = D;
+        RET(gemm(m, p->xln, D, M, D, Lw.pw1, 0, ep, s, lc));
+        RET(trace_tap(p, l, 3, p->glu, true, M, s));
+        CK(launch_dwconv(p->glu, static_cast<char*>(p->conv) + (long long)l * CONV_CACHE * D * ab, p->conv_sstride,
+                         p->ids_dev, p->pos, n, n, Lw.dwT, Lw.bdw, Lw.bng, Lw.bnb, p->yc, D, nb, bf, s));
+        ++*lc;
+        RET(trace_tap(p, l, 4, p->yc, true, M, s));
+        ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.pw2.b; ep.x = p->x; ep.ldx = D; ep.scale = 1.f;
+        RET(gemm(m, p->yc, D, M, D, Lw.pw2, 0, ep, s, lc));
+        RET(trace_tap(p, l, 5, p->x, false, M, s));
+        // FF2
+        CK(launch_layernorm(p->x, M, D, Lw.ff2_g, Lw.ff2_b, nullptr, p->xln, nullptr, nullptr, nullptr, bf,
+                            1 << 30, 0, 0, s));
+        ++*lc;
+        ep = EpiParams(); ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff2_w1.b; ep.out_act = p->h; ep.ldo = F;
+        RET(gemm(m, p->xln, D, M, D, Lw.ff2_w1, 0, ep, s, lc));
+        ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.ff2_w2.b; ep.x = p->x; ep.ldx = D; ep.scale = 0.5f;
+        RET(gemm(m, p->h, F, M, F, Lw.ff2_w2, 0, ep, s, lc));
+        // ln_out, fused with the next layer's FF1 LayerNorm (or, after the last
+        // layer, writing the encoder frames to the caller and the joint input)
+        if (l + 1 < L) {
+            CK(launch_layernorm(p->x, M, D, Lw.out_g, Lw.out_b, p->x, nullptr, m->layers[l + 1].ff1_g,
+                                m->layers[l + 1].ff1_b, p->xln, bf, 1 << 30, 0, 0, s));
+            ++*lc;
+            RET(trace_tap(p, l, 6, p->x, false, M, s));
+        } else {
+            CK(launch_layernorm(p->x, M, D, Lw.out_g, Lw.out_b, enc ? enc : p->x, p->xln, nullptr, nullptr, nullptr,
+                                bf, enc ? n : 1 << 30, enc ? out_bstride : 0, enc ? out_off : 0, s));
+            ++*lc;
+            RET(trace_tap(p, l, 6, p->xln, true, M, s));
+        }
+    }
+    if (joint) {
+        EpiParams ep;
+        ep.kind = EPI_STORE;
+        ep.bias = m->joint.b;
+        ep.out_f32 = joint;
+        ep.ldo = m->J;
+        ep.grp = n; ep.grp_stride = out_bstride; ep.row_off = out_off;
+        RET(gemm(m, p->xln, D, M, D, m->joint, 0, ep, s, lc));
+    }
+    CK(launch_advance(p->pos, p->ids_dev, nb, n, s));
+    ++*lc;
+    return CAC_OK;
+}
+
+// run_step through the graph cache when graphs are enabled
+int step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride, const int* nvalid, float* enc,
+         float* joint, int out_bstride, int out_off, cudaStream_t s) {
+    if (!p->graphs || p->trace)
+        return run_step(p, nb, n, mel, mel_bstride, nvalid, enc, joint, out_bstride, out_off, s);
+    GraphKey key{nb, n, nvalid ? 1 : 0, mel, enc, joint, mel_bstride, out_bstride, out_off};
+    GraphEntry& g = p->gcache[key];
+    if (!g.exec) {
+        if (g.seen++ == 0)  // first sighting runs eagerly (sets kernel attributes, warms up)
+            return run_step(p, nb, n, mel, mel_bstride, nvalid, enc, joint, out_bstride, out_off, s);
+        cudaStream_t cs;
+        CK(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+        const long long before = p->launches;
+        cudaGraph_t graph = nullptr;
+        CK(cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal));
+        const int r = run_step(p, nb, n, mel, mel_bstride, nvalid, enc, joint, out_bstride, out_off, cs);
+        const cudaError_t e = cudaStreamEndCapture(cs, &graph);
+        cudaStreamDestroy(cs);
+        const long long captured = p->launches - before;
+        p->launches = before;
+        if (r != CAC_OK) {
+            if (graph) cudaGraphDestroy(graph);
+            return r;
+        }
+        CK(e);
+        CK(cudaGraphInstantiate(&g.exec, graph, 0));
+        g.kernels = captured;
+        cudaGraphDestroy(graph);
+    }
+    CK(cudaGraphLaunch(g.exec, s));
+    p->launches += g.kernels;
+    return CAC_OK;
+}
+
+}  // namespace
+
+extern "C" int cac_pool_create(cac_model* m, int max_streams, int max_frames_per_step, cac_pool** out) {
+    if (!m || !out || max_streams <= 0 || max_frames_per_step <= 0 || max_frames_per_step > 8) return CAC_E_INVAL;
+    *out = nullptr;
+    cac_pool* p = new (std::nothrow) cac_pool();
+    if (!p) return CAC_E_NOMEM;
+    auto fail = [&](int code) {
+        cac_pool_destroy(p);
+        return code;
+    };
+    p->m = m;
+    p->S = max_streams;
+    p->nmax = max_frames_per_step;
+    const cac_config& c = m->cfg;
+    const int pass = c.right_context > 0 ? c.emit_frames + c.lookahead_frames : p->nmax;
+    const int rows_per = std::max(pass, p->nmax);
+    p->R = ((c.att_left + rows_per + 7) / 8) * 8;
+    const int S = p->S, L = m->L, D = m->D, H = m->H, HD = m->HD, F = m->F;
+    const size_t ab = act_bytes(m);
+    const size_t rows_max = (size_t)S * rows_per;
+    const int n = p->nmax;
+    p->ring_sstride = (long long)L * H * p->R * HD;
+    p->conv_sstride = (long long)L * CONV_CACHE * D;
+    p->tail_elems = (size_t)TAIL * MEL;
+    int r;
+    void* v;
+    if ((r = palloc(p, sizeof(int) * S, &v)) != CAC_OK) return fail(r);
+    p->pos = static_cast<int*>(v);
+    if ((r = palloc(p, ab * S * p->tail_elems, &p->tail)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, ab * S * p->ring_sstride, &p->kring)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, ab * S * p->ring_sstride, &p->vring)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, ab * S * p->conv_sstride, &p->conv)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, ab * ((size_t)S * (TAIL + 8 * n) + 4) * MEL, &p->win1)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, ab * ((size_t)S * (4 * n + 6) + 4) * D, &p->win2)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, ab * ((size_t)S * (2 * n + 2) + 4) * D, &p->win3)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, ab * rows_max * D, &p->y3)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, 4 * rows_max * D, &v)) != CAC_OK) return fail(r);
+    p->x = static_cast<float*>(v);
+    if ((r = palloc(p, ab * rows_max * D, &p->xln)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, ab * rows_max * F, &p->h)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, 4 * rows_max * D, &v)) != CAC_OK) return fail(r);
+    p->q = static_cast<float*>(v);
+    if ((r = palloc(p, ab * rows_max * D, &p->o)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, ab * rows_max * D, &p->glu)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, ab * rows_max * D, &p->yc)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, sizeof(int) * S, &v)) != CAC_OK) return fail(r);
+    p->ids_dev = static_cast<int*>(v);
+    if ((r = palloc(p, sizeof(int) * S, &v)) != CAC_OK) return fail(r);
+    p->rids_dev = static_cast<int*>(v);
+    if ((r = palloc(p, sizeof(int) * S, &v)) != CAC_OK) return fail(r);
+    p->nvalid_dev = static_cast<int*>(v);
+    if ((r = palloc(p, sizeof(int), &v)) != CAC_OK) return fail(r);
+    p->status = static_cast<int*>(v);
+    p->trace_rows = (int)rows_max;
+    if (cudaHostAlloc(reinterpret_cast<void**>(&p->pinned), sizeof(int) * S * ID_SLOTS, cudaHostAllocDefault) !=
+        cudaSuccess)
+        return fail(CAC_E_NOMEM);
+    for (int k = 0; k < ID_SLOTS; ++k)
+        if (cudaEventCreateWithFlags(&p->slot_ev[k], cudaEventDisableTiming) != cudaSuccess) return fail(CAC_E_CUDA);
+    p->alive.assign(S, 0);
+    p->finished.assign(S, 0);
+    p->pos_host.assign(S, 0);
+    if (cudaDeviceSynchronize() != cudaSuccess) return fail(CAC_E_CUDA);
+    *out = p;
+    return CAC_OK;
+}
+
+extern "C" void cac_pool_destroy(cac_pool* p) {
+    if (!p) return;
+    cudaDeviceSynchronize();
+    for (auto& kv : p->gcache)
+        if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+    for (void* d : p->allocs) cudaFree(d);
+    if (p->trace_buf) cudaFree(p->trace_buf);
+    if (p->pinned) cudaFreeHost(p->pinned);
+    if (p->h_mel) cudaFreeHost(p->h_mel);
+    if (p->h_out) cudaFreeHost(p->h_out);
+    if (p->d_mel) cudaFree(p->d_mel);
+    if (p->d_out) cudaFree(p->d_out);
+    for (int k = 0; k < ID_SLOTS; ++k)
+        if (p->slot_ev[k]) cudaEventDestroy(p->slot_ev[k]);
+    delete p;
+}
+
+extern "C" int cac_stream_create(cac_pool* p, int* id) {
+    if (!p || !id) return CAC_E_INVAL;
+    for (int i = 0; i < p->S; ++i) {
+        if (!p->alive[i]) {
+            // a fresh stream starts at position 0
+            CK(cudaDeviceSynchronize());
+            const int zero = 0;
+            CK(cudaMemcpy(p->pos + i, &zero, sizeof(int), cudaMemcpyHostToDevice));
+            p->alive[i] = 1;
+            p->finished[i] = 0;
+            p->pos_host[i] = 0;
+            *id = i;
+            return CAC_OK;
+        }
+    }
+    return CAC_E_NOMEM;
+}
+
+extern "C" int cac_stream_destroy(cac_pool* p, int id) {
+    if (!p || id < 0 || id >= p->S || !p->alive[id]) return CAC_E_INVAL;
+    p->alive[id] = 0;
+    return CAC_OK;
+}
+
+extern "C" int cac_stream_reset(cac_pool* p, int n, const int* ids, void* stream) {
+    if (!p) return CAC_E_INVAL;
+    if (n == 0) return CAC_OK;
+    RET(check_ids(p, n, ids, false));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    RET(upload_ids(p, ids, n, p->rids_dev, s));
+    CK(launch_set_pos(p->pos, p->rids_dev, n, 0, s));
+    ++p->launches;
+    for (int i = 0; i < n; ++i) {
+        p->pos_host[ids[i]] = 0;
+        p->finished[ids[i]] = 0;
+    }
+    return CAC_OK;
+}
+
+extern "C" int cac_stream_push(cac_pool* p, int n, const int* ids, const float* mel, int n_mel, float* enc,
+                               float* joint, int* n_out, void* stream) {
+    if (!p || !mel || !n_out) return CAC_E_INVAL;
+    cac_model* m = p->m;
+    if (m->cfg.right_context > 0) return CAC_E_UNSUPPORTED;
+    RET(check_ids(p, n, ids, true));
+    const int A = m->cfg.att_chunk;
+    if (n_mel <= 0 || n_mel % (8 * A)) return CAC_E_ALIGN;
+    const int chunk = (p->nmax / A) * A;
+    if (chunk <= 0) return CAC_E_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    RET(upload_ids(p, ids, n, p->ids_dev, s));
+    const int frames = n_mel / 8;
+    for (int f0 = 0; f0 < frames; f0 += chunk) {
+        const int nf = std::min(chunk, frames - f0);
+        RET(step(p, n, nf, mel + (size_t)f0 * 8 * MEL, (long long)n_mel * MEL, nullptr, enc, joint, frames, f0, s));
+    }
+    for (int i = 0; i < n; ++i) {
+        p->pos_host[ids[i]] += frames;
+        n_out[i] = frames;
+    }
+    return CAC_OK;
+}
+
+extern "C" int cac_stream_push_host(cac_pool* p, int n, const int* ids, const float* mel, int n_mel, float* enc,
+                                    float* joint, int* n_out, void* stream) {
+    if (!p || !mel || !n_out) return CAC_E_INVAL;
+    cac_model* m = p->m;
+    RET(check_ids(p, n, ids, true));
+    if (n_mel <= 0 || n_mel % (8 * m->cfg.att_chunk)) return CAC_E_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t mel_n = (size_t)n * n_mel * MEL;
+    const int frames = n_mel / 8;
+    const size_t enc_n = (size_t)n * frames * m->D, joint_n = (size_t)n * frames * m->J;
+    if (mel_n > p->h_mel_cap) {
+        CK(cudaStreamSynchronize(s));
+        if (p->h_mel) cudaFreeHost(p->h_mel);
+        if (p->d_mel) cudaFree(p->d_mel);
+        p->h_mel = nullptr;
+        p->d_mel = nullptr;
+        p->h_mel_cap = 0;
+        if (cudaHostAlloc(reinterpret_cast<void**>(&p->h_mel), mel_n * 4, cudaHostAllocDefault) != cudaSuccess ||
+            cudaMalloc(&p->d_mel, mel_n * 4) != cudaSuccess)
+            return CAC_E_NOMEM;
+        p->h_mel_cap = mel_n;
+    }
+    if (enc_n + joint_n > p->h_out_cap) {
+        CK(cudaStreamSynchronize(s));
+        if (p->h_out) cudaFreeHost(p->h_out);
+        if (p->d_out) cudaFree(p->d_out);
+        p->h_out = nullptr;
+        p->d_out = nullptr;
+        p->h_out_cap = 0;
+        if (cudaHostAlloc(reinterpret_cast<void**>(&p->h_out), (enc_n + joint_n) * 4, cudaHostAllocDefault) !=
+                cudaSuccess ||
+            cudaMalloc(&p->d_out, (enc_n + joint_n) * 4) != cudaSuccess)
+            return CAC_E_NOMEM;
+        p->h_out_cap = enc_n + joint_n;
+    }
+    std::memcpy(p->h_mel, mel, mel_n * 4);
+    CK(cudaMemcpyAsync(p->d_mel, p->h_mel, mel_n * 4, cudaMemcpyHostToDevice, s));
+    float* de = enc ? p->d_out : nullptr;
+    float* dj = joint ? p->d_out + enc_n : nullptr;
+    RET(cac_stream_push(p, n, ids, p->d_mel, n_mel, de, dj, n_out, stream));
+    if (enc) CK(cudaMemcpyAsync(p->h_out, de, enc_n * 4, cudaMemcpyDeviceToHost, s));
+    if (joint) CK(cudaMemcpyAsync(p->h_out + enc_n, dj, joint_n * 4, cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    if (enc) std::memcpy(enc, p->h_out, enc_n * 4);
+    if (joint) std::memcpy(joint, p->h_out + enc_n, joint_n * 4);
+    return CAC_OK;
+}
+
+extern "C" int cac_stream_flush_frames(cac_pool* p, int id, int n_mel, int* frames) {
+    if (!p || !frames || id < 0 || id >= p->S || n_mel < 0) return CAC_E_INVAL;
+    *frames = (n_mel + 7) / 8;
+    return CAC_OK;
+}
+
+extern "C" int cac_stream_flush(cac_pool* p, int n, const int* ids, const float* mel, int mel_stride,
+                                const int* n_mel_each, float* enc, float* joint, int out_stride, int* n_out_each,
+                                void* stream) {
+    if (!p || !n_mel_each || !n_out_each) return CAC_E_INVAL;
+    cac_model* m = p->m;
+    if (m->cfg.right_context > 0) return CAC_E_UNSUPPORTED;
+    RET(check_ids(p, n, ids, true));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    for (int b = 0; b < n; ++b) {
+        const int r = n_mel_each[b];
+        if (r < 0 || r > mel_stride || (r + 7) / 8 > out_stride || (r > 0 && !mel)) return CAC_E_INVAL;
+    }
+    // each stream alone: whole chunks as steps, then the ragged remainder
+    const int A = m->cfg.att_chunk;
+    const int chunk = (p->nmax / A) * A;
+    if (chunk <= 0) return CAC_E_UNSUPPORTED;
+    for (int b = 0; b < n; ++b) {
+        const int id = ids[b];
+        const int r = n_mel_each[b];
+        const float* mb = mel ? mel + (size_t)b * mel_stride * MEL : nullptr;
+        float* eb = enc ? enc + (size_t)b * out_stride * m->D : nullptr;
+        float* jb = joint ? joint + (size_t)b * out_stride * m->J : nullptr;
+        RET(upload_ids(p, &id, 1, p->ids_dev, s));
+        int done = 0;                        // frames emitted
+        const int full = r / (8 * A) * A;    // frames of whole chunks
+        while (done < full) {
+            const int nf = std::min(chunk, full - done);
+            RET(step(p, 1, nf, mb + (size_t)done * 8 * MEL, (long long)mel_stride * MEL, nullptr, eb, jb, out_stride,
+                     done, s));
+            done += nf;
+        }
+        const int rem = r - done * 8;
+        if (rem > 0) {
+            const int nf = (rem + 7) / 8;
+            RET(upload_ids(p, &rem, 1, p->nvalid_dev, s));
+            RET(step(p, 1, nf, mb + (size_t)done * 8 * MEL, (long long)mel_stride * MEL, p->nvalid_dev, eb, jb,
+                     out_stride, done, s));
+            done += nf;
+        }
+        n_out_each[b] = done;
+        p->pos_host[id] += done;
+        p->finished[id] = 1;
+    }
+    return CAC_OK;
+}
+
+// ===========================================================================
+// offline chunked-causal encode
+// ===========================================================================
+extern "C" int cac_encode_offline(cac_model* m, int B, const float* mel, const int* mel_len, int t_mel_max, float* enc,
+                                  float* joint, int* out_len, void* stream) {
+    if (!m || B <= 0 || !mel || !mel_len || t_mel_max <= 0 || !enc || !out_len) return CAC_E_INVAL;
+    for (int b = 0; b < B; ++b)
+        if (mel_len[b] < 1 || mel_len[b] > t_mel_max) return CAC_E_INVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int D = m->D, F = m->F, L = m->L;
+    const size_t ab = act_bytes(m);
+    const int bf = m->bf16;
+    auto half = [](int t) { return (t + 1) / 2; };
+    const int T1 = half(t_mel_max), T2 = half(T1), T3 = half(T2);
+    const int W1 = 2 + t_mel_max + (t_mel_max & 1), W2 = 2 + T1 + (T1 & 1), W3 = 2 + T2 + (T2 & 1);
+    const long long M = (long long)B * T3;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += (bytes + 255) & ~size_t(255);
+        return o;
+    };
+    const size_t o_win1 = take(ab * ((size_t)B * W1 + 4) * MEL);
+    const size_t o_win2 = take(ab * ((size_t)B * W2 + 4) * D);
+    const size_t o_win3 = take(ab * ((size_t)B * W3 + 4) * D);
+    const size_t o_y3 = take(ab * M * D);
+    const size_t o_x = take(4 * M * D);
+    const size_t o_xln = take(ab * M * D);
+    const size_t o_h = take(ab * M * F);
+    const size_t o_q = take(4 * M * D);
+    const size_t o_k = take(ab * M * D);
+    const size_t o_v = take(ab * M * D);
+    const size_t o_o = take(ab * M * D);
+    const size_t o_glu = take(ab * M * D);
+    const size_t o_yc = take(ab * M * D);
+    const size_t o_mlen = take(sizeof(int) * B);
+    const size_t o_flen = take(sizeof(int) * B);
+    if (off > m->ws.bytes) {
+        CK(cudaStreamSynchronize(s));
+        if (m->ws.base) cudaFree(m->ws.base);
+        m->ws.base = nullptr;
+        m->ws.bytes = 0;
+        if (cudaMalloc(&m->ws.base, off) != cudaSuccess) return CAC_E_NOMEM;
+        CK(cudaMemset(m->ws.base, 0, off));
+        m->ws.bytes = off;
+    }
+    char* w = static_cast<char*>(m->ws.base);
+    void *win1 = w + o_win1, *win2 = w + o_win2, *win3 = w + o_win3, *y3 = w + o_y3, *xln = w + o_xln, *h = w + o_h,
+         *kd = w + o_k, *vd = w + o_v, *o = w + o_o, *glu = w + o_glu, *yc = w + o_yc;
+    float* x = reinterpret_cast<float*>(w + o_x);
+    float* q = reinterpret_cast<float*>(w + o_q);
+    int* mlen_d = reinterpret_cast<int*>(w + o_mlen);
+    int* flen_d = reinterpret_cast<int*>(w + o_flen);
+    long long lc = 0;
+    std::vector<int> lens(B);
+    for (int b = 0; b < B; ++b) {
+        lens[b] = half(half(half(mel_len[b])));
+        out_len[b] = lens[b];
+    }
+    CK(cudaMemcpyAsync(mlen_d, mel_len, sizeof(int) * B, cudaMemcpyHostToDevice, s));
+    CK(cudaMemcpyAsync(flen_d, lens.data(), sizeof(int) * B, cudaMemcpyHostToDevice, s));
+    CK(cudaStreamSynchronize(s));  // host length arrays must outlive the copies
+    CK(cudaMemsetAsync(win2, 0, ab * ((size_t)B * W2 + 4) * D, s));
+    CK(cudaMemsetAsync(win3, 0, ab * ((size_t)B * W3 + 4) * D, s));
+    CK(launch_stage_mel_offline(mel, t_mel_max, mlen_d, win1, W1, B, bf, m->status, s));
+    ++lc;
+    {
+        EpiParams ep;
+        ep.kind = EPI_SUB;
+        ep.bias = m->sub1.b; ep.out_act = win2; ep.ldo = D;
+        ep.P = W1 / 2; ep.T_out = T1; ep.dst_rows = W2; ep.dst_off = 2;
+        RET(gemm(m, win1, 2 * MEL, B * (W1 / 2), 3 * MEL, m->sub1, MEL, ep, s, &lc));
+        ep.bias = m->sub2.b; ep.out_act = win3;
+        ep.P = W2 / 2; ep.T_out = T2; ep.dst_rows = W3; ep.dst_off = 2;
+        RET(gemm(m, win2, 2 * D, B * (W2 / 2), 3 * D, m->sub2, D, ep, s, &lc));
+        ep.bias = m->sub3.b; ep.out_act = y3;
+        ep.P = W3 / 2; ep.T_out = T3; ep.dst_rows = T3; ep.dst_off = 0;
+        RET(gemm(m, win3, 2 * D, B * (W3 / 2), 3 * D, m->sub3, D, ep, s, &lc));
+        EpiParams eo;
+        eo.kind = EPI_STORE; eo.bias = m->subo.b; eo.out_f32 = x; eo.ldo = D;
+        RET(gemm(m, y3, D, (int)M, D, m->subo, 0, eo, s, &lc));
+    }
+    CK(launch_layernorm(x, (int)M, D, m->layers[0].ff1_g, m->layers[0].ff1_b, nullptr, xln, nullptr, nullptr, nullptr,
+                        bf, 1 << 30, 0, 0, s));
+    ++lc;
+    for (int l = 0; l < L; ++l) {
+        const LayerW& Lw = m->layers[l];
+        EpiParams ep;
+        ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff1_w1.b; ep.out_act = h; ep.ldo = F;
+        RET(gemm(m, xln, D, (int)M, D, Lw.ff1_w1, 0, ep, s, &lc));
+        ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.ff1_w2.b; ep.x = x; ep.ldx = D; ep.scale = 0.5f;
+        RET(gemm(m, h, F, (int)M, F, Lw.ff1_w2, 0, ep, s, &lc));
+        CK(launch_layernorm(x, (int)M, D, Lw.att_g, Lw.att_b, nullptr, xln, nullptr, nullptr, nullptr, bf, 1 << 30, 0,
+                            0, s));
+        ep = EpiParams(); ep.kind = EPI_QKV; ep.bias = Lw.qkv.b; ep.D = D; ep.HD = m->HD; ep.dense = 1;
+        ep.kring = kd; ep.vring = vd; ep.q = q; ep.ldq = D;
+        RET(gemm(m, xln, D, (int)M, D, Lw.qkv, 0, ep, s, &lc));
+        {
+            AttnParams a;
+            a.q = q; a.ldq = D; a.k = kd; a.v = vd; a.ldk = D;
+            a.P = Lw.P; a.rmin = m->rmin; a.NR = m->NR; a.pbu = Lw.pbu; a.pbv = Lw.pbv;
+            a.out = o; a.ldo = D; a.H = m->H; a.D = D; a.HD = m->HD;
+            a.left = m->cfg.att_left; a.chunk = m->cfg.att_chunk; a.rc = m->cfg.right_context;
+            a.nb = B; a.T = T3; a.seq_len = flen_d;
+            a.scale = 1.f / std::sqrt((float)m->HD);
+            CK(launch_attention_offline(a, bf, s));
+        }
+        ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.wo.b; ep.x = x; ep.ldx = D; ep.scale = 1.f;
+        RET(gemm(m, o, D, (int)M, D, Lw.wo, 0, ep, s, &lc));
+        CK(launch_layernorm(x, (int)M, D, Lw.conv_g, Lw.conv_b, nullptr, xln, nullptr, nullptr, nullptr, bf, 1 << 30,
+                            0, 0, s));
+        ep = EpiParams(); ep.kind = EPI_GLU; ep.bias = Lw.pw1.b; ep.out_act = glu; ep.ldo = D;
+        RET(gemm(m, xln, D, (int)M, D, Lw.pw1, 0, ep, s, &lc));
+        CK(launch_dwconv(glu, nullptr, 0, nullptr, nullptr, T3, 0, Lw.dwT, Lw.bdw, Lw.bng, Lw.bnb, yc, D, B, bf, s));
+        ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.pw2.b; ep.x = x; ep.ldx = D; ep.scale = 1.f;
+        RET(gemm(m, yc, D, (int)M, D, Lw.pw2, 0, ep, s, &lc));
+        CK(launch_layernorm(x, (int)M, D, Lw.ff2_g, Lw.ff2_b, nullptr, xln, nullptr, nullptr, nullptr, bf, 1 << 30, 0,
+                            0, s));
+        ep = EpiParams(); ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff2_w1.b; ep.out_act = h; ep.ldo = F;
+        RET(gemm(m, xln, D, (int)M, D, Lw.ff2_w1, 0, ep, s, &lc));
+        ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.ff2_w2.b; ep.x = x; ep.ldx = D; ep.scale = 0.5f;
+        RET(gemm(m, h, F, (int)M, F, Lw.ff2_w2, 0, ep, s, &lc));
+        if (l + 1 < L)
+            CK(launch_layernorm(x, (int)M, D, Lw.out_g, Lw.out_b, x, nullptr, m->layers[l + 1].ff1_g,
+                                m->layers[l + 1].ff1_b, xln, bf, 1 << 30, 0, 0, s));
+        else
+            CK(launch_layernorm(x, (int)M, D, Lw.out_g, Lw.out_b, enc, xln, nullptr, nullptr, nullptr, bf, 1 << 30, 0,
+                                0, s));
+        lc += 7;
+    }
+    if (joint) {
+        EpiParams ep;
+        ep.kind = EPI_STORE; ep.bias = m->joint.b; ep.out_f32 = joint; ep.ldo = m->J;
+        RET(gemm(m, xln, D, (int)M, D, m->joint, 0, ep, s, &lc));
+    }
+    m->launches += lc;
+    return CAC_OK;
+}
+
+// ===========================================================================
+// state export / import, checks, tracing
+// ===========================================================================
+namespace {
+void act_to_host(const cac_model* m, const void* src_raw, float* dst, size_t n) {
+    if (m->bf16) {
+        const uint16_t* s = static_cast<const uint16_t*>(src_raw);
+        for (size_t i = 0; i < n; ++i) dst[i] = bf2f(s[i]);
+    } else {
+        std::memcpy(dst, src_raw, n * 4);
+    }
+}
+void host_to_act(const cac_model* m, const float* src, void* dst_raw, size_t n) {
+    if (m->bf16) {
+        uint16_t* d = static_cast<uint16_t*>(dst_raw);
+        for (size_t i = 0; i < n; ++i) d[i] = f2bf(src[i]);
+    } else {
+        std::memcpy(dst_raw, src, n * 4);
+    }
+}
+}  // namespace
+
+extern "C" int cac_stream_get_state(cac_pool* p, int id, cac_stream_state* st) {
+    if (!p || !st || id < 0 || id >= p->S || !p->alive[id]) return CAC_E_INVAL;
+    cac_model* m = p->m;
+    const int D = m->D, H = m->H, HD = m->HD, L = m->L, R = p->R, left = m->cfg.att_left;
+    const size_t ab = act_bytes(m);
+    CK(cudaDeviceSynchronize());
+    int pos = 0;
+    CK(cudaMemcpy(&pos, p->pos + id, sizeof(int), cudaMemcpyDeviceToHost));
+    st->subT = pos;
+    st->Lc = std::min(pos, left);
+    st->finished = p->finished[id];
+    st->x0_rows = 0;
+    std::vector<char> raw;
+    if (st->mel_tail) {
+        raw.resize(ab * p->tail_elems);
+        CK(cudaMemcpy(raw.data(), static_cast<char*>(p->tail) + ab * p->tail_elems * id, raw.size(),
+                      cudaMemcpyDeviceToHost));
+        if (pos == 0)
+            std::fill(st->mel_tail, st->mel_tail + p->tail_elems, 0.f);
+        else
+            act_to_host(m, raw.data(), st->mel_tail, p->tail_elems);
+    }
+    const size_t ring_layer = (size_t)H * R * HD;
+    std::vector<float> ring(ring_layer);
+    for (int kv = 0; kv < 2; ++kv) {
+        float* dst = kv == 0 ? st->k_cache : st->v_cache;
+        if (!dst) continue;
+        const char* base = static_cast<const char*>(kv == 0 ? p->kring : p->vring) + ab * p->ring_sstride * id;
+        raw.resize(ab * ring_layer);
+        for (int l = 0; l < L; ++l) {
+            CK(cudaMemcpy(raw.data(), base + ab * ring_layer * l, raw.size(), cudaMemcpyDeviceToHost));
+            act_to_host(m, raw.data(), ring.data(), ring_layer);
+            float* out = dst + (size_t)l * left * D;
+            std::fill(out, out + (size_t)left * D, 0.f);
+            for (int j = 0; j < st->Lc; ++j) {
+                const int pk = pos - st->Lc + j, slot = pk % R;
+                for (int hh = 0; hh < H; ++hh)
+                    std::memcpy(out + (size_t)j * D + hh * HD, &ring[((size_t)hh * R + slot) * HD], sizeof(float) * HD);
+            }
+        }
+    }
+    if (st->conv_cache) {
+        const size_t layer = (size_t)CONV_CACHE * D;
+        std::vector<float> cc(layer);
+        raw.resize(ab * layer);
+        const char* base = static_cast<const char*>(p->conv) + ab * p->conv_sstride * id;
+        for (int l = 0; l < L; ++l) {
+            CK(cudaMemcpy(raw.data(), base + ab * layer * l, raw.size(), cudaMemcpyDeviceToHost));
+            act_to_host(m, raw.data(), cc.data(), layer);
+            float* out = st->conv_cache + (size_t)l * layer;
+            for (int k = 0; k < CONV_CACHE; ++k) {
+                const int pk = pos - CONV_CACHE + k;
+                if (pk < 0)
+                    std::fill(out + (size_t)k * D, out + (size_t)(k + 1) * D, 0.f);
+                else
+                    std::memcpy(out + (size_t)k * D, &cc[(size_t)(pk & 7) * D], sizeof(float) * D);
+            }
+        }
+    }
+    return CAC_OK;
+}
+
+extern "C" int cac_stream_set_state(cac_pool* p, int id, const cac_stream_state* st) {
+    if (!p || !st || id < 0 || id >= p->S || !p->alive[id] || st->subT < 0) return CAC_E_INVAL;
+    cac_model* m = p->m;
+    const int D = m->D, H = m->H, HD = m->HD, L = m->L, R = p->R, left = m->cfg.att_left;
+    const size_t ab = act_bytes(m);
+    const int pos = st->subT, Lc = std::min(pos, left);
+    CK(cudaDeviceSynchronize());
+    std::vector<char> raw;
+    if (st->mel_tail) {
+        raw.resize(ab * p->tail_elems);
+        host_to_act(m, st->mel_tail, raw.data(), p->tail_elems);
+        CK(cudaMemcpy(static_cast<char*>(p->tail) + ab * p->tail_elems * id, raw.data(), raw.size(),
+                      cudaMemcpyHostToDevice));
+    }
+    const size_t ring_layer = (size_t)H * R * HD;
+    std::vector<float> ring(ring_layer, 0.f);
+    for (int kv = 0; kv < 2; ++kv) {
+        const float* src = kv == 0 ? st->k_cache : st->v_cache;
+        if (!src) continue;
+        char* base = static_cast<char*>(kv == 0 ? p->kring : p->vring) + ab * p->ring_sstride * id;
+        raw.resize(ab * ring_layer);
+        for (int l = 0; l < L; ++l) {
+            std::fill(ring.begin(), ring.end(), 0.f);
+            const float* in = src + (size_t)l * left * D;
+            for (int j = 0; j < Lc; ++j) {
+                const int pk = pos - Lc + j, slot = pk % R;
+                for (int hh = 0; hh < H; ++hh)
+                    std::memcpy(&ring[((size_t)hh * R + slot) * HD], in + (size_t)j * D + hh * HD, sizeof(float) * HD);
+            }
+            host_to_act(m, ring.data(), raw.data(), ring_layer);
+            CK(cudaMemcpy(base + ab * ring_layer * l, raw.data(), raw.size(), cudaMemcpyHostToDevice));
+        }
+    }
+    if (st->conv_cache) {
+        const size_t layer = (size_t)CONV_CACHE * D;
+        std::vector<float> cc(layer, 0.f);
+        raw.resize(ab * layer);
+        char* base = static_cast<char*>(p->conv) + ab * p->conv_sstride * id;
+        for (int l = 0; l < L; ++l) {
+            const float* in = st->conv_cache + (size_t)l * layer;
+            for (int k = 0; k < CONV_CACHE; ++k) {
+                const int pk = pos - CONV_CACHE + k;
+                if (pk >= 0) std::memcpy(&cc[(size_t)(pk & 7) * D], in + (size_t)k * D, sizeof(float) * D);
+            }
+            host_to_act(m, cc.data(), raw.data(), layer);
+            CK(cudaMemcpy(base + ab * layer * l, raw.data(), raw.size(), cudaMemcpyHostToDevice));
+        }
+    }
+    CK(cudaMemcpy(p->pos + id, &pos, sizeof(int), cudaMemcpyHostToDevice));
+    p->pos_host[id] = pos;
+    p->finished[id] = st->finished ? 1 : 0;
+    return CAC_OK;
+}
+
+extern "C" int cac_pool_check(cac_pool* p) {
+    if (!p) return CAC_E_INVAL;
+    CK(cudaDeviceSynchronize());
+    int st = 0;
+    CK(cudaMemcpy(&st, p->status, sizeof(int), cudaMemcpyDeviceToHost));
+    CK(cudaMemset(p->status, 0, sizeof(int)));
+    const int st2 = cac_model_check(p->m);
+    return st ? st : st2;
+}
+
+extern "C" int cac_pool_set_graphs(cac_pool* p, int enable) {
+    if (!p) return CAC_E_INVAL;
+    p->graphs = enable != 0;
+    return CAC_OK;
+}
+
+extern "C" long long cac_pool_launch_count(cac_pool* p) { return p ? p->launches : -1; }
+
+extern "C" int cac_pool_set_trace(cac_pool* p, int enable) {
+    if (!p) return CAC_E_INVAL;
+    if (enable && !p->trace_buf) {
+        const size_t n = ((size_t)p->m->L * N_TAPS + 1) * p->trace_rows * p->m->D;
+        if (cudaMalloc(reinterpret_cast<void**>(&p->trace_buf), n * 4) != cudaSuccess) return CAC_E_NOMEM;
+        CK(cudaMemset(p->trace_buf, 0, n * 4));
+    }
+    p->trace = enable != 0;
+    return CAC_OK;
+}
+
+extern "C" int cac_pool_read_trace(cac_pool* p, int layer, int tap, float* host, size_t n_floats) {
+    if (!p || !host || !p->trace_buf || tap < 0 || tap > N_TAPS || layer < 0 || layer >= p->m->L) return CAC_E_INVAL;
+    const size_t per = (size_t)p->trace_rows * p->m->D;
+    if (n_floats > per) return CAC_E_INVAL;
+    const float* src = tap == N_TAPS ? p->trace_buf + (size_t)p->m->L * N_TAPS * per
+                                     : p->trace_buf + ((size_t)layer * N_TAPS + tap) * per;
+    CK(cudaDeviceSynchronize());
+    CK(cudaMemcpy(host, src, n_floats * 4, cudaMemcpyDeviceToHost));
+    return CAC_OK;
+}
+
+extern "C" const char* cac_strerror(int code) {
+    switch (code) {
+        case CAC_OK: return "ok";
+        case CAC_E_INVAL: return "invalid argument";
+        case CAC_E_ALIGN: return "push not aligned to the chunk grid (multiple of att_chunk * 8 mel frames)";
+        case CAC_E_STATE: return "stream in the wrong state (dead id, or push after flush without reset)";
+        case CAC_E_NOMEM: return "out of memory or pool full";
+        case CAC_E_CUDA: return "CUDA call failed";
+        case CAC_E_DEVICE: return "device-side error";
+        case CAC_E_NONFINITE: return "non-finite value in input mel";
+        case CAC_E_TIMEOUT: return "bounded device wait gave up";
+        case CAC_E_UNSUPPORTED: return "configuration not supported by these kernels";
+    }
+    return "unknown error";
+}

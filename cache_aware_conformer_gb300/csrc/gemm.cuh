@@ -1,0 +1,182 @@
+// GEMM interface: C[M,N] = A[M,K] * B[N,K]^T with a fused epilogue.
+//
+// A holds activations (row-major, K contiguous).  For a stride-2, kernel-3
+// convolution over time A is a window buffer read in im2col form: GEMM row t,
+// K index k*C + c is window row 2t + k, channel c (the SIMT kernel reads it as
+// overlapping rows with row stride 2C; the tcgen05 kernel through a 3-D tensor
+// map).  B holds weights stored [out][in] (K-major).  Each epilogue call
+// receives one output row's 32 consecutive fp32 accumulators (col0 is a
+// multiple of 32).
+#pragma once
+
+#include "common.cuh"
+
+namespace cac {
+
+enum EpiKind : int {
+    EPI_STORE = 0,  // out = act(acc + bias) to fp32 and/or activation-dtype buffers, optional row remap
+    EPI_RESID = 1,  // x += scale * (acc + bias)                      (fp32 residual stream)
+    EPI_GLU = 2,    // 32-column segments [16 value | 16 gate] -> 16 outputs value * sigmoid(gate)
+    EPI_QKV = 3,    // Q (fp32) and K/V written into per-stream rings (or dense buffers)
+    EPI_SUB = 4,    // subsampling stage: ReLU(acc + bias), zero before stream start, row remap
+};
+enum ActKind : int { ACT_NONE = 0, ACT_RELU = 1, ACT_SILU = 2 };
+
+struct EpiParams {
+    int kind = EPI_STORE;
+    int act = ACT_NONE;
+    int act_bf16 = 1;            // activation-dtype outputs are bf16 (1) or fp32 (0)
+    const float* bias = nullptr;
+    // EPI_STORE / EPI_GLU / EPI_SUB destination
+    float* out_f32 = nullptr;
+    void* out_act = nullptr;
+    int ldo = 0;
+    // EPI_STORE row remap: out row = (r / grp) * grp_stride + (r % grp) + row_off
+    int grp = 1 << 30, grp_stride = 0, row_off = 0;
+    // EPI_RESID
+    float* x = nullptr;
+    int ldx = 0;
+    float scale = 1.f;
+    // EPI_QKV (also uses ids / pos / nq)
+    int D = 0, HD = 0, R = 0;
+    long long ring_sstride = 0;  // elements between consecutive stream ids in a ring
+    void* kring = nullptr;       // ring base already offset to this layer
+    void* vring = nullptr;
+    int dense = 0;               // 1: K/V rows go to kring/vring as dense [M][D]
+    float* q = nullptr;
+    int ldq = 0;
+    const int* ids = nullptr;    // batch slot -> stream id
+    const int* pos = nullptr;    // stream id -> absolute position of its first new frame
+    int nq = 1;                  // rows per batch slot
+    // EPI_SUB
+    int P = 1;                   // A rows (pairs) per group
+    int T_out = 1;               // valid outputs per group (the rest are seams between groups)
+    int dst_rows = 1, dst_off = 0;
+    int tmult = 0, toff = 0;     // absolute time = tmult * pos[id] - toff + t (zeroed when < 0)
+};
+
+// host helpers ---------------------------------------------------------------
+// Encode a 2-D bf16 tensor map [rows][inner] with `row_stride_bytes` between
+// rows, box [box_rows][64], 128-byte swizzle.  Returns false on failure.
+bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
+                    uint64_t row_stride_bytes, uint32_t box_rows);
+
+// Convolution view of a window buffer [rows][C] for a stride-2, kernel-3
+// convolution: 3-D map {C, 2, rows/2} (channel, row parity, row pair), box
+// {64, 1, box_rows}.  GEMM row t, K index k*C + c reads window row 2t + k.
+bool make_tmap_bf16_conv(CUtensorMap* tm, const void* base, uint64_t C, uint64_t pairs, uint32_t box_rows);
+
+// tcgen05/TMEM GEMM, bf16 operands.  K % 64 == 0, N % BN == 0, BN in {64, 128, 256}.
+// conv_C > 0 selects the convolution view of A (tmA from make_tmap_bf16_conv, K = 3 * conv_C).
+cudaError_t launch_gemm_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int BN, int conv_C,
+                           const EpiParams& ep, int* status, cudaStream_t s);
+
+// SIMT GEMM (fp32 or bf16 operands, fp32 accumulate).  N % 32 == 0.
+cudaError_t launch_gemm_simt(int bf16_operands, const void* A, long long lda, const void* B, long long ldb, int M,
+                             int N, int K, const EpiParams& ep, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// epilogue, applied to one row segment of 32 accumulators
+// ---------------------------------------------------------------------------
+template <class T>
+__device__ __forceinline__ void store32(T* dst, const float (&v)[32]);
+
+template <>
+__device__ __forceinline__ void store32<float>(float* dst, const float (&v)[32]) {
+    float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
+template <>
+__device__ __forceinline__ void store32<bf16>(bf16* dst, const float (&v)[32]) {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint4 u;
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(v[8 * i + 0], v[8 * i + 1]);
+        __nv_bfloat162 p1 = __floats2bfloat162_rn(v[8 * i + 2], v[8 * i + 3]);
+        __nv_bfloat162 p2 = __floats2bfloat162_rn(v[8 * i + 4], v[8 * i + 5]);
+        __nv_bfloat162 p3 = __floats2bfloat162_rn(v[8 * i + 6], v[8 * i + 7]);
+        u.x = *reinterpret_cast<uint32_t*>(&p0);
+        u.y = *reinterpret_cast<uint32_t*>(&p1);
+        u.z = *reinterpret_cast<uint32_t*>(&p2);
+        u.w = *reinterpret_cast<uint32_t*>(&p3);
+        d[i] = u;
+    }
+}
+
+template <int KIND, class TAct>
+__device__ __forceinline__ void epilogue32(const EpiParams& e, int row, int col0, float (&v)[32]) {
+    if (e.bias) {
+        const float4* b4 = reinterpret_cast<const float4*>(e.bias + col0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float4 b = __ldg(b4 + i);
+            v[4 * i] += b.x; v[4 * i + 1] += b.y; v[4 * i + 2] += b.z; v[4 * i + 3] += b.w;
+        }
+    }
+    if constexpr (KIND == EPI_STORE) {
+        if (e.act == ACT_SILU) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = siluf_(v[i]);
+        } else if (e.act == ACT_RELU) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.f);
+        }
+        const long long orow = (long long)(row / e.grp) * e.grp_stride + (row % e.grp) + e.row_off;
+        if (e.out_f32) store32<float>(e.out_f32 + orow * e.ldo + col0, v);
+        if (e.out_act) store32<TAct>(reinterpret_cast<TAct*>(e.out_act) + orow * e.ldo + col0, v);
+    } else if constexpr (KIND == EPI_RESID) {
+        float4* x4 = reinterpret_cast<float4*>(e.x + (long long)row * e.ldx + col0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float4 a = x4[i];
+            a.x += e.scale * v[4 * i]; a.y += e.scale * v[4 * i + 1];
+            a.z += e.scale * v[4 * i + 2]; a.w += e.scale * v[4 * i + 3];
+            x4[i] = a;
+        }
+    } else if constexpr (KIND == EPI_GLU) {
+        TAct* o = reinterpret_cast<TAct*>(e.out_act) + (long long)row * e.ldo + (col0 >> 1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] = from_f<TAct>(v[i] * sigmoidf_(v[16 + i]));
+    } else if constexpr (KIND == EPI_QKV) {
+        const int region = col0 / e.D;
+        const int cc = col0 - region * e.D;
+        if (region == 0) {
+            store32<float>(e.q + (long long)row * e.ldq + cc, v);
+            return;
+        }
+        TAct* base = reinterpret_cast<TAct*>(region == 1 ? e.kring : e.vring);
+        if (e.dense) {
+            store32<TAct>(base + (long long)row * e.D + cc, v);
+            return;
+        }
+        const int b = row / e.nq, i = row - (row / e.nq) * e.nq;
+        const int id = e.ids[b];
+        const int p = e.pos[id] + i;
+        const int slot = p % e.R;
+        TAct* sbase = base + (long long)id * e.ring_sstride;
+        if (e.HD >= 32) {
+            const int h = cc / e.HD, d0 = cc - h * e.HD;
+            store32<TAct>(sbase + ((long long)h * e.R + slot) * e.HD + d0, v);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const int d = cc + k, h = d / e.HD, dd = d - h * e.HD;
+                sbase[((long long)h * e.R + slot) * e.HD + dd] = from_f<TAct>(v[k]);
+            }
+        }
+    } else if constexpr (KIND == EPI_SUB) {
+        const int g = row / e.P, t = row - (row / e.P) * e.P;
+        if (t >= e.T_out) return;  // seam row spanning two groups
+        bool zero = false;
+        if (e.ids) zero = (e.tmult * e.pos[e.ids[g]] - e.toff + t) < 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = zero ? 0.f : fmaxf(v[i], 0.f);
+        store32<TAct>(reinterpret_cast<TAct*>(e.out_act) + ((long long)g * e.dst_rows + e.dst_off + t) * e.ldo + col0,
+                      v);
+    }
+}
+
+}  // namespace cac

@@ -1,0 +1,208 @@
+// tcgen05 / TMEM / TMA GEMM for sm_103a: C = A * B^T, bf16 operands, fp32
+// accumulation in tensor memory, fused epilogue read back with tcgen05.ld.
+//
+// One CTA computes a 128 x BN output tile with 4 warps:
+//   warp 0 lane 0  TMA producer: 64-wide K slices of A (128 rows) and B (BN rows)
+//                  into a STAGES-deep ring of 128-byte-swizzled smem tiles;
+//   warp 1 lane 0  MMA issuer: 4 x tcgen05.mma (K = 16 each) per slice, then
+//                  tcgen05.commit to release the slice back to the producer;
+//   warp 1         also owns the TMEM allocation (BN fp32 columns);
+//   warps 0-3      epilogue: warp w reads TMEM lanes 32w..32w+31 (output rows)
+//                  in 32-column chunks and applies the fused epilogue.
+// Every mbarrier wait is bounded; a wait that gives up latches
+// CAC_E_TIMEOUT in the status word and the CTA unwinds without hanging.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "gemm.cuh"
+
+namespace cac {
+
+namespace {
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int A_TILE = BM * BK * 2;  // bytes
+
+template <int BN>
+struct TcCfg {
+    static constexpr int B_TILE = BN * BK * 2;
+    static constexpr int STAGE = A_TILE + B_TILE;
+    static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/;
+};
+}  // namespace
+
+template <int BN, int KIND, class TAct>
+__global__ void __launch_bounds__(128, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
+                   int K, int conv_C, EpiParams ep, int* status) {
+    using C = TcCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + C::STAGES * A_TILE;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_TILE);
+    uint64_t* empty = full + C::STAGES;
+    uint64_t* accb = empty + C::STAGES;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+    const int nk = K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accb, 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, BN);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    bool ok = true;
+    if (warp == 0 && lane == 0) {
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % C::STAGES;
+            const uint32_t ph = (kb / C::STAGES) & 1;
+            if (!mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }
+            mbar_expect_tx(&full[s], C::STAGE);
+            if (conv_C) {
+                const int k0 = kb * BK, tap = k0 / conv_C;
+                tma_load_3d(sA + s * A_TILE, &tmA, k0 - tap * conv_C, tap & 1, m0 + (tap >> 1), &full[s]);
+            } else {
+                tma_load_2d(sA + s * A_TILE, &tmA, kb * BK, m0, &full[s]);
+            }
+            tma_load_2d(sB + s * C::B_TILE, &tmB, kb * BK, n0, &full[s]);
+        }
+    } else if (warp == 1 && lane == 0) {
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % C::STAGES;
+            const uint32_t ph = (kb / C::STAGES) & 1;
+            if (!mbar_wait(&full[s], ph)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t ad = sdesc_k_sw128(sA + s * A_TILE);
+            const uint64_t bd = sdesc_k_sw128(sB + s * C::B_TILE);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+                // +32 bytes along K inside the swizzle atom = +2 in the encoded start address
+                tc_mma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+            }
+            tc_commit(&empty[s]);
+        }
+        tc_commit(accb);
+    }
+    __syncwarp();
+
+    if (!mbar_wait(accb, 0)) ok = false;
+    tc_fence_after();
+    const int row = m0 + warp * 32 + lane;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+        if (ok && row < M) epilogue32<KIND, TAct>(ep, row, n0 + c, v);
+    }
+    if (!ok) latch_error(status, CAC_E_TIMEOUT);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, BN);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void load_encode() {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+}  // namespace
+
+bool make_tmap_bf16_conv(CUtensorMap* tm, const void* base, uint64_t C, uint64_t pairs, uint32_t box_rows) {
+    std::call_once(g_encode_once, load_encode);
+    if (!g_encode) return false;
+    if ((reinterpret_cast<uintptr_t>(base) & 15) || (C % 64) || pairs == 0) return false;
+    cuuint64_t dims[3] = {C, 2, pairs};
+    cuuint64_t strides[2] = {C * 2, C * 4};
+    cuuint32_t box[3] = {64, 1, box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
+                    uint32_t box_rows) {
+    std::call_once(g_encode_once, load_encode);
+    if (!g_encode) return false;
+    if ((reinterpret_cast<uintptr_t>(base) & 15) || (row_stride_bytes & 15) || rows == 0 || inner < 64) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BN, int KIND>
+static cudaError_t launch_bn_kind(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int conv_C,
+                                  const EpiParams& ep, int* status, cudaStream_t s) {
+    using C = TcCfg<BN>;
+    auto kern = gemm_tc_kernel<BN, KIND, bf16>;
+    static bool attr_set = false;  // per instantiation, per process
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    dim3 grid(N / BN, (M + BM - 1) / BM);
+    kern<<<grid, 128, C::SMEM, s>>>(*tmA, *tmB, M, N, K, conv_C, ep, status);
+    return cudaGetLastError();
+}
+
+template <int BN>
+static cudaError_t launch_bn(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int cc,
+                             const EpiParams& ep, int* status, cudaStream_t s) {
+    switch (ep.kind) {
+        case EPI_STORE: return launch_bn_kind<BN, EPI_STORE>(tmA, tmB, M, N, K, cc, ep, status, s);
+        case EPI_RESID: return launch_bn_kind<BN, EPI_RESID>(tmA, tmB, M, N, K, cc, ep, status, s);
+        case EPI_GLU: return launch_bn_kind<BN, EPI_GLU>(tmA, tmB, M, N, K, cc, ep, status, s);
+        case EPI_QKV: return launch_bn_kind<BN, EPI_QKV>(tmA, tmB, M, N, K, cc, ep, status, s);
+        case EPI_SUB: return launch_bn_kind<BN, EPI_SUB>(tmA, tmB, M, N, K, cc, ep, status, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int BN, int conv_C,
+                           const EpiParams& ep, int* status, cudaStream_t s) {
+    if (M <= 0) return cudaSuccess;
+    if (K % BK || K <= 0 || N % BN || !ep.act_bf16) return cudaErrorInvalidValue;
+    if (conv_C && (conv_C % BK || K != 3 * conv_C)) return cudaErrorInvalidValue;
+    switch (BN) {
+        case 64: return launch_bn<64>(tmA, tmB, M, N, K, conv_C, ep, status, s);
+        case 128: return launch_bn<128>(tmA, tmB, M, N, K, conv_C, ep, status, s);
+        case 256: return launch_bn<256>(tmA, tmB, M, N, K, conv_C, ep, status, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace cac

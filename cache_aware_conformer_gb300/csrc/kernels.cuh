@@ -1,0 +1,75 @@
+// Launchers of the non-GEMM kernels of the encoder step.
+#pragma once
+
+#include "common.cuh"
+
+namespace cac {
+
+// LayerNorm over rows of D (eps 1e-5).  y = LN(x; g1, b1) goes to y_f32
+// (row r written at (r / grp) * grp_stride + r % grp + row_off; may alias x
+// when the remap is the identity) and/or y_act; when g2 is set, z = LN(y; g2,
+// b2) goes to z_act.  act buffers are bf16 when act_bf16, else fp32.
+cudaError_t launch_layernorm(const float* x, int M, int D, const float* g1, const float* b1, float* y_f32,
+                             void* y_act, const float* g2, const float* b2, void* z_act, int act_bf16, int grp,
+                             int grp_stride, int row_off, cudaStream_t s);
+
+// Mel staging: window[b] = [melTail(id) | mel[b]] (14 + 8n rows; tail rows are
+// zero when pos[id] == 0), then melTail(id) = last 14 window rows.  mel rows of
+// stream b start at mel + b * mel_bstride; rows >= n_valid[b] (if given) read
+// as zero.  Latches CAC_E_NONFINITE on a non-finite mel value.
+cudaError_t launch_stage_mel(const float* mel, long long mel_bstride, const int* n_valid, void* win, void* tail,
+                             const int* ids, const int* pos, int n, int nb, int act_bf16, int* status,
+                             cudaStream_t s);
+
+// Offline staging: dst[b] = [2 zero rows | mel[b] (rows >= len[b] zero) | pad to W rows]
+cudaError_t launch_stage_mel_offline(const float* mel, int t_mel, const int* len, void* dst, int W, int B,
+                                     int act_bf16, int* status, cudaStream_t s);
+
+struct AttnParams {
+    const float* q = nullptr;   // fp32 queries, row stride ldq, head h at column h*HD
+    int ldq = 0;
+    const void* k = nullptr;    // ring base (layer applied) or dense [rows][ldk]
+    const void* v = nullptr;
+    long long sstride = 0;      // ring: elements between stream ids
+    int R = 0;                  // ring rows (streaming)
+    int ldk = 0;                // dense row stride (offline)
+    const int* ids = nullptr;   // streaming: batch slot -> stream id
+    const int* pos = nullptr;   // streaming: stream id -> position of the first query
+    int nq = 0;                 // streaming: queries per stream
+    const float* P = nullptr;   // position table [NR][D] for rel = rmin .. rmin + NR - 1
+    int rmin = 0, NR = 0;
+    const float* pbu = nullptr; // [H][HD]
+    const float* pbv = nullptr;
+    void* out = nullptr;        // [rows][ldo], activation dtype
+    int ldo = 0;
+    int H = 0, D = 0, HD = 0;
+    int left = 0, chunk = 1, rc = 0;  // rc > 0: window mask [p-left, p+rc]; else chunked mask
+    int nb = 0;                 // streaming: batch slots; offline: sequences
+    int T = 0;                  // offline: frames per sequence (row stride between sequences)
+    const int* seq_len = nullptr;  // offline: valid frames per sequence
+    float scale = 1.f;
+};
+
+cudaError_t launch_attention_stream(const AttnParams& a, int act_bf16, cudaStream_t s);
+cudaError_t launch_attention_offline(const AttnParams& a, int act_bf16, cudaStream_t s);
+
+// Causal depthwise conv (k = 9) + affine + SiLU over [conv cache | glu_new].
+// Streaming: cache = layer base of [S][L][8][D] rings (stride cs_stride per
+// stream id), positions from pos[ids[b]]; the first n_commit GLU rows are
+// committed to the cache.  Offline (cache == nullptr): zero left padding,
+// nq = frames per sequence, b indexes sequences directly.
+cudaError_t launch_dwconv(const void* glu, void* cache, long long cs_stride, const int* ids, const int* pos, int nq,
+                          int n_commit, const float* wT, const float* bdw, const float* bng, const float* bnb,
+                          void* out, int D, int nb, int act_bf16, cudaStream_t s);
+
+// pos[ids[b]] += n  /  pos[ids[b]] = value
+cudaError_t launch_advance(int* pos, const int* ids, int nb, int n, cudaStream_t s);
+cudaError_t launch_set_pos(int* pos, const int* ids, int nb, int value, cudaStream_t s);
+
+// pe[r][2m] = sin(r w_m), pe[r][2m+1] = cos(r w_m), w_m = 10000^(-2m/D), r = rmin + row
+cudaError_t launch_sinusoid(float* pe, int NR, int rmin, int D, cudaStream_t s);
+
+// dst fp32 [n] <- src (bf16 or fp32) [n]
+cudaError_t launch_to_f32(const void* src, float* dst, long long n, int src_bf16, cudaStream_t s);
+
+}  // namespace cac

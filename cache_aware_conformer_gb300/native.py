@@ -1,0 +1,288 @@
+"""ctypes binding of libcac.so (include/cac.h): argument marshalling only.
+
+Every computation happens in the CUDA library; this module converts Python
+objects to pointers and sizes, allocates output tensors with torch (device
+memory is plumbing, not compute) and turns status codes into exceptions.  If
+the library is not built it raises instead of falling back to anything.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_char_p, c_float, c_int, c_int32, c_longlong, c_size_t, c_void_p
+
+import numpy as np
+
+from .config import ModelConfig, DTYPE_BF16, MEL_TAIL
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcac.so")
+
+CAC_OK = 0
+ERRORS = {-1: "CAC_E_INVAL", -2: "CAC_E_ALIGN", -3: "CAC_E_STATE", -4: "CAC_E_NOMEM", -5: "CAC_E_CUDA",
+          -6: "CAC_E_DEVICE", -7: "CAC_E_NONFINITE", -8: "CAC_E_TIMEOUT", -9: "CAC_E_UNSUPPORTED"}
+
+# every symbol include/cac.h declares
+SYMBOLS = ["cac_weights_size", "cac_model_create", "cac_model_destroy", "cac_pool_create", "cac_pool_destroy",
+           "cac_stream_create", "cac_stream_destroy", "cac_stream_reset", "cac_stream_push", "cac_stream_push_host",
+           "cac_stream_flush", "cac_stream_flush_frames", "cac_encode_offline", "cac_stream_get_state",
+           "cac_stream_set_state", "cac_pool_check", "cac_model_check", "cac_pool_set_graphs",
+           "cac_pool_launch_count", "cac_pool_set_trace", "cac_pool_read_trace", "cac_strerror"]
+
+
+class CacError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {ERRORS.get(code, code)} ({_lib().cac_strerror(code).decode()})")
+
+
+class CacConfig(ctypes.Structure):
+    _fields_ = [(n, c_int32) for n in (
+        "n_layers", "d_model", "n_heads", "ff_dim", "dw_kernel", "att_left", "att_chunk", "mel_bins",
+        "joint_dim", "dtype", "right_context", "emit_frames", "lookahead_frames", "gemm_simt")]
+
+
+class CacStreamState(ctypes.Structure):
+    _fields_ = [("subT", c_int32), ("Lc", c_int32), ("finished", c_int32), ("x0_rows", c_int32),
+                ("mel_tail", POINTER(c_float)), ("k_cache", POINTER(c_float)), ("v_cache", POINTER(c_float)),
+                ("conv_cache", POINTER(c_float)), ("x0", POINTER(c_float))]
+
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, ip, fp = c_void_p, POINTER(c_int), POINTER(c_float)
+        sig = {
+            "cac_weights_size": (c_size_t, [POINTER(CacConfig)]),
+            "cac_model_create": (c_int, [POINTER(CacConfig), fp, c_size_t, POINTER(vp)]),
+            "cac_model_destroy": (None, [vp]),
+            "cac_pool_create": (c_int, [vp, c_int, c_int, POINTER(vp)]),
+            "cac_pool_destroy": (None, [vp]),
+            "cac_stream_create": (c_int, [vp, ip]),
+            "cac_stream_destroy": (c_int, [vp, c_int]),
+            "cac_stream_reset": (c_int, [vp, c_int, ip, vp]),
+            "cac_stream_push": (c_int, [vp, c_int, ip, vp, c_int, vp, vp, ip, vp]),
+            "cac_stream_push_host": (c_int, [vp, c_int, ip, fp, c_int, fp, fp, ip, vp]),
+            "cac_stream_flush": (c_int, [vp, c_int, ip, vp, c_int, ip, vp, vp, c_int, ip, vp]),
+            "cac_stream_flush_frames": (c_int, [vp, c_int, c_int, ip]),
+            "cac_encode_offline": (c_int, [vp, c_int, vp, ip, c_int, vp, vp, ip, vp]),
+            "cac_stream_get_state": (c_int, [vp, c_int, POINTER(CacStreamState)]),
+            "cac_stream_set_state": (c_int, [vp, c_int, POINTER(CacStreamState)]),
+            "cac_pool_check": (c_int, [vp]),
+            "cac_model_check": (c_int, [vp]),
+            "cac_pool_set_graphs": (c_int, [vp, c_int]),
+            "cac_pool_launch_count": (c_longlong, [vp]),
+            "cac_pool_set_trace": (c_int, [vp, c_int]),
+            "cac_pool_read_trace": (c_int, [vp, c_int, c_int, fp, c_size_t]),
+            "cac_strerror": (c_char_p, [c_int]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype, f.argtypes = res, args
+        _LIB = L
+    return _LIB
+
+
+def lib():
+    return _lib()
+
+
+def _check(code: int, what: str):
+    if code != CAC_OK:
+        raise CacError(code, what)
+
+
+def make_config(cfg: ModelConfig, gemm_simt: bool = False) -> CacConfig:
+    return CacConfig(cfg.n_layers, cfg.d_model, cfg.n_heads, cfg.ff_dim, cfg.dw_kernel, cfg.att_left,
+                     cfg.att_chunk, cfg.mel_bins, cfg.joint_dim, 1 if cfg.dtype == DTYPE_BF16 else 0,
+                     cfg.right_context, cfg.emit_frames, cfg.lookahead_frames, 1 if gemm_simt else 0)
+
+
+def weights_size(cfg: ModelConfig) -> int:
+    c = make_config(cfg)
+    return int(_lib().cac_weights_size(ctypes.byref(c)))
+
+
+def _ids(ids) -> ctypes.Array:
+    ids = [int(i) for i in ids]
+    return (c_int * len(ids))(*ids)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None) -> int | None:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class Model:
+    """A model on the current CUDA device (cac_model_create)."""
+
+    def __init__(self, cfg: ModelConfig, blob: np.ndarray, gemm_simt: bool = False):
+        self.cfg = cfg
+        blob = np.ascontiguousarray(blob, dtype=np.float32)
+        self._c = make_config(cfg, gemm_simt)
+        h = c_void_p()
+        _check(_lib().cac_model_create(ctypes.byref(self._c), blob.ctypes.data_as(POINTER(c_float)), blob.size,
+                                       ctypes.byref(h)), "cac_model_create")
+        self.h = h
+
+    def close(self):
+        if self.h:
+            _lib().cac_model_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def check(self):
+        _check(_lib().cac_model_check(self.h), "device status")
+
+    def encode_offline(self, mel, mel_len, joint: bool = True, stream=None):
+        """mel: cuda float32 [B, T_mel, 128]; returns (enc [B,T,D], joint [B,T,J] or None, out_len list)."""
+        import torch
+        B, t_mel, _ = mel.shape
+        T = t_mel
+        for _ in range(3):
+            T = (T + 1) // 2
+        enc = torch.empty(B, T, self.cfg.d_model, device=mel.device, dtype=torch.float32)
+        jt = torch.empty(B, T, self.cfg.joint_dim, device=mel.device, dtype=torch.float32) if joint else None
+        out_len = (c_int * B)()
+        _check(_lib().cac_encode_offline(self.h, B, _ptr(mel.contiguous()), _ids(mel_len), t_mel, _ptr(enc),
+                                         _ptr(jt), out_len, _stream(stream)), "cac_encode_offline")
+        return enc, jt, list(out_len)
+
+
+class Pool:
+    """Per-stream state pool (cac_pool_create) with push / flush / reset."""
+
+    def __init__(self, model: Model, max_streams: int, max_frames_per_step: int = 8):
+        self.model = model
+        self.cfg = model.cfg
+        h = c_void_p()
+        _check(_lib().cac_pool_create(model.h, max_streams, max_frames_per_step, ctypes.byref(h)),
+               "cac_pool_create")
+        self.h = h
+
+    def close(self):
+        if self.h:
+            _lib().cac_pool_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def create_stream(self) -> int:
+        i = c_int()
+        _check(_lib().cac_stream_create(self.h, ctypes.byref(i)), "cac_stream_create")
+        return i.value
+
+    def destroy_stream(self, sid: int):
+        _check(_lib().cac_stream_destroy(self.h, sid), "cac_stream_destroy")
+
+    def reset(self, ids, stream=None):
+        ids = list(ids)
+        if ids:
+            _check(_lib().cac_stream_reset(self.h, len(ids), _ids(ids), _stream(stream)), "cac_stream_reset")
+
+    def push_into(self, ids, mel, enc, joint, stream=None):
+        """Push into caller-provided outputs; returns n_out per stream."""
+        ids = list(ids)
+        n_out = (c_int * len(ids))()
+        _check(_lib().cac_stream_push(self.h, len(ids), _ids(ids), _ptr(mel), mel.shape[1], _ptr(enc),
+                                      _ptr(joint), n_out, _stream(stream)), "cac_stream_push")
+        return list(n_out)
+
+    def push(self, ids, mel, joint: bool = True, stream=None):
+        """mel: cuda float32 [n, n_mel, 128]; returns (enc [n, F, D], joint [n, F, J] or None, n_out)."""
+        import torch
+        n, n_mel, _ = mel.shape
+        F = n_mel // 8
+        enc = torch.empty(n, F, self.cfg.d_model, device=mel.device, dtype=torch.float32)
+        jt = torch.empty(n, F, self.cfg.joint_dim, device=mel.device, dtype=torch.float32) if joint else None
+        n_out = self.push_into(ids, mel.contiguous(), enc, jt, stream)
+        return enc, jt, n_out
+
+    def push_host(self, ids, mel: np.ndarray, joint: bool = True, stream=None):
+        """Host-buffer push (cac_stream_push_host): numpy in, numpy out."""
+        ids = list(ids)
+        mel = np.ascontiguousarray(mel, dtype=np.float32)
+        n, n_mel, _ = mel.shape
+        F = n_mel // 8
+        enc = np.empty((n, F, self.cfg.d_model), dtype=np.float32)
+        jt = np.empty((n, F, self.cfg.joint_dim), dtype=np.float32) if joint else None
+        n_out = (c_int * n)()
+        fp = POINTER(c_float)
+        _check(_lib().cac_stream_push_host(self.h, n, _ids(ids), mel.ctypes.data_as(fp), n_mel,
+                                           enc.ctypes.data_as(fp), jt.ctypes.data_as(fp) if jt is not None else None,
+                                           n_out, _stream(stream)), "cac_stream_push_host")
+        return enc, jt, list(n_out)
+
+    def flush(self, ids, mel, n_mel_each, joint: bool = True, stream=None):
+        """mel: cuda float32 [n, mel_stride, 128] (or None when all n_mel_each are 0)."""
+        import torch
+        ids = list(ids)
+        n = len(ids)
+        mel_stride = 0 if mel is None else mel.shape[1]
+        out_stride = max(1, max((m + 7) // 8 for m in n_mel_each))
+        dev = mel.device if mel is not None else torch.device("cuda")
+        enc = torch.zeros(n, out_stride, self.cfg.d_model, device=dev, dtype=torch.float32)
+        jt = torch.zeros(n, out_stride, self.cfg.joint_dim, device=dev, dtype=torch.float32) if joint else None
+        n_out = (c_int * n)()
+        _check(_lib().cac_stream_flush(self.h, n, _ids(ids), _ptr(mel), mel_stride, _ids(n_mel_each), _ptr(enc),
+                                       _ptr(jt), out_stride, n_out, _stream(stream)), "cac_stream_flush")
+        return enc, jt, list(n_out)
+
+    def get_state(self, sid: int) -> dict:
+        c = self.cfg
+        L, A, D = c.n_layers, c.att_left, c.d_model
+        tail = np.zeros((MEL_TAIL, c.mel_bins), np.float32)
+        k = np.zeros((L, A, D), np.float32)
+        v = np.zeros((L, A, D), np.float32)
+        conv = np.zeros((L, c.dw_kernel - 1, D), np.float32)
+        fp = POINTER(c_float)
+        st = CacStreamState(0, 0, 0, 0, tail.ctypes.data_as(fp), k.ctypes.data_as(fp), v.ctypes.data_as(fp),
+                            conv.ctypes.data_as(fp), None)
+        _check(_lib().cac_stream_get_state(self.h, sid, ctypes.byref(st)), "cac_stream_get_state")
+        return {"subT": st.subT, "Lc": st.Lc, "finished": st.finished, "mel_tail": tail, "k": k, "v": v,
+                "conv": conv}
+
+    def set_state(self, sid: int, state: dict):
+        fp = POINTER(c_float)
+        arrs = {n: np.ascontiguousarray(state[n], dtype=np.float32) for n in ("mel_tail", "k", "v", "conv")}
+        st = CacStreamState(int(state["subT"]), 0, int(state.get("finished", 0)), 0,
+                            arrs["mel_tail"].ctypes.data_as(fp), arrs["k"].ctypes.data_as(fp),
+                            arrs["v"].ctypes.data_as(fp), arrs["conv"].ctypes.data_as(fp), None)
+        _check(_lib().cac_stream_set_state(self.h, sid, ctypes.byref(st)), "cac_stream_set_state")
+
+    def check(self):
+        _check(_lib().cac_pool_check(self.h), "device status")
+
+    def set_graphs(self, on: bool):
+        _check(_lib().cac_pool_set_graphs(self.h, 1 if on else 0), "cac_pool_set_graphs")
+
+    def launch_count(self) -> int:
+        return int(_lib().cac_pool_launch_count(self.h))
+
+    def set_trace(self, on: bool):
+        _check(_lib().cac_pool_set_trace(self.h, 1 if on else 0), "cac_pool_set_trace")
+
+    def read_trace(self, layer: int, tap: int, rows: int) -> np.ndarray:
+        out = np.zeros((rows, self.cfg.d_model), np.float32)
+        _check(_lib().cac_pool_read_trace(self.h, layer, tap, out.ctypes.data_as(POINTER(c_float)), out.size),
+               "cac_pool_read_trace")
+        return out

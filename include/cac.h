@@ -1,0 +1,227 @@
+/*
+ * cac.h — C ABI of the GB300 cache-aware Conformer streaming encoder.
+ *
+ * The operation is the cache-aware Conformer encoder chunk step of the
+ * streaming Parakeet-EOU RNN-T recognizer, batched over many independent
+ * streams ("True streaming encode — implementation spec", §Per-chunk flow):
+ *   1. mel staging over [melTail | new mel] (14-frame tail, §State),
+ *   2. causal 8x subsampling, causal padding only at stream start,
+ *   3. per layer: FF1, LN -> Q/K/V, rectangular rel-pos attention over
+ *      [kCache | K_new] with the chunked-causal mask on absolute positions,
+ *      softmax, probs@V, pw1 + GLU, causal depthwise conv over
+ *      [convCache | glu_new], pw2, FF2, ln_out, K/V and conv cache update,
+ *   4. the encoder-side joint projection of every new frame (640 wide,
+ *      "Fast Accuracy-Preserving RNNT Beam Search", §1.3).
+ * Stream life cycle and API shape follow the same page's §Goal / §Status
+ * (push / reset / finish, createEncodeStream / encodeStreamPush /
+ * encodeStreamFlush) and the explicit state tensors of "Parakeet-EOU-120M —
+ * Streaming ASR Model", §Architecture.  The offline encode is the full-sequence
+ * pass with the same mask, which already emulates streaming ("True streaming
+ * encode", §Why this is provably correct).
+ *
+ * Conventions
+ *   - Every call returns CAC_OK (0) or a negative CAC_E_* code; no call throws.
+ *   - "device" pointers are CUDA global memory on the model's device, owned by
+ *     the caller, and must stay valid until the work queued on `stream`
+ *     completes.  "host" pointers are read or written before the call returns
+ *     unless stated otherwise.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls that take it are asynchronous on it.  All calls on one
+ *     pool must be ordered: issue them on one stream (or synchronize between).
+ *   - Layouts are row-major, float32 unless stated.  mel frames are
+ *     [frames][mel_bins]; encoder frames [frames][d_model]; joint frames
+ *     [frames][joint_dim].
+ *   - The library owns weights, per-stream state pools and scratch.
+ *   - Errors detected on the device (a non-finite input, a bounded wait that
+ *     gave up) are latched in a device status word and reported by
+ *     cac_pool_check() / cac_model_check().
+ */
+#ifndef CAC_H_
+#define CAC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define CAC_OK          0
+#define CAC_E_INVAL    -1   /* bad argument (null pointer, id out of range, duplicate id, bad config) */
+#define CAC_E_ALIGN    -2   /* push not a multiple of att_chunk * 8 mel frames (160 ms for chunk 2) */
+#define CAC_E_STATE    -3   /* wrong stream state (push after flush without reset, dead id) */
+#define CAC_E_NOMEM    -4   /* device or pinned-host allocation failed, or pool full */
+#define CAC_E_CUDA     -5   /* a CUDA runtime/driver call failed */
+#define CAC_E_DEVICE   -6   /* an error latched on the device (see cac_pool_check) */
+#define CAC_E_NONFINITE -7  /* non-finite value found in an input mel chunk */
+#define CAC_E_TIMEOUT  -8   /* a bounded device-side wait gave up */
+#define CAC_E_UNSUPPORTED -9 /* configuration outside what the kernels implement */
+
+#define CAC_DTYPE_F32  0    /* everything fp32 (SIMT GEMMs) */
+#define CAC_DTYPE_BF16 1    /* bf16 weights, GEMM operands and caches; fp32 accumulation,
+                               residual stream, LayerNorm, softmax and conv arithmetic */
+
+/* Model shape.  Parakeet-EOU-120M: 17 layers, d_model 512, 8 heads, ff 2048,
+ * dw_kernel 9, att_left 70, att_chunk 2, 128 mel bins, joint 640
+ * ("Parakeet-EOU-120M", §Config; "True streaming encode", §State). */
+typedef struct cac_config {
+    int32_t n_layers;
+    int32_t d_model;
+    int32_t n_heads;
+    int32_t ff_dim;
+    int32_t dw_kernel;       /* must be 9 (conv cache of 8 columns) */
+    int32_t att_left;        /* left attention context in subsampled frames (70) */
+    int32_t att_chunk;       /* chunk of the chunked-causal mask (2 = 160 ms) */
+    int32_t mel_bins;        /* must be 128 */
+    int32_t joint_dim;       /* encoder-side joint projection width (640) */
+    int32_t dtype;           /* CAC_DTYPE_* */
+    int32_t right_context;   /* 0: chunked-causal (exact streaming).  >0: window mask
+                                [p - att_left, p + right_context] with a provisional tail */
+    int32_t emit_frames;     /* provisional tail: frames emitted per pass (C*k) */
+    int32_t lookahead_frames;/* provisional tail: extra frames computed per pass (B) */
+    int32_t gemm_simt;       /* debugging aid: 1 runs bf16 GEMMs on the SIMT kernel
+                                instead of tcgen05 (same arithmetic, slower) */
+} cac_config;
+
+typedef struct cac_model cac_model;
+typedef struct cac_pool cac_pool;
+
+/* Number of floats in the weight blob for `cfg`.  The blob is the
+ * concatenation, in this order, of (all linears [out][in], subsampling convs
+ * [out][tap][in], depthwise [channel][tap]):
+ *   sub.w1[D][3][mel] sub.b1[D] sub.w2[D][3][D] sub.b2[D] sub.w3[D][3][D] sub.b3[D]
+ *   sub.wo[D][D] sub.bo[D]
+ *   per layer l:
+ *     ff1.ln_g[D] ff1.ln_b[D] ff1.w1[F][D] ff1.b1[F] ff1.w2[D][F] ff1.b2[D]
+ *     att.ln_g[D] att.ln_b[D] att.wq[D][D] att.bq[D] att.wk[D][D] att.bk[D]
+ *     att.wv[D][D] att.bv[D] att.wo[D][D] att.bo[D] att.wpos[D][D]
+ *     att.pbu[H][D/H] att.pbv[H][D/H]
+ *     conv.ln_g[D] conv.ln_b[D] conv.w_pw1[2D][D] conv.b_pw1[2D] conv.w_dw[D][9]
+ *     conv.b_dw[D] conv.bn_g[D] conv.bn_b[D] conv.w_pw2[D][D] conv.b_pw2[D]
+ *     ff2.(same six as ff1) out.ln_g[D] out.ln_b[D]
+ *   joint.w[J][D] joint.b[J]
+ * Returns 0 for an invalid config. */
+size_t cac_weights_size(const cac_config* cfg);
+
+/* Create a model on the current CUDA device from a host fp32 blob of
+ * `n_floats` values (layout above).  In bf16 mode the values are rounded to
+ * bf16 on upload.  The caller keeps ownership of `weights`. */
+int  cac_model_create(const cac_config* cfg, const float* weights, size_t n_floats, cac_model** out);
+void cac_model_destroy(cac_model* m);
+
+/* Per-stream state pool for up to `max_streams` concurrent streams and at
+ * most `max_frames_per_step` subsampled frames per internal step (1..8;
+ * larger pushes are split into several steps).  Allocates the GPU-resident
+ * caches: K/V rings [streams][layers][heads][R][head_dim], conv tail
+ * [streams][layers][8][d_model], melTail [streams][14][128], subT. */
+int  cac_pool_create(cac_model* m, int max_streams, int max_frames_per_step, cac_pool** out);
+void cac_pool_destroy(cac_pool* p);
+
+/* Stream ids are small integers in [0, max_streams). */
+int  cac_stream_create(cac_pool* p, int* id);
+int  cac_stream_destroy(cac_pool* p, int id);
+
+/* reset(): zero subT, the caches and melTail of the listed host `ids` (the
+ * caches are invalidated by position, so no memory is cleared); queued on
+ * `stream`, ordered before later pushes on the same stream. */
+int  cac_stream_reset(cac_pool* p, int n, const int* ids, void* stream);
+
+/* push(): encode `n_mel` new mel frames for each of `n` streams.
+ *   ids   host [n] distinct live, unfinished stream ids
+ *   mel   device [n][n_mel][mel_bins]
+ *   enc   device [n][n_mel/8][d_model]   (may be NULL)
+ *   joint device [n][n_mel/8][joint_dim] (may be NULL)
+ *   n_out host [n], receives the frames emitted per stream; stream b's frames
+ *         are rows 0 .. n_out[b]-1 of its enc/joint slab
+ * Chunked-causal mode: n_mel must be a positive multiple of 8*att_chunk
+ * (CAC_E_ALIGN otherwise); exactly n_mel/8 frames are emitted per stream.
+ * Provisional-tail mode: n_mel must be a positive multiple of 8*emit_frames;
+ * a stream emits frames only once lookahead_frames of lookahead exist, so
+ * n_out[b] may be 0 (a fresh stream filling its lookahead). */
+int  cac_stream_push(cac_pool* p, int n, const int* ids, const float* mel, int n_mel,
+                     float* enc, float* joint, int* n_out, void* stream);
+
+/* Same as cac_stream_push with HOST buffers: copies mel in and enc/joint out
+ * on `stream` through pinned staging owned by the pool, and synchronizes
+ * `stream` before returning (enc/joint are valid on return). */
+int  cac_stream_push_host(cac_pool* p, int n, const int* ids, const float* mel, int n_mel,
+                          float* enc, float* joint, int* n_out, void* stream);
+
+/* flush(): final partial chunk of each listed stream; afterwards the stream
+ * needs cac_stream_reset before it can push again.
+ *   mel        device [n][mel_stride][mel_bins]; stream b uses its first
+ *              n_mel_each[b] (>= 0) frames
+ *   enc/joint  device [n][out_stride][d_model / joint_dim] (may be NULL)
+ *   n_out_each host [n] receives ceil(n_mel_each[b] / 8) in chunked mode, and
+ *              every frame still held back in provisional-tail mode
+ * out_stride must be >= the largest n_out_each (see cac_stream_flush_frames). */
+int  cac_stream_flush(cac_pool* p, int n, const int* ids, const float* mel, int mel_stride,
+                      const int* n_mel_each, float* enc, float* joint, int out_stride,
+                      int* n_out_each, void* stream);
+/* Frames the flush of stream `id` with `n_mel` remaining mel frames emits. */
+int  cac_stream_flush_frames(cac_pool* p, int id, int n_mel, int* frames);
+
+/* Offline chunked-causal encode of B independent windows (no streaming state).
+ *   mel     device [B][t_mel_max][mel_bins]; window b uses mel_len[b] frames
+ *   mel_len host [B], 1 <= mel_len[b] <= t_mel_max
+ *   enc     device [B][T][d_model], T = ceil(ceil(ceil(t_mel_max/2)/2)/2)
+ *   joint   device [B][T][joint_dim] (may be NULL)
+ *   out_len host [B] receives ceil(ceil(ceil(mel_len[b]/2)/2)/2)
+ * Frames past out_len[b] are unspecified.  Scratch is owned by the model and
+ * grows on demand (the growth synchronizes `stream`). */
+int  cac_encode_offline(cac_model* m, int B, const float* mel, const int* mel_len, int t_mel_max,
+                        float* enc, float* joint, int* out_len, void* stream);
+
+/* Logical state of one stream, for snapshots and migration ("Parakeet-EOU-120M",
+ * §Architecture: state tensors passed in and returned each step).  All
+ * buffers are host memory sized by the caller (NULL skips that part):
+ *   mel_tail   [14][mel_bins]                rows oldest first (zeros before start)
+ *   k_cache    [n_layers][att_left][d_model] rows oldest first; first Lc rows valid
+ *   v_cache    [n_layers][att_left][d_model]
+ *   conv_cache [n_layers][8][d_model]        GLU outputs, oldest first
+ * get_state synchronizes the device; set_state is visible to the next push. */
+typedef struct cac_stream_state {
+    int32_t subT;      /* subsampled frames consumed (emitted, in chunked mode) */
+    int32_t Lc;        /* valid attention-cache rows = min(subT, att_left) */
+    int32_t finished;  /* 1 after flush */
+    int32_t x0_rows;   /* provisional tail: subsampled frames waiting to be emitted */
+    float* mel_tail;
+    float* k_cache;
+    float* v_cache;
+    float* conv_cache;
+    float* x0;         /* provisional tail only: [emit_frames + lookahead_frames][d_model] */
+} cac_stream_state;
+
+int  cac_stream_get_state(cac_pool* p, int id, cac_stream_state* st);
+int  cac_stream_set_state(cac_pool* p, int id, const cac_stream_state* st);
+
+/* Synchronize the device and return the latched device status (CAC_OK,
+ * CAC_E_NONFINITE, CAC_E_TIMEOUT ...), clearing it. */
+int  cac_pool_check(cac_pool* p);
+int  cac_model_check(cac_model* m);
+
+/* Capture each (batch, frames, buffers) step shape into a CUDA graph on its
+ * second use and replay it afterwards (1), or launch kernels directly (0,
+ * default). */
+int  cac_pool_set_graphs(cac_pool* p, int enable);
+
+/* Kernels this library launched on the pool since creation (a host-side
+ * counter; a graph replay counts its kernel nodes). */
+long long cac_pool_launch_count(cac_pool* p);
+
+/* Per-layer intermediate taps of the most recent push, for kernel-level
+ * parity checks.  enable=1 makes every later push copy, per layer, the fp32
+ * rows of: 0 x after FF1, 1 attention output before the out-projection,
+ * 2 x after attention, 3 GLU output, 4 conv-module activation before pw2,
+ * 5 x after the conv module, 6 x after ln_out; tap 7 = subsampled input x0
+ * (layer ignored).  Rows are the last internal step's [n][frames]. */
+int  cac_pool_set_trace(cac_pool* p, int enable);
+int  cac_pool_read_trace(cac_pool* p, int layer, int tap, float* host, size_t n_floats);
+
+const char* cac_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CAC_H_ */
