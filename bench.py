@@ -1,0 +1,468 @@
+"""Benchmark of the batched cache-aware Conformer streaming step on GB300.
+
+Workload (default): the Parakeet-EOU-120M-shaped encoder (17 layers, d_model
+512, 8 heads, ff 2048, bf16 weights, fp32 accumulation) serving 256 concurrent
+synthetic streams of 60 s.  Every step pushes 160 ms (16 mel frames, 2 encoder
+frames) for all 256 streams through the C-ABI (cac_stream_push), with caches
+resident on the GPU, random per-stream resets at 1 % per step, and stream start
+offsets drawn on 0..499 frames (even) and reached by an untimed pre-roll.
+
+One JSON line on rank 0:  value = streamed audio-seconds per second over all
+ranks (max time over ranks), e2e = the same through cac_stream_push_host with
+host buffers, roofline of the dominant kernel class (CUDA events on the
+launching stream, in a profiled pass of the same steps), the fp64 oracle timed
+on the host cores as cpu_baseline, and the SM clocks sampled during the timed
+region.  `--impl reference` times the oracle itself as the reference arm.
+
+Multi-GPU (torchrun): every rank serves its own 256 streams (its own seeds) on
+its own replica; no collective on the data path (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from cache_aware_conformer_gb300 import synth  # noqa: E402
+from cache_aware_conformer_gb300.config import WORKLOADS, FRAME_SEC  # noqa: E402
+
+METRIC = "streamed audio-sec/sec (B streams, 160 ms chunks) + % of tensor/HBM roofline"
+UNIT = "audio-s/s"
+CHUNKS_60S = 375          # 60 s = 375 pushes of 16 mel frames
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; barrier + max over ranks)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, local, world = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, local, world
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle on the host cores (spawned workers)
+# ---------------------------------------------------------------------------
+def _oracle_worker(conn, blob_path, cfg, sid, mel):
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    from oracle import conformer as O
+    blob = np.load(blob_path, mmap_mode="r")
+    enc = O.StreamingEncoder(synth.unpack_weights(cfg, blob), cfg)
+    k = 0
+    conn.send("ready")
+    while True:
+        cmd = conn.recv()
+        if cmd is None:
+            break
+        for _ in range(cmd):
+            enc.push(mel[16 * k: 16 * (k + 1)])
+            k += 1
+        conn.send("done")
+
+
+class OracleFarm:
+    """`cores` worker processes, one stream each, stepping 160 ms chunks on command."""
+
+    def __init__(self, cfg, blob, cores: int, n_chunks: int):
+        import multiprocessing as mp
+        for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[v] = "1"
+        ctx = mp.get_context("spawn")
+        self.tmp = tempfile.mkdtemp(prefix="cac_oracle_")
+        self.blob_path = os.path.join(self.tmp, "w.npy")
+        np.save(self.blob_path, blob)
+        self.cores = cores
+        self.procs, self.conns = [], []
+        for c in range(cores):
+            a, b = ctx.Pipe()
+            mel = synth.make_mel(16 * n_chunks, 100000 + c)
+            p = ctx.Process(target=_oracle_worker, args=(b, self.blob_path, cfg, c, mel), daemon=True)
+            p.start()
+            self.procs.append(p)
+            self.conns.append(a)
+        for a in self.conns:
+            assert a.recv() == "ready"
+
+    def step(self, chunks: int = 1) -> float:
+        t = time.perf_counter()
+        for a in self.conns:
+            a.send(chunks)
+        for a in self.conns:
+            assert a.recv() == "done"
+        return time.perf_counter() - t
+
+    def close(self):
+        for a in self.conns:
+            a.send(None)
+        for p in self.procs:
+            p.join(timeout=30)
+        try:
+            os.unlink(self.blob_path)
+            os.rmdir(self.tmp)
+        except OSError:
+            pass
+
+
+def cpu_cores() -> int:
+    return max(1, min(os.cpu_count() or 1, 16))
+
+
+# ---------------------------------------------------------------------------
+# roofline bookkeeping: algorithmic work per launch of each kernel class
+# ---------------------------------------------------------------------------
+def algorithmic_work(cfg, S, n, mean_lc):
+    """Per launch: ('tensor', flops) for GEMMs, ('hbm', bytes) for the rest."""
+    D, F, J, L, H = cfg.d_model, cfg.ff_dim, cfg.joint_dim, cfg.n_layers, cfg.n_heads
+    M = S * n
+    W1, W2, W3 = 14 + 8 * n, 4 * n + 6, 2 * n + 2
+    sub_flops = 2 * D * (S * (W1 // 2) * 3 * 128 + S * (W2 // 2) * 3 * D + S * (W3 // 2) * 3 * D) / 3.0
+    kv = S * (mean_lc + n) * D * 2 * 2                  # K and V rows read, bf16
+    nr = cfg.att_left + cfg.att_chunk                   # position-table rows
+    return {
+        "gemm_ff_up": ("tensor", 2.0 * M * F * D),
+        "gemm_ff_down": ("tensor", 2.0 * M * D * F),
+        "gemm_qkv": ("tensor", 2.0 * M * 3 * D * D),
+        "gemm_out_proj": ("tensor", 2.0 * M * D * D),
+        "gemm_pw1_glu": ("tensor", 2.0 * M * 2 * D * D),
+        "gemm_pw2": ("tensor", 2.0 * M * D * D),
+        "gemm_joint": ("tensor", 2.0 * M * J * D),
+        "gemm_sub_out": ("tensor", 2.0 * M * D * D),
+        "gemm_subsample": ("tensor", sub_flops),
+        # q fp32 in, K/V cache + new rows, output bf16, position table fp32
+        "attention": ("hbm", kv + M * D * 4 + M * D * 2 + nr * D * 4),
+        # GLU rows in, conv tail (8 rows) in, n rows committed, output
+        "dwconv": ("hbm", M * D * 2 + S * 8 * D * 2 + M * D * 2 + M * D * 2 + 12 * D * 4),
+        "layernorm": ("hbm", M * D * 4 + M * D * 2 + M * D * 4),
+        "stage_mel": ("hbm", S * (8 * n + 14) * 128 * 4 + S * W1 * 128 * 2 + S * 14 * 128 * 2),
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops_sustained"], "measured"
+    return 6800.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# the streaming workload
+# ---------------------------------------------------------------------------
+class StreamWorkload:
+    def __init__(self, wl, rank: int, device, steps_needed: int, workers: int):
+        import torch
+        from cache_aware_conformer_gb300 import native
+        self.wl, self.cfg = wl, wl.model
+        self.S = wl.streams
+        self.dev = device
+        self.push_mel = wl.push_mel
+        self.n = wl.push_mel // 8
+        base = rank * self.S
+        self.offsets = synth.start_offsets(self.S, wl.max_start_offset, seed=7 + rank)
+        self.pre = (self.offsets // self.n).astype(np.int64)      # pre-roll pushes per stream
+        W = synth.make_weights_parallel(self.cfg, seed=0, workers=workers)
+        self.blob = synth.pack_weights(self.cfg, W)
+        del W
+        mel = synth.make_mels_parallel(CHUNKS_60S * 16, range(base, base + self.S), wl.silence_frac, workers)
+        self.mel = torch.from_numpy(mel).to(device).view(self.S, CHUNKS_60S, 16, 128)
+        del mel
+        self.model = native.Model(self.cfg, self.blob)
+        self.pool = native.Pool(self.model, self.S, max_frames_per_step=max(2, self.n))
+        self.ids = [self.pool.create_stream() for _ in range(self.S)]
+        # pre-roll: stream s pushes its first pre[s] chunks (untimed, eager)
+        for r in range(int(self.pre.max()) if self.S else 0):
+            sel = np.nonzero(self.pre > r)[0]
+            chunk = self.mel[torch.from_numpy(sel).to(device), r].contiguous()
+            self.pool.push([self.ids[i] for i in sel], chunk, joint=False)
+        self.pool.check()
+        # per-step inputs: chunk index of every stream, arranged contiguously per step
+        self.t = 0
+        self.steps = steps_needed
+        cidx = (self.pre[None, :] + np.arange(steps_needed)[:, None]) % CHUNKS_60S       # [steps, S]
+        ar = torch.arange(self.S, device=device)
+        self.step_mel = torch.stack([self.mel[ar, torch.from_numpy(c).to(device)] for c in cidx])
+        self.cidx = cidx
+        self.resets = [np.nonzero(synth.reset_mask(self.S, t, wl.reset_prob, seed=11 + rank) | (cidx[t] == 0))[0]
+                       for t in range(steps_needed)]
+        self.staging = torch.empty(self.S, 16, 128, device=device)
+        self.enc = torch.empty(self.S, self.n, self.cfg.d_model, device=device)
+        self.joint = torch.empty(self.S, self.n, self.cfg.joint_dim, device=device)
+        self.lc_hist = []
+        self.subT = self.pre * self.n
+
+    def step(self):
+        """One timed step: resets drawn for this step, then one 160 ms push of all streams."""
+        t = self.t
+        r = self.resets[t]
+        if len(r):
+            self.pool.reset([self.ids[i] for i in r])
+            self.subT[r] = 0
+        self.lc_hist.append(float(np.minimum(self.subT, self.cfg.att_left).mean()))
+        self.staging.copy_(self.step_mel[t])
+        self.pool.push_into(self.ids, self.staging, self.enc, self.joint)
+        self.subT += self.n
+        self.t += 1
+
+    def step_host(self, mel_host):
+        t = self.t
+        r = self.resets[t]
+        if len(r):
+            self.pool.reset([self.ids[i] for i in r])
+            self.subT[r] = 0
+        enc, joint, _ = self.pool.push_host(self.ids, mel_host)
+        self.subT += self.n
+        self.t += 1
+        return enc, joint
+
+
+def run_ours(args, wl):
+    import torch
+    rank, local, world = dist_init("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    K, Wm = args.steps, args.warmup
+    Kp = min(K, args.profile_steps)
+    Ke = min(K, args.e2e_steps)
+    total_steps = Wm + K + Kp + Ke
+    workers = max(1, min(cpu_cores(), 16))
+    w = StreamWorkload(wl, rank, dev, total_steps, workers)
+    w.pool.set_graphs(True)
+    for _ in range(Wm):
+        w.step()
+    torch.cuda.synchronize()
+    # ---- timed region: K steps, device-timed with CUDA events on the launching stream
+    barrier()
+    torch.cuda.synchronize()
+    vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip().isdigit()]
+    clocks = ClockSampler(int(vis[local]) if local < len(vis) else local)
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = w.pool.launch_count()
+    lc0 = len(w.lc_hist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed")
+    e0.record()
+    for _ in range(K):
+        w.step()
+    e1.record()
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    ms = e0.elapsed_time(e1)
+    launches = w.pool.launch_count() - launches0
+    mean_lc = float(np.mean(w.lc_hist[lc0:]))
+    w.pool.check()
+    ms_max = max_over_ranks(ms, dev)
+    audio = world * w.S * w.n * FRAME_SEC * K
+    value = audio / (ms_max / 1e3)
+
+    # ---- profiled pass of the same steps: per-kernel-class CUDA events
+    w.pool.set_profile(True)
+    w.pool.read_profile()
+    for _ in range(Kp):
+        w.step()
+    prof = w.pool.read_profile()
+    w.pool.set_profile(False)
+    hbm_peak, tf_peak, peak_src = load_peaks()
+    work = algorithmic_work(w.cfg, w.S, w.n, mean_lc)
+    kernels = {}
+    for name, (tot, cnt) in prof.items():
+        if cnt == 0:
+            continue
+        ent = {"total_ms_per_step": tot / Kp, "launches_per_step": cnt / Kp, "avg_us": 1e3 * tot / cnt}
+        if name in work:
+            bound, amount = work[name]
+            if bound == "tensor":
+                ach = amount / (tot / cnt * 1e-3) / 1e12
+                ent.update(bound="tensor", achieved=ach, unit="TFLOP/s", frac=ach / tf_peak)
+            else:
+                ach = amount / (tot / cnt * 1e-3) / 1e9
+                ent.update(bound="hbm", achieved=ach, unit="GB/s", frac=ach / hbm_peak)
+        kernels[name] = ent
+    dom = max((k for k in kernels if "bound" in kernels[k]), key=lambda k: kernels[k]["total_ms_per_step"])
+    d = kernels[dom]
+    roofline = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"],
+                "peak": tf_peak if d["bound"] == "tensor" else hbm_peak, "unit": d["unit"], "frac": d["frac"],
+                "traffic": None,
+                "peak_source": f"{peak_src} ({'bf16 sustained' if d['bound'] == 'tensor' else 'HBM copy'})",
+                "per_launch": work[dom][1], "avg_launch_us": d["avg_us"]}
+
+    # ---- end to end through the C-ABI with host buffers (copies inside the timed region)
+    host_mels = [w.step_mel[w.t + i].cpu().numpy() for i in range(Ke)]
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(Ke):
+        w.step_host(host_mels[i])
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
+    e2e = {"value": world * w.S * w.n * FRAME_SEC * Ke / e2e_s, "unit": UNIT,
+           "h2d_bytes_per_step": w.S * w.push_mel * 128 * 4,
+           "d2h_bytes_per_step": w.S * w.n * (w.cfg.d_model + w.cfg.joint_dim) * 4}
+    w.pool.check()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w.cfg, w.blob, args.cpu_chunks)
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": Wm,
+                "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": wl.name, "streams_per_gpu": w.S, "chunk_ms": 160,
+                           "layers": w.cfg.n_layers, "d_model": w.cfg.d_model, "heads": w.cfg.n_heads,
+                           "ff": w.cfg.ff_dim, "att_left": w.cfg.att_left, "att_chunk": w.cfg.att_chunk,
+                           "reset_prob": wl.reset_prob, "start_offsets": f"even, 0..{wl.max_start_offset - 1}",
+                           "mean_Lc": mean_lc, "parallelism": f"replicas x{world}",
+                           "l2": "inputs larger than L2: each step reads all K/V rings (~713 MB) "
+                                 "and all weights (~210 MB)"},
+                "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches, "clocks": clk}
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(cfg, blob, chunks: int):
+    """The oracle as it stands, one stream per host core, `chunks` pushes each."""
+    cores = cpu_cores()
+    farm = OracleFarm(cfg, blob, cores, chunks + 1)
+    try:
+        farm.step(1)                      # first push (stream start) untimed
+        secs = farm.step(chunks)
+    finally:
+        farm.close()
+    return {"value": cores * chunks * 0.16 / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{cores} streams x {chunks} pushes of 160 ms (one stream per core, fp64 numpy, "
+                      f"17-layer model); {secs:.1f} s wall"}
+
+
+def run_reference(args, wl):
+    """Reference arm: the fp64 oracle itself on the host cores, same metric and config.
+    Each step = one 160 ms push of a sample of streams (one per core)."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    cfg = wl.model
+    W = synth.make_weights_parallel(cfg, seed=0, workers=cpu_cores())
+    blob = synth.pack_weights(cfg, W)
+    del W
+    cores = cpu_cores()
+    K, Wm = min(args.steps, args.ref_steps), min(args.warmup, 3)
+    farm = OracleFarm(cfg, blob, cores, Wm + K + 1)
+    try:
+        farm.step(1 + Wm)
+        secs = farm.step(K)
+    finally:
+        farm.close()
+    value = cores * K * 0.16 / secs
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": Wm, "ms_per_step": 1e3 * secs / K, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "streams_sampled": cores, "chunk_ms": 160,
+                       "layers": cfg.n_layers, "d_model": cfg.d_model},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{cores} of {wl.streams} streams, {K} pushes of 160 ms each"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="eou120m_256streams_60s", choices=sorted(WORKLOADS))
+    ap.add_argument("--profile-steps", type=int, default=40)
+    ap.add_argument("--e2e-steps", type=int, default=40)
+    ap.add_argument("--cpu-chunks", type=int, default=6)
+    ap.add_argument("--ref-steps", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -432,6 +432,11 @@ struct cac_pool {
     long long launches = 0;
     long long ring_sstride = 0, conv_sstride = 0;
     size_t tail_elems = 0;
+    // per-kernel-class CUDA-event timing (eager launches only)
+    bool prof = false;
+    std::vector<cudaEvent_t> ev;          // event pool, reused after each read
+    std::vector<std::pair<int, int>> rec; // (class, index of the start event; end = start + 1)
+    int prof_cls = -1;
 };
 
 namespace {
@@ -481,6 +486,35 @@ int trace_tap(cac_pool* p, int layer, int tap, const void* src, bool src_act, in
     return CAC_OK;
 }
 
+const char* const PROF_NAMES[] = {"stage_mel", "gemm_subsample", "gemm_sub_out", "layernorm",
+                                  "gemm_ff_up", "gemm_ff_down", "gemm_qkv", "attention", "gemm_out_proj",
+                                  "gemm_pw1_glu", "dwconv", "gemm_pw2", "gemm_joint", "advance", "reset"};
+constexpr int N_PROF = 15;
+enum { P_STAGE, P_SUB, P_SUBOUT, P_LN, P_FFUP, P_FFDOWN, P_QKV, P_ATT, P_OUT, P_PW1, P_DW, P_PW2, P_JOINT,
+       P_ADV, P_RESET };
+
+// Open a timed region of class `cls` on stream s (no-op unless profiling).
+int prof_begin(cac_pool* p, int cls, cudaStream_t s) {
+    if (!p->prof) return CAC_OK;
+    const size_t need = 2 * (p->rec.size() + 1);
+    while (p->ev.size() < need) {
+        cudaEvent_t e;
+        CK(cudaEventCreate(&e));
+        p->ev.push_back(e);
+    }
+    const int i = (int)(2 * p->rec.size());
+    p->rec.push_back({cls, i});
+    CK(cudaEventRecord(p->ev[i], s));
+    return CAC_OK;
+}
+int prof_end(cac_pool* p, cudaStream_t s) {
+    if (!p->prof) return CAC_OK;
+    CK(cudaEventRecord(p->ev[p->rec.back().second + 1], s));
+    return CAC_OK;
+}
+#define PB(cls) RET(prof_begin(p, cls, s))
+#define PE() RET(prof_end(p, s))
+
 // One step: nb batch slots (ids already in p->ids_dev), n new frames each.
 //   mel: stream b's first mel row at mel + b * mel_bstride (8n rows; with
 //        nvalid, rows >= nvalid[b] read as zero)
@@ -495,7 +529,9 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
     const int bf = m->bf16;
 
     // 1. mel staging: [melTail | mel] windows, tail update
+    PB(P_STAGE);
     CK(launch_stage_mel(mel, mel_bstride, nvalid, p->win1, p->tail, p->ids_dev, p->pos, n, nb, bf, p->status, s));
+    PE();
     ++*lc;
     // 2. three stride-2 convolutions (implicit GEMMs over the windows) + out linear
     const int W1 = TAIL + 8 * n, W2 = 4 * n + 6, W3 = 2 * n + 2;
@@ -508,15 +544,21 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
         ep.ids = p->ids_dev;
         ep.pos = p->pos;
         ep.P = W1 / 2; ep.T_out = W2; ep.dst_rows = W2; ep.dst_off = 0; ep.tmult = 4; ep.toff = 6;
+        PB(P_SUB);
         RET(gemm(m, p->win1, 2 * MEL, nb * (W1 / 2), 3 * MEL, m->sub1, MEL, ep, s, lc));
+        PE();
         ep.bias = m->sub2.b;
         ep.out_act = p->win3;
         ep.P = W2 / 2; ep.T_out = W3; ep.dst_rows = W3; ep.tmult = 2; ep.toff = 2;
+        PB(P_SUB);
         RET(gemm(m, p->win2, 2 * D, nb * (W2 / 2), 3 * D, m->sub2, D, ep, s, lc));
+        PE();
         ep.bias = m->sub3.b;
         ep.out_act = p->y3;
         ep.P = W3 / 2; ep.T_out = n; ep.dst_rows = n; ep.tmult = 1; ep.toff = 0;
+        PB(P_SUB);
         RET(gemm(m, p->win3, 2 * D, nb * (W3 / 2), 3 * D, m->sub3, D, ep, s, lc));
+        PE();
     }
     {
         EpiParams ep;
@@ -524,11 +566,15 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
         ep.bias = m->subo.b;
         ep.out_f32 = p->x;
         ep.ldo = D;
+        PB(P_SUBOUT);
         RET(gemm(m, p->y3, D, M, D, m->subo, 0, ep, s, lc));
+        PE();
     }
     RET(trace_tap(p, 0, N_TAPS, p->x, false, M, s));
+    PB(P_LN);
     CK(launch_layernorm(p->x, M, D, m->layers[0].ff1_g, m->layers[0].ff1_b, nullptr, p->xln, nullptr, nullptr,
                         nullptr, bf, 1 << 30, 0, 0, s));
+    PE();
     ++*lc;
 
     for (int l = 0; l < L; ++l) {
@@ -536,20 +582,28 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
         EpiParams ep;
         // FF1: x += 1/2 * (W2 SiLU(W1 LN(x) + b1) + b2)   (LN(x) already in xln)
         ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff1_w1.b; ep.out_act = p->h; ep.ldo = F;
+        PB(P_FFUP);
         RET(gemm(m, p->xln, D, M, D, Lw.ff1_w1, 0, ep, s, lc));
+        PE();
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.ff1_w2.b; ep.x = p->x; ep.ldx = D; ep.scale = 0.5f;
+        PB(P_FFDOWN);
         RET(gemm(m, p->h, F, M, F, Lw.ff1_w2, 0, ep, s, lc));
+        PE();
         RET(trace_tap(p, l, 0, p->x, false, M, s));
         // attention: xln = LN(x); Q and K/V into the rings
+        PB(P_LN);
         CK(launch_layernorm(p->x, M, D, Lw.att_g, Lw.att_b, nullptr, p->xln, nullptr, nullptr, nullptr, bf,
                             1 << 30, 0, 0, s));
+        PE();
         ++*lc;
         ep = EpiParams(); ep.kind = EPI_QKV; ep.bias = Lw.qkv.b; ep.D = D; ep.HD = m->HD; ep.R = p->R;
         ep.ring_sstride = p->ring_sstride;
         ep.kring = static_cast<char*>(p->kring) + (long long)l * m->H * p->R * m->HD * ab;
         ep.vring = static_cast<char*>(p->vring) + (long long)l * m->H * p->R * m->HD * ab;
         ep.q = p->q; ep.ldq = D; ep.ids = p->ids_dev; ep.pos = p->pos; ep.nq = n;
+        PB(P_QKV);
         RET(gemm(m, p->xln, D, M, D, Lw.qkv, 0, ep, s, lc));
+        PE();
         {
             AttnParams a;
             a.q = p->q; a.ldq = D;
@@ -561,45 +615,66 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
             a.left = m->cfg.att_left; a.chunk = m->cfg.att_chunk; a.rc = 0;
             a.nb = nb;
             a.scale = 1.f / std::sqrt((float)m->HD);
+            PB(P_ATT);
             CK(launch_attention_stream(a, bf, s));
+            PE();
             ++*lc;
         }
         RET(trace_tap(p, l, 1, p->o, true, M, s));
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.wo.b; ep.x = p->x; ep.ldx = D; ep.scale = 1.f;
+        PB(P_OUT);
         RET(gemm(m, p->o, D, M, D, Lw.wo, 0, ep, s, lc));
+        PE();
         RET(trace_tap(p, l, 2, p->x, false, M, s));
         // conv module
+        PB(P_LN);
         CK(launch_layernorm(p->x, M, D, Lw.conv_g, Lw.conv_b, nullptr, p->xln, nullptr, nullptr, nullptr, bf,
                             1 << 30, 0, 0, s));
+        PE();
         ++*lc;
         ep = EpiParams(); ep.kind = EPI_GLU; ep.bias = Lw.pw1.b; ep.out_act = p->glu; ep.ldo = D;
+        PB(P_PW1);
         RET(gemm(m, p->xln, D, M, D, Lw.pw1, 0, ep, s, lc));
+        PE();
         RET(trace_tap(p, l, 3, p->glu, true, M, s));
+        PB(P_DW);
         CK(launch_dwconv(p->glu, static_cast<char*>(p->conv) + (long long)l * CONV_CACHE * D * ab, p->conv_sstride,
                          p->ids_dev, p->pos, n, n, Lw.dwT, Lw.bdw, Lw.bng, Lw.bnb, p->yc, D, nb, bf, s));
+        PE();
         ++*lc;
         RET(trace_tap(p, l, 4, p->yc, true, M, s));
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.pw2.b; ep.x = p->x; ep.ldx = D; ep.scale = 1.f;
+        PB(P_PW2);
         RET(gemm(m, p->yc, D, M, D, Lw.pw2, 0, ep, s, lc));
+        PE();
         RET(trace_tap(p, l, 5, p->x, false, M, s));
         // FF2
+        PB(P_LN);
         CK(launch_layernorm(p->x, M, D, Lw.ff2_g, Lw.ff2_b, nullptr, p->xln, nullptr, nullptr, nullptr, bf,
                             1 << 30, 0, 0, s));
+        PE();
         ++*lc;
         ep = EpiParams(); ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff2_w1.b; ep.out_act = p->h; ep.ldo = F;
+        PB(P_FFUP);
         RET(gemm(m, p->xln, D, M, D, Lw.ff2_w1, 0, ep, s, lc));
+        PE();
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.ff2_w2.b; ep.x = p->x; ep.ldx = D; ep.scale = 0.5f;
+        PB(P_FFDOWN);
         RET(gemm(m, p->h, F, M, F, Lw.ff2_w2, 0, ep, s, lc));
+        PE();
         // ln_out, fused with the next layer's FF1 LayerNorm (or, after the last
         // layer, writing the encoder frames to the caller and the joint input)
+        PB(P_LN);
         if (l + 1 < L) {
             CK(launch_layernorm(p->x, M, D, Lw.out_g, Lw.out_b, p->x, nullptr, m->layers[l + 1].ff1_g,
                                 m->layers[l + 1].ff1_b, p->xln, bf, 1 << 30, 0, 0, s));
+            PE();
             ++*lc;
             RET(trace_tap(p, l, 6, p->x, false, M, s));
         } else {
             CK(launch_layernorm(p->x, M, D, Lw.out_g, Lw.out_b, enc ? enc : p->x, p->xln, nullptr, nullptr, nullptr,
                                 bf, enc ? n : 1 << 30, enc ? out_bstride : 0, enc ? out_off : 0, s));
+            PE();
             ++*lc;
             RET(trace_tap(p, l, 6, p->xln, true, M, s));
         }
@@ -611,9 +686,13 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
         ep.out_f32 = joint;
         ep.ldo = m->J;
         ep.grp = n; ep.grp_stride = out_bstride; ep.row_off = out_off;
+        PB(P_JOINT);
         RET(gemm(m, p->xln, D, M, D, m->joint, 0, ep, s, lc));
+        PE();
     }
+    PB(P_ADV);
     CK(launch_advance(p->pos, p->ids_dev, nb, n, s));
+    PE();
     ++*lc;
     return CAC_OK;
 }
@@ -621,7 +700,7 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
 // run_step through the graph cache when graphs are enabled
 int step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride, const int* nvalid, float* enc,
          float* joint, int out_bstride, int out_off, cudaStream_t s) {
-    if (!p->graphs || p->trace)
+    if (!p->graphs || p->trace || p->prof)
         return run_step(p, nb, n, mel, mel_bstride, nvalid, enc, joint, out_bstride, out_off, s);
     GraphKey key{nb, n, nvalid ? 1 : 0, mel, enc, joint, mel_bstride, out_bstride, out_off};
     GraphEntry& g = p->gcache[key];
@@ -734,6 +813,7 @@ extern "C" void cac_pool_destroy(cac_pool* p) {
     if (p->d_out) cudaFree(p->d_out);
     for (int k = 0; k < ID_SLOTS; ++k)
         if (p->slot_ev[k]) cudaEventDestroy(p->slot_ev[k]);
+    for (cudaEvent_t e : p->ev) cudaEventDestroy(e);
     delete p;
 }
 
@@ -767,7 +847,9 @@ extern "C" int cac_stream_reset(cac_pool* p, int n, const int* ids, void* stream
     RET(check_ids(p, n, ids, false));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     RET(upload_ids(p, ids, n, p->rids_dev, s));
+    PB(P_RESET);
     CK(launch_set_pos(p->pos, p->rids_dev, n, 0, s));
+    PE();
     ++p->launches;
     for (int i = 0; i < n; ++i) {
         p->pos_host[ids[i]] = 0;
@@ -1214,6 +1296,35 @@ extern "C" int cac_pool_read_trace(cac_pool* p, int layer, int tap, float* host,
                                      : p->trace_buf + ((size_t)layer * N_TAPS + tap) * per;
     CK(cudaDeviceSynchronize());
     CK(cudaMemcpy(host, src, n_floats * 4, cudaMemcpyDeviceToHost));
+    return CAC_OK;
+}
+
+extern "C" int cac_pool_set_profile(cac_pool* p, int enable) {
+    if (!p) return CAC_E_INVAL;
+    p->prof = enable != 0;
+    return CAC_OK;
+}
+
+extern "C" int cac_profile_classes(void) { return N_PROF; }
+
+extern "C" const char* cac_profile_class_name(int cls) {
+    return (cls >= 0 && cls < N_PROF) ? PROF_NAMES[cls] : nullptr;
+}
+
+extern "C" int cac_pool_read_profile(cac_pool* p, int n_classes, double* total_ms, long long* launches) {
+    if (!p || !total_ms || !launches || n_classes < N_PROF) return CAC_E_INVAL;
+    CK(cudaDeviceSynchronize());
+    for (int c = 0; c < n_classes; ++c) {
+        total_ms[c] = 0.0;
+        launches[c] = 0;
+    }
+    for (const auto& r : p->rec) {
+        float ms = 0.f;
+        CK(cudaEventElapsedTime(&ms, p->ev[r.second], p->ev[r.second + 1]));
+        total_ms[r.first] += ms;
+        launches[r.first] += 1;
+    }
+    p->rec.clear();
     return CAC_OK;
 }
 

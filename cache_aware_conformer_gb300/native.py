@@ -26,7 +26,8 @@ SYMBOLS = ["cac_weights_size", "cac_model_create", "cac_model_destroy", "cac_poo
            "cac_stream_create", "cac_stream_destroy", "cac_stream_reset", "cac_stream_push", "cac_stream_push_host",
            "cac_stream_flush", "cac_stream_flush_frames", "cac_encode_offline", "cac_stream_get_state",
            "cac_stream_set_state", "cac_pool_check", "cac_model_check", "cac_pool_set_graphs",
-           "cac_pool_launch_count", "cac_pool_set_trace", "cac_pool_read_trace", "cac_strerror"]
+           "cac_pool_launch_count", "cac_pool_set_trace", "cac_pool_read_trace", "cac_pool_set_profile",
+           "cac_pool_read_profile", "cac_profile_classes", "cac_profile_class_name", "cac_strerror"]
 
 
 class CacError(RuntimeError):
@@ -79,6 +80,10 @@ def _lib():
             "cac_pool_launch_count": (c_longlong, [vp]),
             "cac_pool_set_trace": (c_int, [vp, c_int]),
             "cac_pool_read_trace": (c_int, [vp, c_int, c_int, fp, c_size_t]),
+            "cac_pool_set_profile": (c_int, [vp, c_int]),
+            "cac_pool_read_profile": (c_int, [vp, c_int, POINTER(ctypes.c_double), POINTER(c_longlong)]),
+            "cac_profile_classes": (c_int, []),
+            "cac_profile_class_name": (c_char_p, [c_int]),
             "cac_strerror": (c_char_p, [c_int]),
         }
         for name, (res, args) in sig.items():
@@ -277,6 +282,17 @@ class Pool:
 
     def launch_count(self) -> int:
         return int(_lib().cac_pool_launch_count(self.h))
+
+    def set_profile(self, on: bool):
+        _check(_lib().cac_pool_set_profile(self.h, 1 if on else 0), "cac_pool_set_profile")
+
+    def read_profile(self) -> dict:
+        """{class name: (total ms, launches)} since the previous read (synchronizes)."""
+        n = _lib().cac_profile_classes()
+        ms = (ctypes.c_double * n)()
+        cnt = (c_longlong * n)()
+        _check(_lib().cac_pool_read_profile(self.h, n, ms, cnt), "cac_pool_read_profile")
+        return {_lib().cac_profile_class_name(i).decode(): (ms[i], cnt[i]) for i in range(n)}
 
     def set_trace(self, on: bool):
         _check(_lib().cac_pool_set_trace(self.h, 1 if on else 0), "cac_pool_set_trace")

@@ -123,22 +123,7 @@ def weights_size(cfg: ModelConfig) -> int:
 
 def make_weights(cfg: ModelConfig, seed: int = 0) -> dict:
     """Named float32 parameter arrays (bf16-representable in bf16 configurations)."""
-    out = {}
-    for tid, (name, shape, kind) in enumerate(weight_layout(cfg)):
-        n = int(np.prod(shape))
-        k = key(seed, tid)
-        if kind == "gain":
-            v = 0.9 + 0.2 * uniform(k, np.arange(n, dtype=np.uint64))
-        elif kind == "bias":
-            v = 0.02 * normal(k, n)
-        else:
-            _, fi, fo = kind
-            v = np.sqrt(2.0 / (fi + fo)) * normal(k, n)
-        v = v.astype(np.float32).reshape(shape)
-        if cfg.dtype == DTYPE_BF16:
-            v = round_bf16(v).reshape(shape)
-        out[name] = v
-    return out
+    return dict(_make_tensor((cfg, seed, tid)) for tid in range(len(weight_layout(cfg))))
 
 
 def pack_weights(cfg: ModelConfig, w: dict) -> np.ndarray:
@@ -187,3 +172,53 @@ def reset_mask(n_streams: int, step: int, prob: float, seed: int = 11) -> np.nda
         return np.zeros(n_streams, dtype=bool)
     idx = np.arange(n_streams, dtype=np.uint64) * np.uint64(1 << 32) + np.uint64(step)
     return uniform(key(seed, TID_RESETS), idx) < prob
+
+
+def unpack_weights(cfg: ModelConfig, blob: np.ndarray) -> dict:
+    """Inverse of pack_weights: named views into a flat float32 blob."""
+    out, off = {}, 0
+    for name, shape, _ in weight_layout(cfg):
+        n = int(np.prod(shape))
+        out[name] = np.asarray(blob[off:off + n]).reshape(shape)
+        off += n
+    assert off == blob.size
+    return out
+
+
+def _make_tensor(args):
+    cfg, seed, tid = args
+    name, shape, kind = weight_layout(cfg)[tid]
+    n = int(np.prod(shape))
+    k = key(seed, tid)
+    if kind == "gain":
+        v = 0.9 + 0.2 * uniform(k, np.arange(n, dtype=np.uint64))
+    elif kind == "bias":
+        v = 0.02 * normal(k, n)
+    else:
+        _, fi, fo = kind
+        v = np.sqrt(2.0 / (fi + fo)) * normal(k, n)
+    v = v.astype(np.float32).reshape(shape)
+    if cfg.dtype == DTYPE_BF16:
+        v = round_bf16(v).reshape(shape)
+    return name, v
+
+
+def make_weights_parallel(cfg: ModelConfig, seed: int = 0, workers: int = 8) -> dict:
+    """Same values as make_weights, generated by a spawn process pool."""
+    import multiprocessing as mp
+    tids = list(range(len(weight_layout(cfg))))
+    with mp.get_context("spawn").Pool(workers) as pool:
+        items = pool.map(_make_tensor, [(cfg, seed, t) for t in tids], chunksize=4)
+    return dict(items)
+
+
+def _mel_job(args):
+    n_frames, sid, silence_frac = args
+    return make_mel(n_frames, sid, silence_frac=silence_frac)
+
+
+def make_mels_parallel(n_frames: int, stream_ids, silence_frac: float = 0.2, workers: int = 8) -> np.ndarray:
+    """[len(stream_ids), n_frames, 128] synthetic mel, generated by a spawn process pool."""
+    import multiprocessing as mp
+    with mp.get_context("spawn").Pool(workers) as pool:
+        return np.stack(pool.map(_mel_job, [(n_frames, int(s), silence_frac) for s in stream_ids]))

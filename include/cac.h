@@ -219,6 +219,17 @@ long long cac_pool_launch_count(cac_pool* p);
 int  cac_pool_set_trace(cac_pool* p, int enable);
 int  cac_pool_read_trace(cac_pool* p, int layer, int tap, float* host, size_t n_floats);
 
+/* Per-kernel-class timing with CUDA events recorded on the launching stream
+ * around every kernel of later pushes and resets (launches run eagerly while
+ * enabled).  cac_pool_read_profile synchronizes the device and fills, for each
+ * class 0 .. cac_profile_classes()-1, the summed kernel time in ms and the
+ * launch count since the previous read, then clears them.  Class names:
+ * cac_profile_class_name ("gemm_ff_up", "attention", "dwconv", ...). */
+int  cac_pool_set_profile(cac_pool* p, int enable);
+int  cac_pool_read_profile(cac_pool* p, int n_classes, double* total_ms, long long* launches);
+int  cac_profile_classes(void);
+const char* cac_profile_class_name(int cls);
+
 const char* cac_strerror(int code);
 
 #ifdef __cplusplus
