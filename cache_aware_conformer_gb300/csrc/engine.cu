@@ -138,7 +138,7 @@ int upload_lin(cac_model* m, const float* w, const float* b, int N, int K, Lin* 
         RET(upload_f32(m, hb.data(), N, &lin->b));
     }
     if (m->tc) {
-        lin->BN = (N % 128 == 0) ? 128 : 64;
+        lin->BN = 64;  // 128 x 64 tiles: M = 512 rows already give 4 x N/64 CTAs
         if (N % lin->BN || K % 64) return CAC_E_UNSUPPORTED;
         if (!make_tmap_bf16(&lin->tm, p, K, N, (uint64_t)K * 2, lin->BN)) return CAC_E_CUDA;
     }
@@ -616,7 +616,7 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
             a.nb = nb;
             a.scale = 1.f / std::sqrt((float)m->HD);
             PB(P_ATT);
-            CK(launch_attention_stream(a, bf, s));
+            CK(launch_attention_stream(a, bf, p->status, s));
             PE();
             ++*lc;
         }
@@ -1087,7 +1087,7 @@ extern "C" int cac_encode_offline(cac_model* m, int B, const float* mel, const i
             a.left = m->cfg.att_left; a.chunk = m->cfg.att_chunk; a.rc = m->cfg.right_context;
             a.nb = B; a.T = T3; a.seq_len = flen_d;
             a.scale = 1.f / std::sqrt((float)m->HD);
-            CK(launch_attention_offline(a, bf, s));
+            CK(launch_attention_offline(a, bf, m->status, s));
         }
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.wo.b; ep.x = x; ep.ldx = D; ep.scale = 1.f;
         RET(gemm(m, o, D, (int)M, D, Lw.wo, 0, ep, s, &lc));

@@ -180,76 +180,14 @@ cudaError_t launch_stage_mel_offline(const float* mel, int t_mel, const int* len
 // against Nk keys at positions kpos0 .. kpos0+Nk-1.
 //   score[i][j] = ((q_i + u) . k_j + (q_i + v) . P[pq_i - pk_j]) * scale,
 // masked (chunked-causal on absolute positions, or a window), softmax over j,
-// out_i = sum_j prob[i][j] v_j.  Scores: lane per key (the key row is held in
-// registers and reused by every query); P rows come from a per-head table in
-// shared memory padded to HD + 4 floats (conflict-free for consecutive rel).
-// probs @ V: lane per HD/32 output dims, one coalesced V row per key.
+// out_i = sum_j prob[i][j] v_j.
+// The warp's K and V rows are staged in shared memory by TMA bulk copies
+// (cp.async.bulk on one mbarrier) issued before anything else, so the whole
+// HBM read of the warp is in flight at once; the block's per-head position
+// table is loaded while they land.  Scores: lane per key, 16-byte chunks of
+// the key row read in a lane-rotated order (conflict-free shared loads).
+// probs @ V: lane per HD/32 output dims, V rows from shared memory.
 // ---------------------------------------------------------------------------
-template <class T, int HD>
-__device__ __forceinline__ void load_row(const T* src, float (&dst)[HD]);
-
-template <>
-__device__ __forceinline__ void load_row<bf16, 64>(const bf16* src, float (&dst)[64]) {
-    const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        uint4 u = __ldg(s + i);
-        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            float2 f = __bfloat1622float2(p[k]);
-            dst[8 * i + 2 * k] = f.x;
-            dst[8 * i + 2 * k + 1] = f.y;
-        }
-    }
-}
-template <>
-__device__ __forceinline__ void load_row<float, 64>(const float* src, float (&dst)[64]) {
-    const float4* s = reinterpret_cast<const float4*>(src);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        float4 f = __ldg(s + i);
-        dst[4 * i] = f.x; dst[4 * i + 1] = f.y; dst[4 * i + 2] = f.z; dst[4 * i + 3] = f.w;
-    }
-}
-template <>
-__device__ __forceinline__ void load_row<float, 16>(const float* src, float (&dst)[16]) {
-    const float4* s = reinterpret_cast<const float4*>(src);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float4 f = __ldg(s + i);
-        dst[4 * i] = f.x; dst[4 * i + 1] = f.y; dst[4 * i + 2] = f.z; dst[4 * i + 3] = f.w;
-    }
-}
-template <>
-__device__ __forceinline__ void load_row<bf16, 16>(const bf16* src, float (&dst)[16]) {
-    const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        uint4 u = __ldg(s + i);
-        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            float2 f = __bfloat1622float2(p[k]);
-            dst[8 * i + 2 * k] = f.x;
-            dst[8 * i + 2 * k + 1] = f.y;
-        }
-    }
-}
-
-template <class T>
-struct RingRows {  // key/value rows of one stream and head in a ring of R slots
-    const T* base;
-    int R, HD;
-    __device__ __forceinline__ const T* row(int p) const { return base + (long long)(p % R) * HD; }
-};
-template <class T>
-struct DenseRows {  // rows of one sequence (and head) in a dense [frames][ld] buffer
-    const T* base;
-    int ld;
-    __device__ __forceinline__ const T* row(int p) const { return base + (long long)p * ld; }
-};
-
 __device__ __forceinline__ bool allowed(const AttnParams& a, int pq, int pk) {
     if (pk < 0) return false;
     if (a.rc > 0) return pk >= pq - a.left && pk <= pq + a.rc;
@@ -257,50 +195,122 @@ __device__ __forceinline__ bool allowed(const AttnParams& a, int pq, int pk) {
     return pk >= c - a.left && pk <= c + a.chunk - 1;
 }
 
-template <int HD, int NQ, int NK, class T, class Rows>
-__device__ void attend_warp(const AttnParams& a, int h, const float* Ps, float* wsm, int lane, const float* qsrc,
-                            int pq0, int nq, Rows krows, Rows vrows, int kpos0, int Nk, T* dst) {
+template <int HD, int NQ, int NK, class T>
+struct AttnLayout {
+    static constexpr int KV = NK * HD;                                   // elements of K (or V)
+    static constexpr int WARP_BYTES = 16 + 2 * KV * (int)sizeof(T) + 4 * (2 * NQ * HD + NQ * NK);
+    static constexpr int PS = HD + 4;                                    // padded position-table row
+};
+
+template <int HD, int NQ, int NK, class T>
+__device__ __forceinline__ void attn_carve(uint8_t* wsm, uint64_t*& bar, T*& Ks, T*& Vs, float*& qu, float*& qv,
+                                           float*& S) {
+    using Lay = AttnLayout<HD, NQ, NK, T>;
+    bar = reinterpret_cast<uint64_t*>(wsm);
+    Ks = reinterpret_cast<T*>(wsm + 16);
+    Vs = Ks + Lay::KV;
+    qu = reinterpret_cast<float*>(Vs + Lay::KV);
+    qv = qu + NQ * HD;
+    S = qv + NQ * HD;
+}
+
+template <int HD>
+__device__ void load_ptable(const AttnParams& a, int h, float* Ps) {
     constexpr int PS = HD + 4;
+    for (int e = threadIdx.x; e < a.NR * HD; e += blockDim.x) {
+        const int r = e / HD, d = e - (e / HD) * HD;
+        Ps[r * PS + d] = __ldg(a.P + (long long)r * a.D + h * HD + d);
+    }
+}
+
+template <class T, int EPC>
+__device__ __forceinline__ void chunk_to_f(const T* src, float (&f)[EPC]);
+template <>
+__device__ __forceinline__ void chunk_to_f<bf16, 8>(const bf16* src, float (&f)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(src);
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 t = __bfloat1622float2(p[k]);
+        f[2 * k] = t.x;
+        f[2 * k + 1] = t.y;
+    }
+}
+template <>
+__device__ __forceinline__ void chunk_to_f<float, 4>(const float* src, float (&f)[4]) {
+    const float4 u = *reinterpret_cast<const float4*>(src);
+    f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
+}
+
+// Everything after the K/V copies were issued on `bar`.
+template <int HD, int NQ, int NK, class T>
+__device__ void attend_warp(const AttnParams& a, int h, const float* Ps, uint8_t* wsm, int lane, const float* qsrc,
+                            int pq0, int nq, int kpos0, int Nk, T* dst, int* status) {
+    using Lay = AttnLayout<HD, NQ, NK, T>;
+    constexpr int PS = Lay::PS;
     constexpr int DPL = HD >= 32 ? HD / 32 : 1;
-    float* qu = wsm;
-    float* qv = qu + NQ * HD;
-    float* S = qv + NQ * HD;
+    constexpr int EPC = 16 / (int)sizeof(T);  // elements per 16-byte chunk
+    constexpr int CPR = HD / EPC;             // chunks per row
+    uint64_t* bar;
+    T *Ks, *Vs;
+    float *qu, *qv, *S;
+    attn_carve<HD, NQ, NK, T>(wsm, bar, Ks, Vs, qu, qv, S);
     for (int e = lane; e < nq * HD; e += 32) {
         const int i = e / HD, d = e - (e / HD) * HD;
         const float qq = qsrc[(long long)i * a.ldq + d];
         qu[i * HD + d] = qq + __ldg(a.pbu + h * HD + d);
         qv[i * HD + d] = qq + __ldg(a.pbv + h * HD + d);
     }
+    const bool landed = mbar_wait(bar, 0);
     __syncwarp();
+    if (!landed) {
+        if (lane == 0) latch_error(status, CAC_E_TIMEOUT);
+        return;
+    }
+    // scores
     for (int j0 = 0; j0 < Nk; j0 += 32) {
         const int j = j0 + lane;
         const bool valid = j < Nk;
-        float kr[HD];
         const int pk = kpos0 + j;
-        if (valid) load_row<T, HD>(krows.row(pk), kr);
-#pragma unroll 1
-        for (int i = 0; i < nq; ++i) {
-            const int pq = pq0 + i;
-            float s = -FLT_MAX;
-            if (valid && allowed(a, pq, pk)) {
-                const float* pr = Ps + (pq - pk - a.rmin) * PS;
-                const float* qa = qu + i * HD;
-                const float* qb = qv + i * HD;
-                float acc = 0.f;
+        float acc[NQ];
+        bool ok[NQ];
+        int prow[NQ];
 #pragma unroll
-                for (int d = 0; d < HD; d += 4) {
-                    const float4 p4 = *reinterpret_cast<const float4*>(pr + d);
-                    const float4 ua = *reinterpret_cast<const float4*>(qa + d);
-                    const float4 va = *reinterpret_cast<const float4*>(qb + d);
-                    acc += ua.x * kr[d] + ua.y * kr[d + 1] + ua.z * kr[d + 2] + ua.w * kr[d + 3];
-                    acc += va.x * p4.x + va.y * p4.y + va.z * p4.z + va.w * p4.w;
+        for (int i = 0; i < NQ; ++i) {
+            acc[i] = 0.f;
+            ok[i] = i < nq && valid && allowed(a, pq0 + i, pk);
+            prow[i] = ok[i] ? (pq0 + i - pk - a.rmin) * PS : 0;
+        }
+        if (valid) {
+            const T* krow = Ks + j * HD;
+#pragma unroll 1
+            for (int c = 0; c < CPR; ++c) {
+                const int cc = (c + lane) & (CPR - 1);
+                float kf[EPC];
+                chunk_to_f<T, EPC>(krow + cc * EPC, kf);
+#pragma unroll
+                for (int i = 0; i < NQ; ++i) {
+                    if (!ok[i]) continue;
+                    const float* qa = qu + i * HD + cc * EPC;
+                    const float* qb = qv + i * HD + cc * EPC;
+                    const float* pr = Ps + prow[i] + cc * EPC;
+#pragma unroll
+                    for (int e = 0; e < EPC; e += 4) {
+                        const float4 ua = *reinterpret_cast<const float4*>(qa + e);
+                        const float4 va = *reinterpret_cast<const float4*>(qb + e);
+                        const float4 p4 = *reinterpret_cast<const float4*>(pr + e);
+                        acc[i] += ua.x * kf[e] + ua.y * kf[e + 1] + ua.z * kf[e + 2] + ua.w * kf[e + 3];
+                        acc[i] += va.x * p4.x + va.y * p4.y + va.z * p4.z + va.w * p4.w;
+                    }
                 }
-                s = acc * a.scale;
             }
-            if (valid) S[i * NK + j] = s;
+#pragma unroll
+            for (int i = 0; i < NQ; ++i)
+                if (i < nq) S[i * NK + j] = ok[i] ? acc[i] * a.scale : -FLT_MAX;
         }
     }
     __syncwarp();
+    // softmax over the keys of each query
 #pragma unroll 1
     for (int i = 0; i < nq; ++i) {
         float m = -FLT_MAX;
@@ -318,6 +328,7 @@ __device__ void attend_warp(const AttnParams& a, int h, const float* Ps, float* 
         for (int j = lane; j < Nk; j += 32) S[i * NK + j] *= inv;
     }
     __syncwarp();
+    // probs @ V
     float acc[NQ][DPL];
 #pragma unroll
     for (int i = 0; i < NQ; ++i)
@@ -325,11 +336,11 @@ __device__ void attend_warp(const AttnParams& a, int h, const float* Ps, float* 
         for (int t = 0; t < DPL; ++t) acc[i][t] = 0.f;
     const int d0 = lane * DPL;
     const bool dl = d0 < HD;
+#pragma unroll 4
     for (int j = 0; j < Nk; ++j) {
         float vv[DPL];
-        const T* vr = vrows.row(kpos0 + j);
 #pragma unroll
-        for (int t = 0; t < DPL; ++t) vv[t] = dl ? to_f(vr[d0 + t]) : 0.f;
+        for (int t = 0; t < DPL; ++t) vv[t] = dl ? to_f(Vs[j * HD + d0 + t]) : 0.f;
 #pragma unroll
         for (int i = 0; i < NQ; ++i) {
             if (i >= nq) break;
@@ -350,132 +361,175 @@ __device__ void attend_warp(const AttnParams& a, int h, const float* Ps, float* 
 
 constexpr int ATT_WARPS = 4;
 
-template <int HD, int NQ, int NK>
-__host__ __device__ constexpr int attn_warp_floats() { return 2 * NQ * HD + NQ * NK; }
-
-template <int HD>
-__device__ void load_ptable(const AttnParams& a, int h, float* Ps) {
-    constexpr int PS = HD + 4;
-    for (int e = threadIdx.x; e < a.NR * HD; e += blockDim.x) {
-        const int r = e / HD, d = e - (e / HD) * HD;
-        Ps[r * PS + d] = __ldg(a.P + (long long)r * a.D + h * HD + d);
-    }
-}
-
-// streaming: block = (ATT_WARPS batch slots, head); keys = [cache | new] from the ring
+// streaming: block = (ATT_WARPS batch slots, head); keys = [cache | new] from the ring,
+// whose rows for one stream and head are contiguous modulo R: at most two copies each.
 template <int HD, int NQ, int NK, class T>
-__global__ void __launch_bounds__(ATT_WARPS * 32) attn_stream_kernel(AttnParams a) {
+__global__ void __launch_bounds__(ATT_WARPS * 32) attn_stream_kernel(AttnParams a, int* status) {
+    using Lay = AttnLayout<HD, NQ, NK, T>;
     extern __shared__ float4 sm4[];
-    float* sm = reinterpret_cast<float*>(sm4);
+    uint8_t* sm = reinterpret_cast<uint8_t*>(sm4);
     const int h = blockIdx.y;
-    float* Ps = sm;
-    load_ptable<HD>(a, h, Ps);
-    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * ATT_WARPS + warp;
-    if (b >= a.nb) return;
-    float* wsm = sm + a.NR * (HD + 4) + warp * attn_warp_floats<HD, NQ, NK>();
-    const int id = a.ids[b];
-    const int p0 = a.pos[id];
-    const int Lc = min(p0, a.left);
-    const int kpos0 = p0 - Lc;
-    const int Nk = min(Lc + a.nq, NK);
-    const T* kb = static_cast<const T*>(a.k) + (long long)id * a.sstride + (long long)h * a.R * HD;
-    const T* vb = static_cast<const T*>(a.v) + (long long)id * a.sstride + (long long)h * a.R * HD;
-    attend_warp<HD, NQ, NK, T>(a, h, Ps, wsm, lane, a.q + (long long)b * a.nq * a.ldq + h * HD, p0, a.nq,
-                               RingRows<T>{kb, a.R, HD}, RingRows<T>{vb, a.R, HD}, kpos0, Nk,
-                               static_cast<T*>(a.out) + (long long)b * a.nq * a.ldo + h * HD);
+    const bool live = b < a.nb;
+    float* Ps = reinterpret_cast<float*>(sm);
+    uint8_t* wsm = sm + ((a.NR * Lay::PS * 4 + 15) & ~15) + warp * Lay::WARP_BYTES;
+    int id = 0, p0 = 0, Lc = 0, Nk = 0;
+    if (live) {
+        id = a.ids[b];
+        p0 = a.pos[id];
+        Lc = min(p0, a.left);
+        Nk = min(Lc + a.nq, NK);
+        if (lane == 0) {
+            uint64_t* bar;
+            T *Ks, *Vs;
+            float *qu, *qv, *S;
+            attn_carve<HD, NQ, NK, T>(wsm, bar, Ks, Vs, qu, qv, S);
+            mbar_init(bar, 1);
+            fence_mbar_init();
+            constexpr uint32_t ROW = HD * sizeof(T);
+            mbar_expect_tx(bar, 2u * ROW * Nk);
+            const long long base = (long long)id * a.sstride + (long long)h * a.R * HD;
+            const T* kb = static_cast<const T*>(a.k) + base;
+            const T* vb = static_cast<const T*>(a.v) + base;
+            const int s0 = (p0 - Lc) % a.R;
+            const int n1 = min(Nk, a.R - s0);
+            bulk_g2s(Ks, kb + (long long)s0 * HD, ROW * n1, bar);
+            bulk_g2s(Vs, vb + (long long)s0 * HD, ROW * n1, bar);
+            if (Nk > n1) {
+                bulk_g2s(Ks + n1 * HD, kb, ROW * (Nk - n1), bar);
+                bulk_g2s(Vs + n1 * HD, vb, ROW * (Nk - n1), bar);
+            }
+        }
+    }
+    load_ptable<HD>(a, h, Ps);
+    __syncthreads();
+    if (!live) return;
+    attend_warp<HD, NQ, NK, T>(a, h, Ps, wsm, lane, a.q + (long long)b * a.nq * a.ldq + h * HD, p0, a.nq, p0 - Lc,
+                               Nk, static_cast<T*>(a.out) + (long long)b * a.nq * a.ldo + h * HD, status);
 }
 
 // offline: block = (ATT_WARPS query groups of one sequence, head); keys from dense K/V
+// rows (one bulk copy per row, issued by the lanes of the warp).
 template <int HD, int NQ, int NK, class T>
-__global__ void __launch_bounds__(ATT_WARPS * 32) attn_offline_kernel(AttnParams a, int qgroup) {
+__global__ void __launch_bounds__(ATT_WARPS * 32) attn_offline_kernel(AttnParams a, int qgroup, int* status) {
+    using Lay = AttnLayout<HD, NQ, NK, T>;
     extern __shared__ float4 sm4[];
-    float* sm = reinterpret_cast<float*>(sm4);
+    uint8_t* sm = reinterpret_cast<uint8_t*>(sm4);
     const int h = blockIdx.y, seq = blockIdx.z;
-    float* Ps = sm;
-    load_ptable<HD>(a, h, Ps);
-    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int len = a.seq_len[seq];
     const int pq0 = (blockIdx.x * ATT_WARPS + warp) * qgroup;
-    if (pq0 >= len) return;
-    const int nq = min(qgroup, len - pq0);
-    const int pql = pq0 + nq - 1;
-    int klo, khi;
-    if (a.rc > 0) {
-        klo = max(pq0 - a.left, 0);
-        khi = min(pql + a.rc, len - 1);
-    } else {
-        klo = max((pq0 / a.chunk) * a.chunk - a.left, 0);
-        khi = min((pql / a.chunk) * a.chunk + a.chunk - 1, len - 1);
-    }
-    const int Nk = min(khi - klo + 1, NK);
-    float* wsm = sm + a.NR * (HD + 4) + warp * attn_warp_floats<HD, NQ, NK>();
+    const bool live = pq0 < len;
+    float* Ps = reinterpret_cast<float*>(sm);
+    uint8_t* wsm = sm + ((a.NR * Lay::PS * 4 + 15) & ~15) + warp * Lay::WARP_BYTES;
+    int nq = 0, klo = 0, Nk = 0;
     const long long rb = (long long)seq * a.T;
-    const T* kb = static_cast<const T*>(a.k) + rb * a.ldk + h * HD;
-    const T* vb = static_cast<const T*>(a.v) + rb * a.ldk + h * HD;
-    attend_warp<HD, NQ, NK, T>(a, h, Ps, wsm, lane, a.q + (rb + pq0) * a.ldq + h * HD, pq0, nq,
-                               DenseRows<T>{kb, a.ldk}, DenseRows<T>{vb, a.ldk}, klo, Nk,
-                               static_cast<T*>(a.out) + (rb + pq0) * a.ldo + h * HD);
+    if (live) {
+        nq = min(qgroup, len - pq0);
+        const int pql = pq0 + nq - 1;
+        int khi;
+        if (a.rc > 0) {
+            klo = max(pq0 - a.left, 0);
+            khi = min(pql + a.rc, len - 1);
+        } else {
+            klo = max((pq0 / a.chunk) * a.chunk - a.left, 0);
+            khi = min((pql / a.chunk) * a.chunk + a.chunk - 1, len - 1);
+        }
+        Nk = min(khi - klo + 1, NK);
+        uint64_t* bar;
+        T *Ks, *Vs;
+        float *qu, *qv, *S;
+        attn_carve<HD, NQ, NK, T>(wsm, bar, Ks, Vs, qu, qv, S);
+        constexpr uint32_t ROW = HD * sizeof(T);
+        if (lane == 0) {
+            mbar_init(bar, 1);
+            fence_mbar_init();
+            mbar_expect_tx(bar, 2u * ROW * Nk);
+        }
+        __syncwarp();
+        const T* kb = static_cast<const T*>(a.k) + rb * a.ldk + h * HD;
+        const T* vb = static_cast<const T*>(a.v) + rb * a.ldk + h * HD;
+        for (int j = lane; j < Nk; j += 32) {
+            bulk_g2s(Ks + j * HD, kb + (long long)(klo + j) * a.ldk, ROW, bar);
+            bulk_g2s(Vs + j * HD, vb + (long long)(klo + j) * a.ldk, ROW, bar);
+        }
+    }
+    load_ptable<HD>(a, h, Ps);
+    __syncthreads();
+    if (!live) return;
+    attend_warp<HD, NQ, NK, T>(a, h, Ps, wsm, lane, a.q + (rb + pq0) * a.ldq + h * HD, pq0, nq, klo, Nk,
+                               static_cast<T*>(a.out) + (rb + pq0) * a.ldo + h * HD, status);
 }
 
 template <int HD, int NQ, int NK, class T>
-static cudaError_t attn_stream_launch(const AttnParams& a, cudaStream_t s) {
-    const size_t smem = sizeof(float) * (a.NR * (HD + 4) + ATT_WARPS * attn_warp_floats<HD, NQ, NK>());
+static size_t attn_smem(const AttnParams& a) {
+    using Lay = AttnLayout<HD, NQ, NK, T>;
+    return ((size_t)a.NR * Lay::PS * 4 + 15) / 16 * 16 + (size_t)ATT_WARPS * Lay::WARP_BYTES;
+}
+
+template <class K>
+static cudaError_t raise_smem(K kern, size_t smem, size_t& attr) {
+    if (smem <= attr) return cudaSuccess;
+    if (smem > 200 * 1024) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e == cudaSuccess) attr = 200 * 1024;
+    return e;
+}
+
+template <int HD, int NQ, int NK, class T>
+static cudaError_t attn_stream_launch(const AttnParams& a, int* status, cudaStream_t s) {
+    const size_t smem = attn_smem<HD, NQ, NK, T>(a);
     auto kern = attn_stream_kernel<HD, NQ, NK, T>;
-    static size_t attr = 48 * 1024;  // dynamic smem limit set so far for this instantiation
-    if (smem > attr) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
-        if (e != cudaSuccess) return e;
-        attr = 100 * 1024;
-    }
-    if (smem > attr) return cudaErrorInvalidValue;
+    static size_t attr = 48 * 1024;  // dynamic shared memory limit set so far for this instantiation
+    cudaError_t e = raise_smem(kern, smem, attr);
+    if (e != cudaSuccess) return e;
     dim3 grid((a.nb + ATT_WARPS - 1) / ATT_WARPS, a.H);
-    kern<<<grid, ATT_WARPS * 32, smem, s>>>(a);
+    kern<<<grid, ATT_WARPS * 32, smem, s>>>(a, status);
     return cudaGetLastError();
 }
 
 template <int HD, int NQ, int NK, class T>
-static cudaError_t attn_offline_launch(const AttnParams& a, int qgroup, cudaStream_t s) {
-    const size_t smem = sizeof(float) * (a.NR * (HD + 4) + ATT_WARPS * attn_warp_floats<HD, NQ, NK>());
+static cudaError_t attn_offline_launch(const AttnParams& a, int qgroup, int* status, cudaStream_t s) {
+    const size_t smem = attn_smem<HD, NQ, NK, T>(a);
     auto kern = attn_offline_kernel<HD, NQ, NK, T>;
     static size_t attr = 48 * 1024;
-    if (smem > attr) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
-        if (e != cudaSuccess) return e;
-        attr = 100 * 1024;
-    }
-    if (smem > attr) return cudaErrorInvalidValue;
+    cudaError_t e = raise_smem(kern, smem, attr);
+    if (e != cudaSuccess) return e;
     const int groups = (a.T + qgroup - 1) / qgroup;
     dim3 grid((groups + ATT_WARPS - 1) / ATT_WARPS, a.H, a.nb);
-    kern<<<grid, ATT_WARPS * 32, smem, s>>>(a, qgroup);
+    kern<<<grid, ATT_WARPS * 32, smem, s>>>(a, qgroup, status);
     return cudaGetLastError();
 }
 
-// NQ x NK instantiations: chunked streaming (n <= 8, keys <= left + 8),
-// provisional passes (n <= 24, keys <= left + 24), offline groups of <= 8.
-cudaError_t launch_attention_stream(const AttnParams& a, int act_bf16, cudaStream_t s) {
+#define ATT_DISPATCH(LAUNCH, NQ, NK, ...)                                                                  \
+    do {                                                                                                   \
+        if (a.HD == 64)                                                                                    \
+            return act_bf16 ? LAUNCH<64, NQ, NK, bf16>(__VA_ARGS__) : LAUNCH<64, NQ, NK, float>(__VA_ARGS__); \
+        if (a.HD == 16)                                                                                    \
+            return act_bf16 ? LAUNCH<16, NQ, NK, bf16>(__VA_ARGS__) : LAUNCH<16, NQ, NK, float>(__VA_ARGS__); \
+    } while (0)
+
+// NQ x NK instantiations: 160 ms pushes (2 queries, keys <= left + 2), chunked
+// pushes of up to 8 frames (keys <= left + 8), provisional passes (up to 24
+// queries, keys <= left + 24); offline groups of up to 8 queries.
+cudaError_t launch_attention_stream(const AttnParams& a, int act_bf16, int* status, cudaStream_t s) {
     if (a.nb <= 0) return cudaSuccess;
     const int nk_need = a.left + a.nq;
-    if (a.nq <= 8 && nk_need <= 80) {
-        if (a.HD == 64) return act_bf16 ? attn_stream_launch<64, 8, 80, bf16>(a, s) : attn_stream_launch<64, 8, 80, float>(a, s);
-        if (a.HD == 16) return act_bf16 ? attn_stream_launch<16, 8, 80, bf16>(a, s) : attn_stream_launch<16, 8, 80, float>(a, s);
-    } else if (a.nq <= 24 && nk_need <= 96) {
-        if (a.HD == 64) return act_bf16 ? attn_stream_launch<64, 24, 96, bf16>(a, s) : attn_stream_launch<64, 24, 96, float>(a, s);
-        if (a.HD == 16) return act_bf16 ? attn_stream_launch<16, 24, 96, bf16>(a, s) : attn_stream_launch<16, 24, 96, float>(a, s);
-    }
+    if (a.nq <= 2 && nk_need <= 80) ATT_DISPATCH(attn_stream_launch, 2, 80, a, status, s);
+    if (a.nq <= 8 && nk_need <= 80) ATT_DISPATCH(attn_stream_launch, 8, 80, a, status, s);
+    if (a.nq <= 24 && nk_need <= 96) ATT_DISPATCH(attn_stream_launch, 24, 96, a, status, s);
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_attention_offline(const AttnParams& a, int act_bf16, cudaStream_t s) {
+cudaError_t launch_attention_offline(const AttnParams& a, int act_bf16, int* status, cudaStream_t s) {
     if (a.nb <= 0) return cudaSuccess;
     // queries per warp: one chunk of the chunked mask, or 8 consecutive frames of a window mask
     const int qgroup = a.rc > 0 ? 8 : a.chunk;
     const int nk_need = a.rc > 0 ? a.left + qgroup + a.rc : a.left + a.chunk;
     if (qgroup > 8 || nk_need > 96) return cudaErrorInvalidValue;
-    if (a.HD == 64) return act_bf16 ? attn_offline_launch<64, 8, 96, bf16>(a, qgroup, s) : attn_offline_launch<64, 8, 96, float>(a, qgroup, s);
-    if (a.HD == 16) return act_bf16 ? attn_offline_launch<16, 8, 96, bf16>(a, qgroup, s) : attn_offline_launch<16, 8, 96, float>(a, qgroup, s);
+    if (qgroup <= 2 && nk_need <= 80) ATT_DISPATCH(attn_offline_launch, 2, 80, a, qgroup, status, s);
+    ATT_DISPATCH(attn_offline_launch, 8, 96, a, qgroup, status, s);
     return cudaErrorInvalidValue;
 }
 

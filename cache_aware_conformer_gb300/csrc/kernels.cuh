@@ -50,8 +50,9 @@ struct AttnParams {
     float scale = 1.f;
 };
 
-cudaError_t launch_attention_stream(const AttnParams& a, int act_bf16, cudaStream_t s);
-cudaError_t launch_attention_offline(const AttnParams& a, int act_bf16, cudaStream_t s);
+// A bounded wait on the K/V copies that gives up latches CAC_E_TIMEOUT in *status.
+cudaError_t launch_attention_stream(const AttnParams& a, int act_bf16, int* status, cudaStream_t s);
+cudaError_t launch_attention_offline(const AttnParams& a, int act_bf16, int* status, cudaStream_t s);
 
 // Causal depthwise conv (k = 9) + affine + SiLU over [conv cache | glu_new].
 // Streaming: cache = layer base of [S][L][8][D] rings (stride cs_stride per
