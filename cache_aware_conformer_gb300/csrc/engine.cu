@@ -66,7 +66,7 @@ struct LayerW {
     float *ff1_g = nullptr, *ff1_b = nullptr, *att_g = nullptr, *att_b = nullptr, *conv_g = nullptr,
           *conv_b = nullptr, *ff2_g = nullptr, *ff2_b = nullptr, *out_g = nullptr, *out_b = nullptr;
     Lin ff1_w1, ff1_w2, qkv, wo, pw1, pw2, ff2_w1, ff2_w2;
-    float *pbu = nullptr, *pbv = nullptr, *P = nullptr, *dwT = nullptr, *bdw = nullptr, *bng = nullptr,
+    float *pbu = nullptr, *pbv = nullptr, *P = nullptr, *Ppad = nullptr, *dwT = nullptr, *bdw = nullptr, *bng = nullptr,
           *bnb = nullptr;
 };
 
@@ -319,6 +319,16 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
             ep.out_f32 = Lw.P;
             ep.ldo = D;
             if (launch_gemm_simt(0, pe, D, wpos_d, D, m->NR, D, D, ep, 0) != cudaSuccess) return fail(CAC_E_CUDA);
+            // head-major copy with rows padded to HD + 4 floats: one bulk copy per
+            // (block, head) in the attention kernels, conflict-free rows in shared memory
+            std::vector<float> hp((size_t)m->NR * D), pad((size_t)H * m->NR * (HD + 4), 0.f);
+            if (cudaMemcpy(hp.data(), Lw.P, hp.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+                return fail(CAC_E_CUDA);
+            for (int hh = 0; hh < H; ++hh)
+                for (int rr = 0; rr < m->NR; ++rr)
+                    std::memcpy(&pad[((size_t)hh * m->NR + rr) * (HD + 4)], &hp[(size_t)rr * D + hh * HD],
+                                sizeof(float) * HD);
+            if ((r = upload_f32(m, pad.data(), pad.size(), &Lw.Ppad)) != CAC_OK) return fail(r);
         }
         if ((r = vec(&Lw.pbu, (size_t)H * HD)) || (r = vec(&Lw.pbv, (size_t)H * HD))) return fail(r);
         if ((r = vec(&Lw.conv_g, D)) || (r = vec(&Lw.conv_b, D)) || (r = lin(&Lw.pw1, 2 * D, D, &glu_perm)))
@@ -609,7 +619,7 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
             a.q = p->q; a.ldq = D;
             a.k = ep.kring; a.v = ep.vring; a.sstride = p->ring_sstride; a.R = p->R;
             a.ids = p->ids_dev; a.pos = p->pos; a.nq = n;
-            a.P = Lw.P; a.rmin = m->rmin; a.NR = m->NR; a.pbu = Lw.pbu; a.pbv = Lw.pbv;
+            a.P = Lw.Ppad; a.rmin = m->rmin; a.NR = m->NR; a.pbu = Lw.pbu; a.pbv = Lw.pbv;
             a.out = p->o; a.ldo = D;
             a.H = m->H; a.D = D; a.HD = m->HD;
             a.left = m->cfg.att_left; a.chunk = m->cfg.att_chunk; a.rc = 0;
@@ -1082,7 +1092,7 @@ extern "C" int cac_encode_offline(cac_model* m, int B, const float* mel, const i
         {
             AttnParams a;
             a.q = q; a.ldq = D; a.k = kd; a.v = vd; a.ldk = D;
-            a.P = Lw.P; a.rmin = m->rmin; a.NR = m->NR; a.pbu = Lw.pbu; a.pbv = Lw.pbv;
+            a.P = Lw.Ppad; a.rmin = m->rmin; a.NR = m->NR; a.pbu = Lw.pbu; a.pbv = Lw.pbv;
             a.out = o; a.ldo = D; a.H = m->H; a.D = D; a.HD = m->HD;
             a.left = m->cfg.att_left; a.chunk = m->cfg.att_chunk; a.rc = m->cfg.right_context;
             a.nb = B; a.T = T3; a.seq_len = flen_d;

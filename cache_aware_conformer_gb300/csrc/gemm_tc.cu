@@ -1,14 +1,17 @@
 // tcgen05 / TMEM / TMA GEMM for sm_103a: C = A * B^T, bf16 operands, fp32
 // accumulation in tensor memory, fused epilogue read back with tcgen05.ld.
 //
-// One CTA computes a 128 x BN output tile with 4 warps:
+// One CTA computes a 128 x BN output tile with 8 warps:
 //   warp 0 lane 0  TMA producer: 64-wide K slices of A (128 rows) and B (BN rows)
 //                  into a STAGES-deep ring of 128-byte-swizzled smem tiles;
 //   warp 1 lane 0  MMA issuer: 4 x tcgen05.mma (K = 16 each) per slice, then
 //                  tcgen05.commit to release the slice back to the producer;
 //   warp 1         also owns the TMEM allocation (BN fp32 columns);
-//   warps 0-3      epilogue: warp w reads TMEM lanes 32w..32w+31 (output rows)
-//                  in 32-column chunks and applies the fused epilogue.
+//   warps 0-7      epilogue: warp w reads TMEM lanes 32(w%4)..+31 (output rows),
+//                  column half w/4, in 32-column chunks, and applies the fused
+//                  epilogue.  Eight warps (two per scheduler) keep the
+//                  epilogue's dependent arithmetic from stalling one warp per
+//                  scheduler; at BN = 64 four stages fit two CTAs per SM.
 // Every mbarrier wait is bounded; a wait that gives up latches
 // CAC_E_TIMEOUT in the status word and the CTA unwinds without hanging.
 #include <cudaTypedefs.h>
@@ -28,13 +31,15 @@ template <int BN>
 struct TcCfg {
     static constexpr int B_TILE = BN * BK * 2;
     static constexpr int STAGE = A_TILE + B_TILE;
-    static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 4);
     static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/;
 };
 }  // namespace
 
+constexpr int TC_THREADS = 256;
+
 template <int BN, int KIND, class TAct>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(TC_THREADS, 2)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
                    int K, int conv_C, EpiParams ep, int* status) {
     using C = TcCfg<BN>;
@@ -104,11 +109,12 @@ __global__ void __launch_bounds__(128, 1)
 
     if (!mbar_wait(accb, 0)) ok = false;
     tc_fence_after();
-    const int row = m0 + warp * 32 + lane;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = m0 + quarter * 32 + lane;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
         float v[32];
-        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
         if (ok && row < M) epilogue32<KIND, TAct>(ep, row, n0 + c, v);
     }
     if (!ok) latch_error(status, CAC_E_TIMEOUT);
@@ -175,7 +181,7 @@ static cudaError_t launch_bn_kind(const CUtensorMap* tmA, const CUtensorMap* tmB
         attr_set = true;
     }
     dim3 grid(N / BN, (M + BM - 1) / BM);
-    kern<<<grid, 128, C::SMEM, s>>>(*tmA, *tmB, M, N, K, conv_C, ep, status);
+    kern<<<grid, TC_THREADS, C::SMEM, s>>>(*tmA, *tmB, M, N, K, conv_C, ep, status);
     return cudaGetLastError();
 }
 

@@ -214,12 +214,16 @@ __device__ __forceinline__ void attn_carve(uint8_t* wsm, uint64_t*& bar, T*& Ks,
     S = qv + NQ * HD;
 }
 
+// Block prologue shared by the attention kernels: thread 0 arms the block
+// barrier and bulk-copies this head's padded position table [NR][HD + 4].
 template <int HD>
-__device__ void load_ptable(const AttnParams& a, int h, float* Ps) {
-    constexpr int PS = HD + 4;
-    for (int e = threadIdx.x; e < a.NR * HD; e += blockDim.x) {
-        const int r = e / HD, d = e - (e / HD) * HD;
-        Ps[r * PS + d] = __ldg(a.P + (long long)r * a.D + h * HD + d);
+__device__ __forceinline__ void stage_ptable(const AttnParams& a, int h, float* Ps, uint64_t* pbar) {
+    if (threadIdx.x == 0) {
+        const uint32_t bytes = (uint32_t)a.NR * (HD + 4) * 4;
+        mbar_init(pbar, 1);
+        fence_mbar_init();
+        mbar_expect_tx(pbar, bytes);
+        bulk_g2s(Ps, a.P + (long long)h * a.NR * (HD + 4), bytes, pbar);
     }
 }
 
@@ -244,8 +248,8 @@ __device__ __forceinline__ void chunk_to_f<float, 4>(const float* src, float (&f
 
 // Everything after the K/V copies were issued on `bar`.
 template <int HD, int NQ, int NK, class T>
-__device__ void attend_warp(const AttnParams& a, int h, const float* Ps, uint8_t* wsm, int lane, const float* qsrc,
-                            int pq0, int nq, int kpos0, int Nk, T* dst, int* status) {
+__device__ void attend_warp(const AttnParams& a, int h, const float* Ps, uint64_t* pbar, uint8_t* wsm, int lane,
+                            const float* qsrc, int pq0, int nq, int kpos0, int Nk, T* dst, int* status) {
     using Lay = AttnLayout<HD, NQ, NK, T>;
     constexpr int PS = Lay::PS;
     constexpr int DPL = HD >= 32 ? HD / 32 : 1;
@@ -261,7 +265,7 @@ __device__ void attend_warp(const AttnParams& a, int h, const float* Ps, uint8_t
         qu[i * HD + d] = qq + __ldg(a.pbu + h * HD + d);
         qv[i * HD + d] = qq + __ldg(a.pbv + h * HD + d);
     }
-    const bool landed = mbar_wait(bar, 0);
+    const bool landed = mbar_wait(bar, 0) && mbar_wait(pbar, 0);
     __syncwarp();
     if (!landed) {
         if (lane == 0) latch_error(status, CAC_E_TIMEOUT);
@@ -372,8 +376,10 @@ __global__ void __launch_bounds__(ATT_WARPS * 32) attn_stream_kernel(AttnParams 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.x * ATT_WARPS + warp;
     const bool live = b < a.nb;
-    float* Ps = reinterpret_cast<float*>(sm);
-    uint8_t* wsm = sm + ((a.NR * Lay::PS * 4 + 15) & ~15) + warp * Lay::WARP_BYTES;
+    uint64_t* pbar = reinterpret_cast<uint64_t*>(sm);
+    float* Ps = reinterpret_cast<float*>(sm + 16);
+    uint8_t* wsm = sm + 16 + ((a.NR * Lay::PS * 4 + 15) & ~15) + warp * Lay::WARP_BYTES;
+    stage_ptable<HD>(a, h, Ps, pbar);
     int id = 0, p0 = 0, Lc = 0, Nk = 0;
     if (live) {
         id = a.ids[b];
@@ -402,10 +408,9 @@ __global__ void __launch_bounds__(ATT_WARPS * 32) attn_stream_kernel(AttnParams 
             }
         }
     }
-    load_ptable<HD>(a, h, Ps);
     __syncthreads();
     if (!live) return;
-    attend_warp<HD, NQ, NK, T>(a, h, Ps, wsm, lane, a.q + (long long)b * a.nq * a.ldq + h * HD, p0, a.nq, p0 - Lc,
+    attend_warp<HD, NQ, NK, T>(a, h, Ps, pbar, wsm, lane, a.q + (long long)b * a.nq * a.ldq + h * HD, p0, a.nq, p0 - Lc,
                                Nk, static_cast<T*>(a.out) + (long long)b * a.nq * a.ldo + h * HD, status);
 }
 
@@ -421,8 +426,10 @@ __global__ void __launch_bounds__(ATT_WARPS * 32) attn_offline_kernel(AttnParams
     const int len = a.seq_len[seq];
     const int pq0 = (blockIdx.x * ATT_WARPS + warp) * qgroup;
     const bool live = pq0 < len;
-    float* Ps = reinterpret_cast<float*>(sm);
-    uint8_t* wsm = sm + ((a.NR * Lay::PS * 4 + 15) & ~15) + warp * Lay::WARP_BYTES;
+    uint64_t* pbar = reinterpret_cast<uint64_t*>(sm);
+    float* Ps = reinterpret_cast<float*>(sm + 16);
+    uint8_t* wsm = sm + 16 + ((a.NR * Lay::PS * 4 + 15) & ~15) + warp * Lay::WARP_BYTES;
+    stage_ptable<HD>(a, h, Ps, pbar);
     int nq = 0, klo = 0, Nk = 0;
     const long long rb = (long long)seq * a.T;
     if (live) {
@@ -455,25 +462,25 @@ __global__ void __launch_bounds__(ATT_WARPS * 32) attn_offline_kernel(AttnParams
             bulk_g2s(Vs + j * HD, vb + (long long)(klo + j) * a.ldk, ROW, bar);
         }
     }
-    load_ptable<HD>(a, h, Ps);
     __syncthreads();
     if (!live) return;
-    attend_warp<HD, NQ, NK, T>(a, h, Ps, wsm, lane, a.q + (rb + pq0) * a.ldq + h * HD, pq0, nq, klo, Nk,
+    attend_warp<HD, NQ, NK, T>(a, h, Ps, pbar, wsm, lane, a.q + (rb + pq0) * a.ldq + h * HD, pq0, nq, klo, Nk,
                                static_cast<T*>(a.out) + (rb + pq0) * a.ldo + h * HD, status);
 }
 
 template <int HD, int NQ, int NK, class T>
 static size_t attn_smem(const AttnParams& a) {
     using Lay = AttnLayout<HD, NQ, NK, T>;
-    return ((size_t)a.NR * Lay::PS * 4 + 15) / 16 * 16 + (size_t)ATT_WARPS * Lay::WARP_BYTES;
+    return 16 + ((size_t)a.NR * Lay::PS * 4 + 15) / 16 * 16 + (size_t)ATT_WARPS * Lay::WARP_BYTES;
 }
 
 template <class K>
 static cudaError_t raise_smem(K kern, size_t smem, size_t& attr) {
     if (smem <= attr) return cudaSuccess;
-    if (smem > 200 * 1024) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e == cudaSuccess) attr = 200 * 1024;
+    constexpr size_t kMax = 227 * 1024;  // per-block dynamic shared memory limit of sm_10x
+    if (smem > kMax) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMax);
+    if (e == cudaSuccess) attr = kMax;
     return e;
 }
 
