@@ -188,7 +188,11 @@ int gemm(cac_model* m, const void* A, long long lda, int M, int K, const Lin& W,
         const bool ok = conv_C ? make_tmap_bf16_conv(&tmA, A, conv_C, (uint64_t)M + 1, 128)
                                : make_tmap_bf16(&tmA, A, K, M, (uint64_t)lda * 2, 128);
         if (!ok) return CAC_E_CUDA;
-        CK(launch_gemm_tc(&tmA, &W.tm, M, W.N, K, W.BN, conv_C, ep, m->status, s));
+        // split K until the grid covers most of the 152 SMs (at most 4 ways, >= 2 K slices each)
+        const int tiles = (W.N / W.BN) * ((M + 127) / 128), nk = K / 64;
+        int splits = 1;
+        while (splits < 4 && tiles * splits < 120 && nk / (splits + 1) >= 2) ++splits;
+        CK(launch_gemm_tc(&tmA, &W.tm, M, W.N, K, W.BN, conv_C, splits, ep, m->status, s));
     } else {
         CK(launch_gemm_simt(m->bf16, A, lda, W.w, K, M, W.N, K, ep, s));
     }

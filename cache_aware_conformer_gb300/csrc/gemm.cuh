@@ -68,8 +68,10 @@ bool make_tmap_bf16_conv(CUtensorMap* tm, const void* base, uint64_t C, uint64_t
 
 // tcgen05/TMEM GEMM, bf16 operands.  K % 64 == 0, N % BN == 0, BN in {64, 128, 256}.
 // conv_C > 0 selects the convolution view of A (tmA from make_tmap_bf16_conv, K = 3 * conv_C).
+// splits in 1..4: split-K over a cluster of `splits` CTAs per output tile,
+// reduced deterministically through distributed shared memory.
 cudaError_t launch_gemm_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int BN, int conv_C,
-                           const EpiParams& ep, int* status, cudaStream_t s);
+                           int splits, const EpiParams& ep, int* status, cudaStream_t s);
 
 // SIMT GEMM (fp32 or bf16 operands, fp32 accumulate).  N % 32 == 0.
 cudaError_t launch_gemm_simt(int bf16_operands, const void* A, long long lda, const void* B, long long ldb, int M,

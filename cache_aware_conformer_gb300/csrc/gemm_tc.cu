@@ -12,6 +12,11 @@
 //                  epilogue.  Eight warps (two per scheduler) keep the
 //                  epilogue's dependent arithmetic from stalling one warp per
 //                  scheduler; at BN = 64 four stages fit two CTAs per SM.
+// Split-K: the `splits` CTAs of one output tile form a thread-block cluster
+// along z, each accumulating a contiguous range of K slices.  Ranks > 0 park
+// their fp32 partial tile in their (now idle) pipeline shared memory; rank 0
+// adds them over distributed shared memory in rank order (deterministic) and
+// runs the fused epilogue once.
 // Every mbarrier wait is bounded; a wait that gives up latches
 // CAC_E_TIMEOUT in the status word and the CTA unwinds without hanging.
 #include <cudaTypedefs.h>
@@ -54,7 +59,11 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
-    const int nk = K / BK;
+    const int splits = gridDim.z;
+    const uint32_t crank = splits > 1 ? cluster_rank() : 0;
+    const int nk_all = K / BK;
+    const int kb0 = (int)(crank * nk_all / splits), kb1 = (int)((crank + 1) * nk_all / splits);
+    const int nk = kb1 - kb0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -79,13 +88,14 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
             const uint32_t ph = (kb / C::STAGES) & 1;
             if (!mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }
             mbar_expect_tx(&full[s], C::STAGE);
+            const int k0 = (kb0 + kb) * BK;
             if (conv_C) {
-                const int k0 = kb * BK, tap = k0 / conv_C;
+                const int tap = k0 / conv_C;
                 tma_load_3d(sA + s * A_TILE, &tmA, k0 - tap * conv_C, tap & 1, m0 + (tap >> 1), &full[s]);
             } else {
-                tma_load_2d(sA + s * A_TILE, &tmA, kb * BK, m0, &full[s]);
+                tma_load_2d(sA + s * A_TILE, &tmA, k0, m0, &full[s]);
             }
-            tma_load_2d(sB + s * C::B_TILE, &tmB, kb * BK, n0, &full[s]);
+            tma_load_2d(sB + s * C::B_TILE, &tmB, k0, n0, &full[s]);
         }
     } else if (warp == 1 && lane == 0) {
         constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
@@ -110,13 +120,33 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     if (!mbar_wait(accb, 0)) ok = false;
     tc_fence_after();
     const int quarter = warp & 3, half = warp >> 2;
-    const int row = m0 + quarter * 32 + lane;
+    const int rloc = quarter * 32 + lane;
+    const int row = m0 + rloc;
+    // partial tile [BN columns][128 rows] fp32 in the pipeline buffers (idle now)
+    float* part = reinterpret_cast<float*>(sA);
+    if (splits > 1 && crank != 0) {
 #pragma unroll 1
-    for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
-        if (ok && row < M) epilogue32<KIND, TAct>(ep, row, n0 + c, v);
+        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
+            float v[32];
+            tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) part[(c + k) * BM + rloc] = v[k];
+        }
     }
+    if (splits > 1) cluster_sync();
+    if (crank == 0) {
+#pragma unroll 1
+        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
+            float v[32];
+            tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
+            for (int rr = 1; rr < splits; ++rr) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) v[k] += ld_dsmem(&part[(c + k) * BM + rloc], (uint32_t)rr);
+            }
+            if (ok && row < M) epilogue32<KIND, TAct>(ep, row, n0 + c, v);
+        }
+    }
+    if (splits > 1) cluster_sync();  // keep every rank's partial alive until rank 0 has read it
     if (!ok) latch_error(status, CAC_E_TIMEOUT);
     tc_fence_before();
     __syncthreads();
@@ -171,7 +201,7 @@ bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t 
 
 template <int BN, int KIND>
 static cudaError_t launch_bn_kind(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int conv_C,
-                                  const EpiParams& ep, int* status, cudaStream_t s) {
+                                  int splits, const EpiParams& ep, int* status, cudaStream_t s) {
     using C = TcCfg<BN>;
     auto kern = gemm_tc_kernel<BN, KIND, bf16>;
     static bool attr_set = false;  // per instantiation, per process
@@ -180,33 +210,44 @@ static cudaError_t launch_bn_kind(const CUtensorMap* tmA, const CUtensorMap* tmB
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    dim3 grid(N / BN, (M + BM - 1) / BM);
-    kern<<<grid, TC_THREADS, C::SMEM, s>>>(*tmA, *tmB, M, N, K, conv_C, ep, status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(N / BN, (M + BM - 1) / BM, splits);
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = splits;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, *tmA, *tmB, M, N, K, conv_C, ep, status);
 }
 
 template <int BN>
-static cudaError_t launch_bn(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int cc,
+static cudaError_t launch_bn(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int cc, int sp,
                              const EpiParams& ep, int* status, cudaStream_t s) {
     switch (ep.kind) {
-        case EPI_STORE: return launch_bn_kind<BN, EPI_STORE>(tmA, tmB, M, N, K, cc, ep, status, s);
-        case EPI_RESID: return launch_bn_kind<BN, EPI_RESID>(tmA, tmB, M, N, K, cc, ep, status, s);
-        case EPI_GLU: return launch_bn_kind<BN, EPI_GLU>(tmA, tmB, M, N, K, cc, ep, status, s);
-        case EPI_QKV: return launch_bn_kind<BN, EPI_QKV>(tmA, tmB, M, N, K, cc, ep, status, s);
-        case EPI_SUB: return launch_bn_kind<BN, EPI_SUB>(tmA, tmB, M, N, K, cc, ep, status, s);
+        case EPI_STORE: return launch_bn_kind<BN, EPI_STORE>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+        case EPI_RESID: return launch_bn_kind<BN, EPI_RESID>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+        case EPI_GLU: return launch_bn_kind<BN, EPI_GLU>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+        case EPI_QKV: return launch_bn_kind<BN, EPI_QKV>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+        case EPI_SUB: return launch_bn_kind<BN, EPI_SUB>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
     }
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int BN, int conv_C,
-                           const EpiParams& ep, int* status, cudaStream_t s) {
+                           int splits, const EpiParams& ep, int* status, cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
     if (K % BK || K <= 0 || N % BN || !ep.act_bf16) return cudaErrorInvalidValue;
     if (conv_C && (conv_C % BK || K != 3 * conv_C)) return cudaErrorInvalidValue;
+    if (splits < 1 || splits > 4 || splits > K / BK) return cudaErrorInvalidValue;
     switch (BN) {
-        case 64: return launch_bn<64>(tmA, tmB, M, N, K, conv_C, ep, status, s);
-        case 128: return launch_bn<128>(tmA, tmB, M, N, K, conv_C, ep, status, s);
-        case 256: return launch_bn<256>(tmA, tmB, M, N, K, conv_C, ep, status, s);
+        case 64: return launch_bn<64>(tmA, tmB, M, N, K, conv_C, splits, ep, status, s);
+        case 128: return launch_bn<128>(tmA, tmB, M, N, K, conv_C, splits, ep, status, s);
+        case 256: return launch_bn<256>(tmA, tmB, M, N, K, conv_C, splits, ep, status, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -176,17 +176,22 @@ cudaError_t launch_stage_mel_offline(const float* mel, int t_mel, const int* len
 // ---------------------------------------------------------------------------
 // rectangular rel-pos attention
 //
-// One warp owns (query group, head): nq queries at positions pq0 .. pq0+nq-1
-// against Nk keys at positions kpos0 .. kpos0+Nk-1.
+// Work unit: (query group, head) — the n new frames of one stream (or one
+// chunk of an offline sequence) against their Nk keys at positions
+// kpos0 .. kpos0+Nk-1:
 //   score[i][j] = ((q_i + u) . k_j + (q_i + v) . P[pq_i - pk_j]) * scale,
 // masked (chunked-causal on absolute positions, or a window), softmax over j,
 // out_i = sum_j prob[i][j] v_j.
-// The warp's K and V rows are staged in shared memory by TMA bulk copies
-// (cp.async.bulk on one mbarrier) issued before anything else, so the whole
-// HBM read of the warp is in flight at once; the block's per-head position
-// table is loaded while they land.  Scores: lane per key, 16-byte chunks of
-// the key row read in a lane-rotated order (conflict-free shared loads).
-// probs @ V: lane per HD/32 output dims, V rows from shared memory.
+//
+// A block serves SPB units of one head with WPS warps each (the queries of a
+// unit are dealt round-robin to its warps).  Per unit, one lane issues TMA
+// bulk copies of all K and V rows into shared memory on one mbarrier (the ring
+// span of a stream is at most two contiguous pieces); thread 0 bulk-copies the
+// head's padded position table on a block barrier.  Inside a warp, LPK =
+// HD / 8 lanes share a key: each lane holds 8 dims of (q + u) and (q + v) in
+// registers, reads the matching 8 dims of k_j and of P[rel] from shared
+// memory, and the partial dots are combined with log2(LPK) shuffles.  probs @ V
+// uses the same lane layout over the keys, then reduces across key groups.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ bool allowed(const AttnParams& a, int pq, int pk) {
     if (pk < 0) return false;
@@ -195,27 +200,191 @@ __device__ __forceinline__ bool allowed(const AttnParams& a, int pq, int pk) {
     return pk >= c - a.left && pk <= c + a.chunk - 1;
 }
 
-template <int HD, int NQ, int NK, class T>
-struct AttnLayout {
-    static constexpr int KV = NK * HD;                                   // elements of K (or V)
-    static constexpr int WARP_BYTES = 16 + 2 * KV * (int)sizeof(T) + 4 * (2 * NQ * HD + NQ * NK);
-    static constexpr int PS = HD + 4;                                    // padded position-table row
+template <int HD, int NQW, int WPS, int SPB, int NK, class T>
+struct Attn {
+    static constexpr int NQ = NQW * WPS;              // queries per unit
+    static constexpr int THREADS = SPB * WPS * 32;
+    static constexpr int PS = HD + 4;                 // padded position-table row (floats)
+    static constexpr int LPK = HD / 8;                // lanes per key
+    static constexpr int KPS = 32 / LPK;              // keys per warp step
+    static constexpr int KV = NK * HD;                // elements of K (or V) per unit
+    static constexpr int UNIT_BYTES = 16 + 2 * KV * (int)sizeof(T) + 4 * NQ * NK;
+    static size_t smem(int NR) { return 16 + ((size_t)NR * PS * 4 + 15) / 16 * 16 + (size_t)SPB * UNIT_BYTES; }
 };
 
-template <int HD, int NQ, int NK, class T>
-__device__ __forceinline__ void attn_carve(uint8_t* wsm, uint64_t*& bar, T*& Ks, T*& Vs, float*& qu, float*& qv,
-                                           float*& S) {
-    using Lay = AttnLayout<HD, NQ, NK, T>;
-    bar = reinterpret_cast<uint64_t*>(wsm);
-    Ks = reinterpret_cast<T*>(wsm + 16);
-    Vs = Ks + Lay::KV;
-    qu = reinterpret_cast<float*>(Vs + Lay::KV);
-    qv = qu + NQ * HD;
-    S = qv + NQ * HD;
+// 4 consecutive elements -> float
+__device__ __forceinline__ void ld4f(const bf16* p, float* f) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+}
+__device__ __forceinline__ void ld4f(const float* p, float* f) {
+    const float4 u = *reinterpret_cast<const float4*>(p);
+    f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
+}
+__device__ __forceinline__ void st4(bf16* p, const float* f) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f[2], f[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&a);
+    u.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+__device__ __forceinline__ void st4(float* p, const float* f) {
+    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
 }
 
-// Block prologue shared by the attention kernels: thread 0 arms the block
-// barrier and bulk-copies this head's padded position table [NR][HD + 4].
+// The 8 dims of a row that lane c (of LPK) owns: [c*4, c*4+4) and [HD/2 + c*4, ..+4).
+// Rows of odd keys read the two halves in the other order so that the two keys
+// sharing a half-warp request hit different banks.
+template <int HD, class T>
+__device__ __forceinline__ void ld8(const T* row, int c, int odd, float* lo, float* hi) {
+    float a[4], b[4];
+    ld4f(row + (odd ? HD / 2 : 0) + c * 4, a);
+    ld4f(row + (odd ? 0 : HD / 2) + c * 4, b);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        lo[e] = odd ? b[e] : a[e];
+        hi[e] = odd ? a[e] : b[e];
+    }
+}
+
+// One warp: its queries (i = wsub, wsub + WPS, ...) of one unit, after the
+// unit's K/V copies and the position table were issued.
+template <int HD, int NQW, int WPS, int SPB, int NK, class T>
+__device__ void attend(const AttnParams& a, int h, const float* Ps, uint64_t* pbar, uint8_t* usm, int wsub, int lane,
+                       const float* qsrc, int pq0, int nq, int kpos0, int Nk, T* dst, int* status) {
+    using A = Attn<HD, NQW, WPS, SPB, NK, T>;
+    constexpr int LPK = A::LPK, KPS = A::KPS, PS = A::PS;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(usm);
+    const T* Ks = reinterpret_cast<const T*>(usm + 16);
+    const T* Vs = Ks + A::KV;
+    float* S = reinterpret_cast<float*>(const_cast<T*>(Vs + A::KV));
+    const int c = lane % LPK, g = lane / LPK;
+    // this warp's queries, with both biases folded in, 8 dims per lane in registers
+    float qu[NQW][8], qv[NQW][8];
+#pragma unroll
+    for (int t = 0; t < NQW; ++t) {
+        const int i = wsub + WPS * t;
+        if (i >= nq) break;
+        const float* qr = qsrc + (long long)i * a.ldq;
+        const float* ub = a.pbu + h * HD;
+        const float* vb = a.pbv + h * HD;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int d = half * (HD / 2) + c * 4;
+            const float4 q4 = *reinterpret_cast<const float4*>(qr + d);
+            const float4 u4 = __ldg(reinterpret_cast<const float4*>(ub + d));
+            const float4 v4 = __ldg(reinterpret_cast<const float4*>(vb + d));
+            const float qq[4] = {q4.x, q4.y, q4.z, q4.w}, uu[4] = {u4.x, u4.y, u4.z, u4.w},
+                        vv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                qu[t][half * 4 + e] = qq[e] + uu[e];
+                qv[t][half * 4 + e] = qq[e] + vv[e];
+            }
+        }
+    }
+    const bool landed = mbar_wait(bar, 0) && mbar_wait(pbar, 0);
+    __syncwarp();
+    if (!landed) {
+        if (lane == 0) latch_error(status, CAC_E_TIMEOUT);
+        return;
+    }
+    // scores
+    for (int j0 = 0; j0 < Nk; j0 += KPS) {
+        const int j = j0 + g;
+        const bool valid = j < Nk;
+        const int pk = kpos0 + j;
+        float k8[8];
+        {
+            float lo[4], hi[4];
+            ld8<HD>(Ks + (valid ? j : 0) * HD, c, j & 1, lo, hi);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) { k8[e] = lo[e]; k8[4 + e] = hi[e]; }
+        }
+#pragma unroll
+        for (int t = 0; t < NQW; ++t) {
+            const int i = wsub + WPS * t;
+            if (i >= nq) break;
+            const int pq = pq0 + i;
+            const bool ok = valid && allowed(a, pq, pk);
+            float part = 0.f;
+            if (ok) {
+                float p8[8];
+                const float* pr = Ps + (pq - pk - a.rmin) * PS;
+                ld4f(pr + c * 4, p8);
+                ld4f(pr + HD / 2 + c * 4, p8 + 4);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) part = fmaf(qu[t][e], k8[e], fmaf(qv[t][e], p8[e], part));
+            }
+#pragma unroll
+            for (int o = 1; o < LPK; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            if (valid && c == 0) S[i * NK + j] = ok ? part * a.scale : -FLT_MAX;
+        }
+    }
+    __syncwarp();
+    // softmax over the keys of each of this warp's queries
+#pragma unroll 1
+    for (int t = 0; t < NQW; ++t) {
+        const int i = wsub + WPS * t;
+        if (i >= nq) break;
+        float* Si = S + i * NK;
+        float m = -FLT_MAX;
+        for (int j = lane; j < Nk; j += 32) m = fmaxf(m, Si[j]);
+        m = warp_max(m);
+        float sum = 0.f;
+        for (int j = lane; j < Nk; j += 32) {
+            const float e = (Si[j] == -FLT_MAX) ? 0.f : __expf(Si[j] - m);
+            Si[j] = e;
+            sum += e;
+        }
+        sum = warp_sum(sum);
+        const float inv = 1.f / sum;
+        for (int j = lane; j < Nk; j += 32) Si[j] *= inv;
+    }
+    __syncwarp();
+    // probs @ V: key group g takes keys j = g, g + KPS, ...; each lane 8 dims
+    float acc[NQW][8];
+#pragma unroll
+    for (int t = 0; t < NQW; ++t)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[t][e] = 0.f;
+#pragma unroll 2
+    for (int j = g; j < Nk; j += KPS) {
+        float lo[4], hi[4];
+        ld8<HD>(Vs + j * HD, c, j & 1, lo, hi);
+#pragma unroll
+        for (int t = 0; t < NQW; ++t) {
+            const int i = wsub + WPS * t;
+            if (i >= nq) break;
+            const float pij = S[i * NK + j];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc[t][e] = fmaf(pij, lo[e], acc[t][e]);
+                acc[t][4 + e] = fmaf(pij, hi[e], acc[t][4 + e]);
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < NQW; ++t) {
+        const int i = wsub + WPS * t;
+        if (i >= nq) break;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+#pragma unroll
+            for (int o = LPK; o < 32; o <<= 1) acc[t][e] += __shfl_xor_sync(0xffffffffu, acc[t][e], o);
+        if (g == 0) {
+            T* o = dst + (long long)i * a.ldo;
+            st4(o + c * 4, acc[t]);
+            st4(o + HD / 2 + c * 4, acc[t] + 4);
+        }
+    }
+}
+
+// Block prologue: thread 0 arms the block barrier and bulk-copies this head's
+// padded position table [NR][HD + 4].
 template <int HD>
 __device__ __forceinline__ void stage_ptable(const AttnParams& a, int h, float* Ps, uint64_t* pbar) {
     if (threadIdx.x == 0) {
@@ -227,158 +396,20 @@ __device__ __forceinline__ void stage_ptable(const AttnParams& a, int h, float* 
     }
 }
 
-template <class T, int EPC>
-__device__ __forceinline__ void chunk_to_f(const T* src, float (&f)[EPC]);
-template <>
-__device__ __forceinline__ void chunk_to_f<bf16, 8>(const bf16* src, float (&f)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4*>(src);
-    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float2 t = __bfloat1622float2(p[k]);
-        f[2 * k] = t.x;
-        f[2 * k + 1] = t.y;
-    }
-}
-template <>
-__device__ __forceinline__ void chunk_to_f<float, 4>(const float* src, float (&f)[4]) {
-    const float4 u = *reinterpret_cast<const float4*>(src);
-    f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
-}
-
-// Everything after the K/V copies were issued on `bar`.
-template <int HD, int NQ, int NK, class T>
-__device__ void attend_warp(const AttnParams& a, int h, const float* Ps, uint64_t* pbar, uint8_t* wsm, int lane,
-                            const float* qsrc, int pq0, int nq, int kpos0, int Nk, T* dst, int* status) {
-    using Lay = AttnLayout<HD, NQ, NK, T>;
-    constexpr int PS = Lay::PS;
-    constexpr int DPL = HD >= 32 ? HD / 32 : 1;
-    constexpr int EPC = 16 / (int)sizeof(T);  // elements per 16-byte chunk
-    constexpr int CPR = HD / EPC;             // chunks per row
-    uint64_t* bar;
-    T *Ks, *Vs;
-    float *qu, *qv, *S;
-    attn_carve<HD, NQ, NK, T>(wsm, bar, Ks, Vs, qu, qv, S);
-    for (int e = lane; e < nq * HD; e += 32) {
-        const int i = e / HD, d = e - (e / HD) * HD;
-        const float qq = qsrc[(long long)i * a.ldq + d];
-        qu[i * HD + d] = qq + __ldg(a.pbu + h * HD + d);
-        qv[i * HD + d] = qq + __ldg(a.pbv + h * HD + d);
-    }
-    const bool landed = mbar_wait(bar, 0) && mbar_wait(pbar, 0);
-    __syncwarp();
-    if (!landed) {
-        if (lane == 0) latch_error(status, CAC_E_TIMEOUT);
-        return;
-    }
-    // scores
-    for (int j0 = 0; j0 < Nk; j0 += 32) {
-        const int j = j0 + lane;
-        const bool valid = j < Nk;
-        const int pk = kpos0 + j;
-        float acc[NQ];
-        bool ok[NQ];
-        int prow[NQ];
-#pragma unroll
-        for (int i = 0; i < NQ; ++i) {
-            acc[i] = 0.f;
-            ok[i] = i < nq && valid && allowed(a, pq0 + i, pk);
-            prow[i] = ok[i] ? (pq0 + i - pk - a.rmin) * PS : 0;
-        }
-        if (valid) {
-            const T* krow = Ks + j * HD;
-#pragma unroll 1
-            for (int c = 0; c < CPR; ++c) {
-                const int cc = (c + lane) & (CPR - 1);
-                float kf[EPC];
-                chunk_to_f<T, EPC>(krow + cc * EPC, kf);
-#pragma unroll
-                for (int i = 0; i < NQ; ++i) {
-                    if (!ok[i]) continue;
-                    const float* qa = qu + i * HD + cc * EPC;
-                    const float* qb = qv + i * HD + cc * EPC;
-                    const float* pr = Ps + prow[i] + cc * EPC;
-#pragma unroll
-                    for (int e = 0; e < EPC; e += 4) {
-                        const float4 ua = *reinterpret_cast<const float4*>(qa + e);
-                        const float4 va = *reinterpret_cast<const float4*>(qb + e);
-                        const float4 p4 = *reinterpret_cast<const float4*>(pr + e);
-                        acc[i] += ua.x * kf[e] + ua.y * kf[e + 1] + ua.z * kf[e + 2] + ua.w * kf[e + 3];
-                        acc[i] += va.x * p4.x + va.y * p4.y + va.z * p4.z + va.w * p4.w;
-                    }
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < NQ; ++i)
-                if (i < nq) S[i * NK + j] = ok[i] ? acc[i] * a.scale : -FLT_MAX;
-        }
-    }
-    __syncwarp();
-    // softmax over the keys of each query
-#pragma unroll 1
-    for (int i = 0; i < nq; ++i) {
-        float m = -FLT_MAX;
-        for (int j = lane; j < Nk; j += 32) m = fmaxf(m, S[i * NK + j]);
-        m = warp_max(m);
-        float sum = 0.f;
-        for (int j = lane; j < Nk; j += 32) {
-            const float s = S[i * NK + j];
-            const float e = (s == -FLT_MAX) ? 0.f : __expf(s - m);
-            S[i * NK + j] = e;
-            sum += e;
-        }
-        sum = warp_sum(sum);
-        const float inv = 1.f / sum;
-        for (int j = lane; j < Nk; j += 32) S[i * NK + j] *= inv;
-    }
-    __syncwarp();
-    // probs @ V
-    float acc[NQ][DPL];
-#pragma unroll
-    for (int i = 0; i < NQ; ++i)
-#pragma unroll
-        for (int t = 0; t < DPL; ++t) acc[i][t] = 0.f;
-    const int d0 = lane * DPL;
-    const bool dl = d0 < HD;
-#pragma unroll 4
-    for (int j = 0; j < Nk; ++j) {
-        float vv[DPL];
-#pragma unroll
-        for (int t = 0; t < DPL; ++t) vv[t] = dl ? to_f(Vs[j * HD + d0 + t]) : 0.f;
-#pragma unroll
-        for (int i = 0; i < NQ; ++i) {
-            if (i >= nq) break;
-            const float pij = S[i * NK + j];
-#pragma unroll
-            for (int t = 0; t < DPL; ++t) acc[i][t] = fmaf(pij, vv[t], acc[i][t]);
-        }
-    }
-    if (dl) {
-#pragma unroll
-        for (int i = 0; i < NQ; ++i) {
-            if (i >= nq) break;
-#pragma unroll
-            for (int t = 0; t < DPL; ++t) dst[(long long)i * a.ldo + d0 + t] = from_f<T>(acc[i][t]);
-        }
-    }
-}
-
-constexpr int ATT_WARPS = 4;
-
-// streaming: block = (ATT_WARPS batch slots, head); keys = [cache | new] from the ring,
-// whose rows for one stream and head are contiguous modulo R: at most two copies each.
-template <int HD, int NQ, int NK, class T>
-__global__ void __launch_bounds__(ATT_WARPS * 32) attn_stream_kernel(AttnParams a, int* status) {
-    using Lay = AttnLayout<HD, NQ, NK, T>;
+// streaming: units = batch slots; keys = [cache | new] from the stream's ring
+template <int HD, int NQW, int WPS, int SPB, int NK, class T>
+__global__ void __launch_bounds__(SPB * WPS * 32) attn_stream_kernel(AttnParams a, int* status) {
+    using A = Attn<HD, NQW, WPS, SPB, NK, T>;
     extern __shared__ float4 sm4[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(sm4);
     const int h = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int b = blockIdx.x * ATT_WARPS + warp;
+    const int slot = warp / WPS, wsub = warp % WPS;
+    const int b = blockIdx.x * SPB + slot;
     const bool live = b < a.nb;
     uint64_t* pbar = reinterpret_cast<uint64_t*>(sm);
     float* Ps = reinterpret_cast<float*>(sm + 16);
-    uint8_t* wsm = sm + 16 + ((a.NR * Lay::PS * 4 + 15) & ~15) + warp * Lay::WARP_BYTES;
+    uint8_t* usm = sm + 16 + ((a.NR * A::PS * 4 + 15) & ~15) + slot * A::UNIT_BYTES;
     stage_ptable<HD>(a, h, Ps, pbar);
     int id = 0, p0 = 0, Lc = 0, Nk = 0;
     if (live) {
@@ -386,14 +417,13 @@ __global__ void __launch_bounds__(ATT_WARPS * 32) attn_stream_kernel(AttnParams 
         p0 = a.pos[id];
         Lc = min(p0, a.left);
         Nk = min(Lc + a.nq, NK);
-        if (lane == 0) {
-            uint64_t* bar;
-            T *Ks, *Vs;
-            float *qu, *qv, *S;
-            attn_carve<HD, NQ, NK, T>(wsm, bar, Ks, Vs, qu, qv, S);
+        if (wsub == 0 && lane == 0) {
+            uint64_t* bar = reinterpret_cast<uint64_t*>(usm);
+            T* Ks = reinterpret_cast<T*>(usm + 16);
+            T* Vs = Ks + A::KV;
+            constexpr uint32_t ROW = HD * sizeof(T);
             mbar_init(bar, 1);
             fence_mbar_init();
-            constexpr uint32_t ROW = HD * sizeof(T);
             mbar_expect_tx(bar, 2u * ROW * Nk);
             const long long base = (long long)id * a.sstride + (long long)h * a.R * HD;
             const T* kb = static_cast<const T*>(a.k) + base;
@@ -410,25 +440,27 @@ __global__ void __launch_bounds__(ATT_WARPS * 32) attn_stream_kernel(AttnParams 
     }
     __syncthreads();
     if (!live) return;
-    attend_warp<HD, NQ, NK, T>(a, h, Ps, pbar, wsm, lane, a.q + (long long)b * a.nq * a.ldq + h * HD, p0, a.nq, p0 - Lc,
-                               Nk, static_cast<T*>(a.out) + (long long)b * a.nq * a.ldo + h * HD, status);
+    attend<HD, NQW, WPS, SPB, NK, T>(a, h, Ps, pbar, usm, wsub, lane, a.q + (long long)b * a.nq * a.ldq + h * HD, p0,
+                                     a.nq, p0 - Lc, Nk, static_cast<T*>(a.out) + (long long)b * a.nq * a.ldo + h * HD,
+                                     status);
 }
 
-// offline: block = (ATT_WARPS query groups of one sequence, head); keys from dense K/V
-// rows (one bulk copy per row, issued by the lanes of the warp).
-template <int HD, int NQ, int NK, class T>
-__global__ void __launch_bounds__(ATT_WARPS * 32) attn_offline_kernel(AttnParams a, int qgroup, int* status) {
-    using Lay = AttnLayout<HD, NQ, NK, T>;
+// offline: units = query groups (one mask chunk, or `qgroup` frames of a window
+// mask) of one sequence; keys from the dense K/V rows, one bulk copy per row.
+template <int HD, int NQW, int WPS, int SPB, int NK, class T>
+__global__ void __launch_bounds__(SPB * WPS * 32) attn_offline_kernel(AttnParams a, int qgroup, int* status) {
+    using A = Attn<HD, NQW, WPS, SPB, NK, T>;
     extern __shared__ float4 sm4[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(sm4);
     const int h = blockIdx.y, seq = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slot = warp / WPS, wsub = warp % WPS;
     const int len = a.seq_len[seq];
-    const int pq0 = (blockIdx.x * ATT_WARPS + warp) * qgroup;
+    const int pq0 = (blockIdx.x * SPB + slot) * qgroup;
     const bool live = pq0 < len;
     uint64_t* pbar = reinterpret_cast<uint64_t*>(sm);
     float* Ps = reinterpret_cast<float*>(sm + 16);
-    uint8_t* wsm = sm + 16 + ((a.NR * Lay::PS * 4 + 15) & ~15) + warp * Lay::WARP_BYTES;
+    uint8_t* usm = sm + 16 + ((a.NR * A::PS * 4 + 15) & ~15) + slot * A::UNIT_BYTES;
     stage_ptable<HD>(a, h, Ps, pbar);
     int nq = 0, klo = 0, Nk = 0;
     const long long rb = (long long)seq * a.T;
@@ -444,34 +476,29 @@ __global__ void __launch_bounds__(ATT_WARPS * 32) attn_offline_kernel(AttnParams
             khi = min((pql / a.chunk) * a.chunk + a.chunk - 1, len - 1);
         }
         Nk = min(khi - klo + 1, NK);
-        uint64_t* bar;
-        T *Ks, *Vs;
-        float *qu, *qv, *S;
-        attn_carve<HD, NQ, NK, T>(wsm, bar, Ks, Vs, qu, qv, S);
-        constexpr uint32_t ROW = HD * sizeof(T);
-        if (lane == 0) {
-            mbar_init(bar, 1);
-            fence_mbar_init();
-            mbar_expect_tx(bar, 2u * ROW * Nk);
-        }
-        __syncwarp();
-        const T* kb = static_cast<const T*>(a.k) + rb * a.ldk + h * HD;
-        const T* vb = static_cast<const T*>(a.v) + rb * a.ldk + h * HD;
-        for (int j = lane; j < Nk; j += 32) {
-            bulk_g2s(Ks + j * HD, kb + (long long)(klo + j) * a.ldk, ROW, bar);
-            bulk_g2s(Vs + j * HD, vb + (long long)(klo + j) * a.ldk, ROW, bar);
+        if (wsub == 0) {
+            uint64_t* bar = reinterpret_cast<uint64_t*>(usm);
+            T* Ks = reinterpret_cast<T*>(usm + 16);
+            T* Vs = Ks + A::KV;
+            constexpr uint32_t ROW = HD * sizeof(T);
+            if (lane == 0) {
+                mbar_init(bar, 1);
+                fence_mbar_init();
+                mbar_expect_tx(bar, 2u * ROW * Nk);
+            }
+            __syncwarp();
+            const T* kb = static_cast<const T*>(a.k) + rb * a.ldk + h * HD;
+            const T* vb = static_cast<const T*>(a.v) + rb * a.ldk + h * HD;
+            for (int j = lane; j < Nk; j += 32) {
+                bulk_g2s(Ks + j * HD, kb + (long long)(klo + j) * a.ldk, ROW, bar);
+                bulk_g2s(Vs + j * HD, vb + (long long)(klo + j) * a.ldk, ROW, bar);
+            }
         }
     }
     __syncthreads();
     if (!live) return;
-    attend_warp<HD, NQ, NK, T>(a, h, Ps, pbar, wsm, lane, a.q + (rb + pq0) * a.ldq + h * HD, pq0, nq, klo, Nk,
-                               static_cast<T*>(a.out) + (rb + pq0) * a.ldo + h * HD, status);
-}
-
-template <int HD, int NQ, int NK, class T>
-static size_t attn_smem(const AttnParams& a) {
-    using Lay = AttnLayout<HD, NQ, NK, T>;
-    return 16 + ((size_t)a.NR * Lay::PS * 4 + 15) / 16 * 16 + (size_t)ATT_WARPS * Lay::WARP_BYTES;
+    attend<HD, NQW, WPS, SPB, NK, T>(a, h, Ps, pbar, usm, wsub, lane, a.q + (rb + pq0) * a.ldq + h * HD, pq0, nq, klo,
+                                     Nk, static_cast<T*>(a.out) + (rb + pq0) * a.ldo + h * HD, status);
 }
 
 template <class K>
@@ -484,59 +511,64 @@ static cudaError_t raise_smem(K kern, size_t smem, size_t& attr) {
     return e;
 }
 
-template <int HD, int NQ, int NK, class T>
+template <int HD, int NQW, int WPS, int SPB, int NK, class T>
 static cudaError_t attn_stream_launch(const AttnParams& a, int* status, cudaStream_t s) {
-    const size_t smem = attn_smem<HD, NQ, NK, T>(a);
-    auto kern = attn_stream_kernel<HD, NQ, NK, T>;
+    using A = Attn<HD, NQW, WPS, SPB, NK, T>;
+    const size_t smem = A::smem(a.NR);
+    auto kern = attn_stream_kernel<HD, NQW, WPS, SPB, NK, T>;
     static size_t attr = 48 * 1024;  // dynamic shared memory limit set so far for this instantiation
     cudaError_t e = raise_smem(kern, smem, attr);
     if (e != cudaSuccess) return e;
-    dim3 grid((a.nb + ATT_WARPS - 1) / ATT_WARPS, a.H);
-    kern<<<grid, ATT_WARPS * 32, smem, s>>>(a, status);
+    dim3 grid((a.nb + SPB - 1) / SPB, a.H);
+    kern<<<grid, A::THREADS, smem, s>>>(a, status);
     return cudaGetLastError();
 }
 
-template <int HD, int NQ, int NK, class T>
+template <int HD, int NQW, int WPS, int SPB, int NK, class T>
 static cudaError_t attn_offline_launch(const AttnParams& a, int qgroup, int* status, cudaStream_t s) {
-    const size_t smem = attn_smem<HD, NQ, NK, T>(a);
-    auto kern = attn_offline_kernel<HD, NQ, NK, T>;
+    using A = Attn<HD, NQW, WPS, SPB, NK, T>;
+    const size_t smem = A::smem(a.NR);
+    auto kern = attn_offline_kernel<HD, NQW, WPS, SPB, NK, T>;
     static size_t attr = 48 * 1024;
     cudaError_t e = raise_smem(kern, smem, attr);
     if (e != cudaSuccess) return e;
     const int groups = (a.T + qgroup - 1) / qgroup;
-    dim3 grid((groups + ATT_WARPS - 1) / ATT_WARPS, a.H, a.nb);
-    kern<<<grid, ATT_WARPS * 32, smem, s>>>(a, qgroup, status);
+    dim3 grid((groups + SPB - 1) / SPB, a.H, a.nb);
+    kern<<<grid, A::THREADS, smem, s>>>(a, qgroup, status);
     return cudaGetLastError();
 }
 
-#define ATT_DISPATCH(LAUNCH, NQ, NK, ...)                                                                  \
-    do {                                                                                                   \
-        if (a.HD == 64)                                                                                    \
-            return act_bf16 ? LAUNCH<64, NQ, NK, bf16>(__VA_ARGS__) : LAUNCH<64, NQ, NK, float>(__VA_ARGS__); \
-        if (a.HD == 16)                                                                                    \
-            return act_bf16 ? LAUNCH<16, NQ, NK, bf16>(__VA_ARGS__) : LAUNCH<16, NQ, NK, float>(__VA_ARGS__); \
+#define ATT_DISPATCH(LAUNCH, NQW, WPS, SPB, NK, ...)                                                     \
+    do {                                                                                                 \
+        if (a.HD == 64)                                                                                  \
+            return act_bf16 ? LAUNCH<64, NQW, WPS, SPB, NK, bf16>(__VA_ARGS__)                           \
+                            : LAUNCH<64, NQW, WPS, SPB, NK, float>(__VA_ARGS__);                         \
+        if (a.HD == 16)                                                                                  \
+            return act_bf16 ? LAUNCH<16, NQW, WPS, SPB, NK, bf16>(__VA_ARGS__)                           \
+                            : LAUNCH<16, NQW, WPS, SPB, NK, float>(__VA_ARGS__);                         \
     } while (0)
 
-// NQ x NK instantiations: 160 ms pushes (2 queries, keys <= left + 2), chunked
-// pushes of up to 8 frames (keys <= left + 8), provisional passes (up to 24
-// queries, keys <= left + 24); offline groups of up to 8 queries.
+// Instantiations (queries per unit = NQW * WPS): 160 ms pushes (2 queries,
+// keys <= left + 2: 4 units x 2 warps per block), chunked pushes of up to 8
+// frames (keys <= left + 8: 2 units x 4 warps), provisional passes (up to 24
+// queries, keys <= left + 24: 1 unit x 8 warps); offline groups of <= 8.
 cudaError_t launch_attention_stream(const AttnParams& a, int act_bf16, int* status, cudaStream_t s) {
     if (a.nb <= 0) return cudaSuccess;
     const int nk_need = a.left + a.nq;
-    if (a.nq <= 2 && nk_need <= 80) ATT_DISPATCH(attn_stream_launch, 2, 80, a, status, s);
-    if (a.nq <= 8 && nk_need <= 80) ATT_DISPATCH(attn_stream_launch, 8, 80, a, status, s);
-    if (a.nq <= 24 && nk_need <= 96) ATT_DISPATCH(attn_stream_launch, 24, 96, a, status, s);
+    if (a.nq <= 2 && nk_need <= 80) ATT_DISPATCH(attn_stream_launch, 1, 2, 4, 80, a, status, s);
+    if (a.nq <= 8 && nk_need <= 80) ATT_DISPATCH(attn_stream_launch, 2, 4, 2, 80, a, status, s);
+    if (a.nq <= 24 && nk_need <= 96) ATT_DISPATCH(attn_stream_launch, 3, 8, 1, 96, a, status, s);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attention_offline(const AttnParams& a, int act_bf16, int* status, cudaStream_t s) {
     if (a.nb <= 0) return cudaSuccess;
-    // queries per warp: one chunk of the chunked mask, or 8 consecutive frames of a window mask
+    // queries per unit: one chunk of the chunked mask, or 8 consecutive frames of a window mask
     const int qgroup = a.rc > 0 ? 8 : a.chunk;
     const int nk_need = a.rc > 0 ? a.left + qgroup + a.rc : a.left + a.chunk;
     if (qgroup > 8 || nk_need > 96) return cudaErrorInvalidValue;
-    if (qgroup <= 2 && nk_need <= 80) ATT_DISPATCH(attn_offline_launch, 2, 80, a, qgroup, status, s);
-    ATT_DISPATCH(attn_offline_launch, 8, 96, a, qgroup, status, s);
+    if (qgroup <= 2 && nk_need <= 80) ATT_DISPATCH(attn_offline_launch, 1, 2, 4, 80, a, qgroup, status, s);
+    ATT_DISPATCH(attn_offline_launch, 2, 4, 2, 96, a, qgroup, status, s);
     return cudaErrorInvalidValue;
 }
 
