@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cstdlib>
+
 #include "../../include/cac.h"
 
 namespace cac {
@@ -26,6 +28,51 @@ template <> __device__ __forceinline__ bf16 from_f<bf16>(float v) { return __flo
 // fast-math forms (__expf, __fdividef): a few ulp, far inside the bf16 tolerance
 __device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 __device__ __forceinline__ float siluf_(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
+// ---------------------------------------------------------------------------
+// programmatic dependent launch: every kernel lets its successor launch at
+// entry, and waits for its predecessor's completion (and memory) before it
+// reads anything the predecessor may have written.  Work that needs only
+// weights (their tensor-map prefetch, TMA loads) goes before the wait.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch with the programmatic-serialization attribute (unless CAC_PDL=0 in
+// the environment) and an optional cluster of cluster_z CTAs along z.
+inline bool pdl_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("CAC_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+template <class... KArgs, class... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            int cluster_z, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    int n = 0;
+    if (pdl_enabled()) {
+        at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster_z > 1) {
+        at[n].id = cudaLaunchAttributeClusterDimension;
+        at[n].val.clusterDim.x = 1;
+        at[n].val.clusterDim.y = 1;
+        at[n].val.clusterDim.z = cluster_z;
+        ++n;
+    }
+    cfg.attrs = at;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // ---------------------------------------------------------------------------
 // device status word: first error wins, read back by cac_pool_check

@@ -15,6 +15,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const TA* __restrict__ A
     __shared__ float As[16][64 + 4];
     __shared__ float Bs[16][64 + 4];
     __shared__ float Cs[64][64 + 1];
+    pdl_trigger();
+    pdl_wait();
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
     float acc[4][4] = {};
@@ -63,14 +65,13 @@ static cudaError_t launch_t(const void* A, long long lda, const void* B, long lo
     const TA* a = static_cast<const TA*>(A);
     const TA* b = static_cast<const TA*>(B);
     switch (ep.kind) {
-        case EPI_STORE: gemm_simt_kernel<TA, EPI_STORE, TAct><<<grid, 256, 0, s>>>(a, lda, b, ldb, M, N, K, ep); break;
-        case EPI_RESID: gemm_simt_kernel<TA, EPI_RESID, TAct><<<grid, 256, 0, s>>>(a, lda, b, ldb, M, N, K, ep); break;
-        case EPI_GLU: gemm_simt_kernel<TA, EPI_GLU, TAct><<<grid, 256, 0, s>>>(a, lda, b, ldb, M, N, K, ep); break;
-        case EPI_QKV: gemm_simt_kernel<TA, EPI_QKV, TAct><<<grid, 256, 0, s>>>(a, lda, b, ldb, M, N, K, ep); break;
-        case EPI_SUB: gemm_simt_kernel<TA, EPI_SUB, TAct><<<grid, 256, 0, s>>>(a, lda, b, ldb, M, N, K, ep); break;
-        default: return cudaErrorInvalidValue;
+        case EPI_STORE: return launch_k(gemm_simt_kernel<TA, EPI_STORE, TAct>, grid, dim3(256), 0, s, 1, a, lda, b, ldb, M, N, K, ep);
+        case EPI_RESID: return launch_k(gemm_simt_kernel<TA, EPI_RESID, TAct>, grid, dim3(256), 0, s, 1, a, lda, b, ldb, M, N, K, ep);
+        case EPI_GLU: return launch_k(gemm_simt_kernel<TA, EPI_GLU, TAct>, grid, dim3(256), 0, s, 1, a, lda, b, ldb, M, N, K, ep);
+        case EPI_QKV: return launch_k(gemm_simt_kernel<TA, EPI_QKV, TAct>, grid, dim3(256), 0, s, 1, a, lda, b, ldb, M, N, K, ep);
+        case EPI_SUB: return launch_k(gemm_simt_kernel<TA, EPI_SUB, TAct>, grid, dim3(256), 0, s, 1, a, lda, b, ldb, M, N, K, ep);
     }
-    return cudaGetLastError();
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm_simt(int bf16_operands, const void* A, long long lda, const void* B, long long ldb, int M,

@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     const int kb0 = (int)(crank * nk_all / splits), kb1 = (int)((crank + 1) * nk_all / splits);
     const int nk = kb1 - kb0;
 
+    pdl_trigger();
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -83,19 +84,29 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
 
     bool ok = true;
     if (warp == 0 && lane == 0) {
+        // weights never depend on the previous kernel: start the first stages' B
+        // tiles before waiting for it, then the activations
+        const int pre = nk < C::STAGES ? nk : C::STAGES;
+        for (int kb = 0; kb < pre; ++kb) {
+            mbar_expect_tx(&full[kb], C::STAGE);
+            tma_load_2d(sB + kb * C::B_TILE, &tmB, (kb0 + kb) * BK, n0, &full[kb]);
+        }
+        pdl_wait();
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % C::STAGES;
             const uint32_t ph = (kb / C::STAGES) & 1;
-            if (!mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }
-            mbar_expect_tx(&full[s], C::STAGE);
             const int k0 = (kb0 + kb) * BK;
+            if (kb >= pre) {
+                if (!mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }
+                mbar_expect_tx(&full[s], C::STAGE);
+                tma_load_2d(sB + s * C::B_TILE, &tmB, k0, n0, &full[s]);
+            }
             if (conv_C) {
                 const int tap = k0 / conv_C;
                 tma_load_3d(sA + s * A_TILE, &tmA, k0 - tap * conv_C, tap & 1, m0 + (tap >> 1), &full[s]);
             } else {
                 tma_load_2d(sA + s * A_TILE, &tmA, k0, m0, &full[s]);
             }
-            tma_load_2d(sB + s * C::B_TILE, &tmB, k0, n0, &full[s]);
         }
     } else if (warp == 1 && lane == 0) {
         constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
@@ -116,6 +127,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
         tc_commit(accb);
     }
     __syncwarp();
+    pdl_wait();  // the epilogue reads/writes buffers of earlier kernels
 
     if (!mbar_wait(accb, 0)) ok = false;
     tc_fence_after();
@@ -210,19 +222,8 @@ static cudaError_t launch_bn_kind(const CUtensorMap* tmA, const CUtensorMap* tmB
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(N / BN, (M + BM - 1) / BM, splits);
-    cfg.blockDim = dim3(TC_THREADS);
-    cfg.dynamicSmemBytes = C::SMEM;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = splits;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, *tmA, *tmB, M, N, K, conv_C, ep, status);
+    return launch_k(kern, dim3(N / BN, (M + BM - 1) / BM, splits), dim3(TC_THREADS), C::SMEM, s, splits, *tmA, *tmB,
+                    M, N, K, conv_C, ep, status);
 }
 
 template <int BN>

@@ -43,6 +43,8 @@ template <int VPL, class TA>
 __global__ void __launch_bounds__(256) ln_kernel(const float* x, int M, int D, const float* g1, const float* b1,
                                                  float* y_f32, TA* y_act, const float* g2, const float* b2,
                                                  TA* z_act, int grp, int grp_stride, int row_off) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (row >= M) return;
@@ -75,14 +77,13 @@ static cudaError_t ln_dispatch(const float* x, int M, int D, const float* g1, co
     TA* za = static_cast<TA*>(z_act);
 #define LN_CASE(V)                                                                                       \
     case V:                                                                                              \
-        ln_kernel<V, TA><<<grid, 256, 0, s>>>(x, M, D, g1, b1, y_f32, ya, g2, b2, za, grp, grp_stride, row_off); \
-        break;
+        return launch_k(ln_kernel<V, TA>, grid, dim3(256), 0, s, 1, x, M, D, g1, b1, y_f32, ya, g2, b2, za, grp,   \
+                        grp_stride, row_off);
     switch (D / 32) {
         LN_CASE(2) LN_CASE(4) LN_CASE(8) LN_CASE(16) LN_CASE(24) LN_CASE(32)
         default: return cudaErrorInvalidValue;
     }
 #undef LN_CASE
-    return cudaGetLastError();
 }
 
 cudaError_t launch_layernorm(const float* x, int M, int D, const float* g1, const float* b1, float* y_f32,
@@ -104,6 +105,8 @@ template <class T>
 __global__ void __launch_bounds__(256) stage_mel_kernel(const float* mel, long long mel_bstride, const int* n_valid,
                                                         T* win, T* tail, const int* ids, const int* pos, int n,
                                                         int* status) {
+    pdl_trigger();
+    pdl_wait();
     const int b = blockIdx.x;
     const int id = ids[b];
     const bool first = pos[id] == 0;
@@ -134,17 +137,17 @@ cudaError_t launch_stage_mel(const float* mel, long long mel_bstride, const int*
                              cudaStream_t s) {
     if (nb <= 0) return cudaSuccess;
     if (act_bf16)
-        stage_mel_kernel<bf16><<<nb, 256, 0, s>>>(mel, mel_bstride, n_valid, static_cast<bf16*>(win),
-                                                  static_cast<bf16*>(tail), ids, pos, n, status);
-    else
-        stage_mel_kernel<float><<<nb, 256, 0, s>>>(mel, mel_bstride, n_valid, static_cast<float*>(win),
-                                                   static_cast<float*>(tail), ids, pos, n, status);
-    return cudaGetLastError();
+        return launch_k(stage_mel_kernel<bf16>, dim3(nb), dim3(256), 0, s, 1, mel, mel_bstride, n_valid,
+                        static_cast<bf16*>(win), static_cast<bf16*>(tail), ids, pos, n, status);
+    return launch_k(stage_mel_kernel<float>, dim3(nb), dim3(256), 0, s, 1, mel, mel_bstride, n_valid,
+                    static_cast<float*>(win), static_cast<float*>(tail), ids, pos, n, status);
 }
 
 template <class T>
 __global__ void stage_mel_offline_kernel(const float* mel, int t_mel, const int* len, T* dst, int W, int B,
                                          int* status) {
+    pdl_trigger();
+    pdl_wait();
     const long long total = (long long)B * W * MEL;
     bool bad = false;
     for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
@@ -166,11 +169,10 @@ cudaError_t launch_stage_mel_offline(const float* mel, int t_mel, const int* len
                                      int act_bf16, int* status, cudaStream_t s) {
     const int blocks = 152 * 8;
     if (act_bf16)
-        stage_mel_offline_kernel<bf16><<<blocks, 256, 0, s>>>(mel, t_mel, len, static_cast<bf16*>(dst), W, B, status);
-    else
-        stage_mel_offline_kernel<float><<<blocks, 256, 0, s>>>(mel, t_mel, len, static_cast<float*>(dst), W, B,
-                                                               status);
-    return cudaGetLastError();
+        return launch_k(stage_mel_offline_kernel<bf16>, dim3(blocks), dim3(256), 0, s, 1, mel, t_mel, len,
+                        static_cast<bf16*>(dst), W, B, status);
+    return launch_k(stage_mel_offline_kernel<float>, dim3(blocks), dim3(256), 0, s, 1, mel, t_mel, len,
+                    static_cast<float*>(dst), W, B, status);
 }
 
 // ---------------------------------------------------------------------------
@@ -410,7 +412,9 @@ __global__ void __launch_bounds__(SPB * WPS * 32) attn_stream_kernel(AttnParams 
     uint64_t* pbar = reinterpret_cast<uint64_t*>(sm);
     float* Ps = reinterpret_cast<float*>(sm + 16);
     uint8_t* usm = sm + 16 + ((a.NR * A::PS * 4 + 15) & ~15) + slot * A::UNIT_BYTES;
-    stage_ptable<HD>(a, h, Ps, pbar);
+    pdl_trigger();
+    stage_ptable<HD>(a, h, Ps, pbar);  // weights: before waiting for the QKV projection
+    pdl_wait();
     int id = 0, p0 = 0, Lc = 0, Nk = 0;
     if (live) {
         id = a.ids[b];
@@ -461,7 +465,9 @@ __global__ void __launch_bounds__(SPB * WPS * 32) attn_offline_kernel(AttnParams
     uint64_t* pbar = reinterpret_cast<uint64_t*>(sm);
     float* Ps = reinterpret_cast<float*>(sm + 16);
     uint8_t* usm = sm + 16 + ((a.NR * A::PS * 4 + 15) & ~15) + slot * A::UNIT_BYTES;
+    pdl_trigger();
     stage_ptable<HD>(a, h, Ps, pbar);
+    pdl_wait();
     int nq = 0, klo = 0, Nk = 0;
     const long long rb = (long long)seq * a.T;
     if (live) {
@@ -520,8 +526,7 @@ static cudaError_t attn_stream_launch(const AttnParams& a, int* status, cudaStre
     cudaError_t e = raise_smem(kern, smem, attr);
     if (e != cudaSuccess) return e;
     dim3 grid((a.nb + SPB - 1) / SPB, a.H);
-    kern<<<grid, A::THREADS, smem, s>>>(a, status);
-    return cudaGetLastError();
+    return launch_k(kern, grid, dim3(A::THREADS), smem, s, 1, a, status);
 }
 
 template <int HD, int NQW, int WPS, int SPB, int NK, class T>
@@ -534,8 +539,7 @@ static cudaError_t attn_offline_launch(const AttnParams& a, int qgroup, int* sta
     if (e != cudaSuccess) return e;
     const int groups = (a.T + qgroup - 1) / qgroup;
     dim3 grid((groups + SPB - 1) / SPB, a.H, a.nb);
-    kern<<<grid, A::THREADS, smem, s>>>(a, qgroup, status);
-    return cudaGetLastError();
+    return launch_k(kern, grid, dim3(A::THREADS), smem, s, 1, a, qgroup, status);
 }
 
 #define ATT_DISPATCH(LAUNCH, NQW, WPS, SPB, NK, ...)                                                     \
@@ -582,13 +586,16 @@ __global__ void __launch_bounds__(256) dwconv_kernel(const T* glu, T* cache, lon
                                                      const int* pos, int nq, int n_commit, const float* wT,
                                                      const float* bdw, const float* bng, const float* bnb, T* out,
                                                      int D, int nb) {
+    pdl_trigger();
     const long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-    if (idx >= (long long)nb * D) return;
     const int b = (int)(idx / D), c = (int)(idx % D);
     float w[9];
+    const int cw = idx < (long long)nb * D ? c : 0;
 #pragma unroll
-    for (int k = 0; k < 9; ++k) w[k] = __ldg(wT + k * D + c);
-    const float bias = __ldg(bdw + c), gam = __ldg(bng + c), bet = __ldg(bnb + c);
+    for (int k = 0; k < 9; ++k) w[k] = __ldg(wT + k * D + cw);
+    const float bias = __ldg(bdw + cw), gam = __ldg(bng + cw), bet = __ldg(bnb + cw);
+    pdl_wait();
+    if (idx >= (long long)nb * D) return;
     float win[9];
     int p0 = 0;
     T* cs = nullptr;
@@ -628,37 +635,37 @@ cudaError_t launch_dwconv(const void* glu, void* cache, long long cs_stride, con
     const long long threads = (long long)nb * D;
     const int blocks = (int)((threads + 255) / 256);
     if (act_bf16)
-        dwconv_kernel<bf16><<<blocks, 256, 0, s>>>(static_cast<const bf16*>(glu), static_cast<bf16*>(cache), cs_stride,
-                                                   ids, pos, nq, n_commit, wT, bdw, bng, bnb, static_cast<bf16*>(out),
-                                                   D, nb);
-    else
-        dwconv_kernel<float><<<blocks, 256, 0, s>>>(static_cast<const float*>(glu), static_cast<float*>(cache),
-                                                    cs_stride, ids, pos, nq, n_commit, wT, bdw, bng, bnb,
-                                                    static_cast<float*>(out), D, nb);
-    return cudaGetLastError();
+        return launch_k(dwconv_kernel<bf16>, dim3(blocks), dim3(256), 0, s, 1, static_cast<const bf16*>(glu),
+                        static_cast<bf16*>(cache), cs_stride, ids, pos, nq, n_commit, wT, bdw, bng, bnb,
+                        static_cast<bf16*>(out), D, nb);
+    return launch_k(dwconv_kernel<float>, dim3(blocks), dim3(256), 0, s, 1, static_cast<const float*>(glu),
+                    static_cast<float*>(cache), cs_stride, ids, pos, nq, n_commit, wT, bdw, bng, bnb,
+                    static_cast<float*>(out), D, nb);
 }
 
 // ---------------------------------------------------------------------------
 // bookkeeping and small utilities
 // ---------------------------------------------------------------------------
 __global__ void advance_kernel(int* pos, const int* ids, int nb, int n) {
+    pdl_trigger();
+    pdl_wait();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b < nb) pos[ids[b]] += n;
 }
 __global__ void set_pos_kernel(int* pos, const int* ids, int nb, int value) {
+    pdl_trigger();
+    pdl_wait();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b < nb) pos[ids[b]] = value;
 }
 
 cudaError_t launch_advance(int* pos, const int* ids, int nb, int n, cudaStream_t s) {
     if (nb <= 0) return cudaSuccess;
-    advance_kernel<<<(nb + 255) / 256, 256, 0, s>>>(pos, ids, nb, n);
-    return cudaGetLastError();
+    return launch_k(advance_kernel, dim3((nb + 255) / 256), dim3(256), 0, s, 1, pos, ids, nb, n);
 }
 cudaError_t launch_set_pos(int* pos, const int* ids, int nb, int value, cudaStream_t s) {
     if (nb <= 0) return cudaSuccess;
-    set_pos_kernel<<<(nb + 255) / 256, 256, 0, s>>>(pos, ids, nb, value);
-    return cudaGetLastError();
+    return launch_k(set_pos_kernel, dim3((nb + 255) / 256), dim3(256), 0, s, 1, pos, ids, nb, value);
 }
 
 __global__ void sinusoid_kernel(float* pe, int NR, int rmin, int D) {
@@ -679,6 +686,7 @@ cudaError_t launch_sinusoid(float* pe, int NR, int rmin, int D, cudaStream_t s) 
 
 template <class T>
 __global__ void to_f32_kernel(const T* src, float* dst, long long n) {
+    pdl_wait();
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
         dst[i] = to_f(src[i]);
 }
