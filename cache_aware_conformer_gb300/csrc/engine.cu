@@ -13,6 +13,7 @@
 #include <tuple>
 #include <vector>
 
+#include "../../include/cac_ops.h"
 #include "gemm.cuh"
 #include "kernels.cuh"
 
@@ -176,6 +177,13 @@ int validate(const cac_config* c) {
     return CAC_OK;
 }
 
+int choose_splits(int tiles, int nk) {
+    // split K until the grid covers most of the 152 SMs (at most 4 ways, >= 2 K slices each)
+    int splits = 1;
+    while (splits < 4 && tiles * splits < 120 && nk / (splits + 1) >= 2) ++splits;
+    return splits;
+}
+
 // GEMM dispatch: tcgen05 for bf16 models (unless the SIMT debugging twin is
 // requested), SIMT for fp32 models.  conv_C > 0: A is a stride-2 convolution
 // window read through the im2col view (M output rows = window row pairs).
@@ -188,10 +196,7 @@ int gemm(cac_model* m, const void* A, long long lda, int M, int K, const Lin& W,
         const bool ok = conv_C ? make_tmap_bf16_conv(&tmA, A, conv_C, (uint64_t)M + 1, 128)
                                : make_tmap_bf16(&tmA, A, K, M, (uint64_t)lda * 2, 128);
         if (!ok) return CAC_E_CUDA;
-        // split K until the grid covers most of the 152 SMs (at most 4 ways, >= 2 K slices each)
-        const int tiles = (W.N / W.BN) * ((M + 127) / 128), nk = K / 64;
-        int splits = 1;
-        while (splits < 4 && tiles * splits < 120 && nk / (splits + 1) >= 2) ++splits;
+        const int splits = choose_splits((W.N / W.BN) * ((M + 127) / 128), K / 64);
         CK(launch_gemm_tc(&tmA, &W.tm, M, W.N, K, W.BN, conv_C, splits, ep, m->status, s));
     } else {
         CK(launch_gemm_simt(m->bf16, A, lda, W.w, K, M, W.N, K, ep, s));
@@ -1339,6 +1344,28 @@ extern "C" int cac_pool_read_profile(cac_pool* p, int n_classes, double* total_m
         launches[r.first] += 1;
     }
     p->rec.clear();
+    return CAC_OK;
+}
+
+extern "C" int cac_op_gemm_bf16(int M, int N, int K, const void* A, const void* B, const float* bias, float* C,
+                                int splits, void* stream) {
+    if (M < 1 || N < 64 || K < 64 || N % 64 || K % 64 || !A || !B || !C || splits < 0 || splits > 4 ||
+        splits > K / 64)
+        return CAC_E_INVAL;
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C) |
+         reinterpret_cast<uintptr_t>(bias)) & 15)
+        return CAC_E_ALIGN;
+    CUtensorMap ta, tb;
+    if (!make_tmap_bf16(&ta, A, K, M, (uint64_t)K * 2, 128) || !make_tmap_bf16(&tb, B, K, N, (uint64_t)K * 2, 64))
+        return CAC_E_CUDA;
+    EpiParams ep;
+    ep.kind = EPI_STORE;
+    ep.act_bf16 = 1;
+    ep.bias = bias;
+    ep.out_f32 = C;
+    ep.ldo = N;
+    if (splits == 0) splits = choose_splits((N / 64) * ((M + 127) / 128), K / 64);
+    CK(launch_gemm_tc(&ta, &tb, M, N, K, 64, 0, splits, ep, nullptr, static_cast<cudaStream_t>(stream)));
     return CAC_OK;
 }
 

@@ -65,7 +65,6 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     const int kb0 = (int)(crank * nk_all / splits), kb1 = (int)((crank + 1) * nk_all / splits);
     const int nk = kb1 - kb0;
 
-    pdl_trigger();
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -130,6 +129,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     pdl_wait();  // the epilogue reads/writes buffers of earlier kernels
 
     if (!mbar_wait(accb, 0)) ok = false;
+    pdl_trigger();  // main loop done: let the next kernel launch while the epilogue runs
     tc_fence_after();
     const int quarter = warp & 3, half = warp >> 2;
     const int rloc = quarter * 32 + lane;

@@ -43,7 +43,6 @@ template <int VPL, class TA>
 __global__ void __launch_bounds__(256) ln_kernel(const float* x, int M, int D, const float* g1, const float* b1,
                                                  float* y_f32, TA* y_act, const float* g2, const float* b2,
                                                  TA* z_act, int grp, int grp_stride, int row_off) {
-    pdl_trigger();
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -51,6 +50,7 @@ __global__ void __launch_bounds__(256) ln_kernel(const float* x, int M, int D, c
     float v[VPL];
 #pragma unroll
     for (int k = 0; k < VPL; ++k) v[k] = x[(long long)row * D + lane + 32 * k];
+    pdl_trigger();
     ln_row<VPL>(v, lane, D, g1, b1);
     if (y_f32) {
         const long long orow = (long long)(row / grp) * grp_stride + (row % grp) + row_off;
@@ -347,6 +347,7 @@ __device__ void attend(const AttnParams& a, int h, const float* Ps, uint64_t* pb
         for (int j = lane; j < Nk; j += 32) Si[j] *= inv;
     }
     __syncwarp();
+    pdl_trigger();
     // probs @ V: key group g takes keys j = g, g + KPS, ...; each lane 8 dims
     float acc[NQW][8];
 #pragma unroll
@@ -412,7 +413,6 @@ __global__ void __launch_bounds__(SPB * WPS * 32) attn_stream_kernel(AttnParams 
     uint64_t* pbar = reinterpret_cast<uint64_t*>(sm);
     float* Ps = reinterpret_cast<float*>(sm + 16);
     uint8_t* usm = sm + 16 + ((a.NR * A::PS * 4 + 15) & ~15) + slot * A::UNIT_BYTES;
-    pdl_trigger();
     stage_ptable<HD>(a, h, Ps, pbar);  // weights: before waiting for the QKV projection
     pdl_wait();
     int id = 0, p0 = 0, Lc = 0, Nk = 0;
@@ -465,7 +465,6 @@ __global__ void __launch_bounds__(SPB * WPS * 32) attn_offline_kernel(AttnParams
     uint64_t* pbar = reinterpret_cast<uint64_t*>(sm);
     float* Ps = reinterpret_cast<float*>(sm + 16);
     uint8_t* usm = sm + 16 + ((a.NR * A::PS * 4 + 15) & ~15) + slot * A::UNIT_BYTES;
-    pdl_trigger();
     stage_ptable<HD>(a, h, Ps, pbar);
     pdl_wait();
     int nq = 0, klo = 0, Nk = 0;
@@ -586,7 +585,6 @@ __global__ void __launch_bounds__(256) dwconv_kernel(const T* glu, T* cache, lon
                                                      const int* pos, int nq, int n_commit, const float* wT,
                                                      const float* bdw, const float* bng, const float* bnb, T* out,
                                                      int D, int nb) {
-    pdl_trigger();
     const long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
     const int b = (int)(idx / D), c = (int)(idx % D);
     float w[9];
@@ -623,6 +621,7 @@ __global__ void __launch_bounds__(256) dwconv_kernel(const T* glu, T* cache, lon
 #pragma unroll
         for (int k = 0; k < 8; ++k) win[k] = win[k + 1];
     }
+    pdl_trigger();
     if (cs) {
         for (int t = max(0, n_commit - 8); t < n_commit; ++t) cs[(long long)((p0 + t) & 7) * D + c] = g[(long long)t * D];
     }

@@ -27,7 +27,8 @@ SYMBOLS = ["cac_weights_size", "cac_model_create", "cac_model_destroy", "cac_poo
            "cac_stream_flush", "cac_stream_flush_frames", "cac_encode_offline", "cac_stream_get_state",
            "cac_stream_set_state", "cac_pool_check", "cac_model_check", "cac_pool_set_graphs",
            "cac_pool_launch_count", "cac_pool_set_trace", "cac_pool_read_trace", "cac_pool_set_profile",
-           "cac_pool_read_profile", "cac_profile_classes", "cac_profile_class_name", "cac_strerror"]
+           "cac_pool_read_profile", "cac_profile_classes", "cac_profile_class_name", "cac_strerror",
+           "cac_op_gemm_bf16"]
 
 
 class CacError(RuntimeError):
@@ -85,6 +86,7 @@ def _lib():
             "cac_profile_classes": (c_int, []),
             "cac_profile_class_name": (c_char_p, [c_int]),
             "cac_strerror": (c_char_p, [c_int]),
+            "cac_op_gemm_bf16": (c_int, [c_int, c_int, c_int, vp, vp, vp, vp, c_int, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -126,6 +128,17 @@ def _stream(stream=None) -> int | None:
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
+
+
+def gemm_bf16(A, B, bias=None, splits: int = 0, out=None, stream=None):
+    """C = A @ B^T (+ bias) on the tcgen05 GEMM (cac_op_gemm_bf16); A [M,K], B [N,K] bf16 cuda."""
+    import torch
+    M, K = A.shape
+    N = B.shape[0]
+    C = out if out is not None else torch.empty(M, N, device=A.device, dtype=torch.float32)
+    _check(_lib().cac_op_gemm_bf16(M, N, K, _ptr(A), _ptr(B), _ptr(bias), _ptr(C), splits, _stream(stream)),
+           "cac_op_gemm_bf16")
+    return C
 
 
 class Model:

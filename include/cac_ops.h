@@ -1,0 +1,29 @@
+/*
+ * cac_ops.h — op-level entry points of the GB300 cache-aware Conformer
+ * library, for kernel-level parity tests and microbenchmarks.  Same
+ * conventions as cac.h (status codes, device pointers owned by the caller,
+ * asynchronous on `stream`).
+ */
+#ifndef CAC_OPS_H_
+#define CAC_OPS_H_
+
+#include "cac.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* C[M][N] = A[M][K] * B[N][K]^T (+ bias[N]) on the tcgen05/TMEM tensor-core
+ * GEMM that every projection of the encoder step uses (feed-forward, Q/K/V,
+ * out-projection, pointwise convolutions, joint projection: "True streaming
+ * encode", §Per-chunk flow step 3).  A and B bf16, row-major (K contiguous);
+ * C fp32 row-major; bias fp32 or NULL.  K % 64 == 0, N % 64 == 0, M >= 1;
+ * 16-byte aligned pointers.  splits: 1..4 K-splits per output tile (reduced
+ * in a thread-block cluster), 0 = the library's choice. */
+int cac_op_gemm_bf16(int M, int N, int K, const void* A, const void* B, const float* bias, float* C, int splits,
+                     void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CAC_OPS_H_ */
