@@ -67,7 +67,8 @@ struct LayerW {
     float *ff1_g = nullptr, *ff1_b = nullptr, *att_g = nullptr, *att_b = nullptr, *conv_g = nullptr,
           *conv_b = nullptr, *ff2_g = nullptr, *ff2_b = nullptr, *out_g = nullptr, *out_b = nullptr;
     Lin ff1_w1, ff1_w2, qkv, wo, pw1, pw2, ff2_w1, ff2_w2;
-    float *pbu = nullptr, *pbv = nullptr, *P = nullptr, *Ppad = nullptr, *dwT = nullptr, *bdw = nullptr, *bng = nullptr,
+    void* Ppad = nullptr;  // attention position table [H][NR][HD], activation dtype
+    float *pbu = nullptr, *pbv = nullptr, *P = nullptr, *dwT = nullptr, *bdw = nullptr, *bng = nullptr,
           *bnb = nullptr;
 };
 
@@ -328,16 +329,28 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
             ep.out_f32 = Lw.P;
             ep.ldo = D;
             if (launch_gemm_simt(0, pe, D, wpos_d, D, m->NR, D, D, ep, 0) != cudaSuccess) return fail(CAC_E_CUDA);
-            // head-major copy with rows padded to HD + 4 floats: one bulk copy per
-            // (block, head) in the attention kernels, conflict-free rows in shared memory
-            std::vector<float> hp((size_t)m->NR * D), pad((size_t)H * m->NR * (HD + 4), 0.f);
+            // head-major copy [H][NR][HD] in the activation dtype: one bulk copy per
+            // (block, head) in the attention kernels
+            std::vector<float> hp((size_t)m->NR * D), pad((size_t)H * m->NR * HD, 0.f);
             if (cudaMemcpy(hp.data(), Lw.P, hp.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
                 return fail(CAC_E_CUDA);
             for (int hh = 0; hh < H; ++hh)
                 for (int rr = 0; rr < m->NR; ++rr)
-                    std::memcpy(&pad[((size_t)hh * m->NR + rr) * (HD + 4)], &hp[(size_t)rr * D + hh * HD],
+                    std::memcpy(&pad[((size_t)hh * m->NR + rr) * HD], &hp[(size_t)rr * D + hh * HD],
                                 sizeof(float) * HD);
-            if ((r = upload_f32(m, pad.data(), pad.size(), &Lw.Ppad)) != CAC_OK) return fail(r);
+            if (m->bf16) {
+                std::vector<uint16_t> hb(pad.size());
+                for (size_t k = 0; k < pad.size(); ++k) hb[k] = f2bf(pad[k]);
+                void* pp;
+                if ((r = dalloc(m, hb.size() * 2, &pp)) != CAC_OK) return fail(r);
+                if (cudaMemcpy(pp, hb.data(), hb.size() * 2, cudaMemcpyHostToDevice) != cudaSuccess)
+                    return fail(CAC_E_CUDA);
+                Lw.Ppad = pp;
+            } else {
+                float* pf;
+                if ((r = upload_f32(m, pad.data(), pad.size(), &pf)) != CAC_OK) return fail(r);
+                Lw.Ppad = pf;
+            }
         }
         if ((r = vec(&Lw.pbu, (size_t)H * HD)) || (r = vec(&Lw.pbv, (size_t)H * HD))) return fail(r);
         if ((r = vec(&Lw.conv_g, D)) || (r = vec(&Lw.conv_b, D)) || (r = lin(&Lw.pw1, 2 * D, D, &glu_perm)))

@@ -185,108 +185,121 @@ cudaError_t launch_stage_mel_offline(const float* mel, int t_mel, const int* len
 // masked (chunked-causal on absolute positions, or a window), softmax over j,
 // out_i = sum_j prob[i][j] v_j.
 //
-// A block serves SPB units of one head with WPS warps each (the queries of a
-// unit are dealt round-robin to its warps).  Per unit, one lane issues TMA
-// bulk copies of all K and V rows into shared memory on one mbarrier (the ring
-// span of a stream is at most two contiguous pieces); thread 0 bulk-copies the
-// head's padded position table on a block barrier.  Inside a warp, LPK =
-// HD / 8 lanes share a key: each lane holds 8 dims of (q + u) and (q + v) in
-// registers, reads the matching 8 dims of k_j and of P[rel] from shared
-// memory, and the partial dots are combined with log2(LPK) shuffles.  probs @ V
-// uses the same lane layout over the keys, then reduces across key groups.
+// A block serves SPB units of one head with WPS warps each (queries dealt
+// round-robin to the unit's warps, NQW per warp).  Staging: thread 0
+// bulk-copies the head's position table (activation dtype, [NR][HD]) on a
+// block mbarrier; per unit one lane bulk-copies the K rows (at most two
+// contiguous ring pieces) on the unit's mbarrier.  V is streamed from global
+// memory in the probs @ V phase, four rows in flight per lane.  Lane layout:
+// LPK = HD / EPC lanes share a key (EPC = elements per 16-byte chunk), each
+// holding EPC dims of (q + u) and (q + v) in registers; a quarter-warp reads
+// whole 128-byte rows of K and P (conflict-free), and the partial dot products
+// are combined with log2(LPK) shuffles.  The mask is a per-query window
+// [lo, hi] of absolute key positions computed once per query.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ bool allowed(const AttnParams& a, int pq, int pk) {
-    if (pk < 0) return false;
-    if (a.rc > 0) return pk >= pq - a.left && pk <= pq + a.rc;
-    const int c = (pq / a.chunk) * a.chunk;
-    return pk >= c - a.left && pk <= c + a.chunk - 1;
-}
-
 template <int HD, int NQW, int WPS, int SPB, int NK, class T>
 struct Attn {
     static constexpr int NQ = NQW * WPS;              // queries per unit
     static constexpr int THREADS = SPB * WPS * 32;
-    static constexpr int PS = HD + 4;                 // padded position-table row (floats)
-    static constexpr int LPK = HD / 8;                // lanes per key
+    static constexpr int EPC = 16 / (int)sizeof(T);   // elements per 16-byte chunk
+    static constexpr int LPK = HD / EPC;              // lanes per key
     static constexpr int KPS = 32 / LPK;              // keys per warp step
-    static constexpr int KV = NK * HD;                // elements of K (or V) per unit
-    static constexpr int UNIT_BYTES = 16 + 2 * KV * (int)sizeof(T) + 4 * NQ * NK;
-    static size_t smem(int NR) { return 16 + ((size_t)NR * PS * 4 + 15) / 16 * 16 + (size_t)SPB * UNIT_BYTES; }
+    static constexpr int UNIT_BYTES = 16 + NK * HD * (int)sizeof(T) + 4 * NQ * NK;
+    __host__ __device__ static size_t ptable_bytes(int NR) { return ((size_t)NR * HD * sizeof(T) + 15) / 16 * 16; }
+    static size_t smem(int NR) { return 16 + ptable_bytes(NR) + (size_t)SPB * UNIT_BYTES; }
 };
 
-// 4 consecutive elements -> float
-__device__ __forceinline__ void ld4f(const bf16* p, float* f) {
-    const uint2 u = *reinterpret_cast<const uint2*>(p);
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-}
-__device__ __forceinline__ void ld4f(const float* p, float* f) {
-    const float4 u = *reinterpret_cast<const float4*>(p);
-    f[0] = u.x; f[1] = u.y; f[2] = u.z; f[3] = u.w;
-}
-__device__ __forceinline__ void st4(bf16* p, const float* f) {
-    const __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]);
-    const __nv_bfloat162 b = __floats2bfloat162_rn(f[2], f[3]);
-    uint2 u;
-    u.x = *reinterpret_cast<const uint32_t*>(&a);
-    u.y = *reinterpret_cast<const uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(p) = u;
-}
-__device__ __forceinline__ void st4(float* p, const float* f) {
-    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
-}
-
-// The 8 dims of a row that lane c (of LPK) owns: [c*4, c*4+4) and [HD/2 + c*4, ..+4).
-// Rows of odd keys read the two halves in the other order so that the two keys
-// sharing a half-warp request hit different banks.
-template <int HD, class T>
-__device__ __forceinline__ void ld8(const T* row, int c, int odd, float* lo, float* hi) {
-    float a[4], b[4];
-    ld4f(row + (odd ? HD / 2 : 0) + c * 4, a);
-    ld4f(row + (odd ? 0 : HD / 2) + c * 4, b);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        lo[e] = odd ? b[e] : a[e];
-        hi[e] = odd ? a[e] : b[e];
+__device__ __forceinline__ void key_window(const AttnParams& a, int pq, int& lo, int& hi) {
+    if (a.rc > 0) {
+        lo = max(pq - a.left, 0);
+        hi = pq + a.rc;
+    } else {
+        const int c = (pq / a.chunk) * a.chunk;
+        lo = max(c - a.left, 0);
+        hi = c + a.chunk - 1;
     }
 }
 
-// One warp: its queries (i = wsub, wsub + WPS, ...) of one unit, after the
-// unit's K/V copies and the position table were issued.
+// 16 bytes -> EPC floats
+__device__ __forceinline__ void cvt16(const uint4& u, float (&f)[8]) {
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 t = __bfloat1622float2(p[k]);
+        f[2 * k] = t.x;
+        f[2 * k + 1] = t.y;
+    }
+}
+__device__ __forceinline__ void cvt16(const uint4& u, float (&f)[4]) {
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+}
+template <int EPC>
+__device__ __forceinline__ void st_chunk(bf16* p, const float (&f)[EPC]) {
+    static_assert(EPC == 8, "bf16 chunk");
+    uint4 u;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 t = __floats2bfloat162_rn(f[2 * k], f[2 * k + 1]);
+        w[k] = *reinterpret_cast<const uint32_t*>(&t);
+    }
+    *reinterpret_cast<uint4*>(p) = u;
+}
+template <int EPC>
+__device__ __forceinline__ void st_chunk(float* p, const float (&f)[EPC]) {
+    static_assert(EPC == 4, "fp32 chunk");
+    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+}
+
+// V rows of one unit: a ring of R slots starting at slot s0 (streaming), or
+// dense rows with stride ld (offline).
+template <class T>
+struct VRows {
+    const T* base;
+    int s0, R, ld;  // R > 0: ring; else dense with stride ld
+    __device__ __forceinline__ const T* row(int j) const {
+        if (R > 0) {
+            int s = s0 + j;
+            if (s >= R) s -= R;
+            return base + (long long)s * (ld);
+        }
+        return base + (long long)j * ld;
+    }
+};
+
+// One warp: queries i = wsub + WPS * t (t < NQW) of one unit, after the unit's
+// K copy and the block's position table were issued.
 template <int HD, int NQW, int WPS, int SPB, int NK, class T>
-__device__ void attend(const AttnParams& a, int h, const float* Ps, uint64_t* pbar, uint8_t* usm, int wsub, int lane,
-                       const float* qsrc, int pq0, int nq, int kpos0, int Nk, T* dst, int* status) {
+__device__ void attend(const AttnParams& a, int h, const T* Ps, uint64_t* pbar, uint8_t* usm, int wsub, int lane,
+                       const float* qsrc, int pq0, int nq, int kpos0, int Nk, VRows<T> vr, T* dst, int* status) {
     using A = Attn<HD, NQW, WPS, SPB, NK, T>;
-    constexpr int LPK = A::LPK, KPS = A::KPS, PS = A::PS;
+    constexpr int EPC = A::EPC, LPK = A::LPK, KPS = A::KPS;
     uint64_t* bar = reinterpret_cast<uint64_t*>(usm);
     const T* Ks = reinterpret_cast<const T*>(usm + 16);
-    const T* Vs = Ks + A::KV;
-    float* S = reinterpret_cast<float*>(const_cast<T*>(Vs + A::KV));
+    float* S = reinterpret_cast<float*>(usm + 16 + NK * HD * sizeof(T));
     const int c = lane % LPK, g = lane / LPK;
-    // this warp's queries, with both biases folded in, 8 dims per lane in registers
-    float qu[NQW][8], qv[NQW][8];
+    const int d0 = c * EPC;
+    float qu[NQW][EPC], qv[NQW][EPC];
+    int lo[NQW], hi[NQW], pqv[NQW];
 #pragma unroll
     for (int t = 0; t < NQW; ++t) {
         const int i = wsub + WPS * t;
-        if (i >= nq) break;
-        const float* qr = qsrc + (long long)i * a.ldq;
-        const float* ub = a.pbu + h * HD;
-        const float* vb = a.pbv + h * HD;
+        const bool has = i < nq;
+        const float* qr = qsrc + (long long)(has ? i : 0) * a.ldq + d0;
+        const float* ub = a.pbu + h * HD + d0;
+        const float* vb = a.pbv + h * HD + d0;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int d = half * (HD / 2) + c * 4;
-            const float4 q4 = *reinterpret_cast<const float4*>(qr + d);
-            const float4 u4 = __ldg(reinterpret_cast<const float4*>(ub + d));
-            const float4 v4 = __ldg(reinterpret_cast<const float4*>(vb + d));
-            const float qq[4] = {q4.x, q4.y, q4.z, q4.w}, uu[4] = {u4.x, u4.y, u4.z, u4.w},
-                        vv[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                qu[t][half * 4 + e] = qq[e] + uu[e];
-                qv[t][half * 4 + e] = qq[e] + vv[e];
-            }
+        for (int e = 0; e < EPC; e += 4) {
+            const float4 q4 = *reinterpret_cast<const float4*>(qr + e);
+            const float4 u4 = __ldg(reinterpret_cast<const float4*>(ub + e));
+            const float4 v4 = __ldg(reinterpret_cast<const float4*>(vb + e));
+            qu[t][e] = q4.x + u4.x; qu[t][e + 1] = q4.y + u4.y; qu[t][e + 2] = q4.z + u4.z; qu[t][e + 3] = q4.w + u4.w;
+            qv[t][e] = q4.x + v4.x; qv[t][e + 1] = q4.y + v4.y; qv[t][e + 2] = q4.z + v4.z; qv[t][e + 3] = q4.w + v4.w;
         }
+        pqv[t] = pq0 + i;
+        key_window(a, pqv[t], lo[t], hi[t]);
+        if (!has) { lo[t] = 1; hi[t] = 0; }   // empty window
     }
     const bool landed = mbar_wait(bar, 0) && mbar_wait(pbar, 0);
     __syncwarp();
@@ -294,36 +307,27 @@ __device__ void attend(const AttnParams& a, int h, const float* Ps, uint64_t* pb
         if (lane == 0) latch_error(status, CAC_E_TIMEOUT);
         return;
     }
-    // scores
+    // scores: a quarter-warp covers whole rows of K and P
     for (int j0 = 0; j0 < Nk; j0 += KPS) {
         const int j = j0 + g;
         const bool valid = j < Nk;
         const int pk = kpos0 + j;
-        float k8[8];
-        {
-            float lo[4], hi[4];
-            ld8<HD>(Ks + (valid ? j : 0) * HD, c, j & 1, lo, hi);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) { k8[e] = lo[e]; k8[4 + e] = hi[e]; }
-        }
+        float kf[EPC];
+        cvt16(*reinterpret_cast<const uint4*>(Ks + (valid ? j : 0) * HD + d0), kf);
 #pragma unroll
         for (int t = 0; t < NQW; ++t) {
-            const int i = wsub + WPS * t;
-            if (i >= nq) break;
-            const int pq = pq0 + i;
-            const bool ok = valid && allowed(a, pq, pk);
+            const bool ok = valid && pk >= lo[t] && pk <= hi[t];
             float part = 0.f;
             if (ok) {
-                float p8[8];
-                const float* pr = Ps + (pq - pk - a.rmin) * PS;
-                ld4f(pr + c * 4, p8);
-                ld4f(pr + HD / 2 + c * 4, p8 + 4);
+                float pf[EPC];
+                cvt16(*reinterpret_cast<const uint4*>(Ps + (pqv[t] - pk - a.rmin) * HD + d0), pf);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) part = fmaf(qu[t][e], k8[e], fmaf(qv[t][e], p8[e], part));
+                for (int e = 0; e < EPC; ++e) part = fmaf(qu[t][e], kf[e], fmaf(qv[t][e], pf[e], part));
             }
 #pragma unroll
             for (int o = 1; o < LPK; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            if (valid && c == 0) S[i * NK + j] = ok ? part * a.scale : -FLT_MAX;
+            const int i = wsub + WPS * t;
+            if (valid && c == 0 && i < nq) S[i * NK + j] = ok ? part * a.scale : -FLT_MAX;
         }
     }
     __syncwarp();
@@ -348,25 +352,34 @@ __device__ void attend(const AttnParams& a, int h, const float* Ps, uint64_t* pb
     }
     __syncwarp();
     pdl_trigger();
-    // probs @ V: key group g takes keys j = g, g + KPS, ...; each lane 8 dims
-    float acc[NQW][8];
+    // probs @ V: key group g takes keys g, g + KPS, ...; V rows streamed from
+    // global memory, U rows in flight per lane
+    constexpr int U = 4;
+    float acc[NQW][EPC];
 #pragma unroll
     for (int t = 0; t < NQW; ++t)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[t][e] = 0.f;
-#pragma unroll 2
-    for (int j = g; j < Nk; j += KPS) {
-        float lo[4], hi[4];
-        ld8<HD>(Vs + j * HD, c, j & 1, lo, hi);
+        for (int e = 0; e < EPC; ++e) acc[t][e] = 0.f;
+    for (int jb = g; jb < Nk; jb += U * KPS) {
+        uint4 raw[U];
 #pragma unroll
-        for (int t = 0; t < NQW; ++t) {
-            const int i = wsub + WPS * t;
-            if (i >= nq) break;
-            const float pij = S[i * NK + j];
+        for (int u = 0; u < U; ++u) {
+            const int j = jb + u * KPS;
+            raw[u] = j < Nk ? __ldg(reinterpret_cast<const uint4*>(vr.row(j) + d0)) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                acc[t][e] = fmaf(pij, lo[e], acc[t][e]);
-                acc[t][4 + e] = fmaf(pij, hi[e], acc[t][4 + e]);
+        for (int u = 0; u < U; ++u) {
+            const int j = jb + u * KPS;
+            if (j >= Nk) break;
+            float vf[EPC];
+            cvt16(raw[u], vf);
+#pragma unroll
+            for (int t = 0; t < NQW; ++t) {
+                const int i = wsub + WPS * t;
+                if (i >= nq) break;
+                const float pij = S[i * NK + j];
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) acc[t][e] = fmaf(pij, vf[e], acc[t][e]);
             }
         }
     }
@@ -375,27 +388,23 @@ __device__ void attend(const AttnParams& a, int h, const float* Ps, uint64_t* pb
         const int i = wsub + WPS * t;
         if (i >= nq) break;
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
+        for (int e = 0; e < EPC; ++e)
 #pragma unroll
             for (int o = LPK; o < 32; o <<= 1) acc[t][e] += __shfl_xor_sync(0xffffffffu, acc[t][e], o);
-        if (g == 0) {
-            T* o = dst + (long long)i * a.ldo;
-            st4(o + c * 4, acc[t]);
-            st4(o + HD / 2 + c * 4, acc[t] + 4);
-        }
+        if (g == 0) st_chunk<EPC>(dst + (long long)i * a.ldo + d0, acc[t]);
     }
 }
 
 // Block prologue: thread 0 arms the block barrier and bulk-copies this head's
-// padded position table [NR][HD + 4].
-template <int HD>
-__device__ __forceinline__ void stage_ptable(const AttnParams& a, int h, float* Ps, uint64_t* pbar) {
+// position table [NR][HD] (activation dtype).
+template <int HD, class T>
+__device__ __forceinline__ void stage_ptable(const AttnParams& a, int h, T* Ps, uint64_t* pbar) {
     if (threadIdx.x == 0) {
-        const uint32_t bytes = (uint32_t)a.NR * (HD + 4) * 4;
+        const uint32_t bytes = (uint32_t)a.NR * HD * sizeof(T);
         mbar_init(pbar, 1);
         fence_mbar_init();
         mbar_expect_tx(pbar, bytes);
-        bulk_g2s(Ps, a.P + (long long)h * a.NR * (HD + 4), bytes, pbar);
+        bulk_g2s(Ps, static_cast<const T*>(a.P) + (long long)h * a.NR * HD, bytes, pbar);
     }
 }
 
@@ -411,46 +420,43 @@ __global__ void __launch_bounds__(SPB * WPS * 32) attn_stream_kernel(AttnParams 
     const int b = blockIdx.x * SPB + slot;
     const bool live = b < a.nb;
     uint64_t* pbar = reinterpret_cast<uint64_t*>(sm);
-    float* Ps = reinterpret_cast<float*>(sm + 16);
-    uint8_t* usm = sm + 16 + ((a.NR * A::PS * 4 + 15) & ~15) + slot * A::UNIT_BYTES;
-    stage_ptable<HD>(a, h, Ps, pbar);  // weights: before waiting for the QKV projection
+    T* Ps = reinterpret_cast<T*>(sm + 16);
+    uint8_t* usm = sm + 16 + A::ptable_bytes(a.NR) + slot * A::UNIT_BYTES;
+    stage_ptable<HD, T>(a, h, Ps, pbar);  // weights: before waiting for the QKV projection
     pdl_wait();
-    int id = 0, p0 = 0, Lc = 0, Nk = 0;
+    int id = 0, p0 = 0, Lc = 0, Nk = 0, s0 = 0;
+    const T* kb = nullptr;
+    const T* vb = nullptr;
     if (live) {
         id = a.ids[b];
         p0 = a.pos[id];
         Lc = min(p0, a.left);
         Nk = min(Lc + a.nq, NK);
+        s0 = (p0 - Lc) % a.R;
+        const long long base = (long long)id * a.sstride + (long long)h * a.R * HD;
+        kb = static_cast<const T*>(a.k) + base;
+        vb = static_cast<const T*>(a.v) + base;
         if (wsub == 0 && lane == 0) {
             uint64_t* bar = reinterpret_cast<uint64_t*>(usm);
             T* Ks = reinterpret_cast<T*>(usm + 16);
-            T* Vs = Ks + A::KV;
             constexpr uint32_t ROW = HD * sizeof(T);
             mbar_init(bar, 1);
             fence_mbar_init();
-            mbar_expect_tx(bar, 2u * ROW * Nk);
-            const long long base = (long long)id * a.sstride + (long long)h * a.R * HD;
-            const T* kb = static_cast<const T*>(a.k) + base;
-            const T* vb = static_cast<const T*>(a.v) + base;
-            const int s0 = (p0 - Lc) % a.R;
+            mbar_expect_tx(bar, ROW * Nk);
             const int n1 = min(Nk, a.R - s0);
             bulk_g2s(Ks, kb + (long long)s0 * HD, ROW * n1, bar);
-            bulk_g2s(Vs, vb + (long long)s0 * HD, ROW * n1, bar);
-            if (Nk > n1) {
-                bulk_g2s(Ks + n1 * HD, kb, ROW * (Nk - n1), bar);
-                bulk_g2s(Vs + n1 * HD, vb, ROW * (Nk - n1), bar);
-            }
+            if (Nk > n1) bulk_g2s(Ks + n1 * HD, kb, ROW * (Nk - n1), bar);
         }
     }
     __syncthreads();
     if (!live) return;
     attend<HD, NQW, WPS, SPB, NK, T>(a, h, Ps, pbar, usm, wsub, lane, a.q + (long long)b * a.nq * a.ldq + h * HD, p0,
-                                     a.nq, p0 - Lc, Nk, static_cast<T*>(a.out) + (long long)b * a.nq * a.ldo + h * HD,
-                                     status);
+                                     a.nq, p0 - Lc, Nk, VRows<T>{vb, s0, a.R, HD},
+                                     static_cast<T*>(a.out) + (long long)b * a.nq * a.ldo + h * HD, status);
 }
 
 // offline: units = query groups (one mask chunk, or `qgroup` frames of a window
-// mask) of one sequence; keys from the dense K/V rows, one bulk copy per row.
+// mask) of one sequence; keys from the dense K rows, one bulk copy per row.
 template <int HD, int NQW, int WPS, int SPB, int NK, class T>
 __global__ void __launch_bounds__(SPB * WPS * 32) attn_offline_kernel(AttnParams a, int qgroup, int* status) {
     using A = Attn<HD, NQW, WPS, SPB, NK, T>;
@@ -463,12 +469,14 @@ __global__ void __launch_bounds__(SPB * WPS * 32) attn_offline_kernel(AttnParams
     const int pq0 = (blockIdx.x * SPB + slot) * qgroup;
     const bool live = pq0 < len;
     uint64_t* pbar = reinterpret_cast<uint64_t*>(sm);
-    float* Ps = reinterpret_cast<float*>(sm + 16);
-    uint8_t* usm = sm + 16 + ((a.NR * A::PS * 4 + 15) & ~15) + slot * A::UNIT_BYTES;
-    stage_ptable<HD>(a, h, Ps, pbar);
+    T* Ps = reinterpret_cast<T*>(sm + 16);
+    uint8_t* usm = sm + 16 + A::ptable_bytes(a.NR) + slot * A::UNIT_BYTES;
+    stage_ptable<HD, T>(a, h, Ps, pbar);
     pdl_wait();
     int nq = 0, klo = 0, Nk = 0;
     const long long rb = (long long)seq * a.T;
+    const T* kb = static_cast<const T*>(a.k) + rb * a.ldk + h * HD;
+    const T* vb = static_cast<const T*>(a.v) + rb * a.ldk + h * HD;
     if (live) {
         nq = min(qgroup, len - pq0);
         const int pql = pq0 + nq - 1;
@@ -484,26 +492,21 @@ __global__ void __launch_bounds__(SPB * WPS * 32) attn_offline_kernel(AttnParams
         if (wsub == 0) {
             uint64_t* bar = reinterpret_cast<uint64_t*>(usm);
             T* Ks = reinterpret_cast<T*>(usm + 16);
-            T* Vs = Ks + A::KV;
             constexpr uint32_t ROW = HD * sizeof(T);
             if (lane == 0) {
                 mbar_init(bar, 1);
                 fence_mbar_init();
-                mbar_expect_tx(bar, 2u * ROW * Nk);
+                mbar_expect_tx(bar, ROW * Nk);
             }
             __syncwarp();
-            const T* kb = static_cast<const T*>(a.k) + rb * a.ldk + h * HD;
-            const T* vb = static_cast<const T*>(a.v) + rb * a.ldk + h * HD;
-            for (int j = lane; j < Nk; j += 32) {
-                bulk_g2s(Ks + j * HD, kb + (long long)(klo + j) * a.ldk, ROW, bar);
-                bulk_g2s(Vs + j * HD, vb + (long long)(klo + j) * a.ldk, ROW, bar);
-            }
+            for (int j = lane; j < Nk; j += 32) bulk_g2s(Ks + j * HD, kb + (long long)(klo + j) * a.ldk, ROW, bar);
         }
     }
     __syncthreads();
     if (!live) return;
     attend<HD, NQW, WPS, SPB, NK, T>(a, h, Ps, pbar, usm, wsub, lane, a.q + (rb + pq0) * a.ldq + h * HD, pq0, nq, klo,
-                                     Nk, static_cast<T*>(a.out) + (rb + pq0) * a.ldo + h * HD, status);
+                                     Nk, VRows<T>{vb + (long long)klo * a.ldk, 0, 0, a.ldk},
+                                     static_cast<T*>(a.out) + (rb + pq0) * a.ldo + h * HD, status);
 }
 
 template <class K>
@@ -551,16 +554,16 @@ static cudaError_t attn_offline_launch(const AttnParams& a, int qgroup, int* sta
                             : LAUNCH<16, NQW, WPS, SPB, NK, float>(__VA_ARGS__);                         \
     } while (0)
 
-// Instantiations (queries per unit = NQW * WPS): 160 ms pushes (2 queries,
-// keys <= left + 2: 4 units x 2 warps per block), chunked pushes of up to 8
-// frames (keys <= left + 8: 2 units x 4 warps), provisional passes (up to 24
-// queries, keys <= left + 24: 1 unit x 8 warps); offline groups of <= 8.
+// Instantiations (queries per unit = NQW * WPS; 16 warps per block):
+// 160 ms pushes and offline chunks of 2 (2 queries, one warp, keys <= left + 2),
+// pushes of up to 8 frames and offline window groups of 8 (keys <= left + 8 / 96),
+// provisional passes (up to 24 queries, keys <= left + 24).
 cudaError_t launch_attention_stream(const AttnParams& a, int act_bf16, int* status, cudaStream_t s) {
     if (a.nb <= 0) return cudaSuccess;
     const int nk_need = a.left + a.nq;
-    if (a.nq <= 2 && nk_need <= 80) ATT_DISPATCH(attn_stream_launch, 1, 2, 4, 80, a, status, s);
-    if (a.nq <= 8 && nk_need <= 80) ATT_DISPATCH(attn_stream_launch, 2, 4, 2, 80, a, status, s);
-    if (a.nq <= 24 && nk_need <= 96) ATT_DISPATCH(attn_stream_launch, 3, 8, 1, 96, a, status, s);
+    if (a.nq <= 2 && nk_need <= 80) ATT_DISPATCH(attn_stream_launch, 2, 1, 16, 80, a, status, s);
+    if (a.nq <= 8 && nk_need <= 80) ATT_DISPATCH(attn_stream_launch, 2, 4, 4, 80, a, status, s);
+    if (a.nq <= 24 && nk_need <= 96) ATT_DISPATCH(attn_stream_launch, 3, 8, 2, 96, a, status, s);
     return cudaErrorInvalidValue;
 }
 
@@ -570,8 +573,8 @@ cudaError_t launch_attention_offline(const AttnParams& a, int act_bf16, int* sta
     const int qgroup = a.rc > 0 ? 8 : a.chunk;
     const int nk_need = a.rc > 0 ? a.left + qgroup + a.rc : a.left + a.chunk;
     if (qgroup > 8 || nk_need > 96) return cudaErrorInvalidValue;
-    if (qgroup <= 2 && nk_need <= 80) ATT_DISPATCH(attn_offline_launch, 1, 2, 4, 80, a, qgroup, status, s);
-    ATT_DISPATCH(attn_offline_launch, 2, 4, 2, 96, a, qgroup, status, s);
+    if (qgroup <= 2 && nk_need <= 80) ATT_DISPATCH(attn_offline_launch, 2, 1, 16, 80, a, qgroup, status, s);
+    ATT_DISPATCH(attn_offline_launch, 2, 4, 4, 96, a, qgroup, status, s);
     return cudaErrorInvalidValue;
 }
 

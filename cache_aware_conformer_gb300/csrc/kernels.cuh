@@ -36,7 +36,7 @@ struct AttnParams {
     const int* ids = nullptr;   // streaming: batch slot -> stream id
     const int* pos = nullptr;   // streaming: stream id -> position of the first query
     int nq = 0;                 // streaming: queries per stream
-    const float* P = nullptr;   // position table [H][NR][HD + 4] (rows padded) for rel = rmin .. rmin + NR - 1
+    const void* P = nullptr;    // position table [H][NR][HD], activation dtype, rel = rmin .. rmin + NR - 1
     int rmin = 0, NR = 0;
     const float* pbu = nullptr; // [H][HD]
     const float* pbv = nullptr;
