@@ -9,6 +9,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <new>
 #include <tuple>
 #include <vector>
@@ -1017,50 +1018,76 @@ extern "C" int cac_stream_flush(cac_pool* p, int n, const int* ids, const float*
 // ===========================================================================
 // offline chunked-causal encode
 // ===========================================================================
-extern "C" int cac_encode_offline(cac_model* m, int B, const float* mel, const int* mel_len, int t_mel_max, float* enc,
-                                  float* joint, int* out_len, void* stream) {
-    if (!m || B <= 0 || !mel || !mel_len || t_mel_max <= 0 || !enc || !out_len) return CAC_E_INVAL;
-    for (int b = 0; b < B; ++b)
-        if (mel_len[b] < 1 || mel_len[b] > t_mel_max) return CAC_E_INVAL;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int D = m->D, F = m->F, L = m->L;
+namespace {
+
+// Scratch layout of one offline encode of B windows of up to t_mel_max mel frames.
+struct OfflineLayout {
+    int T1, T2, T3, W1, W2, W3;
+    long long M;
+    size_t o_win1, o_win2, o_win3, o_y3, o_x, o_xln, o_h, o_q, o_k, o_v, o_o, o_glu, o_yc, o_mlen, o_flen;
+    size_t bytes;
+};
+
+OfflineLayout offline_layout(const cac_model* m, int B, int t_mel_max) {
+    OfflineLayout y;
+    const int D = m->D, F = m->F;
     const size_t ab = act_bytes(m);
-    const int bf = m->bf16;
     auto half = [](int t) { return (t + 1) / 2; };
-    const int T1 = half(t_mel_max), T2 = half(T1), T3 = half(T2);
-    const int W1 = 2 + t_mel_max + (t_mel_max & 1), W2 = 2 + T1 + (T1 & 1), W3 = 2 + T2 + (T2 & 1);
-    const long long M = (long long)B * T3;
+    y.T1 = half(t_mel_max);
+    y.T2 = half(y.T1);
+    y.T3 = half(y.T2);
+    y.W1 = 2 + t_mel_max + (t_mel_max & 1);
+    y.W2 = 2 + y.T1 + (y.T1 & 1);
+    y.W3 = 2 + y.T2 + (y.T2 & 1);
+    y.M = (long long)B * y.T3;
+    const long long M = y.M;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;
         off += (bytes + 255) & ~size_t(255);
         return o;
     };
-    const size_t o_win1 = take(ab * ((size_t)B * W1 + 4) * MEL);
-    const size_t o_win2 = take(ab * ((size_t)B * W2 + 4) * D);
-    const size_t o_win3 = take(ab * ((size_t)B * W3 + 4) * D);
-    const size_t o_y3 = take(ab * M * D);
-    const size_t o_x = take(4 * M * D);
-    const size_t o_xln = take(ab * M * D);
-    const size_t o_h = take(ab * M * F);
-    const size_t o_q = take(4 * M * D);
-    const size_t o_k = take(ab * M * D);
-    const size_t o_v = take(ab * M * D);
-    const size_t o_o = take(ab * M * D);
-    const size_t o_glu = take(ab * M * D);
-    const size_t o_yc = take(ab * M * D);
-    const size_t o_mlen = take(sizeof(int) * B);
-    const size_t o_flen = take(sizeof(int) * B);
-    if (off > m->ws.bytes) {
-        CK(cudaStreamSynchronize(s));
-        if (m->ws.base) cudaFree(m->ws.base);
-        m->ws.base = nullptr;
-        m->ws.bytes = 0;
-        if (cudaMalloc(&m->ws.base, off) != cudaSuccess) return CAC_E_NOMEM;
-        CK(cudaMemset(m->ws.base, 0, off));
-        m->ws.bytes = off;
-    }
-    char* w = static_cast<char*>(m->ws.base);
+    y.o_win1 = take(ab * ((size_t)B * y.W1 + 4) * MEL);
+    y.o_win2 = take(ab * ((size_t)B * y.W2 + 4) * D);
+    y.o_win3 = take(ab * ((size_t)B * y.W3 + 4) * D);
+    y.o_y3 = take(ab * M * D);
+    y.o_x = take(4 * M * D);
+    y.o_xln = take(ab * M * D);
+    y.o_h = take(ab * M * F);
+    y.o_q = take(4 * M * D);
+    y.o_k = take(ab * M * D);
+    y.o_v = take(ab * M * D);
+    y.o_o = take(ab * M * D);
+    y.o_glu = take(ab * M * D);
+    y.o_yc = take(ab * M * D);
+    y.o_mlen = take(sizeof(int) * B);
+    y.o_flen = take(sizeof(int) * B);
+    y.bytes = off;
+    return y;
+}
+
+int offline_check_args(cac_model* m, int B, const float* mel, const int* mel_len, int t_mel_max, float* enc,
+                       int* out_len) {
+    if (!m || B <= 0 || !mel || !mel_len || t_mel_max <= 0 || !enc || !out_len) return CAC_E_INVAL;
+    for (int b = 0; b < B; ++b)
+        if (mel_len[b] < 1 || mel_len[b] > t_mel_max) return CAC_E_INVAL;
+    return CAC_OK;
+}
+
+// The offline encode on the scratch at `w` (laid out by `lay`); every scratch
+// byte that is read is written first in this call, except the zero padding
+// rows of the stage-2/3 windows, which are cleared here.
+int offline_run(cac_model* m, char* w, const OfflineLayout& lay, int B, const float* mel, const int* mel_len,
+                int t_mel_max, float* enc, float* joint, int* out_len, cudaStream_t s) {
+    const int D = m->D, F = m->F, L = m->L;
+    const size_t ab = act_bytes(m);
+    const int bf = m->bf16;
+    auto half = [](int t) { return (t + 1) / 2; };
+    const int T1 = lay.T1, T2 = lay.T2, T3 = lay.T3, W1 = lay.W1, W2 = lay.W2, W3 = lay.W3;
+    const long long M = lay.M;
+    const size_t o_win1 = lay.o_win1, o_win2 = lay.o_win2, o_win3 = lay.o_win3, o_y3 = lay.o_y3, o_x = lay.o_x,
+                 o_xln = lay.o_xln, o_h = lay.o_h, o_q = lay.o_q, o_k = lay.o_k, o_v = lay.o_v, o_o = lay.o_o,
+                 o_glu = lay.o_glu, o_yc = lay.o_yc, o_mlen = lay.o_mlen, o_flen = lay.o_flen;
     void *win1 = w + o_win1, *win2 = w + o_win2, *win3 = w + o_win3, *y3 = w + o_y3, *xln = w + o_xln, *h = w + o_h,
          *kd = w + o_k, *vd = w + o_v, *o = w + o_o, *glu = w + o_glu, *yc = w + o_yc;
     float* x = reinterpret_cast<float*>(w + o_x);
@@ -1151,6 +1178,66 @@ extern "C" int cac_encode_offline(cac_model* m, int B, const float* mel, const i
     }
     m->launches += lc;
     return CAC_OK;
+}
+
+}  // namespace
+
+extern "C" int cac_encode_offline(cac_model* m, int B, const float* mel, const int* mel_len, int t_mel_max, float* enc,
+                                  float* joint, int* out_len, void* stream) {
+    RET(offline_check_args(m, B, mel, mel_len, t_mel_max, enc, out_len));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const OfflineLayout lay = offline_layout(m, B, t_mel_max);
+    if (lay.bytes > m->ws.bytes) {
+        CK(cudaStreamSynchronize(s));
+        if (m->ws.base) cudaFree(m->ws.base);
+        m->ws.base = nullptr;
+        m->ws.bytes = 0;
+        if (cudaMalloc(&m->ws.base, lay.bytes) != cudaSuccess) return CAC_E_NOMEM;
+        CK(cudaMemset(m->ws.base, 0, lay.bytes));
+        m->ws.bytes = lay.bytes;
+    }
+    return offline_run(m, static_cast<char*>(m->ws.base), lay, B, mel, mel_len, t_mel_max, enc, joint, out_len, s);
+}
+
+// ===========================================================================
+// offline encode that allocates nothing
+// ===========================================================================
+namespace {
+// Fixed scratch of cac_encode_offline_noalloc: CAC_NOALLOC_SCRATCH_BYTES in
+// every device's memory from module load until process exit, shared by all
+// calls on that device.  Host code must not use the symbol itself as a device
+// address: it is resolved once per device with cudaGetSymbolAddress.
+__device__ __align__(256) unsigned char g_noalloc_scratch[CAC_NOALLOC_SCRATCH_BYTES];
+constexpr int kMaxDevices = 64;
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+}  // namespace
+
+extern "C" int cac_encode_offline_noalloc(cac_model* m, int B, const float* mel, const int* mel_len, int t_mel_max,
+                                          float* enc, float* joint, int* out_len, void* stream) {
+    RET(offline_check_args(m, B, mel, mel_len, t_mel_max, enc, out_len));
+    const OfflineLayout lay = offline_layout(m, B, t_mel_max);
+    if (lay.bytes > (size_t)CAC_NOALLOC_SCRATCH_BYTES) return CAC_E_LIMIT;
+    int dev = -1;
+    CK(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices) return CAC_E_UNSUPPORTED;
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_ptr[dev]) {
+            // first call on this device (current device): resolve the array's device address
+            void* ptr = nullptr;
+            const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+            if (e != cudaSuccess || !ptr) {
+                std::fprintf(stderr, "cac: cudaGetSymbolAddress(scratch) failed: %s\n", cudaGetErrorString(e));
+                return CAC_E_CUDA;
+            }
+            g_noalloc_ptr[dev] = ptr;
+        }
+        scratch = g_noalloc_ptr[dev];
+    }
+    return offline_run(m, static_cast<char*>(scratch), lay, B, mel, mel_len, t_mel_max, enc, joint, out_len,
+                       static_cast<cudaStream_t>(stream));
 }
 
 // ===========================================================================
@@ -1394,6 +1481,7 @@ extern "C" const char* cac_strerror(int code) {
         case CAC_E_NONFINITE: return "non-finite value in input mel";
         case CAC_E_TIMEOUT: return "bounded device wait gave up";
         case CAC_E_UNSUPPORTED: return "configuration not supported by these kernels";
+        case CAC_E_LIMIT: return "request needs more scratch than the fixed CAC_NOALLOC_SCRATCH_BYTES array";
     }
     return "unknown error";
 }

@@ -19,7 +19,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcac.so")
 
 CAC_OK = 0
 ERRORS = {-1: "CAC_E_INVAL", -2: "CAC_E_ALIGN", -3: "CAC_E_STATE", -4: "CAC_E_NOMEM", -5: "CAC_E_CUDA",
-          -6: "CAC_E_DEVICE", -7: "CAC_E_NONFINITE", -8: "CAC_E_TIMEOUT", -9: "CAC_E_UNSUPPORTED"}
+          -6: "CAC_E_DEVICE", -7: "CAC_E_NONFINITE", -8: "CAC_E_TIMEOUT", -9: "CAC_E_UNSUPPORTED",
+          -10: "CAC_E_LIMIT"}
 
 # every symbol include/cac.h declares
 SYMBOLS = ["cac_weights_size", "cac_model_create", "cac_model_destroy", "cac_pool_create", "cac_pool_destroy",
@@ -28,7 +29,7 @@ SYMBOLS = ["cac_weights_size", "cac_model_create", "cac_model_destroy", "cac_poo
            "cac_stream_set_state", "cac_pool_check", "cac_model_check", "cac_pool_set_graphs",
            "cac_pool_launch_count", "cac_pool_set_trace", "cac_pool_read_trace", "cac_pool_set_profile",
            "cac_pool_read_profile", "cac_profile_classes", "cac_profile_class_name", "cac_strerror",
-           "cac_op_gemm_bf16"]
+           "cac_op_gemm_bf16", "cac_encode_offline_noalloc"]
 
 
 class CacError(RuntimeError):
@@ -73,6 +74,7 @@ def _lib():
             "cac_stream_flush": (c_int, [vp, c_int, ip, vp, c_int, ip, vp, vp, c_int, ip, vp]),
             "cac_stream_flush_frames": (c_int, [vp, c_int, c_int, ip]),
             "cac_encode_offline": (c_int, [vp, c_int, vp, ip, c_int, vp, vp, ip, vp]),
+            "cac_encode_offline_noalloc": (c_int, [vp, c_int, vp, ip, c_int, vp, vp, ip, vp]),
             "cac_stream_get_state": (c_int, [vp, c_int, POINTER(CacStreamState)]),
             "cac_stream_set_state": (c_int, [vp, c_int, POINTER(CacStreamState)]),
             "cac_pool_check": (c_int, [vp]),
@@ -167,18 +169,26 @@ class Model:
     def check(self):
         _check(_lib().cac_model_check(self.h), "device status")
 
-    def encode_offline(self, mel, mel_len, joint: bool = True, stream=None):
-        """mel: cuda float32 [B, T_mel, 128]; returns (enc [B,T,D], joint [B,T,J] or None, out_len list)."""
+    def encode_offline(self, mel, mel_len, joint: bool = True, stream=None, out=None, noalloc: bool = False):
+        """mel: cuda float32 [B, T_mel, 128]; returns (enc [B,T,D], joint [B,T,J] or None, out_len list).
+
+        out: optional preallocated (enc, joint) tensors.  noalloc: use
+        cac_encode_offline_noalloc (the library's fixed scratch, no device
+        allocation inside the call)."""
         import torch
         B, t_mel, _ = mel.shape
         T = t_mel
         for _ in range(3):
             T = (T + 1) // 2
-        enc = torch.empty(B, T, self.cfg.d_model, device=mel.device, dtype=torch.float32)
-        jt = torch.empty(B, T, self.cfg.joint_dim, device=mel.device, dtype=torch.float32) if joint else None
+        if out is not None:
+            enc, jt = out
+        else:
+            enc = torch.empty(B, T, self.cfg.d_model, device=mel.device, dtype=torch.float32)
+            jt = torch.empty(B, T, self.cfg.joint_dim, device=mel.device, dtype=torch.float32) if joint else None
         out_len = (c_int * B)()
-        _check(_lib().cac_encode_offline(self.h, B, _ptr(mel.contiguous()), _ids(mel_len), t_mel, _ptr(enc),
-                                         _ptr(jt), out_len, _stream(stream)), "cac_encode_offline")
+        fn = _lib().cac_encode_offline_noalloc if noalloc else _lib().cac_encode_offline
+        _check(fn(self.h, B, _ptr(mel.contiguous()), _ids(mel_len), t_mel, _ptr(enc), _ptr(jt), out_len,
+                  _stream(stream)), "cac_encode_offline_noalloc" if noalloc else "cac_encode_offline")
         return enc, jt, list(out_len)
 
 

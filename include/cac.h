@@ -57,6 +57,7 @@ extern "C" {
 #define CAC_E_NONFINITE -7  /* non-finite value found in an input mel chunk */
 #define CAC_E_TIMEOUT  -8   /* a bounded device-side wait gave up */
 #define CAC_E_UNSUPPORTED -9 /* configuration outside what the kernels implement */
+#define CAC_E_LIMIT    -10  /* request larger than the fixed scratch of cac_encode_offline_noalloc */
 
 #define CAC_DTYPE_F32  0    /* everything fp32 (SIMT GEMMs) */
 #define CAC_DTYPE_BF16 1    /* bf16 weights, GEMM operands and caches; fp32 accumulation,
@@ -172,6 +173,31 @@ int  cac_stream_flush_frames(cac_pool* p, int id, int n_mel, int* frames);
  * grows on demand (the growth synchronizes `stream`). */
 int  cac_encode_offline(cac_model* m, int B, const float* mel, const int* mel_len, int t_mel_max,
                         float* enc, float* joint, int* out_len, void* stream);
+
+/* cac_encode_offline without allocation.  No counterpart on the pages: this
+ * entry point exists for callers that must not allocate device memory while
+ * they run — for example code inside CUDA stream capture, a real-time audio
+ * callback that cannot block on the allocator, or a process whose device
+ * memory is budgeted up front.  cac_encode_offline grows a model-owned
+ * workspace with cudaMalloc when a larger batch arrives; this variant instead
+ * runs the same kernels on a fixed array of CAC_NOALLOC_SCRATCH_BYTES (32 MiB)
+ * that the library declares in device memory: every GPU that loads the
+ * library holds it until the process exits.
+ *   - Arguments, layouts and results are those of cac_encode_offline.
+ *   - Requests whose scratch exceeds the array (roughly B x t_mel_max beyond
+ *     ~11,000 mel frames for the 17-layer d_model-512 model, less for wider
+ *     models) return CAC_E_LIMIT and do nothing.
+ *   - It calls no cudaMalloc / cudaFree and no allocating library routine.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array and leave their contents in
+ *     it; calls whose GPU work overlaps (different streams, or different
+ *     models, without ordering between them) race on it and must be
+ *     serialized by the caller. */
+#define CAC_NOALLOC_SCRATCH_BYTES (32u << 20)
+int  cac_encode_offline_noalloc(cac_model* m, int B, const float* mel, const int* mel_len, int t_mel_max,
+                                float* enc, float* joint, int* out_len, void* stream);
 
 /* Logical state of one stream, for snapshots and migration ("Parakeet-EOU-120M",
  * §Architecture: state tensors passed in and returned each step).  All
