@@ -37,7 +37,6 @@ from cache_aware_conformer_gb300.config import WORKLOADS, FRAME_SEC  # noqa: E40
 
 METRIC = "streamed audio-sec/sec (B streams, 160 ms chunks) + % of tensor/HBM roofline"
 UNIT = "audio-s/s"
-CHUNKS_60S = 375          # 60 s = 375 pushes of 16 mel frames
 
 
 # ---------------------------------------------------------------------------
@@ -199,12 +198,15 @@ def cpu_cores() -> int:
 # roofline bookkeeping: algorithmic work per launch of each kernel class
 # ---------------------------------------------------------------------------
 def algorithmic_work(cfg, S, n, mean_lc):
-    """Per launch: ('tensor', flops) for GEMMs, ('hbm', bytes) for the rest."""
+    """Per launch: ('tensor', flops) for GEMMs, ('hbm', bytes) for the rest.
+    n = frames pushed per stream; the layer stack runs over n rows per stream
+    (emit + lookahead rows per pass in the provisional-tail variant)."""
     D, F, J, L, H = cfg.d_model, cfg.ff_dim, cfg.joint_dim, cfg.n_layers, cfg.n_heads
-    M = S * n
+    rows = cfg.emit_frames + cfg.lookahead_frames if cfg.provisional else n
+    M = S * rows
     W1, W2, W3 = 14 + 8 * n, 4 * n + 6, 2 * n + 2
     sub_flops = 2 * D * (S * (W1 // 2) * 3 * 128 + S * (W2 // 2) * 3 * D + S * (W3 // 2) * 3 * D) / 3.0
-    kv = S * (mean_lc + n) * D * 2 * 2                  # K and V rows read, bf16
+    kv = S * (mean_lc + rows) * D * 2 * 2               # K and V rows read, bf16
     nr = cfg.att_left + cfg.att_chunk                   # position-table rows
     return {
         "gemm_ff_up": ("tensor", 2.0 * M * F * D),
@@ -237,6 +239,9 @@ def load_peaks():
 # the streaming workload
 # ---------------------------------------------------------------------------
 class StreamWorkload:
+    """S synthetic streams of `seconds` of audio pushed `push_mel` mel frames at a
+    time; start offsets reached by an untimed pre-roll; per-step resets."""
+
     def __init__(self, wl, rank: int, device, steps_needed: int, workers: int):
         import torch
         from cache_aware_conformer_gb300 import native
@@ -245,17 +250,18 @@ class StreamWorkload:
         self.dev = device
         self.push_mel = wl.push_mel
         self.n = wl.push_mel // 8
+        self.chunks = int(round(wl.seconds * 100)) // self.push_mel        # pushes per utterance
         base = rank * self.S
         self.offsets = synth.start_offsets(self.S, wl.max_start_offset, seed=7 + rank)
-        self.pre = (self.offsets // self.n).astype(np.int64)      # pre-roll pushes per stream
+        self.pre = (self.offsets // self.n).astype(np.int64)                # pre-roll pushes per stream
         W = synth.make_weights_parallel(self.cfg, seed=0, workers=workers)
         self.blob = synth.pack_weights(self.cfg, W)
         del W
-        mel = synth.make_mels_parallel(CHUNKS_60S * 16, range(base, base + self.S), wl.silence_frac, workers)
-        self.mel = torch.from_numpy(mel).to(device).view(self.S, CHUNKS_60S, 16, 128)
+        mel = synth.make_mels_parallel(self.chunks * self.push_mel, range(base, base + self.S), wl.silence_frac, workers)
+        self.mel = torch.from_numpy(mel).to(device).view(self.S, self.chunks, self.push_mel, 128)
         del mel
         self.model = native.Model(self.cfg, self.blob)
-        self.pool = native.Pool(self.model, self.S, max_frames_per_step=max(2, self.n))
+        self.pool = native.Pool(self.model, self.S, max_frames_per_step=max(2, min(8, self.n)))
         self.ids = [self.pool.create_stream() for _ in range(self.S)]
         # pre-roll: stream s pushes its first pre[s] chunks (untimed, eager)
         for r in range(int(self.pre.max()) if self.S else 0):
@@ -263,23 +269,24 @@ class StreamWorkload:
             chunk = self.mel[torch.from_numpy(sel).to(device), r].contiguous()
             self.pool.push([self.ids[i] for i in sel], chunk, joint=False)
         self.pool.check()
-        # per-step inputs: chunk index of every stream, arranged contiguously per step
+        # per-step inputs: chunk index of every stream, arranged contiguously per step;
+        # an utterance that ends restarts (reset) at its first chunk
         self.t = 0
         self.steps = steps_needed
-        cidx = (self.pre[None, :] + np.arange(steps_needed)[:, None]) % CHUNKS_60S       # [steps, S]
+        cidx = (self.pre[None, :] + np.arange(steps_needed)[:, None]) % self.chunks      # [steps, S]
         ar = torch.arange(self.S, device=device)
         self.step_mel = torch.stack([self.mel[ar, torch.from_numpy(c).to(device)] for c in cidx])
         self.cidx = cidx
         self.resets = [np.nonzero(synth.reset_mask(self.S, t, wl.reset_prob, seed=11 + rank) | (cidx[t] == 0))[0]
                        for t in range(steps_needed)]
-        self.staging = torch.empty(self.S, 16, 128, device=device)
+        self.staging = torch.empty(self.S, self.push_mel, 128, device=device)
         self.enc = torch.empty(self.S, self.n, self.cfg.d_model, device=device)
         self.joint = torch.empty(self.S, self.n, self.cfg.joint_dim, device=device)
         self.lc_hist = []
         self.subT = self.pre * self.n
 
     def step(self):
-        """One timed step: resets drawn for this step, then one 160 ms push of all streams."""
+        """One timed step: resets drawn for this step, then one push of all streams."""
         t = self.t
         r = self.resets[t]
         if len(r):
@@ -301,6 +308,90 @@ class StreamWorkload:
         self.subT += self.n
         self.t += 1
         return enc, joint
+
+
+class OfflineWorkload:
+    """B windows of offline_mel mel frames encoded in one cac_encode_offline call per step."""
+
+    def __init__(self, wl, rank: int, device, workers: int):
+        import torch
+        from cache_aware_conformer_gb300 import native
+        self.wl, self.cfg = wl, wl.model
+        self.B, self.T = wl.offline_batch, wl.offline_mel
+        W = synth.make_weights_parallel(self.cfg, seed=0, workers=workers)
+        self.blob = synth.pack_weights(self.cfg, W)
+        del W
+        base = rank * self.B
+        mel = synth.make_mels_parallel(self.T, range(base, base + self.B), wl.silence_frac, workers)
+        self.mel = torch.from_numpy(mel).to(device)
+        self.lens = [self.T] * self.B
+        self.model = native.Model(self.cfg, self.blob)
+        T3 = self.T
+        for _ in range(3):
+            T3 = (T3 + 1) // 2
+        self.T3 = T3
+        self.enc = torch.empty(self.B, T3, self.cfg.d_model, device=device)
+        self.joint = torch.empty(self.B, T3, self.cfg.joint_dim, device=device)
+
+    def step(self):
+        self.model.encode_offline(self.mel, self.lens, out=(self.enc, self.joint))
+
+
+def run_offline(args, wl):
+    import torch
+    rank, local, world = dist_init("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    K, Wm = args.steps, args.warmup
+    w = OfflineWorkload(wl, rank, dev, max(1, min(cpu_cores(), 16)))
+    for _ in range(Wm):
+        w.step()
+    torch.cuda.synchronize()
+    barrier()
+    vis = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip().isdigit()]
+    clocks = ClockSampler(int(vis[local]) if local < len(vis) else local)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed")
+    e0.record()
+    for _ in range(K):
+        w.step()
+    e1.record()
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    w.model.check()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    audio = world * w.B * w.T * 0.01 * K
+    value = audio / (ms / 1e3)
+    # e2e: host mel in, host frames out, through the same entry point
+    mel_h = w.mel.cpu().pin_memory()
+    t0 = time.perf_counter()
+    for _ in range(max(1, K // 4)):
+        m = mel_h.to(dev, non_blocking=True)
+        w.model.encode_offline(m, w.lens, out=(w.enc, w.joint))
+        enc_h, joint_h = w.enc.cpu(), w.joint.cpu()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
+    e2e = {"value": world * w.B * w.T * 0.01 * max(1, K // 4) / e2e_s, "unit": UNIT,
+           "h2d_bytes_per_step": w.B * w.T * 128 * 4, "d2h_bytes_per_step": w.B * w.T3 * (w.cfg.d_model + w.cfg.joint_dim) * 4}
+    # tensor roofline of the whole encode (GEMM FLOPs per window)
+    _, tf_peak, peak_src = load_peaks()
+    D, F, J, L = w.cfg.d_model, w.cfg.ff_dim, w.cfg.joint_dim, w.cfg.n_layers
+    flops = 2.0 * w.B * w.T3 * (L * (2 * 2 * D * F + 3 * D * D + D * D + 2 * D * D + D * D) + J * D)
+    ach = flops / (ms / K * 1e-3) / 1e12
+    roofline = {"kernel": "whole offline encode (GEMM FLOPs only)", "bound": "tensor", "achieved": ach,
+                "peak": tf_peak, "unit": "TFLOP/s", "frac": ach / tf_peak, "traffic": None,
+                "peak_source": f"{peak_src} (bf16 sustained)"}
+    if rank == 0:
+        print(json.dumps({"metric": "offline encode audio-sec/sec (" + wl.name + ")", "value": value, "unit": UNIT,
+                          "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": ms / K, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                          "config": {"workload": wl.name, "windows": w.B, "mel_frames": w.T, "frames": w.T3,
+                                     "layers": L, "d_model": D, "parallelism": f"replicas x{world}"},
+                          "roofline": roofline, "cpu_baseline": None, "e2e": e2e, "gpu_launches": None,
+                          "clocks": clk}), flush=True)
 
 
 def run_ours(args, wl):
@@ -391,10 +482,11 @@ def run_ours(args, wl):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w.cfg, w.blob, args.cpu_chunks)
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": Wm,
+        line = {"metric": METRIC if wl.name == "eou120m_256streams_60s" else f"streamed audio-sec/sec ({wl.name})",
+                "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": Wm,
                 "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": wl.name, "streams_per_gpu": w.S, "chunk_ms": 160,
+                "config": {"workload": wl.name, "streams_per_gpu": w.S, "chunk_ms": 10 * w.push_mel,
                            "layers": w.cfg.n_layers, "d_model": w.cfg.d_model, "heads": w.cfg.n_heads,
                            "ff": w.cfg.ff_dim, "att_left": w.cfg.att_left, "att_chunk": w.cfg.att_chunk,
                            "reset_prob": wl.reset_prob, "start_offsets": f"even, 0..{wl.max_start_offset - 1}",
@@ -468,6 +560,8 @@ def main(argv=None):
     wl = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, wl)
+    elif wl.offline_batch:
+        run_offline(args, wl)
     else:
         run_ours(args, wl)
 

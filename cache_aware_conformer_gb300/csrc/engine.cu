@@ -465,6 +465,13 @@ struct cac_pool {
     long long launches = 0;
     long long ring_sstride = 0, conv_sstride = 0;
     size_t tail_elems = 0;
+    // provisional tail (right_context > 0): frames subsampled vs emitted
+    int* sub_pos = nullptr;     // [S] frames subsampled so far (pos = frames emitted)
+    float* x0 = nullptr;        // [S][XC][D] exact subsampled frames not yet emitted
+    int XC = 0;
+    int* pids_dev = nullptr;    // stream ids of the current pass
+    int* pmap_dev = nullptr;    // pass slot -> batch slot of the call
+    std::vector<int> sub_host;
     // per-kernel-class CUDA-event timing (eager launches only)
     bool prof = false;
     std::vector<cudaEvent_t> ev;          // event pool, reused after each read
@@ -548,22 +555,21 @@ int prof_end(cac_pool* p, cudaStream_t s) {
 #define PB(cls) RET(prof_begin(p, cls, s))
 #define PE() RET(prof_end(p, s))
 
-// One step: nb batch slots (ids already in p->ids_dev), n new frames each.
+// Subsampling of n new frames for nb slots (ids[b]; the first new frame of
+// stream id sits at posS[id]) into p->x rows [b * n + i].
 //   mel: stream b's first mel row at mel + b * mel_bstride (8n rows; with
 //        nvalid, rows >= nvalid[b] read as zero)
-//   enc/joint: frame i of slot b goes to row b * out_bstride + out_off + i
-int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride, const int* nvalid, float* enc,
-             float* joint, int out_bstride, int out_off, cudaStream_t s) {
+int run_subsample(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride, const int* nvalid,
+                  const int* ids, const int* posS, cudaStream_t s) {
     cac_model* m = p->m;
-    const int D = m->D, F = m->F, L = m->L;
+    const int D = m->D;
     const int M = nb * n;
     long long* lc = &p->launches;
-    const size_t ab = act_bytes(m);
     const int bf = m->bf16;
 
     // 1. mel staging: [melTail | mel] windows, tail update
     PB(P_STAGE);
-    CK(launch_stage_mel(mel, mel_bstride, nvalid, p->win1, p->tail, p->ids_dev, p->pos, n, nb, bf, p->status, s));
+    CK(launch_stage_mel(mel, mel_bstride, nvalid, p->win1, p->tail, ids, posS, n, nb, bf, p->status, s));
     PE();
     ++*lc;
     // 2. three stride-2 convolutions (implicit GEMMs over the windows) + out linear
@@ -574,8 +580,8 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
         ep.bias = m->sub1.b;
         ep.out_act = p->win2;
         ep.ldo = D;
-        ep.ids = p->ids_dev;
-        ep.pos = p->pos;
+        ep.ids = ids;
+        ep.pos = posS;
         ep.P = W1 / 2; ep.T_out = W2; ep.dst_rows = W2; ep.dst_off = 0; ep.tmult = 4; ep.toff = 6;
         PB(P_SUB);
         RET(gemm(m, p->win1, 2 * MEL, nb * (W1 / 2), 3 * MEL, m->sub1, MEL, ep, s, lc));
@@ -604,6 +610,22 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
         PE();
     }
     RET(trace_tap(p, 0, N_TAPS, p->x, false, M, s));
+    return CAC_OK;
+}
+
+// The layer stack over nq rows per slot (p->x rows [b * nq + i], queries at
+// absolute positions pos[ids[b]] + i).  K/V rows of all nq frames go to the
+// rings; the conv cache commits the first n_commit GLU rows.  The last
+// ln_out writes enc (row remap b * out_bstride + out_off + i) or, when enc is
+// null, p->x in place; its activation-dtype copy always lands in p->xln.
+int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float* enc, int out_bstride, int out_off,
+               cudaStream_t s) {
+    cac_model* m = p->m;
+    const int D = m->D, F = m->F, L = m->L;
+    const int M = nb * nq, n = nq;
+    long long* lc = &p->launches;
+    const size_t ab = act_bytes(m);
+    const int bf = m->bf16;
     PB(P_LN);
     CK(launch_layernorm(p->x, M, D, m->layers[0].ff1_g, m->layers[0].ff1_b, nullptr, p->xln, nullptr, nullptr,
                         nullptr, bf, 1 << 30, 0, 0, s));
@@ -633,7 +655,7 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
         ep.ring_sstride = p->ring_sstride;
         ep.kring = static_cast<char*>(p->kring) + (long long)l * m->H * p->R * m->HD * ab;
         ep.vring = static_cast<char*>(p->vring) + (long long)l * m->H * p->R * m->HD * ab;
-        ep.q = p->q; ep.ldq = D; ep.ids = p->ids_dev; ep.pos = p->pos; ep.nq = n;
+        ep.q = p->q; ep.ldq = D; ep.ids = ids; ep.pos = p->pos; ep.nq = n;
         PB(P_QKV);
         RET(gemm(m, p->xln, D, M, D, Lw.qkv, 0, ep, s, lc));
         PE();
@@ -641,11 +663,11 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
             AttnParams a;
             a.q = p->q; a.ldq = D;
             a.k = ep.kring; a.v = ep.vring; a.sstride = p->ring_sstride; a.R = p->R;
-            a.ids = p->ids_dev; a.pos = p->pos; a.nq = n;
+            a.ids = ids; a.pos = p->pos; a.nq = n;
             a.P = Lw.Ppad; a.rmin = m->rmin; a.NR = m->NR; a.pbu = Lw.pbu; a.pbv = Lw.pbv;
             a.out = p->o; a.ldo = D;
             a.H = m->H; a.D = D; a.HD = m->HD;
-            a.left = m->cfg.att_left; a.chunk = m->cfg.att_chunk; a.rc = 0;
+            a.left = m->cfg.att_left; a.chunk = m->cfg.att_chunk; a.rc = m->cfg.right_context;
             a.nb = nb;
             a.scale = 1.f / std::sqrt((float)m->HD);
             PB(P_ATT);
@@ -672,7 +694,7 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
         RET(trace_tap(p, l, 3, p->glu, true, M, s));
         PB(P_DW);
         CK(launch_dwconv(p->glu, static_cast<char*>(p->conv) + (long long)l * CONV_CACHE * D * ab, p->conv_sstride,
-                         p->ids_dev, p->pos, n, n, Lw.dwT, Lw.bdw, Lw.bng, Lw.bnb, p->yc, D, nb, bf, s));
+                         ids, p->pos, n, n_commit, Lw.dwT, Lw.bdw, Lw.bng, Lw.bnb, p->yc, D, nb, bf, s));
         PE();
         ++*lc;
         RET(trace_tap(p, l, 4, p->yc, true, M, s));
@@ -712,21 +734,57 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
             RET(trace_tap(p, l, 6, p->xln, true, M, s));
         }
     }
-    if (joint) {
-        EpiParams ep;
-        ep.kind = EPI_STORE;
-        ep.bias = m->joint.b;
-        ep.out_f32 = joint;
-        ep.ldo = m->J;
-        ep.grp = n; ep.grp_stride = out_bstride; ep.row_off = out_off;
-        PB(P_JOINT);
-        RET(gemm(m, p->xln, D, M, D, m->joint, 0, ep, s, lc));
-        PE();
-    }
+    return CAC_OK;
+}
+
+// Joint projection of the rows of act (activation dtype, grp rows per slot)
+// into joint rows g' * out_bstride + out_off + i, g' = map ? map[g] : g.
+int run_joint(cac_pool* p, const void* act, int M, int grp, float* joint, int out_bstride, int out_off,
+              const int* map, cudaStream_t s) {
+    cac_model* m = p->m;
+    EpiParams ep;
+    ep.kind = EPI_STORE;
+    ep.bias = m->joint.b;
+    ep.out_f32 = joint;
+    ep.ldo = m->J;
+    ep.grp = grp; ep.grp_stride = out_bstride; ep.row_off = out_off; ep.grp_map = map;
+    PB(P_JOINT);
+    RET(gemm(m, act, m->D, M, m->D, m->joint, 0, ep, s, &p->launches));
+    PE();
+    return CAC_OK;
+}
+
+// One chunked-causal step: nb batch slots (ids in p->ids_dev), n new frames each.
+//   enc/joint: frame i of slot b goes to row b * out_bstride + out_off + i
+int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride, const int* nvalid, float* enc,
+             float* joint, int out_bstride, int out_off, cudaStream_t s) {
+    RET(run_subsample(p, nb, n, mel, mel_bstride, nvalid, p->ids_dev, p->pos, s));
+    RET(run_layers(p, nb, n, n, p->ids_dev, enc, out_bstride, out_off, s));
+    if (joint) RET(run_joint(p, p->xln, nb * n, n, joint, out_bstride, out_off, nullptr, s));
     PB(P_ADV);
     CK(launch_advance(p->pos, p->ids_dev, nb, n, s));
     PE();
-    ++*lc;
+    ++p->launches;
+    return CAC_OK;
+}
+
+// Provisional tail, one pass over the nbp streams in p->pids_dev: P frames
+// from the x0 ring starting at the first unemitted one, E of them emitted to
+// enc/joint rows pmap[b] * out_bstride + out_off + i, K/V and conv tail of the
+// emitted frames committed (the other P - E rows are recomputed next pass).
+int run_pass(cac_pool* p, int nbp, int P, int E, float* enc, float* joint, int out_bstride, int out_off,
+             cudaStream_t s) {
+    cac_model* m = p->m;
+    const int D = m->D;
+    CK(launch_x0_gather(p->x0, p->x, p->pids_dev, p->pos, nbp, P, p->XC, D, s));
+    ++p->launches;
+    RET(run_layers(p, nbp, P, E, p->pids_dev, nullptr, 0, 0, s));
+    // compact the emitted rows: fp32 frames to the caller, activation copy for the joint
+    CK(launch_emit_rows(p->x, p->xln, enc, p->o, p->pmap_dev, nbp, P, E, out_bstride, out_off, D, m->bf16, s));
+    ++p->launches;
+    if (joint) RET(run_joint(p, p->o, nbp * E, E, joint, out_bstride, out_off, p->pmap_dev, s));
+    CK(launch_advance(p->pos, p->pids_dev, nbp, E, s));
+    ++p->launches;
     return CAC_OK;
 }
 
@@ -819,6 +877,19 @@ extern "C" int cac_pool_create(cac_model* m, int max_streams, int max_frames_per
     if ((r = palloc(p, sizeof(int), &v)) != CAC_OK) return fail(r);
     p->status = static_cast<int*>(v);
     p->trace_rows = (int)rows_max;
+    if (c.right_context > 0) {
+        // waiting frames stay below emit + lookahead + one push sub-step
+        p->XC = 32;
+        if (c.emit_frames + c.lookahead_frames + p->nmax > p->XC || c.emit_frames % 2) return fail(CAC_E_UNSUPPORTED);
+        if ((r = palloc(p, sizeof(int) * S, &v)) != CAC_OK) return fail(r);
+        p->sub_pos = static_cast<int*>(v);
+        if ((r = palloc(p, sizeof(float) * S * p->XC * D, &v)) != CAC_OK) return fail(r);
+        p->x0 = static_cast<float*>(v);
+        if ((r = palloc(p, sizeof(int) * S, &v)) != CAC_OK) return fail(r);
+        p->pids_dev = static_cast<int*>(v);
+        if ((r = palloc(p, sizeof(int) * S, &v)) != CAC_OK) return fail(r);
+        p->pmap_dev = static_cast<int*>(v);
+    }
     if (cudaHostAlloc(reinterpret_cast<void**>(&p->pinned), sizeof(int) * S * ID_SLOTS, cudaHostAllocDefault) !=
         cudaSuccess)
         return fail(CAC_E_NOMEM);
@@ -827,6 +898,7 @@ extern "C" int cac_pool_create(cac_model* m, int max_streams, int max_frames_per
     p->alive.assign(S, 0);
     p->finished.assign(S, 0);
     p->pos_host.assign(S, 0);
+    p->sub_host.assign(S, 0);
     if (cudaDeviceSynchronize() != cudaSuccess) return fail(CAC_E_CUDA);
     *out = p;
     return CAC_OK;
@@ -858,9 +930,11 @@ extern "C" int cac_stream_create(cac_pool* p, int* id) {
             CK(cudaDeviceSynchronize());
             const int zero = 0;
             CK(cudaMemcpy(p->pos + i, &zero, sizeof(int), cudaMemcpyHostToDevice));
+            if (p->sub_pos) CK(cudaMemcpy(p->sub_pos + i, &zero, sizeof(int), cudaMemcpyHostToDevice));
             p->alive[i] = 1;
             p->finished[i] = 0;
             p->pos_host[i] = 0;
+            p->sub_host[i] = 0;
             *id = i;
             return CAC_OK;
         }
@@ -884,19 +958,133 @@ extern "C" int cac_stream_reset(cac_pool* p, int n, const int* ids, void* stream
     CK(launch_set_pos(p->pos, p->rids_dev, n, 0, s));
     PE();
     ++p->launches;
+    if (p->sub_pos) {
+        CK(launch_set_pos(p->sub_pos, p->rids_dev, n, 0, s));
+        ++p->launches;
+    }
     for (int i = 0; i < n; ++i) {
         p->pos_host[ids[i]] = 0;
+        p->sub_host[ids[i]] = 0;
         p->finished[ids[i]] = 0;
     }
     return CAC_OK;
 }
 
+namespace {
+
+// Subsample `frames` new frames of the listed streams (ids already in
+// p->ids_dev) into their x0 rings; mel rows as in run_subsample.
+int prov_subsample(cac_pool* p, int nb, int frames, const float* mel, long long mel_bstride, const int* nvalid,
+                   cudaStream_t s) {
+    const int chunk = std::max(2, (p->nmax / 2) * 2);  // even sub-steps keep the 160 ms subsampling grid
+    for (int f0 = 0; f0 < frames; f0 += chunk) {
+        const int nf = std::min(chunk, frames - f0);
+        const int* nv = (nvalid && f0 + nf >= frames) ? nvalid : nullptr;
+        RET(run_subsample(p, nb, nf, mel + (size_t)f0 * 8 * MEL, mel_bstride, nv, p->ids_dev, p->sub_pos, s));
+        CK(launch_x0_store(p->x, p->x0, p->ids_dev, p->sub_pos, nb, nf, p->XC, p->m->D, s));
+        CK(launch_advance(p->sub_pos, p->ids_dev, nb, nf, s));
+        p->launches += 2;
+    }
+    return CAC_OK;
+}
+
+// Run passes for the listed streams.  Not final: every stream with
+// emit + lookahead frames waiting takes a full pass (all such streams together,
+// round after round).  Final (flush): each stream's waiting frames are drained
+// with truncated lookahead.  Emitted frames of batch slot b land at rows
+// n_out[b] .. of its slab (out_bstride rows).
+int prov_drain(cac_pool* p, int n, const int* ids, bool final, float* enc, float* joint, int out_bstride, int* n_out,
+               cudaStream_t s) {
+    const cac_config& c = p->m->cfg;
+    const int E = c.emit_frames, need = c.emit_frames + c.lookahead_frames;
+    std::vector<int> pids, pmap;
+    if (!final) {
+        for (;;) {
+            pids.clear();
+            pmap.clear();
+            int off = -1;
+            for (int b = 0; b < n; ++b) {
+                const int id = ids[b];
+                if (p->sub_host[id] - p->pos_host[id] < need) continue;
+                if (off < 0) off = n_out[b];
+                if (n_out[b] != off) return CAC_E_STATE;  // ready streams emit in lockstep
+                pids.push_back(id);
+                pmap.push_back(b);
+            }
+            if (pids.empty()) return CAC_OK;
+            if (off + E > out_bstride) return CAC_E_INVAL;
+            RET(upload_ids(p, pids.data(), (int)pids.size(), p->pids_dev, s));
+            RET(upload_ids(p, pmap.data(), (int)pmap.size(), p->pmap_dev, s));
+            RET(run_pass(p, (int)pids.size(), need, E, enc, joint, out_bstride, off, s));
+            for (size_t k = 0; k < pids.size(); ++k) {
+                p->pos_host[pids[k]] += E;
+                n_out[pmap[k]] += E;
+            }
+        }
+    }
+    for (int b = 0; b < n; ++b) {
+        int id = ids[b];
+        while (p->sub_host[id] - p->pos_host[id] > 0) {
+            const int P = std::min(need, p->sub_host[id] - p->pos_host[id]), Ee = std::min(E, P);
+            if (n_out[b] + Ee > out_bstride) return CAC_E_INVAL;
+            RET(upload_ids(p, &id, 1, p->pids_dev, s));
+            RET(upload_ids(p, &b, 1, p->pmap_dev, s));
+            RET(run_pass(p, 1, P, Ee, enc, joint, out_bstride, n_out[b], s));
+            p->pos_host[id] += Ee;
+            n_out[b] += Ee;
+        }
+    }
+    return CAC_OK;
+}
+
+int push_prov(cac_pool* p, int n, const int* ids, const float* mel, int n_mel, float* enc, float* joint, int* n_out,
+              cudaStream_t s) {
+    const cac_config& c = p->m->cfg;
+    if (n_mel <= 0 || n_mel % (8 * c.emit_frames) || n_mel % (8 * c.att_chunk)) return CAC_E_ALIGN;
+    const int frames = n_mel / 8;
+    RET(upload_ids(p, ids, n, p->ids_dev, s));
+    RET(prov_subsample(p, n, frames, mel, (long long)n_mel * MEL, nullptr, s));
+    for (int b = 0; b < n; ++b) {
+        p->sub_host[ids[b]] += frames;
+        n_out[b] = 0;
+    }
+    return prov_drain(p, n, ids, false, enc, joint, frames, n_out, s);
+}
+
+int flush_prov(cac_pool* p, int n, const int* ids, const float* mel, int mel_stride, const int* n_mel_each,
+               float* enc, float* joint, int out_stride, int* n_out_each, cudaStream_t s) {
+    for (int b = 0; b < n; ++b) {
+        const int id = ids[b];
+        const int r = n_mel_each[b];
+        n_out_each[b] = 0;
+        if (r <= 0) continue;
+        const float* mb = mel + (size_t)b * mel_stride * MEL;
+        RET(upload_ids(p, &id, 1, p->ids_dev, s));
+        const int whole = r / 16 * 2;  // frames of whole 160 ms chunks
+        if (whole) RET(prov_subsample(p, 1, whole, mb, (long long)mel_stride * MEL, nullptr, s));
+        const int rem = r - whole * 8;
+        int frames = whole;
+        if (rem > 0) {
+            const int nf = (rem + 7) / 8;
+            RET(upload_ids(p, &rem, 1, p->nvalid_dev, s));
+            RET(prov_subsample(p, 1, nf, mb + (size_t)whole * 8 * MEL, (long long)mel_stride * MEL, p->nvalid_dev, s));
+            frames += nf;
+        }
+        p->sub_host[id] += frames;
+    }
+    RET(prov_drain(p, n, ids, true, enc, joint, out_stride, n_out_each, s));
+    for (int b = 0; b < n; ++b) p->finished[ids[b]] = 1;
+    return CAC_OK;
+}
+
+}  // namespace
+
 extern "C" int cac_stream_push(cac_pool* p, int n, const int* ids, const float* mel, int n_mel, float* enc,
                                float* joint, int* n_out, void* stream) {
     if (!p || !mel || !n_out) return CAC_E_INVAL;
     cac_model* m = p->m;
-    if (m->cfg.right_context > 0) return CAC_E_UNSUPPORTED;
     RET(check_ids(p, n, ids, true));
+    if (m->cfg.right_context > 0) return push_prov(p, n, ids, mel, n_mel, enc, joint, n_out, static_cast<cudaStream_t>(stream));
     const int A = m->cfg.att_chunk;
     if (n_mel <= 0 || n_mel % (8 * A)) return CAC_E_ALIGN;
     const int chunk = (p->nmax / A) * A;
@@ -966,6 +1154,7 @@ extern "C" int cac_stream_push_host(cac_pool* p, int n, const int* ids, const fl
 extern "C" int cac_stream_flush_frames(cac_pool* p, int id, int n_mel, int* frames) {
     if (!p || !frames || id < 0 || id >= p->S || n_mel < 0) return CAC_E_INVAL;
     *frames = (n_mel + 7) / 8;
+    if (p->m->cfg.right_context > 0) *frames += p->sub_host[id] - p->pos_host[id];  // frames still held back
     return CAC_OK;
 }
 
@@ -974,13 +1163,16 @@ extern "C" int cac_stream_flush(cac_pool* p, int n, const int* ids, const float*
                                 void* stream) {
     if (!p || !n_mel_each || !n_out_each) return CAC_E_INVAL;
     cac_model* m = p->m;
-    if (m->cfg.right_context > 0) return CAC_E_UNSUPPORTED;
     RET(check_ids(p, n, ids, true));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     for (int b = 0; b < n; ++b) {
         const int r = n_mel_each[b];
-        if (r < 0 || r > mel_stride || (r + 7) / 8 > out_stride || (r > 0 && !mel)) return CAC_E_INVAL;
+        int frames = 0;
+        RET(cac_stream_flush_frames(p, ids[b], r, &frames));
+        if (r < 0 || r > mel_stride || frames > out_stride || (r > 0 && !mel)) return CAC_E_INVAL;
     }
+    if (m->cfg.right_context > 0)
+        return flush_prov(p, n, ids, mel, mel_stride, n_mel_each, enc, joint, out_stride, n_out_each, s);
     // each stream alone: whole chunks as steps, then the ragged remainder
     const int A = m->cfg.att_chunk;
     const int chunk = (p->nmax / A) * A;
@@ -1274,6 +1466,15 @@ extern "C" int cac_stream_get_state(cac_pool* p, int id, cac_stream_state* st) {
     st->Lc = std::min(pos, left);
     st->finished = p->finished[id];
     st->x0_rows = 0;
+    if (p->x0) {
+        int sub = 0;
+        CK(cudaMemcpy(&sub, p->sub_pos + id, sizeof(int), cudaMemcpyDeviceToHost));
+        st->x0_rows = sub - pos;
+        if (st->x0)
+            for (int i = 0; i < st->x0_rows; ++i)
+                CK(cudaMemcpy(st->x0 + (size_t)i * D, p->x0 + ((size_t)id * p->XC + (pos + i) % p->XC) * D,
+                              sizeof(float) * D, cudaMemcpyDeviceToHost));
+    }
     std::vector<char> raw;
     if (st->mel_tail) {
         raw.resize(ab * p->tail_elems);
@@ -1375,6 +1576,16 @@ extern "C" int cac_stream_set_state(cac_pool* p, int id, const cac_stream_state*
     CK(cudaMemcpy(p->pos + id, &pos, sizeof(int), cudaMemcpyHostToDevice));
     p->pos_host[id] = pos;
     p->finished[id] = st->finished ? 1 : 0;
+    if (p->x0) {
+        const int rows = st->x0_rows;
+        if (rows < 0 || rows > p->XC || (rows > 0 && !st->x0)) return CAC_E_INVAL;
+        for (int i = 0; i < rows; ++i)
+            CK(cudaMemcpy(p->x0 + ((size_t)id * p->XC + (pos + i) % p->XC) * D, st->x0 + (size_t)i * D,
+                          sizeof(float) * D, cudaMemcpyHostToDevice));
+        const int sub = pos + rows;
+        CK(cudaMemcpy(p->sub_pos + id, &sub, sizeof(int), cudaMemcpyHostToDevice));
+        p->sub_host[id] = sub;
+    }
     return CAC_OK;
 }
 

@@ -31,8 +31,10 @@ struct EpiParams {
     float* out_f32 = nullptr;
     void* out_act = nullptr;
     int ldo = 0;
-    // EPI_STORE row remap: out row = (r / grp) * grp_stride + (r % grp) + row_off
+    // EPI_STORE row remap: out row = g' * grp_stride + (r % grp) + row_off with
+    // g = r / grp and g' = grp_map ? grp_map[g] : g
     int grp = 1 << 30, grp_stride = 0, row_off = 0;
+    const int* grp_map = nullptr;
     // EPI_RESID
     float* x = nullptr;
     int ldx = 0;
@@ -108,15 +110,36 @@ __device__ __forceinline__ void store32<bf16>(bf16* dst, const float (&v)[32]) {
     }
 }
 
-template <int KIND, class TAct>
-__device__ __forceinline__ void epilogue32(const EpiParams& e, int row, int col0, float (&v)[32]) {
+// Operands of the epilogue that do not depend on the accumulators (bias, and
+// the residual rows for EPI_RESID): loaded ahead, while the main loop runs.
+struct EpiPre {
+    float4 b[8];
+    float4 x[8];
+};
+
+template <int KIND>
+__device__ __forceinline__ void epi_prefetch(const EpiParams& e, int row, int col0, EpiPre& pre) {
     if (e.bias) {
         const float4* b4 = reinterpret_cast<const float4*>(e.bias + col0);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float4 b = __ldg(b4 + i);
-            v[4 * i] += b.x; v[4 * i + 1] += b.y; v[4 * i + 2] += b.z; v[4 * i + 3] += b.w;
-        }
+        for (int i = 0; i < 8; ++i) pre.b[i] = __ldg(b4 + i);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pre.b[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if constexpr (KIND == EPI_RESID) {
+        const float4* x4 = reinterpret_cast<const float4*>(e.x + (long long)row * e.ldx + col0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pre.x[i] = x4[i];
+    }
+}
+
+template <int KIND, class TAct>
+__device__ __forceinline__ void epilogue32(const EpiParams& e, int row, int col0, float (&v)[32], const EpiPre& pre) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 b = pre.b[i];
+        v[4 * i] += b.x; v[4 * i + 1] += b.y; v[4 * i + 2] += b.z; v[4 * i + 3] += b.w;
     }
     if constexpr (KIND == EPI_STORE) {
         if (e.act == ACT_SILU) {
@@ -126,14 +149,15 @@ __device__ __forceinline__ void epilogue32(const EpiParams& e, int row, int col0
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.f);
         }
-        const long long orow = (long long)(row / e.grp) * e.grp_stride + (row % e.grp) + e.row_off;
+        const int g = row / e.grp;
+        const long long orow = (long long)(e.grp_map ? e.grp_map[g] : g) * e.grp_stride + (row % e.grp) + e.row_off;
         if (e.out_f32) store32<float>(e.out_f32 + orow * e.ldo + col0, v);
         if (e.out_act) store32<TAct>(reinterpret_cast<TAct*>(e.out_act) + orow * e.ldo + col0, v);
     } else if constexpr (KIND == EPI_RESID) {
         float4* x4 = reinterpret_cast<float4*>(e.x + (long long)row * e.ldx + col0);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float4 a = x4[i];
+            float4 a = pre.x[i];
             a.x += e.scale * v[4 * i]; a.y += e.scale * v[4 * i + 1];
             a.z += e.scale * v[4 * i + 2]; a.w += e.scale * v[4 * i + 3];
             x4[i] = a;

@@ -53,7 +53,9 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const TA* __restrict__ A
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = Cs[r][32 * seg + i];
-            epilogue32<KIND, TAct>(ep, row, col0, v);
+            EpiPre pre;
+            epi_prefetch<KIND>(ep, row, col0, pre);
+            epilogue32<KIND, TAct>(ep, row, col0, v, pre);
         }
     }
 }

@@ -11,7 +11,9 @@
 //                  column half w/4, in 32-column chunks, and applies the fused
 //                  epilogue.  Eight warps (two per scheduler) keep the
 //                  epilogue's dependent arithmetic from stalling one warp per
-//                  scheduler; at BN = 64 four stages fit two CTAs per SM.
+//                  scheduler.  At BN = 64, eight stages put K = 512 in flight
+//                  at once (one TMA round trip per tile); the epilogue warps
+//                  load bias and residual rows while the main loop runs.
 // Split-K: the `splits` CTAs of one output tile form a thread-block cluster
 // along z, each accumulating a contiguous range of K slices.  Ranks > 0 park
 // their fp32 partial tile in their (now idle) pipeline shared memory; rank 0
@@ -36,7 +38,7 @@ template <int BN>
 struct TcCfg {
     static constexpr int B_TILE = BN * BK * 2;
     static constexpr int STAGE = A_TILE + B_TILE;
-    static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 4);
+    static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
     static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/;
 };
 }  // namespace
@@ -44,7 +46,7 @@ struct TcCfg {
 constexpr int TC_THREADS = 256;
 
 template <int BN, int KIND, class TAct>
-__global__ void __launch_bounds__(TC_THREADS, 2)
+__global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
                    int K, int conv_C, EpiParams ep, int* status) {
     using C = TcCfg<BN>;
@@ -127,13 +129,16 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
     }
     __syncwarp();
     pdl_wait();  // the epilogue reads/writes buffers of earlier kernels
+    const int quarter = warp & 3, half = warp >> 2;
+    const int rloc = quarter * 32 + lane;
+    const int row = m0 + rloc;
+    const int c_first = half * (BN / 2);
+    EpiPre pre;
+    if (crank == 0 && row < M) epi_prefetch<KIND>(ep, row, n0 + c_first, pre);
 
     if (!mbar_wait(accb, 0)) ok = false;
     pdl_trigger();  // main loop done: let the next kernel launch while the epilogue runs
     tc_fence_after();
-    const int quarter = warp & 3, half = warp >> 2;
-    const int rloc = quarter * 32 + lane;
-    const int row = m0 + rloc;
     // partial tile [BN columns][128 rows] fp32 in the pipeline buffers (idle now)
     float* part = reinterpret_cast<float*>(sA);
     if (splits > 1 && crank != 0) {
@@ -155,7 +160,10 @@ __global__ void __launch_bounds__(TC_THREADS, 2)
 #pragma unroll
                 for (int k = 0; k < 32; ++k) v[k] += ld_dsmem(&part[(c + k) * BM + rloc], (uint32_t)rr);
             }
-            if (ok && row < M) epilogue32<KIND, TAct>(ep, row, n0 + c, v);
+            if (ok && row < M) {
+                if (c != c_first) epi_prefetch<KIND>(ep, row, n0 + c, pre);
+                epilogue32<KIND, TAct>(ep, row, n0 + c, v, pre);
+            }
         }
     }
     if (splits > 1) cluster_sync();  // keep every rank's partial alive until rank 0 has read it

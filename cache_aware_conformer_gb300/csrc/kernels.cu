@@ -646,6 +646,82 @@ cudaError_t launch_dwconv(const void* glu, void* cache, long long cs_stride, con
 }
 
 // ---------------------------------------------------------------------------
+// provisional tail: x0 ring and emitted rows (float4 per thread)
+// ---------------------------------------------------------------------------
+__global__ void x0_store_kernel(const float* x, float* x0, const int* ids, const int* pos, int nb, int n, int XC,
+                                int D) {
+    pdl_wait();
+    const int D4 = D / 4;
+    const long long total = (long long)nb * n * D4;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int c = (int)(e % D4);
+        const long long r = e / D4;
+        const int b = (int)(r / n), i = (int)(r % n);
+        const int id = ids[b];
+        const int slot = (pos[id] + i) % XC;
+        reinterpret_cast<float4*>(x0 + ((long long)id * XC + slot) * D)[c] = reinterpret_cast<const float4*>(x + r * D)[c];
+    }
+}
+
+__global__ void x0_gather_kernel(const float* x0, float* x, const int* ids, const int* pos, int nb, int P, int XC,
+                                 int D) {
+    pdl_wait();
+    const int D4 = D / 4;
+    const long long total = (long long)nb * P * D4;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int c = (int)(e % D4);
+        const long long r = e / D4;
+        const int b = (int)(r / P), i = (int)(r % P);
+        const int id = ids[b];
+        const int slot = (pos[id] + i) % XC;
+        reinterpret_cast<float4*>(x + r * D)[c] = reinterpret_cast<const float4*>(x0 + ((long long)id * XC + slot) * D)[c];
+    }
+}
+
+template <class T>
+__global__ void emit_rows_kernel(const float* x, const T* act_src, float* dst, T* act_dst, const int* map, int nb,
+                                 int P, int E, int out_bstride, int out_off, int D) {
+    pdl_wait();
+    const long long total = (long long)nb * E * D;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int c = (int)(e % D);
+        const long long r = e / D;
+        const int b = (int)(r / E), i = (int)(r % E);
+        const long long src = ((long long)b * P + i) * D + c;
+        if (dst) dst[((long long)map[b] * out_bstride + out_off + i) * D + c] = x[src];
+        act_dst[r * D + c] = act_src[src];
+    }
+}
+
+static int grid_for(long long work) { return (int)std::min<long long>((work + 255) / 256, 152 * 8); }
+
+cudaError_t launch_x0_store(const float* x, float* x0, const int* ids, const int* pos, int nb, int n, int XC, int D,
+                            cudaStream_t s) {
+    if (nb <= 0 || n <= 0) return cudaSuccess;
+    return launch_k(x0_store_kernel, dim3(grid_for((long long)nb * n * D / 4)), dim3(256), 0, s, 1, x, x0, ids, pos,
+                    nb, n, XC, D);
+}
+cudaError_t launch_x0_gather(const float* x0, float* x, const int* ids, const int* pos, int nb, int P, int XC, int D,
+                             cudaStream_t s) {
+    if (nb <= 0 || P <= 0) return cudaSuccess;
+    return launch_k(x0_gather_kernel, dim3(grid_for((long long)nb * P * D / 4)), dim3(256), 0, s, 1, x0, x, ids, pos,
+                    nb, P, XC, D);
+}
+cudaError_t launch_emit_rows(const float* x, const void* act_src, float* dst, void* act_dst, const int* map, int nb,
+                             int P, int E, int out_bstride, int out_off, int D, int act_bf16, cudaStream_t s) {
+    if (nb <= 0 || E <= 0) return cudaSuccess;
+    const dim3 g(grid_for((long long)nb * E * D));
+    if (act_bf16)
+        return launch_k(emit_rows_kernel<bf16>, g, dim3(256), 0, s, 1, x, static_cast<const bf16*>(act_src), dst,
+                        static_cast<bf16*>(act_dst), map, nb, P, E, out_bstride, out_off, D);
+    return launch_k(emit_rows_kernel<float>, g, dim3(256), 0, s, 1, x, static_cast<const float*>(act_src), dst,
+                    static_cast<float*>(act_dst), map, nb, P, E, out_bstride, out_off, D);
+}
+
+// ---------------------------------------------------------------------------
 // bookkeeping and small utilities
 // ---------------------------------------------------------------------------
 __global__ void advance_kernel(int* pos, const int* ids, int nb, int n) {

@@ -63,6 +63,19 @@ cudaError_t launch_dwconv(const void* glu, void* cache, long long cs_stride, con
                           int n_commit, const float* wT, const float* bdw, const float* bng, const float* bnb,
                           void* out, int D, int nb, int act_bf16, cudaStream_t s);
 
+// Provisional tail: the exact subsampled frames that wait to be emitted live
+// in a per-stream ring x0[id][XC][D] (fp32), slot = absolute frame mod XC.
+// store:  x0[id][(pos[id] + i) % XC] = x[b * n + i]            (i < n)
+// gather: x[b * P + i] = x0[id][(pos[id] + i) % XC]            (i < P)
+// emit:   dst[map[b] * out_bstride + out_off + i] = x[b * P + i] and
+//         act_dst[b * E + i] = act_src[b * P + i]              (i < E)
+cudaError_t launch_x0_store(const float* x, float* x0, const int* ids, const int* pos, int nb, int n, int XC, int D,
+                            cudaStream_t s);
+cudaError_t launch_x0_gather(const float* x0, float* x, const int* ids, const int* pos, int nb, int P, int XC, int D,
+                             cudaStream_t s);
+cudaError_t launch_emit_rows(const float* x, const void* act_src, float* dst, void* act_dst, const int* map, int nb,
+                             int P, int E, int out_bstride, int out_off, int D, int act_bf16, cudaStream_t s);
+
 // pos[ids[b]] += n  /  pos[ids[b]] = value
 cudaError_t launch_advance(int* pos, const int* ids, int nb, int n, cudaStream_t s);
 cudaError_t launch_set_pos(int* pos, const int* ids, int nb, int value, cudaStream_t s);

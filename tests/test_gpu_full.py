@@ -22,7 +22,6 @@ DEV = "cuda"
 
 def _oracle_stream_30s(args):
     cfg, blob_path = args
-    os.environ["OPENBLAS_NUM_THREADS"] = "1"
     from oracle import conformer as O
     W = synth.unpack_weights(cfg, np.load(blob_path, mmap_mode="r"))
     mel = synth.make_mel(3000, 0)
@@ -35,7 +34,6 @@ def _oracle_stream_30s(args):
 def _oracle_schedule(args):
     """Replay one stream of the 256-stream schedule: pre-roll, then steps with resets."""
     cfg, blob_path, sid, pre, chunks, resets = args
-    os.environ["OPENBLAS_NUM_THREADS"] = "1"
     from oracle import conformer as O
     W = synth.unpack_weights(cfg, np.load(blob_path, mmap_mode="r"))
     mel = synth.make_mel(375 * 16, sid)
@@ -49,6 +47,22 @@ def _oracle_schedule(args):
         e, j = enc.push(mel[16 * c: 16 * (c + 1)])
         out.append((e, j, enc.subT, enc.Lc))
     return out
+
+
+@pytest.fixture(scope="module", autouse=True)
+def single_threaded_blas_children():
+    """Spawned oracle workers inherit these before they import numpy (one BLAS
+    thread each, so parallel workers do not oversubscribe the host cores)."""
+    keys = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+    old = {k: os.environ.get(k) for k in keys}
+    for k in keys:
+        os.environ[k] = "1"
+    yield
+    for k, v in old.items():
+        if v is None:
+            os.environ.pop(k, None)
+        else:
+            os.environ[k] = v
 
 
 @pytest.fixture(scope="module")
