@@ -83,6 +83,7 @@ struct OfflineWs {
 struct cac_model {
     cac_config cfg{};
     int bf16 = 1, tc = 1;
+    int split = 1;  // bf16: LayerNorm outputs enter their GEMMs as split (hi, lo) operands
     int D = 0, H = 0, HD = 0, F = 0, L = 0, J = 0;
     int rmin = 0, NR = 0;
     std::vector<void*> allocs;
@@ -180,28 +181,33 @@ int validate(const cac_config* c) {
 }
 
 int choose_splits(int tiles, int nk) {
-    // split K until the grid covers most of the 152 SMs (at most 4 ways, >= 2 K slices each)
+    // split K until the grid covers most of the 152 SMs, at most 4 ways and only
+    // while every split keeps >= 8 K slices: below that the cluster reduction
+    // costs more than the shorter main loop saves (measured at M = 512: K = 512
+    // runs faster unsplit at every N of the encoder, K = 2048 fastest 4-way)
     int splits = 1;
-    while (splits < 4 && tiles * splits < 120 && nk / (splits + 1) >= 2) ++splits;
+    while (splits < 4 && tiles * splits < 120 && nk / (splits + 1) >= 8) ++splits;
     return splits;
 }
 
 // GEMM dispatch: tcgen05 for bf16 models (unless the SIMT debugging twin is
 // requested), SIMT for fp32 models.  conv_C > 0: A is a stride-2 convolution
 // window read through the im2col view (M output rows = window row pairs).
+// a_split: A is a split operand (hi | lo, row stride lda >= 2K), see launch_layernorm.
 int gemm(cac_model* m, const void* A, long long lda, int M, int K, const Lin& W, int conv_C, EpiParams ep,
-         cudaStream_t s, long long* launches) {
+         cudaStream_t s, long long* launches, int a_split = 0) {
     if (M <= 0) return CAC_OK;
+    if (a_split && lda < 2LL * K) return CAC_E_INVAL;
     ep.act_bf16 = m->bf16;
     if (m->tc) {
         CUtensorMap tmA;
         const bool ok = conv_C ? make_tmap_bf16_conv(&tmA, A, conv_C, (uint64_t)M + 1, 128)
-                               : make_tmap_bf16(&tmA, A, K, M, (uint64_t)lda * 2, 128);
+                               : make_tmap_bf16(&tmA, A, a_split ? 2 * K : K, M, (uint64_t)lda * 2, 128);
         if (!ok) return CAC_E_CUDA;
         const int splits = choose_splits((W.N / W.BN) * ((M + 127) / 128), K / 64);
-        CK(launch_gemm_tc(&tmA, &W.tm, M, W.N, K, W.BN, conv_C, splits, ep, m->status, s));
+        CK(launch_gemm_tc(&tmA, &W.tm, M, W.N, K, W.BN, conv_C, splits, a_split, ep, m->status, s));
     } else {
-        CK(launch_gemm_simt(m->bf16, A, lda, W.w, K, M, W.N, K, ep, s));
+        CK(launch_gemm_simt(m->bf16, A, lda, W.w, K, M, W.N, K, a_split, ep, s));
     }
     ++*launches;
     return CAC_OK;
@@ -237,6 +243,7 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
     m->cfg = *cfg;
     m->bf16 = cfg->dtype == CAC_DTYPE_BF16;
     m->tc = m->bf16 && !cfg->gemm_simt;
+    m->split = m->bf16;
     m->D = cfg->d_model;
     m->H = cfg->n_heads;
     m->HD = m->D / m->H;
@@ -329,7 +336,7 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
             ep.act_bf16 = 0;
             ep.out_f32 = Lw.P;
             ep.ldo = D;
-            if (launch_gemm_simt(0, pe, D, wpos_d, D, m->NR, D, D, ep, 0) != cudaSuccess) return fail(CAC_E_CUDA);
+            if (launch_gemm_simt(0, pe, D, wpos_d, D, m->NR, D, D, 0, ep, 0) != cudaSuccess) return fail(CAC_E_CUDA);
             // head-major copy [H][NR][HD] in the activation dtype: one bulk copy per
             // (block, head) in the attention kernels
             std::vector<float> hp((size_t)m->NR * D), pad((size_t)H * m->NR * HD, 0.f);
@@ -515,13 +522,18 @@ int check_ids(cac_pool* p, int n, const int* ids, bool need_unfinished) {
     return CAC_OK;
 }
 
-int trace_tap(cac_pool* p, int layer, int tap, const void* src, bool src_act, int rows, cudaStream_t s) {
+// split: src is a bf16 split operand [rows][2D]; the tap records hi + lo.
+int trace_tap(cac_pool* p, int layer, int tap, const void* src, bool src_act, int rows, cudaStream_t s,
+              bool split = false) {
     if (!p->trace) return CAC_OK;
     cac_model* m = p->m;
     const long long per = (long long)p->trace_rows * m->D;
     float* dst = tap == N_TAPS ? p->trace_buf + (long long)m->L * N_TAPS * per
                                : p->trace_buf + ((long long)layer * N_TAPS + tap) * per;
-    CK(launch_to_f32(src, dst, (long long)rows * m->D, src_act && m->bf16, s));
+    if (split)
+        CK(launch_split_to_f32(src, dst, rows, m->D, s));
+    else
+        CK(launch_to_f32(src, dst, (long long)rows * m->D, src_act && m->bf16, s));
     ++p->launches;
     return CAC_OK;
 }
@@ -625,10 +637,11 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
     const int M = nb * nq, n = nq;
     long long* lc = &p->launches;
     const size_t ab = act_bytes(m);
-    const int bf = m->bf16;
+    const int bf = m->bf16, sp = m->split;
+    const long long ldl = sp ? 2LL * D : D;  // row stride of the split LayerNorm outputs in xln
     PB(P_LN);
     CK(launch_layernorm(p->x, M, D, m->layers[0].ff1_g, m->layers[0].ff1_b, nullptr, p->xln, nullptr, nullptr,
-                        nullptr, bf, 1 << 30, 0, 0, s));
+                        nullptr, bf, 1 << 30, 0, 0, sp, s));
     PE();
     ++*lc;
 
@@ -638,7 +651,7 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
         // FF1: x += 1/2 * (W2 SiLU(W1 LN(x) + b1) + b2)   (LN(x) already in xln)
         ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff1_w1.b; ep.out_act = p->h; ep.ldo = F;
         PB(P_FFUP);
-        RET(gemm(m, p->xln, D, M, D, Lw.ff1_w1, 0, ep, s, lc));
+        RET(gemm(m, p->xln, ldl, M, D, Lw.ff1_w1, 0, ep, s, lc, sp));
         PE();
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.ff1_w2.b; ep.x = p->x; ep.ldx = D; ep.scale = 0.5f;
         PB(P_FFDOWN);
@@ -648,7 +661,7 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
         // attention: xln = LN(x); Q and K/V into the rings
         PB(P_LN);
         CK(launch_layernorm(p->x, M, D, Lw.att_g, Lw.att_b, nullptr, p->xln, nullptr, nullptr, nullptr, bf,
-                            1 << 30, 0, 0, s));
+                            1 << 30, 0, 0, sp, s));
         PE();
         ++*lc;
         ep = EpiParams(); ep.kind = EPI_QKV; ep.bias = Lw.qkv.b; ep.D = D; ep.HD = m->HD; ep.R = p->R;
@@ -657,7 +670,7 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
         ep.vring = static_cast<char*>(p->vring) + (long long)l * m->H * p->R * m->HD * ab;
         ep.q = p->q; ep.ldq = D; ep.ids = ids; ep.pos = p->pos; ep.nq = n;
         PB(P_QKV);
-        RET(gemm(m, p->xln, D, M, D, Lw.qkv, 0, ep, s, lc));
+        RET(gemm(m, p->xln, ldl, M, D, Lw.qkv, 0, ep, s, lc, sp));
         PE();
         {
             AttnParams a;
@@ -665,7 +678,7 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
             a.k = ep.kring; a.v = ep.vring; a.sstride = p->ring_sstride; a.R = p->R;
             a.ids = ids; a.pos = p->pos; a.nq = n;
             a.P = Lw.Ppad; a.rmin = m->rmin; a.NR = m->NR; a.pbu = Lw.pbu; a.pbv = Lw.pbv;
-            a.out = p->o; a.ldo = D;
+            a.out = p->o; a.ldo = (int)ldl; a.out_split = sp ? D : 0;
             a.H = m->H; a.D = D; a.HD = m->HD;
             a.left = m->cfg.att_left; a.chunk = m->cfg.att_chunk; a.rc = m->cfg.right_context;
             a.nb = nb;
@@ -675,21 +688,21 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
             PE();
             ++*lc;
         }
-        RET(trace_tap(p, l, 1, p->o, true, M, s));
+        RET(trace_tap(p, l, 1, p->o, true, M, s, sp));
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.wo.b; ep.x = p->x; ep.ldx = D; ep.scale = 1.f;
         PB(P_OUT);
-        RET(gemm(m, p->o, D, M, D, Lw.wo, 0, ep, s, lc));
+        RET(gemm(m, p->o, ldl, M, D, Lw.wo, 0, ep, s, lc, sp));
         PE();
         RET(trace_tap(p, l, 2, p->x, false, M, s));
         // conv module
         PB(P_LN);
         CK(launch_layernorm(p->x, M, D, Lw.conv_g, Lw.conv_b, nullptr, p->xln, nullptr, nullptr, nullptr, bf,
-                            1 << 30, 0, 0, s));
+                            1 << 30, 0, 0, sp, s));
         PE();
         ++*lc;
         ep = EpiParams(); ep.kind = EPI_GLU; ep.bias = Lw.pw1.b; ep.out_act = p->glu; ep.ldo = D;
         PB(P_PW1);
-        RET(gemm(m, p->xln, D, M, D, Lw.pw1, 0, ep, s, lc));
+        RET(gemm(m, p->xln, ldl, M, D, Lw.pw1, 0, ep, s, lc, sp));
         PE();
         RET(trace_tap(p, l, 3, p->glu, true, M, s));
         PB(P_DW);
@@ -706,12 +719,12 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
         // FF2
         PB(P_LN);
         CK(launch_layernorm(p->x, M, D, Lw.ff2_g, Lw.ff2_b, nullptr, p->xln, nullptr, nullptr, nullptr, bf,
-                            1 << 30, 0, 0, s));
+                            1 << 30, 0, 0, sp, s));
         PE();
         ++*lc;
         ep = EpiParams(); ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff2_w1.b; ep.out_act = p->h; ep.ldo = F;
         PB(P_FFUP);
-        RET(gemm(m, p->xln, D, M, D, Lw.ff2_w1, 0, ep, s, lc));
+        RET(gemm(m, p->xln, ldl, M, D, Lw.ff2_w1, 0, ep, s, lc, sp));
         PE();
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.ff2_w2.b; ep.x = p->x; ep.ldx = D; ep.scale = 0.5f;
         PB(P_FFDOWN);
@@ -722,13 +735,13 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
         PB(P_LN);
         if (l + 1 < L) {
             CK(launch_layernorm(p->x, M, D, Lw.out_g, Lw.out_b, p->x, nullptr, m->layers[l + 1].ff1_g,
-                                m->layers[l + 1].ff1_b, p->xln, bf, 1 << 30, 0, 0, s));
+                                m->layers[l + 1].ff1_b, p->xln, bf, 1 << 30, 0, 0, sp, s));
             PE();
             ++*lc;
             RET(trace_tap(p, l, 6, p->x, false, M, s));
         } else {
             CK(launch_layernorm(p->x, M, D, Lw.out_g, Lw.out_b, enc ? enc : p->x, p->xln, nullptr, nullptr, nullptr,
-                                bf, enc ? n : 1 << 30, enc ? out_bstride : 0, enc ? out_off : 0, s));
+                                bf, enc ? n : 1 << 30, enc ? out_bstride : 0, enc ? out_off : 0, 0, s));
             PE();
             ++*lc;
             RET(trace_tap(p, l, 6, p->xln, true, M, s));
@@ -769,20 +782,20 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
 }
 
 // Provisional tail, one pass over the nbp streams in p->pids_dev: P frames
-// from the x0 ring starting at the first unemitted one, E of them emitted to
-// enc/joint rows pmap[b] * out_bstride + out_off + i, K/V and conv tail of the
-// emitted frames committed (the other P - E rows are recomputed next pass).
-int run_pass(cac_pool* p, int nbp, int P, int E, float* enc, float* joint, int out_bstride, int out_off,
-             cudaStream_t s) {
+// from the x0 ring starting at the first unemitted one; E of them are emitted,
+// frame i of batch slot k to enc/joint row p->pmap_dev[k] + i; K/V and the conv
+// tail of the emitted frames are committed (the other P - E rows are
+// recomputed by the next pass).
+int run_pass(cac_pool* p, int nbp, int P, int E, float* enc, float* joint, cudaStream_t s) {
     cac_model* m = p->m;
     const int D = m->D;
     CK(launch_x0_gather(p->x0, p->x, p->pids_dev, p->pos, nbp, P, p->XC, D, s));
     ++p->launches;
     RET(run_layers(p, nbp, P, E, p->pids_dev, nullptr, 0, 0, s));
     // compact the emitted rows: fp32 frames to the caller, activation copy for the joint
-    CK(launch_emit_rows(p->x, p->xln, enc, p->o, p->pmap_dev, nbp, P, E, out_bstride, out_off, D, m->bf16, s));
+    CK(launch_emit_rows(p->x, p->xln, enc, p->o, p->pmap_dev, nbp, P, E, D, m->bf16, s));
     ++p->launches;
-    if (joint) RET(run_joint(p, p->o, nbp * E, E, joint, out_bstride, out_off, p->pmap_dev, s));
+    if (joint) RET(run_joint(p, p->o, nbp * E, E, joint, 1, 0, p->pmap_dev, s));
     CK(launch_advance(p->pos, p->pids_dev, nbp, E, s));
     ++p->launches;
     return CAC_OK;
@@ -861,11 +874,11 @@ extern "C" int cac_pool_create(cac_model* m, int max_streams, int max_frames_per
     if ((r = palloc(p, ab * rows_max * D, &p->y3)) != CAC_OK) return fail(r);
     if ((r = palloc(p, 4 * rows_max * D, &v)) != CAC_OK) return fail(r);
     p->x = static_cast<float*>(v);
-    if ((r = palloc(p, ab * rows_max * D, &p->xln)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, ab * rows_max * D * (m->split ? 2 : 1), &p->xln)) != CAC_OK) return fail(r);
     if ((r = palloc(p, ab * rows_max * F, &p->h)) != CAC_OK) return fail(r);
     if ((r = palloc(p, 4 * rows_max * D, &v)) != CAC_OK) return fail(r);
     p->q = static_cast<float*>(v);
-    if ((r = palloc(p, ab * rows_max * D, &p->o)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, ab * rows_max * D * (m->split ? 2 : 1), &p->o)) != CAC_OK) return fail(r);
     if ((r = palloc(p, ab * rows_max * D, &p->glu)) != CAC_OK) return fail(r);
     if ((r = palloc(p, ab * rows_max * D, &p->yc)) != CAC_OK) return fail(r);
     if ((r = palloc(p, sizeof(int) * S, &v)) != CAC_OK) return fail(r);
@@ -973,63 +986,60 @@ extern "C" int cac_stream_reset(cac_pool* p, int n, const int* ids, void* stream
 namespace {
 
 // Subsample `frames` new frames of the listed streams (ids already in
-// p->ids_dev) into their x0 rings; mel rows as in run_subsample.
+// p->ids_dev) into their x0 rings; mel rows as in run_subsample.  The caller
+// keeps frames <= p->nmax, so a ring of XC >= emit + lookahead + nmax rows never
+// overwrites a frame that still waits.
 int prov_subsample(cac_pool* p, int nb, int frames, const float* mel, long long mel_bstride, const int* nvalid,
                    cudaStream_t s) {
-    const int chunk = std::max(2, (p->nmax / 2) * 2);  // even sub-steps keep the 160 ms subsampling grid
-    for (int f0 = 0; f0 < frames; f0 += chunk) {
-        const int nf = std::min(chunk, frames - f0);
-        const int* nv = (nvalid && f0 + nf >= frames) ? nvalid : nullptr;
-        RET(run_subsample(p, nb, nf, mel + (size_t)f0 * 8 * MEL, mel_bstride, nv, p->ids_dev, p->sub_pos, s));
-        CK(launch_x0_store(p->x, p->x0, p->ids_dev, p->sub_pos, nb, nf, p->XC, p->m->D, s));
-        CK(launch_advance(p->sub_pos, p->ids_dev, nb, nf, s));
-        p->launches += 2;
-    }
+    if (frames > p->nmax) return CAC_E_INVAL;
+    RET(run_subsample(p, nb, frames, mel, mel_bstride, nvalid, p->ids_dev, p->sub_pos, s));
+    CK(launch_x0_store(p->x, p->x0, p->ids_dev, p->sub_pos, nb, frames, p->XC, p->m->D, s));
+    CK(launch_advance(p->sub_pos, p->ids_dev, nb, frames, s));
+    p->launches += 2;
     return CAC_OK;
 }
 
-// Run passes for the listed streams.  Not final: every stream with
-// emit + lookahead frames waiting takes a full pass (all such streams together,
-// round after round).  Final (flush): each stream's waiting frames are drained
-// with truncated lookahead.  Emitted frames of batch slot b land at rows
-// n_out[b] .. of its slab (out_bstride rows).
+// Run passes for the listed streams.  Rounds of full passes first: every
+// stream with emit + lookahead frames waiting takes one (all such streams in
+// one batch), until none has.  Final (flush): then each stream's remaining
+// frames are drained with truncated lookahead.  Emitted frame i of batch slot b
+// lands at row b * out_bstride + n_out[b] + i (n_out[b] grows as it emits).
 int prov_drain(cac_pool* p, int n, const int* ids, bool final, float* enc, float* joint, int out_bstride, int* n_out,
                cudaStream_t s) {
     const cac_config& c = p->m->cfg;
     const int E = c.emit_frames, need = c.emit_frames + c.lookahead_frames;
-    std::vector<int> pids, pmap;
-    if (!final) {
-        for (;;) {
-            pids.clear();
-            pmap.clear();
-            int off = -1;
-            for (int b = 0; b < n; ++b) {
-                const int id = ids[b];
-                if (p->sub_host[id] - p->pos_host[id] < need) continue;
-                if (off < 0) off = n_out[b];
-                if (n_out[b] != off) return CAC_E_STATE;  // ready streams emit in lockstep
-                pids.push_back(id);
-                pmap.push_back(b);
-            }
-            if (pids.empty()) return CAC_OK;
-            if (off + E > out_bstride) return CAC_E_INVAL;
-            RET(upload_ids(p, pids.data(), (int)pids.size(), p->pids_dev, s));
-            RET(upload_ids(p, pmap.data(), (int)pmap.size(), p->pmap_dev, s));
-            RET(run_pass(p, (int)pids.size(), need, E, enc, joint, out_bstride, off, s));
-            for (size_t k = 0; k < pids.size(); ++k) {
-                p->pos_host[pids[k]] += E;
-                n_out[pmap[k]] += E;
-            }
+    std::vector<int> pids, prow, slot;
+    for (;;) {
+        pids.clear();
+        prow.clear();
+        slot.clear();
+        for (int b = 0; b < n; ++b) {
+            const int id = ids[b];
+            if (p->sub_host[id] - p->pos_host[id] < need) continue;
+            if (n_out[b] + E > out_bstride) return CAC_E_INVAL;
+            pids.push_back(id);
+            prow.push_back(b * out_bstride + n_out[b]);
+            slot.push_back(b);
+        }
+        if (pids.empty()) break;
+        RET(upload_ids(p, pids.data(), (int)pids.size(), p->pids_dev, s));
+        RET(upload_ids(p, prow.data(), (int)prow.size(), p->pmap_dev, s));
+        RET(run_pass(p, (int)pids.size(), need, E, enc, joint, s));
+        for (size_t k = 0; k < pids.size(); ++k) {
+            p->pos_host[pids[k]] += E;
+            n_out[slot[k]] += E;
         }
     }
+    if (!final) return CAC_OK;
     for (int b = 0; b < n; ++b) {
         int id = ids[b];
         while (p->sub_host[id] - p->pos_host[id] > 0) {
             const int P = std::min(need, p->sub_host[id] - p->pos_host[id]), Ee = std::min(E, P);
             if (n_out[b] + Ee > out_bstride) return CAC_E_INVAL;
+            int row = b * out_bstride + n_out[b];
             RET(upload_ids(p, &id, 1, p->pids_dev, s));
-            RET(upload_ids(p, &b, 1, p->pmap_dev, s));
-            RET(run_pass(p, 1, P, Ee, enc, joint, out_bstride, n_out[b], s));
+            RET(upload_ids(p, &row, 1, p->pmap_dev, s));
+            RET(run_pass(p, 1, P, Ee, enc, joint, s));
             p->pos_host[id] += Ee;
             n_out[b] += Ee;
         }
@@ -1037,43 +1047,60 @@ int prov_drain(cac_pool* p, int n, const int* ids, bool final, float* enc, float
     return CAC_OK;
 }
 
+// Frames subsampled per piece before the passes they enable are run (even, so
+// the 160 ms subsampling grid is kept; at most nmax).
+int prov_piece(const cac_pool* p) { return std::max(2, (p->nmax / 2) * 2); }
+
 int push_prov(cac_pool* p, int n, const int* ids, const float* mel, int n_mel, float* enc, float* joint, int* n_out,
               cudaStream_t s) {
     const cac_config& c = p->m->cfg;
     if (n_mel <= 0 || n_mel % (8 * c.emit_frames) || n_mel % (8 * c.att_chunk)) return CAC_E_ALIGN;
     const int frames = n_mel / 8;
     RET(upload_ids(p, ids, n, p->ids_dev, s));
-    RET(prov_subsample(p, n, frames, mel, (long long)n_mel * MEL, nullptr, s));
-    for (int b = 0; b < n; ++b) {
-        p->sub_host[ids[b]] += frames;
-        n_out[b] = 0;
+    for (int b = 0; b < n; ++b) n_out[b] = 0;
+    for (int f0 = 0; f0 < frames;) {
+        const int nf = std::min(prov_piece(p), frames - f0);
+        RET(prov_subsample(p, n, nf, mel + (size_t)f0 * 8 * MEL, (long long)n_mel * MEL, nullptr, s));
+        for (int b = 0; b < n; ++b) p->sub_host[ids[b]] += nf;
+        RET(prov_drain(p, n, ids, false, enc, joint, frames, n_out, s));
+        f0 += nf;
     }
-    return prov_drain(p, n, ids, false, enc, joint, frames, n_out, s);
+    return CAC_OK;
 }
 
 int flush_prov(cac_pool* p, int n, const int* ids, const float* mel, int mel_stride, const int* n_mel_each,
                float* enc, float* joint, int out_stride, int* n_out_each, cudaStream_t s) {
+    const int D = p->m->D, J = p->m->J;
     for (int b = 0; b < n; ++b) {
         const int id = ids[b];
         const int r = n_mel_each[b];
+        float* eb = enc ? enc + (size_t)b * out_stride * D : nullptr;
+        float* jb = joint ? joint + (size_t)b * out_stride * J : nullptr;
         n_out_each[b] = 0;
-        if (r <= 0) continue;
-        const float* mb = mel + (size_t)b * mel_stride * MEL;
-        RET(upload_ids(p, &id, 1, p->ids_dev, s));
-        const int whole = r / 16 * 2;  // frames of whole 160 ms chunks
-        if (whole) RET(prov_subsample(p, 1, whole, mb, (long long)mel_stride * MEL, nullptr, s));
-        const int rem = r - whole * 8;
-        int frames = whole;
-        if (rem > 0) {
-            const int nf = (rem + 7) / 8;
-            RET(upload_ids(p, &rem, 1, p->nvalid_dev, s));
-            RET(prov_subsample(p, 1, nf, mb + (size_t)whole * 8 * MEL, (long long)mel_stride * MEL, p->nvalid_dev, s));
-            frames += nf;
+        if (r > 0) {
+            const float* mb = mel + (size_t)b * mel_stride * MEL;
+            RET(upload_ids(p, &id, 1, p->ids_dev, s));
+            const int whole = r / 16 * 2;  // frames of whole 160 ms chunks
+            for (int f0 = 0; f0 < whole;) {
+                const int nf = std::min(prov_piece(p), whole - f0);
+                RET(prov_subsample(p, 1, nf, mb + (size_t)f0 * 8 * MEL, (long long)mel_stride * MEL, nullptr, s));
+                p->sub_host[id] += nf;
+                RET(prov_drain(p, 1, &id, false, eb, jb, out_stride, &n_out_each[b], s));
+                f0 += nf;
+            }
+            const int rem = r - whole * 8;
+            if (rem > 0) {
+                const int nf = (rem + 7) / 8;
+                RET(upload_ids(p, &id, 1, p->ids_dev, s));
+                RET(upload_ids(p, &rem, 1, p->nvalid_dev, s));
+                RET(prov_subsample(p, 1, nf, mb + (size_t)whole * 8 * MEL, (long long)mel_stride * MEL,
+                                   p->nvalid_dev, s));
+                p->sub_host[id] += nf;
+            }
         }
-        p->sub_host[id] += frames;
+        RET(prov_drain(p, 1, &id, true, eb, jb, out_stride, &n_out_each[b], s));
+        p->finished[id] = 1;
     }
-    RET(prov_drain(p, n, ids, true, enc, joint, out_stride, n_out_each, s));
-    for (int b = 0; b < n; ++b) p->finished[ids[b]] = 1;
     return CAC_OK;
 }
 
@@ -1244,12 +1271,12 @@ OfflineLayout offline_layout(const cac_model* m, int B, int t_mel_max) {
     y.o_win3 = take(ab * ((size_t)B * y.W3 + 4) * D);
     y.o_y3 = take(ab * M * D);
     y.o_x = take(4 * M * D);
-    y.o_xln = take(ab * M * D);
+    y.o_xln = take(ab * M * D * (m->split ? 2 : 1));
     y.o_h = take(ab * M * F);
     y.o_q = take(4 * M * D);
     y.o_k = take(ab * M * D);
     y.o_v = take(ab * M * D);
-    y.o_o = take(ab * M * D);
+    y.o_o = take(ab * M * D * (m->split ? 2 : 1));
     y.o_glu = take(ab * M * D);
     y.o_yc = take(ab * M * D);
     y.o_mlen = take(sizeof(int) * B);
@@ -1315,52 +1342,54 @@ int offline_run(cac_model* m, char* w, const OfflineLayout& lay, int B, const fl
         eo.kind = EPI_STORE; eo.bias = m->subo.b; eo.out_f32 = x; eo.ldo = D;
         RET(gemm(m, y3, D, (int)M, D, m->subo, 0, eo, s, &lc));
     }
+    const int sp = m->split;
+    const long long ldl = sp ? 2LL * D : D;  // row stride of the split LayerNorm outputs in xln
     CK(launch_layernorm(x, (int)M, D, m->layers[0].ff1_g, m->layers[0].ff1_b, nullptr, xln, nullptr, nullptr, nullptr,
-                        bf, 1 << 30, 0, 0, s));
+                        bf, 1 << 30, 0, 0, sp, s));
     ++lc;
     for (int l = 0; l < L; ++l) {
         const LayerW& Lw = m->layers[l];
         EpiParams ep;
         ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff1_w1.b; ep.out_act = h; ep.ldo = F;
-        RET(gemm(m, xln, D, (int)M, D, Lw.ff1_w1, 0, ep, s, &lc));
+        RET(gemm(m, xln, ldl, (int)M, D, Lw.ff1_w1, 0, ep, s, &lc, sp));
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.ff1_w2.b; ep.x = x; ep.ldx = D; ep.scale = 0.5f;
         RET(gemm(m, h, F, (int)M, F, Lw.ff1_w2, 0, ep, s, &lc));
         CK(launch_layernorm(x, (int)M, D, Lw.att_g, Lw.att_b, nullptr, xln, nullptr, nullptr, nullptr, bf, 1 << 30, 0,
-                            0, s));
+                            0, sp, s));
         ep = EpiParams(); ep.kind = EPI_QKV; ep.bias = Lw.qkv.b; ep.D = D; ep.HD = m->HD; ep.dense = 1;
         ep.kring = kd; ep.vring = vd; ep.q = q; ep.ldq = D;
-        RET(gemm(m, xln, D, (int)M, D, Lw.qkv, 0, ep, s, &lc));
+        RET(gemm(m, xln, ldl, (int)M, D, Lw.qkv, 0, ep, s, &lc, sp));
         {
             AttnParams a;
             a.q = q; a.ldq = D; a.k = kd; a.v = vd; a.ldk = D;
             a.P = Lw.Ppad; a.rmin = m->rmin; a.NR = m->NR; a.pbu = Lw.pbu; a.pbv = Lw.pbv;
-            a.out = o; a.ldo = D; a.H = m->H; a.D = D; a.HD = m->HD;
+            a.out = o; a.ldo = (int)ldl; a.out_split = sp ? D : 0; a.H = m->H; a.D = D; a.HD = m->HD;
             a.left = m->cfg.att_left; a.chunk = m->cfg.att_chunk; a.rc = m->cfg.right_context;
             a.nb = B; a.T = T3; a.seq_len = flen_d;
             a.scale = 1.f / std::sqrt((float)m->HD);
             CK(launch_attention_offline(a, bf, m->status, s));
         }
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.wo.b; ep.x = x; ep.ldx = D; ep.scale = 1.f;
-        RET(gemm(m, o, D, (int)M, D, Lw.wo, 0, ep, s, &lc));
+        RET(gemm(m, o, ldl, (int)M, D, Lw.wo, 0, ep, s, &lc, sp));
         CK(launch_layernorm(x, (int)M, D, Lw.conv_g, Lw.conv_b, nullptr, xln, nullptr, nullptr, nullptr, bf, 1 << 30,
-                            0, 0, s));
+                            0, 0, sp, s));
         ep = EpiParams(); ep.kind = EPI_GLU; ep.bias = Lw.pw1.b; ep.out_act = glu; ep.ldo = D;
-        RET(gemm(m, xln, D, (int)M, D, Lw.pw1, 0, ep, s, &lc));
+        RET(gemm(m, xln, ldl, (int)M, D, Lw.pw1, 0, ep, s, &lc, sp));
         CK(launch_dwconv(glu, nullptr, 0, nullptr, nullptr, T3, 0, Lw.dwT, Lw.bdw, Lw.bng, Lw.bnb, yc, D, B, bf, s));
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.pw2.b; ep.x = x; ep.ldx = D; ep.scale = 1.f;
         RET(gemm(m, yc, D, (int)M, D, Lw.pw2, 0, ep, s, &lc));
         CK(launch_layernorm(x, (int)M, D, Lw.ff2_g, Lw.ff2_b, nullptr, xln, nullptr, nullptr, nullptr, bf, 1 << 30, 0,
-                            0, s));
+                            0, sp, s));
         ep = EpiParams(); ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff2_w1.b; ep.out_act = h; ep.ldo = F;
-        RET(gemm(m, xln, D, (int)M, D, Lw.ff2_w1, 0, ep, s, &lc));
+        RET(gemm(m, xln, ldl, (int)M, D, Lw.ff2_w1, 0, ep, s, &lc, sp));
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.ff2_w2.b; ep.x = x; ep.ldx = D; ep.scale = 0.5f;
         RET(gemm(m, h, F, (int)M, F, Lw.ff2_w2, 0, ep, s, &lc));
         if (l + 1 < L)
             CK(launch_layernorm(x, (int)M, D, Lw.out_g, Lw.out_b, x, nullptr, m->layers[l + 1].ff1_g,
-                                m->layers[l + 1].ff1_b, xln, bf, 1 << 30, 0, 0, s));
+                                m->layers[l + 1].ff1_b, xln, bf, 1 << 30, 0, 0, sp, s));
         else
             CK(launch_layernorm(x, (int)M, D, Lw.out_g, Lw.out_b, enc, xln, nullptr, nullptr, nullptr, bf, 1 << 30, 0,
-                                0, s));
+                                0, 0, s));
         lc += 7;
     }
     if (joint) {
@@ -1659,7 +1688,7 @@ extern "C" int cac_pool_read_profile(cac_pool* p, int n_classes, double* total_m
 }
 
 extern "C" int cac_op_gemm_bf16(int M, int N, int K, const void* A, const void* B, const float* bias, float* C,
-                                int splits, void* stream) {
+                                int splits, int a_split, void* stream) {
     if (M < 1 || N < 64 || K < 64 || N % 64 || K % 64 || !A || !B || !C || splits < 0 || splits > 4 ||
         splits > K / 64)
         return CAC_E_INVAL;
@@ -1667,7 +1696,8 @@ extern "C" int cac_op_gemm_bf16(int M, int N, int K, const void* A, const void* 
          reinterpret_cast<uintptr_t>(bias)) & 15)
         return CAC_E_ALIGN;
     CUtensorMap ta, tb;
-    if (!make_tmap_bf16(&ta, A, K, M, (uint64_t)K * 2, 128) || !make_tmap_bf16(&tb, B, K, N, (uint64_t)K * 2, 64))
+    const uint64_t ka = a_split ? 2ull * K : (uint64_t)K;
+    if (!make_tmap_bf16(&ta, A, ka, M, ka * 2, 128) || !make_tmap_bf16(&tb, B, K, N, (uint64_t)K * 2, 64))
         return CAC_E_CUDA;
     EpiParams ep;
     ep.kind = EPI_STORE;
@@ -1676,7 +1706,8 @@ extern "C" int cac_op_gemm_bf16(int M, int N, int K, const void* A, const void* 
     ep.out_f32 = C;
     ep.ldo = N;
     if (splits == 0) splits = choose_splits((N / 64) * ((M + 127) / 128), K / 64);
-    CK(launch_gemm_tc(&ta, &tb, M, N, K, 64, 0, splits, ep, nullptr, static_cast<cudaStream_t>(stream)));
+    CK(launch_gemm_tc(&ta, &tb, M, N, K, 64, 0, splits, a_split ? 1 : 0, ep, nullptr,
+                      static_cast<cudaStream_t>(stream)));
     return CAC_OK;
 }
 

@@ -72,12 +72,15 @@ bool make_tmap_bf16_conv(CUtensorMap* tm, const void* base, uint64_t C, uint64_t
 // conv_C > 0 selects the convolution view of A (tmA from make_tmap_bf16_conv, K = 3 * conv_C).
 // splits in 1..4: split-K over a cluster of `splits` CTAs per output tile,
 // reduced deterministically through distributed shared memory.
+// a_split: A is a split operand [M][2K] (hi in columns [0, K), lo = residual of
+// the bf16 rounding in [K, 2K)); the product is (hi + lo) * B^T.
 cudaError_t launch_gemm_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int BN, int conv_C,
-                           int splits, const EpiParams& ep, int* status, cudaStream_t s);
+                           int splits, int a_split, const EpiParams& ep, int* status, cudaStream_t s);
 
-// SIMT GEMM (fp32 or bf16 operands, fp32 accumulate).  N % 32 == 0.
+// SIMT GEMM (fp32 or bf16 operands, fp32 accumulate).  N % 32 == 0.  a_split
+// (bf16 only): A row r holds hi at A + r * lda and lo at A + r * lda + K.
 cudaError_t launch_gemm_simt(int bf16_operands, const void* A, long long lda, const void* B, long long ldb, int M,
-                             int N, int K, const EpiParams& ep, cudaStream_t s);
+                             int N, int K, int a_split, const EpiParams& ep, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // epilogue, applied to one row segment of 32 accumulators

@@ -14,6 +14,10 @@
 //                  scheduler.  At BN = 64, eight stages put K = 512 in flight
 //                  at once (one TMA round trip per tile); the epilogue warps
 //                  load bias and residual rows while the main loop runs.
+// Split operands: with SPLIT the A slice is a (hi, lo) pair of bf16 tiles and
+// each slice issues 8 MMAs (hi then lo against the same B tile), so an fp32
+// activation enters the product with ~16 significant bits while the
+// contraction stays bf16 x bf16 with fp32 accumulation.
 // Split-K: the `splits` CTAs of one output tile form a thread-block cluster
 // along z, each accumulating a contiguous range of K slices.  Ranks > 0 park
 // their fp32 partial tile in their (now idle) pipeline shared memory; rank 0
@@ -34,26 +38,32 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int A_TILE = BM * BK * 2;  // bytes
 
-template <int BN>
+// SPLIT: the A operand is a split pair (hi, lo) of bf16 tiles per K slice (hi
+// at column k, lo at column K + k of the A tensor map); both are multiplied by
+// the same B tile into the same accumulator.
+template <int BN, int SPLIT>
 struct TcCfg {
     static constexpr int B_TILE = BN * BK * 2;
-    static constexpr int STAGE = A_TILE + B_TILE;
-    static constexpr int STAGES = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int A_TILES = A_TILE * (1 + SPLIT);
+    static constexpr int STAGE = A_TILES + B_TILE;
+    static constexpr int STAGES = SPLIT ? ((BN == 256) ? 3 : (BN == 128 ? 4 : 5)) : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
     static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/;
+    static_assert(STAGES * STAGE >= BN * BM * 4, "split-K partial tile must fit the pipeline buffers");
+    static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 }  // namespace
 
 constexpr int TC_THREADS = 256;
 
-template <int BN, int KIND, class TAct>
+template <int BN, int KIND, class TAct, int SPLIT>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
                    int K, int conv_C, EpiParams ep, int* status) {
-    using C = TcCfg<BN>;
+    using C = TcCfg<BN, SPLIT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
-    uint8_t* sB = smem + C::STAGES * A_TILE;
+    uint8_t* sB = smem + C::STAGES * C::A_TILES;
     uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_TILE);
     uint64_t* empty = full + C::STAGES;
     uint64_t* accb = empty + C::STAGES;
@@ -104,9 +114,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             if (conv_C) {
                 const int tap = k0 / conv_C;
-                tma_load_3d(sA + s * A_TILE, &tmA, k0 - tap * conv_C, tap & 1, m0 + (tap >> 1), &full[s]);
+                tma_load_3d(sA + s * C::A_TILES, &tmA, k0 - tap * conv_C, tap & 1, m0 + (tap >> 1), &full[s]);
             } else {
-                tma_load_2d(sA + s * A_TILE, &tmA, k0, m0, &full[s]);
+                tma_load_2d(sA + s * C::A_TILES, &tmA, k0, m0, &full[s]);
+                if (SPLIT) tma_load_2d(sA + s * C::A_TILES + A_TILE, &tmA, K + k0, m0, &full[s]);
             }
         }
     } else if (warp == 1 && lane == 0) {
@@ -116,12 +127,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint32_t ph = (kb / C::STAGES) & 1;
             if (!mbar_wait(&full[s], ph)) { ok = false; break; }
             tc_fence_after();
-            const uint64_t ad = sdesc_k_sw128(sA + s * A_TILE);
+            const uint64_t ad = sdesc_k_sw128(sA + s * C::A_TILES);
             const uint64_t bd = sdesc_k_sw128(sB + s * C::B_TILE);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
                 // +32 bytes along K inside the swizzle atom = +2 in the encoded start address
                 tc_mma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+            }
+            if (SPLIT) {
+                const uint64_t al = sdesc_k_sw128(sA + s * C::A_TILES + A_TILE);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) tc_mma_bf16(tmem, al + 2 * kk, bd + 2 * kk, idesc, 1u);
             }
             tc_commit(&empty[s]);
         }
@@ -219,11 +235,11 @@ bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t 
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, int KIND>
+template <int BN, int KIND, int SPLIT>
 static cudaError_t launch_bn_kind(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int conv_C,
                                   int splits, const EpiParams& ep, int* status, cudaStream_t s) {
-    using C = TcCfg<BN>;
-    auto kern = gemm_tc_kernel<BN, KIND, bf16>;
+    using C = TcCfg<BN, SPLIT>;
+    auto kern = gemm_tc_kernel<BN, KIND, bf16, SPLIT>;
     static bool attr_set = false;  // per instantiation, per process
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -236,27 +252,37 @@ static cudaError_t launch_bn_kind(const CUtensorMap* tmA, const CUtensorMap* tmB
 
 template <int BN>
 static cudaError_t launch_bn(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int cc, int sp,
-                             const EpiParams& ep, int* status, cudaStream_t s) {
+                             int a_split, const EpiParams& ep, int* status, cudaStream_t s) {
+    if (a_split) {
+        // split operands come from LayerNorm outputs and the attention output
+        switch (ep.kind) {
+            case EPI_STORE: return launch_bn_kind<BN, EPI_STORE, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+            case EPI_RESID: return launch_bn_kind<BN, EPI_RESID, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+            case EPI_GLU: return launch_bn_kind<BN, EPI_GLU, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+            case EPI_QKV: return launch_bn_kind<BN, EPI_QKV, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+        }
+        return cudaErrorInvalidValue;
+    }
     switch (ep.kind) {
-        case EPI_STORE: return launch_bn_kind<BN, EPI_STORE>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
-        case EPI_RESID: return launch_bn_kind<BN, EPI_RESID>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
-        case EPI_GLU: return launch_bn_kind<BN, EPI_GLU>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
-        case EPI_QKV: return launch_bn_kind<BN, EPI_QKV>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
-        case EPI_SUB: return launch_bn_kind<BN, EPI_SUB>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+        case EPI_STORE: return launch_bn_kind<BN, EPI_STORE, 0>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+        case EPI_RESID: return launch_bn_kind<BN, EPI_RESID, 0>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+        case EPI_GLU: return launch_bn_kind<BN, EPI_GLU, 0>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+        case EPI_QKV: return launch_bn_kind<BN, EPI_QKV, 0>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+        case EPI_SUB: return launch_bn_kind<BN, EPI_SUB, 0>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
     }
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int BN, int conv_C,
-                           int splits, const EpiParams& ep, int* status, cudaStream_t s) {
+                           int splits, int a_split, const EpiParams& ep, int* status, cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
     if (K % BK || K <= 0 || N % BN || !ep.act_bf16) return cudaErrorInvalidValue;
-    if (conv_C && (conv_C % BK || K != 3 * conv_C)) return cudaErrorInvalidValue;
+    if (conv_C && (conv_C % BK || K != 3 * conv_C || a_split)) return cudaErrorInvalidValue;
     if (splits < 1 || splits > 4 || splits > K / BK) return cudaErrorInvalidValue;
     switch (BN) {
-        case 64: return launch_bn<64>(tmA, tmB, M, N, K, conv_C, splits, ep, status, s);
-        case 128: return launch_bn<128>(tmA, tmB, M, N, K, conv_C, splits, ep, status, s);
-        case 256: return launch_bn<256>(tmA, tmB, M, N, K, conv_C, splits, ep, status, s);
+        case 64: return launch_bn<64>(tmA, tmB, M, N, K, conv_C, splits, a_split, ep, status, s);
+        case 128: return launch_bn<128>(tmA, tmB, M, N, K, conv_C, splits, a_split, ep, status, s);
+        case 256: return launch_bn<256>(tmA, tmB, M, N, K, conv_C, splits, a_split, ep, status, s);
     }
     return cudaErrorInvalidValue;
 }

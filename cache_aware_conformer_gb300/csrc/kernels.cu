@@ -39,10 +39,30 @@ __device__ __forceinline__ void ln_row(float (&v)[VPL], int lane, int D, const f
     }
 }
 
+// Activation-dtype row store; split (bf16 only): row stride 2D, the bf16
+// rounding hi = bf16(v) in columns [0, D) and the residual lo = bf16(v - hi) in
+// [D, 2D), so that hi + lo carries v to about 16 significant bits.
+template <int VPL, class TA>
+__device__ __forceinline__ void store_act_row(TA* dst, long long row, int D, int lane, const float (&v)[VPL],
+                                              int split) {
+    if (split) {
+        TA* d = dst + row * 2 * D;
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) {
+            const TA hi = from_f<TA>(v[k]);
+            d[lane + 32 * k] = hi;
+            d[D + lane + 32 * k] = from_f<TA>(v[k] - to_f(hi));
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < VPL; ++k) dst[row * D + lane + 32 * k] = from_f<TA>(v[k]);
+    }
+}
+
 template <int VPL, class TA>
 __global__ void __launch_bounds__(256) ln_kernel(const float* x, int M, int D, const float* g1, const float* b1,
                                                  float* y_f32, TA* y_act, const float* g2, const float* b2,
-                                                 TA* z_act, int grp, int grp_stride, int row_off) {
+                                                 TA* z_act, int grp, int grp_stride, int row_off, int split) {
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -57,28 +77,24 @@ __global__ void __launch_bounds__(256) ln_kernel(const float* x, int M, int D, c
 #pragma unroll
         for (int k = 0; k < VPL; ++k) y_f32[orow * D + lane + 32 * k] = v[k];
     }
-    if (y_act) {
-#pragma unroll
-        for (int k = 0; k < VPL; ++k) y_act[(long long)row * D + lane + 32 * k] = from_f<TA>(v[k]);
-    }
+    if (y_act) store_act_row<VPL, TA>(y_act, row, D, lane, v, split);
     if (g2) {
         ln_row<VPL>(v, lane, D, g2, b2);
-#pragma unroll
-        for (int k = 0; k < VPL; ++k) z_act[(long long)row * D + lane + 32 * k] = from_f<TA>(v[k]);
+        store_act_row<VPL, TA>(z_act, row, D, lane, v, split);
     }
 }
 
 template <class TA>
 static cudaError_t ln_dispatch(const float* x, int M, int D, const float* g1, const float* b1, float* y_f32,
                                void* y_act, const float* g2, const float* b2, void* z_act, int grp, int grp_stride,
-                               int row_off, cudaStream_t s) {
+                               int row_off, int split, cudaStream_t s) {
     dim3 grid((M + 7) / 8);
     TA* ya = static_cast<TA*>(y_act);
     TA* za = static_cast<TA*>(z_act);
 #define LN_CASE(V)                                                                                       \
     case V:                                                                                              \
         return launch_k(ln_kernel<V, TA>, grid, dim3(256), 0, s, 1, x, M, D, g1, b1, y_f32, ya, g2, b2, za, grp,   \
-                        grp_stride, row_off);
+                        grp_stride, row_off, split);
     switch (D / 32) {
         LN_CASE(2) LN_CASE(4) LN_CASE(8) LN_CASE(16) LN_CASE(24) LN_CASE(32)
         default: return cudaErrorInvalidValue;
@@ -88,11 +104,12 @@ static cudaError_t ln_dispatch(const float* x, int M, int D, const float* g1, co
 
 cudaError_t launch_layernorm(const float* x, int M, int D, const float* g1, const float* b1, float* y_f32,
                              void* y_act, const float* g2, const float* b2, void* z_act, int act_bf16, int grp,
-                             int grp_stride, int row_off, cudaStream_t s) {
+                             int grp_stride, int row_off, int split, cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
-    if (D % 32) return cudaErrorInvalidValue;
-    return act_bf16 ? ln_dispatch<bf16>(x, M, D, g1, b1, y_f32, y_act, g2, b2, z_act, grp, grp_stride, row_off, s)
-                    : ln_dispatch<float>(x, M, D, g1, b1, y_f32, y_act, g2, b2, z_act, grp, grp_stride, row_off, s);
+    if (D % 32 || (split && !act_bf16)) return cudaErrorInvalidValue;
+    return act_bf16
+               ? ln_dispatch<bf16>(x, M, D, g1, b1, y_f32, y_act, g2, b2, z_act, grp, grp_stride, row_off, split, s)
+               : ln_dispatch<float>(x, M, D, g1, b1, y_f32, y_act, g2, b2, z_act, grp, grp_stride, row_off, 0, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -251,6 +268,19 @@ __device__ __forceinline__ void st_chunk(float* p, const float (&f)[EPC]) {
     static_assert(EPC == 4, "fp32 chunk");
     *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
 }
+// hi chunk at p and, when lo_off > 0 (bf16 only), the rounding residual at p + lo_off
+template <int EPC, class T>
+__device__ __forceinline__ void st_out(T* p, int lo_off, const float (&f)[EPC]) {
+    st_chunk<EPC>(p, f);
+    if constexpr (sizeof(T) == 2) {
+        if (lo_off > 0) {
+            float r[EPC];
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) r[e] = f[e] - __bfloat162float(__float2bfloat16_rn(f[e]));
+            st_chunk<EPC>(p + lo_off, r);
+        }
+    }
+}
 
 // V rows of one unit: a ring of R slots starting at slot s0 (streaming), or
 // dense rows with stride ld (offline).
@@ -391,7 +421,7 @@ __device__ void attend(const AttnParams& a, int h, const T* Ps, uint64_t* pbar, 
         for (int e = 0; e < EPC; ++e)
 #pragma unroll
             for (int o = LPK; o < 32; o <<= 1) acc[t][e] += __shfl_xor_sync(0xffffffffu, acc[t][e], o);
-        if (g == 0) st_chunk<EPC>(dst + (long long)i * a.ldo + d0, acc[t]);
+        if (g == 0) st_out<EPC>(dst + (long long)i * a.ldo + d0, a.out_split, acc[t]);
     }
 }
 
@@ -682,7 +712,7 @@ __global__ void x0_gather_kernel(const float* x0, float* x, const int* ids, cons
 
 template <class T>
 __global__ void emit_rows_kernel(const float* x, const T* act_src, float* dst, T* act_dst, const int* map, int nb,
-                                 int P, int E, int out_bstride, int out_off, int D) {
+                                 int P, int E, int D) {
     pdl_wait();
     const long long total = (long long)nb * E * D;
     for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
@@ -691,7 +721,7 @@ __global__ void emit_rows_kernel(const float* x, const T* act_src, float* dst, T
         const long long r = e / D;
         const int b = (int)(r / E), i = (int)(r % E);
         const long long src = ((long long)b * P + i) * D + c;
-        if (dst) dst[((long long)map[b] * out_bstride + out_off + i) * D + c] = x[src];
+        if (dst) dst[((long long)map[b] + i) * D + c] = x[src];
         act_dst[r * D + c] = act_src[src];
     }
 }
@@ -711,14 +741,14 @@ cudaError_t launch_x0_gather(const float* x0, float* x, const int* ids, const in
                     nb, P, XC, D);
 }
 cudaError_t launch_emit_rows(const float* x, const void* act_src, float* dst, void* act_dst, const int* map, int nb,
-                             int P, int E, int out_bstride, int out_off, int D, int act_bf16, cudaStream_t s) {
+                             int P, int E, int D, int act_bf16, cudaStream_t s) {
     if (nb <= 0 || E <= 0) return cudaSuccess;
     const dim3 g(grid_for((long long)nb * E * D));
     if (act_bf16)
         return launch_k(emit_rows_kernel<bf16>, g, dim3(256), 0, s, 1, x, static_cast<const bf16*>(act_src), dst,
-                        static_cast<bf16*>(act_dst), map, nb, P, E, out_bstride, out_off, D);
+                        static_cast<bf16*>(act_dst), map, nb, P, E, D);
     return launch_k(emit_rows_kernel<float>, g, dim3(256), 0, s, 1, x, static_cast<const float*>(act_src), dst,
-                    static_cast<float*>(act_dst), map, nb, P, E, out_bstride, out_off, D);
+                    static_cast<float*>(act_dst), map, nb, P, E, D);
 }
 
 // ---------------------------------------------------------------------------
@@ -767,6 +797,23 @@ __global__ void to_f32_kernel(const T* src, float* dst, long long n) {
     pdl_wait();
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
         dst[i] = to_f(src[i]);
+}
+
+__global__ void split_to_f32_kernel(const bf16* src, float* dst, int rows, int D) {
+    pdl_wait();
+    const long long n = (long long)rows * D;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const long long r = i / D, c = i - r * D;
+        dst[i] = __bfloat162float(src[r * 2 * D + c]) + __bfloat162float(src[r * 2 * D + D + c]);
+    }
+}
+
+cudaError_t launch_split_to_f32(const void* src, float* dst, int rows, int D, cudaStream_t s) {
+    const long long n = (long long)rows * D;
+    if (n <= 0) return cudaSuccess;
+    const int blocks = (int)std::min<long long>((n + 255) / 256, 152 * 16);
+    split_to_f32_kernel<<<blocks, 256, 0, s>>>(static_cast<const bf16*>(src), dst, rows, D);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_to_f32(const void* src, float* dst, long long n, int src_bf16, cudaStream_t s) {

@@ -8,10 +8,12 @@ namespace cac {
 // LayerNorm over rows of D (eps 1e-5).  y = LN(x; g1, b1) goes to y_f32
 // (row r written at (r / grp) * grp_stride + r % grp + row_off; may alias x
 // when the remap is the identity) and/or y_act; when g2 is set, z = LN(y; g2,
-// b2) goes to z_act.  act buffers are bf16 when act_bf16, else fp32.
+// b2) goes to z_act.  act buffers are bf16 when act_bf16, else fp32, with row
+// stride D; split (bf16 only) writes them as split operands instead: row
+// stride 2D, hi = bf16(v) in columns [0, D), lo = bf16(v - hi) in [D, 2D).
 cudaError_t launch_layernorm(const float* x, int M, int D, const float* g1, const float* b1, float* y_f32,
                              void* y_act, const float* g2, const float* b2, void* z_act, int act_bf16, int grp,
-                             int grp_stride, int row_off, cudaStream_t s);
+                             int grp_stride, int row_off, int split, cudaStream_t s);
 
 // Mel staging: window[b] = [melTail(id) | mel[b]] (14 + 8n rows; tail rows are
 // zero when pos[id] == 0), then melTail(id) = last 14 window rows.  mel rows of
@@ -42,6 +44,8 @@ struct AttnParams {
     const float* pbv = nullptr;
     void* out = nullptr;        // [rows][ldo], activation dtype
     int ldo = 0;
+    int out_split = 0;          // bf16 only, > 0: also write lo = bf16(o - hi) at column out_split + c
+                                // (a split operand for the out-projection; ldo >= 2 * out_split)
     int H = 0, D = 0, HD = 0;
     int left = 0, chunk = 1, rc = 0;  // rc > 0: window mask [p-left, p+rc]; else chunked mask
     int nb = 0;                 // streaming: batch slots; offline: sequences
@@ -67,14 +71,14 @@ cudaError_t launch_dwconv(const void* glu, void* cache, long long cs_stride, con
 // in a per-stream ring x0[id][XC][D] (fp32), slot = absolute frame mod XC.
 // store:  x0[id][(pos[id] + i) % XC] = x[b * n + i]            (i < n)
 // gather: x[b * P + i] = x0[id][(pos[id] + i) % XC]            (i < P)
-// emit:   dst[map[b] * out_bstride + out_off + i] = x[b * P + i] and
+// emit:   dst[map[b] + i] = x[b * P + i] (map[b] = output row of the first) and
 //         act_dst[b * E + i] = act_src[b * P + i]              (i < E)
 cudaError_t launch_x0_store(const float* x, float* x0, const int* ids, const int* pos, int nb, int n, int XC, int D,
                             cudaStream_t s);
 cudaError_t launch_x0_gather(const float* x0, float* x, const int* ids, const int* pos, int nb, int P, int XC, int D,
                              cudaStream_t s);
 cudaError_t launch_emit_rows(const float* x, const void* act_src, float* dst, void* act_dst, const int* map, int nb,
-                             int P, int E, int out_bstride, int out_off, int D, int act_bf16, cudaStream_t s);
+                             int P, int E, int D, int act_bf16, cudaStream_t s);
 
 // pos[ids[b]] += n  /  pos[ids[b]] = value
 cudaError_t launch_advance(int* pos, const int* ids, int nb, int n, cudaStream_t s);
@@ -85,5 +89,7 @@ cudaError_t launch_sinusoid(float* pe, int NR, int rmin, int D, cudaStream_t s);
 
 // dst fp32 [n] <- src (bf16 or fp32) [n]
 cudaError_t launch_to_f32(const void* src, float* dst, long long n, int src_bf16, cudaStream_t s);
+// dst[r][c] = hi[r][c] + lo[r][c] of a bf16 split operand [rows][2D]
+cudaError_t launch_split_to_f32(const void* src, float* dst, int rows, int D, cudaStream_t s);
 
 }  // namespace cac

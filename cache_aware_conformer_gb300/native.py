@@ -88,7 +88,7 @@ def _lib():
             "cac_profile_classes": (c_int, []),
             "cac_profile_class_name": (c_char_p, [c_int]),
             "cac_strerror": (c_char_p, [c_int]),
-            "cac_op_gemm_bf16": (c_int, [c_int, c_int, c_int, vp, vp, vp, vp, c_int, vp]),
+            "cac_op_gemm_bf16": (c_int, [c_int, c_int, c_int, vp, vp, vp, vp, c_int, c_int, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -132,14 +132,17 @@ def _stream(stream=None) -> int | None:
     return s.cuda_stream
 
 
-def gemm_bf16(A, B, bias=None, splits: int = 0, out=None, stream=None):
-    """C = A @ B^T (+ bias) on the tcgen05 GEMM (cac_op_gemm_bf16); A [M,K], B [N,K] bf16 cuda."""
+def gemm_bf16(A, B, bias=None, splits: int = 0, out=None, stream=None, split: bool = False):
+    """C = A @ B^T (+ bias) on the tcgen05 GEMM (cac_op_gemm_bf16); A [M,K], B [N,K] bf16 cuda.
+    split: A is [M, 2K] = [hi | lo] and the product is (hi + lo) @ B^T."""
     import torch
     M, K = A.shape
+    if split:
+        K //= 2
     N = B.shape[0]
     C = out if out is not None else torch.empty(M, N, device=A.device, dtype=torch.float32)
-    _check(_lib().cac_op_gemm_bf16(M, N, K, _ptr(A), _ptr(B), _ptr(bias), _ptr(C), splits, _stream(stream)),
-           "cac_op_gemm_bf16")
+    _check(_lib().cac_op_gemm_bf16(M, N, K, _ptr(A), _ptr(B), _ptr(bias), _ptr(C), splits, int(split),
+                                   _stream(stream)), "cac_op_gemm_bf16")
     return C
 
 
@@ -260,13 +263,20 @@ class Pool:
                                            n_out, _stream(stream)), "cac_stream_push_host")
         return enc, jt, list(n_out)
 
+    def flush_frames(self, sid: int, n_mel: int) -> int:
+        """Frames a flush of `n_mel` remaining mel frames emits for stream `sid`
+        (held-back provisional frames included)."""
+        f = c_int(0)
+        _check(_lib().cac_stream_flush_frames(self.h, sid, n_mel, ctypes.byref(f)), "cac_stream_flush_frames")
+        return f.value
+
     def flush(self, ids, mel, n_mel_each, joint: bool = True, stream=None):
         """mel: cuda float32 [n, mel_stride, 128] (or None when all n_mel_each are 0)."""
         import torch
         ids = list(ids)
         n = len(ids)
         mel_stride = 0 if mel is None else mel.shape[1]
-        out_stride = max(1, max((m + 7) // 8 for m in n_mel_each))
+        out_stride = max([1] + [self.flush_frames(i, m) for i, m in zip(ids, n_mel_each)])
         dev = mel.device if mel is not None else torch.device("cuda")
         enc = torch.zeros(n, out_stride, self.cfg.d_model, device=dev, dtype=torch.float32)
         jt = torch.zeros(n, out_stride, self.cfg.joint_dim, device=dev, dtype=torch.float32) if joint else None

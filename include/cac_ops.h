@@ -19,9 +19,13 @@ extern "C" {
  * encode", §Per-chunk flow step 3).  A and B bf16, row-major (K contiguous);
  * C fp32 row-major; bias fp32 or NULL.  K % 64 == 0, N % 64 == 0, M >= 1;
  * 16-byte aligned pointers.  splits: 1..4 K-splits per output tile (reduced
- * in a thread-block cluster), 0 = the library's choice. */
+ * in a thread-block cluster), 0 = the library's choice.
+ * a_split != 0: A is a split operand [M][2K] — row r holds hi[r][0..K) then
+ * lo[r][0..K), two bf16 terms of one higher-precision activation — and the
+ * product is (hi + lo) * B^T (the form in which the encoder's LayerNorm
+ * outputs enter their projections). */
 int cac_op_gemm_bf16(int M, int N, int K, const void* A, const void* B, const float* bias, float* C, int splits,
-                     void* stream);
+                     int a_split, void* stream);
 
 #ifdef __cplusplus
 }

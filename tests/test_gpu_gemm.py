@@ -42,3 +42,23 @@ def test_gemm_rejects_bad_shapes():
     A = torch.zeros(4, 96, device="cuda", dtype=torch.bfloat16)
     with pytest.raises(native.CacError):
         native.gemm_bf16(A, torch.zeros(64, 96, device="cuda", dtype=torch.bfloat16))   # K % 64
+
+
+@pytest.mark.parametrize("M,N,K", [(130, 128, 192), (512, 2048, 512), (512, 512, 2048)])
+@pytest.mark.parametrize("splits", [1, 2])
+def test_split_operand_gemm(M, N, K, splits):
+    """A split operand [hi | lo] enters the product as hi + lo: exact against
+    fp64 of (hi + lo), and far closer to the fp32 activation than hi alone."""
+    from cache_aware_conformer_gb300 import native
+    g = torch.Generator().manual_seed(M + 5 * N + 11 * K)
+    X = torch.randn(M, K, generator=g)
+    hi = X.to(torch.bfloat16)
+    lo = (X - hi.float()).to(torch.bfloat16)
+    B = (torch.randn(N, K, generator=g) / 8).to(torch.bfloat16)
+    Bd = B.cuda()
+    C = native.gemm_bf16(torch.cat([hi, lo], dim=1).cuda(), Bd, splits=splits, split=True).cpu().double()
+    C1 = native.gemm_bf16(hi.cuda(), Bd, splits=splits).cpu().double()
+    ref_pair = (hi.double() + lo.double()) @ B.double().T
+    assert (C - ref_pair).abs().max().item() <= 2e-6 * np.sqrt(K) * ref_pair.abs().max().item() + 1e-6
+    ref_x = X.double() @ B.double().T
+    assert (C - ref_x).abs().max().item() < (C1 - ref_x).abs().max().item() / 20
