@@ -197,17 +197,17 @@ int choose_splits(int tiles, int nk) {
 int gemm(cac_model* m, const void* A, long long lda, int M, int K, const Lin& W, int conv_C, EpiParams ep,
          cudaStream_t s, long long* launches, int a_split = 0) {
     if (M <= 0) return CAC_OK;
-    if (a_split && lda < 2LL * K) return CAC_E_INVAL;
+    if (a_split && !conv_C && lda < 2LL * K) return CAC_E_INVAL;
     ep.act_bf16 = m->bf16;
     if (m->tc) {
         CUtensorMap tmA;
-        const bool ok = conv_C ? make_tmap_bf16_conv(&tmA, A, conv_C, (uint64_t)M + 1, 128)
+        const bool ok = conv_C ? make_tmap_bf16_conv(&tmA, A, (uint64_t)conv_C * (a_split ? 2 : 1), (uint64_t)M + 1, 128)
                                : make_tmap_bf16(&tmA, A, a_split ? 2 * K : K, M, (uint64_t)lda * 2, 128);
         if (!ok) return CAC_E_CUDA;
         const int splits = choose_splits((W.N / W.BN) * ((M + 127) / 128), K / 64);
         CK(launch_gemm_tc(&tmA, &W.tm, M, W.N, K, W.BN, conv_C, splits, a_split, ep, m->status, s));
     } else {
-        CK(launch_gemm_simt(m->bf16, A, lda, W.w, K, M, W.N, K, a_split, ep, s));
+        CK(launch_gemm_simt(m->bf16, A, lda, W.w, K, M, W.N, K, conv_C, a_split, ep, s));
     }
     ++*launches;
     return CAC_OK;
@@ -336,7 +336,7 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
             ep.act_bf16 = 0;
             ep.out_f32 = Lw.P;
             ep.ldo = D;
-            if (launch_gemm_simt(0, pe, D, wpos_d, D, m->NR, D, D, 0, ep, 0) != cudaSuccess) return fail(CAC_E_CUDA);
+            if (launch_gemm_simt(0, pe, D, wpos_d, D, m->NR, D, D, 0, 0, ep, 0) != cudaSuccess) return fail(CAC_E_CUDA);
             // head-major copy [H][NR][HD] in the activation dtype: one bulk copy per
             // (block, head) in the attention kernels
             std::vector<float> hp((size_t)m->NR * D), pad((size_t)H * m->NR * HD, 0.f);
@@ -437,7 +437,7 @@ struct cac_pool {
     std::vector<void*> allocs;
     // per-stream device state
     int* pos = nullptr;        // subsampled frames consumed
-    void* tail = nullptr;      // [S][14][128]
+    float* tail = nullptr;     // [S][14][128] fp32
     void* kring = nullptr;     // [S][L][H][R][HD]
     void* vring = nullptr;
     void* conv = nullptr;      // [S][L][8][D]
@@ -577,11 +577,12 @@ int run_subsample(cac_pool* p, int nb, int n, const float* mel, long long mel_bs
     const int D = m->D;
     const int M = nb * n;
     long long* lc = &p->launches;
-    const int bf = m->bf16;
+    const int bf = m->bf16, sp = m->split;
+    const int rwm = MEL * (1 + sp), rwd = D * (1 + sp);  // window row widths (split: hi | lo)
 
     // 1. mel staging: [melTail | mel] windows, tail update
     PB(P_STAGE);
-    CK(launch_stage_mel(mel, mel_bstride, nvalid, p->win1, p->tail, ids, posS, n, nb, bf, p->status, s));
+    CK(launch_stage_mel(mel, mel_bstride, nvalid, p->win1, p->tail, ids, posS, n, nb, bf, sp, p->status, s));
     PE();
     ++*lc;
     // 2. three stride-2 convolutions (implicit GEMMs over the windows) + out linear
@@ -591,24 +592,25 @@ int run_subsample(cac_pool* p, int nb, int n, const float* mel, long long mel_bs
         ep.kind = EPI_SUB;
         ep.bias = m->sub1.b;
         ep.out_act = p->win2;
-        ep.ldo = D;
+        ep.ldo = rwd;
+        ep.split_out = sp ? D : 0;
         ep.ids = ids;
         ep.pos = posS;
         ep.P = W1 / 2; ep.T_out = W2; ep.dst_rows = W2; ep.dst_off = 0; ep.tmult = 4; ep.toff = 6;
         PB(P_SUB);
-        RET(gemm(m, p->win1, 2 * MEL, nb * (W1 / 2), 3 * MEL, m->sub1, MEL, ep, s, lc));
+        RET(gemm(m, p->win1, 2 * rwm, nb * (W1 / 2), 3 * MEL, m->sub1, MEL, ep, s, lc, sp));
         PE();
         ep.bias = m->sub2.b;
         ep.out_act = p->win3;
         ep.P = W2 / 2; ep.T_out = W3; ep.dst_rows = W3; ep.tmult = 2; ep.toff = 2;
         PB(P_SUB);
-        RET(gemm(m, p->win2, 2 * D, nb * (W2 / 2), 3 * D, m->sub2, D, ep, s, lc));
+        RET(gemm(m, p->win2, 2 * rwd, nb * (W2 / 2), 3 * D, m->sub2, D, ep, s, lc, sp));
         PE();
         ep.bias = m->sub3.b;
         ep.out_act = p->y3;
         ep.P = W3 / 2; ep.T_out = n; ep.dst_rows = n; ep.tmult = 1; ep.toff = 0;
         PB(P_SUB);
-        RET(gemm(m, p->win3, 2 * D, nb * (W3 / 2), 3 * D, m->sub3, D, ep, s, lc));
+        RET(gemm(m, p->win3, 2 * rwd, nb * (W3 / 2), 3 * D, m->sub3, D, ep, s, lc, sp));
         PE();
     }
     {
@@ -618,7 +620,7 @@ int run_subsample(cac_pool* p, int nb, int n, const float* mel, long long mel_bs
         ep.out_f32 = p->x;
         ep.ldo = D;
         PB(P_SUBOUT);
-        RET(gemm(m, p->y3, D, M, D, m->subo, 0, ep, s, lc));
+        RET(gemm(m, p->y3, rwd, M, D, m->subo, 0, ep, s, lc, sp));
         PE();
     }
     RET(trace_tap(p, 0, N_TAPS, p->x, false, M, s));
@@ -864,14 +866,16 @@ extern "C" int cac_pool_create(cac_model* m, int max_streams, int max_frames_per
     void* v;
     if ((r = palloc(p, sizeof(int) * S, &v)) != CAC_OK) return fail(r);
     p->pos = static_cast<int*>(v);
-    if ((r = palloc(p, ab * S * p->tail_elems, &p->tail)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, sizeof(float) * S * p->tail_elems, &v)) != CAC_OK) return fail(r);
+    p->tail = static_cast<float*>(v);
     if ((r = palloc(p, ab * S * p->ring_sstride, &p->kring)) != CAC_OK) return fail(r);
     if ((r = palloc(p, ab * S * p->ring_sstride, &p->vring)) != CAC_OK) return fail(r);
     if ((r = palloc(p, ab * S * p->conv_sstride, &p->conv)) != CAC_OK) return fail(r);
-    if ((r = palloc(p, ab * ((size_t)S * (TAIL + 8 * n) + 4) * MEL, &p->win1)) != CAC_OK) return fail(r);
-    if ((r = palloc(p, ab * ((size_t)S * (4 * n + 6) + 4) * D, &p->win2)) != CAC_OK) return fail(r);
-    if ((r = palloc(p, ab * ((size_t)S * (2 * n + 2) + 4) * D, &p->win3)) != CAC_OK) return fail(r);
-    if ((r = palloc(p, ab * rows_max * D, &p->y3)) != CAC_OK) return fail(r);
+    const size_t wsp = m->split ? 2 : 1;  // split windows: rows hi | lo
+    if ((r = palloc(p, wsp * ab * ((size_t)S * (TAIL + 8 * n) + 4) * MEL, &p->win1)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, wsp * ab * ((size_t)S * (4 * n + 6) + 4) * D, &p->win2)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, wsp * ab * ((size_t)S * (2 * n + 2) + 4) * D, &p->win3)) != CAC_OK) return fail(r);
+    if ((r = palloc(p, wsp * ab * rows_max * D, &p->y3)) != CAC_OK) return fail(r);
     if ((r = palloc(p, 4 * rows_max * D, &v)) != CAC_OK) return fail(r);
     p->x = static_cast<float*>(v);
     if ((r = palloc(p, ab * rows_max * D * (m->split ? 2 : 1), &p->xln)) != CAC_OK) return fail(r);
@@ -1266,10 +1270,11 @@ OfflineLayout offline_layout(const cac_model* m, int B, int t_mel_max) {
         off += (bytes + 255) & ~size_t(255);
         return o;
     };
-    y.o_win1 = take(ab * ((size_t)B * y.W1 + 4) * MEL);
-    y.o_win2 = take(ab * ((size_t)B * y.W2 + 4) * D);
-    y.o_win3 = take(ab * ((size_t)B * y.W3 + 4) * D);
-    y.o_y3 = take(ab * M * D);
+    const size_t wsp = m->split ? 2 : 1;  // split windows: rows hi | lo
+    y.o_win1 = take(wsp * ab * ((size_t)B * y.W1 + 4) * MEL);
+    y.o_win2 = take(wsp * ab * ((size_t)B * y.W2 + 4) * D);
+    y.o_win3 = take(wsp * ab * ((size_t)B * y.W3 + 4) * D);
+    y.o_y3 = take(wsp * ab * M * D);
     y.o_x = take(4 * M * D);
     y.o_xln = take(ab * M * D * (m->split ? 2 : 1));
     y.o_h = take(ab * M * F);
@@ -1322,27 +1327,28 @@ int offline_run(cac_model* m, char* w, const OfflineLayout& lay, int B, const fl
     CK(cudaMemcpyAsync(mlen_d, mel_len, sizeof(int) * B, cudaMemcpyHostToDevice, s));
     CK(cudaMemcpyAsync(flen_d, lens.data(), sizeof(int) * B, cudaMemcpyHostToDevice, s));
     CK(cudaStreamSynchronize(s));  // host length arrays must outlive the copies
-    CK(cudaMemsetAsync(win2, 0, ab * ((size_t)B * W2 + 4) * D, s));
-    CK(cudaMemsetAsync(win3, 0, ab * ((size_t)B * W3 + 4) * D, s));
-    CK(launch_stage_mel_offline(mel, t_mel_max, mlen_d, win1, W1, B, bf, m->status, s));
+    const int sp = m->split;
+    const int rwm = MEL * (1 + sp), rwd = D * (1 + sp);  // window row widths (split: hi | lo)
+    CK(cudaMemsetAsync(win2, 0, ab * ((size_t)B * W2 + 4) * rwd, s));
+    CK(cudaMemsetAsync(win3, 0, ab * ((size_t)B * W3 + 4) * rwd, s));
+    CK(launch_stage_mel_offline(mel, t_mel_max, mlen_d, win1, W1, B, bf, sp, m->status, s));
     ++lc;
     {
         EpiParams ep;
         ep.kind = EPI_SUB;
-        ep.bias = m->sub1.b; ep.out_act = win2; ep.ldo = D;
+        ep.bias = m->sub1.b; ep.out_act = win2; ep.ldo = rwd; ep.split_out = sp ? D : 0;
         ep.P = W1 / 2; ep.T_out = T1; ep.dst_rows = W2; ep.dst_off = 2;
-        RET(gemm(m, win1, 2 * MEL, B * (W1 / 2), 3 * MEL, m->sub1, MEL, ep, s, &lc));
+        RET(gemm(m, win1, 2 * rwm, B * (W1 / 2), 3 * MEL, m->sub1, MEL, ep, s, &lc, sp));
         ep.bias = m->sub2.b; ep.out_act = win3;
         ep.P = W2 / 2; ep.T_out = T2; ep.dst_rows = W3; ep.dst_off = 2;
-        RET(gemm(m, win2, 2 * D, B * (W2 / 2), 3 * D, m->sub2, D, ep, s, &lc));
+        RET(gemm(m, win2, 2 * rwd, B * (W2 / 2), 3 * D, m->sub2, D, ep, s, &lc, sp));
         ep.bias = m->sub3.b; ep.out_act = y3;
         ep.P = W3 / 2; ep.T_out = T3; ep.dst_rows = T3; ep.dst_off = 0;
-        RET(gemm(m, win3, 2 * D, B * (W3 / 2), 3 * D, m->sub3, D, ep, s, &lc));
+        RET(gemm(m, win3, 2 * rwd, B * (W3 / 2), 3 * D, m->sub3, D, ep, s, &lc, sp));
         EpiParams eo;
         eo.kind = EPI_STORE; eo.bias = m->subo.b; eo.out_f32 = x; eo.ldo = D;
-        RET(gemm(m, y3, D, (int)M, D, m->subo, 0, eo, s, &lc));
+        RET(gemm(m, y3, rwd, (int)M, D, m->subo, 0, eo, s, &lc, sp));
     }
-    const int sp = m->split;
     const long long ldl = sp ? 2LL * D : D;  // row stride of the split LayerNorm outputs in xln
     CK(launch_layernorm(x, (int)M, D, m->layers[0].ff1_g, m->layers[0].ff1_b, nullptr, xln, nullptr, nullptr, nullptr,
                         bf, 1 << 30, 0, 0, sp, s));
@@ -1506,13 +1512,11 @@ extern "C" int cac_stream_get_state(cac_pool* p, int id, cac_stream_state* st) {
     }
     std::vector<char> raw;
     if (st->mel_tail) {
-        raw.resize(ab * p->tail_elems);
-        CK(cudaMemcpy(raw.data(), static_cast<char*>(p->tail) + ab * p->tail_elems * id, raw.size(),
-                      cudaMemcpyDeviceToHost));
         if (pos == 0)
             std::fill(st->mel_tail, st->mel_tail + p->tail_elems, 0.f);
         else
-            act_to_host(m, raw.data(), st->mel_tail, p->tail_elems);
+            CK(cudaMemcpy(st->mel_tail, p->tail + p->tail_elems * id, sizeof(float) * p->tail_elems,
+                          cudaMemcpyDeviceToHost));
     }
     const size_t ring_layer = (size_t)H * R * HD;
     std::vector<float> ring(ring_layer);
@@ -1562,12 +1566,9 @@ extern "C" int cac_stream_set_state(cac_pool* p, int id, const cac_stream_state*
     const int pos = st->subT, Lc = std::min(pos, left);
     CK(cudaDeviceSynchronize());
     std::vector<char> raw;
-    if (st->mel_tail) {
-        raw.resize(ab * p->tail_elems);
-        host_to_act(m, st->mel_tail, raw.data(), p->tail_elems);
-        CK(cudaMemcpy(static_cast<char*>(p->tail) + ab * p->tail_elems * id, raw.data(), raw.size(),
+    if (st->mel_tail)
+        CK(cudaMemcpy(p->tail + p->tail_elems * id, st->mel_tail, sizeof(float) * p->tail_elems,
                       cudaMemcpyHostToDevice));
-    }
     const size_t ring_layer = (size_t)H * R * HD;
     std::vector<float> ring(ring_layer, 0.f);
     for (int kv = 0; kv < 2; ++kv) {

@@ -55,6 +55,7 @@ struct EpiParams {
     int T_out = 1;               // valid outputs per group (the rest are seams between groups)
     int dst_rows = 1, dst_off = 0;
     int tmult = 0, toff = 0;     // absolute time = tmult * pos[id] - toff + t (zeroed when < 0)
+    int split_out = 0;           // bf16 only, > 0: also store lo = bf16(v - hi) at column split_out + c
 };
 
 // host helpers ---------------------------------------------------------------
@@ -69,7 +70,8 @@ bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t 
 bool make_tmap_bf16_conv(CUtensorMap* tm, const void* base, uint64_t C, uint64_t pairs, uint32_t box_rows);
 
 // tcgen05/TMEM GEMM, bf16 operands.  K % 64 == 0, N % BN == 0, BN in {64, 128, 256}.
-// conv_C > 0 selects the convolution view of A (tmA from make_tmap_bf16_conv, K = 3 * conv_C).
+// conv_C > 0 selects the convolution view of A (tmA from make_tmap_bf16_conv, K = 3 * conv_C;
+// with a_split the window rows are 2 * conv_C wide, hi | lo).
 // splits in 1..4: split-K over a cluster of `splits` CTAs per output tile,
 // reduced deterministically through distributed shared memory.
 // a_split: A is a split operand [M][2K] (hi in columns [0, K), lo = residual of
@@ -79,8 +81,11 @@ cudaError_t launch_gemm_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, int M
 
 // SIMT GEMM (fp32 or bf16 operands, fp32 accumulate).  N % 32 == 0.  a_split
 // (bf16 only): A row r holds hi at A + r * lda and lo at A + r * lda + K.
+// conv_C > 0: A is a stride-2 convolution window (lda = row-pair stride), K
+// index k * conv_C + c reads channel c of window row 2r + k; window rows are
+// conv_C wide, or 2 * conv_C (hi | lo) with a_split.
 cudaError_t launch_gemm_simt(int bf16_operands, const void* A, long long lda, const void* B, long long ldb, int M,
-                             int N, int K, int a_split, const EpiParams& ep, cudaStream_t s);
+                             int N, int K, int conv_C, int a_split, const EpiParams& ep, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // epilogue, applied to one row segment of 32 accumulators
@@ -203,8 +208,13 @@ __device__ __forceinline__ void epilogue32(const EpiParams& e, int row, int col0
         if (e.ids) zero = (e.tmult * e.pos[e.ids[g]] - e.toff + t) < 0;
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = zero ? 0.f : fmaxf(v[i], 0.f);
-        store32<TAct>(reinterpret_cast<TAct*>(e.out_act) + ((long long)g * e.dst_rows + e.dst_off + t) * e.ldo + col0,
-                      v);
+        TAct* dst = reinterpret_cast<TAct*>(e.out_act) + ((long long)g * e.dst_rows + e.dst_off + t) * e.ldo + col0;
+        store32<TAct>(dst, v);
+        if (e.split_out > 0) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] -= to_f(from_f<TAct>(v[i]));
+            store32<TAct>(dst + e.split_out, v);
+        }
     }
 }
 

@@ -11,7 +11,7 @@ namespace cac {
 template <class TA, int KIND, class TAct>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const TA* __restrict__ A, long long lda,
                                                         const TA* __restrict__ B, long long ldb, int M, int N,
-                                                        int K, int a_split, EpiParams ep) {
+                                                        int K, int conv_C, int a_split, EpiParams ep) {
     __shared__ float As[16][64 + 4];
     __shared__ float Bs[16][64 + 4];
     __shared__ float Cs[64][64 + 1];
@@ -25,9 +25,21 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const TA* __restrict__ A
         for (int j = 0; j < 4; ++j) {
             const int e = tid * 4 + j, r = e >> 4, kk = e & 15;
             const int gm = m0 + r, gn = n0 + r, gk = k0 + kk;
-            As[kk][r] = (gm < M && gk < K)
-                            ? to_f(A[(long long)gm * lda + gk]) + (a_split ? to_f(A[(long long)gm * lda + K + gk]) : 0.f)
-                            : 0.f;
+            float av = 0.f;
+            if (gm < M && gk < K) {
+                long long off;
+                int lo;
+                if (conv_C) {
+                    const int tap = gk / conv_C;
+                    off = (long long)gm * lda + (long long)tap * conv_C * (1 + a_split) + (gk - tap * conv_C);
+                    lo = conv_C;
+                } else {
+                    off = (long long)gm * lda + gk;
+                    lo = K;
+                }
+                av = to_f(A[off]) + (a_split ? to_f(A[off + lo]) : 0.f);
+            }
+            As[kk][r] = av;
             Bs[kk][r] = (gn < N && gk < K) ? to_f(B[(long long)gn * ldb + gk]) : 0.f;
         }
         __syncthreads();
@@ -64,27 +76,27 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const TA* __restrict__ A
 
 template <class TA, class TAct>
 static cudaError_t launch_t(const void* A, long long lda, const void* B, long long ldb, int M, int N, int K,
-                           int sp, const EpiParams& ep, cudaStream_t s) {
+                           int cc, int sp, const EpiParams& ep, cudaStream_t s) {
     dim3 grid((N + 63) / 64, (M + 63) / 64);
     const TA* a = static_cast<const TA*>(A);
     const TA* b = static_cast<const TA*>(B);
     switch (ep.kind) {
-        case EPI_STORE: return launch_k(gemm_simt_kernel<TA, EPI_STORE, TAct>, grid, dim3(256), 0, s, 1, a, lda, b, ldb, M, N, K, sp, ep);
-        case EPI_RESID: return launch_k(gemm_simt_kernel<TA, EPI_RESID, TAct>, grid, dim3(256), 0, s, 1, a, lda, b, ldb, M, N, K, sp, ep);
-        case EPI_GLU: return launch_k(gemm_simt_kernel<TA, EPI_GLU, TAct>, grid, dim3(256), 0, s, 1, a, lda, b, ldb, M, N, K, sp, ep);
-        case EPI_QKV: return launch_k(gemm_simt_kernel<TA, EPI_QKV, TAct>, grid, dim3(256), 0, s, 1, a, lda, b, ldb, M, N, K, sp, ep);
-        case EPI_SUB: return launch_k(gemm_simt_kernel<TA, EPI_SUB, TAct>, grid, dim3(256), 0, s, 1, a, lda, b, ldb, M, N, K, sp, ep);
+        case EPI_STORE: return launch_k(gemm_simt_kernel<TA, EPI_STORE, TAct>, grid, dim3(256), 0, s, 1, a, lda, b, ldb, M, N, K, cc, sp, ep);
+        case EPI_RESID: return launch_k(gemm_simt_kernel<TA, EPI_RESID, TAct>, grid, dim3(256), 0, s, 1, a, lda, b, ldb, M, N, K, cc, sp, ep);
+        case EPI_GLU: return launch_k(gemm_simt_kernel<TA, EPI_GLU, TAct>, grid, dim3(256), 0, s, 1, a, lda, b, ldb, M, N, K, cc, sp, ep);
+        case EPI_QKV: return launch_k(gemm_simt_kernel<TA, EPI_QKV, TAct>, grid, dim3(256), 0, s, 1, a, lda, b, ldb, M, N, K, cc, sp, ep);
+        case EPI_SUB: return launch_k(gemm_simt_kernel<TA, EPI_SUB, TAct>, grid, dim3(256), 0, s, 1, a, lda, b, ldb, M, N, K, cc, sp, ep);
     }
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm_simt(int bf16_operands, const void* A, long long lda, const void* B, long long ldb, int M,
-                             int N, int K, int a_split, const EpiParams& ep, cudaStream_t s) {
+                             int N, int K, int conv_C, int a_split, const EpiParams& ep, cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
-    if (N % 32) return cudaErrorInvalidValue;
-    if (bf16_operands) return launch_t<bf16, bf16>(A, lda, B, ldb, M, N, K, a_split, ep, s);
+    if (N % 32 || (conv_C && K != 3 * conv_C)) return cudaErrorInvalidValue;
+    if (bf16_operands) return launch_t<bf16, bf16>(A, lda, B, ldb, M, N, K, conv_C, a_split, ep, s);
     if (ep.act_bf16 || a_split) return cudaErrorInvalidValue;
-    return launch_t<float, float>(A, lda, B, ldb, M, N, K, 0, ep, s);
+    return launch_t<float, float>(A, lda, B, ldb, M, N, K, conv_C, 0, ep, s);
 }
 
 }  // namespace cac

@@ -115,6 +115,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (conv_C) {
                 const int tap = k0 / conv_C;
                 tma_load_3d(sA + s * C::A_TILES, &tmA, k0 - tap * conv_C, tap & 1, m0 + (tap >> 1), &full[s]);
+                if (SPLIT)
+                    tma_load_3d(sA + s * C::A_TILES + A_TILE, &tmA, conv_C + k0 - tap * conv_C, tap & 1,
+                                m0 + (tap >> 1), &full[s]);
             } else {
                 tma_load_2d(sA + s * C::A_TILES, &tmA, k0, m0, &full[s]);
                 if (SPLIT) tma_load_2d(sA + s * C::A_TILES + A_TILE, &tmA, K + k0, m0, &full[s]);
@@ -254,12 +257,13 @@ template <int BN>
 static cudaError_t launch_bn(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int cc, int sp,
                              int a_split, const EpiParams& ep, int* status, cudaStream_t s) {
     if (a_split) {
-        // split operands come from LayerNorm outputs and the attention output
+        // split operands: LayerNorm outputs, the attention output, the subsampling windows
         switch (ep.kind) {
             case EPI_STORE: return launch_bn_kind<BN, EPI_STORE, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
             case EPI_RESID: return launch_bn_kind<BN, EPI_RESID, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
             case EPI_GLU: return launch_bn_kind<BN, EPI_GLU, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
             case EPI_QKV: return launch_bn_kind<BN, EPI_QKV, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+            case EPI_SUB: return launch_bn_kind<BN, EPI_SUB, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
         }
         return cudaErrorInvalidValue;
     }
@@ -277,7 +281,7 @@ cudaError_t launch_gemm_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, int M
                            int splits, int a_split, const EpiParams& ep, int* status, cudaStream_t s) {
     if (M <= 0) return cudaSuccess;
     if (K % BK || K <= 0 || N % BN || !ep.act_bf16) return cudaErrorInvalidValue;
-    if (conv_C && (conv_C % BK || K != 3 * conv_C || a_split)) return cudaErrorInvalidValue;
+    if (conv_C && (conv_C % BK || K != 3 * conv_C)) return cudaErrorInvalidValue;
     if (splits < 1 || splits > 4 || splits > K / BK) return cudaErrorInvalidValue;
     switch (BN) {
         case 64: return launch_bn<64>(tmA, tmB, M, N, K, conv_C, splits, a_split, ep, status, s);

@@ -118,54 +118,69 @@ cudaError_t launch_layernorm(const float* x, int M, int D, const float* g1, cons
 constexpr int MEL = 128;
 constexpr int TAIL = 14;
 
+// One window element: hi at row offset c and, for a split window (bf16 only),
+// the rounding residual at c + MEL.
+template <class T>
+__device__ __forceinline__ void put_win(T* row, int c, float v, int split) {
+    const T hi = from_f<T>(v);
+    row[c] = hi;
+    if constexpr (sizeof(T) == 2) {
+        if (split) row[MEL + c] = from_f<T>(v - to_f(hi));
+    }
+}
+
 template <class T>
 __global__ void __launch_bounds__(256) stage_mel_kernel(const float* mel, long long mel_bstride, const int* n_valid,
-                                                        T* win, T* tail, const int* ids, const int* pos, int n,
-                                                        int* status) {
+                                                        T* win, float* tail, const int* ids, const int* pos, int n,
+                                                        int split, int* status) {
+    __shared__ float ntail[TAIL * MEL];
     pdl_trigger();
     pdl_wait();
     const int b = blockIdx.x;
     const int id = ids[b];
     const bool first = pos[id] == 0;
     const int W = TAIL + 8 * n;
+    const int RW = MEL * (1 + split);
     const int nv = n_valid ? n_valid[b] : 8 * n;
-    T* w = win + (long long)b * W * MEL;
-    T* tl = tail + (long long)id * TAIL * MEL;
+    T* w = win + (long long)b * W * RW;
+    float* tl = tail + (long long)id * TAIL * MEL;
     bool bad = false;
     for (int e = threadIdx.x; e < W * MEL; e += blockDim.x) {
         const int r = e / MEL, c = e - (e / MEL) * MEL;
-        T v;
+        float v;
         if (r < TAIL) {
-            v = first ? from_f<T>(0.f) : tl[r * MEL + c];
+            v = first ? 0.f : tl[r * MEL + c];
         } else {
-            const float m = (r - TAIL < nv) ? mel[(long long)b * mel_bstride + (long long)(r - TAIL) * MEL + c] : 0.f;
-            bad |= !isfinite(m);
-            v = from_f<T>(m);
+            v = (r - TAIL < nv) ? mel[(long long)b * mel_bstride + (long long)(r - TAIL) * MEL + c] : 0.f;
+            bad |= !isfinite(v);
         }
-        w[e] = v;
+        put_win<T>(w + (long long)r * RW, c, v, split);
+        if (r >= 8 * n) ntail[(r - 8 * n) * MEL + c] = v;
     }
     if (bad) latch_error(status, CAC_E_NONFINITE);
     __syncthreads();
-    for (int e = threadIdx.x; e < TAIL * MEL; e += blockDim.x) tl[e] = w[8 * n * MEL + e];
+    for (int e = threadIdx.x; e < TAIL * MEL; e += blockDim.x) tl[e] = ntail[e];
 }
 
-cudaError_t launch_stage_mel(const float* mel, long long mel_bstride, const int* n_valid, void* win, void* tail,
-                             const int* ids, const int* pos, int n, int nb, int act_bf16, int* status,
+cudaError_t launch_stage_mel(const float* mel, long long mel_bstride, const int* n_valid, void* win, float* tail,
+                             const int* ids, const int* pos, int n, int nb, int act_bf16, int split, int* status,
                              cudaStream_t s) {
     if (nb <= 0) return cudaSuccess;
+    if (split && !act_bf16) return cudaErrorInvalidValue;
     if (act_bf16)
         return launch_k(stage_mel_kernel<bf16>, dim3(nb), dim3(256), 0, s, 1, mel, mel_bstride, n_valid,
-                        static_cast<bf16*>(win), static_cast<bf16*>(tail), ids, pos, n, status);
+                        static_cast<bf16*>(win), tail, ids, pos, n, split, status);
     return launch_k(stage_mel_kernel<float>, dim3(nb), dim3(256), 0, s, 1, mel, mel_bstride, n_valid,
-                    static_cast<float*>(win), static_cast<float*>(tail), ids, pos, n, status);
+                    static_cast<float*>(win), tail, ids, pos, n, 0, status);
 }
 
 template <class T>
-__global__ void stage_mel_offline_kernel(const float* mel, int t_mel, const int* len, T* dst, int W, int B,
+__global__ void stage_mel_offline_kernel(const float* mel, int t_mel, const int* len, T* dst, int W, int B, int split,
                                          int* status) {
     pdl_trigger();
     pdl_wait();
     const long long total = (long long)B * W * MEL;
+    const int RW = MEL * (1 + split);
     bool bad = false;
     for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
          e += (long long)gridDim.x * blockDim.x) {
@@ -177,19 +192,20 @@ __global__ void stage_mel_offline_kernel(const float* mel, int t_mel, const int*
             m = mel[((long long)b * t_mel + r) * MEL + c];
             bad |= !isfinite(m);
         }
-        dst[e] = from_f<T>(m);
+        put_win<T>(dst + rr * RW, c, m, split);
     }
     if (bad) latch_error(status, CAC_E_NONFINITE);
 }
 
 cudaError_t launch_stage_mel_offline(const float* mel, int t_mel, const int* len, void* dst, int W, int B,
-                                     int act_bf16, int* status, cudaStream_t s) {
+                                     int act_bf16, int split, int* status, cudaStream_t s) {
     const int blocks = 152 * 8;
+    if (split && !act_bf16) return cudaErrorInvalidValue;
     if (act_bf16)
         return launch_k(stage_mel_offline_kernel<bf16>, dim3(blocks), dim3(256), 0, s, 1, mel, t_mel, len,
-                        static_cast<bf16*>(dst), W, B, status);
+                        static_cast<bf16*>(dst), W, B, split, status);
     return launch_k(stage_mel_offline_kernel<float>, dim3(blocks), dim3(256), 0, s, 1, mel, t_mel, len,
-                    static_cast<float*>(dst), W, B, status);
+                    static_cast<float*>(dst), W, B, 0, status);
 }
 
 // ---------------------------------------------------------------------------

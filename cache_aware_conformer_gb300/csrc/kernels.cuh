@@ -16,16 +16,19 @@ cudaError_t launch_layernorm(const float* x, int M, int D, const float* g1, cons
                              int grp_stride, int row_off, int split, cudaStream_t s);
 
 // Mel staging: window[b] = [melTail(id) | mel[b]] (14 + 8n rows; tail rows are
-// zero when pos[id] == 0), then melTail(id) = last 14 window rows.  mel rows of
-// stream b start at mel + b * mel_bstride; rows >= n_valid[b] (if given) read
-// as zero.  Latches CAC_E_NONFINITE on a non-finite mel value.
-cudaError_t launch_stage_mel(const float* mel, long long mel_bstride, const int* n_valid, void* win, void* tail,
-                             const int* ids, const int* pos, int n, int nb, int act_bf16, int* status,
+// zero when pos[id] == 0), then melTail(id) = last 14 window rows (the tail is
+// kept in fp32 [S][14][128]).  mel rows of stream b start at mel + b *
+// mel_bstride; rows >= n_valid[b] (if given) read as zero.  Window rows are in
+// the activation dtype, 128 wide, or (split, bf16 only) 256 wide: hi | lo.
+// Latches CAC_E_NONFINITE on a non-finite mel value.
+cudaError_t launch_stage_mel(const float* mel, long long mel_bstride, const int* n_valid, void* win, float* tail,
+                             const int* ids, const int* pos, int n, int nb, int act_bf16, int split, int* status,
                              cudaStream_t s);
 
-// Offline staging: dst[b] = [2 zero rows | mel[b] (rows >= len[b] zero) | pad to W rows]
+// Offline staging: dst[b] = [2 zero rows | mel[b] (rows >= len[b] zero) | pad to W rows],
+// rows as in launch_stage_mel.
 cudaError_t launch_stage_mel_offline(const float* mel, int t_mel, const int* len, void* dst, int W, int B,
-                                     int act_bf16, int* status, cudaStream_t s);
+                                     int act_bf16, int split, int* status, cudaStream_t s);
 
 struct AttnParams {
     const float* q = nullptr;   // fp32 queries, row stride ldq, head h at column h*HD
@@ -56,6 +59,11 @@ struct AttnParams {
 
 // A bounded wait on the K/V copies that gives up latches CAC_E_TIMEOUT in *status.
 cudaError_t launch_attention_stream(const AttnParams& a, int act_bf16, int* status, cudaStream_t s);
+// Tensor-core variant of the streaming attention (bf16, head_dim 64, <= 4
+// queries per stream, <= 80 keys and table rows); launch_attention_stream
+// takes it whenever attention_stream_mma_ok holds.
+bool attention_stream_mma_ok(const AttnParams& a, int act_bf16);
+cudaError_t launch_attention_stream_mma(const AttnParams& a, int* status, cudaStream_t s);
 cudaError_t launch_attention_offline(const AttnParams& a, int act_bf16, int* status, cudaStream_t s);
 
 // Causal depthwise conv (k = 9) + affine + SiLU over [conv cache | glu_new].

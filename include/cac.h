@@ -115,7 +115,7 @@ void cac_model_destroy(cac_model* m);
  * most `max_frames_per_step` subsampled frames per internal step (1..8;
  * larger pushes are split into several steps).  Allocates the GPU-resident
  * caches: K/V rings [streams][layers][heads][R][head_dim], conv tail
- * [streams][layers][8][d_model], melTail [streams][14][128], subT. */
+ * [streams][layers][8][d_model], melTail [streams][14][128] (fp32), subT. */
 int  cac_pool_create(cac_model* m, int max_streams, int max_frames_per_step, cac_pool** out);
 void cac_pool_destroy(cac_pool* p);
 

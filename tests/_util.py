@@ -21,6 +21,7 @@ def cosine(a, b):
 def assert_close(gpu, ref, cfg, what=""):
     """The tolerance the workload states: fp32 1e-4; bf16 3e-2 and cosine 0.999."""
     d = max_abs(gpu, ref)
+    print(f"[parity] {what}: max|d| {d:.3e} cos {cosine(gpu, ref):.7f} ({cfg.dtype})")
     if cfg.dtype == "fp32":
         assert d <= F32_MAX_ABS, f"{what}: max|d| {d:.3e} > {F32_MAX_ABS}"
     else:
