@@ -606,6 +606,7 @@ static cudaError_t attn_offline_launch(const AttnParams& a, int qgroup, int* sta
 // provisional passes (up to 24 queries, keys <= left + 24).
 cudaError_t launch_attention_stream(const AttnParams& a, int act_bf16, int* status, cudaStream_t s) {
     if (a.nb <= 0) return cudaSuccess;
+    if (attention_stream_mma_ok(a, act_bf16)) return launch_attention_stream_mma(a, status, s);
     const int nk_need = a.left + a.nq;
     if (a.nq <= 2 && nk_need <= 80) ATT_DISPATCH(attn_stream_launch, 2, 1, 16, 80, a, status, s);
     if (a.nq <= 8 && nk_need <= 80) ATT_DISPATCH(attn_stream_launch, 2, 4, 4, 80, a, status, s);
