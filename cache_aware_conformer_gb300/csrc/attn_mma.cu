@@ -23,7 +23,9 @@
 // conflict-free.  Keys are stored in logical order (ring slot (s0 + j) mod R
 // -> row j); rows j >= Nk and table rows r >= NR are zero-filled.  The
 // position table is weights: it is copied before the wait on the previous
-// kernel, the K/V rows after it.
+// kernel, the K/V rows after it, by a producer warp that runs up to
+// AW_STAGES units ahead of the consumer warps (persistent blocks, one per SM).
+#include <algorithm>
 #include <cfloat>
 
 #include "kernels.cuh"
@@ -31,13 +33,20 @@
 namespace cac {
 
 namespace {
-constexpr int AM_WARPS = 4;                      // units per block
 constexpr int AM_ROWS = 80;                      // key / rel rows per unit (5 tiles of 16)
 constexpr int AM_ROWB = 128;                     // bytes per row (64 bf16)
 constexpr int AM_MAT = AM_ROWS * AM_ROWB;        // one [80][64] bf16 matrix
 constexpr int AM_SLD = 84;                       // fp32 row stride of the score arrays
-constexpr int AM_UNIT = 2 * AM_MAT + 2 * 4 * AM_SLD * 4;
-constexpr int AM_SMEM = AM_MAT + AM_WARPS * AM_UNIT;
+constexpr int AW_CONS = 8;                       // consumer warps per block
+constexpr int AW_STAGES = 8;                     // ring stages, one unit's K and V rows each
+constexpr int AW_THREADS = 32 * (1 + AW_CONS);
+constexpr int AW_STAGE = 2 * AM_MAT;
+constexpr int AW_SCORES = 2 * 4 * AM_SLD * 4;    // per consumer: [4][AM_SLD] ac / probs + bd / output
+constexpr int AW_OFF_RING = AM_MAT;              // after the position table
+constexpr int AW_OFF_SC = AW_OFF_RING + AW_STAGES * AW_STAGE;
+constexpr int AW_OFF_BAR = AW_OFF_SC + AW_CONS * AW_SCORES;
+constexpr int AW_SMEM = AW_OFF_BAR + 2 * AW_STAGES * 8;
+static_assert(AW_SMEM <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return (uint32_t)(row * AM_ROWB + ((chunk ^ (row & 7)) << 4));
@@ -107,81 +116,35 @@ __device__ __forceinline__ void score_tiles(uint32_t mat, const uint32_t (&b)[4]
     }
 }
 
-__global__ void __launch_bounds__(AM_WARPS * 32) attn_stream_mma_kernel(AttnParams a, int* status) {
-    extern __shared__ __align__(1024) uint8_t sm[];
-    const int h = blockIdx.y;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__device__ __forceinline__ float wmax(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float wsum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ void mbar_arrive_local(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// arrive on `bar` once every cp.async this thread issued so far has landed
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// One unit's scores, softmax and probs @ V (the consumer side).  Km / Vm: the
+// unit's K and V rows in shared memory; bu / bv: the split-query B fragments.
+__device__ __forceinline__ void attend_unit(const AttnParams& a, uint32_t Pm, uint32_t Km, uint32_t Vm,
+                                            const uint32_t (&bu)[4][2], const uint32_t (&bv)[4][2], float* Sac,
+                                            float* Sbd, int p0, int Lc, int nq, int lane, float (&acc)[4][4]) {
     const int g = lane >> 2, c = lane & 3;
-    const int b = blockIdx.x * AM_WARPS + warp;
-    const bool live = b < a.nb;
-    const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(sm);
-    const uint32_t Pm = sbase;
-    uint8_t* usm = sm + AM_MAT + warp * AM_UNIT;
-    const uint32_t Km = sbase + AM_MAT + warp * AM_UNIT, Vm = Km + AM_MAT;
-    float* Sac = reinterpret_cast<float*>(usm + 2 * AM_MAT);  // [4][AM_SLD]: ac, then probabilities
-    float* Sbd = Sac + 4 * AM_SLD;                           // [4][AM_SLD]: bd, then the output staging
-    constexpr int HD = 64;
-
-    // position table of this head (weights): rows >= NR zero
-    {
-        const bf16* P = static_cast<const bf16*>(a.P) + (long long)h * a.NR * HD;
-        for (int e = threadIdx.x; e < AM_ROWS * 8; e += blockDim.x) {
-            const int r = e >> 3, ch = e & 7;
-            const bool ok = r < a.NR;
-            cp_async16(Pm + swz(r, ch), P + (ok ? r : 0) * HD + ch * 8, ok);
-        }
-    }
-    pdl_wait();
-    int p0 = 0, Lc = 0, Nk = 0, nq = a.nq;
-    const float* q = nullptr;
-    if (live) {
-        const int id = a.ids[b];
-        p0 = a.pos[id];
-        Lc = min(p0, a.left);
-        Nk = Lc + nq;
-        const int s0 = (p0 - Lc) % a.R;
-        const long long base = (long long)id * a.sstride + (long long)h * a.R * HD;
-        const bf16* kb = static_cast<const bf16*>(a.k) + base;
-        const bf16* vb = static_cast<const bf16*>(a.v) + base;
-        for (int e = lane; e < AM_ROWS * 8; e += 32) {
-            const int j = e >> 3, ch = e & 7;
-            const bool ok = j < Nk;
-            int sl = s0 + j;
-            if (sl >= a.R) sl -= a.R;
-            const long long off = (long long)(ok ? sl : 0) * HD + ch * 8;
-            cp_async16(Km + swz(j, ch), kb + off, ok);
-            cp_async16(Vm + swz(j, ch), vb + off, ok);
-        }
-        q = a.q + (long long)b * nq * a.ldq + h * HD;
-    }
-    cp_async_wait_all();
-    __syncthreads();
-    if (!live) return;
-
-    // B fragments of the split queries: column g -> query g & 3, half g >> 2;
-    // rows (dims) 16 ks + 2c, +1 and 16 ks + 2c + 8, +9
-    uint32_t bu[4][2], bv[4][2];
-    {
-        const int qi = g & 3, half = g >> 2;
-        const bool has = qi < nq;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int d = ks * 16 + 2 * c + 8 * hh;
-                float2 qq = make_float2(0.f, 0.f);
-                if (has) qq = *reinterpret_cast<const float2*>(q + (long long)qi * a.ldq + d);
-                const float2 uu = *reinterpret_cast<const float2*>(a.pbu + h * HD + d);
-                const float2 vv = *reinterpret_cast<const float2*>(a.pbv + h * HD + d);
-                bu[ks][hh] = has ? pack2(split_part(qq.x + uu.x, half), split_part(qq.y + uu.y, half)) : 0u;
-                bv[ks][hh] = has ? pack2(split_part(qq.x + vv.x, half), split_part(qq.y + vv.y, half)) : 0u;
-            }
-        }
-    }
+    const int Nk = Lc + nq;
     score_tiles(Km, bu, Sac, lane);
     score_tiles(Pm, bv, Sbd, lane);
     __syncwarp();
-
     // masked softmax per query over its key window (absolute positions)
     const int kpos0 = p0 - Lc;
     for (int i = 0; i < nq; ++i) {
@@ -204,18 +167,15 @@ __global__ void __launch_bounds__(AM_WARPS * 32) attn_stream_mma_kernel(AttnPara
             sv[t] = ok ? (Sac[i * AM_SLD + j] + Sbd[i * AM_SLD + (pq - pk - a.rmin)]) * a.scale : -FLT_MAX;
             m = fmaxf(m, sv[t]);
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        m = wmax(m);
         float sum = 0.f;
 #pragma unroll
         for (int t = 0; t < 3; ++t) {
             sv[t] = sv[t] == -FLT_MAX ? 0.f : __expf(sv[t] - m);
             sum += sv[t];
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        sum = wsum(sum);
         const float inv = 1.f / sum;
-        __syncwarp();  // every lane has read Sac row i before it is overwritten
 #pragma unroll
         for (int t = 0; t < 3; ++t) {
             const int j = lane + 32 * t;
@@ -223,66 +183,180 @@ __global__ void __launch_bounds__(AM_WARPS * 32) attn_stream_mma_kernel(AttnPara
         }
     }
     __syncwarp();
-    pdl_trigger();
-
     // out^T[d][col] = V^T[d][:] . prob^T[:][col]; B column g -> query g & 3, half g >> 2
-    float acc[4][4];
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc[mt][k] = 0.f;
-    {
-        const int qi = g & 3, half = g >> 2;
-        const bool has = qi < nq;
+    const int qi = g & 3, half = g >> 2;
+    const bool has = qi < nq;
 #pragma unroll
-        for (int ks = 0; ks < AM_ROWS / 16; ++ks) {
-            uint32_t bp[2];
+    for (int ks = 0; ks < AM_ROWS / 16; ++ks) {
+        uint32_t bp[2];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int j = ks * 16 + 2 * c + 8 * hh;
-                const float p0v = has ? Sac[qi * AM_SLD + j] : 0.f;
-                const float p1v = has ? Sac[qi * AM_SLD + j + 1] : 0.f;
-                bp[hh] = pack2(split_part(p0v, half), split_part(p1v, half));
-            }
-            const int key = ks * 16 + (lane & 7) + ((lane >> 4) << 3);
-#pragma unroll
-            for (int mt = 0; mt < 4; ++mt) {
-                uint32_t av[4];
-                ldsm_x4_t(Vm + swz(key, mt * 2 + ((lane >> 3) & 1)), av);
-                mma16816(acc[mt], av, bp[0], bp[1]);
-            }
+        for (int hh = 0; hh < 2; ++hh) {
+            const int j = ks * 16 + 2 * c + 8 * hh;
+            const float p0v = has ? Sac[qi * AM_SLD + j] : 0.f;
+            const float p1v = has ? Sac[qi * AM_SLD + j + 1] : 0.f;
+            bp[hh] = pack2(split_part(p0v, half), split_part(p1v, half));
         }
-    }
-    // recombine hi + lo, stage out[i][d] (fp32) in Sbd, then write the rows
-    float* O = Sbd;
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) acc[mt][k] += __shfl_xor_sync(0xffffffffu, acc[mt][k], 2);
-    }
-    __syncwarp();  // Sbd (bd scores) fully consumed by the softmax
-    if (c < 2) {
+        const int key = ks * 16 + (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
-            const int d = mt * 16 + g;
-            O[(2 * c) * 64 + d] = acc[mt][0];
-            O[(2 * c + 1) * 64 + d] = acc[mt][1];
-            O[(2 * c) * 64 + d + 8] = acc[mt][2];
-            O[(2 * c + 1) * 64 + d + 8] = acc[mt][3];
+            uint32_t av[4];
+            ldsm_x4_t(Vm + swz(key, mt * 2 + ((lane >> 3) & 1)), av);
+            mma16816(acc[mt], av, bp[0], bp[1]);
         }
     }
-    __syncwarp();
-    bf16* dst = static_cast<bf16*>(a.out) + (long long)b * nq * a.ldo + h * HD;
-    for (int i = 0; i < nq; ++i) {
-        const float2 o = *reinterpret_cast<const float2*>(O + i * 64 + 2 * lane);
-        const __nv_bfloat162 hi2 = __floats2bfloat162_rn(o.x, o.y);
-        bf16* row = dst + (long long)i * a.ldo + 2 * lane;
-        *reinterpret_cast<__nv_bfloat162*>(row) = hi2;
-        if (a.out_split > 0) {
-            const float2 hf = __bfloat1622float2(hi2);
-            *reinterpret_cast<__nv_bfloat162*>(row + a.out_split) = __floats2bfloat162_rn(o.x - hf.x, o.y - hf.y);
+}
+
+// Split-query B fragments: column g -> query g & 3, half g >> 2; rows (dims)
+// 16 ks + 2c, +1 and 16 ks + 2c + 8, +9.
+__device__ __forceinline__ void query_frags(const AttnParams& a, const float* q, int h, int nq, int lane,
+                                            uint32_t (&bu)[4][2], uint32_t (&bv)[4][2]) {
+    constexpr int HD = 64;
+    const int g = lane >> 2, c = lane & 3;
+    const int qi = g & 3, half = g >> 2;
+    const bool has = qi < nq;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int d = ks * 16 + 2 * c + 8 * hh;
+            float2 qq = make_float2(0.f, 0.f);
+            if (has) qq = *reinterpret_cast<const float2*>(q + (long long)qi * a.ldq + d);
+            const float2 uu = __ldg(reinterpret_cast<const float2*>(a.pbu + h * HD + d));
+            const float2 vv = __ldg(reinterpret_cast<const float2*>(a.pbv + h * HD + d));
+            bu[ks][hh] = has ? pack2(split_part(qq.x + uu.x, half), split_part(qq.y + uu.y, half)) : 0u;
+            bv[ks][hh] = has ? pack2(split_part(qq.x + vv.x, half), split_part(qq.y + vv.y, half)) : 0u;
         }
     }
+}
+
+// Persistent, warp-specialized: block (x, h) serves the streams b = x, x +
+// gridDim.x, ... of head h.  Warp 0 produces: per unit it waits for a free
+// ring stage, copies the unit's K and V rows into it and arms the stage's
+// barrier with cp.async arrivals.  Warps 1..AW_CONS consume units round-robin
+// (consumer w takes units w-1, w-1+AW_CONS, ...; unit k lives in stage k mod
+// AW_STAGES), loading their query fragments before waiting for the stage.
+__global__ void __launch_bounds__(AW_THREADS, 1) attn_stream_ws_kernel(AttnParams a, int* status) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    const int h = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t Pm = sbase;
+    const uint32_t ring = sbase + AW_OFF_RING;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + AW_OFF_BAR);
+    uint64_t* empty = full + AW_STAGES;
+    constexpr int HD = 64;
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < AW_STAGES; ++st) {
+            mbar_init(&full[st], 32);
+            mbar_init(&empty[st], 1);
+        }
+        fence_mbar_init();
+    }
+    // position table of this head (weights): before the wait on the previous kernel; rows >= NR zero
+    {
+        const bf16* P = static_cast<const bf16*>(a.P) + (long long)h * a.NR * HD;
+        for (int e = threadIdx.x; e < AM_ROWS * 8; e += blockDim.x) {
+            const int r = e >> 3, ch = e & 7;
+            const bool ok = r < a.NR;
+            cp_async16(Pm + swz(r, ch), P + (ok ? r : 0) * HD + ch * 8, ok);
+        }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    pdl_wait();
+
+    if (warp == 0) {
+        for (int k = 0;; ++k) {
+            const int b = blockIdx.x + k * gridDim.x;
+            if (b >= a.nb) break;
+            const int st = k % AW_STAGES;
+            if (!mbar_wait(&empty[st], ((k / AW_STAGES) & 1) ^ 1)) {
+                if (lane == 0) latch_error(status, CAC_E_TIMEOUT);
+                break;
+            }
+            const int id = a.ids[b];
+            const int p0 = a.pos[id];
+            const int Lc = min(p0, a.left);
+            const int Nk = Lc + a.nq;
+            const int s0 = (p0 - Lc) % a.R;
+            const long long base = (long long)id * a.sstride + (long long)h * a.R * HD;
+            const bf16* kb = static_cast<const bf16*>(a.k) + base;
+            const bf16* vb = static_cast<const bf16*>(a.v) + base;
+            const uint32_t Ks = ring + st * AW_STAGE, Vs = Ks + AM_MAT;
+            for (int e = lane; e < AM_ROWS * 8; e += 32) {
+                const int j = e >> 3, ch = e & 7;
+                const bool ok = j < Nk;
+                int sl = s0 + j;
+                if (sl >= a.R) sl -= a.R;
+                const long long off = (long long)(ok ? sl : 0) * HD + ch * 8;
+                cp_async16(Ks + swz(j, ch), kb + off, ok);
+                cp_async16(Vs + swz(j, ch), vb + off, ok);
+            }
+            cp_async_arrive(&full[st]);
+        }
+        return;
+    }
+
+    const int cw = warp - 1;
+    float* Sac = reinterpret_cast<float*>(sm + AW_OFF_SC + cw * AW_SCORES);  // ac, then probabilities
+    float* Sbd = Sac + 4 * AM_SLD;                                          // bd, then the output rows
+    const int nq = a.nq;
+    const int g = lane >> 2, c = lane & 3;
+    for (int k = cw;; k += AW_CONS) {
+        const int b = blockIdx.x + k * gridDim.x;
+        if (b >= a.nb) break;
+        const int st = k % AW_STAGES;
+        const int id = a.ids[b];
+        const int p0 = a.pos[id];
+        const int Lc = min(p0, a.left);
+        uint32_t bu[4][2], bv[4][2];
+        query_frags(a, a.q + (long long)b * nq * a.ldq + h * HD, h, nq, lane, bu, bv);
+        if (!mbar_wait(&full[st], (k / AW_STAGES) & 1)) {
+            if (lane == 0) latch_error(status, CAC_E_TIMEOUT);
+            break;
+        }
+        const uint32_t Km = ring + st * AW_STAGE, Vm = Km + AM_MAT;
+        float acc[4][4];
+        attend_unit(a, Pm, Km, Vm, bu, bv, Sac, Sbd, p0, Lc, nq, lane, acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_local(&empty[st]);  // the stage's last shared-memory read is done
+        // recombine hi + lo, stage out[i][d] (fp32) in Sbd, then write the rows
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) acc[mt][q4] += __shfl_xor_sync(0xffffffffu, acc[mt][q4], 2);
+        float* O = Sbd;
+        if (c < 2) {
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                const int d = mt * 16 + g;
+                O[(2 * c) * 64 + d] = acc[mt][0];
+                O[(2 * c + 1) * 64 + d] = acc[mt][1];
+                O[(2 * c) * 64 + d + 8] = acc[mt][2];
+                O[(2 * c + 1) * 64 + d + 8] = acc[mt][3];
+            }
+        }
+        __syncwarp();
+        bf16* dst = static_cast<bf16*>(a.out) + (long long)b * nq * a.ldo + h * HD;
+        for (int i = 0; i < nq; ++i) {
+            const float2 o = *reinterpret_cast<const float2*>(O + i * 64 + 2 * lane);
+            const __nv_bfloat162 hi2 = __floats2bfloat162_rn(o.x, o.y);
+            bf16* row = dst + (long long)i * a.ldo + 2 * lane;
+            *reinterpret_cast<__nv_bfloat162*>(row) = hi2;
+            if (a.out_split > 0) {
+                const float2 hf = __bfloat1622float2(hi2);
+                *reinterpret_cast<__nv_bfloat162*>(row + a.out_split) =
+                    __floats2bfloat162_rn(o.x - hf.x, o.y - hf.y);
+            }
+        }
+        __syncwarp();  // the output staging is read before the next unit's bd scores overwrite it
+    }
+    pdl_trigger();
 }
 }  // namespace
 
@@ -293,14 +367,20 @@ bool attention_stream_mma_ok(const AttnParams& a, int act_bf16) {
 
 cudaError_t launch_attention_stream_mma(const AttnParams& a, int* status, cudaStream_t s) {
     static bool attr = false;
+    static int sms = 0;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(attn_stream_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             AM_SMEM);
+        cudaError_t e = cudaFuncSetAttribute(attn_stream_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             AW_SMEM);
         if (e != cudaSuccess) return e;
+        int dev = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
         attr = true;
     }
-    dim3 grid((a.nb + AM_WARPS - 1) / AM_WARPS, a.H);
-    return launch_k(attn_stream_mma_kernel, grid, dim3(AM_WARPS * 32), AM_SMEM, s, 1, a, status);
+    // one block per SM in total: the heads split the SMs, each block serves a strided share of the streams
+    const int per_head = std::max(1, std::min((a.nb + AW_CONS - 1) / AW_CONS, sms / std::max(1, a.H)));
+    dim3 grid(per_head, a.H);
+    return launch_k(attn_stream_ws_kernel, grid, dim3(AW_THREADS), AW_SMEM, s, 1, a, status);
 }
 
 }  // namespace cac
