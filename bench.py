@@ -218,13 +218,49 @@ def algorithmic_work(cfg, S, n, mean_lc):
         "gemm_joint": ("tensor", 2.0 * M * J * D),
         "gemm_sub_out": ("tensor", 2.0 * M * D * D),
         "gemm_subsample": ("tensor", sub_flops),
-        # q fp32 in, K/V cache + new rows, output bf16, position table fp32
-        "attention": ("hbm", kv + M * D * 4 + M * D * 2 + nr * D * 4),
+        # q fp32 in, K/V cache + new rows, output as a split (hi, lo) bf16 pair, bf16 position table
+        "attention": ("hbm", kv + M * D * 4 + M * D * 4 + nr * D * 2),
         # GLU rows in, conv tail (8 rows) in, n rows committed, output
         "dwconv": ("hbm", M * D * 2 + S * 8 * D * 2 + M * D * 2 + M * D * 2 + 12 * D * 4),
-        "layernorm": ("hbm", M * D * 4 + M * D * 2 + M * D * 4),
+        # per launch, averaged over the step's LayerNorms: x in (4 B) and a split
+        # (hi, lo) bf16 output (4 B) for 1 + 3L of them; ln_out also writes x
+        # in place (4 B) for L - 1, and the last writes fp32 frames + plain bf16
+        "layernorm": ("hbm", M * D * ((1 + 3 * L) * 8 + (L - 1) * 12 + 10) / (4 * L + 1)),
         "stage_mel": ("hbm", S * (8 * n + 14) * 128 * 4 + S * W1 * 128 * 2 + S * 14 * 128 * 2),
     }
+
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of one
+# ncu capture of the kernel on this workload, with the source files it was
+# built from; reported only while those files are unchanged (see profiles/).
+NCU_TRAFFIC = {
+    "layernorm": (1.069312e6, {"csrc/kernels.cu": "0e003eedcaa93feae2fc3fd550b450c5f478f2d4d8a914faaef8545165bf86db",
+                               "csrc/common.cuh": "1cde4c011b99176dc3625ec3ef613dc325ce852cc62c634440f08710442dfefe"}),
+    "attention": (35.244544e6 + 6.656e3,
+                  {"csrc/attn_mma.cu": "b59d8ea918e0f4554cfcfe9d92fa837db2e9bc9cf613e5aef0902ff31678a461",
+                   "csrc/common.cuh": "1cde4c011b99176dc3625ec3ef613dc325ce852cc62c634440f08710442dfefe"}),
+    "gemm_ff_down": (5.265664e6, {"csrc/gemm_tc.cu": "eb30c869d201935c21973199c48aa4a3976f61d496e6fd74349838cc13037883",
+                                  "csrc/gemm.cuh": "a8085c49820af5f3bba3ea831a8c1f39d10bf36c1da373dd2057bd76be6cb2ea",
+                                  "csrc/common.cuh": "1cde4c011b99176dc3625ec3ef613dc325ce852cc62c634440f08710442dfefe"}),
+    "gemm_ff_up": (3.1808e6, {"csrc/gemm_tc.cu": "eb30c869d201935c21973199c48aa4a3976f61d496e6fd74349838cc13037883",
+                              "csrc/gemm.cuh": "a8085c49820af5f3bba3ea831a8c1f39d10bf36c1da373dd2057bd76be6cb2ea",
+                              "csrc/common.cuh": "1cde4c011b99176dc3625ec3ef613dc325ce852cc62c634440f08710442dfefe"}),
+}
+
+
+def measured_traffic(kernel_class: str, workload: str):
+    """ncu DRAM bytes per launch for the 256-stream workload, or None when not
+    captured for this class or when its sources changed since the capture."""
+    import hashlib
+    if workload != "eou120m_256streams_60s" or kernel_class not in NCU_TRAFFIC:
+        return None
+    nbytes, files = NCU_TRAFFIC[kernel_class]
+    pkg = os.path.join(ROOT, "cache_aware_conformer_gb300")
+    for rel, digest in files.items():
+        with open(os.path.join(pkg, rel), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != digest:
+                return None
+    return nbytes
 
 
 def load_peaks():
@@ -461,7 +497,7 @@ def run_ours(args, wl):
     d = kernels[dom]
     roofline = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"],
                 "peak": tf_peak if d["bound"] == "tensor" else hbm_peak, "unit": d["unit"], "frac": d["frac"],
-                "traffic": None,
+                "traffic": measured_traffic(dom, wl.name),
                 "peak_source": f"{peak_src} ({'bf16 sustained' if d['bound'] == 'tensor' else 'HBM copy'})",
                 "per_launch": work[dom][1], "avg_launch_us": d["avg_us"]}
 
