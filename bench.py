@@ -518,17 +518,11 @@ def run_ours(args, wl):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w.cfg, w.blob, args.cpu_chunks)
     if rank == 0:
-        line = {"metric": METRIC if wl.name == "eou120m_256streams_60s" else f"streamed audio-sec/sec ({wl.name})",
+        line = {"metric": workload_metric(wl),
                 "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": Wm,
                 "ms_per_step": ms_max / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": wl.name, "streams_per_gpu": w.S, "chunk_ms": 10 * w.push_mel,
-                           "layers": w.cfg.n_layers, "d_model": w.cfg.d_model, "heads": w.cfg.n_heads,
-                           "ff": w.cfg.ff_dim, "att_left": w.cfg.att_left, "att_chunk": w.cfg.att_chunk,
-                           "reset_prob": wl.reset_prob, "start_offsets": f"even, 0..{wl.max_start_offset - 1}",
-                           "mean_Lc": mean_lc, "parallelism": f"replicas x{world}",
-                           "l2": "inputs larger than L2: each step reads all K/V rings (~713 MB) "
-                                 "and all weights (~210 MB)"},
+                "config": dict(workload_config(wl, world), mean_Lc=mean_lc),
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches, "clocks": clk}
         print(json.dumps(line), flush=True)
@@ -546,6 +540,20 @@ def cpu_baseline(cfg, blob, chunks: int):
     return {"value": cores * chunks * 0.16 / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{cores} streams x {chunks} pushes of 160 ms (one stream per core, fp64 numpy, "
                       f"17-layer model); {secs:.1f} s wall"}
+
+
+def workload_metric(wl) -> str:
+    return METRIC if wl.name == "eou120m_256streams_60s" else f"streamed audio-sec/sec ({wl.name})"
+
+
+def workload_config(wl, world: int) -> dict:
+    """The static description of a streaming workload, shared by both arms."""
+    cfg = wl.model
+    return {"workload": wl.name, "streams_per_gpu": wl.streams, "chunk_ms": 10 * wl.push_mel,
+            "layers": cfg.n_layers, "d_model": cfg.d_model, "heads": cfg.n_heads, "ff": cfg.ff_dim,
+            "att_left": cfg.att_left, "att_chunk": cfg.att_chunk, "reset_prob": wl.reset_prob,
+            "start_offsets": f"even, 0..{max(wl.max_start_offset - 1, 0)}", "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2: each step reads all K/V rings and all weights"}
 
 
 def run_reference(args, wl):
@@ -567,11 +575,10 @@ def run_reference(args, wl):
     finally:
         farm.close()
     value = cores * K * 0.16 / secs
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-            "warmup": Wm, "ms_per_step": 1e3 * secs / K, "higher_is_better": True, "scaling": "weak",
+    line = {"impl": "reference", "metric": workload_metric(wl), "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": Wm, "ms_per_step": 1e3 * secs / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "streams_sampled": cores, "chunk_ms": 160,
-                       "layers": cfg.n_layers, "d_model": cfg.d_model},
+            "config": dict(workload_config(wl, world), streams_sampled=cores),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"{cores} of {wl.streams} streams, {K} pushes of 160 ms each"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
