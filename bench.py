@@ -438,7 +438,7 @@ def run_ours(args, wl):
     K, Wm = args.steps, args.warmup
     Kp = min(K, args.profile_steps)
     Ke = min(K, args.e2e_steps)
-    total_steps = Wm + K + Kp + Ke
+    total_steps = Wm + K + 2 * Kp + Ke
     workers = max(1, min(cpu_cores(), 16))
     w = StreamWorkload(wl, rank, dev, total_steps, workers)
     w.pool.set_graphs(True)
@@ -469,6 +469,19 @@ def run_ours(args, wl):
     mean_lc = float(np.mean(w.lc_hist[lc0:]))
     w.pool.check()
     value, ms_max = aggregate_throughput(ms, w.S, w.n, K, dev)
+
+    # ---- per-push latency: one push at a time (graph replay), CUDA events
+    # around each push, synchronized between pushes
+    lat = []
+    for _ in range(Kp):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        w.step()
+        a1.record()
+        a1.synchronize()
+        lat.append(a0.elapsed_time(a1))
+    latency = {"p50_ms": float(np.percentile(lat, 50)), "p95_ms": float(np.percentile(lat, 95)),
+               "pushes": len(lat), "note": "one push of all streams, graph replay, device time"}
 
     # ---- profiled pass of the same steps: per-kernel-class CUDA events
     w.pool.set_profile(True)
@@ -524,7 +537,7 @@ def run_ours(args, wl):
                 "dtype": "bf16", "data": "synthetic",
                 "config": dict(workload_config(wl, world), mean_Lc=mean_lc),
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches, "clocks": clk}
+                "latency": latency, "gpu_launches": launches, "clocks": clk}
         print(json.dumps(line), flush=True)
 
 

@@ -237,3 +237,34 @@ def test_push_host_matches_device_push():
     e0, j0, _ = _push(pools[0], [ids[0]], [mel])
     e1, j1, n1 = pools[1].push_host([ids[1]], mel[None])
     assert n1 == [8] and np.array_equal(e0, e1) and np.array_equal(j0, j1)
+
+
+def test_c600m_shape_multistream():
+    """The 600M encoder's layer shapes (d_model 1024, 16 heads, ff 4096), two
+    layers, three streams with 160 / 320 / 640 ms pushes and a ragged flush."""
+    from dataclasses import replace
+    from cache_aware_conformer_gb300 import native
+    from cache_aware_conformer_gb300.config import C600M
+    cfg = replace(C600M, n_layers=2)
+    W, model = make_model(cfg)
+    pool = native.Pool(model, 4, 8)
+    ids = [pool.create_stream() for _ in range(3)]
+    refs = [O.StreamingEncoder(W, cfg) for _ in ids]
+    mels = [synth.make_mel(300, 40 + k) for k in range(3)]
+    pos = 0
+    got = [[] for _ in ids]
+    want = [[] for _ in ids]
+    for n in [16, 32, 16, 64, 16, 32, 64]:
+        e, j, n_out = _push(pool, ids, [m[pos:pos + n] for m in mels])
+        for b, r in enumerate(refs):
+            er, jr = r.push(mels[b][pos:pos + n])
+            got[b].append(e[b]); want[b].append(er)
+        pos += n
+    rem = [300 - pos - 5 * k for k in range(3)]
+    mel_t = torch.from_numpy(np.stack([m[pos:] for m in mels])).to(DEV)
+    e, j, n_out = pool.flush(ids, mel_t, rem)
+    for b, r in enumerate(refs):
+        er, jr = r.flush(mels[b][pos:pos + rem[b]])
+        got[b].append(e[b, :n_out[b]].cpu().numpy()); want[b].append(er)
+        assert_close(np.concatenate(got[b]), np.concatenate(want[b]), cfg, f"c600m stream {b}")
+    pool.check()
