@@ -18,13 +18,16 @@
 // fp32 accumulators with one shuffle.  K, V and the position table are bf16
 // already (exact operands).
 //
-// Staging: cp.async 16-byte copies into 128-byte-swizzled shared rows (chunk
-// c of row r at chunk position c ^ (r & 7)), so the ldmatrix row reads are
-// conflict-free.  Keys are stored in logical order (ring slot (s0 + j) mod R
-// -> row j); rows j >= Nk and table rows r >= NR are zero-filled.  The
-// position table is weights: it is copied before the wait on the previous
-// kernel, the K/V rows after it, by a producer warp that runs up to
-// AW_STAGES units ahead of the consumer warps (persistent blocks, one per SM).
+// Staging: TMA tensor copies with the 128-byte swizzle (chunk c of row r at
+// chunk position c ^ (r & 7)), so the ldmatrix row reads are conflict-free.
+// One copy brings a whole ring (R <= 80 rows, in slot order) of one stream,
+// layer and head; logical key j lives in row (s0 + j) mod R, which each lane
+// folds into its ldmatrix row address (rows R .. 79 stay zero).  Ring rows
+// that hold no key of this step (logical j >= Nk) are masked in the softmax,
+// and their V rows are zeroed in shared memory before probs @ V.  The position table (weights, rows
+// r >= NR zeroed) is copied before the wait on the previous kernel, the rings
+// after it, by one producer thread that runs up to AW_STAGES units ahead of
+// the consumer warps (persistent blocks, one per SM).
 #include <algorithm>
 #include <cfloat>
 
@@ -45,19 +48,11 @@ constexpr int AW_SCORES = 2 * 4 * AM_SLD * 4;    // per consumer: [4][AM_SLD] ac
 constexpr int AW_OFF_RING = AM_MAT;              // after the position table
 constexpr int AW_OFF_SC = AW_OFF_RING + AW_STAGES * AW_STAGE;
 constexpr int AW_OFF_BAR = AW_OFF_SC + AW_CONS * AW_SCORES;
-constexpr int AW_SMEM = AW_OFF_BAR + 2 * AW_STAGES * 8;
+constexpr int AW_SMEM = AW_OFF_BAR + (2 * AW_STAGES + 1) * 8 + 1024 /*alignment slack*/;
 static_assert(AW_SMEM <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return (uint32_t)(row * AM_ROWB + ((chunk ^ (row & 7)) << 4));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -91,12 +86,21 @@ __device__ __forceinline__ uint32_t pack2(bf16 lo16, bf16 hi16) {
 
 // ac or bd for the five 16-row tiles of one [80][64] matrix against the
 // split-query B fragments; result rows (keys / rels) x queries into S[i][row].
-__device__ __forceinline__ void score_tiles(uint32_t mat, const uint32_t (&b)[4][2], float* S, int lane) {
+// Shared row of logical row j of a ring of R rows copied in slot order
+// starting at slot s0: (s0 + j) mod R for j < R, else j (a zero row).
+__device__ __forceinline__ int ring_row(int j, int s0, int R) {
+    if (j >= R) return j;
+    j += s0;
+    return j >= R ? j - R : j;
+}
+
+__device__ __forceinline__ void score_tiles(uint32_t mat, int s0, int R, const uint32_t (&b)[4][2], float* S,
+                                            int lane) {
     const int g = lane >> 2, c = lane & 3;
 #pragma unroll
     for (int mt = 0; mt < AM_ROWS / 16; ++mt) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const int row = mt * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int row = ring_row(mt * 16 + (lane & 7) + (((lane >> 3) & 1) << 3), s0, R);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
             uint32_t a[4];
@@ -130,20 +134,15 @@ __device__ __forceinline__ float wsum(float v) {
 __device__ __forceinline__ void mbar_arrive_local(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-// arrive on `bar` once every cp.async this thread issued so far has landed
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 // One unit's scores, softmax and probs @ V (the consumer side).  Km / Vm: the
 // unit's K and V rows in shared memory; bu / bv: the split-query B fragments.
-__device__ __forceinline__ void attend_unit(const AttnParams& a, uint32_t Pm, uint32_t Km, uint32_t Vm,
+__device__ __forceinline__ void attend_unit(const AttnParams& a, uint32_t Pm, uint32_t Km, uint32_t Vm, int s0,
                                             const uint32_t (&bu)[4][2], const uint32_t (&bv)[4][2], float* Sac,
                                             float* Sbd, int p0, int Lc, int nq, int lane, float (&acc)[4][4]) {
     const int g = lane >> 2, c = lane & 3;
     const int Nk = Lc + nq;
-    score_tiles(Km, bu, Sac, lane);
-    score_tiles(Pm, bv, Sbd, lane);
+    score_tiles(Km, s0, a.R, bu, Sac, lane);
+    score_tiles(Pm, 0, AM_ROWS, bv, Sbd, lane);
     __syncwarp();
     // masked softmax per query over its key window (absolute positions)
     const int kpos0 = p0 - Lc;
@@ -200,7 +199,7 @@ __device__ __forceinline__ void attend_unit(const AttnParams& a, uint32_t Pm, ui
             const float p1v = has ? Sac[qi * AM_SLD + j + 1] : 0.f;
             bp[hh] = pack2(split_part(p0v, half), split_part(p1v, half));
         }
-        const int key = ks * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int key = ring_row(ks * 16 + (lane & 7) + ((lane >> 4) << 3), s0, a.R);
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
             uint32_t av[4];
@@ -234,13 +233,15 @@ __device__ __forceinline__ void query_frags(const AttnParams& a, const float* q,
 }
 
 // Persistent, warp-specialized: block (x, h) serves the streams b = x, x +
-// gridDim.x, ... of head h.  Warp 0 produces: per unit it waits for a free
-// ring stage, copies the unit's K and V rows into it and arms the stage's
-// barrier with cp.async arrivals.  Warps 1..AW_CONS consume units round-robin
-// (consumer w takes units w-1, w-1+AW_CONS, ...; unit k lives in stage k mod
-// AW_STAGES), loading their query fragments before waiting for the stage.
-__global__ void __launch_bounds__(AW_THREADS, 1) attn_stream_ws_kernel(AttnParams a, int* status) {
-    extern __shared__ __align__(1024) uint8_t sm[];
+// gridDim.x, ... of head h.  Warp 0 lane 0 produces: per unit it waits for a
+// free ring stage and issues the TMA copies of the unit's K and V rings into
+// it.  Warps 1..AW_CONS consume units round-robin (consumer w takes units w-1,
+// w-1+AW_CONS, ...; unit k lives in stage k mod AW_STAGES), loading their query
+// fragments before waiting for the stage.
+__global__ void __launch_bounds__(AW_THREADS, 1)
+    attn_stream_ws_kernel(const __grid_constant__ AttnMaps tm, AttnParams a, int* status) {
+    extern __shared__ uint8_t sm_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
     const int h = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t sbase = smem_u32(sm);
@@ -248,56 +249,56 @@ __global__ void __launch_bounds__(AW_THREADS, 1) attn_stream_ws_kernel(AttnParam
     const uint32_t ring = sbase + AW_OFF_RING;
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + AW_OFF_BAR);
     uint64_t* empty = full + AW_STAGES;
+    uint64_t* pbar = empty + AW_STAGES;
     constexpr int HD = 64;
 
+    // position table rows NR .. AM_ROWS-1 are zero (rel values no key reaches),
+    // and so are the ring rows R .. AM_ROWS-1 of every stage (no copy writes them)
+    for (int e = threadIdx.x; e < (AM_ROWS - a.NR) * 8; e += blockDim.x) {
+        const int r = a.NR + (e >> 3);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(Pm + swz(r, e & 7)), "r"(0) : "memory");
+    }
+    {
+        const int per = (AM_ROWS - a.R) * 8;  // 16-byte chunks per matrix
+        for (int e = threadIdx.x; e < 2 * AW_STAGES * per; e += blockDim.x) {
+            const int mtx = e / per, r = a.R + (e % per >> 3);
+            const uint32_t base = sbase + AW_OFF_RING + mtx * AM_MAT;  // stage st: matrices 2 st (K), 2 st + 1 (V)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(base + swz(r, e & 7)), "r"(0) : "memory");
+        }
+    }
     if (threadIdx.x == 0) {
         for (int st = 0; st < AW_STAGES; ++st) {
-            mbar_init(&full[st], 32);
+            mbar_init(&full[st], 1);
             mbar_init(&empty[st], 1);
         }
+        mbar_init(pbar, 1);
         fence_mbar_init();
+        tma_prefetch_desc(&tm.k);
+        tma_prefetch_desc(&tm.v);
+        // weights: before the wait on the previous kernel
+        mbar_expect_tx(pbar, (uint32_t)a.NR * AM_ROWB);
+        tma_load_3d(sm, &tm.p, 0, 0, h, pbar);
     }
-    // position table of this head (weights): before the wait on the previous kernel; rows >= NR zero
-    {
-        const bf16* P = static_cast<const bf16*>(a.P) + (long long)h * a.NR * HD;
-        for (int e = threadIdx.x; e < AM_ROWS * 8; e += blockDim.x) {
-            const int r = e >> 3, ch = e & 7;
-            const bool ok = r < a.NR;
-            cp_async16(Pm + swz(r, ch), P + (ok ? r : 0) * HD + ch * 8, ok);
-        }
-    }
-    cp_async_wait_all();
     __syncthreads();
     pdl_wait();
 
     if (warp == 0) {
-        for (int k = 0;; ++k) {
-            const int b = blockIdx.x + k * gridDim.x;
-            if (b >= a.nb) break;
-            const int st = k % AW_STAGES;
-            if (!mbar_wait(&empty[st], ((k / AW_STAGES) & 1) ^ 1)) {
-                if (lane == 0) latch_error(status, CAC_E_TIMEOUT);
-                break;
+        if (lane == 0) {
+            for (int k = 0;; ++k) {
+                const int b = blockIdx.x + k * gridDim.x;
+                if (b >= a.nb) break;
+                const int st = k % AW_STAGES;
+                if (!mbar_wait(&empty[st], ((k / AW_STAGES) & 1) ^ 1)) {
+                    latch_error(status, CAC_E_TIMEOUT);
+                    break;
+                }
+                const int id = a.ids[b];
+                const int blk = (id * a.L + a.layer) * a.H + h;
+                uint8_t* Ks = sm + AW_OFF_RING + st * AW_STAGE;
+                mbar_expect_tx(&full[st], 2u * a.R * AM_ROWB);
+                tma_load_3d(Ks, &tm.k, 0, 0, blk, &full[st]);
+                tma_load_3d(Ks + AM_MAT, &tm.v, 0, 0, blk, &full[st]);
             }
-            const int id = a.ids[b];
-            const int p0 = a.pos[id];
-            const int Lc = min(p0, a.left);
-            const int Nk = Lc + a.nq;
-            const int s0 = (p0 - Lc) % a.R;
-            const long long base = (long long)id * a.sstride + (long long)h * a.R * HD;
-            const bf16* kb = static_cast<const bf16*>(a.k) + base;
-            const bf16* vb = static_cast<const bf16*>(a.v) + base;
-            const uint32_t Ks = ring + st * AW_STAGE, Vs = Ks + AM_MAT;
-            for (int e = lane; e < AM_ROWS * 8; e += 32) {
-                const int j = e >> 3, ch = e & 7;
-                const bool ok = j < Nk;
-                int sl = s0 + j;
-                if (sl >= a.R) sl -= a.R;
-                const long long off = (long long)(ok ? sl : 0) * HD + ch * 8;
-                cp_async16(Ks + swz(j, ch), kb + off, ok);
-                cp_async16(Vs + swz(j, ch), vb + off, ok);
-            }
-            cp_async_arrive(&full[st]);
         }
         return;
     }
@@ -307,6 +308,7 @@ __global__ void __launch_bounds__(AW_THREADS, 1) attn_stream_ws_kernel(AttnParam
     float* Sbd = Sac + 4 * AM_SLD;                                          // bd, then the output rows
     const int nq = a.nq;
     const int g = lane >> 2, c = lane & 3;
+    bool table = false;
     for (int k = cw;; k += AW_CONS) {
         const int b = blockIdx.x + k * gridDim.x;
         if (b >= a.nb) break;
@@ -314,17 +316,33 @@ __global__ void __launch_bounds__(AW_THREADS, 1) attn_stream_ws_kernel(AttnParam
         const int id = a.ids[b];
         const int p0 = a.pos[id];
         const int Lc = min(p0, a.left);
+        const int s0 = (p0 - Lc) % a.R;
         uint32_t bu[4][2], bv[4][2];
         query_frags(a, a.q + (long long)b * nq * a.ldq + h * HD, h, nq, lane, bu, bv);
+        if (!table) {
+            if (!mbar_wait(pbar, 0)) {
+                if (lane == 0) latch_error(status, CAC_E_TIMEOUT);
+                break;
+            }
+            table = true;
+        }
         if (!mbar_wait(&full[st], (k / AW_STAGES) & 1)) {
             if (lane == 0) latch_error(status, CAC_E_TIMEOUT);
             break;
         }
         const uint32_t Km = ring + st * AW_STAGE, Vm = Km + AM_MAT;
-        float acc[4][4];
-        attend_unit(a, Pm, Km, Vm, bu, bv, Sac, Sbd, p0, Lc, nq, lane, acc);
+        // V rows that hold no key of this step enter probs @ V with probability
+        // 0: make them zero, whatever the ring slot held
+        for (int e = lane; e < (a.R - (Lc + nq)) * 8; e += 32) {
+            const int r = ring_row(Lc + nq + (e >> 3), s0, a.R);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(Vm + swz(r, e & 7)), "r"(0) : "memory");
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive_local(&empty[st]);  // the stage's last shared-memory read is done
+        float acc[4][4];
+        attend_unit(a, Pm, Km, Vm, s0, bu, bv, Sac, Sbd, p0, Lc, nq, lane, acc);
+        fence_proxy_async_smem();  // the zeroed V rows before the next TMA copy into this stage
+        __syncwarp();
+        if (lane == 0) mbar_arrive_local(&empty[st]);  // the stage's last shared-memory access is done
         // recombine hi + lo, stage out[i][d] (fp32) in Sbd, then write the rows
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt)
@@ -361,8 +379,9 @@ __global__ void __launch_bounds__(AW_THREADS, 1) attn_stream_ws_kernel(AttnParam
 }  // namespace
 
 bool attention_stream_mma_ok(const AttnParams& a, int act_bf16) {
-    return act_bf16 && a.HD == 64 && a.nq >= 1 && a.nq <= 4 && a.left + a.nq <= AM_ROWS && a.NR <= AM_ROWS &&
-           a.rmin <= 0 && a.ldq % 2 == 0 && a.ldo % 2 == 0 && a.out_split % 2 == 0;
+    return act_bf16 && a.maps && a.HD == 64 && a.R <= AM_ROWS && a.R >= a.left + a.nq && a.nq >= 1 && a.nq <= 4 &&
+           a.left + a.nq <= AM_ROWS && a.NR <= AM_ROWS && a.rmin <= 0 && a.ldq % 2 == 0 && a.ldo % 2 == 0 &&
+           a.out_split % 2 == 0;
 }
 
 cudaError_t launch_attention_stream_mma(const AttnParams& a, int* status, cudaStream_t s) {
@@ -380,7 +399,7 @@ cudaError_t launch_attention_stream_mma(const AttnParams& a, int* status, cudaSt
     // one block per SM in total: the heads split the SMs, each block serves a strided share of the streams
     const int per_head = std::max(1, std::min((a.nb + AW_CONS - 1) / AW_CONS, sms / std::max(1, a.H)));
     dim3 grid(per_head, a.H);
-    return launch_k(attn_stream_ws_kernel, grid, dim3(AW_THREADS), AW_SMEM, s, 1, a, status);
+    return launch_k(attn_stream_ws_kernel, grid, dim3(AW_THREADS), AW_SMEM, s, 1, *a.maps, a, status);
 }
 
 }  // namespace cac

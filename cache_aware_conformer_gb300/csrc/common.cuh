@@ -186,6 +186,12 @@ __device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
 // ---------------------------------------------------------------------------
 // tcgen05 (5th-gen tensor core) wrappers
 // ---------------------------------------------------------------------------
+// generic-proxy shared-memory writes ordered before later async-proxy (TMA,
+// tensor core) accesses of the same bytes
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }

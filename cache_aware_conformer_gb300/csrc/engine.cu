@@ -204,7 +204,8 @@ int gemm(cac_model* m, const void* A, long long lda, int M, int K, const Lin& W,
         const bool ok = conv_C ? make_tmap_bf16_conv(&tmA, A, (uint64_t)conv_C * (a_split ? 2 : 1), (uint64_t)M + 1, 128)
                                : make_tmap_bf16(&tmA, A, a_split ? 2 * K : K, M, (uint64_t)lda * 2, 128);
         if (!ok) return CAC_E_CUDA;
-        const int splits = choose_splits((W.N / W.BN) * ((M + 127) / 128), K / 64);
+        // the fused depthwise conv reads its stream's rows within one CTA: no split-K
+        const int splits = ep.kind == EPI_GLUDW ? 1 : choose_splits((W.N / W.BN) * ((M + 127) / 128), K / 64);
         CK(launch_gemm_tc(&tmA, &W.tm, M, W.N, K, W.BN, conv_C, splits, a_split, ep, m->status, s));
     } else {
         CK(launch_gemm_simt(m->bf16, A, lda, W.w, K, M, W.N, K, conv_C, a_split, ep, s));
@@ -438,6 +439,7 @@ struct cac_pool {
     // per-stream device state
     int* pos = nullptr;        // subsampled frames consumed
     float* tail = nullptr;     // [S][14][128] fp32
+    std::vector<AttnMaps> amaps;  // per layer: K/V ring and position-table tensor maps (tensor-core attention)
     void* kring = nullptr;     // [S][L][H][R][HD]
     void* vring = nullptr;
     void* conv = nullptr;      // [S][L][8][D]
@@ -685,6 +687,7 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
             a.left = m->cfg.att_left; a.chunk = m->cfg.att_chunk; a.rc = m->cfg.right_context;
             a.nb = nb;
             a.scale = 1.f / std::sqrt((float)m->HD);
+            if (!p->amaps.empty()) { a.maps = &p->amaps[l]; a.layer = l; a.L = L; }
             PB(P_ATT);
             CK(launch_attention_stream(a, bf, p->status, s));
             PE();
@@ -702,16 +705,27 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
                             1 << 30, 0, 0, sp, s));
         PE();
         ++*lc;
-        ep = EpiParams(); ep.kind = EPI_GLU; ep.bias = Lw.pw1.b; ep.out_act = p->glu; ep.ldo = D;
+        void* conv_l = static_cast<char*>(p->conv) + (long long)l * CONV_CACHE * D * ab;
+        // tcgen05 path, chunked steps whose frames per stream divide a warp: the
+        // depthwise conv runs in the pw1 + GLU epilogue (a stream's rows share a warp)
+        const bool fuse_dw = m->tc && sp && 32 % n == 0 && n_commit == n;
+        ep = EpiParams(); ep.kind = fuse_dw ? EPI_GLUDW : EPI_GLU; ep.bias = Lw.pw1.b; ep.out_act = p->glu; ep.ldo = D;
+        if (fuse_dw) {
+            ep.D = D; ep.nq = n; ep.ids = ids; ep.pos = p->pos;
+            ep.dw_ring = conv_l; ep.dw_sstride = p->conv_sstride;
+            ep.dw_wT = Lw.dwT; ep.dw_bias = Lw.bdw; ep.dw_gamma = Lw.bng; ep.dw_beta = Lw.bnb; ep.dw_out = p->yc;
+        }
         PB(P_PW1);
         RET(gemm(m, p->xln, ldl, M, D, Lw.pw1, 0, ep, s, lc, sp));
         PE();
         RET(trace_tap(p, l, 3, p->glu, true, M, s));
-        PB(P_DW);
-        CK(launch_dwconv(p->glu, static_cast<char*>(p->conv) + (long long)l * CONV_CACHE * D * ab, p->conv_sstride,
-                         ids, p->pos, n, n_commit, Lw.dwT, Lw.bdw, Lw.bng, Lw.bnb, p->yc, D, nb, bf, s));
-        PE();
-        ++*lc;
+        if (!fuse_dw) {
+            PB(P_DW);
+            CK(launch_dwconv(p->glu, conv_l, p->conv_sstride, ids, p->pos, n, n_commit, Lw.dwT, Lw.bdw, Lw.bng,
+                             Lw.bnb, p->yc, D, nb, bf, s));
+            PE();
+            ++*lc;
+        }
         RET(trace_tap(p, l, 4, p->yc, true, M, s));
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.pw2.b; ep.x = p->x; ep.ldx = D; ep.scale = 1.f;
         PB(P_PW2);
@@ -870,6 +884,19 @@ extern "C" int cac_pool_create(cac_model* m, int max_streams, int max_frames_per
     p->tail = static_cast<float*>(v);
     if ((r = palloc(p, ab * S * p->ring_sstride, &p->kring)) != CAC_OK) return fail(r);
     if ((r = palloc(p, ab * S * p->ring_sstride, &p->vring)) != CAC_OK) return fail(r);
+    if (m->bf16 && HD == 64 && p->R <= 80) {
+        // tensor maps of the tensor-core attention: one copy = one head's ring of
+        // one stream and layer (R rows), or one head's position table (NR rows)
+        p->amaps.resize(L);
+        for (int l = 0; l < L; ++l) {
+            AttnMaps& am = p->amaps[l];
+            const uint64_t blocks = (uint64_t)S * L * H, bstride = (uint64_t)p->R * HD * 2;
+            if (!make_tmap_bf16_blocks(&am.k, p->kring, p->R, blocks, bstride, p->R) ||
+                !make_tmap_bf16_blocks(&am.v, p->vring, p->R, blocks, bstride, p->R) ||
+                !make_tmap_bf16_blocks(&am.p, m->layers[l].Ppad, m->NR, H, (uint64_t)m->NR * HD * 2, m->NR))
+                return fail(CAC_E_CUDA);
+        }
+    }
     if ((r = palloc(p, ab * S * p->conv_sstride, &p->conv)) != CAC_OK) return fail(r);
     const size_t wsp = m->split ? 2 : 1;  // split windows: rows hi | lo
     if ((r = palloc(p, wsp * ab * ((size_t)S * (TAIL + 8 * n) + 4) * MEL, &p->win1)) != CAC_OK) return fail(r);

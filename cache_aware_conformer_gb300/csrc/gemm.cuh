@@ -19,6 +19,7 @@ enum EpiKind : int {
     EPI_GLU = 2,    // 32-column segments [16 value | 16 gate] -> 16 outputs value * sigmoid(gate)
     EPI_QKV = 3,    // Q (fp32) and K/V written into per-stream rings (or dense buffers)
     EPI_SUB = 4,    // subsampling stage: ReLU(acc + bias), zero before stream start, row remap
+    EPI_GLUDW = 5,  // EPI_GLU, then the causal depthwise conv + affine + SiLU and the conv-ring commit
 };
 enum ActKind : int { ACT_NONE = 0, ACT_RELU = 1, ACT_SILU = 2 };
 
@@ -56,6 +57,21 @@ struct EpiParams {
     int dst_rows = 1, dst_off = 0;
     int tmult = 0, toff = 0;     // absolute time = tmult * pos[id] - toff + t (zeroed when < 0)
     int split_out = 0;           // bf16 only, > 0: also store lo = bf16(v - hi) at column split_out + c
+    // EPI_GLUDW (tcgen05 path, streaming steps): rows b * nq + i (frame i of
+    // batch slot b, 32 % nq == 0, so a stream's rows lie in one warp).  The GLU
+    // value g (rounded to the activation dtype, as stored) goes to out_act
+    // (when set); then, per channel c,
+    //   y = SiLU(dw_gamma[c] * (dw_bias[c] + sum_k dw_wT[k][c] * win_k) + dw_beta[c]) -> dw_out,
+    // win_k = g of frame i - 8 + k: from the conv ring (dw_ring + id * dw_sstride,
+    // slot = absolute frame mod 8, zero before the stream start) or from this
+    // step's rows; afterwards the step's g rows are committed to the ring.
+    void* dw_ring = nullptr;
+    long long dw_sstride = 0;
+    const float* dw_wT = nullptr;   // [9][D]
+    const float* dw_bias = nullptr;
+    const float* dw_gamma = nullptr;
+    const float* dw_beta = nullptr;
+    void* dw_out = nullptr;
 };
 
 // host helpers ---------------------------------------------------------------
@@ -63,6 +79,13 @@ struct EpiParams {
 // rows, box [box_rows][64], 128-byte swizzle.  Returns false on failure.
 bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
                     uint64_t row_stride_bytes, uint32_t box_rows);
+
+// Blocks of 64-wide bf16 rows: 3-D map {64, rows, blocks} (row stride 128 B,
+// block stride block_stride_bytes), box {64, box_rows, 1}, 128-byte swizzle —
+// e.g. one head's K or V ring of one stream and layer, or one head's position
+// table, per copy.
+bool make_tmap_bf16_blocks(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t blocks,
+                           uint64_t block_stride_bytes, uint32_t box_rows);
 
 // Convolution view of a window buffer [rows][C] for a stride-2, kernel-3
 // convolution: 3-D map {C, 2, rows/2} (channel, row parity, row pair), box
@@ -215,6 +238,117 @@ __device__ __forceinline__ void epilogue32(const EpiParams& e, int row, int col0
             for (int i = 0; i < 32; ++i) v[i] -= to_f(from_f<TAct>(v[i]));
             store32<TAct>(dst + e.split_out, v);
         }
+    }
+}
+
+// EPI_GLUDW for one 32-column accumulator segment (16 output channels); every
+// lane of the warp calls it (shuffles), `live` marks rows < M.
+__device__ __forceinline__ void epilogue_gludw(const EpiParams& e, int row, bool live, int col0, float (&v)[32],
+                                               const EpiPre& pre) {
+    const int lane = threadIdx.x & 31;
+    const int D = e.D, C = col0 >> 1, nq = e.nq;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 b = pre.b[i];
+        v[4 * i] += b.x; v[4 * i + 1] += b.y; v[4 * i + 2] += b.z; v[4 * i + 3] += b.w;
+    }
+    float g[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) g[i] = __bfloat162float(__float2bfloat16_rn(v[i] * sigmoidf_(v[16 + i])));
+    const int fi = row % nq, b = row / nq;
+    int id = 0, p0 = 0;
+    if (live) {
+        id = e.ids[b];
+        p0 = e.pos[id];
+    }
+    bf16* ring = static_cast<bf16*>(e.dw_ring) + (long long)id * e.dw_sstride;
+    float acc[16];
+    {
+        const float4* b4 = reinterpret_cast<const float4*>(e.dw_bias + C);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 t = __ldg(b4 + q);
+            acc[4 * q] = t.x; acc[4 * q + 1] = t.y; acc[4 * q + 2] = t.z; acc[4 * q + 3] = t.w;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 9; ++k) {
+        const int d = 8 - k;  // frames back from this row's frame
+        float win[16];
+        if (d == 0) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) win[i] = g[i];
+        } else {
+            // this step's rows (d <= fi): lane - d holds frame fi - d of the same stream
+            float sh[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sh[i] = d < nq ? __shfl_sync(0xffffffffu, g[i], (lane - d) & 31) : 0.f;
+            const int pabs = p0 + fi - d;
+            if (d <= fi) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) win[i] = sh[i];
+            } else if (live && pabs >= 0) {
+                const uint4* src = reinterpret_cast<const uint4*>(ring + (long long)(pabs & 7) * D + C);
+                const uint4 r0 = src[0], r1 = src[1];
+                const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&r0);
+                const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&r1);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 a0 = __bfloat1622float2(h0[i]), a1 = __bfloat1622float2(h1[i]);
+                    win[2 * i] = a0.x; win[2 * i + 1] = a0.y; win[8 + 2 * i] = a1.x; win[8 + 2 * i + 1] = a1.y;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) win[i] = 0.f;
+            }
+        }
+        const float4* w4 = reinterpret_cast<const float4*>(e.dw_wT + (long long)k * D + C);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 w = __ldg(w4 + q);
+            acc[4 * q] = fmaf(w.x, win[4 * q], acc[4 * q]);
+            acc[4 * q + 1] = fmaf(w.y, win[4 * q + 1], acc[4 * q + 1]);
+            acc[4 * q + 2] = fmaf(w.z, win[4 * q + 2], acc[4 * q + 2]);
+            acc[4 * q + 3] = fmaf(w.w, win[4 * q + 3], acc[4 * q + 3]);
+        }
+    }
+    __syncwarp();  // every lane has read the ring before this step's rows are committed
+    if (!live) return;
+    const float4* g4 = reinterpret_cast<const float4*>(e.dw_gamma + C);
+    const float4* be4 = reinterpret_cast<const float4*>(e.dw_beta + C);
+    float y[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 gg = __ldg(g4 + q), bb = __ldg(be4 + q);
+        y[4 * q] = siluf_(fmaf(gg.x, acc[4 * q], bb.x));
+        y[4 * q + 1] = siluf_(fmaf(gg.y, acc[4 * q + 1], bb.y));
+        y[4 * q + 2] = siluf_(fmaf(gg.z, acc[4 * q + 2], bb.z));
+        y[4 * q + 3] = siluf_(fmaf(gg.w, acc[4 * q + 3], bb.w));
+    }
+    auto pack16 = [](const float (&f)[16], uint4& u0, uint4& u1) {
+        uint32_t* w0 = reinterpret_cast<uint32_t*>(&u0);
+        uint32_t* w1 = reinterpret_cast<uint32_t*>(&u1);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 a = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+            const __nv_bfloat162 c = __floats2bfloat162_rn(f[8 + 2 * i], f[8 + 2 * i + 1]);
+            w0[i] = *reinterpret_cast<const uint32_t*>(&a);
+            w1[i] = *reinterpret_cast<const uint32_t*>(&c);
+        }
+    };
+    uint4 u0, u1;
+    pack16(y, u0, u1);
+    uint4* yo = reinterpret_cast<uint4*>(static_cast<bf16*>(e.dw_out) + (long long)row * D + C);
+    yo[0] = u0;
+    yo[1] = u1;
+    pack16(g, u0, u1);
+    uint4* rs = reinterpret_cast<uint4*>(ring + (long long)((p0 + fi) & 7) * D + C);
+    rs[0] = u0;
+    rs[1] = u1;
+    if (e.out_act) {
+        uint4* go = reinterpret_cast<uint4*>(static_cast<bf16*>(e.out_act) + (long long)row * D + C);
+        go[0] = u0;
+        go[1] = u1;
     }
 }
 

@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int row = m0 + rloc;
     const int c_first = half * (BN / 2);
     EpiPre pre;
-    if (crank == 0 && row < M) epi_prefetch<KIND>(ep, row, n0 + c_first, pre);
+    if (crank == 0 && (row < M || KIND == EPI_GLUDW)) epi_prefetch<KIND>(ep, row, n0 + c_first, pre);
 
     if (!mbar_wait(accb, 0)) ok = false;
     pdl_trigger();  // main loop done: let the next kernel launch while the epilogue runs
@@ -179,7 +179,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll
                 for (int k = 0; k < 32; ++k) v[k] += ld_dsmem(&part[(c + k) * BM + rloc], (uint32_t)rr);
             }
-            if (ok && row < M) {
+            if constexpr (KIND == EPI_GLUDW) {
+                if (c != c_first) epi_prefetch<KIND>(ep, row, n0 + c, pre);  // bias only: any row
+                epilogue_gludw(ep, row, ok && row < M, n0 + c, v, pre);
+            } else if (ok && row < M) {
                 if (c != c_first) epi_prefetch<KIND>(ep, row, n0 + c, pre);
                 epilogue32<KIND, TAct>(ep, row, n0 + c, v, pre);
             }
@@ -216,6 +219,23 @@ bool make_tmap_bf16_conv(CUtensorMap* tm, const void* base, uint64_t C, uint64_t
     cuuint64_t dims[3] = {C, 2, pairs};
     cuuint64_t strides[2] = {C * 2, C * 4};
     cuuint32_t box[3] = {64, 1, box_rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_bf16_blocks(CUtensorMap* tm, const void* base, uint64_t rows, uint64_t blocks,
+                           uint64_t block_stride_bytes, uint32_t box_rows) {
+    std::call_once(g_encode_once, load_encode);
+    if (!g_encode) return false;
+    if ((reinterpret_cast<uintptr_t>(base) & 15) || (block_stride_bytes & 15) || rows == 0 || blocks == 0 ||
+        box_rows == 0 || box_rows > 256 || box_rows > rows)
+        return false;
+    cuuint64_t dims[3] = {64, rows, blocks};
+    cuuint64_t strides[2] = {128, block_stride_bytes};
+    cuuint32_t box[3] = {64, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -264,6 +284,7 @@ static cudaError_t launch_bn(const CUtensorMap* tmA, const CUtensorMap* tmB, int
             case EPI_GLU: return launch_bn_kind<BN, EPI_GLU, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
             case EPI_QKV: return launch_bn_kind<BN, EPI_QKV, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
             case EPI_SUB: return launch_bn_kind<BN, EPI_SUB, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+            case EPI_GLUDW: return launch_bn_kind<BN, EPI_GLUDW, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
         }
         return cudaErrorInvalidValue;
     }
@@ -283,6 +304,8 @@ cudaError_t launch_gemm_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, int M
     if (K % BK || K <= 0 || N % BN || !ep.act_bf16) return cudaErrorInvalidValue;
     if (conv_C && (conv_C % BK || K != 3 * conv_C)) return cudaErrorInvalidValue;
     if (splits < 1 || splits > 4 || splits > K / BK) return cudaErrorInvalidValue;
+    if (ep.kind == EPI_GLUDW && (splits != 1 || !a_split || ep.nq < 1 || 32 % ep.nq || 2 * ep.D != N || ep.D % 16))
+        return cudaErrorInvalidValue;
     switch (BN) {
         case 64: return launch_bn<64>(tmA, tmB, M, N, K, conv_C, splits, a_split, ep, status, s);
         case 128: return launch_bn<128>(tmA, tmB, M, N, K, conv_C, splits, a_split, ep, status, s);

@@ -30,6 +30,13 @@ cudaError_t launch_stage_mel(const float* mel, long long mel_bstride, const int*
 cudaError_t launch_stage_mel_offline(const float* mel, int t_mel, const int* len, void* dst, int W, int B,
                                      int act_bf16, int split, int* status, cudaStream_t s);
 
+// Tensor maps of the tensor-core streaming attention (see attn_mma.cu): the K
+// and V rings as blocks of R rows ((stream * L + layer) * H + head), the
+// layer's position table as blocks of NR rows (head).
+struct AttnMaps {
+    CUtensorMap k, v, p;
+};
+
 struct AttnParams {
     const float* q = nullptr;   // fp32 queries, row stride ldq, head h at column h*HD
     int ldq = 0;
@@ -48,6 +55,8 @@ struct AttnParams {
     void* out = nullptr;        // [rows][ldo], activation dtype
     int ldo = 0;
     int out_split = 0;          // bf16 only, > 0: also write lo = bf16(o - hi) at column out_split + c
+    const AttnMaps* maps = nullptr;  // host pointer; tensor-core streaming path only
+    int layer = 0, L = 0;            // ring block coordinate (stream * L + layer) * H + head
                                 // (a split operand for the out-projection; ldo >= 2 * out_split)
     int H = 0, D = 0, HD = 0;
     int left = 0, chunk = 1, rc = 0;  // rc > 0: window mask [p-left, p+rc]; else chunked mask
