@@ -84,6 +84,89 @@ __global__ void __launch_bounds__(256) ln_kernel(const float* x, int M, int D, c
     }
 }
 
+// Vectorized layout for D % 128 == 0: lane holds columns 128 j + 4 lane + e
+// (e < 4) in v[4 j + e]; 16-byte loads, 8- or 16-byte stores.
+template <int VPL>
+__device__ __forceinline__ void ln_row4(float (&v)[VPL], int lane, int D, const float* g, const float* b) {
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) s += v[k];
+    const float mean = warp_sum(s) / D;
+    float q = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPL; ++k) { const float d = v[k] - mean; q += d * d; }
+    const float rstd = rsqrtf(warp_sum(q) / D + 1e-5f);
+#pragma unroll
+    for (int j = 0; j < VPL / 4; ++j) {
+        const int c = 128 * j + 4 * lane;
+        const float4 gg = __ldg(reinterpret_cast<const float4*>(g + c));
+        const float4 bb = __ldg(reinterpret_cast<const float4*>(b + c));
+        v[4 * j] = (v[4 * j] - mean) * rstd * gg.x + bb.x;
+        v[4 * j + 1] = (v[4 * j + 1] - mean) * rstd * gg.y + bb.y;
+        v[4 * j + 2] = (v[4 * j + 2] - mean) * rstd * gg.z + bb.z;
+        v[4 * j + 3] = (v[4 * j + 3] - mean) * rstd * gg.w + bb.w;
+    }
+}
+
+__device__ __forceinline__ uint2 pack4_bf16(float a, float b, float c, float d) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    return make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
+
+template <int VPL, class TA>
+__device__ __forceinline__ void store_act_row4(TA* dst, long long row, int D, int lane, const float (&v)[VPL],
+                                               int split) {
+#pragma unroll
+    for (int j = 0; j < VPL / 4; ++j) {
+        const int c = 128 * j + 4 * lane;
+        const float a0 = v[4 * j], a1 = v[4 * j + 1], a2 = v[4 * j + 2], a3 = v[4 * j + 3];
+        if constexpr (sizeof(TA) == 2) {
+            const uint2 h = pack4_bf16(a0, a1, a2, a3);
+            if (split) {
+                TA* d = dst + row * 2 * D + c;
+                *reinterpret_cast<uint2*>(d) = h;
+                const __nv_bfloat162* hp = reinterpret_cast<const __nv_bfloat162*>(&h);
+                const float2 f0 = __bfloat1622float2(hp[0]), f1 = __bfloat1622float2(hp[1]);
+                *reinterpret_cast<uint2*>(d + D) = pack4_bf16(a0 - f0.x, a1 - f0.y, a2 - f1.x, a3 - f1.y);
+            } else {
+                *reinterpret_cast<uint2*>(dst + row * D + c) = h;
+            }
+        } else {
+            *reinterpret_cast<float4*>(dst + row * D + c) = make_float4(a0, a1, a2, a3);
+        }
+    }
+}
+
+template <int VPL, class TA>
+__global__ void __launch_bounds__(256) ln4_kernel(const float* x, int M, int D, const float* g1, const float* b1,
+                                                  float* y_f32, TA* y_act, const float* g2, const float* b2,
+                                                  TA* z_act, int grp, int grp_stride, int row_off, int split) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= M) return;
+    float v[VPL];
+#pragma unroll
+    for (int j = 0; j < VPL / 4; ++j) {
+        const float4 t = *reinterpret_cast<const float4*>(x + (long long)row * D + 128 * j + 4 * lane);
+        v[4 * j] = t.x; v[4 * j + 1] = t.y; v[4 * j + 2] = t.z; v[4 * j + 3] = t.w;
+    }
+    pdl_trigger();
+    ln_row4<VPL>(v, lane, D, g1, b1);
+    if (y_f32) {
+        const long long orow = (long long)(row / grp) * grp_stride + (row % grp) + row_off;
+#pragma unroll
+        for (int j = 0; j < VPL / 4; ++j)
+            *reinterpret_cast<float4*>(y_f32 + orow * D + 128 * j + 4 * lane) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+    if (y_act) store_act_row4<VPL, TA>(y_act, row, D, lane, v, split);
+    if (g2) {
+        ln_row4<VPL>(v, lane, D, g2, b2);
+        store_act_row4<VPL, TA>(z_act, row, D, lane, v, split);
+    }
+}
+
 template <class TA>
 static cudaError_t ln_dispatch(const float* x, int M, int D, const float* g1, const float* b1, float* y_f32,
                                void* y_act, const float* g2, const float* b2, void* z_act, int grp, int grp_stride,
@@ -95,6 +178,17 @@ static cudaError_t ln_dispatch(const float* x, int M, int D, const float* g1, co
     case V:                                                                                              \
         return launch_k(ln_kernel<V, TA>, grid, dim3(256), 0, s, 1, x, M, D, g1, b1, y_f32, ya, g2, b2, za, grp,   \
                         grp_stride, row_off, split);
+#define LN4_CASE(V)                                                                                      \
+    case V:                                                                                              \
+        return launch_k(ln4_kernel<V, TA>, grid, dim3(256), 0, s, 1, x, M, D, g1, b1, y_f32, ya, g2, b2, za, grp,  \
+                        grp_stride, row_off, split);
+    if (D % 128 == 0) {
+        switch (D / 32) {
+            LN4_CASE(4) LN4_CASE(8) LN4_CASE(16) LN4_CASE(24) LN4_CASE(32)
+            default: return cudaErrorInvalidValue;
+        }
+    }
+#undef LN4_CASE
     switch (D / 32) {
         LN_CASE(2) LN_CASE(4) LN_CASE(8) LN_CASE(16) LN_CASE(24) LN_CASE(32)
         default: return cudaErrorInvalidValue;
