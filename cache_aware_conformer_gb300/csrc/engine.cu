@@ -420,9 +420,12 @@ struct GraphKey {
     const void *mel, *enc, *joint;
     long long mel_bstride;
     int out_bstride, out_off;
+    const void* ids;  // batch slot -> stream id array (a sub-batch's slice)
+    int group;        // scratch set
     bool operator<(const GraphKey& o) const {
-        return std::tie(nb, n, nvalid, mel, enc, joint, mel_bstride, out_bstride, out_off) <
-               std::tie(o.nb, o.n, o.nvalid, o.mel, o.enc, o.joint, o.mel_bstride, o.out_bstride, o.out_off);
+        return std::tie(nb, n, nvalid, mel, enc, joint, mel_bstride, out_bstride, out_off, ids, group) <
+               std::tie(o.nb, o.n, o.nvalid, o.mel, o.enc, o.joint, o.mel_bstride, o.out_bstride, o.out_off, o.ids,
+                        o.group);
     }
 };
 struct GraphEntry {
@@ -431,6 +434,15 @@ struct GraphEntry {
     long long kernels = 0;
 };
 }  // namespace
+
+// Scratch of one step: activations and windows of its rows
+struct Scratch {
+    void *win1 = nullptr, *win2 = nullptr, *win3 = nullptr, *y3 = nullptr;
+    float* x = nullptr;
+    void *xln = nullptr, *h = nullptr, *o = nullptr, *glu = nullptr, *yc = nullptr;
+    float* q = nullptr;
+};
+constexpr int MAX_GROUPS = 4;
 
 struct cac_pool {
     cac_model* m = nullptr;
@@ -443,11 +455,19 @@ struct cac_pool {
     void* kring = nullptr;     // [S][L][H][R][HD]
     void* vring = nullptr;
     void* conv = nullptr;      // [S][L][8][D]
-    // step scratch
+    // step scratch in use (one of sc[], see use_scratch)
     void *win1 = nullptr, *win2 = nullptr, *win3 = nullptr, *y3 = nullptr;
     float* x = nullptr;
     void *xln = nullptr, *h = nullptr, *o = nullptr, *glu = nullptr, *yc = nullptr;
     float* q = nullptr;
+    // A chunked step over many streams runs as up to `groups` concurrent
+    // sub-batches of at most group_streams streams each, forked onto the pool's
+    // own CUDA streams: independent kernel chains overlap one another's
+    // per-kernel latency.  sc[0] holds all S streams (every other path uses it).
+    std::vector<Scratch> sc;
+    int groups = 1, group_streams = 0;
+    cudaStream_t gs[MAX_GROUPS] = {};
+    cudaEvent_t fork_ev = nullptr, join_ev[MAX_GROUPS] = {};
     int* ids_dev = nullptr;     // batch slot -> stream id for the current push
     int* rids_dev = nullptr;    // ids of the current reset
     int* nvalid_dev = nullptr;  // flush: valid mel frames per batch slot
@@ -497,6 +517,13 @@ int palloc(cac_pool* p, size_t bytes, void** out, bool zero = true) {
     if (zero && cudaMemset(d, 0, std::max<size_t>(bytes, 16)) != cudaSuccess) return CAC_E_CUDA;
     *out = d;
     return CAC_OK;
+}
+
+// Make scratch set g the one the step functions use.
+void use_scratch(cac_pool* p, int g) {
+    const Scratch& sc = p->sc[g];
+    p->win1 = sc.win1; p->win2 = sc.win2; p->win3 = sc.win3; p->y3 = sc.y3;
+    p->x = sc.x; p->xln = sc.xln; p->h = sc.h; p->o = sc.o; p->glu = sc.glu; p->yc = sc.yc; p->q = sc.q;
 }
 
 // Copy `n` ids into the next pinned slot and queue their upload to `dst`.
@@ -786,12 +813,13 @@ int run_joint(cac_pool* p, const void* act, int M, int grp, float* joint, int ou
 // One chunked-causal step: nb batch slots (ids in p->ids_dev), n new frames each.
 //   enc/joint: frame i of slot b goes to row b * out_bstride + out_off + i
 int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride, const int* nvalid, float* enc,
-             float* joint, int out_bstride, int out_off, cudaStream_t s) {
-    RET(run_subsample(p, nb, n, mel, mel_bstride, nvalid, p->ids_dev, p->pos, s));
-    RET(run_layers(p, nb, n, n, p->ids_dev, enc, out_bstride, out_off, s));
+             float* joint, int out_bstride, int out_off, cudaStream_t s, const int* ids = nullptr) {
+    if (!ids) ids = p->ids_dev;
+    RET(run_subsample(p, nb, n, mel, mel_bstride, nvalid, ids, p->pos, s));
+    RET(run_layers(p, nb, n, n, ids, enc, out_bstride, out_off, s));
     if (joint) RET(run_joint(p, p->xln, nb * n, n, joint, out_bstride, out_off, nullptr, s));
     PB(P_ADV);
-    CK(launch_advance(p->pos, p->ids_dev, nb, n, s));
+    CK(launch_advance(p->pos, ids, nb, n, s));
     PE();
     ++p->launches;
     return CAC_OK;
@@ -817,24 +845,33 @@ int run_pass(cac_pool* p, int nbp, int P, int E, float* enc, float* joint, cudaS
     return CAC_OK;
 }
 
-// run_step through the graph cache when graphs are enabled
-int step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride, const int* nvalid, float* enc,
-         float* joint, int out_bstride, int out_off, cudaStream_t s) {
-    if (!p->graphs || p->trace || p->prof)
-        return run_step(p, nb, n, mel, mel_bstride, nvalid, enc, joint, out_bstride, out_off, s);
-    GraphKey key{nb, n, nvalid ? 1 : 0, mel, enc, joint, mel_bstride, out_bstride, out_off};
+// One (sub-)batch step with scratch set `group` on stream s, through the
+// graph cache when graphs are enabled (captured on its second sighting).
+int step_one(cac_pool* p, int group, int nb, int n, const float* mel, long long mel_bstride, const int* nvalid,
+             float* enc, float* joint, int out_bstride, int out_off, const int* ids, cudaStream_t s) {
+    use_scratch(p, group);
+    if (!p->graphs || p->trace || p->prof) {
+        const int r = run_step(p, nb, n, mel, mel_bstride, nvalid, enc, joint, out_bstride, out_off, s, ids);
+        use_scratch(p, 0);
+        return r;
+    }
+    GraphKey key{nb, n, nvalid ? 1 : 0, mel, enc, joint, mel_bstride, out_bstride, out_off, ids, group};
     GraphEntry& g = p->gcache[key];
     if (!g.exec) {
-        if (g.seen++ == 0)  // first sighting runs eagerly (sets kernel attributes, warms up)
-            return run_step(p, nb, n, mel, mel_bstride, nvalid, enc, joint, out_bstride, out_off, s);
+        if (g.seen++ == 0) {  // first sighting runs eagerly (sets kernel attributes, warms up)
+            const int r = run_step(p, nb, n, mel, mel_bstride, nvalid, enc, joint, out_bstride, out_off, s, ids);
+            use_scratch(p, 0);
+            return r;
+        }
         cudaStream_t cs;
         CK(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
         const long long before = p->launches;
         cudaGraph_t graph = nullptr;
         CK(cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal));
-        const int r = run_step(p, nb, n, mel, mel_bstride, nvalid, enc, joint, out_bstride, out_off, cs);
+        const int r = run_step(p, nb, n, mel, mel_bstride, nvalid, enc, joint, out_bstride, out_off, cs, ids);
         const cudaError_t e = cudaStreamEndCapture(cs, &graph);
         cudaStreamDestroy(cs);
+        use_scratch(p, 0);
         const long long captured = p->launches - before;
         p->launches = before;
         if (r != CAC_OK) {
@@ -846,8 +883,36 @@ int step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride, co
         g.kernels = captured;
         cudaGraphDestroy(graph);
     }
+    use_scratch(p, 0);
     CK(cudaGraphLaunch(g.exec, s));
     p->launches += g.kernels;
+    return CAC_OK;
+}
+
+// One chunked step.  Over many streams it runs as up to p->groups concurrent
+// sub-batches (contiguous batch slots, <= group_streams each), each on its own
+// pool stream with its own scratch and graph, forked from and joined back into
+// s; traced, profiled and flush steps stay one batch on s.
+int step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride, const int* nvalid, float* enc,
+         float* joint, int out_bstride, int out_off, cudaStream_t s) {
+    const int G = (p->groups > 1 && !nvalid && !p->trace && !p->prof)
+                      ? std::min(p->groups, (nb + p->group_streams - 1) / p->group_streams)
+                      : 1;
+    if (G <= 1) return step_one(p, 0, nb, n, mel, mel_bstride, nvalid, enc, joint, out_bstride, out_off, p->ids_dev, s);
+    const int per = (nb + G - 1) / G;
+    const int D = p->m->D, J = p->m->J;
+    CK(cudaEventRecord(p->fork_ev, s));
+    for (int g = 0; g < G; ++g) {
+        const int b0 = g * per, nbg = std::min(per, nb - b0);
+        if (nbg <= 0) break;
+        CK(cudaStreamWaitEvent(p->gs[g], p->fork_ev, 0));
+        RET(step_one(p, g, nbg, n, mel + (size_t)b0 * mel_bstride, mel_bstride, nullptr,
+                     enc ? enc + (size_t)b0 * out_bstride * D : nullptr,
+                     joint ? joint + (size_t)b0 * out_bstride * J : nullptr, out_bstride, out_off, p->ids_dev + b0,
+                     p->gs[g]));
+        CK(cudaEventRecord(p->join_ev[g], p->gs[g]));
+        CK(cudaStreamWaitEvent(s, p->join_ev[g], 0));
+    }
     return CAC_OK;
 }
 
@@ -899,19 +964,41 @@ extern "C" int cac_pool_create(cac_model* m, int max_streams, int max_frames_per
     }
     if ((r = palloc(p, ab * S * p->conv_sstride, &p->conv)) != CAC_OK) return fail(r);
     const size_t wsp = m->split ? 2 : 1;  // split windows: rows hi | lo
-    if ((r = palloc(p, wsp * ab * ((size_t)S * (TAIL + 8 * n) + 4) * MEL, &p->win1)) != CAC_OK) return fail(r);
-    if ((r = palloc(p, wsp * ab * ((size_t)S * (4 * n + 6) + 4) * D, &p->win2)) != CAC_OK) return fail(r);
-    if ((r = palloc(p, wsp * ab * ((size_t)S * (2 * n + 2) + 4) * D, &p->win3)) != CAC_OK) return fail(r);
-    if ((r = palloc(p, wsp * ab * rows_max * D, &p->y3)) != CAC_OK) return fail(r);
-    if ((r = palloc(p, 4 * rows_max * D, &v)) != CAC_OK) return fail(r);
-    p->x = static_cast<float*>(v);
-    if ((r = palloc(p, ab * rows_max * D * (m->split ? 2 : 1), &p->xln)) != CAC_OK) return fail(r);
-    if ((r = palloc(p, ab * rows_max * F, &p->h)) != CAC_OK) return fail(r);
-    if ((r = palloc(p, 4 * rows_max * D, &v)) != CAC_OK) return fail(r);
-    p->q = static_cast<float*>(v);
-    if ((r = palloc(p, ab * rows_max * D * (m->split ? 2 : 1), &p->o)) != CAC_OK) return fail(r);
-    if ((r = palloc(p, ab * rows_max * D, &p->glu)) != CAC_OK) return fail(r);
-    if ((r = palloc(p, ab * rows_max * D, &p->yc)) != CAC_OK) return fail(r);
+    // scratch for Ss streams of rows_per rows each
+    auto alloc_scratch = [&](int Ss, Scratch& sc) -> int {
+        const size_t rows = (size_t)Ss * rows_per;
+        void* w;
+        int e;
+        if ((e = palloc(p, wsp * ab * ((size_t)Ss * (TAIL + 8 * n) + 4) * MEL, &sc.win1)) != CAC_OK) return e;
+        if ((e = palloc(p, wsp * ab * ((size_t)Ss * (4 * n + 6) + 4) * D, &sc.win2)) != CAC_OK) return e;
+        if ((e = palloc(p, wsp * ab * ((size_t)Ss * (2 * n + 2) + 4) * D, &sc.win3)) != CAC_OK) return e;
+        if ((e = palloc(p, wsp * ab * rows * D, &sc.y3)) != CAC_OK) return e;
+        if ((e = palloc(p, 4 * rows * D, &w)) != CAC_OK) return e;
+        sc.x = static_cast<float*>(w);
+        if ((e = palloc(p, ab * rows * D * wsp, &sc.xln)) != CAC_OK) return e;
+        if ((e = palloc(p, ab * rows * F, &sc.h)) != CAC_OK) return e;
+        if ((e = palloc(p, 4 * rows * D, &w)) != CAC_OK) return e;
+        sc.q = static_cast<float*>(w);
+        if ((e = palloc(p, ab * rows * D * wsp, &sc.o)) != CAC_OK) return e;
+        if ((e = palloc(p, ab * rows * D, &sc.glu)) != CAC_OK) return e;
+        if ((e = palloc(p, ab * rows * D, &sc.yc)) != CAC_OK) return e;
+        return CAC_OK;
+    };
+    // concurrent sub-batches of 64 streams for chunked steps (2 .. 4 of them)
+    p->groups = c.right_context > 0 ? 1 : std::max(1, std::min(MAX_GROUPS, S / 64));
+    p->group_streams = (S + p->groups - 1) / p->groups;
+    p->sc.resize(p->groups);
+    if ((r = alloc_scratch(S, p->sc[0])) != CAC_OK) return fail(r);
+    for (int g = 1; g < p->groups; ++g)
+        if ((r = alloc_scratch(p->group_streams, p->sc[g])) != CAC_OK) return fail(r);
+    for (int g = 0; g < p->groups && p->groups > 1; ++g) {
+        if (cudaStreamCreateWithFlags(&p->gs[g], cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&p->join_ev[g], cudaEventDisableTiming) != cudaSuccess)
+            return fail(CAC_E_CUDA);
+    }
+    if (p->groups > 1 && cudaEventCreateWithFlags(&p->fork_ev, cudaEventDisableTiming) != cudaSuccess)
+        return fail(CAC_E_CUDA);
+    use_scratch(p, 0);
     if ((r = palloc(p, sizeof(int) * S, &v)) != CAC_OK) return fail(r);
     p->ids_dev = static_cast<int*>(v);
     if ((r = palloc(p, sizeof(int) * S, &v)) != CAC_OK) return fail(r);
@@ -963,6 +1050,11 @@ extern "C" void cac_pool_destroy(cac_pool* p) {
     for (int k = 0; k < ID_SLOTS; ++k)
         if (p->slot_ev[k]) cudaEventDestroy(p->slot_ev[k]);
     for (cudaEvent_t e : p->ev) cudaEventDestroy(e);
+    for (int g = 0; g < MAX_GROUPS; ++g) {
+        if (p->gs[g]) cudaStreamDestroy(p->gs[g]);
+        if (p->join_ev[g]) cudaEventDestroy(p->join_ev[g]);
+    }
+    if (p->fork_ev) cudaEventDestroy(p->fork_ev);
     delete p;
 }
 
