@@ -234,17 +234,14 @@ def algorithmic_work(cfg, S, n, mean_lc):
 # ncu capture of the kernel on this workload, with the source files it was
 # built from; reported only while those files are unchanged (see profiles/).
 NCU_TRAFFIC = {
-    "layernorm": (1.069312e6, {"csrc/kernels.cu": "0e003eedcaa93feae2fc3fd550b450c5f478f2d4d8a914faaef8545165bf86db",
-                               "csrc/common.cuh": "1cde4c011b99176dc3625ec3ef613dc325ce852cc62c634440f08710442dfefe"}),
-    "attention": (35.244544e6 + 6.656e3,
-                  {"csrc/attn_mma.cu": "b59d8ea918e0f4554cfcfe9d92fa837db2e9bc9cf613e5aef0902ff31678a461",
-                   "csrc/common.cuh": "1cde4c011b99176dc3625ec3ef613dc325ce852cc62c634440f08710442dfefe"}),
-    "gemm_ff_down": (5.265664e6, {"csrc/gemm_tc.cu": "eb30c869d201935c21973199c48aa4a3976f61d496e6fd74349838cc13037883",
-                                  "csrc/gemm.cuh": "a8085c49820af5f3bba3ea831a8c1f39d10bf36c1da373dd2057bd76be6cb2ea",
-                                  "csrc/common.cuh": "1cde4c011b99176dc3625ec3ef613dc325ce852cc62c634440f08710442dfefe"}),
-    "gemm_ff_up": (3.1808e6, {"csrc/gemm_tc.cu": "eb30c869d201935c21973199c48aa4a3976f61d496e6fd74349838cc13037883",
-                              "csrc/gemm.cuh": "a8085c49820af5f3bba3ea831a8c1f39d10bf36c1da373dd2057bd76be6cb2ea",
-                              "csrc/common.cuh": "1cde4c011b99176dc3625ec3ef613dc325ce852cc62c634440f08710442dfefe"}),
+    "layernorm": (1.06624e6, {"csrc/kernels.cu": "9c7cde9eeb9557b8eabc72fdb61ba180d02e6dd962b88789d6a091ffd04cf867",
+                              "csrc/common.cuh": "2ab32ebd03d406822545c0c7098a0ee10556350c4c503c05c497f403799fbf80"}),
+    "gemm_ff_down": (5.26592e6, {"csrc/gemm_tc.cu": "16899f1c5bbe8c7c060fae79a89ec996fbe3b263a83d4725be0e08bf60bbbd9b",
+                                 "csrc/gemm.cuh": "630556336d7b718b8e46c2f39dc89bac02fb6a0cafc461a266ed4e0eaa74f2f9",
+                                 "csrc/common.cuh": "2ab32ebd03d406822545c0c7098a0ee10556350c4c503c05c497f403799fbf80"}),
+    "gemm_ff_up": (3.180544e6, {"csrc/gemm_tc.cu": "16899f1c5bbe8c7c060fae79a89ec996fbe3b263a83d4725be0e08bf60bbbd9b",
+                                "csrc/gemm.cuh": "630556336d7b718b8e46c2f39dc89bac02fb6a0cafc461a266ed4e0eaa74f2f9",
+                                "csrc/common.cuh": "2ab32ebd03d406822545c0c7098a0ee10556350c4c503c05c497f403799fbf80"}),
 }
 
 
@@ -483,11 +480,14 @@ def run_ours(args, wl):
     latency = {"p50_ms": float(np.percentile(lat, 50)), "p95_ms": float(np.percentile(lat, 95)),
                "pushes": len(lat), "note": "one push of all streams, graph replay, device time"}
 
-    # ---- profiled pass of the same steps: per-kernel-class CUDA events
+    # ---- profiled pass of the same steps: per-kernel-class CUDA events (one
+    # batch of all streams, eager launches; NVTX range "profiled")
     w.pool.set_profile(True)
     w.pool.read_profile()
+    torch.cuda.nvtx.range_push("profiled")
     for _ in range(Kp):
         w.step()
+    torch.cuda.nvtx.range_pop()
     prof = w.pool.read_profile()
     w.pool.set_profile(False)
     hbm_peak, tf_peak, peak_src = load_peaks()
