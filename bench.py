@@ -236,6 +236,9 @@ def algorithmic_work(cfg, S, n, mean_lc):
 NCU_TRAFFIC = {
     "layernorm": (1.06624e6, {"csrc/kernels.cu": "9c7cde9eeb9557b8eabc72fdb61ba180d02e6dd962b88789d6a091ffd04cf867",
                               "csrc/common.cuh": "2ab32ebd03d406822545c0c7098a0ee10556350c4c503c05c497f403799fbf80"}),
+    "attention": (38.913792e6 + 32.768e3,
+                  {"csrc/attn_mma.cu": "130cc104b62a9dffd71e83597ef47cf9b7849c2e7c90856730dc4d56c69b9bde",
+                   "csrc/common.cuh": "2ab32ebd03d406822545c0c7098a0ee10556350c4c503c05c497f403799fbf80"}),
     "gemm_ff_down": (5.26592e6, {"csrc/gemm_tc.cu": "16899f1c5bbe8c7c060fae79a89ec996fbe3b263a83d4725be0e08bf60bbbd9b",
                                  "csrc/gemm.cuh": "630556336d7b718b8e46c2f39dc89bac02fb6a0cafc461a266ed4e0eaa74f2f9",
                                  "csrc/common.cuh": "2ab32ebd03d406822545c0c7098a0ee10556350c4c503c05c497f403799fbf80"}),
