@@ -1288,16 +1288,28 @@ extern "C" int cac_stream_push_host(cac_pool* p, int n, const int* ids, const fl
             return CAC_E_NOMEM;
         p->h_out_cap = enc_n + joint_n;
     }
-    std::memcpy(p->h_mel, mel, mel_n * 4);
-    CK(cudaMemcpyAsync(p->d_mel, p->h_mel, mel_n * 4, cudaMemcpyHostToDevice, s));
+    // page-locked caller buffers are copied directly, pageable ones staged
+    auto locked = [](const void* ptr) {
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        return a.type == cudaMemoryTypeHost;
+    };
+    const bool mel_locked = locked(mel);
+    const bool enc_locked = enc && locked(enc), joint_locked = joint && locked(joint);
+    if (!mel_locked) std::memcpy(p->h_mel, mel, mel_n * 4);
+    CK(cudaMemcpyAsync(p->d_mel, mel_locked ? mel : p->h_mel, mel_n * 4, cudaMemcpyHostToDevice, s));
     float* de = enc ? p->d_out : nullptr;
     float* dj = joint ? p->d_out + enc_n : nullptr;
     RET(cac_stream_push(p, n, ids, p->d_mel, n_mel, de, dj, n_out, stream));
-    if (enc) CK(cudaMemcpyAsync(p->h_out, de, enc_n * 4, cudaMemcpyDeviceToHost, s));
-    if (joint) CK(cudaMemcpyAsync(p->h_out + enc_n, dj, joint_n * 4, cudaMemcpyDeviceToHost, s));
+    if (enc) CK(cudaMemcpyAsync(enc_locked ? enc : p->h_out, de, enc_n * 4, cudaMemcpyDeviceToHost, s));
+    if (joint)
+        CK(cudaMemcpyAsync(joint_locked ? joint : p->h_out + enc_n, dj, joint_n * 4, cudaMemcpyDeviceToHost, s));
     CK(cudaStreamSynchronize(s));
-    if (enc) std::memcpy(enc, p->h_out, enc_n * 4);
-    if (joint) std::memcpy(joint, p->h_out + enc_n, joint_n * 4);
+    if (enc && !enc_locked) std::memcpy(enc, p->h_out, enc_n * 4);
+    if (joint && !joint_locked) std::memcpy(joint, p->h_out + enc_n, joint_n * 4);
     return CAC_OK;
 }
 

@@ -70,7 +70,7 @@ def _lib():
             "cac_stream_destroy": (c_int, [vp, c_int]),
             "cac_stream_reset": (c_int, [vp, c_int, ip, vp]),
             "cac_stream_push": (c_int, [vp, c_int, ip, vp, c_int, vp, vp, ip, vp]),
-            "cac_stream_push_host": (c_int, [vp, c_int, ip, fp, c_int, fp, fp, ip, vp]),
+            "cac_stream_push_host": (c_int, [vp, c_int, ip, vp, c_int, vp, vp, ip, vp]),
             "cac_stream_flush": (c_int, [vp, c_int, ip, vp, c_int, ip, vp, vp, c_int, ip, vp]),
             "cac_stream_flush_frames": (c_int, [vp, c_int, c_int, ip]),
             "cac_encode_offline": (c_int, [vp, c_int, vp, ip, c_int, vp, vp, ip, vp]),
@@ -248,19 +248,34 @@ class Pool:
         n_out = self.push_into(ids, mel.contiguous(), enc, jt, stream)
         return enc, jt, n_out
 
-    def push_host(self, ids, mel: np.ndarray, joint: bool = True, stream=None):
-        """Host-buffer push (cac_stream_push_host): numpy in, numpy out."""
+    def push_host(self, ids, mel, joint: bool = True, stream=None, out=None):
+        """Host-buffer push (cac_stream_push_host).  mel: numpy array or CPU torch
+        tensor [n, n_mel, 128] float32 (pinned tensors are copied directly);
+        out: optional (enc, joint) CPU tensors / arrays to write, else new numpy
+        arrays are returned."""
         ids = list(ids)
-        mel = np.ascontiguousarray(mel, dtype=np.float32)
-        n, n_mel, _ = mel.shape
+        if hasattr(mel, "data_ptr"):  # torch CPU tensor
+            assert mel.dtype.is_floating_point and mel.is_contiguous() and not mel.is_cuda
+            n, n_mel, _ = mel.shape
+            mel_ptr = c_void_p(mel.data_ptr())
+        else:
+            mel = np.ascontiguousarray(mel, dtype=np.float32)
+            n, n_mel, _ = mel.shape
+            mel_ptr = mel.ctypes.data_as(c_void_p)
         F = n_mel // 8
-        enc = np.empty((n, F, self.cfg.d_model), dtype=np.float32)
-        jt = np.empty((n, F, self.cfg.joint_dim), dtype=np.float32) if joint else None
+        if out is not None:
+            enc, jt = out
+        else:
+            enc = np.empty((n, F, self.cfg.d_model), dtype=np.float32)
+            jt = np.empty((n, F, self.cfg.joint_dim), dtype=np.float32) if joint else None
+
+        def addr(a):
+            if a is None:
+                return None
+            return c_void_p(a.data_ptr()) if hasattr(a, "data_ptr") else a.ctypes.data_as(c_void_p)
         n_out = (c_int * n)()
-        fp = POINTER(c_float)
-        _check(_lib().cac_stream_push_host(self.h, n, _ids(ids), mel.ctypes.data_as(fp), n_mel,
-                                           enc.ctypes.data_as(fp), jt.ctypes.data_as(fp) if jt is not None else None,
-                                           n_out, _stream(stream)), "cac_stream_push_host")
+        _check(_lib().cac_stream_push_host(self.h, n, _ids(ids), mel_ptr, n_mel, addr(enc), addr(jt), n_out,
+                                           _stream(stream)), "cac_stream_push_host")
         return enc, jt, list(n_out)
 
     def flush_frames(self, sid: int, n_mel: int) -> int:

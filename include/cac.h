@@ -144,8 +144,10 @@ int  cac_stream_push(cac_pool* p, int n, const int* ids, const float* mel, int n
                      float* enc, float* joint, int* n_out, void* stream);
 
 /* Same as cac_stream_push with HOST buffers: copies mel in and enc/joint out
- * on `stream` through pinned staging owned by the pool, and synchronizes
- * `stream` before returning (enc/joint are valid on return). */
+ * on `stream` and synchronizes `stream` before returning (enc/joint are valid
+ * on return).  Page-locked caller buffers (cudaHostAlloc / cudaHostRegister)
+ * are copied directly; pageable ones go through pinned staging owned by the
+ * pool (one extra host copy each way). */
 int  cac_stream_push_host(cac_pool* p, int n, const int* ids, const float* mel, int n_mel,
                           float* enc, float* joint, int* n_out, void* stream);
 

@@ -237,6 +237,13 @@ def test_push_host_matches_device_push():
     e0, j0, _ = _push(pools[0], [ids[0]], [mel])
     e1, j1, n1 = pools[1].push_host([ids[1]], mel[None])
     assert n1 == [8] and np.array_equal(e0, e1) and np.array_equal(j0, j1)
+    # page-locked buffers take the direct-copy path: same results
+    pools.append(native.Pool(model, 2, 8))
+    ids.append(pools[2].create_stream())
+    mel_p = torch.from_numpy(mel[None]).pin_memory()
+    out = (torch.empty(1, 8, cfg.d_model).pin_memory(), torch.empty(1, 8, cfg.joint_dim).pin_memory())
+    e2, j2, n2 = pools[2].push_host([ids[2]], mel_p, out=out)
+    assert n2 == [8] and np.array_equal(e0, e2.numpy()) and np.array_equal(j0, j2.numpy())
 
 
 def test_c600m_shape_multistream():
