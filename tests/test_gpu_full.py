@@ -135,3 +135,110 @@ def test_config3_256_streams_sampled(eou_blob):
         assert_close(ge, re, cfg, f"stream {s}")
         # bookkeeping: subT and Lc after the last step are exact
         assert states[s]["subT"] == ref[k][-1][2] and states[s]["Lc"] == ref[k][-1][3]
+
+
+# ---------------------------------------------------------------------------
+# the 600M encoder (24 layers, d_model 1024) and the provisional-tail variant,
+# each in the launch configuration the benchmark times, on sampled outputs
+# ---------------------------------------------------------------------------
+def _oracle_offline_window(args):
+    cfg, blob_path, wid, T, silence = args
+    from oracle import conformer as O
+    W = synth.unpack_weights(cfg, np.load(blob_path, mmap_mode="r"))
+    enc, joint = O.encode_offline(synth.make_mel(T, wid, silence_frac=silence), W, cfg)
+    return enc, joint
+
+
+def _oracle_schedule_any(args):
+    """Replay one stream of a benchmark schedule (pre-roll, then steps with
+    resets); chunked or provisional-tail encoder by the config."""
+    cfg, blob_path, sid, pre, chunks, resets, push_mel, n_chunks, silence = args
+    from oracle import conformer as O
+    W = synth.unpack_weights(cfg, np.load(blob_path, mmap_mode="r"))
+    mel = synth.make_mel(n_chunks * push_mel, sid, silence_frac=silence)
+    enc = O.ProvisionalTailEncoder(W, cfg) if cfg.provisional else O.StreamingEncoder(W, cfg)
+    for r in range(pre):
+        enc.push(mel[push_mel * r: push_mel * (r + 1)])
+    out = []
+    for c, rs in zip(chunks, resets):
+        if rs:
+            enc.reset()
+        e, _ = enc.push(mel[push_mel * c: push_mel * (c + 1)])
+        out.append(e)
+    return out
+
+
+@pytest.fixture(scope="module")
+def c600m_blob(tmp_path_factory):
+    from cache_aware_conformer_gb300.config import C600M
+    W = synth.make_weights_parallel(C600M, seed=0, workers=8)
+    blob = synth.pack_weights(C600M, W)
+    del W
+    path = str(tmp_path_factory.mktemp("w600") / "c600m.npy")
+    np.save(path, blob)
+    return C600M, path
+
+
+def test_config4a_offline_600m_sampled(c600m_blob):
+    """32 windows of 1501 mel through the offline encode the benchmark times;
+    windows 0 and 31 against the oracle's offline encode."""
+    import bench
+    cfg, path = c600m_blob
+    wl = WORKLOADS["c600m_offline_32x15s"]
+    sample = [0, wl.offline_batch - 1]
+    jobs = [(cfg, path, w, wl.offline_mel, wl.silence_frac) for w in sample]
+    with mp.get_context("spawn").Pool(len(sample)) as pool:
+        fut = pool.map_async(_oracle_offline_window, jobs)
+        w = bench.OfflineWorkload(wl, 0, torch.device(DEV), workers=8)
+        w.step()
+        torch.cuda.synchronize()
+        got = [(w.enc[k].cpu().numpy(), w.joint[k].cpu().numpy()) for k in sample]
+        w.model.check()
+        ref = fut.get()
+    for (ge, gj), (re, rj), k in zip(got, ref, sample):
+        assert ge.shape == re.shape == (188, cfg.d_model)
+        assert_close(ge, re, cfg, f"offline window {k}")
+
+
+def _stream_schedule_test(wl, cfg, path, steps, sample):
+    import bench
+    w = bench.StreamWorkload(wl, 0, torch.device(DEV), steps, workers=8)
+    jobs = [(cfg, path, s, int(w.pre[s]), [int(w.cidx[t][s]) for t in range(steps)],
+             [bool(s in set(w.resets[t].tolist())) for t in range(steps)], w.push_mel, w.chunks, wl.silence_frac)
+            for s in sample]
+    with mp.get_context("spawn").Pool(len(sample)) as pool:
+        fut = pool.map_async(_oracle_schedule_any, jobs)
+        w.pool.set_graphs(True)
+        got = {s: [] for s in sample}
+        for t in range(steps):
+            r = w.resets[t]
+            if len(r):
+                w.pool.reset([w.ids[i] for i in r])
+            w.staging.copy_(w.step_mel[t])
+            n_out = w.pool.push_into(w.ids, w.staging, w.enc, w.joint)
+            for s in sample:
+                got[s].append(w.enc[s, :n_out[s]].cpu().numpy())
+            w.t += 1
+        w.pool.check()
+        ref = fut.get()
+    for k, s in enumerate(sample):
+        assert [g.shape[0] for g in got[s]] == [e.shape[0] for e in ref[k]], f"stream {s}: emitted frame counts"
+        ge, re = np.concatenate(got[s]), np.concatenate(ref[k])
+        assert_close(ge, re, cfg, f"stream {s}")
+
+
+def test_config4b_600m_64_streams_sampled(c600m_blob):
+    cfg, path = c600m_blob
+    wl = WORKLOADS["c600m_64streams_30s"]
+    _stream_schedule_test(wl, cfg, path, 16, [0, 31, wl.streams - 1])
+
+
+def test_config5_provisional_128_streams_sampled(eou_blob):
+    from cache_aware_conformer_gb300.config import EOU_RC3
+    wl = WORKLOADS["eou120m_rc3_128streams_30s"]
+    cfg = wl.model
+    W = synth.make_weights_parallel(cfg, seed=0, workers=8)
+    path = eou_blob[2].replace("eou.npy", "rc3.npy")
+    np.save(path, synth.pack_weights(cfg, W))
+    del W
+    _stream_schedule_test(wl, cfg, path, 16, [0, 64, wl.streams - 1])
