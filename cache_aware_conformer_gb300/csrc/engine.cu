@@ -84,6 +84,7 @@ struct cac_model {
     cac_config cfg{};
     int bf16 = 1, tc = 1;
     int split = 1;  // bf16: LayerNorm outputs enter their GEMMs as split (hi, lo) operands
+    int split_ffh = 0;  // bf16, d_model >= 1024: the FF hidden activations enter the down-projection split too
     int D = 0, H = 0, HD = 0, F = 0, L = 0, J = 0;
     int rmin = 0, NR = 0;
     std::vector<void*> allocs;
@@ -245,6 +246,7 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
     m->bf16 = cfg->dtype == CAC_DTYPE_BF16;
     m->tc = m->bf16 && !cfg->gemm_simt;
     m->split = m->bf16;
+    m->split_ffh = m->bf16 && cfg->d_model >= 1024;
     m->D = cfg->d_model;
     m->H = cfg->n_heads;
     m->HD = m->D / m->H;
@@ -670,6 +672,8 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
     const size_t ab = act_bytes(m);
     const int bf = m->bf16, sp = m->split;
     const long long ldl = sp ? 2LL * D : D;  // row stride of the split LayerNorm outputs in xln
+    const int shf = m->split_ffh;
+    const long long ldh = shf ? 2LL * F : F;  // row stride of the FF hidden activations (split: hi | lo)
     PB(P_LN);
     CK(launch_layernorm(p->x, M, D, m->layers[0].ff1_g, m->layers[0].ff1_b, nullptr, p->xln, nullptr, nullptr,
                         nullptr, bf, 1 << 30, 0, 0, sp, s));
@@ -680,13 +684,13 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
         const LayerW& Lw = m->layers[l];
         EpiParams ep;
         // FF1: x += 1/2 * (W2 SiLU(W1 LN(x) + b1) + b2)   (LN(x) already in xln)
-        ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff1_w1.b; ep.out_act = p->h; ep.ldo = F;
+        ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff1_w1.b; ep.out_act = p->h; ep.ldo = ldh; ep.split_out = shf ? F : 0;
         PB(P_FFUP);
         RET(gemm(m, p->xln, ldl, M, D, Lw.ff1_w1, 0, ep, s, lc, sp));
         PE();
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.ff1_w2.b; ep.x = p->x; ep.ldx = D; ep.scale = 0.5f;
         PB(P_FFDOWN);
-        RET(gemm(m, p->h, F, M, F, Lw.ff1_w2, 0, ep, s, lc));
+        RET(gemm(m, p->h, ldh, M, F, Lw.ff1_w2, 0, ep, s, lc, shf));
         PE();
         RET(trace_tap(p, l, 0, p->x, false, M, s));
         // attention: xln = LN(x); Q and K/V into the rings
@@ -765,13 +769,13 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
                             1 << 30, 0, 0, sp, s));
         PE();
         ++*lc;
-        ep = EpiParams(); ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff2_w1.b; ep.out_act = p->h; ep.ldo = F;
+        ep = EpiParams(); ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff2_w1.b; ep.out_act = p->h; ep.ldo = ldh; ep.split_out = shf ? F : 0;
         PB(P_FFUP);
         RET(gemm(m, p->xln, ldl, M, D, Lw.ff2_w1, 0, ep, s, lc, sp));
         PE();
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.ff2_w2.b; ep.x = p->x; ep.ldx = D; ep.scale = 0.5f;
         PB(P_FFDOWN);
-        RET(gemm(m, p->h, F, M, F, Lw.ff2_w2, 0, ep, s, lc));
+        RET(gemm(m, p->h, ldh, M, F, Lw.ff2_w2, 0, ep, s, lc, shf));
         PE();
         // ln_out, fused with the next layer's FF1 LayerNorm (or, after the last
         // layer, writing the encoder frames to the caller and the joint input)
@@ -976,7 +980,7 @@ extern "C" int cac_pool_create(cac_model* m, int max_streams, int max_frames_per
         if ((e = palloc(p, 4 * rows * D, &w)) != CAC_OK) return e;
         sc.x = static_cast<float*>(w);
         if ((e = palloc(p, ab * rows * D * wsp, &sc.xln)) != CAC_OK) return e;
-        if ((e = palloc(p, ab * rows * F, &sc.h)) != CAC_OK) return e;
+        if ((e = palloc(p, ab * rows * F * (m->split_ffh ? 2 : 1), &sc.h)) != CAC_OK) return e;
         if ((e = palloc(p, 4 * rows * D, &w)) != CAC_OK) return e;
         sc.q = static_cast<float*>(w);
         if ((e = palloc(p, ab * rows * D * wsp, &sc.o)) != CAC_OK) return e;
@@ -1408,7 +1412,7 @@ OfflineLayout offline_layout(const cac_model* m, int B, int t_mel_max) {
     y.o_y3 = take(wsp * ab * M * D);
     y.o_x = take(4 * M * D);
     y.o_xln = take(ab * M * D * (m->split ? 2 : 1));
-    y.o_h = take(ab * M * F);
+    y.o_h = take(ab * M * F * (m->split_ffh ? 2 : 1));
     y.o_q = take(4 * M * D);
     y.o_k = take(ab * M * D);
     y.o_v = take(ab * M * D);
@@ -1481,16 +1485,18 @@ int offline_run(cac_model* m, char* w, const OfflineLayout& lay, int B, const fl
         RET(gemm(m, y3, rwd, (int)M, D, m->subo, 0, eo, s, &lc, sp));
     }
     const long long ldl = sp ? 2LL * D : D;  // row stride of the split LayerNorm outputs in xln
+    const int shf = m->split_ffh;
+    const long long ldh = shf ? 2LL * F : F;  // row stride of the FF hidden activations (split: hi | lo)
     CK(launch_layernorm(x, (int)M, D, m->layers[0].ff1_g, m->layers[0].ff1_b, nullptr, xln, nullptr, nullptr, nullptr,
                         bf, 1 << 30, 0, 0, sp, s));
     ++lc;
     for (int l = 0; l < L; ++l) {
         const LayerW& Lw = m->layers[l];
         EpiParams ep;
-        ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff1_w1.b; ep.out_act = h; ep.ldo = F;
+        ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff1_w1.b; ep.out_act = h; ep.ldo = ldh; ep.split_out = shf ? F : 0;
         RET(gemm(m, xln, ldl, (int)M, D, Lw.ff1_w1, 0, ep, s, &lc, sp));
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.ff1_w2.b; ep.x = x; ep.ldx = D; ep.scale = 0.5f;
-        RET(gemm(m, h, F, (int)M, F, Lw.ff1_w2, 0, ep, s, &lc));
+        RET(gemm(m, h, ldh, (int)M, F, Lw.ff1_w2, 0, ep, s, &lc, shf));
         CK(launch_layernorm(x, (int)M, D, Lw.att_g, Lw.att_b, nullptr, xln, nullptr, nullptr, nullptr, bf, 1 << 30, 0,
                             0, sp, s));
         ep = EpiParams(); ep.kind = EPI_QKV; ep.bias = Lw.qkv.b; ep.D = D; ep.HD = m->HD; ep.dense = 1;
@@ -1517,10 +1523,10 @@ int offline_run(cac_model* m, char* w, const OfflineLayout& lay, int B, const fl
         RET(gemm(m, yc, D, (int)M, D, Lw.pw2, 0, ep, s, &lc));
         CK(launch_layernorm(x, (int)M, D, Lw.ff2_g, Lw.ff2_b, nullptr, xln, nullptr, nullptr, nullptr, bf, 1 << 30, 0,
                             0, sp, s));
-        ep = EpiParams(); ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff2_w1.b; ep.out_act = h; ep.ldo = F;
+        ep = EpiParams(); ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff2_w1.b; ep.out_act = h; ep.ldo = ldh; ep.split_out = shf ? F : 0;
         RET(gemm(m, xln, ldl, (int)M, D, Lw.ff2_w1, 0, ep, s, &lc, sp));
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.ff2_w2.b; ep.x = x; ep.ldx = D; ep.scale = 0.5f;
-        RET(gemm(m, h, F, (int)M, F, Lw.ff2_w2, 0, ep, s, &lc));
+        RET(gemm(m, h, ldh, (int)M, F, Lw.ff2_w2, 0, ep, s, &lc, shf));
         if (l + 1 < L)
             CK(launch_layernorm(x, (int)M, D, Lw.out_g, Lw.out_b, x, nullptr, m->layers[l + 1].ff1_g,
                                 m->layers[l + 1].ff1_b, xln, bf, 1 << 30, 0, 0, sp, s));

@@ -183,7 +183,15 @@ __device__ __forceinline__ void epilogue32(const EpiParams& e, int row, int col0
         const int g = row / e.grp;
         const long long orow = (long long)(e.grp_map ? e.grp_map[g] : g) * e.grp_stride + (row % e.grp) + e.row_off;
         if (e.out_f32) store32<float>(e.out_f32 + orow * e.ldo + col0, v);
-        if (e.out_act) store32<TAct>(reinterpret_cast<TAct*>(e.out_act) + orow * e.ldo + col0, v);
+        if (e.out_act) {
+            TAct* dst = reinterpret_cast<TAct*>(e.out_act) + orow * e.ldo + col0;
+            store32<TAct>(dst, v);
+            if (e.split_out > 0) {  // split operand for the next GEMM: lo = bf16(v - hi)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] -= to_f(from_f<TAct>(v[i]));
+                store32<TAct>(dst + e.split_out, v);
+            }
+        }
     } else if constexpr (KIND == EPI_RESID) {
         float4* x4 = reinterpret_cast<float4*>(e.x + (long long)row * e.ldx + col0);
 #pragma unroll
