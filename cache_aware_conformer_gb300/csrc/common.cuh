@@ -113,6 +113,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
     return done != 0;
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // Bounded wait: gives up after ~2^32 SM clock cycles (about 2 s at 2 GHz)
 // and returns false, so that a logic error turns into a latched status instead
 // of a hung GPU.

@@ -61,7 +61,9 @@ struct Lin {
     float* b = nullptr;  // [N] or null
     int N = 0, K = 0;
     int BN = 128;
-    CUtensorMap tm;      // bf16 weights on the tcgen05 path
+    CUtensorMap tm;      // bf16 weights on the tcgen05 path (BN-row boxes)
+    CUtensorMap tm128;   // the same with 128-row boxes (persistent GEMM), when N % 128 == 0
+    bool has128 = false;
 };
 
 struct LayerW {
@@ -85,6 +87,7 @@ struct cac_model {
     int bf16 = 1, tc = 1;
     int split = 1;  // bf16: LayerNorm outputs enter their GEMMs as split (hi, lo) operands
     int split_ffh = 0;  // bf16, d_model >= 1024: the FF hidden activations enter the down-projection split too
+    int sms = 152;      // streaming multiprocessors of the device
     int D = 0, H = 0, HD = 0, F = 0, L = 0, J = 0;
     int rmin = 0, NR = 0;
     std::vector<void*> allocs;
@@ -146,6 +149,8 @@ int upload_lin(cac_model* m, const float* w, const float* b, int N, int K, Lin* 
         lin->BN = 64;  // 128 x 64 tiles: M = 512 rows already give 4 x N/64 CTAs
         if (N % lin->BN || K % 64) return CAC_E_UNSUPPORTED;
         if (!make_tmap_bf16(&lin->tm, p, K, N, (uint64_t)K * 2, lin->BN)) return CAC_E_CUDA;
+        lin->has128 = N % 128 == 0;
+        if (lin->has128 && !make_tmap_bf16(&lin->tm128, p, K, N, (uint64_t)K * 2, 128)) return CAC_E_CUDA;
     }
     return CAC_OK;
 }
@@ -205,6 +210,13 @@ int gemm(cac_model* m, const void* A, long long lda, int M, int K, const Lin& W,
         const bool ok = conv_C ? make_tmap_bf16_conv(&tmA, A, (uint64_t)conv_C * (a_split ? 2 : 1), (uint64_t)M + 1, 128)
                                : make_tmap_bf16(&tmA, A, a_split ? 2 * K : K, M, (uint64_t)lda * 2, 128);
         if (!ok) return CAC_E_CUDA;
+        // many output tiles (the offline encode): the persistent kernel, whose
+        // epilogue of one tile overlaps the main loop of the next
+        if (W.has128 && ep.kind != EPI_GLUDW && (long long)((M + 127) / 128) * (W.N / 128) >= 2 * m->sms) {
+            CK(launch_gemm_tc_persistent(&tmA, &W.tm128, M, W.N, K, conv_C, a_split, ep, m->status, s));
+            ++*launches;
+            return CAC_OK;
+        }
         // the fused depthwise conv reads its stream's rows within one CTA: no split-K
         const int splits = ep.kind == EPI_GLUDW ? 1 : choose_splits((W.N / W.BN) * ((M + 127) / 128), K / 64);
         CK(launch_gemm_tc(&tmA, &W.tm, M, W.N, K, W.BN, conv_C, splits, a_split, ep, m->status, s));
@@ -247,6 +259,10 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
     m->tc = m->bf16 && !cfg->gemm_simt;
     m->split = m->bf16;
     m->split_ffh = m->bf16 && cfg->d_model >= 1024;
+    {
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&m->sms, cudaDevAttrMultiProcessorCount, dev);
+    }
     m->D = cfg->d_model;
     m->H = cfg->n_heads;
     m->HD = m->D / m->H;

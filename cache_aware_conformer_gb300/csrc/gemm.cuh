@@ -102,6 +102,13 @@ bool make_tmap_bf16_conv(CUtensorMap* tm, const void* base, uint64_t C, uint64_t
 cudaError_t launch_gemm_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int BN, int conv_C,
                            int splits, int a_split, const EpiParams& ep, int* status, cudaStream_t s);
 
+// Persistent tcgen05 GEMM for many output tiles (128 x 128 tiles, one CTA per
+// SM, two TMEM accumulators so epilogue and main loop overlap).  tmB128: the
+// weight map with 128-row boxes.  N % 128 == 0; other rules as launch_gemm_tc
+// (no split-K, no EPI_GLUDW).
+cudaError_t launch_gemm_tc_persistent(const CUtensorMap* tmA, const CUtensorMap* tmB128, int M, int N, int K,
+                                      int conv_C, int a_split, const EpiParams& ep, int* status, cudaStream_t s);
+
 // SIMT GEMM (fp32 or bf16 operands, fp32 accumulate).  N % 32 == 0.  a_split
 // (bf16 only): A row r holds hi at A + r * lda and lo at A + r * lda + K.
 // conv_C > 0: A is a stride-2 convolution window (lda = row-pair stride), K

@@ -58,3 +58,29 @@ def test_gpu_streaming_equals_gpu_offline():
     st = np.concatenate(outs)
     assert st.shape[0] == out_len[0] == 151
     assert_close(st, enc_off[0, :151].cpu().numpy(), cfg, "stream vs offline")
+
+
+def test_offline_many_tiles_persistent_gemm():
+    """Enough windows that every projection of the 600M layer shapes has more
+    than two 128 x 128 output tiles per SM (the persistent GEMM path), with
+    ragged lengths so the last row tile is partial; sampled windows against the
+    oracle."""
+    cfg = replace(C600M, n_layers=2)
+    W, model = make_model(cfg)
+    lens = [1501] * 40
+    lens[17], lens[39] = 777, 1203
+    batch = np.zeros((len(lens), 1501, 128), np.float32)
+    sample = [0, 17, 39]
+    mels = {}
+    for k, n in enumerate(lens):
+        m = synth.make_mel(n, 300 + k)
+        batch[k, :n] = m
+        if k in sample:
+            mels[k] = m
+    enc, joint, out_len = model.encode_offline(torch.from_numpy(batch).to(DEV), lens)
+    model.check()
+    for k in sample:
+        er, jr = O.encode_offline(mels[k], W, cfg)
+        assert out_len[k] == er.shape[0]
+        assert_close(enc[k, :out_len[k]].cpu().numpy(), er, cfg, f"enc window {k}")
+        assert_close(joint[k, :out_len[k]].cpu().numpy(), jr, cfg, f"joint window {k}")
