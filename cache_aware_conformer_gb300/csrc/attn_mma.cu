@@ -376,12 +376,143 @@ __global__ void __launch_bounds__(AW_THREADS, 1)
     }
     pdl_trigger();
 }
+// Offline encode, chunked mask: block (h, sequence) stages the sequence's K
+// and V rows of head h once (one TMA copy each) plus the head's position
+// table; AO_WARPS warps take the sequence's query chunks round-robin.  A chunk
+// of nq <= chunk queries at q0 (a multiple of chunk) sees the keys klo =
+// max(q0 - left, 0) .. q0 + nq - 1: the streaming unit with Lc = q0 - klo whose
+// logical key j sits in shared row klo + j.  Its score tiles read the 80 rows
+// klo .. klo + 79, so the staged block holds ao_rows(T, left) >= T + 79 - left
+// rows; rows from the sequence length on are zeroed (their probabilities are
+// 0, and 0 * V must stay 0).
+constexpr int AO_WARPS = 8;
+constexpr int AO_THREADS = 32 * AO_WARPS;
+
+__host__ __device__ constexpr int ao_rows(int T, int left) {
+    return ((T + 80 - left > AM_ROWS ? T + 80 - left : AM_ROWS) + 15) / 16 * 16;
+}
+inline size_t ao_smem(int rows) {
+    return 1024 /*align*/ + AM_MAT + 2 * (size_t)rows * AM_ROWB + (size_t)AO_WARPS * AW_SCORES + 2 * 8;
+}
+
+__global__ void __launch_bounds__(AO_THREADS)
+    attn_offline_mma_kernel(const __grid_constant__ AttnMaps tm, AttnParams a, int* status) {
+    extern __shared__ uint8_t sm_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
+    const int h = blockIdx.x, seq = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rows = ao_rows(a.T, a.left);
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t Pm = sbase, Km = sbase + AM_MAT, Vm = Km + rows * AM_ROWB;
+    float* scores = reinterpret_cast<float*>(sm + AM_MAT + 2 * rows * AM_ROWB);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(scores + AO_WARPS * AW_SCORES / 4);  // [0] table, [1] K/V
+    constexpr int HD = 64;
+
+    for (int e = threadIdx.x; e < (AM_ROWS - a.NR) * 8; e += blockDim.x)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(Pm + swz(a.NR + (e >> 3), e & 7)), "r"(0)
+                     : "memory");
+    if (threadIdx.x == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+        mbar_expect_tx(&bar[0], (uint32_t)a.NR * AM_ROWB);
+        tma_load_3d(sm, &tm.p, 0, 0, h, &bar[0]);  // weights: before the wait on the previous kernel
+    }
+    __syncthreads();
+    pdl_wait();
+    if (threadIdx.x == 0) {
+        mbar_expect_tx(&bar[1], 2u * rows * AM_ROWB);
+        tma_load_2d(sm + AM_MAT, &tm.k, h * HD, seq * a.T, &bar[1]);
+        tma_load_2d(sm + AM_MAT + rows * AM_ROWB, &tm.v, h * HD, seq * a.T, &bar[1]);
+    }
+    const int len = a.seq_len[seq];
+    const bool landed = mbar_wait(&bar[0], 0) && mbar_wait(&bar[1], 0);
+    if (!__syncthreads_and(landed)) {
+        if (threadIdx.x == 0) latch_error(status, CAC_E_TIMEOUT);
+        return;
+    }
+    for (int e = threadIdx.x; e < (rows - len) * 8; e += blockDim.x) {
+        const int r = len + (e >> 3);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(Km + swz(r, e & 7)), "r"(0) : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(Vm + swz(r, e & 7)), "r"(0) : "memory");
+    }
+    __syncthreads();
+
+    AttnParams ao = a;
+    ao.R = 1 << 20;  // no ring: logical key j of a chunk at shared row klo + j
+    float* Sac = scores + warp * (AW_SCORES / 4);
+    float* Sbd = Sac + 4 * AM_SLD;
+    const int g = lane >> 2, c = lane & 3;
+    const long long rb = (long long)seq * a.T;
+    for (int u = warp; u * a.chunk < len; u += AO_WARPS) {
+        const int q0 = u * a.chunk, nq = min(a.chunk, len - q0);
+        const int klo = max(q0 - a.left, 0), Lc = q0 - klo;
+        uint32_t bu[4][2], bv[4][2];
+        query_frags(a, a.q + (rb + q0) * a.ldq + h * HD, h, nq, lane, bu, bv);
+        float acc[4][4];
+        attend_unit(ao, Pm, Km, Vm, klo, bu, bv, Sac, Sbd, q0, Lc, nq, lane, acc);
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) acc[mt][q4] += __shfl_xor_sync(0xffffffffu, acc[mt][q4], 2);
+        float* O = Sbd;
+        if (c < 2) {
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                const int d = mt * 16 + g;
+                O[(2 * c) * 64 + d] = acc[mt][0];
+                O[(2 * c + 1) * 64 + d] = acc[mt][1];
+                O[(2 * c) * 64 + d + 8] = acc[mt][2];
+                O[(2 * c + 1) * 64 + d + 8] = acc[mt][3];
+            }
+        }
+        __syncwarp();
+        bf16* dst = static_cast<bf16*>(a.out) + (rb + q0) * a.ldo + h * HD;
+        for (int i = 0; i < nq; ++i) {
+            const float2 o = *reinterpret_cast<const float2*>(O + i * 64 + 2 * lane);
+            const __nv_bfloat162 hi2 = __floats2bfloat162_rn(o.x, o.y);
+            bf16* row = dst + (long long)i * a.ldo + 2 * lane;
+            *reinterpret_cast<__nv_bfloat162*>(row) = hi2;
+            if (a.out_split > 0) {
+                const float2 hf = __bfloat1622float2(hi2);
+                *reinterpret_cast<__nv_bfloat162*>(row + a.out_split) =
+                    __floats2bfloat162_rn(o.x - hf.x, o.y - hf.y);
+            }
+        }
+        __syncwarp();  // the output staging is read before the next chunk's bd scores overwrite it
+    }
+    pdl_trigger();
+}
+
 }  // namespace
 
 bool attention_stream_mma_ok(const AttnParams& a, int act_bf16) {
     return act_bf16 && a.maps && a.HD == 64 && a.R <= AM_ROWS && a.R >= a.left + a.nq && a.nq >= 1 && a.nq <= 4 &&
            a.left + a.nq <= AM_ROWS && a.NR <= AM_ROWS && a.rmin <= 0 && a.ldq % 2 == 0 && a.ldo % 2 == 0 &&
            a.out_split % 2 == 0;
+}
+
+bool attention_offline_mma_ok(const AttnParams& a, int act_bf16) {
+    // keys of a chunk: q0 - left .. q0 + chunk - 1 (<= 80 rows); rel = p_q - p_k in
+    // -(chunk - 1) .. left + chunk - 1 must index the table rows 0 .. NR - 1 < 80
+    return act_bf16 && a.maps && a.HD == 64 && a.rc == 0 && a.chunk >= 1 && a.chunk <= 4 && a.left >= 0 &&
+           a.left + a.chunk <= AM_ROWS && a.NR <= AM_ROWS && a.rmin <= -(a.chunk - 1) &&
+           a.left + a.chunk - 1 - a.rmin < a.NR && a.T >= 1 && ao_rows(a.T, a.left) <= 256 &&
+           ao_smem(ao_rows(a.T, a.left)) <= 227 * 1024 && a.ldq % 2 == 0 && a.ldo % 2 == 0 && a.out_split % 2 == 0;
+}
+
+int attention_offline_box_rows(int T, int left) { return ao_rows(T, left); }
+
+cudaError_t launch_attention_offline_mma(const AttnParams& a, int* status, cudaStream_t s) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(attn_offline_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             227 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    return launch_k(attn_offline_mma_kernel, dim3(a.H, a.nb), dim3(AO_THREADS), ao_smem(ao_rows(a.T, a.left)), s, 1,
+                    *a.maps, a, status);
 }
 
 cudaError_t launch_attention_stream_mma(const AttnParams& a, int* status, cudaStream_t s) {

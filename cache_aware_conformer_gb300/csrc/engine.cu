@@ -71,6 +71,8 @@ struct LayerW {
           *conv_b = nullptr, *ff2_g = nullptr, *ff2_b = nullptr, *out_g = nullptr, *out_b = nullptr;
     Lin ff1_w1, ff1_w2, qkv, wo, pw1, pw2, ff2_w1, ff2_w2;
     void* Ppad = nullptr;  // attention position table [H][NR][HD], activation dtype
+    CUtensorMap Pmap;      // bf16, HD 64: one copy = one head's table (NR rows)
+    bool has_pmap = false;
     float *pbu = nullptr, *pbv = nullptr, *P = nullptr, *dwT = nullptr, *bdw = nullptr, *bng = nullptr,
           *bnb = nullptr;
 };
@@ -373,6 +375,11 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
                 if (cudaMemcpy(pp, hb.data(), hb.size() * 2, cudaMemcpyHostToDevice) != cudaSuccess)
                     return fail(CAC_E_CUDA);
                 Lw.Ppad = pp;
+                if (HD == 64 && m->NR <= 256) {
+                    if (!make_tmap_bf16_blocks(&Lw.Pmap, pp, m->NR, H, (uint64_t)m->NR * HD * 2, m->NR))
+                        return fail(CAC_E_CUDA);
+                    Lw.has_pmap = true;
+                }
             } else {
                 float* pf;
                 if ((r = upload_f32(m, pad.data(), pad.size(), &pf)) != CAC_OK) return fail(r);
@@ -976,10 +983,10 @@ extern "C" int cac_pool_create(cac_model* m, int max_streams, int max_frames_per
         for (int l = 0; l < L; ++l) {
             AttnMaps& am = p->amaps[l];
             const uint64_t blocks = (uint64_t)S * L * H, bstride = (uint64_t)p->R * HD * 2;
-            if (!make_tmap_bf16_blocks(&am.k, p->kring, p->R, blocks, bstride, p->R) ||
-                !make_tmap_bf16_blocks(&am.v, p->vring, p->R, blocks, bstride, p->R) ||
-                !make_tmap_bf16_blocks(&am.p, m->layers[l].Ppad, m->NR, H, (uint64_t)m->NR * HD * 2, m->NR))
+            if (!m->layers[l].has_pmap || !make_tmap_bf16_blocks(&am.k, p->kring, p->R, blocks, bstride, p->R) ||
+                !make_tmap_bf16_blocks(&am.v, p->vring, p->R, blocks, bstride, p->R))
                 return fail(CAC_E_CUDA);
+            am.p = m->layers[l].Pmap;
         }
     }
     if ((r = palloc(p, ab * S * p->conv_sstride, &p->conv)) != CAC_OK) return fail(r);
@@ -1503,6 +1510,14 @@ int offline_run(cac_model* m, char* w, const OfflineLayout& lay, int B, const fl
     const long long ldl = sp ? 2LL * D : D;  // row stride of the split LayerNorm outputs in xln
     const int shf = m->split_ffh;
     const long long ldh = shf ? 2LL * F : F;  // row stride of the FF hidden activations (split: hi | lo)
+    // tensor-core attention: one copy = one head's K (or V) rows of one sequence
+    AttnMaps om;
+    bool omaps = bf && m->HD == 64 && m->layers[0].has_pmap && m->cfg.right_context == 0;
+    if (omaps) {
+        const uint32_t box = (uint32_t)attention_offline_box_rows(T3, m->cfg.att_left);
+        omaps = box <= 256 && box <= (uint32_t)M && make_tmap_bf16(&om.k, kd, D, M, (uint64_t)D * 2, box) &&
+                make_tmap_bf16(&om.v, vd, D, M, (uint64_t)D * 2, box);
+    }
     CK(launch_layernorm(x, (int)M, D, m->layers[0].ff1_g, m->layers[0].ff1_b, nullptr, xln, nullptr, nullptr, nullptr,
                         bf, 1 << 30, 0, 0, sp, s));
     ++lc;
@@ -1526,6 +1541,12 @@ int offline_run(cac_model* m, char* w, const OfflineLayout& lay, int B, const fl
             a.left = m->cfg.att_left; a.chunk = m->cfg.att_chunk; a.rc = m->cfg.right_context;
             a.nb = B; a.T = T3; a.seq_len = flen_d;
             a.scale = 1.f / std::sqrt((float)m->HD);
+            AttnMaps lm;
+            if (omaps) {
+                lm = om;
+                lm.p = Lw.Pmap;
+                a.maps = &lm;
+            }
             CK(launch_attention_offline(a, bf, m->status, s));
         }
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.wo.b; ep.x = x; ep.ldx = D; ep.scale = 1.f;

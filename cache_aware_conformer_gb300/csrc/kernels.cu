@@ -710,6 +710,7 @@ cudaError_t launch_attention_stream(const AttnParams& a, int act_bf16, int* stat
 
 cudaError_t launch_attention_offline(const AttnParams& a, int act_bf16, int* status, cudaStream_t s) {
     if (a.nb <= 0) return cudaSuccess;
+    if (attention_offline_mma_ok(a, act_bf16)) return launch_attention_offline_mma(a, status, s);
     // queries per unit: one chunk of the chunked mask, or 8 consecutive frames of a window mask
     const int qgroup = a.rc > 0 ? 8 : a.chunk;
     const int nk_need = a.rc > 0 ? a.left + qgroup + a.rc : a.left + a.chunk;
@@ -771,10 +772,46 @@ __global__ void __launch_bounds__(256) dwconv_kernel(const T* glu, T* cache, lon
     }
 }
 
+// Offline (no cache, zero left padding): one thread per (sequence, frame,
+// channel pair); the 9 taps are read straight from the GLU rows (L1/L2 hits).
+template <class T>
+__global__ void __launch_bounds__(256) dwconv_offline_kernel(const T* glu, int T_len, const float* wT,
+                                                             const float* bdw, const float* bng, const float* bnb,
+                                                             T* out, int D, long long pairs) {
+    pdl_wait();
+    const long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (e >= pairs) return;
+    const int D2 = D / 2;
+    const int c = (int)(e % D2) * 2;
+    const long long r = e / D2;  // row = sequence * T_len + t
+    const int t = (int)(r % T_len);
+    float a0 = __ldg(bdw + c), a1 = __ldg(bdw + c + 1);
+#pragma unroll
+    for (int k = 0; k < 9; ++k) {
+        const int tt = t - 8 + k;
+        if (tt < 0) continue;
+        const T* g = glu + (r - 8 + k) * D + c;
+        a0 = fmaf(__ldg(wT + k * D + c), to_f(g[0]), a0);
+        a1 = fmaf(__ldg(wT + k * D + c + 1), to_f(g[1]), a1);
+    }
+    out[r * D + c] = from_f<T>(siluf_(__ldg(bng + c) * a0 + __ldg(bnb + c)));
+    out[r * D + c + 1] = from_f<T>(siluf_(__ldg(bng + c + 1) * a1 + __ldg(bnb + c + 1)));
+    pdl_trigger();
+}
+
 cudaError_t launch_dwconv(const void* glu, void* cache, long long cs_stride, const int* ids, const int* pos, int nq,
                           int n_commit, const float* wT, const float* bdw, const float* bng, const float* bnb,
                           void* out, int D, int nb, int act_bf16, cudaStream_t s) {
     if (nb <= 0) return cudaSuccess;
+    if (!cache && D % 2 == 0) {
+        const long long pairs = (long long)nb * nq * (D / 2);
+        const int blocks = (int)((pairs + 255) / 256);
+        if (act_bf16)
+            return launch_k(dwconv_offline_kernel<bf16>, dim3(blocks), dim3(256), 0, s, 1, static_cast<const bf16*>(glu),
+                            nq, wT, bdw, bng, bnb, static_cast<bf16*>(out), D, pairs);
+        return launch_k(dwconv_offline_kernel<float>, dim3(blocks), dim3(256), 0, s, 1, static_cast<const float*>(glu),
+                        nq, wT, bdw, bng, bnb, static_cast<float*>(out), D, pairs);
+    }
     const long long threads = (long long)nb * D;
     const int blocks = (int)((threads + 255) / 256);
     if (act_bf16)

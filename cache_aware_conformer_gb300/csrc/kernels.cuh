@@ -73,6 +73,14 @@ cudaError_t launch_attention_stream(const AttnParams& a, int act_bf16, int* stat
 // takes it whenever attention_stream_mma_ok holds.
 bool attention_stream_mma_ok(const AttnParams& a, int act_bf16);
 cudaError_t launch_attention_stream_mma(const AttnParams& a, int* status, cudaStream_t s);
+// Tensor-core variant of the offline chunked-causal attention (bf16, head_dim
+// 64, chunk <= 4, one block per (head, sequence) with the sequence's K/V
+// staged once); maps->k / maps->v: 2-D maps over the dense K / V rows [rows][D]
+// with boxes of {64, attention_offline_box_rows(T, left)} rows, maps->p the
+// layer's table (as for the streaming path).
+bool attention_offline_mma_ok(const AttnParams& a, int act_bf16);
+int attention_offline_box_rows(int T, int left);
+cudaError_t launch_attention_offline_mma(const AttnParams& a, int* status, cudaStream_t s);
 cudaError_t launch_attention_offline(const AttnParams& a, int act_bf16, int* status, cudaStream_t s);
 
 // Causal depthwise conv (k = 9) + affine + SiLU over [conv cache | glu_new].

@@ -21,7 +21,10 @@ DEV = "cuda"
     (TINY, [320, 203, 57]),
     (replace(EOU_120M, n_layers=2), [1501, 800, 9]),
     (replace(C600M, n_layers=2), [1501, 1337]),
-], ids=["fp32-tiny", "bf16-eou", "bf16-600m"])
+    (replace(EOU_120M, n_layers=2, att_chunk=4, att_left=20), [1501, 1100, 37]),
+    (replace(EOU_120M, n_layers=2, att_chunk=1, att_left=33), [1400, 1501]),
+    (replace(EOU_120M, n_layers=1), [1203]),
+], ids=["fp32-tiny", "bf16-eou", "bf16-600m", "bf16-chunk4-left20", "bf16-chunk1-left33", "bf16-one-short"])
 def test_offline_encode_matches_oracle(cfg, lens):
     W, model = make_model(cfg)
     t = max(lens)
