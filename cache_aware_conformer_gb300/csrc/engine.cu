@@ -73,6 +73,10 @@ struct LayerW {
     void* Ppad = nullptr;  // attention position table [H][NR][HD], activation dtype
     CUtensorMap Pmap;      // bf16, HD 64: one copy = one head's table (NR rows)
     bool has_pmap = false;
+    // LayerNorm folded into the projection after it (fold_ln): bias b + W beta and
+    // column sums sum_k gamma_k W[n][k] of the attention, conv and FF2 LayerNorms
+    float *qkv_fb = nullptr, *pw1_fb = nullptr, *ff2_fb = nullptr;
+    float *qkv_cs = nullptr, *pw1_cs = nullptr, *ff2_cs = nullptr;
     float *pbu = nullptr, *pbv = nullptr, *P = nullptr, *dwT = nullptr, *bdw = nullptr, *bng = nullptr,
           *bnb = nullptr;
 };
@@ -89,6 +93,7 @@ struct cac_model {
     int bf16 = 1, tc = 1;
     int split = 1;  // bf16: LayerNorm outputs enter their GEMMs as split (hi, lo) operands
     int split_ffh = 0;  // bf16, d_model >= 1024: the FF hidden activations enter the down-projection split too
+    int fold_ln = 0;    // streaming steps: the attention, conv and FF2 LayerNorms run inside the GEMMs
     int sms = 152;      // streaming multiprocessors of the device
     int D = 0, H = 0, HD = 0, F = 0, L = 0, J = 0;
     int rmin = 0, NR = 0;
@@ -155,6 +160,31 @@ int upload_lin(cac_model* m, const float* w, const float* b, int N, int K, Lin* 
         if (lin->has128 && !make_tmap_bf16(&lin->tm128, p, K, N, (uint64_t)K * 2, 128)) return CAC_E_CUDA;
     }
     return CAC_OK;
+}
+
+// Constants of a projection W (stored [N][K], bias b) that consumes LN(x) =
+// gamma * z + beta with the LayerNorm folded into its GEMM: the GEMM's A operand
+// is gamma * x (written by the producer of x), and
+//   LN(x) W^T + b = rstd (sum_k gamma_k x_k W_k - mean colsum) + bias_f,
+// colsum[n] = sum_k gamma_k W[n][k] over the stored (rounded) weights, bias_f[n]
+// = b[n] + sum_k W[n][k] beta_k (fp64 on the host).  perm reorders the outputs
+// as in upload_lin.
+int upload_ln_fold(cac_model* m, const float* w, const float* b, const float* gamma, const float* beta, int N, int K,
+                   const std::vector<int>* perm, float** bias_f, float** colsum) {
+    std::vector<float> bf(N), cs(N);
+    for (int r = 0; r < N; ++r) {
+        const int src = perm ? (*perm)[r] : r;
+        double acc_b = b[src], acc_c = 0.0;
+        for (int k = 0; k < K; ++k) {
+            const float wv = w[(size_t)src * K + k];
+            acc_b += (double)wv * beta[k];
+            acc_c += (double)gamma[k] * (m->bf16 ? (double)bf2f(f2bf(wv)) : (double)wv);
+        }
+        bf[r] = (float)acc_b;
+        cs[r] = (float)acc_c;
+    }
+    RET(upload_f32(m, bf.data(), N, bias_f));
+    return upload_f32(m, cs.data(), N, colsum);
 }
 
 struct Cursor {
@@ -261,6 +291,7 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
     m->tc = m->bf16 && !cfg->gemm_simt;
     m->split = m->bf16;
     m->split_ffh = m->bf16 && cfg->d_model >= 1024;
+    m->fold_ln = m->bf16 && m->tc && cfg->d_model % 32 == 0;
     {
         int dev = 0;
         if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&m->sms, cudaDevAttrMultiProcessorCount, dev);
@@ -321,15 +352,31 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
             const float* s = c.take(n);
             return s ? upload_f32(m, s, n, dst) : CAC_E_INVAL;
         };
-        auto lin = [&](Lin* dst, int N, int K, const std::vector<int>* perm) {
+        // the host copy of the last vec() upload (a LayerNorm's gamma / beta)
+        const float* host_g = nullptr;
+        const float* host_b = nullptr;
+        auto vec_ln = [&](float** g, float** be) {
+            host_g = c.take(D);
+            host_b = c.take(D);
+            if (!host_g || !host_b) return CAC_E_INVAL;
+            int e = upload_f32(m, host_g, D, g);
+            return e ? e : upload_f32(m, host_b, D, be);
+        };
+        // a projection that consumes the last vec_ln() LayerNorm; also stored folded (fold_ln)
+        auto lin = [&](Lin* dst, int N, int K, const std::vector<int>* perm, float** fold_b = nullptr,
+                       float** colsum = nullptr) {
             const float* ww = c.take((size_t)N * K);
             const float* bb = c.take(N);
-            return (ww && bb) ? upload_lin(m, ww, bb, N, K, dst, perm) : CAC_E_INVAL;
+            if (!ww || !bb) return CAC_E_INVAL;
+            int e = upload_lin(m, ww, bb, N, K, dst, perm);
+            if (e == CAC_OK && fold_b && m->fold_ln)
+                e = upload_ln_fold(m, ww, bb, host_g, host_b, N, K, perm, fold_b, colsum);
+            return e;
         };
         if ((r = vec(&Lw.ff1_g, D)) || (r = vec(&Lw.ff1_b, D)) || (r = lin(&Lw.ff1_w1, F, D, nullptr)) ||
             (r = lin(&Lw.ff1_w2, D, F, nullptr)))
             return fail(r);
-        if ((r = vec(&Lw.att_g, D)) || (r = vec(&Lw.att_b, D))) return fail(r);
+        if ((r = vec_ln(&Lw.att_g, &Lw.att_b))) return fail(r);
         {   // q, k, v concatenated into one [3D][D] projection
             const float *wq = c.take((size_t)D * D), *bq = c.take(D), *wk = c.take((size_t)D * D), *bk = c.take(D),
                         *wv = c.take((size_t)D * D), *bv = c.take(D);
@@ -342,6 +389,9 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
             std::memcpy(&bqkv[D], bk, sizeof(float) * D);
             std::memcpy(&bqkv[2 * D], bv, sizeof(float) * D);
             if ((r = upload_lin(m, wqkv.data(), bqkv.data(), 3 * D, D, &Lw.qkv, nullptr)) != CAC_OK) return fail(r);
+            if (m->fold_ln && (r = upload_ln_fold(m, wqkv.data(), bqkv.data(), host_g, host_b, 3 * D, D, nullptr,
+                                                  &Lw.qkv_fb, &Lw.qkv_cs)) != CAC_OK)
+                return fail(r);
         }
         if ((r = lin(&Lw.wo, D, D, nullptr))) return fail(r);
         {   // P = pe @ wpos^T, computed once per layer in fp32
@@ -387,7 +437,7 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
             }
         }
         if ((r = vec(&Lw.pbu, (size_t)H * HD)) || (r = vec(&Lw.pbv, (size_t)H * HD))) return fail(r);
-        if ((r = vec(&Lw.conv_g, D)) || (r = vec(&Lw.conv_b, D)) || (r = lin(&Lw.pw1, 2 * D, D, &glu_perm)))
+        if ((r = vec_ln(&Lw.conv_g, &Lw.conv_b)) || (r = lin(&Lw.pw1, 2 * D, D, &glu_perm, &Lw.pw1_fb, &Lw.pw1_cs)))
             return fail(r);
         {   // depthwise [D][9] -> [9][D]
             const float* wdw = c.take((size_t)D * 9);
@@ -400,7 +450,7 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
         if ((r = vec(&Lw.bdw, D)) || (r = vec(&Lw.bng, D)) || (r = vec(&Lw.bnb, D)) ||
             (r = lin(&Lw.pw2, D, D, nullptr)))
             return fail(r);
-        if ((r = vec(&Lw.ff2_g, D)) || (r = vec(&Lw.ff2_b, D)) || (r = lin(&Lw.ff2_w1, F, D, nullptr)) ||
+        if ((r = vec_ln(&Lw.ff2_g, &Lw.ff2_b)) || (r = lin(&Lw.ff2_w1, F, D, nullptr, &Lw.ff2_fb, &Lw.ff2_cs)) ||
             (r = lin(&Lw.ff2_w2, D, F, nullptr)))
             return fail(r);
         if ((r = vec(&Lw.out_g, D)) || (r = vec(&Lw.out_b, D))) return fail(r);
@@ -466,6 +516,7 @@ struct Scratch {
     float* x = nullptr;
     void *xln = nullptr, *h = nullptr, *o = nullptr, *glu = nullptr, *yc = nullptr;
     float* q = nullptr;
+    float2* stats = nullptr;  // fold_ln: per-row partials (sum, centred sum of squares) of 32 columns of x
 };
 constexpr int MAX_GROUPS = 4;
 
@@ -485,6 +536,7 @@ struct cac_pool {
     float* x = nullptr;
     void *xln = nullptr, *h = nullptr, *o = nullptr, *glu = nullptr, *yc = nullptr;
     float* q = nullptr;
+    float2* stats = nullptr;
     // A chunked step over many streams runs as up to `groups` concurrent
     // sub-batches of at most group_streams streams each, forked onto the pool's
     // own CUDA streams: independent kernel chains overlap one another's
@@ -549,6 +601,7 @@ void use_scratch(cac_pool* p, int g) {
     const Scratch& sc = p->sc[g];
     p->win1 = sc.win1; p->win2 = sc.win2; p->win3 = sc.win3; p->y3 = sc.y3;
     p->x = sc.x; p->xln = sc.xln; p->h = sc.h; p->o = sc.o; p->glu = sc.glu; p->yc = sc.yc; p->q = sc.q;
+    p->stats = sc.stats;
 }
 
 // Copy `n` ids into the next pinned slot and queue their upload to `dst`.
@@ -697,6 +750,18 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
     const long long ldl = sp ? 2LL * D : D;  // row stride of the split LayerNorm outputs in xln
     const int shf = m->split_ffh;
     const long long ldh = shf ? 2LL * F : F;  // row stride of the FF hidden activations (split: hi | lo)
+    // fold_ln: the residual GEMM before the attention, conv and FF2 LayerNorms
+    // writes the split operand of x into xln and its row partials into stats;
+    // the GEMM after it applies the LayerNorm in its epilogue
+    const bool fold = m->fold_ln && sp && p->stats;
+    auto emit_split = [&](EpiParams& e, const float* gamma) {
+        if (!fold) return;
+        e.xs = static_cast<bf16*>(p->xln); e.ldxs = ldl; e.xs_lo = D; e.xs_gamma = gamma;
+        e.stats_out = p->stats; e.stats_parts = D / 32;
+    };
+    auto use_fold = [&](EpiParams& e, const float* colsum) {
+        e.ln_stats = p->stats; e.ln_colsum = colsum; e.ln_parts = D / 32; e.ln_rows = M;
+    };
     PB(P_LN);
     CK(launch_layernorm(p->x, M, D, m->layers[0].ff1_g, m->layers[0].ff1_b, nullptr, p->xln, nullptr, nullptr,
                         nullptr, bf, 1 << 30, 0, 0, sp, s));
@@ -712,17 +777,21 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
         RET(gemm(m, p->xln, ldl, M, D, Lw.ff1_w1, 0, ep, s, lc, sp));
         PE();
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.ff1_w2.b; ep.x = p->x; ep.ldx = D; ep.scale = 0.5f;
+        emit_split(ep, Lw.att_g);
         PB(P_FFDOWN);
         RET(gemm(m, p->h, ldh, M, F, Lw.ff1_w2, 0, ep, s, lc, shf));
         PE();
         RET(trace_tap(p, l, 0, p->x, false, M, s));
         // attention: xln = LN(x); Q and K/V into the rings
-        PB(P_LN);
-        CK(launch_layernorm(p->x, M, D, Lw.att_g, Lw.att_b, nullptr, p->xln, nullptr, nullptr, nullptr, bf,
-                            1 << 30, 0, 0, sp, s));
-        PE();
-        ++*lc;
-        ep = EpiParams(); ep.kind = EPI_QKV; ep.bias = Lw.qkv.b; ep.D = D; ep.HD = m->HD; ep.R = p->R;
+        if (!fold) {
+            PB(P_LN);
+            CK(launch_layernorm(p->x, M, D, Lw.att_g, Lw.att_b, nullptr, p->xln, nullptr, nullptr, nullptr, bf,
+                                1 << 30, 0, 0, sp, s));
+            PE();
+            ++*lc;
+        }
+        ep = EpiParams(); ep.kind = EPI_QKV; ep.bias = fold ? Lw.qkv_fb : Lw.qkv.b; ep.D = D; ep.HD = m->HD; ep.R = p->R;
+        if (fold) use_fold(ep, Lw.qkv_cs);
         ep.ring_sstride = p->ring_sstride;
         ep.kring = static_cast<char*>(p->kring) + (long long)l * m->H * p->R * m->HD * ab;
         ep.vring = static_cast<char*>(p->vring) + (long long)l * m->H * p->R * m->HD * ab;
@@ -749,21 +818,26 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
         }
         RET(trace_tap(p, l, 1, p->o, true, M, s, sp));
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.wo.b; ep.x = p->x; ep.ldx = D; ep.scale = 1.f;
+        emit_split(ep, Lw.conv_g);
         PB(P_OUT);
         RET(gemm(m, p->o, ldl, M, D, Lw.wo, 0, ep, s, lc, sp));
         PE();
         RET(trace_tap(p, l, 2, p->x, false, M, s));
         // conv module
-        PB(P_LN);
-        CK(launch_layernorm(p->x, M, D, Lw.conv_g, Lw.conv_b, nullptr, p->xln, nullptr, nullptr, nullptr, bf,
-                            1 << 30, 0, 0, sp, s));
-        PE();
-        ++*lc;
+        if (!fold) {
+            PB(P_LN);
+            CK(launch_layernorm(p->x, M, D, Lw.conv_g, Lw.conv_b, nullptr, p->xln, nullptr, nullptr, nullptr, bf,
+                                1 << 30, 0, 0, sp, s));
+            PE();
+            ++*lc;
+        }
         void* conv_l = static_cast<char*>(p->conv) + (long long)l * CONV_CACHE * D * ab;
         // tcgen05 path, chunked steps whose frames per stream divide a warp: the
         // depthwise conv runs in the pw1 + GLU epilogue (a stream's rows share a warp)
         const bool fuse_dw = m->tc && sp && 32 % n == 0 && n_commit == n;
-        ep = EpiParams(); ep.kind = fuse_dw ? EPI_GLUDW : EPI_GLU; ep.bias = Lw.pw1.b; ep.out_act = p->glu; ep.ldo = D;
+        ep = EpiParams(); ep.kind = fuse_dw ? EPI_GLUDW : EPI_GLU; ep.bias = fold ? Lw.pw1_fb : Lw.pw1.b;
+        ep.out_act = p->glu; ep.ldo = D;
+        if (fold) use_fold(ep, Lw.pw1_cs);
         if (fuse_dw) {
             ep.D = D; ep.nq = n; ep.ids = ids; ep.pos = p->pos;
             ep.dw_ring = conv_l; ep.dw_sstride = p->conv_sstride;
@@ -782,17 +856,22 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
         }
         RET(trace_tap(p, l, 4, p->yc, true, M, s));
         ep = EpiParams(); ep.kind = EPI_RESID; ep.bias = Lw.pw2.b; ep.x = p->x; ep.ldx = D; ep.scale = 1.f;
+        emit_split(ep, Lw.ff2_g);
         PB(P_PW2);
         RET(gemm(m, p->yc, D, M, D, Lw.pw2, 0, ep, s, lc));
         PE();
         RET(trace_tap(p, l, 5, p->x, false, M, s));
         // FF2
-        PB(P_LN);
-        CK(launch_layernorm(p->x, M, D, Lw.ff2_g, Lw.ff2_b, nullptr, p->xln, nullptr, nullptr, nullptr, bf,
-                            1 << 30, 0, 0, sp, s));
-        PE();
-        ++*lc;
-        ep = EpiParams(); ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = Lw.ff2_w1.b; ep.out_act = p->h; ep.ldo = ldh; ep.split_out = shf ? F : 0;
+        if (!fold) {
+            PB(P_LN);
+            CK(launch_layernorm(p->x, M, D, Lw.ff2_g, Lw.ff2_b, nullptr, p->xln, nullptr, nullptr, nullptr, bf,
+                                1 << 30, 0, 0, sp, s));
+            PE();
+            ++*lc;
+        }
+        ep = EpiParams(); ep.kind = EPI_STORE; ep.act = ACT_SILU; ep.bias = fold ? Lw.ff2_fb : Lw.ff2_w1.b;
+        ep.out_act = p->h; ep.ldo = ldh; ep.split_out = shf ? F : 0;
+        if (fold) use_fold(ep, Lw.ff2_cs);
         PB(P_FFUP);
         RET(gemm(m, p->xln, ldl, M, D, Lw.ff2_w1, 0, ep, s, lc, sp));
         PE();
@@ -1009,6 +1088,10 @@ extern "C" int cac_pool_create(cac_model* m, int max_streams, int max_frames_per
         if ((e = palloc(p, ab * rows * D * wsp, &sc.o)) != CAC_OK) return e;
         if ((e = palloc(p, ab * rows * D, &sc.glu)) != CAC_OK) return e;
         if ((e = palloc(p, ab * rows * D, &sc.yc)) != CAC_OK) return e;
+        if (m->fold_ln) {
+            if ((e = palloc(p, sizeof(float2) * rows * (D / 32), &w)) != CAC_OK) return e;
+            sc.stats = static_cast<float2*>(w);
+        }
         return CAC_OK;
     };
     // concurrent sub-batches of 64 streams for chunked steps (2 .. 4 of them)

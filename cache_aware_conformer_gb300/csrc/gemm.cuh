@@ -72,6 +72,26 @@ struct EpiParams {
     const float* dw_gamma = nullptr;
     const float* dw_beta = nullptr;
     void* dw_out = nullptr;
+    // LayerNorm folded into this GEMM (EPI_STORE / EPI_GLU / EPI_QKV / EPI_GLUDW):
+    // A is the split operand of gamma * x (x the residual rows), bias = b + W beta
+    // and ln_colsum[n] = sum_k gamma_k W[n][k], so that LN(x) W^T + b =
+    // rstd_r (acc - mean_r ln_colsum) + bias.  Before the bias: v = rstd_r * (acc -
+    // mean_r * ln_colsum[c]), with mean_r and rstd_r of x from the row's ln_parts
+    // partials (sum, centred sum of squares of 32 columns each) at ln_stats + r *
+    // ln_parts; rows >= ln_rows are not read.
+    const float2* ln_stats = nullptr;
+    const float* ln_colsum = nullptr;
+    int ln_parts = 0, ln_rows = 0;
+    // EPI_RESID (bf16): also emit the split operand of xs_gamma * (updated x) (hi
+    // at xs + r * ldxs + c, lo xs_lo columns further) and the per-32-column
+    // partials of x at stats_out + r * stats_parts + c / 32, for a GEMM that
+    // folds the next LayerNorm (xs_gamma: that LayerNorm's gain)
+    bf16* xs = nullptr;
+    const float* xs_gamma = nullptr;
+    long long ldxs = 0;
+    int xs_lo = 0;
+    float2* stats_out = nullptr;
+    int stats_parts = 0;
 };
 
 // host helpers ---------------------------------------------------------------
@@ -148,12 +168,116 @@ __device__ __forceinline__ void store32<bf16>(bf16* dst, const float (&v)[32]) {
     }
 }
 
+// Warp-cooperative row stores: lane l holds 32 consecutive elements of its
+// own row, to be written at dst (lane's row pointer).  The rows go through the
+// warp's shared-memory slice `stage` (EPI_STAGE_FLOATS floats) so that every
+// global store instruction writes whole lines: 4 rows x 128 B (fp32) or 8 rows x
+// 64 B (bf16) per instruction instead of 32 scattered 16-byte pieces.  Rows
+// whose lane has live == false are not written.  Every lane of the warp calls.
+constexpr int EPI_STAGE_FLOATS = 32 * 36;
+
+__device__ __forceinline__ void rows_store(float* stage, float* dst, const float (&v)[32], bool live) {
+    const int lane = threadIdx.x & 31;
+    float4* s = reinterpret_cast<float4*>(stage + lane * 36);  // 144-byte rows: conflict-free v4 writes
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    __syncwarp();
+    const unsigned live_mask = __ballot_sync(0xffffffffu, live);
+    const unsigned long long p = reinterpret_cast<unsigned long long>(dst);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 4 * i + (lane >> 3), c = lane & 7;
+        const unsigned long long pr = __shfl_sync(0xffffffffu, p, r);
+        const float4 q = reinterpret_cast<const float4*>(stage + r * 36)[c];
+        if ((live_mask >> r) & 1u) reinterpret_cast<float4*>(pr)[c] = q;
+    }
+    __syncwarp();  // the slice is free for the next call
+}
+
+__device__ __forceinline__ void rows_store(float* stage, bf16* dst, const float (&v)[32], bool live) {
+    const int lane = threadIdx.x & 31;
+    uint32_t* su = reinterpret_cast<uint32_t*>(stage);
+    uint4* s = reinterpret_cast<uint4*>(su + lane * 20);  // 80-byte rows
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint4 u;
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(v[8 * j + 0], v[8 * j + 1]);
+        __nv_bfloat162 p1 = __floats2bfloat162_rn(v[8 * j + 2], v[8 * j + 3]);
+        __nv_bfloat162 p2 = __floats2bfloat162_rn(v[8 * j + 4], v[8 * j + 5]);
+        __nv_bfloat162 p3 = __floats2bfloat162_rn(v[8 * j + 6], v[8 * j + 7]);
+        u.x = *reinterpret_cast<uint32_t*>(&p0);
+        u.y = *reinterpret_cast<uint32_t*>(&p1);
+        u.z = *reinterpret_cast<uint32_t*>(&p2);
+        u.w = *reinterpret_cast<uint32_t*>(&p3);
+        s[j] = u;
+    }
+    __syncwarp();
+    const unsigned live_mask = __ballot_sync(0xffffffffu, live);
+    const unsigned long long p = reinterpret_cast<unsigned long long>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = 8 * i + (lane >> 2), c = lane & 3;
+        const unsigned long long pr = __shfl_sync(0xffffffffu, p, r);
+        const uint4 q = reinterpret_cast<const uint4*>(su + r * 20)[c];
+        if ((live_mask >> r) & 1u) reinterpret_cast<uint4*>(pr)[c] = q;
+    }
+    __syncwarp();
+}
+
+// store32 through the warp's staging slice when there is one (every lane
+// calls), else directly (live lanes only)
+template <class T>
+__device__ __forceinline__ void put32(float* stage, T* dst, const float (&v)[32], bool live) {
+    if (stage)
+        rows_store(stage, dst, v, live);
+    else if (live)
+        store32<T>(dst, v);
+}
+
 // Operands of the epilogue that do not depend on the accumulators (bias, and
 // the residual rows for EPI_RESID): loaded ahead, while the main loop runs.
 struct EpiPre {
     float4 b[8];
     float4 x[8];
+    float4 g[8];  // EPI_RESID with xs: the next LayerNorm's gain
+    float ln_mean, ln_rstd;
 };
+
+// mean and 1/sqrt(var + 1e-5) of a row from its partials (sum_j, M2_j) over 32
+// columns each (parts even, <= 32): var = (sum_j M2_j + 32 sum_j (mean_j -
+// mean)^2) / (32 parts).  The loads are issued together (one float4 = two parts).
+__device__ __forceinline__ void ln_row_stats(const float2* st, int parts, float& mean, float& rstd) {
+    const float4* s4 = reinterpret_cast<const float4*>(st);
+    float4 q[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) q[j] = 2 * j < parts ? s4[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) s += q[j].x + q[j].z;
+    const float n = 32.f * (float)parts;
+    mean = s / n;
+    float m2 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        if (2 * j < parts) {
+            const float d0 = q[j].x * (1.f / 32.f) - mean, d1 = q[j].z * (1.f / 32.f) - mean;
+            m2 += q[j].y + q[j].w + 32.f * (d0 * d0 + d1 * d1);
+        }
+    }
+    rstd = rsqrtf(m2 / n + 1e-5f);
+}
+
+__device__ __forceinline__ void ln_fold32(const EpiParams& e, int col0, const EpiPre& pre, float (&v)[32]) {
+    const float4* c4 = reinterpret_cast<const float4*>(e.ln_colsum + col0);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 c = __ldg(c4 + i);
+        v[4 * i] = pre.ln_rstd * fmaf(-pre.ln_mean, c.x, v[4 * i]);
+        v[4 * i + 1] = pre.ln_rstd * fmaf(-pre.ln_mean, c.y, v[4 * i + 1]);
+        v[4 * i + 2] = pre.ln_rstd * fmaf(-pre.ln_mean, c.z, v[4 * i + 2]);
+        v[4 * i + 3] = pre.ln_rstd * fmaf(-pre.ln_mean, c.w, v[4 * i + 3]);
+    }
+}
 
 template <int KIND>
 __device__ __forceinline__ void epi_prefetch(const EpiParams& e, int row, int col0, EpiPre& pre) {
@@ -169,11 +293,28 @@ __device__ __forceinline__ void epi_prefetch(const EpiParams& e, int row, int co
         const float4* x4 = reinterpret_cast<const float4*>(e.x + (long long)row * e.ldx + col0);
 #pragma unroll
         for (int i = 0; i < 8; ++i) pre.x[i] = x4[i];
+        if (e.xs) {
+            const float4* g4 = reinterpret_cast<const float4*>(e.xs_gamma + col0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) pre.g[i] = __ldg(g4 + i);
+        }
+    } else {
+        pre.ln_mean = 0.f;
+        pre.ln_rstd = 1.f;
+        if (e.ln_stats && row < e.ln_rows)
+            ln_row_stats(e.ln_stats + (long long)row * e.ln_parts, e.ln_parts, pre.ln_mean, pre.ln_rstd);
     }
 }
 
+// stage == nullptr: called by live lanes only, per-thread stores.  stage !=
+// nullptr: called by every lane of the warp (live marks rows < M), row stores
+// through the warp's staging slice.
 template <int KIND, class TAct>
-__device__ __forceinline__ void epilogue32(const EpiParams& e, int row, int col0, float (&v)[32], const EpiPre& pre) {
+__device__ __forceinline__ void epilogue32(const EpiParams& e, int row, int col0, float (&v)[32], const EpiPre& pre,
+                                           float* stage = nullptr, bool live = true) {
+    if constexpr (KIND != EPI_RESID) {
+        if (e.ln_stats) ln_fold32(e, col0, pre, v);
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const float4 b = pre.b[i];
@@ -187,52 +328,80 @@ __device__ __forceinline__ void epilogue32(const EpiParams& e, int row, int col0
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.f);
         }
-        const int g = row / e.grp;
-        const long long orow = (long long)(e.grp_map ? e.grp_map[g] : g) * e.grp_stride + (row % e.grp) + e.row_off;
-        if (e.out_f32) store32<float>(e.out_f32 + orow * e.ldo + col0, v);
+        long long orow = 0;
+        if (live) {
+            const int g = row / e.grp;
+            orow = (long long)(e.grp_map ? e.grp_map[g] : g) * e.grp_stride + (row % e.grp) + e.row_off;
+        }
+        if (e.out_f32) put32<float>(stage, e.out_f32 + orow * e.ldo + col0, v, live);
         if (e.out_act) {
             TAct* dst = reinterpret_cast<TAct*>(e.out_act) + orow * e.ldo + col0;
-            store32<TAct>(dst, v);
+            put32<TAct>(stage, dst, v, live);
             if (e.split_out > 0) {  // split operand for the next GEMM: lo = bf16(v - hi)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] -= to_f(from_f<TAct>(v[i]));
-                store32<TAct>(dst + e.split_out, v);
+                put32<TAct>(stage, dst + e.split_out, v, live);
             }
         }
     } else if constexpr (KIND == EPI_RESID) {
-        float4* x4 = reinterpret_cast<float4*>(e.x + (long long)row * e.ldx + col0);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float4 a = pre.x[i];
-            a.x += e.scale * v[4 * i]; a.y += e.scale * v[4 * i + 1];
-            a.z += e.scale * v[4 * i + 2]; a.w += e.scale * v[4 * i + 3];
-            x4[i] = a;
+            const float4 a = pre.x[i];
+            v[4 * i] = fmaf(e.scale, v[4 * i], a.x);
+            v[4 * i + 1] = fmaf(e.scale, v[4 * i + 1], a.y);
+            v[4 * i + 2] = fmaf(e.scale, v[4 * i + 2], a.z);
+            v[4 * i + 3] = fmaf(e.scale, v[4 * i + 3], a.w);
+        }
+        put32<float>(stage, e.x + (long long)row * e.ldx + col0, v, live);
+        if (e.xs) {
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sum += v[i];
+            const float mu = sum * (1.f / 32.f);
+            float m2 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) m2 = fmaf(v[i] - mu, v[i] - mu, m2);
+            if (live) e.stats_out[(long long)row * e.stats_parts + (col0 >> 5)] = make_float2(sum, m2);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 g = pre.g[i];
+                v[4 * i] *= g.x; v[4 * i + 1] *= g.y; v[4 * i + 2] *= g.z; v[4 * i + 3] *= g.w;
+            }
+            bf16* dst = e.xs + (long long)row * e.ldxs + col0;
+            put32<bf16>(stage, dst, v, live);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] -= __bfloat162float(__float2bfloat16_rn(v[i]));
+            put32<bf16>(stage, dst + e.xs_lo, v, live);
         }
     } else if constexpr (KIND == EPI_GLU) {
-        TAct* o = reinterpret_cast<TAct*>(e.out_act) + (long long)row * e.ldo + (col0 >> 1);
+        if (live) {
+            TAct* o = reinterpret_cast<TAct*>(e.out_act) + (long long)row * e.ldo + (col0 >> 1);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] = from_f<TAct>(v[i] * sigmoidf_(v[16 + i]));
+            for (int i = 0; i < 16; ++i) o[i] = from_f<TAct>(v[i] * sigmoidf_(v[16 + i]));
+        }
     } else if constexpr (KIND == EPI_QKV) {
         const int region = col0 / e.D;
         const int cc = col0 - region * e.D;
         if (region == 0) {
-            store32<float>(e.q + (long long)row * e.ldq + cc, v);
+            put32<float>(stage, e.q + (long long)row * e.ldq + cc, v, live);
             return;
         }
         TAct* base = reinterpret_cast<TAct*>(region == 1 ? e.kring : e.vring);
         if (e.dense) {
-            store32<TAct>(base + (long long)row * e.D + cc, v);
+            put32<TAct>(stage, base + (long long)row * e.D + cc, v, live);
             return;
         }
-        const int b = row / e.nq, i = row - (row / e.nq) * e.nq;
-        const int id = e.ids[b];
-        const int p = e.pos[id] + i;
-        const int slot = p % e.R;
+        int id = 0, slot = 0;
+        if (live) {
+            const int b = row / e.nq, i = row - (row / e.nq) * e.nq;
+            id = e.ids[b];
+            slot = (e.pos[id] + i) % e.R;
+        }
         TAct* sbase = base + (long long)id * e.ring_sstride;
         if (e.HD >= 32) {
             const int h = cc / e.HD, d0 = cc - h * e.HD;
-            store32<TAct>(sbase + ((long long)h * e.R + slot) * e.HD + d0, v);
-        } else {
+            put32<TAct>(stage, sbase + ((long long)h * e.R + slot) * e.HD + d0, v, live);
+        } else if (live) {
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
                 const int d = cc + k, h = d / e.HD, dd = d - h * e.HD;
@@ -241,17 +410,17 @@ __device__ __forceinline__ void epilogue32(const EpiParams& e, int row, int col0
         }
     } else if constexpr (KIND == EPI_SUB) {
         const int g = row / e.P, t = row - (row / e.P) * e.P;
-        if (t >= e.T_out) return;  // seam row spanning two groups
+        const bool on = live && t < e.T_out;  // seam rows spanning two groups are not written
         bool zero = false;
-        if (e.ids) zero = (e.tmult * e.pos[e.ids[g]] - e.toff + t) < 0;
+        if (on && e.ids) zero = (e.tmult * e.pos[e.ids[g]] - e.toff + t) < 0;
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = zero ? 0.f : fmaxf(v[i], 0.f);
         TAct* dst = reinterpret_cast<TAct*>(e.out_act) + ((long long)g * e.dst_rows + e.dst_off + t) * e.ldo + col0;
-        store32<TAct>(dst, v);
+        put32<TAct>(stage, dst, v, on);
         if (e.split_out > 0) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] -= to_f(from_f<TAct>(v[i]));
-            store32<TAct>(dst + e.split_out, v);
+            put32<TAct>(stage, dst + e.split_out, v, on);
         }
     }
 }
@@ -262,6 +431,7 @@ __device__ __forceinline__ void epilogue_gludw(const EpiParams& e, int row, bool
                                                const EpiPre& pre) {
     const int lane = threadIdx.x & 31;
     const int D = e.D, C = col0 >> 1, nq = e.nq;
+    if (e.ln_stats) ln_fold32(e, col0, pre, v);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const float4 b = pre.b[i];

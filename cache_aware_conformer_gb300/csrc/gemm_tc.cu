@@ -160,6 +160,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_fence_after();
     // partial tile [BN columns][128 rows] fp32 in the pipeline buffers (idle now)
     float* part = reinterpret_cast<float*>(sA);
+    static_assert(C::STAGES * C::B_TILE >= 8 * EPI_STAGE_FLOATS * 4, "epilogue staging");
+    float* stage = reinterpret_cast<float*>(sB) + warp * EPI_STAGE_FLOATS;
     if (splits > 1 && crank != 0) {
 #pragma unroll 1
         for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
@@ -182,9 +184,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if constexpr (KIND == EPI_GLUDW) {
                 if (c != c_first) epi_prefetch<KIND>(ep, row, n0 + c, pre);  // bias only: any row
                 epilogue_gludw(ep, row, ok && row < M, n0 + c, v, pre);
-            } else if (ok && row < M) {
-                if (c != c_first) epi_prefetch<KIND>(ep, row, n0 + c, pre);
-                epilogue32<KIND, TAct>(ep, row, n0 + c, v, pre);
+            } else {
+                // every lane: the row stores go through this warp's slice of the
+                // (idle) B ring
+                const bool live = ok && row < M;
+                if (c != c_first && live) epi_prefetch<KIND>(ep, row, n0 + c, pre);
+                epilogue32<KIND, TAct>(ep, row, n0 + c, v, pre, stage, live);
             }
         }
     }
