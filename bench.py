@@ -222,10 +222,15 @@ def algorithmic_work(cfg, S, n, mean_lc):
         "attention": ("hbm", kv + M * D * 4 + M * D * 4 + nr * D * 2),
         # GLU rows in, conv tail (8 rows) in, n rows committed, output
         "dwconv": ("hbm", M * D * 2 + S * 8 * D * 2 + M * D * 2 + M * D * 2 + 12 * D * 4),
-        # per launch, averaged over the step's LayerNorms: x in (4 B) and a split
-        # (hi, lo) bf16 output (4 B) for 1 + 3L of them; ln_out also writes x
-        # in place (4 B) for L - 1, and the last writes fp32 frames + plain bf16
-        "layernorm": ("hbm", M * D * ((1 + 3 * L) * 8 + (L - 1) * 12 + 10) / (4 * L + 1)),
+        # per launch, averaged over the step's LayerNorm launches.  bf16: the
+        # attention, conv and FF2 LayerNorms run inside the GEMMs after them, so
+        # the launches are the first FF1 LayerNorm (x in 4 B, split (hi, lo)
+        # bf16 out 4 B), ln_out fused with the next FF1 LayerNorm for L - 1
+        # layers (x in, x in place, split out: 12 B) and the last ln_out (x in,
+        # fp32 frames + plain bf16 out: 10 B).  fp32: 1 + 3L plain LayerNorms
+        # as well (8 B).
+        "layernorm": ("hbm", M * D * (8 + (L - 1) * 12 + 10) / (L + 1) if cfg.dtype == "bf16"
+                      else M * D * ((1 + 3 * L) * 8 + (L - 1) * 12 + 10) / (4 * L + 1)),
         "stage_mel": ("hbm", S * (8 * n + 14) * 128 * 4 + S * W1 * 128 * 2 + S * 14 * 128 * 2),
     }
 

@@ -85,6 +85,35 @@ WORKLOADS = {
 }
 
 
+@dataclass(frozen=True)
+class DecoderConfig:
+    """Greedy RNN-T decoder with an end-of-utterance class: an LSTM predictor
+    over the last emitted token, a joint ReLU(enc_proj + pred_proj) -> logits
+    over vocab + blank + EOU, argmax per decision.  Ids: tokens 0 .. vocab-1,
+    blank = vocab, eou = vocab + 1."""
+    vocab: int = 1024
+    pred_dim: int = 640           # LSTM hidden / embedding width
+    joint_dim: int = 640          # width of both projections into the joint
+    max_symbols: int = 10         # emissions per encoder frame before forcing a blank
+    blank_bias: float = 3.4       # synthetic init: offset on the blank bias (about 0.3 emissions per frame)
+
+    @property
+    def blank(self) -> int:
+        return self.vocab
+
+    @property
+    def eou(self) -> int:
+        return self.vocab + 1
+
+    @property
+    def classes(self) -> int:
+        return self.vocab + 2
+
+
+EOU_DECODER = DecoderConfig()
+TINY_DECODER = DecoderConfig(vocab=30, pred_dim=32, joint_dim=64, max_symbols=3)
+
+
 def subsampled_len(t_mel: int) -> int:
     """Encoder frames produced from t_mel mel frames: ceil(.) three times."""
     t = t_mel

@@ -212,6 +212,62 @@ def make_weights_parallel(cfg: ModelConfig, seed: int = 0, workers: int = 8) -> 
     return dict(items)
 
 
+# ---------------------------------------------------------------------------
+# Greedy RNN-T decoder (fp32): weights and projected encoder frames
+# ---------------------------------------------------------------------------
+
+TID_DEC = 1 << 21          # decoder weights: TID_DEC + index in decoder_layout
+TID_JOINT_FRAMES = (1 << 21) + 1000
+
+
+def decoder_layout(dcfg):
+    """Ordered (name, shape, kind) of the decoder parameters; linears [out, in],
+    LSTM gate rows in the order input, forget, cell, output."""
+    C, P, J = dcfg.classes, dcfg.pred_dim, dcfg.joint_dim
+    return [("emb", (C, P), "embed"),
+            ("lstm.w_ih", (4 * P, P), ("xavier", P, 4 * P)), ("lstm.w_hh", (4 * P, P), ("xavier", P, 4 * P)),
+            ("lstm.b_ih", (4 * P,), "bias"), ("lstm.b_hh", (4 * P,), "bias"),
+            ("pred.w", (J, P), ("xavier", P, J)), ("pred.b", (J,), "bias"),
+            ("out.w", (C, J), ("xavier", J, C)), ("out.b", (C,), "out_bias")]
+
+
+def make_decoder_weights(dcfg, seed: int = 0) -> dict:
+    """Named float32 decoder parameters: Xavier-normal linears, N(0, 1)
+    embedding rows, N(0, 0.02^2) biases; the output bias of the blank class is
+    raised by dcfg.blank_bias so that most decisions are blank, as in speech."""
+    out = {}
+    for tid, (name, shape, kind) in enumerate(decoder_layout(dcfg)):
+        n = int(np.prod(shape))
+        k = key(seed, TID_DEC + tid)
+        if kind == "embed":
+            v = normal(k, n)
+        elif kind in ("bias", "out_bias"):
+            v = 0.02 * normal(k, n)
+            if kind == "out_bias":
+                v[dcfg.blank] += dcfg.blank_bias
+        else:
+            _, fi, fo = kind
+            v = np.sqrt(2.0 / (fi + fo)) * normal(k, n)
+        out[name] = v.astype(np.float32).reshape(shape)
+    return out
+
+
+def pack_decoder_weights(dcfg, w: dict) -> np.ndarray:
+    """Flat float32 blob in decoder_layout order (the C library's input format)."""
+    parts = []
+    for name, shape, _ in decoder_layout(dcfg):
+        a = np.asarray(w[name], dtype=np.float32)
+        assert a.shape == tuple(shape), (name, a.shape, shape)
+        parts.append(a.reshape(-1))
+    return np.ascontiguousarray(np.concatenate(parts))
+
+
+def make_joint_frames(n_frames: int, stream_id: int, joint_dim: int = 640, seed_base: int = 3000) -> np.ndarray:
+    """[n_frames, joint_dim] float32 stand-in for projected encoder frames: N(0, 1)."""
+    k = key(seed_base + stream_id, TID_JOINT_FRAMES)
+    return normal(k, n_frames * joint_dim).reshape(n_frames, joint_dim).astype(np.float32)
+
+
 def _mel_job(args):
     n_frames, sid, silence_frac = args
     return make_mel(n_frames, sid, silence_frac=silence_frac)
