@@ -111,7 +111,7 @@ class DecoderConfig:
 
 
 EOU_DECODER = DecoderConfig()
-TINY_DECODER = DecoderConfig(vocab=30, pred_dim=32, joint_dim=64, max_symbols=3)
+TINY_DECODER = DecoderConfig(vocab=30, pred_dim=64, joint_dim=64, max_symbols=3)
 
 
 def subsampled_len(t_mel: int) -> int:

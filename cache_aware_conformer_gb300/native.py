@@ -29,7 +29,10 @@ SYMBOLS = ["cac_weights_size", "cac_model_create", "cac_model_destroy", "cac_poo
            "cac_stream_set_state", "cac_pool_check", "cac_model_check", "cac_pool_set_graphs",
            "cac_pool_launch_count", "cac_pool_set_trace", "cac_pool_read_trace", "cac_pool_set_profile",
            "cac_pool_read_profile", "cac_profile_classes", "cac_profile_class_name", "cac_strerror",
-           "cac_op_gemm_bf16", "cac_encode_offline_noalloc"]
+           "cac_op_gemm_bf16", "cac_encode_offline_noalloc",
+           # include/cac_decode.h
+           "cac_decoder_create", "cac_decoder_destroy", "cac_decoder_reset", "cac_decoder_step",
+           "cac_decoder_check", "cac_decoder_get_state"]
 
 
 class CacError(RuntimeError):
@@ -42,6 +45,10 @@ class CacConfig(ctypes.Structure):
     _fields_ = [(n, c_int32) for n in (
         "n_layers", "d_model", "n_heads", "ff_dim", "dw_kernel", "att_left", "att_chunk", "mel_bins",
         "joint_dim", "dtype", "right_context", "emit_frames", "lookahead_frames", "gemm_simt")]
+
+
+class CacDecConfig(ctypes.Structure):
+    _fields_ = [(n, c_int32) for n in ("vocab", "pred_dim", "joint_dim", "max_symbols")]
 
 
 class CacStreamState(ctypes.Structure):
@@ -89,6 +96,12 @@ def _lib():
             "cac_profile_class_name": (c_char_p, [c_int]),
             "cac_strerror": (c_char_p, [c_int]),
             "cac_op_gemm_bf16": (c_int, [c_int, c_int, c_int, vp, vp, vp, vp, c_int, c_int, vp]),
+            "cac_decoder_create": (c_int, [POINTER(CacDecConfig), fp, c_size_t, c_int, POINTER(vp)]),
+            "cac_decoder_destroy": (None, [vp]),
+            "cac_decoder_reset": (c_int, [vp, c_int, ip, vp]),
+            "cac_decoder_step": (c_int, [vp, c_int, ip, vp, c_longlong, c_int, vp, vp, vp, vp]),
+            "cac_decoder_check": (c_int, [vp]),
+            "cac_decoder_get_state": (c_int, [vp, c_int, fp, fp, fp, ip]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -350,3 +363,63 @@ class Pool:
         _check(_lib().cac_pool_read_trace(self.h, layer, tap, out.ctypes.data_as(POINTER(c_float)), out.size),
                "cac_pool_read_trace")
         return out
+
+
+class Decoder:
+    """Batched greedy RNN-T + EOU decoder on the current CUDA device
+    (include/cac_decode.h): per-stream predictor state for ids 0 .. max_streams-1."""
+
+    def __init__(self, dcfg, blob: np.ndarray, max_streams: int):
+        self.cfg = dcfg
+        blob = np.ascontiguousarray(blob, dtype=np.float32)
+        self._c = CacDecConfig(dcfg.vocab, dcfg.pred_dim, dcfg.joint_dim, dcfg.max_symbols)
+        h = c_void_p()
+        _check(_lib().cac_decoder_create(ctypes.byref(self._c), blob.ctypes.data_as(POINTER(c_float)), blob.size,
+                                         max_streams, ctypes.byref(h)), "cac_decoder_create")
+        self.h = h
+        self.max_streams = max_streams
+
+    def close(self):
+        if self.h:
+            _lib().cac_decoder_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def reset(self, ids, stream=None):
+        _check(_lib().cac_decoder_reset(self.h, len(ids), _ids(ids), _stream(stream)), "cac_decoder_reset")
+
+    def step_into(self, ids, z, tokens, frames, counts, stream=None):
+        """z: cuda fp32 [n, T, joint_dim] (slots may be strided); outputs int32
+        cuda tensors [n, T * max_symbols], [n, T * max_symbols], [n]."""
+        n, T, J = z.shape
+        assert J == self.cfg.joint_dim and z.stride(2) == 1 and (T <= 1 or z.stride(1) == J)
+        bstride = z.stride(0) if n > 1 else T * J  # a size-1 dimension may carry any stride
+        _check(_lib().cac_decoder_step(self.h, n, _ids(ids), _ptr(z), bstride, T, _ptr(tokens), _ptr(frames),
+                                       _ptr(counts), _stream(stream)), "cac_decoder_step")
+
+    def step(self, ids, z, stream=None):
+        import torch
+        n, T, _ = z.shape
+        w = T * self.cfg.max_symbols
+        tokens = torch.full((n, w), -1, dtype=torch.int32, device=z.device)
+        frames = torch.full((n, w), -1, dtype=torch.int32, device=z.device)
+        counts = torch.zeros(n, dtype=torch.int32, device=z.device)
+        self.step_into(ids, z, tokens, frames, counts, stream)
+        return tokens, frames, counts
+
+    def check(self):
+        _check(_lib().cac_decoder_check(self.h), "cac_decoder_check")
+
+    def state(self, sid: int):
+        P, J = self.cfg.pred_dim, self.cfg.joint_dim
+        h, c, p = np.zeros(P, np.float32), np.zeros(P, np.float32), np.zeros(J, np.float32)
+        primed = c_int(0)
+        fp = POINTER(c_float)
+        _check(_lib().cac_decoder_get_state(self.h, sid, h.ctypes.data_as(fp), c.ctypes.data_as(fp),
+                                            p.ctypes.data_as(fp), ctypes.byref(primed)), "cac_decoder_get_state")
+        return h, c, p, primed.value
