@@ -33,7 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from cache_aware_conformer_gb300 import synth  # noqa: E402
-from cache_aware_conformer_gb300.config import WORKLOADS, FRAME_SEC  # noqa: E402
+from cache_aware_conformer_gb300.config import WORKLOADS, FRAME_SEC, EOU_DECODER  # noqa: E402
 
 METRIC = "streamed audio-sec/sec (B streams, 160 ms chunks) + % of tensor/HBM roofline"
 UNIT = "audio-s/s"
@@ -444,7 +444,8 @@ def run_ours(args, wl):
     K, Wm = args.steps, args.warmup
     Kp = min(K, args.profile_steps)
     Ke = min(K, args.e2e_steps)
-    total_steps = Wm + K + 2 * Kp + Ke
+    Kd = min(K, args.decode_steps) if wl.model.joint_dim == EOU_DECODER.joint_dim and not wl.model.provisional else 0
+    total_steps = Wm + K + 2 * Kp + Ke + (Kd + 3 if Kd else 0)
     workers = max(1, min(cpu_cores(), 16))
     w = StreamWorkload(wl, rank, dev, total_steps, workers)
     w.pool.set_graphs(True)
@@ -539,6 +540,8 @@ def run_ours(args, wl):
            "d2h_bytes_per_step": w.S * w.n * (w.cfg.d_model + w.cfg.joint_dim) * 4}
     w.pool.check()
 
+    decode = measure_decode(w, Kd, dev, clk) if Kd else None
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w.cfg, w.blob, args.cpu_chunks)
@@ -549,8 +552,81 @@ def run_ours(args, wl):
                 "dtype": "bf16", "data": "synthetic",
                 "config": dict(workload_config(wl, world), mean_Lc=mean_lc),
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-                "latency": latency, "gpu_launches": launches, "clocks": clk}
+                "latency": latency, "gpu_launches": launches, "clocks": clk, "decode": decode}
         print(json.dumps(line), flush=True)
+
+
+def fp32_alu_peak(sm_mhz: float) -> float:
+    """FP32 FMA peak, TFLOP/s: SMs x 128 FP32 lanes x 2 FLOP x SM clock."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def measure_decode(w, Kd: int, dev, clk):
+    """The greedy RNN-T + EOU decoder (fp32, include/cac_decode.h), 2 frames
+    per stream per step: (a) encoder step + decode step back to back, (b) the
+    decode step alone, CUDA events on the launching stream; decisions and
+    emissions per step from an untimed pass over the same frames.  The decoder
+    reads seeded projected frames (synth.make_joint_frames, about 0.3
+    emissions per frame with the synthetic decoder weights) resident on the
+    device, not the random-weight encoder's projections, on which a blank
+    always wins."""
+    import torch
+    from cache_aware_conformer_gb300 import native
+    dc = EOU_DECODER
+    Wd = synth.make_decoder_weights(dc, 0)
+    dec = native.Decoder(dc, synth.pack_decoder_weights(dc, Wd), w.S)
+    ids = list(range(w.S))
+    T = w.n
+    tok = torch.empty(w.S, T * dc.max_symbols, dtype=torch.int32, device=dev)
+    fr = torch.empty_like(tok)
+    cn = torch.empty(w.S, dtype=torch.int32, device=dev)
+    nz = Kd + 3
+    zs = torch.from_numpy(np.stack([synth.make_joint_frames(nz * T, s, dc.joint_dim) for s in ids])).to(dev)
+    frames_of = lambda i: zs[:, (i % nz) * T:(i % nz + 1) * T]
+    for i in range(3):
+        w.step()
+        dec.step_into(ids, frames_of(i), tok, fr, cn)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(Kd):
+        w.step()
+        dec.step_into(ids, frames_of(3 + i), tok, fr, cn)
+    e1.record()
+    torch.cuda.synchronize()
+    both_ms = e0.elapsed_time(e1) / Kd
+    dec.reset(ids)
+    e0.record()
+    for i in range(Kd):
+        dec.step_into(ids, frames_of(i), tok, fr, cn)
+    e1.record()
+    torch.cuda.synchronize()
+    dec_ms = e0.elapsed_time(e1) / Kd
+    dec.reset(ids)
+    em = dcs = 0
+    for i in range(Kd):
+        dec.step_into(ids, frames_of(i), tok, fr, cn)
+        c = cn.cpu().numpy()
+        f = fr.cpu().numpy()
+        forced = sum(int(np.sum(np.bincount(f[b, :c[b]], minlength=T) == dc.max_symbols)) for b in range(w.S))
+        em += int(c.sum())
+        dcs += int(c.sum()) + w.S * T - forced
+    dec.check()
+    dec.close()
+    em, dcs = em / Kd, dcs / Kd
+    C, P, J = dc.classes, dc.pred_dim, dc.joint_dim
+    flops = dcs * 2.0 * C * J + em * (2.0 * 4 * P * P + 2.0 * J * P)   # joint per decision, LSTM + projection per emission
+    peak = fp32_alu_peak(clk.get("sm_max_mhz") or 2070.0)
+    ach = flops / (dec_ms * 1e-3) / 1e12
+    return {"what": "greedy RNN-T + EOU decode of the step's 2 frames per stream (fp32, one cooperative launch)",
+            "dtype": "f32", "ms_per_step": dec_ms, "decisions_per_step": dcs, "emissions_per_step": em,
+            "encode_plus_decode": {"value": w.S * T * FRAME_SEC / (both_ms * 1e-3), "unit": UNIT,
+                                   "ms_per_step": both_ms},
+            "roofline": {"bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                         "traffic": None,
+                         "peak_source": "derived: SMs x 128 FP32 lanes x 2 FLOP x max SM clock"}}
 
 
 def cpu_baseline(cfg, blob, chunks: int):
@@ -622,6 +698,7 @@ def main(argv=None):
     ap.add_argument("--cpu-chunks", type=int, default=6)
     ap.add_argument("--ref-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-steps", type=int, default=40)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -25,6 +25,7 @@
 // other waiter, and returns.  Everything is fp32 on the CUDA cores (the pages
 // fix fp32 for the decoder, so every argmax is decided in fp32).
 #include <cfloat>
+#include <climits>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -38,9 +39,7 @@ namespace {
 
 constexpr int DT = 256;        // threads per CTA
 constexpr int TS = 32;         // slots per tile
-constexpr int TN = 64;         // output columns per tile
-constexpr int KC = 64;         // K chunk staged in shared memory
-constexpr int WLD = KC + 4;    // row stride of the staged weight chunk
+constexpr int TN = 16;         // output columns per tile
 constexpr int OLD = TN + 1;    // row stride of the output tile
 
 struct DecParams {
@@ -102,186 +101,252 @@ __device__ bool grid_sync(const DecParams& d) {
 
 __device__ __forceinline__ float sigm(float x) { return 1.f / (1.f + expf(-x)); }
 
-// acc[s][j] += sum_k As[slot row][k] * W[row j][k] for the thread's 2 slots (sx,
-// sx + 16) and 4 columns (cx + 16 j); W rows come from wrow(r) (nullptr: zero),
-// K a multiple of KC.  As: [TS][K + 4] in shared memory, filled by the caller.
-template <class WRow>
-__device__ __forceinline__ void mac_tile(int K, const float* As, float* Ws, WRow wrow, float (&acc)[2][4]) {
-    const int tid = threadIdx.x, sx = tid & 15, cx = tid >> 4;
-    const int lda = K + 4;
-    for (int k0 = 0; k0 < K; k0 += KC) {
-        for (int e = tid; e < TN * KC / 4; e += DT) {
-            const int r = e >> 4, q = e & 15;
-            const float* src = wrow(r);
-            const float4 w = src ? __ldg(reinterpret_cast<const float4*>(src + k0) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-            *reinterpret_cast<float4*>(Ws + r * WLD + 4 * q) = w;
-        }
-        __syncthreads();
-#pragma unroll 4
-        for (int kk = 0; kk < KC; kk += 4) {
-            const float4 a0 = *reinterpret_cast<const float4*>(As + sx * lda + k0 + kk);
-            const float4 a1 = *reinterpret_cast<const float4*>(As + (sx + 16) * lda + k0 + kk);
+// Os[slot][col] = sum_k As[slot][k] * Ws[col][k] for the tile's 32 slots x
+// TN columns.  Warp w takes the K segment [w K/8, (w + 1) K/8) for all 512
+// outputs (lane = slot, 16 independent accumulators, weights broadcast to the
+// warp), so the tile's latency is one segment whatever the number of live
+// slots; the 8 partial tiles are summed through `red` (8 x 512 floats).  K a
+// multiple of 32, rows K + 4 floats apart.
+__device__ __forceinline__ void mac16(int K, const float* As, const float* Ws, float* Os, float* red) {
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, ld = K + 4;
+    const int seg = K / 8, k0 = w * seg;
+    float acc[TN];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float4 w = *reinterpret_cast<const float4*>(Ws + (cx + 16 * j) * WLD + kk);
-                acc[0][j] = fmaf(a0.x, w.x, acc[0][j]);
-                acc[0][j] = fmaf(a0.y, w.y, acc[0][j]);
-                acc[0][j] = fmaf(a0.z, w.z, acc[0][j]);
-                acc[0][j] = fmaf(a0.w, w.w, acc[0][j]);
-                acc[1][j] = fmaf(a1.x, w.x, acc[1][j]);
-                acc[1][j] = fmaf(a1.y, w.y, acc[1][j]);
-                acc[1][j] = fmaf(a1.z, w.z, acc[1][j]);
-                acc[1][j] = fmaf(a1.w, w.w, acc[1][j]);
-            }
+    for (int c = 0; c < TN; ++c) acc[c] = 0.f;
+    const float* ap = As + lane * ld + k0;
+    const float* wp = Ws + k0;
+#pragma unroll 2
+    for (int k = 0; k < seg; k += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(ap + k);
+#pragma unroll
+        for (int c = 0; c < TN; ++c) {
+            const float4 v = *reinterpret_cast<const float4*>(wp + c * ld + k);
+            acc[c] = fmaf(a.x, v.x, acc[c]);
+            acc[c] = fmaf(a.y, v.y, acc[c]);
+            acc[c] = fmaf(a.z, v.z, acc[c]);
+            acc[c] = fmaf(a.w, v.w, acc[c]);
         }
-        __syncthreads();
+    }
+    float4* rp = reinterpret_cast<float4*>(red + w * TS * TN + lane * TN);
+#pragma unroll
+    for (int q = 0; q < TN / 4; ++q) rp[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+    __syncthreads();
+    for (int o = tid; o < TS * TN; o += DT) {
+        float sum = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < 8; ++ww) sum += red[ww * TS * TN + o];
+        Os[(o / TN) * OLD + (o % TN)] = sum;
     }
 }
 
-// thread's accumulators into the output tile Os [TS][OLD]
-__device__ __forceinline__ void store_tile(float* Os, const float (&acc)[2][4]) {
-    const int tid = threadIdx.x, sx = tid & 15, cx = tid >> 4;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        Os[sx * OLD + cx + 16 * j] = acc[0][j];
-        Os[(sx + 16) * OLD + cx + 16 * j] = acc[1][j];
+// Stage one tile's rows with the TMA engine: every row is contiguous (K
+// floats), so one bulk copy per row lands it in shared memory (rows K + 4
+// floats apart) and completes on `bar`.  Sources: A rows from a0[r] into A0
+// and, if a1, from a1[r] into A1 (only when load_a), weight rows wrow(r) into
+// Ws; nullptr rows are zero-filled.  Every thread calls; false when the wait
+// gave up (CAC_E_TIMEOUT latched, abort raised).
+template <class WRow>
+__device__ bool stage_tile(const DecParams& d, int K, bool load_a, float* A0, const float* const* a0, float* A1,
+                           const float* const* a1, float* Ws, WRow wrow, uint64_t* bar, uint32_t& phase) {
+    const int q4 = K / 4, ld = K + 4, tid = threadIdx.x;
+    if (load_a) {
+        for (int e = tid; e < TS * q4; e += DT) {
+            const int r = e / q4, q = e - r * q4;
+            if (!a0[r]) *reinterpret_cast<float4*>(A0 + r * ld + 4 * q) = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (a1 && !a1[r]) *reinterpret_cast<float4*>(A1 + r * ld + 4 * q) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
+    for (int e = tid; e < TN * q4; e += DT) {
+        const int r = e / q4, q = e - r * q4;
+        if (!wrow(r)) *reinterpret_cast<float4*>(Ws + r * ld + 4 * q) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();  // zero fills and every earlier read of these buffers are done
+    if (tid < 32) {  // warp 0: lane 0 posts the byte count, the lanes issue one row each
+        const uint32_t rb = (uint32_t)K * 4;
+        if (tid == 0) {
+            fence_proxy_async_smem();
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            uint32_t bytes = 0;
+            for (int r = 0; r < TN; ++r) bytes += wrow(r) ? rb : 0;
+            if (load_a)
+                for (int r = 0; r < TS; ++r) bytes += (a0[r] ? rb : 0) + (a1 && a1[r] ? rb : 0);
+            mbar_expect_tx(bar, bytes);
+        }
+        __syncwarp();
+        if (tid < TN)
+            if (const float* w = wrow(tid)) bulk_g2s(Ws + tid * ld, w, rb, bar);
+        if (load_a) {
+            if (a0[tid]) bulk_g2s(A0 + tid * ld, a0[tid], rb, bar);
+            if (a1 && a1[tid]) bulk_g2s(A1 + tid * ld, a1[tid], rb, bar);
+        }
+    }
+    const bool ok = __syncthreads_and(mbar_wait(bar, phase));
+    phase ^= 1u;
+    if (!ok && tid == 0) {
+        latch_error(d.status, CAC_E_TIMEOUT);
+        atomicExch(d.abort_flag, 1);
+    }
+    return ok;
 }
+
+// Per-tile row table in shared memory: the slot b, stream id and (phase A)
+// token-independent row pointers of the tile's 32 rows, resolved once by 32
+// threads so that the bulk row loads that follow are independent.
+struct RowTab {
+    int b[TS], id[TS], k[TS];
+    const float* src[TS];  // A row source (nullptr: padding row)
+    const float* aux[TS];  // phase A: the stream's predictor projection p
+};
 
 // Phase C: LSTM step of the queued slots em[0 .. ne) with tokens emk[.]:
-// tile (32 slots, 16 hidden units = the 4 x 16 gate rows of those units).
+// tile = (32 slots, 4 hidden units = the 4 x 4 gate rows of those units).
 __device__ void phase_lstm(const DecParams& d, const int* em, const int* emk, int ne, float* As, float* Ws,
-                           float* Os) {
-    const int P = d.P, lda = P + 4, tid = threadIdx.x;
-    const int ut = P / 16, tiles = ((ne + TS - 1) / TS) * ut;
+                           float* Os, float* red, RowTab& rt, uint64_t* bar, uint32_t& phase) {
+    const int P = d.P, tid = threadIdx.x;
+    const int ut = P / 4, tiles = ((ne + TS - 1) / TS) * ut;
     int loaded = -1;  // slot tile whose h rows sit in As
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
-        const int st = t / ut, j0 = (t % ut) * 16;
-        if (st != loaded) {
+        const int st = t / ut, j0 = (t % ut) * 4;
+        const bool load_a = st != loaded;
+        if (load_a) {
             __syncthreads();
-            for (int e = tid; e < TS * P / 4; e += DT) {
-                const int r = e / (P / 4), q = e % (P / 4), i = st * TS + r;
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (tid < TS) {
+                const int i = st * TS + tid;
+                rt.src[tid] = nullptr;
                 if (i < ne) {
-                    const int id = d.ids[__ldcg(em + i)];
-                    v = __ldcg(reinterpret_cast<const float4*>(d.h + (long long)id * P) + q);
+                    const int b = __ldcg(em + i), id = d.ids[b];
+                    rt.b[tid] = b;
+                    rt.id[tid] = id;
+                    rt.k[tid] = __ldcg(emk + i);
+                    rt.src[tid] = d.h + (long long)id * P;
                 }
-                *reinterpret_cast<float4*>(As + r * lda + 4 * q) = v;
             }
             __syncthreads();
             loaded = st;
         }
-        float acc[2][4] = {};
-        mac_tile(P, As, Ws, [&](int r) { return d.whh + (long long)((r >> 4) * P + j0 + (r & 15)) * P; }, acc);
-        store_tile(Os, acc);
+        if (!stage_tile(d, P, load_a, As, rt.src, nullptr, nullptr, Ws,
+                        [&](int r) -> const float* { return d.whh + (long long)((r >> 2) * P + j0 + (r & 3)) * P; },
+                        bar, phase))
+            return;
+        mac16(P, As, Ws, Os, red);
         __syncthreads();
-        // cell update of (slot r, unit jj): two per thread
-        for (int e = tid; e < TS * 16; e += DT) {
-            const int r = e >> 4, jj = e & 15, i = st * TS + r;
-            if (i >= ne) continue;
-            const int b = __ldcg(em + i), k = __ldcg(emk + i), id = d.ids[b], j = j0 + jj;
-            const float* tb = d.tab + (long long)k * 4 * P;
-            const float gi = Os[r * OLD + jj] + __ldg(tb + j);
-            const float gf = Os[r * OLD + 16 + jj] + __ldg(tb + P + j);
-            const float gg = Os[r * OLD + 32 + jj] + __ldg(tb + 2 * P + j);
-            const float go = Os[r * OLD + 48 + jj] + __ldg(tb + 3 * P + j);
-            float* cp = d.c + (long long)id * P + j;
-            const float c2 = sigm(gf) * __ldcg(cp) + sigm(gi) * tanhf(gg);
-            *cp = c2;
-            d.hnext[(long long)b * P + j] = sigm(go) * tanhf(c2);
+        if (tid < TS * 4) {  // cell update of (slot r, unit jj)
+            const int r = tid >> 2, jj = tid & 3;
+            if (rt.src[r]) {
+                const int b = rt.b[r], id = rt.id[r], j = j0 + jj;
+                const float* tb = d.tab + (long long)rt.k[r] * 4 * P;
+                const float gi = Os[r * OLD + jj] + __ldg(tb + j);
+                const float gf = Os[r * OLD + 4 + jj] + __ldg(tb + P + j);
+                const float gg = Os[r * OLD + 8 + jj] + __ldg(tb + 2 * P + j);
+                const float go = Os[r * OLD + 12 + jj] + __ldg(tb + 3 * P + j);
+                float* cp = d.c + (long long)id * P + j;
+                const float c2 = sigm(gf) * __ldcg(cp) + sigm(gi) * tanhf(gg);
+                *cp = c2;
+                d.hnext[(long long)b * P + j] = sigm(go) * tanhf(c2);
+            }
         }
-        __syncthreads();
+        __syncthreads();  // Ws, Os and the row table are reused by the next tile
     }
 }
 
 // Phase D: p = W_pred h' + b_pred for the queued slots, and h <- h'.
-__device__ void phase_proj(const DecParams& d, const int* em, int ne, float* As, float* Ws) {
-    const int P = d.P, J = d.J, lda = P + 4, tid = threadIdx.x;
+__device__ void phase_proj(const DecParams& d, const int* em, int ne, float* As, float* Ws, float* Os,
+                           float* red, RowTab& rt, uint64_t* bar, uint32_t& phase) {
+    const int P = d.P, J = d.J, tid = threadIdx.x;
     const int jt = J / TN, tiles = ((ne + TS - 1) / TS) * jt;
     int loaded = -1;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
         const int st = t / jt, c0 = (t % jt) * TN;
-        if (st != loaded) {
+        const bool load_a = st != loaded;
+        if (load_a) {
             __syncthreads();
-            for (int e = tid; e < TS * P / 4; e += DT) {
-                const int r = e / (P / 4), q = e % (P / 4), i = st * TS + r;
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (tid < TS) {
+                const int i = st * TS + tid;
+                rt.src[tid] = nullptr;
                 if (i < ne) {
                     const int b = __ldcg(em + i);
-                    v = __ldcg(reinterpret_cast<const float4*>(d.hnext + (long long)b * P) + q);
+                    rt.b[tid] = b;
+                    rt.id[tid] = d.ids[b];
+                    rt.src[tid] = d.hnext + (long long)b * P;
                 }
-                *reinterpret_cast<float4*>(As + r * lda + 4 * q) = v;
             }
             __syncthreads();
             loaded = st;
         }
+        if (!stage_tile(d, P, load_a, As, rt.src, nullptr, nullptr, Ws,
+                        [&](int r) -> const float* { return d.wpp + (long long)(c0 + r) * P; }, bar, phase))
+            return;
         if (c0 == 0) {  // the first column tile of each slot tile commits h <- h'
             for (int e = tid; e < TS * P / 4; e += DT) {
-                const int r = e / (P / 4), q = e % (P / 4), i = st * TS + r;
-                if (i < ne)
-                    reinterpret_cast<float4*>(d.h + (long long)d.ids[__ldcg(em + i)] * P)[q] =
-                        *reinterpret_cast<const float4*>(As + r * lda + 4 * q);
+                const int r = e / (P / 4), q = e % (P / 4);
+                if (rt.src[r])
+                    reinterpret_cast<float4*>(d.h + (long long)rt.id[r] * P)[q] =
+                        *reinterpret_cast<const float4*>(As + r * (P + 4) + 4 * q);
             }
         }
-        float acc[2][4] = {};
-        mac_tile(P, As, Ws, [&](int r) { return d.wpp + (long long)(c0 + r) * P; }, acc);
-        const int sx = tid & 15, cx = tid >> 4;
-#pragma unroll
-        for (int s2 = 0; s2 < 2; ++s2) {
-            const int i = st * TS + sx + 16 * s2;
-            if (i >= ne) continue;
-            const int id = d.ids[__ldcg(em + i)];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int col = c0 + cx + 16 * j;
-                d.p[(long long)id * J + col] = acc[s2][j] + __ldg(d.bpp + col);
-            }
+        mac16(P, As, Ws, Os, red);
+        __syncthreads();
+        for (int e = tid; e < TS * TN; e += DT) {
+            const int r = e / TN, cc = e % TN;
+            if (rt.src[r]) d.p[(long long)rt.id[r] * J + c0 + cc] = Os[r * OLD + cc] + __ldg(d.bpp + c0 + cc);
         }
+        __syncthreads();
     }
 }
 
 // Phase A: logits of the active slots act[0 .. na) at their current frame,
-// partial first-maximum per 64-class tile into pval / pidx [slot][nct].
-__device__ void phase_joint(const DecParams& d, const int* act, int na, float* As, float* Ws, float* Os) {
-    const int J = d.J, C = d.C, lda = J + 4, tid = threadIdx.x;
+// partial first-maximum per TN-class tile into pval / pidx [slot][nct].
+__device__ void phase_joint(const DecParams& d, const int* act, int na, float* As, float* Ws, float* Os,
+                            float* Ps, float* red, RowTab& rt, uint64_t* bar, uint32_t& phase) {
+    const int J = d.J, C = d.C, tid = threadIdx.x;
     const int tiles = ((na + TS - 1) / TS) * d.nct;
     int loaded = -1;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
         const int st = t / d.nct, ct = t % d.nct, c0 = ct * TN;
-        if (st != loaded) {
+        const bool load_a = st != loaded;
+        if (load_a) {
             __syncthreads();
-            for (int e = tid; e < TS * J / 4; e += DT) {
-                const int r = e / (J / 4), q = e % (J / 4), i = st * TS + r;
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (tid < TS) {
+                const int i = st * TS + tid;
+                rt.src[tid] = nullptr;
+                rt.aux[tid] = nullptr;
                 if (i < na) {
                     const int b = __ldcg(act + i), id = d.ids[b], f = __ldcg(d.frame + b);
-                    const float4 zz = __ldg(reinterpret_cast<const float4*>(d.z + b * d.zb + (long long)f * J) + q);
-                    const float4 pp = __ldcg(reinterpret_cast<const float4*>(d.p + (long long)id * J) + q);
-                    v = make_float4(fmaxf(zz.x + pp.x, 0.f), fmaxf(zz.y + pp.y, 0.f), fmaxf(zz.z + pp.z, 0.f),
-                                    fmaxf(zz.w + pp.w, 0.f));
+                    rt.b[tid] = b;
+                    rt.src[tid] = d.z + b * d.zb + (long long)f * J;
+                    rt.aux[tid] = d.p + (long long)id * J;
                 }
-                *reinterpret_cast<float4*>(As + r * lda + 4 * q) = v;
+            }
+            __syncthreads();
+        }
+        if (!stage_tile(d, J, load_a, As, rt.src, Ps, rt.aux, Ws,
+                        [&](int r) -> const float* { return c0 + r < C ? d.wout + (long long)(c0 + r) * J : nullptr; },
+                        bar, phase))
+            return;
+        if (load_a) {
+            for (int e = tid; e < TS * J / 4; e += DT) {  // As <- ReLU(z + p)
+                const int r = e / (J / 4), q = e % (J / 4);
+                float4* a = reinterpret_cast<float4*>(As + r * (J + 4) + 4 * q);
+                const float4 pp = *reinterpret_cast<const float4*>(Ps + r * (J + 4) + 4 * q);
+                const float4 zz = *a;
+                *a = make_float4(fmaxf(zz.x + pp.x, 0.f), fmaxf(zz.y + pp.y, 0.f), fmaxf(zz.z + pp.z, 0.f),
+                                 fmaxf(zz.w + pp.w, 0.f));
             }
             __syncthreads();
             loaded = st;
         }
-        float acc[2][4] = {};
-        mac_tile(J, As, Ws, [&](int r) { return c0 + r < C ? d.wout + (long long)(c0 + r) * J : nullptr; }, acc);
-        store_tile(Os, acc);
+        mac16(J, As, Ws, Os, red);
         __syncthreads();
-        if (tid < TS) {
-            const int i = st * TS + tid;
-            if (i < na) {
-                float best = -FLT_MAX;
-                int bi = c0;
-                for (int q = 0; q < TN && c0 + q < C; ++q) {
-                    const float v = Os[tid * OLD + q] + __ldg(d.bout + c0 + q);
-                    if (v > best) { best = v; bi = c0 + q; }
-                }
-                const int b = __ldcg(act + i);
-                d.pval[(long long)b * d.nct + ct] = best;
-                d.pidx[(long long)b * d.nct + ct] = bi;
+        if (tid < TS && rt.src[tid]) {
+            float best = -FLT_MAX;
+            int bi = c0;
+            for (int q = 0; q < TN && c0 + q < C; ++q) {
+                const float v = Os[tid * OLD + q] + __ldg(d.bout + c0 + q);
+                if (v > best) { best = v; bi = c0 + q; }
             }
+            const int b = rt.b[tid];
+            d.pval[(long long)b * d.nct + ct] = best;
+            d.pidx[(long long)b * d.nct + ct] = bi;
         }
         __syncthreads();
     }
@@ -296,7 +361,17 @@ __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
     const int K = d.P > d.J ? d.P : d.J;
     float* As = smem;
     float* Ws = As + TS * (K + 4);
-    float* Os = Ws + TN * WLD;
+    float* Os = Ws + TN * (K + 4);
+    float* Ps = Os + TS * OLD;  // phase A: the p rows (TS x (J + 4))
+    float* red = Ps + TS * (d.J + 4);  // partial tiles of mac16 (8 x TS x TN)
+    __shared__ RowTab rt;
+    __shared__ __align__(8) uint64_t tbar;
+    uint32_t tphase = 0;
+    if (threadIdx.x == 0) {
+        mbar_init(&tbar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
     const int gtid = blockIdx.x * DT + threadIdx.x, gstride = gridDim.x * DT;
     const long long tsym = (long long)d.T * d.max_sym;
 
@@ -320,32 +395,44 @@ __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
     if (!grid_sync(d)) return;
     int ne = __ldcg(d.cnt + 1);
     if (ne > 0) {
-        phase_lstm(d, d.em, d.emk, ne, As, Ws, Os);
+        phase_lstm(d, d.em, d.emk, ne, As, Ws, Os, red, rt, &tbar, tphase);
         if (!grid_sync(d)) return;
-        phase_proj(d, d.em, ne, As, Ws);
+        phase_proj(d, d.em, ne, As, Ws, Os, red, rt, &tbar, tphase);
         if (!grid_sync(d)) return;
     }
     for (int it = 1; it <= d.maxit; ++it) {
         const int na = __ldcg(d.cnt + 2 * it);
         if (na == 0) break;
         const int* act = d.act + (it & 1) * d.n;
-        phase_joint(d, act, na, As, Ws, Os);
+        phase_joint(d, act, na, As, Ws, Os, Ps, red, rt, &tbar, tphase);
         if (!grid_sync(d)) return;
         int* nact = d.act + ((it + 1) & 1) * d.n;
         int* em = d.em + (it & 1) * d.n;
         int* emk = d.emk + (it & 1) * d.n;
-        for (int i = gtid; i < na; i += gstride) {
+        // one warp per active slot: first maximum over the slot's partials
+        const int lane = threadIdx.x & 31;
+        for (int i = gtid >> 5; i < na; i += gstride >> 5) {
             const int b = __ldcg(act + i);
             const long long pb = (long long)b * d.nct;
-            float best = __ldcg(d.pval + pb);
-            int k = __ldcg(d.pidx + pb);
-            for (int q = 1; q < d.nct; ++q) {  // tiles in class order: strict > keeps the lowest index
+            float best = -FLT_MAX;
+            int k = INT_MAX;
+            for (int q = lane; q < d.nct; q += 32) {  // tiles in class order: strict > keeps the lowest index
                 const float v = __ldcg(d.pval + pb + q);
                 if (v > best) {
                     best = v;
                     k = __ldcg(d.pidx + pb + q);
                 }
             }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {  // larger value wins, equal values: the lower class
+                const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+                const int ok = __shfl_xor_sync(0xffffffffu, k, o);
+                if (ov > best || (ov == best && ok < k)) {
+                    best = ov;
+                    k = ok;
+                }
+            }
+            if (lane != 0) continue;
             int f = __ldcg(d.frame + b), sy = __ldcg(d.sym + b);
             bool next = k == d.blank;
             if (!next) {
@@ -369,9 +456,9 @@ __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
         if (!grid_sync(d)) return;
         ne = __ldcg(d.cnt + 2 * it + 1);
         if (ne > 0) {
-            phase_lstm(d, em, emk, ne, As, Ws, Os);
+            phase_lstm(d, em, emk, ne, As, Ws, Os, red, rt, &tbar, tphase);
             if (!grid_sync(d)) return;
-            phase_proj(d, em, ne, As, Ws);
+            phase_proj(d, em, ne, As, Ws, Os, red, rt, &tbar, tphase);
             if (!grid_sync(d)) return;
         }
     }
@@ -511,7 +598,7 @@ extern "C" int cac_decoder_create(const cac_dec_config* cfg, const float* weight
         if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return fail(CAC_E_CUDA);
     // one CTA per SM, all co-resident (cooperative launch)
     const int K = (int)(P > J ? P : J);
-    d->smem = sizeof(float) * ((size_t)TS * (K + 4) + (size_t)TN * WLD + (size_t)TS * OLD);
+    d->smem = sizeof(float) * ((size_t)(TS + TN) * (K + 4) + (size_t)TS * OLD + (size_t)TS * (J + 4) + 8 * TS * TN);
     if (d->smem > 227 * 1024) return fail(CAC_E_UNSUPPORTED);
     int dev = 0, sms = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
