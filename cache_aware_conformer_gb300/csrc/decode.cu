@@ -14,11 +14,15 @@
 //   B  decisions: per active slot the first maximum over the partials; blank
 //      (or max_symbols reached) moves the slot to its next frame, anything else
 //      is emitted and queued for the predictor;
-//   C  LSTM step of the queued slots, tiled (32 slots x 16 hidden units = 64
+//   C  LSTM step of the queued slots, tiled (32 slots x 4 hidden units = 16
 //      gate rows): gates = tab[token] + W_hh h, with tab = emb W_ih^T + b_ih +
 //      b_hh computed once at load (the input half of the gates depends on the
 //      token only), then the cell update in the tile;
 //   D  predictor projection p = W_pred h' + b_pred of the queued slots.
+// h is kept twice per stream ([2][S][P]): a queued emission carries the index
+// of the stream's current copy, phase C reads it and writes the new h into
+// the other one, which becomes current (the index flips when the emission is
+// queued, so phase D reads the new copy and nothing is copied back).
 // Grid-wide barriers separate the phases: an arrival counter and a generation
 // word in global memory, every spin bounded (about a second) after which the
 // kernel latches CAC_E_TIMEOUT, raises an abort word that releases every
@@ -51,10 +55,11 @@ struct DecParams {
     const float *tab, *whh, *wpp, *bpp, *wout, *bout;
     float *h, *c, *p;
     int* primed;
-    int *frame, *sym, *act, *em, *emk, *cnt;
+    int *frame, *sym, *act, *emk, *emid, *cnt;  // emid: stream id * 2 + current h copy
     float* pval;
     int* pidx;
-    float* hnext;
+    int* hsel;  // [S] index of the stream's current h copy
+    int S;
     unsigned* bar;  // [0] arrivals, [1] generation
     int* abort_flag;
     int* status;
@@ -143,24 +148,15 @@ __device__ __forceinline__ void mac16(int K, const float* As, const float* Ws, f
 // floats), so one bulk copy per row lands it in shared memory (rows K + 4
 // floats apart) and completes on `bar`.  Sources: A rows from a0[r] into A0
 // and, if a1, from a1[r] into A1 (only when load_a), weight rows wrow(r) into
-// Ws; nullptr rows are zero-filled.  Every thread calls; false when the wait
-// gave up (CAC_E_TIMEOUT latched, abort raised).
+// Ws; nullptr rows are left as they are (their outputs are never used:
+// padding slots are not stored, classes past the last are masked).  Every
+// thread calls; false when the wait gave up (CAC_E_TIMEOUT latched, abort
+// raised).
 template <class WRow>
 __device__ bool stage_tile(const DecParams& d, int K, bool load_a, float* A0, const float* const* a0, float* A1,
                            const float* const* a1, float* Ws, WRow wrow, uint64_t* bar, uint32_t& phase) {
-    const int q4 = K / 4, ld = K + 4, tid = threadIdx.x;
-    if (load_a) {
-        for (int e = tid; e < TS * q4; e += DT) {
-            const int r = e / q4, q = e - r * q4;
-            if (!a0[r]) *reinterpret_cast<float4*>(A0 + r * ld + 4 * q) = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (a1 && !a1[r]) *reinterpret_cast<float4*>(A1 + r * ld + 4 * q) = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    }
-    for (int e = tid; e < TN * q4; e += DT) {
-        const int r = e / q4, q = e - r * q4;
-        if (!wrow(r)) *reinterpret_cast<float4*>(Ws + r * ld + 4 * q) = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    __syncthreads();  // zero fills and every earlier read of these buffers are done
+    const int ld = K + 4, tid = threadIdx.x;
+    __syncthreads();  // every earlier read of these buffers is done
     if (tid < 32) {  // warp 0: lane 0 posts the byte count, the lanes issue one row each
         const uint32_t rb = (uint32_t)K * 4;
         if (tid == 0) {
@@ -198,9 +194,9 @@ struct RowTab {
     const float* aux[TS];  // phase A: the stream's predictor projection p
 };
 
-// Phase C: LSTM step of the queued slots em[0 .. ne) with tokens emk[.]:
+// Phase C: LSTM step of the queued emissions 0 .. ne (token emk[.], stream and h copy emid[.]):
 // tile = (32 slots, 4 hidden units = the 4 x 4 gate rows of those units).
-__device__ void phase_lstm(const DecParams& d, const int* em, const int* emk, int ne, float* As, float* Ws,
+__device__ void phase_lstm(const DecParams& d, const int* emk, const int* emid, int ne, float* As, float* Ws,
                            float* Os, float* red, RowTab& rt, uint64_t* bar, uint32_t& phase) {
     const int P = d.P, tid = threadIdx.x;
     const int ut = P / 4, tiles = ((ne + TS - 1) / TS) * ut;
@@ -214,11 +210,11 @@ __device__ void phase_lstm(const DecParams& d, const int* em, const int* emk, in
                 const int i = st * TS + tid;
                 rt.src[tid] = nullptr;
                 if (i < ne) {
-                    const int b = __ldcg(em + i), id = d.ids[b];
-                    rt.b[tid] = b;
+                    const int e2 = __ldcg(emid + i), id = e2 >> 1, cur = e2 & 1;
                     rt.id[tid] = id;
                     rt.k[tid] = __ldcg(emk + i);
-                    rt.src[tid] = d.h + (long long)id * P;
+                    rt.src[tid] = d.h + ((long long)cur * d.S + id) * P;
+                    rt.aux[tid] = d.h + ((long long)(cur ^ 1) * d.S + id) * P;  // the new h goes to the other copy
                 }
             }
             __syncthreads();
@@ -233,7 +229,7 @@ __device__ void phase_lstm(const DecParams& d, const int* em, const int* emk, in
         if (tid < TS * 4) {  // cell update of (slot r, unit jj)
             const int r = tid >> 2, jj = tid & 3;
             if (rt.src[r]) {
-                const int b = rt.b[r], id = rt.id[r], j = j0 + jj;
+                const int id = rt.id[r], j = j0 + jj;
                 const float* tb = d.tab + (long long)rt.k[r] * 4 * P;
                 const float gi = Os[r * OLD + jj] + __ldg(tb + j);
                 const float gf = Os[r * OLD + 4 + jj] + __ldg(tb + P + j);
@@ -242,15 +238,15 @@ __device__ void phase_lstm(const DecParams& d, const int* em, const int* emk, in
                 float* cp = d.c + (long long)id * P + j;
                 const float c2 = sigm(gf) * __ldcg(cp) + sigm(gi) * tanhf(gg);
                 *cp = c2;
-                d.hnext[(long long)b * P + j] = sigm(go) * tanhf(c2);
+                const_cast<float*>(rt.aux[r])[j] = sigm(go) * tanhf(c2);
             }
         }
         __syncthreads();  // Ws, Os and the row table are reused by the next tile
     }
 }
 
-// Phase D: p = W_pred h' + b_pred for the queued slots, and h <- h'.
-__device__ void phase_proj(const DecParams& d, const int* em, int ne, float* As, float* Ws, float* Os,
+// Phase D: p = W_pred h' + b_pred for the queued slots.
+__device__ void phase_proj(const DecParams& d, const int* emid, int ne, float* As, float* Ws, float* Os,
                            float* red, RowTab& rt, uint64_t* bar, uint32_t& phase) {
     const int P = d.P, J = d.J, tid = threadIdx.x;
     const int jt = J / TN, tiles = ((ne + TS - 1) / TS) * jt;
@@ -264,10 +260,9 @@ __device__ void phase_proj(const DecParams& d, const int* em, int ne, float* As,
                 const int i = st * TS + tid;
                 rt.src[tid] = nullptr;
                 if (i < ne) {
-                    const int b = __ldcg(em + i);
-                    rt.b[tid] = b;
-                    rt.id[tid] = d.ids[b];
-                    rt.src[tid] = d.hnext + (long long)b * P;
+                    const int e2 = __ldcg(emid + i), id = e2 >> 1;
+                    rt.id[tid] = id;
+                    rt.src[tid] = d.h + ((long long)((e2 & 1) ^ 1) * d.S + id) * P;  // the new h
                 }
             }
             __syncthreads();
@@ -276,14 +271,6 @@ __device__ void phase_proj(const DecParams& d, const int* em, int ne, float* As,
         if (!stage_tile(d, P, load_a, As, rt.src, nullptr, nullptr, Ws,
                         [&](int r) -> const float* { return d.wpp + (long long)(c0 + r) * P; }, bar, phase))
             return;
-        if (c0 == 0) {  // the first column tile of each slot tile commits h <- h'
-            for (int e = tid; e < TS * P / 4; e += DT) {
-                const int r = e / (P / 4), q = e % (P / 4);
-                if (rt.src[r])
-                    reinterpret_cast<float4*>(d.h + (long long)rt.id[r] * P)[q] =
-                        *reinterpret_cast<const float4*>(As + r * (P + 4) + 4 * q);
-            }
-        }
         mac16(P, As, Ws, Os, red);
         __syncthreads();
         for (int e = tid; e < TS * TN; e += DT) {
@@ -354,7 +341,7 @@ __device__ void phase_joint(const DecParams& d, const int* act, int na, float* A
 
 // The whole step (see the top of the file).  Iteration it reads the active
 // list act[it & 1] (length cnt[2 it]) and writes the next one act[(it + 1) & 1]
-// (length cnt[2 it + 2]) and its emissions em/emk[it & 1] (length cnt[2 it +
+// (length cnt[2 it + 2]) and its emissions emk/emid[it & 1] (length cnt[2 it +
 // 1]); iteration 0 only builds the first active list and primes reset streams.
 __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
     extern __shared__ float smem[];
@@ -382,22 +369,24 @@ __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
         d.counts[b] = 0;
         if (d.T > 0) d.act[d.n + atomicAdd(&d.cnt[2], 1)] = b;
         if (__ldcg(d.primed + id) == 0) {  // stream start: zero state, one predictor step on blank
+            const int cur = __ldcg(d.hsel + id);
             for (int j = 0; j < d.P; ++j) {
-                d.h[(long long)id * d.P + j] = 0.f;
+                d.h[((long long)cur * d.S + id) * d.P + j] = 0.f;
                 d.c[(long long)id * d.P + j] = 0.f;
             }
             d.primed[id] = 1;
+            d.hsel[id] = cur ^ 1;
             const int q = atomicAdd(&d.cnt[1], 1);
-            d.em[q] = b;
             d.emk[q] = d.blank;
+            d.emid[q] = id * 2 + cur;
         }
     }
     if (!grid_sync(d)) return;
     int ne = __ldcg(d.cnt + 1);
     if (ne > 0) {
-        phase_lstm(d, d.em, d.emk, ne, As, Ws, Os, red, rt, &tbar, tphase);
+        phase_lstm(d, d.emk, d.emid, ne, As, Ws, Os, red, rt, &tbar, tphase);
         if (!grid_sync(d)) return;
-        phase_proj(d, d.em, ne, As, Ws, Os, red, rt, &tbar, tphase);
+        phase_proj(d, d.emid, ne, As, Ws, Os, red, rt, &tbar, tphase);
         if (!grid_sync(d)) return;
     }
     for (int it = 1; it <= d.maxit; ++it) {
@@ -407,8 +396,8 @@ __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
         phase_joint(d, act, na, As, Ws, Os, Ps, red, rt, &tbar, tphase);
         if (!grid_sync(d)) return;
         int* nact = d.act + ((it + 1) & 1) * d.n;
-        int* em = d.em + (it & 1) * d.n;
         int* emk = d.emk + (it & 1) * d.n;
+        int* emid = d.emid + (it & 1) * d.n;
         // one warp per active slot: first maximum over the slot's partials
         const int lane = threadIdx.x & 31;
         for (int i = gtid >> 5; i < na; i += gstride >> 5) {
@@ -441,8 +430,10 @@ __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
                 d.frames[b * tsym + cn] = f;
                 d.counts[b] = cn + 1;
                 const int q = atomicAdd(&d.cnt[2 * it + 1], 1);
-                em[q] = b;
+                const int id = d.ids[b], cur = __ldcg(d.hsel + id);
+                d.hsel[id] = cur ^ 1;
                 emk[q] = k;
+                emid[q] = id * 2 + cur;
                 next = ++sy == d.max_sym;
             }
             if (next) {
@@ -456,9 +447,9 @@ __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
         if (!grid_sync(d)) return;
         ne = __ldcg(d.cnt + 2 * it + 1);
         if (ne > 0) {
-            phase_lstm(d, em, emk, ne, As, Ws, Os, red, rt, &tbar, tphase);
+            phase_lstm(d, emk, emid, ne, As, Ws, Os, red, rt, &tbar, tphase);
             if (!grid_sync(d)) return;
-            phase_proj(d, em, ne, As, Ws, Os, red, rt, &tbar, tphase);
+            phase_proj(d, emid, ne, As, Ws, Os, red, rt, &tbar, tphase);
             if (!grid_sync(d)) return;
         }
     }
@@ -497,12 +488,12 @@ struct cac_decoder {
     float *h = nullptr, *c = nullptr, *p = nullptr;
     int* primed = nullptr;
     // step scratch for up to S slots
-    int *ids = nullptr, *frame = nullptr, *sym = nullptr, *act = nullptr, *em = nullptr, *emk = nullptr;
+    int *ids = nullptr, *frame = nullptr, *sym = nullptr, *act = nullptr, *emk = nullptr, *emid = nullptr;
     int* cnt = nullptr;  // [2 (maxit + 2)] iteration counters, then arrivals / generation / abort
     int cnt_ints = 0;
     float* pval = nullptr;
     int* pidx = nullptr;
-    float* hnext = nullptr;
+    int* hsel = nullptr;  // [S]
     int* status = nullptr;
     int* pinned = nullptr;  // ID_SLOTS x S host ids
     cudaEvent_t slot_ev[ID_SLOTS] = {};
@@ -579,17 +570,17 @@ extern "C" int cac_decoder_create(const cac_dec_config* cfg, const float* weight
         if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) return fail(CAC_E_CUDA);
     }
     const size_t S = max_streams;
-    if ((r = dalloc_t(d, S * P, &d->h)) || (r = dalloc_t(d, S * P, &d->c)) || (r = dalloc_t(d, S * J, &d->p)) ||
+    if ((r = dalloc_t(d, 2 * S * P, &d->h)) || (r = dalloc_t(d, S, &d->hsel)) || (r = dalloc_t(d, S * P, &d->c)) || (r = dalloc_t(d, S * J, &d->p)) ||
         (r = dalloc_t(d, S, &d->primed)) || (r = dalloc_t(d, S, &d->ids)) || (r = dalloc_t(d, S, &d->frame)) ||
-        (r = dalloc_t(d, S, &d->sym)) || (r = dalloc_t(d, 2 * S, &d->act)) || (r = dalloc_t(d, 2 * S, &d->em)) ||
+        (r = dalloc_t(d, S, &d->sym)) || (r = dalloc_t(d, 2 * S, &d->act)) || (r = dalloc_t(d, 2 * S, &d->emid)) ||
         (r = dalloc_t(d, 2 * S, &d->emk)) || (r = dalloc_t(d, S * d->nct, &d->pval)) ||
-        (r = dalloc_t(d, S * d->nct, &d->pidx)) || (r = dalloc_t(d, S * P, &d->hnext)) ||
+        (r = dalloc_t(d, S * d->nct, &d->pidx)) ||
         (r = dalloc_t(d, 1, &d->status)))
         return fail(r);
     d->cnt_ints = 2 * (maxit_for(*cfg, MAX_T) + 2) + 4;
     if ((r = dalloc_t(d, d->cnt_ints, &d->cnt))) return fail(r);
     if (cudaMemset(d->primed, 0, S * 4) != cudaSuccess || cudaMemset(d->status, 0, 4) != cudaSuccess ||
-        cudaMemset(d->h, 0, S * P * 4) != cudaSuccess || cudaMemset(d->c, 0, S * P * 4) != cudaSuccess ||
+        cudaMemset(d->h, 0, 2 * S * P * 4) != cudaSuccess || cudaMemset(d->hsel, 0, S * 4) != cudaSuccess || cudaMemset(d->c, 0, S * P * 4) != cudaSuccess ||
         cudaMemset(d->p, 0, S * J * 4) != cudaSuccess)
         return fail(CAC_E_CUDA);
     if (cudaMallocHost(reinterpret_cast<void**>(&d->pinned), sizeof(int) * S * ID_SLOTS) != cudaSuccess)
@@ -678,9 +669,9 @@ extern "C" int cac_decoder_step(cac_decoder* d, int n, const int* ids, const flo
     p.blank = d->cfg.vocab; p.nct = d->nct; p.maxit = maxit;
     p.ids = d->ids; p.z = z; p.zb = z_bstride; p.tokens = tokens; p.frames = frames; p.counts = counts;
     p.tab = d->tab; p.whh = d->whh; p.wpp = d->wpp; p.bpp = d->bpp; p.wout = d->wout; p.bout = d->bout;
-    p.h = d->h; p.c = d->c; p.p = d->p; p.primed = d->primed;
-    p.frame = d->frame; p.sym = d->sym; p.act = d->act; p.em = d->em; p.emk = d->emk; p.cnt = d->cnt;
-    p.pval = d->pval; p.pidx = d->pidx; p.hnext = d->hnext;
+    p.h = d->h; p.c = d->c; p.p = d->p; p.primed = d->primed; p.hsel = d->hsel; p.S = d->S;
+    p.frame = d->frame; p.sym = d->sym; p.act = d->act; p.emk = d->emk; p.emid = d->emid; p.cnt = d->cnt;
+    p.pval = d->pval; p.pidx = d->pidx;
     p.bar = reinterpret_cast<unsigned*>(d->cnt + nc);
     p.abort_flag = d->cnt + nc + 2;
     p.status = d->status;
@@ -710,7 +701,9 @@ extern "C" int cac_decoder_get_state(cac_decoder* d, int id, float* h, float* c,
     if (!d || id < 0 || id >= d->S) return CAC_E_INVAL;
     const size_t P = d->cfg.pred_dim, J = d->cfg.joint_dim;
     if (cudaDeviceSynchronize() != cudaSuccess) return CAC_E_CUDA;
-    if ((h && cudaMemcpy(h, d->h + id * P, P * 4, cudaMemcpyDeviceToHost) != cudaSuccess) ||
+    int sel = 0;
+    if (cudaMemcpy(&sel, d->hsel + id, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return CAC_E_CUDA;
+    if ((h && cudaMemcpy(h, d->h + ((size_t)sel * d->S + id) * P, P * 4, cudaMemcpyDeviceToHost) != cudaSuccess) ||
         (c && cudaMemcpy(c, d->c + id * P, P * 4, cudaMemcpyDeviceToHost) != cudaSuccess) ||
         (p && cudaMemcpy(p, d->p + id * J, J * 4, cudaMemcpyDeviceToHost) != cudaSuccess) ||
         (primed && cudaMemcpy(primed, d->primed + id, 4, cudaMemcpyDeviceToHost) != cudaSuccess))
