@@ -471,6 +471,22 @@ __global__ void dec_reset_kernel(const int* ids, int n, int* primed) {
     if (i < n) primed[ids[i]] = 0;
 }
 
+// Failure-path self-test kernels (cac_op_wait_selftest): the production waits
+// with nothing that satisfies them.
+__global__ void wait_selftest_mbar_kernel(int* status) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        if (!mbar_wait(&bar, 0)) latch_error(status, CAC_E_TIMEOUT);  // no thread ever arrives
+    }
+}
+
+__global__ void wait_selftest_grid_kernel(DecParams d) {
+    if (blockIdx.x == 0) return;  // the first block never reaches the barrier
+    grid_sync(d);
+}
+
 constexpr int ID_SLOTS = 4;
 constexpr int MAX_T = 1024;
 
@@ -709,4 +725,43 @@ extern "C" int cac_decoder_get_state(cac_decoder* d, int id, float* h, float* c,
         (primed && cudaMemcpy(primed, d->primed + id, 4, cudaMemcpyDeviceToHost) != cudaSuccess))
         return CAC_E_CUDA;
     return CAC_OK;
+}
+
+extern "C" int cac_op_wait_selftest(int which, void* stream) {
+    if (which != 0 && which != 1) return CAC_E_INVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int* buf = nullptr;  // [0] status, [1] abort, [2..3] barrier words
+    if (cudaMalloc(&buf, 4 * sizeof(int)) != cudaSuccess) return CAC_E_NOMEM;
+    int rc = CAC_E_CUDA;
+    if (cudaMemsetAsync(buf, 0, 4 * sizeof(int), s) == cudaSuccess) {
+        cudaError_t e;
+        if (which == 0) {
+            wait_selftest_mbar_kernel<<<1, 32, 0, s>>>(buf);
+            e = cudaGetLastError();
+        } else {
+            int dev = 0, sms = 0;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            DecParams p{};
+            p.status = buf;
+            p.abort_flag = buf + 1;
+            p.bar = reinterpret_cast<unsigned*>(buf + 2);
+            cudaLaunchConfig_t lc = {};
+            lc.gridDim = dim3(sms > 1 ? sms : 2);
+            lc.blockDim = dim3(DT);
+            lc.stream = s;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeCooperative;
+            at[0].val.cooperative = 1;
+            lc.attrs = at;
+            lc.numAttrs = 1;
+            e = cudaLaunchKernelEx(&lc, wait_selftest_grid_kernel, p);
+        }
+        int st = 0;
+        if (e == cudaSuccess && cudaStreamSynchronize(s) == cudaSuccess &&
+            cudaMemcpy(&st, buf, sizeof(int), cudaMemcpyDeviceToHost) == cudaSuccess)
+            rc = st;
+    }
+    cudaFree(buf);
+    return rc;
 }

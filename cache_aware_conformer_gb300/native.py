@@ -32,7 +32,8 @@ SYMBOLS = ["cac_weights_size", "cac_model_create", "cac_model_destroy", "cac_poo
            "cac_op_gemm_bf16", "cac_encode_offline_noalloc",
            # include/cac_decode.h
            "cac_decoder_create", "cac_decoder_destroy", "cac_decoder_reset", "cac_decoder_step",
-           "cac_decoder_check", "cac_decoder_get_state"]
+           "cac_decoder_check", "cac_decoder_get_state",
+           "cac_op_wait_selftest"]
 
 
 class CacError(RuntimeError):
@@ -102,6 +103,7 @@ def _lib():
             "cac_decoder_step": (c_int, [vp, c_int, ip, vp, c_longlong, c_int, vp, vp, vp, vp]),
             "cac_decoder_check": (c_int, [vp]),
             "cac_decoder_get_state": (c_int, [vp, c_int, fp, fp, fp, ip]),
+            "cac_op_wait_selftest": (c_int, [c_int, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -363,6 +365,12 @@ class Pool:
         _check(_lib().cac_pool_read_trace(self.h, layer, tap, out.ctypes.data_as(POINTER(c_float)), out.size),
                "cac_pool_read_trace")
         return out
+
+
+def wait_selftest(which: int, stream=None) -> int:
+    """Status latched by a bounded device wait that nothing satisfies
+    (cac_op_wait_selftest): CAC_E_TIMEOUT (-8) when the wait gave up."""
+    return int(_lib().cac_op_wait_selftest(int(which), _stream(stream)))
 
 
 class Decoder:

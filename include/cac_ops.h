@@ -27,6 +27,18 @@ extern "C" {
 int cac_op_gemm_bf16(int M, int N, int K, const void* A, const void* B, const float* bias, float* C, int splits,
                      int a_split, void* stream);
 
+/* Failure-path self-test of the library's bounded device waits: runs the
+ * wait the library uses with nothing that can satisfy it and returns the
+ * status the device latched — CAC_E_TIMEOUT when the wait gave up as designed.
+ *   which 0: an mbarrier wait (the TMA / tensor-core pipelines' wait) on a
+ *            barrier no thread arrives at; gives up after about 2 s;
+ *   which 1: the decoder's grid-wide barrier in a cooperative launch whose
+ *            first block never arrives; the others give up after about 1 s,
+ *            raise the abort word and return.
+ * Synchronous; the kernels exit normally, so the context stays usable.
+ * CAC_E_INVAL for another `which`, CAC_E_CUDA if a launch failed. */
+int cac_op_wait_selftest(int which, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -192,3 +192,15 @@ def test_degenerate_calls():
             dec.step(bad, zz)
     dec.check()
     dec.close()
+
+
+def test_bounded_waits_give_up_and_context_survives():
+    """Failure detection without a GPU fault: the library's mbarrier wait and
+    the decoder's grid barrier, given nothing that satisfies them, give up
+    after their limits and latch CAC_E_TIMEOUT; the context keeps working."""
+    native = _native()
+    assert native.wait_selftest(0) == -8   # CAC_E_TIMEOUT
+    assert native.wait_selftest(1) == -8
+    assert native.wait_selftest(2) == -1   # CAC_E_INVAL
+    em, nd, ties, live = _run(TINY_DECODER, 2, 6, 2)
+    assert live + ties == 2
