@@ -842,6 +842,7 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
             ep.D = D; ep.nq = n; ep.ids = ids; ep.pos = p->pos;
             ep.dw_ring = conv_l; ep.dw_sstride = p->conv_sstride;
             ep.dw_wT = Lw.dwT; ep.dw_bias = Lw.bdw; ep.dw_gamma = Lw.bng; ep.dw_beta = Lw.bnb; ep.dw_out = p->yc;
+            ep.dw_rows = M;
         }
         PB(P_PW1);
         RET(gemm(m, p->xln, ldl, M, D, Lw.pw1, 0, ep, s, lc, sp));

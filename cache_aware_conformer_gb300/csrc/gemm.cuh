@@ -72,6 +72,7 @@ struct EpiParams {
     const float* dw_gamma = nullptr;
     const float* dw_beta = nullptr;
     void* dw_out = nullptr;
+    int dw_rows = 0;                // rows of the GEMM (M): rows past it have no stream
     // LayerNorm folded into this GEMM (EPI_STORE / EPI_GLU / EPI_QKV / EPI_GLUDW):
     // A is the split operand of gamma * x (x the residual rows), bias = b + W beta
     // and ln_colsum[n] = sum_k gamma_k W[n][k], so that LN(x) W^T + b =
@@ -241,6 +242,7 @@ struct EpiPre {
     float4 x[8];
     float4 g[8];  // EPI_RESID with xs: the next LayerNorm's gain
     float ln_mean, ln_rstd;
+    int dw_id, dw_p0;  // EPI_GLUDW: the row's stream id and position of its first new frame
 };
 
 // mean and 1/sqrt(var + 1e-5) of a row from its partials (sum_j, M2_j) over 32
@@ -303,6 +305,14 @@ __device__ __forceinline__ void epi_prefetch(const EpiParams& e, int row, int co
         pre.ln_rstd = 1.f;
         if (e.ln_stats && row < e.ln_rows)
             ln_row_stats(e.ln_stats + (long long)row * e.ln_parts, e.ln_parts, pre.ln_mean, pre.ln_rstd);
+        if constexpr (KIND == EPI_GLUDW) {
+            pre.dw_id = 0;
+            pre.dw_p0 = 0;
+            if (row < e.dw_rows) {
+                pre.dw_id = e.ids[row / e.nq];
+                pre.dw_p0 = e.pos[pre.dw_id];
+            }
+        }
     }
 }
 
@@ -440,12 +450,8 @@ __device__ __forceinline__ void epilogue_gludw(const EpiParams& e, int row, bool
     float g[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) g[i] = __bfloat162float(__float2bfloat16_rn(v[i] * sigmoidf_(v[16 + i])));
-    const int fi = row % nq, b = row / nq;
-    int id = 0, p0 = 0;
-    if (live) {
-        id = e.ids[b];
-        p0 = e.pos[id];
-    }
+    const int fi = row % nq;
+    const int id = live ? pre.dw_id : 0, p0 = live ? pre.dw_p0 : 0;  // loaded ahead (epi_prefetch)
     bf16* ring = static_cast<bf16*>(e.dw_ring) + (long long)id * e.dw_sstride;
     float acc[16];
     {
@@ -456,45 +462,63 @@ __device__ __forceinline__ void epilogue_gludw(const EpiParams& e, int row, bool
             acc[4 * q] = t.x; acc[4 * q + 1] = t.y; acc[4 * q + 2] = t.z; acc[4 * q + 3] = t.w;
         }
     }
+    // taps k = 0 .. 7 (d = 8 - k frames back): this step's earlier rows by
+    // shuffle, older frames from the conv ring (slot = frame mod 8, zero before
+    // the stream start); the ring rows of four taps are loaded before any is used
+    constexpr int TB = 4;  // taps whose ring rows are in flight together
 #pragma unroll
-    for (int k = 0; k < 9; ++k) {
-        const int d = 8 - k;  // frames back from this row's frame
-        float win[16];
-        if (d == 0) {
+    for (int k0 = 0; k0 < 8; k0 += TB) {
+        uint4 r[TB][2];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) win[i] = g[i];
-        } else {
-            // this step's rows (d <= fi): lane - d holds frame fi - d of the same stream
-            float sh[16];
+        for (int j = 0; j < TB; ++j) {
+            const int d = 8 - (k0 + j), pabs = p0 + fi - d;
+            if (d > fi && live && pabs >= 0) {
+                const uint4* src = reinterpret_cast<const uint4*>(ring + (long long)(pabs & 7) * D + C);
+                r[j][0] = src[0];
+                r[j][1] = src[1];
+            } else {
+                r[j][0] = make_uint4(0u, 0u, 0u, 0u);  // bf16 zeros
+                r[j][1] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < TB; ++j) {
+            const int k = k0 + j, d = 8 - k;
+            float sh[16], win[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) sh[i] = d < nq ? __shfl_sync(0xffffffffu, g[i], (lane - d) & 31) : 0.f;
-            const int pabs = p0 + fi - d;
             if (d <= fi) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) win[i] = sh[i];
-            } else if (live && pabs >= 0) {
-                const uint4* src = reinterpret_cast<const uint4*>(ring + (long long)(pabs & 7) * D + C);
-                const uint4 r0 = src[0], r1 = src[1];
-                const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&r0);
-                const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&r1);
+            } else {
+                const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&r[j][0]);
+                const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&r[j][1]);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float2 a0 = __bfloat1622float2(h0[i]), a1 = __bfloat1622float2(h1[i]);
                     win[2 * i] = a0.x; win[2 * i + 1] = a0.y; win[8 + 2 * i] = a1.x; win[8 + 2 * i + 1] = a1.y;
                 }
-            } else {
+            }
+            const float4* w4 = reinterpret_cast<const float4*>(e.dw_wT + (long long)k * D + C);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) win[i] = 0.f;
+            for (int q = 0; q < 4; ++q) {
+                const float4 w = __ldg(w4 + q);
+                acc[4 * q] = fmaf(w.x, win[4 * q], acc[4 * q]);
+                acc[4 * q + 1] = fmaf(w.y, win[4 * q + 1], acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(w.z, win[4 * q + 2], acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(w.w, win[4 * q + 3], acc[4 * q + 3]);
             }
         }
-        const float4* w4 = reinterpret_cast<const float4*>(e.dw_wT + (long long)k * D + C);
+    }
+    {   // tap 8 (d = 0): this row's own GLU value
+        const float4* w4 = reinterpret_cast<const float4*>(e.dw_wT + 8LL * D + C);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float4 w = __ldg(w4 + q);
-            acc[4 * q] = fmaf(w.x, win[4 * q], acc[4 * q]);
-            acc[4 * q + 1] = fmaf(w.y, win[4 * q + 1], acc[4 * q + 1]);
-            acc[4 * q + 2] = fmaf(w.z, win[4 * q + 2], acc[4 * q + 2]);
-            acc[4 * q + 3] = fmaf(w.w, win[4 * q + 3], acc[4 * q + 3]);
+            acc[4 * q] = fmaf(w.x, g[4 * q], acc[4 * q]);
+            acc[4 * q + 1] = fmaf(w.y, g[4 * q + 1], acc[4 * q + 1]);
+            acc[4 * q + 2] = fmaf(w.z, g[4 * q + 2], acc[4 * q + 2]);
+            acc[4 * q + 3] = fmaf(w.w, g[4 * q + 3], acc[4 * q + 3]);
         }
     }
     __syncwarp();  // every lane has read the ring before this step's rows are committed
