@@ -245,10 +245,10 @@ NCU_TRAFFIC = {
                   {"csrc/attn_mma.cu": "3534d37c9941a64e9b10378c760396808ea05e4fc2a37903792d882c2631931f",
                    "csrc/common.cuh": "a878ff38ad1c5afea1ea1f7c7258291545de59eb566da1388d9503ba322103c3"}),
     "gemm_ff_down": (5.27488e6, {"csrc/gemm_tc.cu": "1834a8cf10007e4e3cfb3a995f936576ea82c0c21964e8a464a6004509692216",
-                                 "csrc/gemm.cuh": "54c881bbe94753edf718d540af96d006efc5b91b1357159f9b0e3f2c50062cde",
+                                 "csrc/gemm.cuh": "d09c5741b881ba8356934895342ebca8b0040bb104e88f6554e96eba4455fb11",
                                  "csrc/common.cuh": "a878ff38ad1c5afea1ea1f7c7258291545de59eb566da1388d9503ba322103c3"}),
-    "gemm_ff_up": (3.192576e6, {"csrc/gemm_tc.cu": "1834a8cf10007e4e3cfb3a995f936576ea82c0c21964e8a464a6004509692216",
-                                "csrc/gemm.cuh": "54c881bbe94753edf718d540af96d006efc5b91b1357159f9b0e3f2c50062cde",
+    "gemm_ff_up": (3.192832e6, {"csrc/gemm_tc.cu": "1834a8cf10007e4e3cfb3a995f936576ea82c0c21964e8a464a6004509692216",
+                                "csrc/gemm.cuh": "d09c5741b881ba8356934895342ebca8b0040bb104e88f6554e96eba4455fb11",
                                 "csrc/common.cuh": "a878ff38ad1c5afea1ea1f7c7258291545de59eb566da1388d9503ba322103c3"}),
 }
 
