@@ -534,6 +534,16 @@ int dalloc_t(cac_decoder* d, size_t count, T** out) {
 
 int maxit_for(const cac_dec_config& c, int T) { return T * (c.max_symbols + 1) + 1; }
 
+// free one allocation of d early (it leaves d's list, so destroy does not free it again)
+void dfree(cac_decoder* d, void* p) {
+    for (auto it = d->allocs.begin(); it != d->allocs.end(); ++it)
+        if (*it == p) {
+            cudaFree(p);
+            d->allocs.erase(it);
+            return;
+        }
+}
+
 }  // namespace
 
 extern "C" void cac_decoder_destroy(cac_decoder* d) {
@@ -584,9 +594,14 @@ extern "C" int cac_decoder_create(const cac_dec_config* cfg, const float* weight
         const long long nt = (long long)C * 4 * P;
         dec_tab_kernel<<<(unsigned)((nt + 255) / 256), 256>>>(emb_d, wih_d, bih_d, bhh_d, d->tab, (int)C, (int)P);
         if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) return fail(CAC_E_CUDA);
+        // the embedding and the input weights live on only inside tab
+        for (void* t : {static_cast<void*>(emb_d), static_cast<void*>(wih_d), static_cast<void*>(bih_d),
+                        static_cast<void*>(bhh_d)})
+            dfree(d, t);
     }
     const size_t S = max_streams;
-    if ((r = dalloc_t(d, 2 * S * P, &d->h)) || (r = dalloc_t(d, S, &d->hsel)) || (r = dalloc_t(d, S * P, &d->c)) || (r = dalloc_t(d, S * J, &d->p)) ||
+    if ((r = dalloc_t(d, 2 * S * P, &d->h)) || (r = dalloc_t(d, S, &d->hsel)) || (r = dalloc_t(d, S * P, &d->c)) ||
+        (r = dalloc_t(d, S * J, &d->p)) ||
         (r = dalloc_t(d, S, &d->primed)) || (r = dalloc_t(d, S, &d->ids)) || (r = dalloc_t(d, S, &d->frame)) ||
         (r = dalloc_t(d, S, &d->sym)) || (r = dalloc_t(d, 2 * S, &d->act)) || (r = dalloc_t(d, 2 * S, &d->emid)) ||
         (r = dalloc_t(d, 2 * S, &d->emk)) || (r = dalloc_t(d, S * d->nct, &d->pval)) ||
@@ -616,14 +631,6 @@ extern "C" int cac_decoder_create(const cac_dec_config* cfg, const float* weight
         return fail(CAC_E_CUDA);
     if (per_sm < 1) return fail(CAC_E_UNSUPPORTED);
     d->grid = sms;
-    cudaFree(emb_d);
-    cudaFree(wih_d);
-    cudaFree(bih_d);
-    cudaFree(bhh_d);
-    for (void* a : {static_cast<void*>(emb_d), static_cast<void*>(wih_d), static_cast<void*>(bih_d),
-                    static_cast<void*>(bhh_d)})
-        for (auto& x : d->allocs)
-            if (x == a) x = nullptr;
     *out = d;
     return CAC_OK;
 }
@@ -740,8 +747,9 @@ extern "C" int cac_op_wait_selftest(int which, void* stream) {
             e = cudaGetLastError();
         } else {
             int dev = 0, sms = 0;
-            cudaGetDevice(&dev);
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (cudaGetDevice(&dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                sms = 2;
             DecParams p{};
             p.status = buf;
             p.abort_flag = buf + 1;

@@ -64,7 +64,9 @@ int cac_decoder_reset(cac_decoder* d, int n, const int* ids, void* stream);
  * reset streams.  T <= 1024.
  * Entries of tokens/frames past counts[b] are left unchanged.  Pointers must be
  * 4-byte aligned, z 16-byte aligned with z_bstride a multiple of 4.
- * Asynchronous on `stream`; the per-stream state is updated on the device. */
+ * Asynchronous on `stream`; the per-stream state is updated on the device.
+ * Calls on one decoder (step and reset) share its device scratch and pinned
+ * id slots: issue them on one CUDA stream, or order them across streams. */
 int cac_decoder_step(cac_decoder* d, int n, const int* ids, const float* z, long long z_bstride, int T,
                      int* tokens, int* frames, int* counts, void* stream);
 
