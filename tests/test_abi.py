@@ -55,3 +55,18 @@ def test_invalid_config_has_no_size(native):
     from dataclasses import replace
     assert native.weights_size(replace(TINY, n_heads=3)) == 0       # d_model % n_heads != 0
     assert native.lib().cac_strerror(-2).decode().startswith("push not aligned")
+
+
+def test_decoder_blob_layout_matches_the_header():
+    """include/cac_decode.h: emb [C][P], w_ih, w_hh [4P][P], b_ih, b_hh [4P],
+    pred.w [J][P], pred.b [J], out.w [C][J], out.b [C]; C = vocab + 2."""
+    from cache_aware_conformer_gb300.config import EOU_DECODER, TINY_DECODER
+    for dc in (TINY_DECODER, EOU_DECODER):
+        C, P, J = dc.vocab + 2, dc.pred_dim, dc.joint_dim
+        names = [n for n, _, _ in synth.decoder_layout(dc)]
+        assert names == ["emb", "lstm.w_ih", "lstm.w_hh", "lstm.b_ih", "lstm.b_hh", "pred.w", "pred.b",
+                         "out.w", "out.b"]
+        blob = synth.pack_decoder_weights(dc, synth.make_decoder_weights(dc, 0))
+        assert blob.size == C * P + 2 * 4 * P * P + 2 * 4 * P + J * P + J + C * J + C
+        assert (dc.blank, dc.eou, dc.classes) == (dc.vocab, dc.vocab + 1, C)
+        assert P % 64 == 0 and J % 64 == 0  # the kernel's tiling rule (CAC_E_UNSUPPORTED otherwise)
