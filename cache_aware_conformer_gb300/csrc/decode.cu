@@ -9,7 +9,7 @@
 // persistent kernel (one 256-thread CTA per SM).  The streams advance in
 // lockstep iterations; each iteration is
 //   A  joint + argmax: logits of every still-active slot at its current frame,
-//      tiled (32 slots x 64 classes) over the CTAs, K = joint_dim, written as
+//      tiled (32 slots x 16 classes) over the CTAs, K = joint_dim, written as
 //      per-tile partial maxima;
 //   B  decisions: per active slot the first maximum over the partials; blank
 //      (or max_symbols reached) moves the slot to its next frame, anything else
@@ -18,7 +18,11 @@
 //      gate rows): gates = tab[token] + W_hh h, with tab = emb W_ih^T + b_ih +
 //      b_hh computed once at load (the input half of the gates depends on the
 //      token only), then the cell update in the tile;
-//   D  predictor projection p = W_pred h' + b_pred of the queued slots.
+//   D  predictor projection p = W_pred h' + b_pred of the queued slots, tiled
+//      (32 slots x 16 outputs).
+// Every tile stages its rows (weights, and slot rows when its slot tile
+// changes) with one TMA bulk copy per row; the 8 warps split K and reduce
+// their partial tiles through shared memory.
 // h is kept twice per stream ([2][S][P]): a queued emission carries the index
 // of the stream's current copy, phase C reads it and writes the new h into
 // the other one, which becomes current (the index flips when the emission is
