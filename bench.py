@@ -540,7 +540,12 @@ def run_ours(args, wl):
            "d2h_bytes_per_step": w.S * w.n * (w.cfg.d_model + w.cfg.joint_dim) * 4}
     w.pool.check()
 
-    decode = measure_decode(w, Kd, dev, clk) if Kd else None
+    decode = None
+    if Kd:
+        try:
+            decode = measure_decode(w, Kd, dev, clk)
+        except Exception as exc:  # the decoder leg is reported beside the encoder, never instead of it
+            decode = {"error": f"{type(exc).__name__}: {exc}"[:300]}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
