@@ -33,7 +33,10 @@ SYMBOLS = ["cac_weights_size", "cac_model_create", "cac_model_destroy", "cac_poo
            # include/cac_decode.h
            "cac_decoder_create", "cac_decoder_destroy", "cac_decoder_reset", "cac_decoder_step",
            "cac_decoder_check", "cac_decoder_get_state",
-           "cac_op_wait_selftest"]
+           "cac_op_wait_selftest",
+           # include/cac_frontend.h
+           "cac_frontend_create", "cac_frontend_destroy", "cac_frontend_reset", "cac_frontend_push",
+           "cac_frontend_flush", "cac_frontend_get_state", "cac_frontend_schedule"]
 
 
 class CacError(RuntimeError):
@@ -104,6 +107,13 @@ def _lib():
             "cac_decoder_check": (c_int, [vp]),
             "cac_decoder_get_state": (c_int, [vp, c_int, fp, fp, fp, ip]),
             "cac_op_wait_selftest": (c_int, [c_int, vp]),
+            "cac_frontend_create": (c_int, [c_int, POINTER(vp)]),
+            "cac_frontend_destroy": (None, [vp]),
+            "cac_frontend_reset": (c_int, [vp, c_int, ip]),
+            "cac_frontend_push": (c_int, [vp, c_int, ip, vp, c_longlong, c_int, vp, c_longlong, c_int, ip, vp]),
+            "cac_frontend_flush": (c_int, [vp, c_int, ip, vp, c_longlong, ip, vp, c_longlong, c_int, ip, vp]),
+            "cac_frontend_get_state": (c_int, [vp, c_int, POINTER(c_longlong), POINTER(c_longlong), ip]),
+            "cac_frontend_schedule": (c_longlong, [c_longlong, c_longlong, c_longlong, c_int]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -431,3 +441,91 @@ class Decoder:
         _check(_lib().cac_decoder_get_state(self.h, sid, h.ctypes.data_as(fp), c.ctypes.data_as(fp),
                                             p.ctypes.data_as(fp), ctypes.byref(primed)), "cac_decoder_get_state")
         return h, c, p, primed.value
+
+
+def frontend_schedule(samples_before: int, frames_before: int, n_samples: int, flush: bool) -> int:
+    """Frames a push (or flush) of n_samples emits (cac_frontend_schedule; host only)."""
+    return int(_lib().cac_frontend_schedule(samples_before, frames_before, n_samples, 1 if flush else 0))
+
+
+class Frontend:
+    """Streaming log-mel front end on the current CUDA device
+    (include/cac_frontend.h): 16 kHz audio -> 128-bin log-mel frames for
+    stream ids 0 .. max_streams-1."""
+
+    N_MELS = 128
+
+    def __init__(self, max_streams: int):
+        h = c_void_p()
+        _check(_lib().cac_frontend_create(max_streams, ctypes.byref(h)), "cac_frontend_create")
+        self.h = h
+        self.max_streams = max_streams
+
+    def close(self):
+        if self.h:
+            _lib().cac_frontend_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def reset(self, ids):
+        _check(_lib().cac_frontend_reset(self.h, len(ids), _ids(ids)), "cac_frontend_reset")
+
+    def _bstride(self, t, n, inner):
+        if t is None:
+            return 0
+        assert t.stride(-1) == 1
+        return t.stride(0) if n > 1 else inner  # a size-1 dimension may carry any stride
+
+    def push_into(self, ids, audio, mel, stream=None):
+        """audio: cuda fp32 [n, samples]; mel: cuda fp32 [n, max_frames, 128]
+        (slots may be strided).  Returns the frames written per slot."""
+        n = len(ids)
+        ns = 0 if audio is None else audio.shape[1]
+        max_frames = mel.shape[1]
+        assert mel.shape[2] == self.N_MELS and (max_frames <= 1 or mel.stride(1) == self.N_MELS)
+        out = (c_int * n)()
+        _check(_lib().cac_frontend_push(self.h, n, _ids(ids), _ptr(audio), self._bstride(audio, n, ns), ns,
+                                        _ptr(mel), self._bstride(mel, n, max_frames * self.N_MELS), max_frames,
+                                        out, _stream(stream)), "cac_frontend_push")
+        return list(out)
+
+    def flush_into(self, ids, audio, n_samples_each, mel, stream=None):
+        """Last samples (audio [n, >= max(n_samples_each)]) and every remaining frame."""
+        n = len(ids)
+        ns = int(max(n_samples_each)) if n else 0
+        max_frames = mel.shape[1]
+        assert mel.shape[2] == self.N_MELS and (max_frames <= 1 or mel.stride(1) == self.N_MELS)
+        out = (c_int * n)()
+        lda = 0 if audio is None else self._bstride(audio, n, audio.shape[1])
+        _check(_lib().cac_frontend_flush(self.h, n, _ids(ids), _ptr(audio), lda, _ids(n_samples_each), _ptr(mel),
+                                         self._bstride(mel, n, max_frames * self.N_MELS), max_frames, out,
+                                         _stream(stream)), "cac_frontend_flush")
+        return list(out)
+
+    def push(self, ids, audio, max_frames=None, flush=False, n_samples_each=None, stream=None):
+        """Frames of one push (or flush) as a list of cuda [frames, 128] tensors."""
+        import torch
+        n = len(ids)
+        ns = 0 if audio is None else audio.shape[1]
+        if max_frames is None:
+            max_frames = ns // 160 + 2
+        mel = torch.empty((n, max(max_frames, 1), self.N_MELS), dtype=torch.float32,
+                          device=audio.device if audio is not None else "cuda")
+        if flush:
+            counts = self.flush_into(ids, audio, n_samples_each if n_samples_each is not None else [ns] * n, mel,
+                                     stream)
+        else:
+            counts = self.push_into(ids, audio, mel, stream)
+        return [mel[b, :counts[b]] for b in range(n)]
+
+    def state(self, sid: int):
+        """(samples received, frames emitted, finished) of one stream."""
+        s, f, fin = c_longlong(0), c_longlong(0), c_int(0)
+        _check(_lib().cac_frontend_get_state(self.h, sid, ctypes.byref(s), ctypes.byref(f), ctypes.byref(fin)),
+               "cac_frontend_get_state")
+        return s.value, f.value, fin.value
