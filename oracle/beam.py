@@ -38,12 +38,17 @@ Readings where the pages are silent (each is listed in the design notes):
     path that the alignment sum would have counted);
   * the final choice maximises score / (non-blank length + 1) when score_norm,
     else the raw score (ties: lower slot);
-  * scores are accumulated in fp32 (the pages fix fp32), log-sum-exp in fp32.
+  * scores are accumulated in fp32 (the pages fix fp32), log-sum-exp in fp32;
+  * streaming (frames in chunks): an iteration that a running hypothesis
+    cannot take because its frame has not arrived waits for the next push,
+    and only the end of the utterance makes hypotheses final, so the chunked
+    search runs the very iterations of the one-shot search.
 
 Parity pins: tests/test_oracle_beam_pins.py (toy-table fixtures of §2.5,
 beam 1 == the greedy decoder of oracle/decoder.py, and with a beam wide enough
 never to prune and a symbol limit that never binds, every final score equals
-the brute-force log-sum-exp over all alignments of its transcript).
+the brute-force log-sum-exp over all alignments of its transcript; chunked
+pushes equal the one-shot search).
 """
 from __future__ import annotations
 
@@ -78,64 +83,114 @@ class Hyp:
             score, time, last, tokens, sym_t, state
 
 
+def initial_beam(scorer, beam, blank):
+    """Slot 0: score 0, empty transcript, last label blank; K - 1 empty slots."""
+    return [Hyp(F32(0.0), 0, blank, (), 0, scorer.init_state())] + [None] * (beam - 1)
+
+
+def malsd_iteration(hyps, scorer, n_frames, blank, max_symbols):
+    """One alignment iteration over the beam `hyps` (K slots, None = empty):
+    candidates, pruning to K, labels applied, recombination.  A hypothesis
+    whose time has reached n_frames is final and offers one keep candidate."""
+    K = len(hyps)
+    cands = []  # (score, parent slot, label or None for "keep"), in candidate-position order
+    for k, h in enumerate(hyps):
+        if h is None:
+            cands += [(NEG, k, None)] * K
+            continue
+        if h.time >= n_frames:  # final: one keep candidate
+            cands += [(h.score, k, None)] + [(NEG, k, None)] * (K - 1)
+            continue
+        lp = np.asarray(scorer.log_probs(h.time, h.state), dtype=F32)
+        if h.sym_t >= max_symbols:  # forced blank
+            cands += [(F32(h.score + lp[blank]), k, blank)] + [(NEG, k, None)] * (K - 1)
+            continue
+        for lab in topk_lowest_index(lp, K):
+            cands.append((F32(h.score + lp[lab]), k, lab))
+    keep = topk_lowest_index([c[0] for c in cands], K)
+    new = []
+    for pos in keep:
+        s, k, lab = cands[pos]
+        h = hyps[k]
+        if not np.isfinite(s):
+            new.append(None)
+        elif lab is None:
+            new.append(Hyp(s, h.time, h.last, h.tokens, h.sym_t, h.state))
+        elif lab == blank:
+            new.append(Hyp(s, h.time + 1, h.last, h.tokens, 0, h.state))
+        else:
+            new.append(Hyp(s, h.time, lab, h.tokens + (lab,), h.sym_t + 1, scorer.advance(h.state, lab)))
+    # recombination of identical survivors (transcript, last label, length)
+    groups = {}
+    for i, h in enumerate(new):
+        if h is not None:
+            groups.setdefault((h.tokens, h.last, len(h.tokens)), []).append(i)
+    for members in groups.values():
+        if len(members) < 2:
+            continue
+        best = min(members, key=lambda i: (-float(new[i].score), i))
+        merged = logsumexp32([new[i].score for i in members])
+        for i in members:
+            if i != best:
+                new[i] = None
+        new[best].score = merged
+    return new
+
+
+def best_hypothesis(hyps, score_norm=True):
+    """Slot of the winner: the highest score, or score / (length + 1) when
+    score_norm; ties to the lower slot."""
+    live = [i for i, h in enumerate(hyps) if h is not None]
+    key = (lambda i: float(hyps[i].score) / (len(hyps[i].tokens) + 1)) if score_norm else \
+        (lambda i: float(hyps[i].score))
+    return min(live, key=lambda i: (-key(i), i))
+
+
+def _finals(hyps):
+    return [(h.tokens, h.score) if h is not None else None for h in hyps]
+
+
 def malsd_beam(n_frames, scorer, beam, blank, max_symbols=10, score_norm=True):
     """Beam search over n_frames with a scorer providing
          init_state(), log_probs(time, state) -> [V+1] fp32 log-probabilities,
          advance(state, label) -> new state.
     Returns (best token tuple, final hypotheses as (tokens, score) per slot)."""
-    K = beam
-    hyps = [Hyp(F32(0.0), 0, blank, (), 0, scorer.init_state())] + [None] * (K - 1)
+    hyps = initial_beam(scorer, beam, blank)
     for _ in range(n_frames * (max_symbols + 1) + 1):
         if not any(h is not None and h.time < n_frames for h in hyps):
             break
-        cands = []  # (score, parent slot, label or None for "keep"), in candidate-position order
-        for k, h in enumerate(hyps):
-            if h is None:
-                cands += [(NEG, k, None)] * K
-                continue
-            if h.time >= n_frames:  # final: one keep candidate
-                cands += [(h.score, k, None)] + [(NEG, k, None)] * (K - 1)
-                continue
-            lp = np.asarray(scorer.log_probs(h.time, h.state), dtype=F32)
-            if h.sym_t >= max_symbols:  # forced blank
-                cands += [(F32(h.score + lp[blank]), k, blank)] + [(NEG, k, None)] * (K - 1)
-                continue
-            for lab in topk_lowest_index(lp, K):
-                cands.append((F32(h.score + lp[lab]), k, lab))
-        keep = topk_lowest_index([c[0] for c in cands], K)
-        new = []
-        for pos in keep:
-            s, k, lab = cands[pos]
-            h = hyps[k]
-            if not np.isfinite(s):
-                new.append(None)
-            elif lab is None:
-                new.append(Hyp(s, h.time, h.last, h.tokens, h.sym_t, h.state))
-            elif lab == blank:
-                new.append(Hyp(s, h.time + 1, h.last, h.tokens, 0, h.state))
-            else:
-                new.append(Hyp(s, h.time, lab, h.tokens + (lab,), h.sym_t + 1, scorer.advance(h.state, lab)))
-        # recombination of identical survivors (transcript, last label, length)
-        groups = {}
-        for i, h in enumerate(new):
-            if h is not None:
-                groups.setdefault((h.tokens, h.last, len(h.tokens)), []).append(i)
-        for members in groups.values():
-            if len(members) < 2:
-                continue
-            best = min(members, key=lambda i: (-float(new[i].score), i))
-            merged = logsumexp32([new[i].score for i in members])
-            for i in members:
-                if i != best:
-                    new[i] = None
-            new[best].score = merged
-        hyps = new
-    finals = [(h.tokens, h.score) if h is not None else None for h in hyps]
-    live = [i for i, h in enumerate(hyps) if h is not None]
-    key = (lambda i: float(hyps[i].score) / (len(hyps[i].tokens) + 1)) if score_norm else \
-        (lambda i: float(hyps[i].score))
-    best = min(live, key=lambda i: (-key(i), i))
-    return hyps[best].tokens, finals
+        hyps = malsd_iteration(hyps, scorer, n_frames, blank, max_symbols)
+    return hyps[best_hypothesis(hyps, score_norm)].tokens, _finals(hyps)
+
+
+class StreamingMalsd:
+    """The same search over frames that arrive in chunks.  Iterations keep
+    every hypothesis at one alignment length, so an iteration whose running
+    hypotheses need a frame that has not arrived waits for the next push;
+    flush() marks the utterance's end (hypotheses at the last frame become
+    final) and finishes.  The result equals malsd_beam over all frames.
+    The scorer is asked only for frames already pushed."""
+
+    def __init__(self, scorer, beam, blank, max_symbols=10, score_norm=True):
+        self.scorer, self.blank, self.max_symbols, self.score_norm = scorer, blank, max_symbols, score_norm
+        self.hyps = initial_beam(scorer, beam, blank)
+        self.available = 0
+        self.iterations = 0
+
+    def _run(self, n_frames):
+        while any(h is not None and h.time < n_frames for h in self.hyps):
+            if any(h is not None and self.available <= h.time < n_frames for h in self.hyps):
+                break  # a running hypothesis needs a frame that has not arrived
+            self.hyps = malsd_iteration(self.hyps, self.scorer, n_frames, self.blank, self.max_symbols)
+            self.iterations += 1
+
+    def push(self, n_new):
+        self.available += n_new
+        self._run(n_frames=1 << 62)  # the end is unknown: nothing is final yet
+
+    def flush(self):
+        self._run(n_frames=self.available)
+        return self.hyps[best_hypothesis(self.hyps, self.score_norm)].tokens, _finals(self.hyps)
 
 
 class TableScorer:

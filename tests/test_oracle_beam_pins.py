@@ -154,3 +154,21 @@ def test_equal_last_label_and_length_alone_do_not_merge():
     got = {tok: float(s) for f in finals if f is not None for tok, s in [f]}
     assert set(got) == {(), (0,), (1,), (0, 1), (1, 1)}
     assert abs(got[(0, 1)] - math.log(0.15)) < 1e-6 and abs(got[(1, 1)] - math.log(0.15)) < 1e-6
+
+
+@pytest.mark.parametrize("chunks", [[16], [2] * 8, [1, 0, 3, 5, 0, 7], [0, 16]])
+def test_streamed_beam_equals_the_whole_utterance(chunks):
+    """Frames pushed in chunks (iterations wait while a running hypothesis
+    needs a frame not yet pushed) give the same beam as all frames at once."""
+    dc = TINY_DECODER
+    W = synth.make_decoder_weights(dc, 0)
+    for s in range(3):
+        z = synth.make_joint_frames(16, 10 + s, dc.joint_dim)
+        best, finals = B.malsd_beam(16, B.PredictorScorer(z, W, dc), beam=4, blank=dc.blank,
+                                    max_symbols=dc.max_symbols)
+        st = B.StreamingMalsd(B.PredictorScorer(z, W, dc), beam=4, blank=dc.blank, max_symbols=dc.max_symbols)
+        for n in chunks:
+            st.push(n)
+        got_best, got_finals = st.flush()
+        assert got_best == best
+        assert [f and (f[0], float(f[1])) for f in got_finals] == [f and (f[0], float(f[1])) for f in finals]
