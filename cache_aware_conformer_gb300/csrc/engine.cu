@@ -218,13 +218,25 @@ int validate(const cac_config* c) {
     return CAC_OK;
 }
 
+// Split-K policy knobs: CAC_SPLIT_TARGET (CTAs the split aims for, default
+// 120) and CAC_SPLIT_MIN_SLICES (64-wide K slices each split keeps, default 8,
+// at least 2), read once from the environment for tuning sweeps.
+int env_int(const char* name, int dflt, int lo, int hi) {
+    const char* e = std::getenv(name);
+    if (!e || !*e) return dflt;
+    const int v = std::atoi(e);
+    return v < lo ? lo : (v > hi ? hi : v);
+}
+
 int choose_splits(int tiles, int nk) {
     // split K until the grid covers most of the 152 SMs, at most 4 ways and only
     // while every split keeps >= 8 K slices: below that the cluster reduction
     // costs more than the shorter main loop saves (measured at M = 512: K = 512
     // runs faster unsplit at every N of the encoder, K = 2048 fastest 4-way)
+    static const int target = env_int("CAC_SPLIT_TARGET", 120, 1, 1 << 20);
+    static const int min_slices = env_int("CAC_SPLIT_MIN_SLICES", 8, 2, 1 << 20);
     int splits = 1;
-    while (splits < 4 && tiles * splits < 120 && nk / (splits + 1) >= 8) ++splits;
+    while (splits < 4 && tiles * splits < target && nk / (splits + 1) >= min_slices) ++splits;
     return splits;
 }
 
