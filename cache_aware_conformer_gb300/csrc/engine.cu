@@ -530,7 +530,7 @@ struct Scratch {
     float* q = nullptr;
     float2* stats = nullptr;  // fold_ln: per-row partials (sum, centred sum of squares) of 32 columns of x
 };
-constexpr int MAX_GROUPS = 4;
+constexpr int MAX_GROUPS = 8;
 
 struct cac_pool {
     cac_model* m = nullptr;
@@ -1107,8 +1107,10 @@ extern "C" int cac_pool_create(cac_model* m, int max_streams, int max_frames_per
         }
         return CAC_OK;
     };
-    // concurrent sub-batches of 64 streams for chunked steps (2 .. 4 of them)
-    p->groups = c.right_context > 0 ? 1 : std::max(1, std::min(MAX_GROUPS, S / 64));
+    // concurrent sub-batches of 64 streams for chunked steps (2 .. 4 of them;
+    // CAC_GROUPS in the environment sets the count, 1 .. MAX_GROUPS, for tuning)
+    const int g_default = std::max(1, std::min(4, S / 64));
+    p->groups = c.right_context > 0 ? 1 : std::min(env_int("CAC_GROUPS", g_default, 1, MAX_GROUPS), S);
     p->group_streams = (S + p->groups - 1) / p->groups;
     p->sc.resize(p->groups);
     if ((r = alloc_scratch(S, p->sc[0])) != CAC_OK) return fail(r);
