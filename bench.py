@@ -659,7 +659,9 @@ def workload_config(wl, world: int) -> dict:
             "layers": cfg.n_layers, "d_model": cfg.d_model, "heads": cfg.n_heads, "ff": cfg.ff_dim,
             "att_left": cfg.att_left, "att_chunk": cfg.att_chunk, "reset_prob": wl.reset_prob,
             "start_offsets": f"even, 0..{max(wl.max_start_offset - 1, 0)}", "parallelism": f"replicas x{world}",
-            "l2": "inputs larger than L2: each step reads all K/V rings and all weights"}
+            "l2": "inputs larger than L2: each step reads all K/V rings and all weights",
+            "knobs": {k: os.environ[k] for k in ("CAC_PDL", "CAC_GROUPS", "CAC_SPLIT_TARGET",
+                                                 "CAC_SPLIT_MIN_SLICES") if os.environ.get(k)}}
 
 
 def run_reference(args, wl):
