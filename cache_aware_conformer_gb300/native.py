@@ -36,7 +36,10 @@ SYMBOLS = ["cac_weights_size", "cac_model_create", "cac_model_destroy", "cac_poo
            "cac_op_wait_selftest",
            # include/cac_frontend.h
            "cac_frontend_create", "cac_frontend_destroy", "cac_frontend_reset", "cac_frontend_push",
-           "cac_frontend_flush", "cac_frontend_get_state", "cac_frontend_schedule"]
+           "cac_frontend_flush", "cac_frontend_get_state", "cac_frontend_schedule",
+           # include/cac_beam.h
+           "cac_beam_create", "cac_beam_destroy", "cac_beam_reset", "cac_beam_step", "cac_beam_check",
+           "cac_beam_get"]
 
 
 class CacError(RuntimeError):
@@ -114,6 +117,12 @@ def _lib():
             "cac_frontend_flush": (c_int, [vp, c_int, ip, vp, c_longlong, ip, vp, c_longlong, c_int, ip, vp]),
             "cac_frontend_get_state": (c_int, [vp, c_int, POINTER(c_longlong), POINTER(c_longlong), ip]),
             "cac_frontend_schedule": (c_longlong, [c_longlong, c_longlong, c_longlong, c_int]),
+            "cac_beam_create": (c_int, [POINTER(CacDecConfig), fp, c_size_t, c_int, c_int, c_int, POINTER(vp)]),
+            "cac_beam_destroy": (None, [vp]),
+            "cac_beam_reset": (c_int, [vp, c_int, ip]),
+            "cac_beam_step": (c_int, [vp, c_int, ip, vp, c_longlong, c_int, c_int, vp]),
+            "cac_beam_check": (c_int, [vp]),
+            "cac_beam_get": (c_int, [vp, c_int, c_int, fp, ip, ip, ip]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -529,3 +538,60 @@ class Frontend:
         _check(_lib().cac_frontend_get_state(self.h, sid, ctypes.byref(s), ctypes.byref(f), ctypes.byref(fin)),
                "cac_frontend_get_state")
         return s.value, f.value, fin.value
+
+
+class BeamDecoder:
+    """Batched MALSD RNN-T beam search on the current CUDA device
+    (include/cac_beam.h) for stream ids 0 .. max_streams-1; the weights and
+    config are those of the greedy decoder."""
+
+    def __init__(self, dcfg, blob: np.ndarray, beam: int, max_streams: int, max_tokens: int = 1024):
+        self.cfg, self.K, self.lmax = dcfg, beam, max_tokens
+        blob = np.ascontiguousarray(blob, dtype=np.float32)
+        self._c = CacDecConfig(dcfg.vocab, dcfg.pred_dim, dcfg.joint_dim, dcfg.max_symbols)
+        h = c_void_p()
+        _check(_lib().cac_beam_create(ctypes.byref(self._c), blob.ctypes.data_as(POINTER(c_float)), blob.size, beam,
+                                      max_streams, max_tokens, ctypes.byref(h)), "cac_beam_create")
+        self.h = h
+
+    def close(self):
+        if self.h:
+            _lib().cac_beam_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def reset(self, ids):
+        _check(_lib().cac_beam_reset(self.h, len(ids), _ids(ids)), "cac_beam_reset")
+
+    def step(self, ids, z, final: bool = False, stream=None):
+        """z: cuda fp32 [n, T, joint_dim] (slots may be strided) or None with T = 0."""
+        n = len(ids)
+        if z is None:
+            T, bstride = 0, 0
+        else:
+            _, T, J = z.shape
+            assert J == self.cfg.joint_dim and z.stride(2) == 1 and (T <= 1 or z.stride(1) == J)
+            bstride = z.stride(0) if n > 1 else T * J
+        _check(_lib().cac_beam_step(self.h, n, _ids(ids), _ptr(z), bstride, T, 1 if final else 0, _stream(stream)),
+               "cac_beam_step")
+
+    def check(self):
+        _check(_lib().cac_beam_check(self.h), "cac_beam_check")
+
+    def beam(self, sid: int, score_norm: bool = True):
+        """(slots as (tokens, score) or None, index of the winner)."""
+        K, L = self.K, self.lmax
+        sc, ln = np.zeros(K, np.float32), np.zeros(K, np.int32)
+        tok = np.zeros((K, L), np.int32)
+        best = c_int(-1)
+        ip = POINTER(c_int)
+        _check(_lib().cac_beam_get(self.h, sid, 1 if score_norm else 0, sc.ctypes.data_as(POINTER(c_float)),
+                                   ln.ctypes.data_as(ip), tok.ctypes.data_as(ip), ctypes.byref(best)), "cac_beam_get")
+        slots = [None if not np.isfinite(sc[k]) else (tuple(int(t) for t in tok[k, :ln[k]]), float(sc[k]))
+                 for k in range(K)]
+        return slots, best.value

@@ -88,10 +88,19 @@ def initial_beam(scorer, beam, blank):
     return [Hyp(F32(0.0), 0, blank, (), 0, scorer.init_state())] + [None] * (beam - 1)
 
 
-def malsd_iteration(hyps, scorer, n_frames, blank, max_symbols):
+def _cut_gap(values, k):
+    """Gap between the k-th and (k+1)-th largest finite values (inf if none)."""
+    v = np.sort(np.asarray([x for x in values if np.isfinite(x)], dtype=np.float64))[::-1]
+    return float(v[k - 1] - v[k]) if v.size > k else float("inf")
+
+
+def malsd_iteration(hyps, scorer, n_frames, blank, max_symbols, margins=None):
     """One alignment iteration over the beam `hyps` (K slots, None = empty):
     candidates, pruning to K, labels applied, recombination.  A hypothesis
-    whose time has reached n_frames is final and offers one keep candidate."""
+    whose time has reached n_frames is final and offers one keep candidate.
+    margins: a list that, when given, receives the gaps at every top-K cut
+    and within every recombined group (diagnostics for comparisons with a
+    differently rounded implementation; the search itself is unchanged)."""
     K = len(hyps)
     cands = []  # (score, parent slot, label or None for "keep"), in candidate-position order
     for k, h in enumerate(hyps):
@@ -107,7 +116,12 @@ def malsd_iteration(hyps, scorer, n_frames, blank, max_symbols):
             continue
         for lab in topk_lowest_index(lp, K):
             cands.append((F32(h.score + lp[lab]), k, lab))
+        cands += [(NEG, k, None)] * (K - min(K, len(lp)))  # fewer classes than K
+        if margins is not None:
+            margins.append(_cut_gap(lp, K))
     keep = topk_lowest_index([c[0] for c in cands], K)
+    if margins is not None:
+        margins.append(_cut_gap([c[0] for c in cands], K))
     new = []
     for pos in keep:
         s, k, lab = cands[pos]
@@ -129,6 +143,9 @@ def malsd_iteration(hyps, scorer, n_frames, blank, max_symbols):
         if len(members) < 2:
             continue
         best = min(members, key=lambda i: (-float(new[i].score), i))
+        if margins is not None:
+            sc = sorted((float(new[i].score) for i in members), reverse=True)
+            margins.append(sc[0] - sc[1])
         merged = logsumexp32([new[i].score for i in members])
         for i in members:
             if i != best:
@@ -171,17 +188,19 @@ class StreamingMalsd:
     final) and finishes.  The result equals malsd_beam over all frames.
     The scorer is asked only for frames already pushed."""
 
-    def __init__(self, scorer, beam, blank, max_symbols=10, score_norm=True):
+    def __init__(self, scorer, beam, blank, max_symbols=10, score_norm=True, margins=None):
         self.scorer, self.blank, self.max_symbols, self.score_norm = scorer, blank, max_symbols, score_norm
         self.hyps = initial_beam(scorer, beam, blank)
         self.available = 0
         self.iterations = 0
+        self.margins = margins
 
     def _run(self, n_frames):
         while any(h is not None and h.time < n_frames for h in self.hyps):
             if any(h is not None and self.available <= h.time < n_frames for h in self.hyps):
                 break  # a running hypothesis needs a frame that has not arrived
-            self.hyps = malsd_iteration(self.hyps, self.scorer, n_frames, self.blank, self.max_symbols)
+            self.hyps = malsd_iteration(self.hyps, self.scorer, n_frames, self.blank, self.max_symbols,
+                                        self.margins)
             self.iterations += 1
 
     def push(self, n_new):

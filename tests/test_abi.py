@@ -23,7 +23,7 @@ def native():
 
 
 def declared_functions():
-    text = "".join(open(os.path.join(ROOT, "include", h)).read() for h in ("cac.h", "cac_ops.h", "cac_decode.h", "cac_frontend.h"))
+    text = "".join(open(os.path.join(ROOT, "include", h)).read() for h in ("cac.h", "cac_ops.h", "cac_decode.h", "cac_frontend.h", "cac_beam.h"))
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(cac_\w+)\s*\(", text)))
 
