@@ -973,12 +973,21 @@ extern "C" int cac_beam_step(cac_beam* bd, int n, const int* ids, const float* z
         int r = launch_piece(bd, n, ids, z, z_bstride, off, Tp, fin, first, st);
         if (r != CAC_OK) return r;
         first = false;
-        while (fin) {  // the last piece of an utterance runs the search to its end
+        // The last piece of an utterance runs the search to its end.  Every
+        // hypothesis of alignment length i has time >= (i - max_symbols) /
+        // (max_symbols + 1), so the search ends by i = (frames + 1) (max_symbols
+        // + 1); the relaunches are capped accordingly (CAC_E_LIMIT beyond).
+        int tmax = 0;
+        for (int b = 0; b < n; ++b) tmax = bd->tb[ids[b]] > tmax ? bd->tb[ids[b]] : tmax;
+        const long long bound = ((long long)tmax + T + 2) * (bd->cfg.max_symbols + 1);
+        const long long cap = bound / maxit_for(bd->cfg, Tp, bd->K) + 2;
+        for (long long tries = 0; fin; ++tries) {
             if (cudaMemcpyAsync(bd->h_pending, bd->proto.pending, sizeof(int), cudaMemcpyDeviceToHost, st) !=
                     cudaSuccess ||
                 cudaStreamSynchronize(st) != cudaSuccess)
                 return CAC_E_CUDA;
             if (!*bd->h_pending) break;
+            if (tries >= cap) return CAC_E_LIMIT;
             if ((r = launch_piece(bd, n, ids, z, z_bstride, off, Tp, fin, false, st)) != CAC_OK) return r;
         }
         off += Tp;
