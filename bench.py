@@ -547,6 +547,16 @@ def run_ours(args, wl):
         except Exception as exc:  # the decoder leg is reported beside the encoder, never instead of it
             decode = {"error": f"{type(exc).__name__}: {exc}"[:300]}
 
+    legs = {}
+    for name, steps, fn in (("frontend", args.frontend_steps,
+                             lambda: measure_frontend(w.S, args.frontend_steps, dev, load_peaks()[0])),
+                            ("beam", args.beam_steps, lambda: measure_beam(w.S, args.beam_steps, dev))):
+        if steps > 0:
+            try:
+                legs[name] = fn()
+            except Exception as exc:  # reported beside the encoder, never instead of it
+                legs[name] = {"error": f"{type(exc).__name__}: {exc}"[:300]}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w.cfg, w.blob, args.cpu_chunks)
@@ -558,6 +568,7 @@ def run_ours(args, wl):
                 "config": dict(workload_config(wl, world), mean_Lc=mean_lc),
                 "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
                 "latency": latency, "gpu_launches": launches, "clocks": clk, "decode": decode}
+        line.update(legs)
         print(json.dumps(line), flush=True)
 
 
@@ -634,6 +645,67 @@ def measure_decode(w, Kd: int, dev, clk):
                          "peak_source": "derived: SMs x 128 FP32 lanes x 2 FLOP x max SM clock"}}
 
 
+def measure_frontend(S: int, Kf: int, dev, peak_gbs: float):
+    """The streaming log-mel front end (include/cac_frontend.h): Kf pushes of
+    160 ms (2560 samples) for S streams of seeded speech-like audio resident on
+    the device, CUDA events on the launching stream.  HBM bytes per push and
+    stream: the new audio read, the frames written, the 512-sample tail read
+    and rewritten."""
+    import torch
+    from cache_aware_conformer_gb300 import native
+    fe = native.Frontend(S)
+    ids, ns = list(range(S)), 2560
+    n_push = Kf + 4
+    audio = torch.from_numpy(np.stack([synth.make_audio(n_push * ns, s) for s in ids])).to(dev)
+    mel = torch.empty((S, 20, 128), dtype=torch.float32, device=dev)
+    frames = 0
+    for i in range(3):
+        frames = sum(fe.push_into(ids, audio[:, i * ns:(i + 1) * ns], mel))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(3, 3 + Kf):
+        frames = sum(fe.push_into(ids, audio[:, i * ns:(i + 1) * ns], mel))
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / Kf
+    fe.close()
+    nbytes = S * (ns * 4 + (frames / S) * 128 * 4 + 2 * 512 * 4)
+    ach = nbytes / (ms * 1e-3) / 1e9
+    return {"what": "streaming log-mel front end: 160 ms of 16 kHz audio per stream per push (fp32, one launch)",
+            "dtype": "f32", "ms_per_push": ms, "value": S * 0.16 / (ms * 1e-3), "unit": UNIT,
+            "frames_per_push": frames,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peak_gbs, "unit": "GB/s", "frac": ach / peak_gbs,
+                         "traffic": None}}
+
+
+def measure_beam(S: int, Kb: int, dev, beam: int = 8):
+    """The batched MALSD beam search (include/cac_beam.h, beam 8) over 2 seeded
+    projected frames per stream per step, CUDA events around Kb steps."""
+    import torch
+    from cache_aware_conformer_gb300 import native
+    dc = EOU_DECODER
+    Wd = synth.make_decoder_weights(dc, 0)
+    bd = native.BeamDecoder(dc, synth.pack_decoder_weights(dc, Wd), beam, S, max_tokens=256)
+    ids, T = list(range(S)), 2
+    zs = torch.from_numpy(np.stack([synth.make_joint_frames((Kb + 3) * T, s, dc.joint_dim) for s in ids])).to(dev)
+    for i in range(3):
+        bd.step(ids, zs[:, i * T:(i + 1) * T])
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(3, 3 + Kb):
+        bd.step(ids, zs[:, i * T:(i + 1) * T])
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / Kb
+    bd.check()
+    bd.close()
+    return {"what": f"MALSD beam search, beam {beam}, 2 projected frames per stream per step (fp32, cooperative "
+                    f"launch)", "dtype": "f32", "ms_per_step": ms, "value": S * T * FRAME_SEC / (ms * 1e-3),
+            "unit": UNIT, "roofline": None}
+
+
 def cpu_baseline(cfg, blob, chunks: int):
     """The oracle as it stands, one stream per host core, `chunks` pushes each."""
     cores = cpu_cores()
@@ -706,6 +778,8 @@ def main(argv=None):
     ap.add_argument("--ref-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-steps", type=int, default=40)
+    ap.add_argument("--frontend-steps", type=int, default=0, help="log-mel front-end pushes to time (0: skip)")
+    ap.add_argument("--beam-steps", type=int, default=0, help="beam-search steps to time (0: skip)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

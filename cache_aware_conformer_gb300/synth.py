@@ -278,3 +278,27 @@ def make_mels_parallel(n_frames: int, stream_ids, silence_frac: float = 0.2, wor
     import multiprocessing as mp
     with mp.get_context("spawn").Pool(workers) as pool:
         return np.stack(pool.map(_mel_job, [(n_frames, int(s), silence_frac) for s in stream_ids]))
+
+
+TID_AUDIO = (1 << 21) + 2000
+
+
+def make_audio(n_samples: int, stream_id: int, silence_frac: float = 0.2, seed_base: int = 5000) -> np.ndarray:
+    """[n_samples] float32 speech-like 16 kHz audio: a voiced source (five
+    harmonics of a pitch gliding between 100 and 250 Hz, amplitude 0.2) plus
+    white noise (0.02), with silent spans (exact zeros) covering about
+    silence_frac of the signal."""
+    k = key(seed_base + stream_id, TID_AUDIO)
+    u = uniform(k, np.arange(4, dtype=np.uint64))
+    t = np.arange(n_samples) / 16000.0
+    f0 = 100.0 + 150.0 * (0.5 + 0.5 * np.sin(2 * np.pi * (0.3 + 0.4 * u[0]) * t + 6.283 * u[1]))
+    phase = 2 * np.pi * np.cumsum(f0) / 16000.0
+    x = sum((0.2 / h) * np.sin(h * phase) for h in range(1, 6))
+    x = x + 0.02 * normal(k, n_samples, start=2)
+    span = 4800                                      # 0.3 s silent spans
+    n_span = int(round(silence_frac * n_samples / span))
+    ks = key(seed_base + stream_id, TID_AUDIO + 1)
+    starts = (uniform(ks, np.arange(n_span, dtype=np.uint64)) * max(1, n_samples - span)).astype(np.int64)
+    for s0 in starts:
+        x[s0:s0 + span] = 0.0
+    return x.astype(np.float32)
