@@ -178,6 +178,13 @@ class OracleFarm:
             assert a.recv() == "done"
         return time.perf_counter() - t
 
+    def step_one(self, chunks: int = 1) -> float:
+        """Worker 0 alone (the others idle): the one-core figure."""
+        t = time.perf_counter()
+        self.conns[0].send(chunks)
+        assert self.conns[0].recv() == "done"
+        return time.perf_counter() - t
+
     def close(self):
         for a in self.conns:
             a.send(None)
@@ -709,15 +716,18 @@ def measure_beam(S: int, Kb: int, dev, beam: int = 8):
 def cpu_baseline(cfg, blob, chunks: int):
     """The oracle as it stands, one stream per host core, `chunks` pushes each."""
     cores = cpu_cores()
-    farm = OracleFarm(cfg, blob, cores, chunks + 1)
+    farm = OracleFarm(cfg, blob, cores, 2 * chunks + 1)
     try:
         farm.step(1)                      # first push (stream start) untimed
         secs = farm.step(chunks)
+        one = farm.step_one(chunks)       # the same stream length on one core, the others idle
     finally:
         farm.close()
     return {"value": cores * chunks * 0.16 / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{cores} streams x {chunks} pushes of 160 ms (one stream per core, fp64 numpy, "
-                      f"17-layer model); {secs:.1f} s wall"}
+                      f"17-layer model); {secs:.1f} s wall",
+            "single_core": {"value": chunks * 0.16 / one, "unit": UNIT, "cores": 1,
+                            "sample": f"1 stream x {chunks} pushes of 160 ms; {one:.1f} s wall"}}
 
 
 def workload_metric(wl) -> str:
