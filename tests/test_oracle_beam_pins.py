@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 from cache_aware_conformer_gb300 import synth
-from cache_aware_conformer_gb300.config import TINY_DECODER
+from cache_aware_conformer_gb300.config import EOU_DECODER, TINY_DECODER
 from oracle import beam as B
 from oracle import decoder as D
 
@@ -87,15 +87,15 @@ def test_score_normalisation_changes_the_winner():
     assert raw == () and norm == (0, 1)
 
 
-def test_beam_one_is_the_greedy_decoder():
+@pytest.mark.parametrize("dc,n", [(TINY_DECODER, 16), (EOU_DECODER, 6)])
+def test_beam_one_is_the_greedy_decoder(dc, n):
     """Beam 1 takes the argmax of the log-softmax at every step: the greedy
     loop of oracle/decoder.py on the same predictor and frames."""
-    dc = TINY_DECODER
     W = synth.make_decoder_weights(dc, 0)
-    for s in range(4):
-        z = synth.make_joint_frames(16, s, dc.joint_dim)
+    for s in range(4 if dc is TINY_DECODER else 2):
+        z = synth.make_joint_frames(n, s, dc.joint_dim)
         em, _ = D.decode_chunk(z, D.DecoderState.fresh(W, dc), W, dc)
-        best, _ = B.malsd_beam(16, B.PredictorScorer(z, W, dc), beam=1, blank=dc.blank,
+        best, _ = B.malsd_beam(n, B.PredictorScorer(z, W, dc), beam=1, blank=dc.blank,
                                max_symbols=dc.max_symbols)
         assert best == tuple(k for _, k in em)
 
