@@ -450,7 +450,13 @@ __device__ void phase_bc(const BeamParams& d, int it, float* wsm) {
     int* cl = reinterpret_cast<int*>(cv + KMAX * KMAX);  // [K * K] candidate labels
     const long long nK = (long long)d.n * K;
     for (int b = gw; b < d.n; b += nw) {
-        if (!__ldcg(d.run + par * d.n + b)) continue;
+        if (!__ldcg(d.run + par * d.n + b)) {
+            // a stream that sits out stays out for the rest of the launch (its beam and
+            // the frames it has do not change); clear its flag for the next iteration,
+            // which still holds the value of two iterations ago
+            if (lane == 0) d.run[(par ^ 1) * d.n + b] = 0;
+            continue;
+        }
         const int s = d.ids[b];
         const int lim = d.fin ? __ldg(d.tb + b) + d.T : INT_MAX;
         const int buf = __ldcg(d.cur + s), nb = buf ^ 1;
