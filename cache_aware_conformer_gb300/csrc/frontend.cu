@@ -236,6 +236,17 @@ extern "C" long long cac_frontend_schedule(long long samples_before, long long f
     return last > frames_before ? last - frames_before : 0;
 }
 
+extern "C" int cac_frontend_tables(float* window, float* twiddles, int* mel_start, float* mel_w) {
+    if (!window || !twiddles || !mel_start || !mel_w) return CAC_E_INVAL;
+    Tables T;
+    if (!build_tables(T)) return CAC_E_UNSUPPORTED;
+    std::memcpy(window, T.win.data(), sizeof(float) * NFFT);
+    std::memcpy(twiddles, T.tw.data(), sizeof(float2) * NFFT / 2);
+    std::memcpy(mel_start, T.mstart.data(), sizeof(int) * NMEL);
+    std::memcpy(mel_w, T.mw.data(), sizeof(float) * NMEL * MW);
+    return CAC_OK;
+}
+
 extern "C" void cac_frontend_destroy(cac_frontend* fe) {
     if (!fe) return;
     for (cudaEvent_t e : fe->ev)

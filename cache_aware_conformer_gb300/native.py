@@ -36,7 +36,7 @@ SYMBOLS = ["cac_weights_size", "cac_model_create", "cac_model_destroy", "cac_poo
            "cac_op_wait_selftest",
            # include/cac_frontend.h
            "cac_frontend_create", "cac_frontend_destroy", "cac_frontend_reset", "cac_frontend_push",
-           "cac_frontend_flush", "cac_frontend_get_state", "cac_frontend_schedule",
+           "cac_frontend_flush", "cac_frontend_get_state", "cac_frontend_schedule", "cac_frontend_tables",
            # include/cac_beam.h
            "cac_beam_create", "cac_beam_destroy", "cac_beam_reset", "cac_beam_step", "cac_beam_check",
            "cac_beam_get"]
@@ -117,6 +117,7 @@ def _lib():
             "cac_frontend_flush": (c_int, [vp, c_int, ip, vp, c_longlong, ip, vp, c_longlong, c_int, ip, vp]),
             "cac_frontend_get_state": (c_int, [vp, c_int, POINTER(c_longlong), POINTER(c_longlong), ip]),
             "cac_frontend_schedule": (c_longlong, [c_longlong, c_longlong, c_longlong, c_int]),
+            "cac_frontend_tables": (c_int, [fp, fp, ip, fp]),
             "cac_beam_create": (c_int, [POINTER(CacDecConfig), fp, c_size_t, c_int, c_int, c_int, POINTER(vp)]),
             "cac_beam_destroy": (None, [vp]),
             "cac_beam_reset": (c_int, [vp, c_int, ip]),
@@ -455,6 +456,17 @@ class Decoder:
 def frontend_schedule(samples_before: int, frames_before: int, n_samples: int, flush: bool) -> int:
     """Frames a push (or flush) of n_samples emits (cac_frontend_schedule; host only)."""
     return int(_lib().cac_frontend_schedule(samples_before, frames_before, n_samples, 1 if flush else 0))
+
+
+def frontend_tables():
+    """(window [512], twiddles [256, 2], mel_start [128], mel_w [128, 16]) as the
+    front-end kernel uses them (cac_frontend_tables; host only)."""
+    win, tw = np.zeros(512, np.float32), np.zeros((256, 2), np.float32)
+    st, mw = np.zeros(128, np.int32), np.zeros((128, 16), np.float32)
+    fp, ip = POINTER(c_float), POINTER(c_int)
+    _check(_lib().cac_frontend_tables(win.ctypes.data_as(fp), tw.ctypes.data_as(fp), st.ctypes.data_as(ip),
+                                      mw.ctypes.data_as(fp)), "cac_frontend_tables")
+    return win, tw, st, mw
 
 
 class Frontend:

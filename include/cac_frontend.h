@@ -82,6 +82,15 @@ int cac_frontend_flush(cac_frontend* fe, int n, const int* ids, const float* aud
 /* Host counters of one stream: samples received, frames emitted, flushed. */
 int cac_frontend_get_state(const cac_frontend* fe, int id, long long* samples, long long* frames, int* finished);
 
+/* The constant tables the kernel uses (host arithmetic only; needs no
+ * device): window [512] (zero outside the centred 400 points), twiddles [256]
+ * as (cos, -sin)(2 pi k / 512) pairs, and the mel filters as 16-bin rows:
+ * mel_start [128] (first bin of row m) and mel_w [128][16] (weights of bins
+ * mel_start[m] .. mel_start[m] + 15; every nonzero weight of filter m lies in
+ * that span).  Each value is computed in fp64 and rounded once to fp32.
+ * Returns CAC_OK, CAC_E_INVAL for a NULL pointer. */
+int cac_frontend_tables(float* window, float* twiddles, int* mel_start, float* mel_w);
+
 /* Frames a push (flush = 0) or a flush (flush = 1) of n_samples emits for a
  * stream that has received samples_before samples and emitted frames_before
  * frames (host arithmetic only; needs no device).  Returns the count, or

@@ -51,3 +51,21 @@ def test_schedule_flush_after_a_ragged_stream(native):
             n, t = n + int(k), t + f
         tail = int(rng.integers(0, 500))
         assert t + native.frontend_schedule(n, t, tail, True) == F.n_frames(n + tail)
+
+
+def test_kernel_tables_match_the_oracle(native):
+    """The window, twiddles and sparse mel rows the kernel reads equal the
+    oracle's fp64 definitions rounded once to fp32, and the 16-bin rows hold
+    every nonzero weight of each filter."""
+    win, tw, st, mw = native.frontend_tables()
+    np.testing.assert_array_equal(win, F.frame_window().astype(np.float32))
+    k = np.arange(256)
+    np.testing.assert_array_equal(tw[:, 0], np.cos(2 * np.pi * k / 512).astype(np.float32))
+    np.testing.assert_array_equal(tw[:, 1], (-np.sin(2 * np.pi * k / 512)).astype(np.float32))
+    fb = F.mel_filterbank()
+    dense = np.zeros_like(fb)
+    for m in range(F.N_MELS):
+        assert 0 <= st[m] <= fb.shape[1] - 16
+        dense[m, st[m]:st[m] + 16] = mw[m]
+    np.testing.assert_allclose(dense, fb.astype(np.float32), rtol=0, atol=1e-9)
+    assert np.array_equal(dense != 0, fb != 0)
