@@ -533,8 +533,9 @@ class Frontend:
         import torch
         n = len(ids)
         ns = 0 if audio is None else audio.shape[1]
-        if max_frames is None:
-            max_frames = ns // 160 + 2
+        if max_frames is None:  # a push emits at most ns/160 + 1 frames, a flush up to ns/160 + 3
+            ns_max = int(max(n_samples_each)) if (flush and n_samples_each is not None and n) else ns
+            max_frames = ns_max // 160 + (4 if flush else 2)
         mel = torch.empty((n, max(max_frames, 1), self.N_MELS), dtype=torch.float32,
                           device=audio.device if audio is not None else "cuda")
         if flush:

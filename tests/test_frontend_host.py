@@ -69,3 +69,15 @@ def test_kernel_tables_match_the_oracle(native):
         dense[m, st[m]:st[m] + 16] = mw[m]
     np.testing.assert_allclose(dense, fb.astype(np.float32), rtol=0, atol=1e-9)
     assert np.array_equal(dense != 0, fb != 0)
+
+
+def test_frames_per_call_stay_within_the_bindings_capacity(native):
+    """A push emits at most n/160 + 1 frames and a flush at most n/160 + 3
+    (the binding sizes its default output by these bounds)."""
+    rng = np.random.default_rng(8)
+    for _ in range(3000):
+        n = int(rng.integers(0, 200000))
+        t = native.frontend_schedule(0, 0, n, False)
+        ns = int(rng.integers(0, 6000))
+        assert native.frontend_schedule(n, t, ns, False) <= ns // 160 + 1
+        assert native.frontend_schedule(n, t, ns, True) <= ns // 160 + 3
