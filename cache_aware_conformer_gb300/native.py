@@ -33,7 +33,7 @@ SYMBOLS = ["cac_weights_size", "cac_model_create", "cac_model_destroy", "cac_poo
            # include/cac_decode.h
            "cac_decoder_create", "cac_decoder_destroy", "cac_decoder_reset", "cac_decoder_step",
            "cac_decoder_check", "cac_decoder_get_state",
-           "cac_op_wait_selftest",
+           "cac_op_wait_selftest", "cac_op_gemm_palette",
            # include/cac_frontend.h
            "cac_frontend_create", "cac_frontend_destroy", "cac_frontend_reset", "cac_frontend_push",
            "cac_frontend_flush", "cac_frontend_get_state", "cac_frontend_schedule", "cac_frontend_tables",
@@ -110,6 +110,7 @@ def _lib():
             "cac_decoder_check": (c_int, [vp]),
             "cac_decoder_get_state": (c_int, [vp, c_int, fp, fp, fp, ip]),
             "cac_op_wait_selftest": (c_int, [c_int, vp]),
+            "cac_op_gemm_palette": (c_int, [c_int, c_int, c_int, vp, vp, vp, vp, vp, vp, vp]),
             "cac_frontend_create": (c_int, [c_int, POINTER(vp)]),
             "cac_frontend_destroy": (None, [vp]),
             "cac_frontend_reset": (c_int, [vp, c_int, ip]),
@@ -385,6 +386,21 @@ class Pool:
         _check(_lib().cac_pool_read_trace(self.h, layer, tap, out.ctypes.data_as(POINTER(c_float)), out.size),
                "cac_pool_read_trace")
         return out
+
+
+def gemm_palette(A, packed, table, bias=None, out=None, status=None, stream=None):
+    """C = A W^T (+ bias) with W[n][k] = table[6-bit index k of packed row n]
+    (cac_op_gemm_palette).  A: cuda bf16 [M, K]; packed: cuda uint8 [N, 3K/4];
+    table: cuda bf16 [64]; returns fp32 [M, N]."""
+    import torch
+    M, K = A.shape
+    N = packed.shape[0]
+    assert packed.shape[1] * 4 == 3 * K and A.is_contiguous() and packed.is_contiguous()
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _check(_lib().cac_op_gemm_palette(M, N, K, _ptr(A), _ptr(packed), _ptr(table), _ptr(bias), _ptr(out),
+                                      _ptr(status), _stream(stream)), "cac_op_gemm_palette")
+    return out
 
 
 def wait_selftest(which: int, stream=None) -> int:

@@ -27,6 +27,21 @@ extern "C" {
 int cac_op_gemm_bf16(int M, int N, int K, const void* A, const void* B, const float* bias, float* C, int splits,
                      int a_split, void* stream);
 
+/* C = A W^T (+ bias) with palette weights ("Fast Accuracy-Preserving RNNT Beam
+ * Search on Apple Silicon", §1.3: 64-entry lookup tables, 6-bit palettes) on
+ * the tensor cores (bf16 x bf16, fp32 accumulation).
+ *   A       device bf16 [M][K], row-major, 16-byte aligned
+ *   packed  device bytes [N][3K/4]: row n's indices as a little-endian bit
+ *           stream, index k in bits [6k, 6k + 6); 16-byte aligned
+ *   table   device bf16 [64]: W[n][k] = table[index]
+ *   bias    device fp32 [N] or NULL;  C  device fp32 [M][N], 16-byte aligned
+ *   status  device int or NULL: a bounded wait that gave up latches
+ *           CAC_E_TIMEOUT there (first error wins)
+ * N and K multiples of 64.  Asynchronous on `stream`.  CAC_E_INVAL for bad
+ * sizes or NULL operands, CAC_E_ALIGN for misaligned pointers. */
+int cac_op_gemm_palette(int M, int N, int K, const void* A, const void* packed, const void* table,
+                        const float* bias, float* C, int* status, void* stream);
+
 /* Failure-path self-test of the library's bounded device waits: runs the
  * wait the library uses with nothing that can satisfy it and returns the
  * status the device latched — CAC_E_TIMEOUT when the wait gave up as designed.
