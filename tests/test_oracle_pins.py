@@ -333,8 +333,10 @@ def _prov(cfg, W, mel, push=32):
 
 
 def test_provisional_tail_right_context_zero_is_exact():
-    """With no right context the mask needs no lookahead (window [p-left, p] ==
-    chunk mask with chunk 1), so the provisional tail must equal offline exactly."""
+    """With right context 0 the oracle takes the chunked mask (chunk 1 here), whose
+    window [p-left, p] needs no lookahead, so the provisional-tail schedule must
+    equal offline exactly.  (window_mask itself is pinned by the receptive-field
+    test below and by its equality with chunk_mask at chunk 1.)"""
     cfg = tiny(right_context=0, att_chunk=1, emit_frames=4, lookahead_frames=16, att_left=10)
     W = weights(cfg)
     mel = synth.make_mel(483, 6)
@@ -357,3 +359,53 @@ def test_provisional_tail_bounded_lookahead_drift_shrinks_with_lookahead():
     off, _ = O.encode_offline(mel, W, cfg)
     d = [np.abs(_prov(replace(cfg, lookahead_frames=B), W, mel) - off).max() for B in (4, 8, 16)]
     assert d[0] > 0 and d[2] < d[0]
+
+
+# ---------------------------------------------------------------------------
+# right-context window mask ("True streaming encode", §Status: the Nemotron
+# variant with right context 3, whose lookahead cascades through the layers)
+# ---------------------------------------------------------------------------
+
+def test_window_mask_with_no_right_context_is_chunk_mask_of_chunk_one():
+    pq = np.arange(0, 90)
+    pk = np.arange(-5, 95)
+    for left in (0, 6, 70):
+        np.testing.assert_array_equal(O.window_mask(pq, pk, left, 0), O.chunk_mask(pq, pk, 1, left))
+
+
+def test_window_mask_receptive_field_of_one_layer():
+    """One layer with right context 3 and left context 6 through layer_step and the
+    window mask: perturbing frame p changes the attention output exactly at
+    queries q in [p - 3, p + 6] (q sees keys [q - 6, q + 3]); the causal k = 9
+    depthwise conv after it then reaches 8 frames further right, so the layer
+    output changes exactly at [p - 3, p + 14] and is bit-identical elsewhere.
+    An off-by-one at either edge of the mask moves one end of that set."""
+    cfg = tiny(right_context=3, att_left=6, n_layers=1)
+    W = weights(cfg)
+    D = cfg.d_model
+    x0 = rng(40).normal(size=(48, D))
+
+    def run(x):
+        tr = {}
+        y, _, _, _ = O.layer_step(x, W, 0, cfg, np.zeros((0, D)), np.zeros((0, D)), np.zeros((8, D)), 0, tr)
+        return y, tr["att"][0]
+
+    base, base_att = run(x0)
+    for p in (3, 10, 20, 33):
+        x = x0.copy()
+        x[p] += rng(p).normal(size=D)   # not a constant shift: LayerNorm removes those
+        y, att = run(x)
+        att_changed = np.nonzero(np.any(att != base_att, axis=1))[0]
+        assert list(att_changed) == [q for q in range(48) if p - 3 <= q <= p + 6], p
+        changed = np.nonzero(np.any(y != base, axis=1))[0]
+        assert list(changed) == [q for q in range(48) if p - 3 <= q <= p + 14], p
+
+
+def test_window_mask_edges_on_absolute_positions():
+    """Keys before the stream start are absent; a query at p sees exactly the
+    keys p - left .. p + right that exist."""
+    pq = np.array([0, 1, 5, 40])
+    pk = np.arange(-3, 60)
+    m = O.window_mask(pq, pk, 6, 3)
+    for i, p in enumerate(pq):
+        assert list(pk[m[i]]) == [k for k in range(max(0, p - 6), p + 4)]
