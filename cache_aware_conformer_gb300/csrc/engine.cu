@@ -95,6 +95,7 @@ struct cac_model {
     int split_ffh = 0;  // bf16, d_model >= 1024: the FF hidden activations enter the down-projection split too
     int fold_ln = 0;    // streaming steps: the attention, conv and FF2 LayerNorms run inside the GEMMs
     int sms = 152;      // streaming multiprocessors of the device
+    int device = -1;    // the device current at creation: weights and pools live there
     int D = 0, H = 0, HD = 0, F = 0, L = 0, J = 0;
     int rmin = 0, NR = 0;
     std::vector<void*> allocs;
@@ -306,7 +307,10 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
     m->fold_ln = m->bf16 && m->tc && cfg->d_model % 32 == 0;
     {
         int dev = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&m->sms, cudaDevAttrMultiProcessorCount, dev);
+        if (cudaGetDevice(&dev) == cudaSuccess) {
+            m->device = dev;
+            cudaDeviceGetAttribute(&m->sms, cudaDevAttrMultiProcessorCount, dev);
+        }
     }
     m->D = cfg->d_model;
     m->H = cfg->n_heads;
@@ -1720,6 +1724,8 @@ extern "C" int cac_encode_offline_noalloc(cac_model* m, int B, const float* mel,
     int dev = -1;
     CK(cudaGetDevice(&dev));
     if (dev < 0 || dev >= kMaxDevices) return CAC_E_UNSUPPORTED;
+    // the array is the current device's: it must be the one holding the weights
+    if (dev != m->device) return CAC_E_INVAL;
     void* scratch = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_noalloc_mu);

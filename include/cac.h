@@ -177,19 +177,24 @@ int  cac_encode_offline(cac_model* m, int B, const float* mel, const int* mel_le
                         float* enc, float* joint, int* out_len, void* stream);
 
 /* cac_encode_offline without allocation.  No counterpart on the pages: this
- * entry point exists for callers that must not allocate device memory while
- * they run — for example code inside CUDA stream capture, a real-time audio
- * callback that cannot block on the allocator, or a process whose device
- * memory is budgeted up front.  cac_encode_offline grows a model-owned
- * workspace with cudaMalloc when a larger batch arrives; this variant instead
- * runs the same kernels on a fixed array of CAC_NOALLOC_SCRATCH_BYTES (32 MiB)
- * that the library declares in device memory: every GPU that loads the
- * library holds it until the process exits.
+ * entry point exists for callers that may not allocate device memory once
+ * they are running.  cudaMalloc can block the calling thread and synchronize
+ * the device, which a real-time audio callback cannot afford, and some hosts
+ * hand the library a fixed device-memory budget up front (a sandbox, a
+ * serving process that reserves memory per model at start).
+ * cac_encode_offline grows a model-owned workspace with cudaMalloc when a
+ * larger batch arrives; this variant runs the same kernels on a fixed array of
+ * CAC_NOALLOC_SCRATCH_BYTES (32 MiB) that the library declares in device
+ * memory: every GPU that loads the library holds it until the process exits.
  *   - Arguments, layouts and results are those of cac_encode_offline.
  *   - Requests whose scratch exceeds the array (roughly B x t_mel_max beyond
  *     ~11,000 mel frames for the 17-layer d_model-512 model, less for wider
  *     models) return CAC_E_LIMIT and do nothing.
  *   - It calls no cudaMalloc / cudaFree and no allocating library routine.
+ *     It copies the B lengths from mel_len to the device and waits for that
+ *     copy on `stream` before it returns (mel_len may be pageable memory).
+ *   - The model's device must be the current device (CAC_E_INVAL otherwise):
+ *     the array used is the current device's.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.

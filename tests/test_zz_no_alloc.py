@@ -1,8 +1,10 @@
 """The offline encode entry point that allocates nothing (cac_encode_offline_noalloc).
 
-It serves callers that may not allocate device memory while they run (code
-under CUDA stream capture, real-time audio callbacks, budgeted processes): it
-runs the offline encode on the library's fixed device-side scratch array.
+It serves callers that may not allocate device memory once they are running:
+a real-time audio callback cannot wait on cudaMalloc (which may block and
+synchronize the device), and some hosts give the library a fixed memory
+budget up front.  The entry point runs the offline encode on the library's
+fixed device-side scratch array instead of a cudaMalloc-grown workspace.
 These checks call it through the C ABI and compare it with the allocating
 cac_encode_offline on the same inputs, twice in a row (the shared array keeps
 the previous call's contents, so the second call shows nothing stale leaks),
