@@ -20,7 +20,7 @@
 //                  tcgen05.mma (K = 16 each), commits to `empty`;
 //   all warps      epilogue: TMEM -> registers (+ bias) -> fp32 rows of C.
 // Every wait is bounded; a wait that gives up latches CAC_E_TIMEOUT in the
-// optional status word and the CTA unwinds.
+// optional status word, and the CTA unwinds without storing any of its tile.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -125,6 +125,8 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     }
     __syncwarp();
     if (!mbar_wait(accb, 0)) ok = false;
+    // a wait that gave up in any thread voids the whole tile: no thread stores
+    const bool tile_ok = __syncthreads_or(!ok) == 0;
     tc_fence_after();
     const int quarter = warp & 3, half = warp >> 2;
     const int row = m0 + quarter * 32 + lane;
@@ -132,7 +134,7 @@ __global__ void __launch_bounds__(PTHREADS, 1)
         const int c = half * (PBN / 2);
         float v[32];
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
-        if (ok && row < M) {
+        if (tile_ok && row < M) {
             float* dst = C + (long long)row * ldc + n0 + c;
 #pragma unroll
             for (int k = 0; k < 32; ++k) dst[k] = v[k] + (bias ? __ldg(bias + n0 + c + k) : 0.f);
