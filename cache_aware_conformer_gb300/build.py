@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libcac.so")
-SOURCES = ["gemm_tc.cu", "gemm_tc_persist.cu", "gemm_simt.cu", "kernels.cu", "attn_mma.cu", "engine.cu", "decode.cu", "frontend.cu", "beam.cu", "gemm_palette.cu"]
+SOURCES = ["gemm_tc.cu", "gemm_tc_persist.cu", "gemm_simt.cu", "kernels.cu", "attn_mma.cu", "engine.cu", "decode.cu", "frontend.cu", "beam.cu", "gemm_palette.cu", "chain.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

@@ -15,6 +15,7 @@
 #include <vector>
 
 #include "../../include/cac_ops.h"
+#include "chain.cuh"
 #include "gemm.cuh"
 #include "kernels.cuh"
 
@@ -104,6 +105,7 @@ struct cac_model {
     int* status = nullptr;
     OfflineWs ws;
     long long launches = 0;
+    struct ChainRec* rec = nullptr;  // set while a pool step records GEMM / LayerNorm phases into chains
 };
 
 namespace {
@@ -241,6 +243,149 @@ int choose_splits(int tiles, int nk) {
     return splits;
 }
 
+// ---------------------------------------------------------------------------
+// chains: consecutive projections / LayerNorms of a step recorded as phases and
+// run by one persistent launch (chain.cu) when something that cannot join the
+// chain (an attention launch, the end of the step) comes next.
+// ---------------------------------------------------------------------------
+struct ChainKey {
+    int nb, n, nvalid;
+    const void *mel, *enc, *joint, *ids, *scratch;
+    long long mel_bstride;
+    int out_bstride, out_off, seq;
+    bool operator<(const ChainKey& o) const {
+        return std::tie(nb, n, nvalid, mel, enc, joint, ids, scratch, mel_bstride, out_bstride, out_off, seq) <
+               std::tie(o.nb, o.n, o.nvalid, o.mel, o.enc, o.joint, o.ids, o.scratch, o.mel_bstride, o.out_bstride,
+                        o.out_off, o.seq);
+    }
+};
+struct ChainProg {
+    ChainPhase* d = nullptr;  // device copy of the phases
+    int n = 0;
+    int M = 0;
+};
+}  // namespace
+
+struct ChainRec {
+    bool on = false;
+    std::vector<ChainPhase> ph;  // phases recorded since the last flush
+    int M = 0;
+    ChainKey ctx{};              // the step being recorded (seq counts its flushes)
+    std::map<ChainKey, ChainProg> cache;
+    ChainCtl ctl;                // device counters and split-K workspace
+    long long ws_floats = 0, tcnt_n = 0;
+    int sms = 152;
+    long long* launches = nullptr;
+    cac_pool* pool = nullptr;    // for per-class timing of the chain launches
+    bool recorded = false;       // the last GEMM call was recorded (profiling: no launch to time)
+    void release() {
+        for (auto& kv : cache)
+            if (kv.second.d) cudaFree(kv.second.d);
+        cache.clear();
+    }
+};
+
+namespace {
+
+// Split-K of a chained projection: enough tasks to cover most SMs (K ranges of
+// at least two 64-wide slices, at most 4 splits).
+int chain_splits(int tiles, int nk) {
+    static const int max_s = env_int("CAC_CHAIN_MAX_SPLITS", 4, 1, 4);  // tuning knob
+    int s = 1;
+    while (s < max_s && tiles * s < 120 && nk / (s + 1) >= 2) ++s;
+    return s;
+}
+
+int prof_begin(cac_pool* p, int cls, cudaStream_t s);
+int prof_end(cac_pool* p, cudaStream_t s);
+
+// Run the recorded phases as one chain launch (building and caching the
+// device program on its first use; never while the stream is being captured).
+int chain_flush(ChainRec* r, cudaStream_t s) {
+    if (!r || r->ph.empty()) return CAC_OK;
+    const int n_rb = (r->M + 127) / 128;
+    ChainKey key = r->ctx;
+    key.seq = r->ctx.seq++;
+    auto it = r->cache.find(key);
+    if (it == r->cache.end() || it->second.n != (int)r->ph.size() || it->second.M != r->M) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        CK(cudaStreamIsCapturing(s, &cs));
+        if (cs != cudaStreamCaptureStatusNone) return CAC_E_STATE;  // programs are built by an eager run first
+        if (r->cache.size() >= 512) {  // eager callers with ever-new buffers: start over
+            CK(cudaStreamSynchronize(s));
+            r->release();
+        }
+        long long ws = 0, tc = 0;
+        for (ChainPhase& P : r->ph) {
+            if (P.op == CH_GEMM && P.splits > 1) {
+                P.ws_off = ws;
+                ws += chain_ws_floats(P, n_rb);
+                P.tc_off = (int)tc;
+                tc += (long long)n_rb * P.tiles_n;
+            }
+        }
+        if (ws > r->ws_floats) {
+            CK(cudaStreamSynchronize(s));
+            if (r->ctl.ws) cudaFree(r->ctl.ws);
+            r->ctl.ws = nullptr;
+            r->ws_floats = 0;
+            if (cudaMalloc(&r->ctl.ws, sizeof(float) * ws) != cudaSuccess) return CAC_E_NOMEM;
+            r->ws_floats = ws;
+        }
+        if (tc > r->tcnt_n) {
+            CK(cudaStreamSynchronize(s));
+            if (r->ctl.tcnt) cudaFree(r->ctl.tcnt);
+            r->ctl.tcnt = nullptr;
+            r->tcnt_n = 0;
+            if (cudaMalloc(&r->ctl.tcnt, sizeof(int) * tc) != cudaSuccess) return CAC_E_NOMEM;
+            CK(cudaMemset(r->ctl.tcnt, 0, sizeof(int) * tc));
+            r->tcnt_n = tc;
+        }
+        ChainProg prog;
+        prog.n = (int)r->ph.size();
+        prog.M = r->M;
+        if (cudaMalloc(&prog.d, sizeof(ChainPhase) * prog.n) != cudaSuccess) return CAC_E_NOMEM;
+        CK(cudaMemcpy(prog.d, r->ph.data(), sizeof(ChainPhase) * prog.n, cudaMemcpyHostToDevice));
+        if (it != r->cache.end() && it->second.d) {
+            CK(cudaStreamSynchronize(s));
+            cudaFree(it->second.d);
+        }
+        r->cache[key] = prog;
+        it = r->cache.find(key);
+    }
+    if (r->pool) RET(prof_begin(r->pool, 15 /* chain */, s));
+    CK(launch_chain(it->second.d, it->second.n, it->second.M, r->ctl, r->sms, s));
+    if (r->pool) RET(prof_end(r->pool, s));
+    if (r->launches) ++*r->launches;
+    r->ph.clear();
+    return CAC_OK;
+}
+
+// Record a LayerNorm (launch_layernorm's arguments, bf16 activations) as a
+// chain phase; false when it cannot join a chain.
+bool chain_record_ln(ChainRec* r, const float* x, int M, int D, const float* g1, const float* b1, float* y_f32,
+                     void* y_act, const float* g2, const float* b2, void* z_act, int grp, int grp_stride,
+                     int row_off, int split) {
+    if (!r || !r->on || (D != 512 && D != 1024) || (!r->ph.empty() && r->M != M) ||
+        (int)r->ph.size() >= CH_MAX_PHASES || (M + 127) / 128 > CH_MAX_RB)
+        return false;
+    ChainPhase P;
+    std::memset(static_cast<void*>(&P), 0, sizeof(P));
+    P.op = CH_LN;
+    P.tasks_rb = 128 / CH_LN_ROWS;
+    P.done_rb = P.tasks_rb;
+    P.splits = 1;
+    P.ep = EpiParams();
+    P.x = x; P.g1 = g1; P.b1 = b1; P.g2 = g2; P.b2 = b2;
+    P.y_f32 = y_f32;
+    P.y_act = static_cast<bf16*>(y_act);
+    P.z_act = static_cast<bf16*>(z_act);
+    P.D = D; P.grp = grp; P.grp_stride = grp_stride; P.row_off = row_off; P.split = split;
+    r->M = M;
+    r->ph.push_back(P);
+    return true;
+}
+
 // GEMM dispatch: tcgen05 for bf16 models (unless the SIMT debugging twin is
 // requested), SIMT for fp32 models.  conv_C > 0: A is a stride-2 convolution
 // window read through the im2col view (M output rows = window row pairs).
@@ -250,6 +395,34 @@ int gemm(cac_model* m, const void* A, long long lda, int M, int K, const Lin& W,
     if (M <= 0) return CAC_OK;
     if (a_split && !conv_C && lda < 2LL * K) return CAC_E_INVAL;
     ep.act_bf16 = m->bf16;
+    if (m->tc && m->rec && m->rec->on) {
+        ChainRec* r = m->rec;
+        const bool chainable = !conv_C && W.BN == 64 && W.N % 64 == 0 &&
+                               (ep.kind == EPI_STORE || ep.kind == EPI_RESID || ep.kind == EPI_QKV ||
+                                ep.kind == EPI_GLUDW) &&
+                               (r->ph.empty() || r->M == M) && (int)r->ph.size() < CH_MAX_PHASES &&
+                               (M + 127) / 128 <= CH_MAX_RB;
+        if (chainable) {
+            ChainPhase P;
+            std::memset(static_cast<void*>(&P), 0, sizeof(P));
+            if (!make_tmap_bf16(&P.ta, A, a_split ? 2 * K : K, M, (uint64_t)lda * 2, 128)) return CAC_E_CUDA;
+            P.tb = W.tm;
+            P.op = CH_GEMM;
+            P.K = K;
+            P.N = W.N;
+            P.a_split = a_split ? 1 : 0;
+            P.tiles_n = W.N / 64;
+            P.splits = chain_splits(P.tiles_n * ((M + 127) / 128), K / 64);
+            P.tasks_rb = P.tiles_n * P.splits;
+            P.done_rb = P.tiles_n;
+            P.ep = ep;
+            r->M = M;
+            r->ph.push_back(P);
+            r->recorded = true;
+            return CAC_OK;
+        }
+        RET(chain_flush(r, s));  // run what is pending before a launch that cannot join
+    }
     if (m->tc) {
         CUtensorMap tmA;
         const bool ok = conv_C ? make_tmap_bf16_conv(&tmA, A, (uint64_t)conv_C * (a_split ? 2 : 1), (uint64_t)M + 1, 128)
@@ -594,6 +767,10 @@ struct cac_pool {
     int* pids_dev = nullptr;    // stream ids of the current pass
     int* pmap_dev = nullptr;    // pass slot -> batch slot of the call
     std::vector<int> sub_host;
+    // chains of projection / LayerNorm phases (chunked steps on the tcgen05 path)
+    ChainRec chain;
+    bool chains = false;  // cac_pool_set_chains (off by default: measured slower, see chain.cu)
+    int cur_group = 0;   // scratch set in use
     // per-kernel-class CUDA-event timing (eager launches only)
     bool prof = false;
     std::vector<cudaEvent_t> ev;          // event pool, reused after each read
@@ -615,6 +792,7 @@ int palloc(cac_pool* p, size_t bytes, void** out, bool zero = true) {
 // Make scratch set g the one the step functions use.
 void use_scratch(cac_pool* p, int g) {
     const Scratch& sc = p->sc[g];
+    p->cur_group = g;
     p->win1 = sc.win1; p->win2 = sc.win2; p->win3 = sc.win3; p->y3 = sc.y3;
     p->x = sc.x; p->xln = sc.xln; p->h = sc.h; p->o = sc.o; p->glu = sc.glu; p->yc = sc.yc; p->q = sc.q;
     p->stats = sc.stats;
@@ -663,10 +841,11 @@ int trace_tap(cac_pool* p, int layer, int tap, const void* src, bool src_act, in
 
 const char* const PROF_NAMES[] = {"stage_mel", "gemm_subsample", "gemm_sub_out", "layernorm",
                                   "gemm_ff_up", "gemm_ff_down", "gemm_qkv", "attention", "gemm_out_proj",
-                                  "gemm_pw1_glu", "dwconv", "gemm_pw2", "gemm_joint", "advance", "reset"};
-constexpr int N_PROF = 15;
+                                  "gemm_pw1_glu", "dwconv", "gemm_pw2", "gemm_joint", "advance", "reset",
+                                  "chain"};
+constexpr int N_PROF = 16;
 enum { P_STAGE, P_SUB, P_SUBOUT, P_LN, P_FFUP, P_FFDOWN, P_QKV, P_ATT, P_OUT, P_PW1, P_DW, P_PW2, P_JOINT,
-       P_ADV, P_RESET };
+       P_ADV, P_RESET, P_CHAIN };
 
 // Open a timed region of class `cls` on stream s (no-op unless profiling).
 int prof_begin(cac_pool* p, int cls, cudaStream_t s) {
@@ -679,11 +858,16 @@ int prof_begin(cac_pool* p, int cls, cudaStream_t s) {
     }
     const int i = (int)(2 * p->rec.size());
     p->rec.push_back({cls, i});
+    p->chain.recorded = false;
     CK(cudaEventRecord(p->ev[i], s));
     return CAC_OK;
 }
 int prof_end(cac_pool* p, cudaStream_t s) {
     if (!p->prof) return CAC_OK;
+    if (p->chain.recorded) {  // nothing launched: a GEMM recorded into a chain
+        p->rec.pop_back();
+        return CAC_OK;
+    }
     CK(cudaEventRecord(p->ev[p->rec.back().second + 1], s));
     return CAC_OK;
 }
@@ -778,11 +962,21 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
     auto use_fold = [&](EpiParams& e, const float* colsum) {
         e.ln_stats = p->stats; e.ln_colsum = colsum; e.ln_parts = D / 32; e.ln_rows = M;
     };
-    PB(P_LN);
-    CK(launch_layernorm(p->x, M, D, m->layers[0].ff1_g, m->layers[0].ff1_b, nullptr, p->xln, nullptr, nullptr,
-                        nullptr, bf, 1 << 30, 0, 0, sp, s));
-    PE();
-    ++*lc;
+    // a LayerNorm launch, or a chain phase while the step records chains
+    auto layernorm = [&](const float* x, const float* g1, const float* b1, float* y_f32, void* y_act,
+                         const float* g2, const float* b2, void* z_act, int grp, int grp_stride, int row_off,
+                         int split) -> int {
+        if (chain_record_ln(m->rec, x, M, D, g1, b1, y_f32, y_act, g2, b2, z_act, grp, grp_stride, row_off, split))
+            return CAC_OK;
+        RET(chain_flush(m->rec, s));
+        PB(P_LN);
+        CK(launch_layernorm(x, M, D, g1, b1, y_f32, y_act, g2, b2, z_act, bf, grp, grp_stride, row_off, split, s));
+        PE();
+        ++*lc;
+        return CAC_OK;
+    };
+    RET(layernorm(p->x, m->layers[0].ff1_g, m->layers[0].ff1_b, nullptr, p->xln, nullptr, nullptr, nullptr, 1 << 30,
+                  0, 0, sp));
 
     for (int l = 0; l < L; ++l) {
         const LayerW& Lw = m->layers[l];
@@ -827,6 +1021,7 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
             a.nb = nb;
             a.scale = 1.f / std::sqrt((float)m->HD);
             if (!p->amaps.empty()) { a.maps = &p->amaps[l]; a.layer = l; a.L = L; }
+            RET(chain_flush(m->rec, s));  // the projections before attention run first
             PB(P_ATT);
             CK(launch_attention_stream(a, bf, p->status, s));
             PE();
@@ -898,18 +1093,13 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
         PE();
         // ln_out, fused with the next layer's FF1 LayerNorm (or, after the last
         // layer, writing the encoder frames to the caller and the joint input)
-        PB(P_LN);
         if (l + 1 < L) {
-            CK(launch_layernorm(p->x, M, D, Lw.out_g, Lw.out_b, p->x, nullptr, m->layers[l + 1].ff1_g,
-                                m->layers[l + 1].ff1_b, p->xln, bf, 1 << 30, 0, 0, sp, s));
-            PE();
-            ++*lc;
+            RET(layernorm(p->x, Lw.out_g, Lw.out_b, p->x, nullptr, m->layers[l + 1].ff1_g, m->layers[l + 1].ff1_b,
+                          p->xln, 1 << 30, 0, 0, sp));
             RET(trace_tap(p, l, 6, p->x, false, M, s));
         } else {
-            CK(launch_layernorm(p->x, M, D, Lw.out_g, Lw.out_b, enc ? enc : p->x, p->xln, nullptr, nullptr, nullptr,
-                                bf, enc ? n : 1 << 30, enc ? out_bstride : 0, enc ? out_off : 0, 0, s));
-            PE();
-            ++*lc;
+            RET(layernorm(p->x, Lw.out_g, Lw.out_b, enc ? enc : p->x, p->xln, nullptr, nullptr, nullptr,
+                          enc ? n : 1 << 30, enc ? out_bstride : 0, enc ? out_off : 0, 0));
             RET(trace_tap(p, l, 6, p->xln, true, M, s));
         }
     }
@@ -933,14 +1123,49 @@ int run_joint(cac_pool* p, const void* act, int M, int grp, float* joint, int ou
     return CAC_OK;
 }
 
+// Whether a chunked step runs its projections and LayerNorms as chains: the
+// pool asked for them (cac_pool_set_chains, or CAC_CHAIN=1 in the environment
+// for every pool), the tcgen05 path with the folded LayerNorms and the fused
+// depthwise conv, and no tracing.
+bool chain_env() {
+    static const bool on = [] {
+        const char* e = std::getenv("CAC_CHAIN");
+        return e && e[0] == '1';
+    }();
+    return on;
+}
+bool chain_step_ok(const cac_pool* p, int nb, int n) {
+    const cac_model* m = p->m;
+    return (p->chains || chain_env()) && m->tc && m->fold_ln && m->split && p->stats && 32 % n == 0 && !p->trace &&
+           (m->D == 512 || m->D == 1024) && (nb * n + 127) / 128 <= CH_MAX_RB &&
+           p->chain.ctl.cnt != nullptr;
+}
+
 // One chunked-causal step: nb batch slots (ids in p->ids_dev), n new frames each.
 //   enc/joint: frame i of slot b goes to row b * out_bstride + out_off + i
 int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride, const int* nvalid, float* enc,
              float* joint, int out_bstride, int out_off, cudaStream_t s, const int* ids = nullptr) {
     if (!ids) ids = p->ids_dev;
-    RET(run_subsample(p, nb, n, mel, mel_bstride, nvalid, ids, p->pos, s));
-    RET(run_layers(p, nb, n, n, ids, enc, out_bstride, out_off, s));
-    if (joint) RET(run_joint(p, p->xln, nb * n, n, joint, out_bstride, out_off, nullptr, s));
+    cac_model* m = p->m;
+    const bool chained = chain_step_ok(p, nb, n);
+    if (chained) {
+        ChainRec& r = p->chain;
+        r.on = true;
+        r.ph.clear();
+        r.ctx = ChainKey{nb, n, nvalid ? 1 : 0, mel, enc, joint, ids, p->x, mel_bstride, out_bstride, out_off, 0};
+        r.launches = &p->launches;
+        m->rec = &r;
+    }
+    int rc = run_subsample(p, nb, n, mel, mel_bstride, nvalid, ids, p->pos, s);
+    if (rc == CAC_OK) rc = run_layers(p, nb, n, n, ids, enc, out_bstride, out_off, s);
+    if (rc == CAC_OK && joint) rc = run_joint(p, p->xln, nb * n, n, joint, out_bstride, out_off, nullptr, s);
+    if (chained) {
+        if (rc == CAC_OK) rc = chain_flush(&p->chain, s);
+        p->chain.on = false;
+        p->chain.ph.clear();
+        m->rec = nullptr;
+    }
+    RET(rc);
     PB(P_ADV);
     CK(launch_advance(p->pos, ids, nb, n, s));
     PE();
@@ -1012,15 +1237,23 @@ int step_one(cac_pool* p, int group, int nb, int n, const float* mel, long long 
     return CAC_OK;
 }
 
+// Concurrent sub-batches of a chunked step over nb streams: flush and traced
+// steps and chained steps (the chain kernel keeps its row blocks apart itself)
+// run as one batch.  Profiled steps keep the sub-batches, so that per-class
+// timings describe the launch configuration of unprofiled steps.
+int step_groups(const cac_pool* p, int nb, int n, bool flush) {
+    return (p->groups > 1 && !flush && !p->trace && !chain_step_ok(p, nb, n))
+               ? std::min(p->groups, (nb + p->group_streams - 1) / p->group_streams)
+               : 1;
+}
+
 // One chunked step.  Over many streams it runs as up to p->groups concurrent
 // sub-batches (contiguous batch slots, <= group_streams each), each on its own
 // pool stream with its own scratch and graph, forked from and joined back into
 // s; traced, profiled and flush steps stay one batch on s.
 int step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride, const int* nvalid, float* enc,
          float* joint, int out_bstride, int out_off, cudaStream_t s) {
-    const int G = (p->groups > 1 && !nvalid && !p->trace && !p->prof)
-                      ? std::min(p->groups, (nb + p->group_streams - 1) / p->group_streams)
-                      : 1;
+    const int G = step_groups(p, nb, n, nvalid != nullptr);
     if (G <= 1) return step_one(p, 0, nb, n, mel, mel_bstride, nvalid, enc, joint, out_bstride, out_off, p->ids_dev, s);
     const int per = (nb + G - 1) / G;
     const int D = p->m->D, J = p->m->J;
@@ -1136,6 +1369,15 @@ extern "C" int cac_pool_create(cac_model* m, int max_streams, int max_frames_per
     p->nvalid_dev = static_cast<int*>(v);
     if ((r = palloc(p, sizeof(int), &v)) != CAC_OK) return fail(r);
     p->status = static_cast<int*>(v);
+    if (m->tc) {  // chain counters: completion [phase][row block], exit counter, abort word
+        if ((r = palloc(p, sizeof(int) * (CH_MAX_PHASES * CH_MAX_RB + 2), &v)) != CAC_OK) return fail(r);
+        p->chain.ctl.cnt = static_cast<int*>(v);
+        p->chain.ctl.done = p->chain.ctl.cnt + CH_MAX_PHASES * CH_MAX_RB;
+        p->chain.ctl.abort = p->chain.ctl.done + 1;
+        p->chain.ctl.status = p->status;
+        p->chain.sms = m->sms;
+        p->chain.pool = p;
+    }
     p->trace_rows = (int)rows_max;
     if (c.right_context > 0) {
         // waiting frames stay below emit + lookahead + one push sub-step
@@ -1169,6 +1411,9 @@ extern "C" void cac_pool_destroy(cac_pool* p) {
     cudaDeviceSynchronize();
     for (auto& kv : p->gcache)
         if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+    p->chain.release();
+    if (p->chain.ctl.ws) cudaFree(p->chain.ctl.ws);
+    if (p->chain.ctl.tcnt) cudaFree(p->chain.ctl.tcnt);
     for (void* d : p->allocs) cudaFree(d);
     if (p->trace_buf) cudaFree(p->trace_buf);
     if (p->pinned) cudaFreeHost(p->pinned);
@@ -1914,6 +2159,19 @@ extern "C" int cac_pool_set_graphs(cac_pool* p, int enable) {
 }
 
 extern "C" long long cac_pool_launch_count(cac_pool* p) { return p ? p->launches : -1; }
+
+extern "C" int cac_pool_sub_batches(cac_pool* p, int n_streams, int n_frames) {
+    if (!p || n_streams < 1 || n_streams > p->S || n_frames < 1) return CAC_E_INVAL;
+    if (p->m->cfg.right_context > 0) return 1;
+    return step_groups(p, n_streams, n_frames, false);
+}
+
+extern "C" int cac_pool_set_chains(cac_pool* p, int enable) {
+    if (!p) return CAC_E_INVAL;
+    if (cudaDeviceSynchronize() != cudaSuccess) return CAC_E_CUDA;
+    p->chains = enable != 0;
+    return CAC_OK;
+}
 
 extern "C" int cac_pool_set_trace(cac_pool* p, int enable) {
     if (!p) return CAC_E_INVAL;

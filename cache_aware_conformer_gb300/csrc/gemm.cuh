@@ -251,8 +251,9 @@ struct EpiPre {
 __device__ __forceinline__ void ln_row_stats(const float2* st, int parts, float& mean, float& rstd) {
     const float4* s4 = reinterpret_cast<const float4*>(st);
     float4 q[16];
+    // through L2: the partials may come from another CTA of the same launch
 #pragma unroll
-    for (int j = 0; j < 16; ++j) q[j] = 2 * j < parts ? s4[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < 16; ++j) q[j] = 2 * j < parts ? __ldcg(s4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
     float s = 0.f;
 #pragma unroll
     for (int j = 0; j < 16; ++j) s += q[j].x + q[j].z;
@@ -294,7 +295,7 @@ __device__ __forceinline__ void epi_prefetch(const EpiParams& e, int row, int co
     if constexpr (KIND == EPI_RESID) {
         const float4* x4 = reinterpret_cast<const float4*>(e.x + (long long)row * e.ldx + col0);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) pre.x[i] = x4[i];
+        for (int i = 0; i < 8; ++i) pre.x[i] = __ldcg(x4 + i);  // L2: may be another CTA's write
         if (e.xs) {
             const float4* g4 = reinterpret_cast<const float4*>(e.xs_gamma + col0);
 #pragma unroll

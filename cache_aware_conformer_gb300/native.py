@@ -27,7 +27,7 @@ SYMBOLS = ["cac_weights_size", "cac_model_create", "cac_model_destroy", "cac_poo
            "cac_stream_create", "cac_stream_destroy", "cac_stream_reset", "cac_stream_push", "cac_stream_push_host",
            "cac_stream_flush", "cac_stream_flush_frames", "cac_encode_offline", "cac_stream_get_state",
            "cac_stream_set_state", "cac_pool_check", "cac_model_check", "cac_pool_set_graphs",
-           "cac_pool_launch_count", "cac_pool_set_trace", "cac_pool_read_trace", "cac_pool_set_profile",
+           "cac_pool_launch_count", "cac_pool_set_chains", "cac_pool_sub_batches", "cac_pool_set_trace", "cac_pool_read_trace", "cac_pool_set_profile",
            "cac_pool_read_profile", "cac_profile_classes", "cac_profile_class_name", "cac_strerror",
            "cac_op_gemm_bf16", "cac_encode_offline_noalloc",
            # include/cac_decode.h
@@ -95,6 +95,8 @@ def _lib():
             "cac_model_check": (c_int, [vp]),
             "cac_pool_set_graphs": (c_int, [vp, c_int]),
             "cac_pool_launch_count": (c_longlong, [vp]),
+            "cac_pool_set_chains": (c_int, [vp, c_int]),
+            "cac_pool_sub_batches": (c_int, [vp, c_int, c_int]),
             "cac_pool_set_trace": (c_int, [vp, c_int]),
             "cac_pool_read_trace": (c_int, [vp, c_int, c_int, fp, c_size_t]),
             "cac_pool_set_profile": (c_int, [vp, c_int]),
@@ -366,6 +368,16 @@ class Pool:
 
     def launch_count(self) -> int:
         return int(_lib().cac_pool_launch_count(self.h))
+
+    def sub_batches(self, n_streams: int, n_frames: int) -> int:
+        """Concurrent sub-batches a push of n_streams x n_frames runs as (cac_pool_sub_batches)."""
+        r = int(_lib().cac_pool_sub_batches(self.h, n_streams, n_frames))
+        _check(min(r, 0), "cac_pool_sub_batches")
+        return r
+
+    def set_chains(self, on: bool):
+        """Chained steps (default) or one launch per projection (cac_pool_set_chains)."""
+        _check(_lib().cac_pool_set_chains(self.h, 1 if on else 0), "cac_pool_set_chains")
 
     def set_profile(self, on: bool):
         _check(_lib().cac_pool_set_profile(self.h, 1 if on else 0), "cac_pool_set_profile")

@@ -243,6 +243,25 @@ int  cac_pool_set_graphs(cac_pool* p, int enable);
  * counter; a graph replay counts its kernel nodes). */
 long long cac_pool_launch_count(cac_pool* p);
 
+/* The number of concurrent sub-batches a push of n_streams streams with
+ * n_frames frames each runs as (1 when the step is not split; a profiled push
+ * keeps the split).  Host-only; CAC_E_INVAL for bad arguments. */
+int  cac_pool_sub_batches(cac_pool* p, int n_streams, int n_frames);
+
+/* Chained steps (1): on the tensor-core path a chunked step runs the
+ * projections and LayerNorms between two attention launches as one
+ * persistent kernel whose 128-row blocks advance phase by phase on
+ * completion counters ("True streaming encode", §Per-chunk flow steps 2-4,
+ * as one submission per stretch of the layer stack), all streams as one
+ * batch.  0 (default): one launch per projection, the step split into
+ * concurrent sub-batches of 64 streams, each replayed from its own CUDA
+ * graph — measured faster on a GB300 (1.43 against 3.2 ms for 256 streams),
+ * because a chained phase's latency (main loop, epilogue, completion signal)
+ * is exposed while the sub-batches overlap one another's.  Both compute the
+ * same step; split-K sums differ in order only.  Synchronizes the device.
+ * CAC_CHAIN=1 in the environment turns chains on for every pool. */
+int  cac_pool_set_chains(cac_pool* p, int enable);
+
 /* Per-layer intermediate taps of the most recent push, for kernel-level
  * parity checks.  enable=1 makes every later push copy, per layer, the fp32
  * rows of: 0 x after FF1, 1 attention output before the out-projection,

@@ -5,6 +5,7 @@ offsets reached by pre-roll, 1 % resets per step, CUDA graphs on), checked on
 sampled streams that the oracle replays one by one."""
 import multiprocessing as mp
 import os
+from dataclasses import replace
 
 import numpy as np
 import pytest
@@ -107,19 +108,33 @@ def test_config2_one_stream_30s(eou_blob):
 
 
 def test_config3_256_streams_sampled(eou_blob):
+    """The benchmark's 256-stream schedule (pre-roll to even start offsets, 1 %
+    resets per step, an utterance that ends restarts) for long enough that the
+    sampled stream closest to its end wraps around: streams 0, S-1, that stream
+    and 13 seeded others, every step compared with the oracle's replay."""
     import bench
     cfg, blob, path = eou_blob
     wl = WORKLOADS["eou120m_256streams_60s"]
-    steps = 24
-    w = bench.StreamWorkload(wl, 0, torch.device(DEV), steps, workers=8)
-    S = w.S
+    S = wl.streams
+    n = wl.push_mel // 8
+    chunks = int(round(wl.seconds * 100)) // wl.push_mel
+    pre = synth.start_offsets(S, wl.max_start_offset, seed=7) // n
+    wrap = int(np.argmax(pre))                                  # nearest to its utterance's end
+    steps = max(100, chunks - int(pre[wrap]) + 4)
     rng = np.random.default_rng(3)
-    sample = sorted({0, S - 1, *rng.choice(np.arange(1, S - 1), 2, replace=False).tolist()})
+    others = rng.choice([s for s in range(1, S - 1) if s != wrap], 13, replace=False).tolist()
+    sample = sorted({0, S - 1, wrap, *others})
+    w = bench.StreamWorkload(wl, 0, torch.device(DEV), steps, workers=8)
+    assert (w.pre == pre).all()
+    # the schedule exercises what it should: mid-run resets and an utterance wrap
+    reset_streams = {s for t in range(1, steps) for s in w.resets[t].tolist() if s in sample}
+    assert len(reset_streams) >= 2, reset_streams
+    assert any(int(w.cidx[t][wrap]) == 0 for t in range(1, steps))
     jobs = []
     for s in sample:
         jobs.append((cfg, path, s, int(w.pre[s]), [int(w.cidx[t][s]) for t in range(steps)],
                      [bool(s in set(w.resets[t].tolist())) for t in range(steps)]))
-    with mp.get_context("spawn").Pool(len(sample)) as pool:
+    with mp.get_context("spawn").Pool(min(len(sample), os.cpu_count() or 1)) as pool:
         fut = pool.map_async(_oracle_schedule, jobs)
         w.pool.set_graphs(True)
         got = []
@@ -132,7 +147,7 @@ def test_config3_256_streams_sampled(eou_blob):
     for k, s in enumerate(sample):
         ge = np.concatenate([g[0][k] for g in got])
         re = np.concatenate([r[0] for r in ref[k]])
-        assert_close(ge, re, cfg, f"stream {s}")
+        assert_close(ge, re, cfg, f"stream {s} ({steps} steps)")
         # bookkeeping: subT and Lc after the last step are exact
         assert states[s]["subT"] == ref[k][-1][2] and states[s]["Lc"] == ref[k][-1][3]
 
@@ -228,9 +243,13 @@ def _stream_schedule_test(wl, cfg, path, steps, sample):
 
 
 def test_config4b_600m_64_streams_sampled(c600m_blob):
+    """Config 4b's 64-stream launch configuration, with resets added (5 % per
+    stream and step) so that sampled streams restart mid-run."""
     cfg, path = c600m_blob
-    wl = WORKLOADS["c600m_64streams_30s"]
-    _stream_schedule_test(wl, cfg, path, 16, [0, 31, wl.streams - 1])
+    wl = replace(WORKLOADS["c600m_64streams_30s"], reset_prob=0.05)
+    sample = [0, 31, wl.streams - 1]
+    assert any(synth.reset_mask(wl.streams, t, wl.reset_prob, seed=11)[s] for t in range(1, 16) for s in sample)
+    _stream_schedule_test(wl, cfg, path, 16, sample)
 
 
 def test_config5_provisional_128_streams_sampled(eou_blob):
@@ -242,3 +261,18 @@ def test_config5_provisional_128_streams_sampled(eou_blob):
     np.save(path, synth.pack_weights(cfg, W))
     del W
     _stream_schedule_test(wl, cfg, path, 16, [0, 64, wl.streams - 1])
+
+
+def test_config5_provisional_resets_with_pending_lookahead(eou_blob):
+    """Provisional-tail pool reset between passes while subsampled frames wait
+    in the x0 ring (16 lookahead frames are always pending mid-stream): the
+    reset stream must restart like the oracle's ProvisionalTailEncoder.reset()."""
+    wl = replace(WORKLOADS["eou120m_rc3_128streams_30s"], reset_prob=0.05)
+    cfg = wl.model
+    sample = [0, 64, wl.streams - 1]
+    assert sum(synth.reset_mask(wl.streams, t, wl.reset_prob, seed=11)[s] for t in range(1, 16) for s in sample) >= 2
+    W = synth.make_weights_parallel(cfg, seed=0, workers=8)
+    path = eou_blob[2].replace("eou.npy", "rc3r.npy")
+    np.save(path, synth.pack_weights(cfg, W))
+    del W
+    _stream_schedule_test(wl, cfg, path, 16, sample)
