@@ -20,6 +20,7 @@ its own replica; no collective on the data path (weak scaling).
 from __future__ import annotations
 
 import argparse
+from dataclasses import replace
 import json
 import os
 import subprocess
@@ -502,7 +503,7 @@ def run_ours(args, wl):
         a1.synchronize()
         lat.append(a0.elapsed_time(a1))
     latency = {"p50_ms": float(np.percentile(lat, 50)), "p95_ms": float(np.percentile(lat, 95)),
-               "pushes": len(lat), "note": "one push of all streams, graph replay, device time"}
+               "pushes": len(lat), "note": "one push of all streams, graph replay, device time"} if lat else None
 
     # ---- profiled pass of the same steps: per-kernel-class CUDA events (the
     # timed steps' sub-batches, eager launches; NVTX range "profiled")
@@ -731,7 +732,10 @@ def measure_beam(S: int, Kb: int, dev, beam: int = 8):
     bd.close()
     return {"what": f"MALSD beam search, beam {beam}, 2 projected frames per stream per step (fp32, cooperative "
                     f"launch)", "dtype": "f32", "ms_per_step": ms, "value": S * T * FRAME_SEC / (ms * 1e-3),
-            "unit": UNIT, "roofline": None}
+            "unit": UNIT,
+            "roofline": None,
+            "roofline_note": "not reported: the joint evaluations and label expansions per step depend on the "
+                             "search and are not counted on the device"}
 
 
 def cpu_baseline(cfg, blob, chunks: int):
@@ -763,7 +767,8 @@ def workload_config(wl, world: int) -> dict:
             "att_left": cfg.att_left, "att_chunk": cfg.att_chunk, "reset_prob": wl.reset_prob,
             "start_offsets": f"even, 0..{max(wl.max_start_offset - 1, 0)}", "parallelism": f"replicas x{world}",
             "l2": "inputs larger than L2: each step reads all K/V rings and all weights",
-            "knobs": {k: os.environ[k] for k in ("CAC_PDL", "CAC_GROUPS", "CAC_SPLIT_TARGET",
+            "knobs": {k: os.environ[k] for k in ("CAC_PDL", "CAC_GROUPS", "CAC_SPLIT_TARGET", "CAC_CHAIN",
+                                                 "CAC_CHAIN_MAX_SPLITS",
                                                  "CAC_SPLIT_MIN_SLICES") if os.environ.get(k)}}
 
 
@@ -805,16 +810,20 @@ def main(argv=None):
     ap.add_argument("--workload", default="eou120m_256streams_60s", choices=sorted(WORKLOADS))
     ap.add_argument("--profile-steps", type=int, default=40)
     ap.add_argument("--e2e-steps", type=int, default=40)
-    ap.add_argument("--cpu-chunks", type=int, default=6)
+    ap.add_argument("--cpu-chunks", type=int, default=100)
     ap.add_argument("--ref-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-steps", type=int, default=40)
-    ap.add_argument("--frontend-steps", type=int, default=0, help="log-mel front-end pushes to time (0: skip)")
-    ap.add_argument("--beam-steps", type=int, default=0, help="beam-search steps to time (0: skip)")
+    ap.add_argument("--frontend-steps", type=int, default=20, help="log-mel front-end pushes to time (0: skip)")
+    ap.add_argument("--beam-steps", type=int, default=10, help="beam-search steps to time (0: skip)")
+    ap.add_argument("--streams", type=int, default=0,
+                    help="override the workload's stream count (small cases for profiler captures; 0: the workload's)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     wl = WORKLOADS[args.workload]
+    if args.streams > 0:
+        wl = replace(wl, streams=args.streams)
     if args.impl == "reference":
         run_reference(args, wl)
     elif wl.offline_batch:

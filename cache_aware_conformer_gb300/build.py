@@ -31,8 +31,8 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found (CUDA 13 toolkit required)")
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, extra: list[str], objdir: str = BUILD) -> str:
+    obj = os.path.join(objdir, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -42,21 +42,29 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(extra: list[str] | None = None, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
-    extra = list(extra or [])
+LIB_CHECKED = os.path.join(PKG, "libcac_checked.so")
+
+
+def build(extra: list[str] | None = None, verbose: bool = False, checked: bool = False) -> str:
+    """checked=True: the CAC_CHECKED variant (index checks in the step's
+    kernels) as libcac_checked.so, selected at run time with CAC_LIB=checked."""
+    objdir = os.path.join(BUILD, "checked") if checked else BUILD
+    lib = LIB_CHECKED if checked else LIB
+    os.makedirs(objdir, exist_ok=True)
+    extra = list(extra or []) + (["-DCAC_CHECKED"] if checked else [])
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, extra, objdir), SOURCES))
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-ldl", "-lpthread", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose:
-        print("built", LIB)
-    return LIB
+        print("built", lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(sys.argv[1:], verbose=True)
+    args = sys.argv[1:]
+    build([a for a in args if a != "--checked"], verbose=True, checked="--checked" in args)

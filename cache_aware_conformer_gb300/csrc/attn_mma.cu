@@ -292,7 +292,8 @@ __global__ void __launch_bounds__(AW_THREADS, 1)
                     latch_error(status, CAC_E_TIMEOUT);
                     break;
                 }
-                const int id = a.ids[b];
+                int id = a.ids[b];
+                if (!in_range(id, a.n_streams, status)) id = 0;  // checked build: latched, stay in bounds
                 const int blk = (id * a.L + a.layer) * a.H + h;
                 uint8_t* Ks = sm + AW_OFF_RING + st * AW_STAGE;
                 mbar_expect_tx(&full[st], 2u * a.R * AM_ROWB);
@@ -313,9 +314,12 @@ __global__ void __launch_bounds__(AW_THREADS, 1)
         const int b = blockIdx.x + k * gridDim.x;
         if (b >= a.nb) break;
         const int st = k % AW_STAGES;
-        const int id = a.ids[b];
-        const int p0 = a.pos[id];
+        int id = a.ids[b];
+        if (!in_range(id, a.n_streams, status)) id = 0;  // checked build: latched, stay in bounds
+        int p0 = a.pos[id];
+        if (!in_range(p0, 1 << 30, status)) p0 = 0;
         const int Lc = min(p0, a.left);
+        if (!in_range(Lc + nq - 1, a.R, status)) break;   // more keys than ring rows
         const int s0 = (p0 - Lc) % a.R;
         uint32_t bu[4][2], bv[4][2];
         query_frags(a, a.q + (long long)b * nq * a.ldq + h * HD, h, nq, lane, bu, bv);

@@ -82,6 +82,23 @@ __device__ __forceinline__ void latch_error(int* status, int code) {
 }
 
 // ---------------------------------------------------------------------------
+// checked build (-DCAC_CHECKED): index checks that latch CAC_E_BOUNDS and let
+// the caller skip the access; in the default build they compile to nothing
+// ---------------------------------------------------------------------------
+#ifdef CAC_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+// true when 0 <= v < n (always true in the default build)
+__device__ __forceinline__ bool in_range(long long v, long long n, int* status) {
+    if (!kChecked) return true;
+    if (v >= 0 && v < n) return true;
+    latch_error(status, CAC_E_BOUNDS);
+    return false;
+}
+
+// ---------------------------------------------------------------------------
 // shared-memory addresses and mbarriers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

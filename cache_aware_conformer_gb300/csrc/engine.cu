@@ -767,6 +767,7 @@ struct cac_pool {
     int* pids_dev = nullptr;    // stream ids of the current pass
     int* pmap_dev = nullptr;    // pass slot -> batch slot of the call
     std::vector<int> sub_host;
+    std::vector<char*> guards;   // guard zones around the per-stream pools (palloc_guarded)
     // chains of projection / LayerNorm phases (chunked steps on the tcgen05 path)
     ChainRec chain;
     bool chains = false;  // cac_pool_set_chains (off by default: measured slower, see chain.cu)
@@ -779,6 +780,23 @@ struct cac_pool {
 };
 
 namespace {
+
+// A per-stream pool between two guard zones of GUARD_BYTES filled with 0xFF
+// bytes (NaN in bf16 and fp32), checked by cac_pool_check_guards.
+constexpr size_t GUARD_BYTES = 4096;
+int palloc_guarded(cac_pool* p, size_t bytes, void** out) {
+    char* d = nullptr;
+    const size_t total = bytes + 2 * GUARD_BYTES;
+    if (cudaMalloc(&d, total) != cudaSuccess) return CAC_E_NOMEM;
+    p->allocs.push_back(d);
+    if (cudaMemset(d, 0, total) != cudaSuccess || cudaMemset(d, 0xFF, GUARD_BYTES) != cudaSuccess ||
+        cudaMemset(d + GUARD_BYTES + bytes, 0xFF, GUARD_BYTES) != cudaSuccess)
+        return CAC_E_CUDA;
+    p->guards.push_back(d);
+    p->guards.push_back(d + GUARD_BYTES + bytes);
+    *out = d + GUARD_BYTES;
+    return CAC_OK;
+}
 
 int palloc(cac_pool* p, size_t bytes, void** out, bool zero = true) {
     void* d = nullptr;
@@ -889,7 +907,7 @@ int run_subsample(cac_pool* p, int nb, int n, const float* mel, long long mel_bs
 
     // 1. mel staging: [melTail | mel] windows, tail update
     PB(P_STAGE);
-    CK(launch_stage_mel(mel, mel_bstride, nvalid, p->win1, p->tail, ids, posS, n, nb, bf, sp, p->status, s));
+    CK(launch_stage_mel(mel, mel_bstride, nvalid, p->win1, p->tail, ids, posS, n, nb, bf, sp, p->status, s, p->S));
     PE();
     ++*lc;
     // 2. three stride-2 convolutions (implicit GEMMs over the windows) + out linear
@@ -903,6 +921,8 @@ int run_subsample(cac_pool* p, int nb, int n, const float* mel, long long mel_bs
         ep.split_out = sp ? D : 0;
         ep.ids = ids;
         ep.pos = posS;
+        ep.n_streams = p->S;
+        ep.status = p->status;
         ep.P = W1 / 2; ep.T_out = W2; ep.dst_rows = W2; ep.dst_off = 0; ep.tmult = 4; ep.toff = 6;
         PB(P_SUB);
         RET(gemm(m, p->win1, 2 * rwm, nb * (W1 / 2), 3 * MEL, m->sub1, MEL, ep, s, lc, sp));
@@ -1006,6 +1026,7 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
         ep.kring = static_cast<char*>(p->kring) + (long long)l * m->H * p->R * m->HD * ab;
         ep.vring = static_cast<char*>(p->vring) + (long long)l * m->H * p->R * m->HD * ab;
         ep.q = p->q; ep.ldq = D; ep.ids = ids; ep.pos = p->pos; ep.nq = n;
+        ep.n_streams = p->S; ep.status = p->status;
         PB(P_QKV);
         RET(gemm(m, p->xln, ldl, M, D, Lw.qkv, 0, ep, s, lc, sp));
         PE();
@@ -1013,7 +1034,7 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
             AttnParams a;
             a.q = p->q; a.ldq = D;
             a.k = ep.kring; a.v = ep.vring; a.sstride = p->ring_sstride; a.R = p->R;
-            a.ids = ids; a.pos = p->pos; a.nq = n;
+            a.ids = ids; a.pos = p->pos; a.nq = n; a.n_streams = p->S;
             a.P = Lw.Ppad; a.rmin = m->rmin; a.NR = m->NR; a.pbu = Lw.pbu; a.pbv = Lw.pbv;
             a.out = p->o; a.ldo = (int)ldl; a.out_split = sp ? D : 0;
             a.H = m->H; a.D = D; a.HD = m->HD;
@@ -1051,6 +1072,7 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
         if (fold) use_fold(ep, Lw.pw1_cs);
         if (fuse_dw) {
             ep.D = D; ep.nq = n; ep.ids = ids; ep.pos = p->pos;
+            ep.n_streams = p->S; ep.status = p->status;
             ep.dw_ring = conv_l; ep.dw_sstride = p->conv_sstride;
             ep.dw_wT = Lw.dwT; ep.dw_bias = Lw.bdw; ep.dw_gamma = Lw.bng; ep.dw_beta = Lw.bnb; ep.dw_out = p->yc;
             ep.dw_rows = M;
@@ -1062,7 +1084,7 @@ int run_layers(cac_pool* p, int nb, int nq, int n_commit, const int* ids, float*
         if (!fuse_dw) {
             PB(P_DW);
             CK(launch_dwconv(p->glu, conv_l, p->conv_sstride, ids, p->pos, n, n_commit, Lw.dwT, Lw.bdw, Lw.bng,
-                             Lw.bnb, p->yc, D, nb, bf, s));
+                             Lw.bnb, p->yc, D, nb, bf, s, p->S, p->status));
             PE();
             ++*lc;
         }
@@ -1167,7 +1189,7 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
     }
     RET(rc);
     PB(P_ADV);
-    CK(launch_advance(p->pos, ids, nb, n, s));
+    CK(launch_advance(p->pos, ids, nb, n, s, p->S, p->status));
     PE();
     ++p->launches;
     return CAC_OK;
@@ -1181,14 +1203,14 @@ int run_step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride
 int run_pass(cac_pool* p, int nbp, int P, int E, float* enc, float* joint, cudaStream_t s) {
     cac_model* m = p->m;
     const int D = m->D;
-    CK(launch_x0_gather(p->x0, p->x, p->pids_dev, p->pos, nbp, P, p->XC, D, s));
+    CK(launch_x0_gather(p->x0, p->x, p->pids_dev, p->pos, nbp, P, p->XC, D, s, p->S, p->status));
     ++p->launches;
     RET(run_layers(p, nbp, P, E, p->pids_dev, nullptr, 0, 0, s));
     // compact the emitted rows: fp32 frames to the caller, activation copy for the joint
     CK(launch_emit_rows(p->x, p->xln, enc, p->o, p->pmap_dev, nbp, P, E, D, m->bf16, s));
     ++p->launches;
     if (joint) RET(run_joint(p, p->o, nbp * E, E, joint, 1, 0, p->pmap_dev, s));
-    CK(launch_advance(p->pos, p->pids_dev, nbp, E, s));
+    CK(launch_advance(p->pos, p->pids_dev, nbp, E, s, p->S, p->status));
     ++p->launches;
     return CAC_OK;
 }
@@ -1303,8 +1325,8 @@ extern "C" int cac_pool_create(cac_model* m, int max_streams, int max_frames_per
     p->pos = static_cast<int*>(v);
     if ((r = palloc(p, sizeof(float) * S * p->tail_elems, &v)) != CAC_OK) return fail(r);
     p->tail = static_cast<float*>(v);
-    if ((r = palloc(p, ab * S * p->ring_sstride, &p->kring)) != CAC_OK) return fail(r);
-    if ((r = palloc(p, ab * S * p->ring_sstride, &p->vring)) != CAC_OK) return fail(r);
+    if ((r = palloc_guarded(p, ab * S * p->ring_sstride, &p->kring)) != CAC_OK) return fail(r);
+    if ((r = palloc_guarded(p, ab * S * p->ring_sstride, &p->vring)) != CAC_OK) return fail(r);
     if (m->bf16 && HD == 64 && p->R <= 80) {
         // tensor maps of the tensor-core attention: one copy = one head's ring of
         // one stream and layer (R rows), or one head's position table (NR rows)
@@ -1318,7 +1340,7 @@ extern "C" int cac_pool_create(cac_model* m, int max_streams, int max_frames_per
             am.p = m->layers[l].Pmap;
         }
     }
-    if ((r = palloc(p, ab * S * p->conv_sstride, &p->conv)) != CAC_OK) return fail(r);
+    if ((r = palloc_guarded(p, ab * S * p->conv_sstride, &p->conv)) != CAC_OK) return fail(r);
     const size_t wsp = m->split ? 2 : 1;  // split windows: rows hi | lo
     // scratch for Ss streams of rows_per rows each
     auto alloc_scratch = [&](int Ss, Scratch& sc) -> int {
@@ -1385,7 +1407,7 @@ extern "C" int cac_pool_create(cac_model* m, int max_streams, int max_frames_per
         if (c.emit_frames + c.lookahead_frames + p->nmax > p->XC || c.emit_frames % 2) return fail(CAC_E_UNSUPPORTED);
         if ((r = palloc(p, sizeof(int) * S, &v)) != CAC_OK) return fail(r);
         p->sub_pos = static_cast<int*>(v);
-        if ((r = palloc(p, sizeof(float) * S * p->XC * D, &v)) != CAC_OK) return fail(r);
+        if ((r = palloc_guarded(p, sizeof(float) * S * p->XC * D, &v)) != CAC_OK) return fail(r);
         p->x0 = static_cast<float*>(v);
         if ((r = palloc(p, sizeof(int) * S, &v)) != CAC_OK) return fail(r);
         p->pids_dev = static_cast<int*>(v);
@@ -1465,11 +1487,11 @@ extern "C" int cac_stream_reset(cac_pool* p, int n, const int* ids, void* stream
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     RET(upload_ids(p, ids, n, p->rids_dev, s));
     PB(P_RESET);
-    CK(launch_set_pos(p->pos, p->rids_dev, n, 0, s));
+    CK(launch_set_pos(p->pos, p->rids_dev, n, 0, s, p->S, p->status));
     PE();
     ++p->launches;
     if (p->sub_pos) {
-        CK(launch_set_pos(p->sub_pos, p->rids_dev, n, 0, s));
+        CK(launch_set_pos(p->sub_pos, p->rids_dev, n, 0, s, p->S, p->status));
         ++p->launches;
     }
     for (int i = 0; i < n; ++i) {
@@ -1490,8 +1512,8 @@ int prov_subsample(cac_pool* p, int nb, int frames, const float* mel, long long 
                    cudaStream_t s) {
     if (frames > p->nmax) return CAC_E_INVAL;
     RET(run_subsample(p, nb, frames, mel, mel_bstride, nvalid, p->ids_dev, p->sub_pos, s));
-    CK(launch_x0_store(p->x, p->x0, p->ids_dev, p->sub_pos, nb, frames, p->XC, p->m->D, s));
-    CK(launch_advance(p->sub_pos, p->ids_dev, nb, frames, s));
+    CK(launch_x0_store(p->x, p->x0, p->ids_dev, p->sub_pos, nb, frames, p->XC, p->m->D, s, p->S, p->status));
+    CK(launch_advance(p->sub_pos, p->ids_dev, nb, frames, s, p->S, p->status));
     p->launches += 2;
     return CAC_OK;
 }
@@ -2160,6 +2182,20 @@ extern "C" int cac_pool_set_graphs(cac_pool* p, int enable) {
 
 extern "C" long long cac_pool_launch_count(cac_pool* p) { return p ? p->launches : -1; }
 
+extern "C" int cac_pool_check_guards(cac_pool* p) {
+    if (!p) return CAC_E_INVAL;
+    CK(cudaDeviceSynchronize());
+    std::vector<unsigned char> h(GUARD_BYTES);
+    for (char* g : p->guards) {
+        CK(cudaMemcpy(h.data(), g, GUARD_BYTES, cudaMemcpyDeviceToHost));
+        for (unsigned char b : h)
+            if (b != 0xFF) return CAC_E_BOUNDS;
+    }
+    return CAC_OK;
+}
+
+extern "C" int cac_build_checked(void) { return kChecked ? 1 : 0; }
+
 extern "C" int cac_pool_sub_batches(cac_pool* p, int n_streams, int n_frames) {
     if (!p || n_streams < 1 || n_streams > p->S || n_frames < 1) return CAC_E_INVAL;
     if (p->m->cfg.right_context > 0) return 1;
@@ -2260,6 +2296,7 @@ extern "C" const char* cac_strerror(int code) {
         case CAC_E_NONFINITE: return "non-finite value in input mel";
         case CAC_E_TIMEOUT: return "bounded device wait gave up";
         case CAC_E_UNSUPPORTED: return "configuration not supported by these kernels";
+        case CAC_E_BOUNDS: return "index out of range (checked build) or a pool guard zone overwritten";
         case CAC_E_LIMIT: return "request needs more scratch than the fixed CAC_NOALLOC_SCRATCH_BYTES array";
     }
     return "unknown error";

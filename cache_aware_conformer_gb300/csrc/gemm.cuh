@@ -93,6 +93,10 @@ struct EpiParams {
     int xs_lo = 0;
     float2* stats_out = nullptr;
     int stats_parts = 0;
+    // checked build: ids index n_streams streams and positions are >= 0; a
+    // violation latches CAC_E_BOUNDS in status and the row is not written
+    int n_streams = 1 << 30;
+    int* status = nullptr;
 };
 
 // host helpers ---------------------------------------------------------------
@@ -282,8 +286,23 @@ __device__ __forceinline__ void ln_fold32(const EpiParams& e, int col0, const Ep
     }
 }
 
+// mean and rstd of a row's LayerNorm (folded into the GEMM) from the partials
+// at ln_stats; (0, 1) when there is none.
+__device__ __forceinline__ float2 epi_row_stats(const EpiParams& e, int row) {
+    float2 r = make_float2(0.f, 1.f);
+    if (e.ln_stats && row < e.ln_rows) ln_row_stats(e.ln_stats + (long long)row * e.ln_parts, e.ln_parts, r.x, r.y);
+    return r;
+}
+
+__device__ __forceinline__ void epi_apply_stats(float2 st, EpiPre& pre) {
+    pre.ln_mean = st.x;
+    pre.ln_rstd = st.y;
+}
+
+// stats = false: the caller supplies the row's LayerNorm statistics later
+// through epi_apply_stats (computed once per row elsewhere).
 template <int KIND>
-__device__ __forceinline__ void epi_prefetch(const EpiParams& e, int row, int col0, EpiPre& pre) {
+__device__ __forceinline__ void epi_prefetch(const EpiParams& e, int row, int col0, EpiPre& pre, bool stats = true) {
     if (e.bias) {
         const float4* b4 = reinterpret_cast<const float4*>(e.bias + col0);
 #pragma unroll
@@ -304,14 +323,31 @@ __device__ __forceinline__ void epi_prefetch(const EpiParams& e, int row, int co
     } else {
         pre.ln_mean = 0.f;
         pre.ln_rstd = 1.f;
-        if (e.ln_stats && row < e.ln_rows)
-            ln_row_stats(e.ln_stats + (long long)row * e.ln_parts, e.ln_parts, pre.ln_mean, pre.ln_rstd);
+        if (stats && e.ln_stats && row < e.ln_rows) epi_apply_stats(epi_row_stats(e, row), pre);
         if constexpr (KIND == EPI_GLUDW) {
             pre.dw_id = 0;
             pre.dw_p0 = 0;
             if (row < e.dw_rows) {
                 pre.dw_id = e.ids[row / e.nq];
-                pre.dw_p0 = e.pos[pre.dw_id];
+                if (!in_range(pre.dw_id, e.n_streams, e.status)) {
+                    pre.dw_id = -1;  // checked build: the row is skipped
+                } else {
+                    pre.dw_p0 = e.pos[pre.dw_id];
+                    if (!in_range(pre.dw_p0, 1 << 30, e.status)) {
+                        pre.dw_id = -1;
+                    } else {
+                        // warm L2 with the conv-ring rows the epilogue reads (written a
+                        // step ago, usually evicted since); this runs during the main loop
+                        const int fi = row % e.nq;
+                        const bf16* ring = static_cast<const bf16*>(e.dw_ring) + (long long)pre.dw_id * e.dw_sstride +
+                                           (col0 >> 1);
+                        for (int d = fi + 1; d <= 8; ++d) {
+                            const int pabs = pre.dw_p0 + fi - d;
+                            if (pabs >= 0)
+                                asm volatile("prefetch.global.L2 [%0];" ::"l"(ring + (long long)(pabs & 7) * e.D));
+                        }
+                    }
+                }
             }
         }
     }
@@ -406,7 +442,14 @@ __device__ __forceinline__ void epilogue32(const EpiParams& e, int row, int col0
         if (live) {
             const int b = row / e.nq, i = row - (row / e.nq) * e.nq;
             id = e.ids[b];
-            slot = (e.pos[id] + i) % e.R;
+            if (!in_range(id, e.n_streams, e.status)) {
+                live = false;  // checked build: the row is skipped
+                id = 0;
+            } else {
+                const int p = e.pos[id];
+                if (!in_range(p, 1 << 30, e.status)) live = false;
+                slot = live ? (p + i) % e.R : 0;
+            }
         }
         TAct* sbase = base + (long long)id * e.ring_sstride;
         if (e.HD >= 32) {
@@ -421,9 +464,14 @@ __device__ __forceinline__ void epilogue32(const EpiParams& e, int row, int col0
         }
     } else if constexpr (KIND == EPI_SUB) {
         const int g = row / e.P, t = row - (row / e.P) * e.P;
-        const bool on = live && t < e.T_out;  // seam rows spanning two groups are not written
+        bool on = live && t < e.T_out;  // seam rows spanning two groups are not written
         bool zero = false;
-        if (on && e.ids) zero = (e.tmult * e.pos[e.ids[g]] - e.toff + t) < 0;
+        if (on && e.ids) {
+            if (in_range(e.ids[g], e.n_streams, e.status))
+                zero = (e.tmult * e.pos[e.ids[g]] - e.toff + t) < 0;
+            else
+                on = false;  // checked build: the row is skipped
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = zero ? 0.f : fmaxf(v[i], 0.f);
         TAct* dst = reinterpret_cast<TAct*>(e.out_act) + ((long long)g * e.dst_rows + e.dst_off + t) * e.ldo + col0;
@@ -442,6 +490,7 @@ __device__ __forceinline__ void epilogue_gludw(const EpiParams& e, int row, bool
                                                const EpiPre& pre) {
     const int lane = threadIdx.x & 31;
     const int D = e.D, C = col0 >> 1, nq = e.nq;
+    if (kChecked && pre.dw_id < 0) live = false;  // an id or position out of range (latched)
     if (e.ln_stats) ln_fold32(e, col0, pre, v);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {

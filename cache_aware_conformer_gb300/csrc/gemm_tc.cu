@@ -47,7 +47,7 @@ struct TcCfg {
     static constexpr int A_TILES = A_TILE * (1 + SPLIT);
     static constexpr int STAGE = A_TILES + B_TILE;
     static constexpr int STAGES = SPLIT ? ((BN == 256) ? 3 : (BN == 128 ? 4 : 5)) : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
-    static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/;
+    static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/ + BM * 8 /*row stats*/;
     static_assert(STAGES * STAGE >= BN * BM * 4, "split-K partial tile must fit the pipeline buffers");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -68,6 +68,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint64_t* empty = full + C::STAGES;
     uint64_t* accb = empty + C::STAGES;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
+    // LayerNorm statistics of the tile's rows, computed once per row by warps
+    // 2-5 while the main loop runs (warps 0 and 1 are busy in it)
+    float2* rowstat = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(full) + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
@@ -153,9 +156,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int row = m0 + rloc;
     const int c_first = half * (BN / 2);
     EpiPre pre;
-    if (crank == 0 && (row < M || KIND == EPI_GLUDW)) epi_prefetch<KIND>(ep, row, n0 + c_first, pre);
+    const bool row_stats = ep.ln_stats != nullptr && crank == 0;
+    if (crank == 0 && (row < M || KIND == EPI_GLUDW)) epi_prefetch<KIND>(ep, row, n0 + c_first, pre, !row_stats);
+    if (row_stats && warp >= 2 && warp < 6) rowstat[(warp - 2) * 32 + lane] = epi_row_stats(ep, m0 + (warp - 2) * 32 + lane);
 
     if (!mbar_wait(accb, 0)) ok = false;
+    if (row_stats) {
+        __syncthreads();  // the row statistics are in shared memory
+        if (row < M || KIND == EPI_GLUDW) epi_apply_stats(rowstat[rloc], pre);
+    }
     pdl_trigger();  // main loop done: let the next kernel launch while the epilogue runs
     tc_fence_after();
     // partial tile [BN columns][128 rows] fp32 in the pipeline buffers (idle now)
@@ -182,13 +191,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int k = 0; k < 32; ++k) v[k] += ld_dsmem(&part[(c + k) * BM + rloc], (uint32_t)rr);
             }
             if constexpr (KIND == EPI_GLUDW) {
-                if (c != c_first) epi_prefetch<KIND>(ep, row, n0 + c, pre);  // bias only: any row
+                if (c != c_first) {  // bias only: any row
+                    epi_prefetch<KIND>(ep, row, n0 + c, pre, !row_stats);
+                    if (row_stats) epi_apply_stats(rowstat[rloc], pre);
+                }
                 epilogue_gludw(ep, row, ok && row < M, n0 + c, v, pre);
             } else {
                 // every lane: the row stores go through this warp's slice of the
                 // (idle) B ring
                 const bool live = ok && row < M;
-                if (c != c_first && live) epi_prefetch<KIND>(ep, row, n0 + c, pre);
+                if (c != c_first && live) {
+                    epi_prefetch<KIND>(ep, row, n0 + c, pre, !row_stats);
+                    if (row_stats) epi_apply_stats(rowstat[rloc], pre);
+                }
                 epilogue32<KIND, TAct>(ep, row, n0 + c, v, pre, stage, live);
             }
         }

@@ -226,12 +226,13 @@ __device__ __forceinline__ void put_win(T* row, int c, float v, int split) {
 template <class T>
 __global__ void __launch_bounds__(256) stage_mel_kernel(const float* mel, long long mel_bstride, const int* n_valid,
                                                         T* win, float* tail, const int* ids, const int* pos, int n,
-                                                        int split, int* status) {
+                                                        int split, int* status, int S) {
     __shared__ float ntail[TAIL * MEL];
     pdl_trigger();
     pdl_wait();
     const int b = blockIdx.x;
     const int id = ids[b];
+    if (!in_range(id, S, status)) return;
     const bool first = pos[id] == 0;
     const int W = TAIL + 8 * n;
     const int RW = MEL * (1 + split);
@@ -258,14 +259,14 @@ __global__ void __launch_bounds__(256) stage_mel_kernel(const float* mel, long l
 
 cudaError_t launch_stage_mel(const float* mel, long long mel_bstride, const int* n_valid, void* win, float* tail,
                              const int* ids, const int* pos, int n, int nb, int act_bf16, int split, int* status,
-                             cudaStream_t s) {
+                             cudaStream_t s, int S) {
     if (nb <= 0) return cudaSuccess;
     if (split && !act_bf16) return cudaErrorInvalidValue;
     if (act_bf16)
         return launch_k(stage_mel_kernel<bf16>, dim3(nb), dim3(256), 0, s, 1, mel, mel_bstride, n_valid,
-                        static_cast<bf16*>(win), tail, ids, pos, n, split, status);
+                        static_cast<bf16*>(win), tail, ids, pos, n, split, status, S);
     return launch_k(stage_mel_kernel<float>, dim3(nb), dim3(256), 0, s, 1, mel, mel_bstride, n_valid,
-                    static_cast<float*>(win), tail, ids, pos, n, 0, status);
+                    static_cast<float*>(win), tail, ids, pos, n, 0, status, S);
 }
 
 template <class T>
@@ -569,7 +570,9 @@ __global__ void __launch_bounds__(SPB * WPS * 32) attn_stream_kernel(AttnParams 
     const T* vb = nullptr;
     if (live) {
         id = a.ids[b];
+        if (!in_range(id, a.n_streams, status)) id = 0;  // checked build: latched, stay in bounds
         p0 = a.pos[id];
+        if (!in_range(p0, 1 << 30, status)) p0 = 0;
         Lc = min(p0, a.left);
         Nk = min(Lc + a.nq, NK);
         s0 = (p0 - Lc) % a.R;
@@ -729,7 +732,7 @@ template <class T>
 __global__ void __launch_bounds__(256) dwconv_kernel(const T* glu, T* cache, long long cs_stride, const int* ids,
                                                      const int* pos, int nq, int n_commit, const float* wT,
                                                      const float* bdw, const float* bng, const float* bnb, T* out,
-                                                     int D, int nb) {
+                                                     int D, int nb, int S, int* status) {
     const long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
     const int b = (int)(idx / D), c = (int)(idx % D);
     float w[9];
@@ -744,7 +747,9 @@ __global__ void __launch_bounds__(256) dwconv_kernel(const T* glu, T* cache, lon
     T* cs = nullptr;
     if (cache) {
         const int id = ids[b];
+        if (!in_range(id, S, status)) return;
         p0 = pos[id];
+        if (!in_range(p0, 1 << 30, status)) return;
         cs = cache + (long long)id * cs_stride;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -801,7 +806,7 @@ __global__ void __launch_bounds__(256) dwconv_offline_kernel(const T* glu, int T
 
 cudaError_t launch_dwconv(const void* glu, void* cache, long long cs_stride, const int* ids, const int* pos, int nq,
                           int n_commit, const float* wT, const float* bdw, const float* bng, const float* bnb,
-                          void* out, int D, int nb, int act_bf16, cudaStream_t s) {
+                          void* out, int D, int nb, int act_bf16, cudaStream_t s, int S, int* status) {
     if (nb <= 0) return cudaSuccess;
     if (!cache && D % 2 == 0) {
         const long long pairs = (long long)nb * nq * (D / 2);
@@ -817,17 +822,17 @@ cudaError_t launch_dwconv(const void* glu, void* cache, long long cs_stride, con
     if (act_bf16)
         return launch_k(dwconv_kernel<bf16>, dim3(blocks), dim3(256), 0, s, 1, static_cast<const bf16*>(glu),
                         static_cast<bf16*>(cache), cs_stride, ids, pos, nq, n_commit, wT, bdw, bng, bnb,
-                        static_cast<bf16*>(out), D, nb);
+                        static_cast<bf16*>(out), D, nb, S, status);
     return launch_k(dwconv_kernel<float>, dim3(blocks), dim3(256), 0, s, 1, static_cast<const float*>(glu),
                     static_cast<float*>(cache), cs_stride, ids, pos, nq, n_commit, wT, bdw, bng, bnb,
-                    static_cast<float*>(out), D, nb);
+                    static_cast<float*>(out), D, nb, S, status);
 }
 
 // ---------------------------------------------------------------------------
 // provisional tail: x0 ring and emitted rows (float4 per thread)
 // ---------------------------------------------------------------------------
 __global__ void x0_store_kernel(const float* x, float* x0, const int* ids, const int* pos, int nb, int n, int XC,
-                                int D) {
+                                int D, int S, int* status) {
     pdl_wait();
     const int D4 = D / 4;
     const long long total = (long long)nb * n * D4;
@@ -837,13 +842,14 @@ __global__ void x0_store_kernel(const float* x, float* x0, const int* ids, const
         const long long r = e / D4;
         const int b = (int)(r / n), i = (int)(r % n);
         const int id = ids[b];
+        if (!in_range(id, S, status) || !in_range(pos[id], 1 << 30, status)) continue;
         const int slot = (pos[id] + i) % XC;
         reinterpret_cast<float4*>(x0 + ((long long)id * XC + slot) * D)[c] = reinterpret_cast<const float4*>(x + r * D)[c];
     }
 }
 
 __global__ void x0_gather_kernel(const float* x0, float* x, const int* ids, const int* pos, int nb, int P, int XC,
-                                 int D) {
+                                 int D, int S, int* status) {
     pdl_wait();
     const int D4 = D / 4;
     const long long total = (long long)nb * P * D4;
@@ -853,6 +859,7 @@ __global__ void x0_gather_kernel(const float* x0, float* x, const int* ids, cons
         const long long r = e / D4;
         const int b = (int)(r / P), i = (int)(r % P);
         const int id = ids[b];
+        if (!in_range(id, S, status) || !in_range(pos[id], 1 << 30, status)) continue;
         const int slot = (pos[id] + i) % XC;
         reinterpret_cast<float4*>(x + r * D)[c] = reinterpret_cast<const float4*>(x0 + ((long long)id * XC + slot) * D)[c];
     }
@@ -877,16 +884,16 @@ __global__ void emit_rows_kernel(const float* x, const T* act_src, float* dst, T
 static int grid_for(long long work) { return (int)std::min<long long>((work + 255) / 256, 152 * 8); }
 
 cudaError_t launch_x0_store(const float* x, float* x0, const int* ids, const int* pos, int nb, int n, int XC, int D,
-                            cudaStream_t s) {
+                            cudaStream_t s, int S, int* status) {
     if (nb <= 0 || n <= 0) return cudaSuccess;
     return launch_k(x0_store_kernel, dim3(grid_for((long long)nb * n * D / 4)), dim3(256), 0, s, 1, x, x0, ids, pos,
-                    nb, n, XC, D);
+                    nb, n, XC, D, S, status);
 }
 cudaError_t launch_x0_gather(const float* x0, float* x, const int* ids, const int* pos, int nb, int P, int XC, int D,
-                             cudaStream_t s) {
+                             cudaStream_t s, int S, int* status) {
     if (nb <= 0 || P <= 0) return cudaSuccess;
     return launch_k(x0_gather_kernel, dim3(grid_for((long long)nb * P * D / 4)), dim3(256), 0, s, 1, x0, x, ids, pos,
-                    nb, P, XC, D);
+                    nb, P, XC, D, S, status);
 }
 cudaError_t launch_emit_rows(const float* x, const void* act_src, float* dst, void* act_dst, const int* map, int nb,
                              int P, int E, int D, int act_bf16, cudaStream_t s) {
@@ -902,26 +909,34 @@ cudaError_t launch_emit_rows(const float* x, const void* act_src, float* dst, vo
 // ---------------------------------------------------------------------------
 // bookkeeping and small utilities
 // ---------------------------------------------------------------------------
-__global__ void advance_kernel(int* pos, const int* ids, int nb, int n) {
+__global__ void advance_kernel(int* pos, const int* ids, int nb, int n, int S, int* status) {
     pdl_trigger();
     pdl_wait();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b < nb) pos[ids[b]] += n;
+    if (b < nb && in_range(ids[b], S, status)) pos[ids[b]] += n;
 }
-__global__ void set_pos_kernel(int* pos, const int* ids, int nb, int value) {
+__global__ void set_pos_kernel(int* pos, const int* ids, int nb, int value, int S, int* status) {
     pdl_trigger();
     pdl_wait();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b < nb) pos[ids[b]] = value;
+    if (b < nb && in_range(ids[b], S, status)) pos[ids[b]] = value;
 }
 
-cudaError_t launch_advance(int* pos, const int* ids, int nb, int n, cudaStream_t s) {
-    if (nb <= 0) return cudaSuccess;
-    return launch_k(advance_kernel, dim3((nb + 255) / 256), dim3(256), 0, s, 1, pos, ids, nb, n);
+// Self-test of the checked build's index checks: thread t would write buf[t]
+// for t < n_threads, but buf holds only n_valid floats; the check keeps every
+// access in bounds and latches CAC_E_BOUNDS for the others.
+__global__ void bounds_selftest_kernel(float* buf, int n_valid, int* status) {
+    const int t = threadIdx.x;
+    if (in_range(t, n_valid, status)) buf[t] = (float)t;
 }
-cudaError_t launch_set_pos(int* pos, const int* ids, int nb, int value, cudaStream_t s) {
+
+cudaError_t launch_advance(int* pos, const int* ids, int nb, int n, cudaStream_t s, int S, int* status) {
     if (nb <= 0) return cudaSuccess;
-    return launch_k(set_pos_kernel, dim3((nb + 255) / 256), dim3(256), 0, s, 1, pos, ids, nb, value);
+    return launch_k(advance_kernel, dim3((nb + 255) / 256), dim3(256), 0, s, 1, pos, ids, nb, n, S, status);
+}
+cudaError_t launch_set_pos(int* pos, const int* ids, int nb, int value, cudaStream_t s, int S, int* status) {
+    if (nb <= 0) return cudaSuccess;
+    return launch_k(set_pos_kernel, dim3((nb + 255) / 256), dim3(256), 0, s, 1, pos, ids, nb, value, S, status);
 }
 
 __global__ void sinusoid_kernel(float* pe, int NR, int rmin, int D) {
@@ -975,3 +990,29 @@ cudaError_t launch_to_f32(const void* src, float* dst, long long n, int src_bf16
 }
 
 }  // namespace cac
+
+extern "C" int cac_op_bounds_selftest(void* stream) {
+    using namespace cac;
+    if (!kChecked) return CAC_E_UNSUPPORTED;  // the default build has no checks to exercise
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float* buf = nullptr;
+    int* st = nullptr;
+    if (cudaMalloc(&buf, 32 * sizeof(float)) != cudaSuccess) return CAC_E_NOMEM;
+    if (cudaMalloc(&st, sizeof(int)) != cudaSuccess) {
+        cudaFree(buf);
+        return CAC_E_NOMEM;
+    }
+    int h = CAC_E_CUDA;
+    if (cudaMemsetAsync(st, 0, sizeof(int), s) == cudaSuccess) {
+        bounds_selftest_kernel<<<1, 64, 0, s>>>(buf, 32, st);
+        if (cudaGetLastError() == cudaSuccess && cudaMemcpyAsync(&h, st, sizeof(int), cudaMemcpyDeviceToHost, s) ==
+                                                     cudaSuccess &&
+            cudaStreamSynchronize(s) == cudaSuccess) {
+        } else {
+            h = CAC_E_CUDA;
+        }
+    }
+    cudaFree(buf);
+    cudaFree(st);
+    return h;
+}

@@ -23,7 +23,7 @@ cudaError_t launch_layernorm(const float* x, int M, int D, const float* g1, cons
 // Latches CAC_E_NONFINITE on a non-finite mel value.
 cudaError_t launch_stage_mel(const float* mel, long long mel_bstride, const int* n_valid, void* win, float* tail,
                              const int* ids, const int* pos, int n, int nb, int act_bf16, int split, int* status,
-                             cudaStream_t s);
+                             cudaStream_t s, int S = 1 << 30);
 
 // Offline staging: dst[b] = [2 zero rows | mel[b] (rows >= len[b] zero) | pad to W rows],
 // rows as in launch_stage_mel.
@@ -64,6 +64,7 @@ struct AttnParams {
     int T = 0;                  // offline: frames per sequence (row stride between sequences)
     const int* seq_len = nullptr;  // offline: valid frames per sequence
     float scale = 1.f;
+    int n_streams = 1 << 30;    // streaming (checked build): ids index this many streams
 };
 
 // A bounded wait on the K/V copies that gives up latches CAC_E_TIMEOUT in *status.
@@ -90,7 +91,8 @@ cudaError_t launch_attention_offline(const AttnParams& a, int act_bf16, int* sta
 // nq = frames per sequence, b indexes sequences directly.
 cudaError_t launch_dwconv(const void* glu, void* cache, long long cs_stride, const int* ids, const int* pos, int nq,
                           int n_commit, const float* wT, const float* bdw, const float* bng, const float* bnb,
-                          void* out, int D, int nb, int act_bf16, cudaStream_t s);
+                          void* out, int D, int nb, int act_bf16, cudaStream_t s, int S = 1 << 30,
+                          int* status = nullptr);
 
 // Provisional tail: the exact subsampled frames that wait to be emitted live
 // in a per-stream ring x0[id][XC][D] (fp32), slot = absolute frame mod XC.
@@ -99,15 +101,18 @@ cudaError_t launch_dwconv(const void* glu, void* cache, long long cs_stride, con
 // emit:   dst[map[b] + i] = x[b * P + i] (map[b] = output row of the first) and
 //         act_dst[b * E + i] = act_src[b * P + i]              (i < E)
 cudaError_t launch_x0_store(const float* x, float* x0, const int* ids, const int* pos, int nb, int n, int XC, int D,
-                            cudaStream_t s);
+                            cudaStream_t s, int S = 1 << 30, int* status = nullptr);
 cudaError_t launch_x0_gather(const float* x0, float* x, const int* ids, const int* pos, int nb, int P, int XC, int D,
-                             cudaStream_t s);
+                             cudaStream_t s, int S = 1 << 30, int* status = nullptr);
 cudaError_t launch_emit_rows(const float* x, const void* act_src, float* dst, void* act_dst, const int* map, int nb,
                              int P, int E, int D, int act_bf16, cudaStream_t s);
 
 // pos[ids[b]] += n  /  pos[ids[b]] = value
-cudaError_t launch_advance(int* pos, const int* ids, int nb, int n, cudaStream_t s);
-cudaError_t launch_set_pos(int* pos, const int* ids, int nb, int value, cudaStream_t s);
+// S, status (checked build): ids index S streams; an id outside latches CAC_E_BOUNDS
+cudaError_t launch_advance(int* pos, const int* ids, int nb, int n, cudaStream_t s, int S = 1 << 30,
+                           int* status = nullptr);
+cudaError_t launch_set_pos(int* pos, const int* ids, int nb, int value, cudaStream_t s, int S = 1 << 30,
+                           int* status = nullptr);
 
 // pe[r][2m] = sin(r w_m), pe[r][2m+1] = cos(r w_m), w_m = 10000^(-2m/D), r = rmin + row
 cudaError_t launch_sinusoid(float* pe, int NR, int rmin, int D, cudaStream_t s);

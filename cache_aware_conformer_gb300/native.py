@@ -15,7 +15,10 @@ import numpy as np
 
 from .config import ModelConfig, DTYPE_BF16, MEL_TAIL
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcac.so")
+# CAC_LIB=checked selects the CAC_CHECKED build (libcac_checked.so, built with
+# build.build(checked=True)); the default build otherwise.
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                        "libcac_checked.so" if os.environ.get("CAC_LIB") == "checked" else "libcac.so")
 
 CAC_OK = 0
 ERRORS = {-1: "CAC_E_INVAL", -2: "CAC_E_ALIGN", -3: "CAC_E_STATE", -4: "CAC_E_NOMEM", -5: "CAC_E_CUDA",
@@ -27,7 +30,8 @@ SYMBOLS = ["cac_weights_size", "cac_model_create", "cac_model_destroy", "cac_poo
            "cac_stream_create", "cac_stream_destroy", "cac_stream_reset", "cac_stream_push", "cac_stream_push_host",
            "cac_stream_flush", "cac_stream_flush_frames", "cac_encode_offline", "cac_stream_get_state",
            "cac_stream_set_state", "cac_pool_check", "cac_model_check", "cac_pool_set_graphs",
-           "cac_pool_launch_count", "cac_pool_set_chains", "cac_pool_sub_batches", "cac_pool_set_trace", "cac_pool_read_trace", "cac_pool_set_profile",
+           "cac_pool_launch_count", "cac_pool_set_chains", "cac_pool_sub_batches", "cac_pool_check_guards",
+           "cac_build_checked", "cac_op_bounds_selftest", "cac_pool_set_trace", "cac_pool_read_trace", "cac_pool_set_profile",
            "cac_pool_read_profile", "cac_profile_classes", "cac_profile_class_name", "cac_strerror",
            "cac_op_gemm_bf16", "cac_encode_offline_noalloc",
            # include/cac_decode.h
@@ -97,6 +101,9 @@ def _lib():
             "cac_pool_launch_count": (c_longlong, [vp]),
             "cac_pool_set_chains": (c_int, [vp, c_int]),
             "cac_pool_sub_batches": (c_int, [vp, c_int, c_int]),
+            "cac_pool_check_guards": (c_int, [vp]),
+            "cac_build_checked": (c_int, []),
+            "cac_op_bounds_selftest": (c_int, [vp]),
             "cac_pool_set_trace": (c_int, [vp, c_int]),
             "cac_pool_read_trace": (c_int, [vp, c_int, c_int, fp, c_size_t]),
             "cac_pool_set_profile": (c_int, [vp, c_int]),
@@ -375,6 +382,10 @@ class Pool:
         _check(min(r, 0), "cac_pool_sub_batches")
         return r
 
+    def check_guards(self):
+        """Raise CacError(CAC_E_BOUNDS) when a kernel wrote into a pool guard zone."""
+        _check(_lib().cac_pool_check_guards(self.h), "cac_pool_check_guards")
+
     def set_chains(self, on: bool):
         """Chained steps (default) or one launch per projection (cac_pool_set_chains)."""
         _check(_lib().cac_pool_set_chains(self.h, 1 if on else 0), "cac_pool_set_chains")
@@ -413,6 +424,18 @@ def gemm_palette(A, packed, table, bias=None, out=None, status=None, stream=None
     _check(_lib().cac_op_gemm_palette(M, N, K, _ptr(A), _ptr(packed), _ptr(table), _ptr(bias), _ptr(out),
                                       _ptr(status), _stream(stream)), "cac_op_gemm_palette")
     return out
+
+
+def build_checked() -> bool:
+    """True when the loaded library is the CAC_CHECKED build."""
+    return bool(_lib().cac_build_checked())
+
+
+def bounds_selftest(stream=None) -> int:
+    """Status latched by the checked build's index check on an out-of-range
+    index (cac_op_bounds_selftest): CAC_E_BOUNDS (-11); CAC_E_UNSUPPORTED (-9)
+    in the default build."""
+    return int(_lib().cac_op_bounds_selftest(_stream(stream)))
 
 
 def wait_selftest(which: int, stream=None) -> int:

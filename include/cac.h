@@ -58,6 +58,8 @@ extern "C" {
 #define CAC_E_TIMEOUT  -8   /* a bounded device-side wait gave up */
 #define CAC_E_UNSUPPORTED -9 /* configuration outside what the kernels implement */
 #define CAC_E_LIMIT    -10  /* request larger than the fixed scratch of cac_encode_offline_noalloc */
+#define CAC_E_BOUNDS   -11  /* an index outside its buffer: caught (and the access skipped) by the checked
+                               build, or a pool guard zone found overwritten (cac_pool_check_guards) */
 
 #define CAC_DTYPE_F32  0    /* everything fp32 (SIMT GEMMs) */
 #define CAC_DTYPE_BF16 1    /* bf16 weights, GEMM operands and caches; fp32 accumulation,
@@ -281,6 +283,19 @@ int  cac_pool_set_profile(cac_pool* p, int enable);
 int  cac_pool_read_profile(cac_pool* p, int n_classes, double* total_ms, long long* launches);
 int  cac_profile_classes(void);
 const char* cac_profile_class_name(int cls);
+
+/* Guard zones: every per-stream device pool (K/V rings, conv ring, provisional
+ * x0 ring) sits between two 4 KiB zones filled with NaN bit patterns at pool
+ * creation.  Synchronizes the device and returns CAC_OK when all zones are
+ * intact, CAC_E_BOUNDS when a kernel wrote into one. */
+int  cac_pool_check_guards(cac_pool* p);
+
+/* 1 when this library was built with CAC_CHECKED: every kernel of the
+ * streaming step checks stream ids, positions and ring slots before it uses
+ * them, latches CAC_E_BOUNDS in the status word and skips the access when one
+ * is out of range (a stand-in for a memory checker; no trap, no wait).  0 in
+ * the default build. */
+int  cac_build_checked(void);
 
 const char* cac_strerror(int code);
 

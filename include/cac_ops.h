@@ -54,6 +54,13 @@ int cac_op_gemm_palette(int M, int N, int K, const void* A, const void* packed, 
  * CAC_E_INVAL for another `which`, CAC_E_CUDA if a launch failed. */
 int cac_op_wait_selftest(int which, void* stream);
 
+/* Self-test of the checked build (cac_build_checked() == 1): a kernel whose
+ * threads index past a 32-float buffer runs with the library's index check,
+ * which keeps every access in bounds; returns the status it latched —
+ * CAC_E_BOUNDS as designed.  Synchronous.  CAC_E_UNSUPPORTED in the default
+ * build (nothing is launched). */
+int cac_op_bounds_selftest(void* stream);
+
 #ifdef __cplusplus
 }
 #endif
