@@ -47,13 +47,16 @@ def test_kernel_taps_match_oracle(cfg):
         ref.push(chunk, trace=tr)
         _push(pool, [sid], [chunk])
         pool.check()
+        # the whole-step bars, at every tap and every layer (no growth with
+        # depth): the residual stream keeps a scale of about one, so a kernel
+        # that adds error in a deeper layer fails here as it would in the first
         tol = 1e-4 if cfg.dtype == "fp32" else 3e-2
         assert max_abs(pool.read_trace(0, 7, 4), tr["sub"]) <= tol, ("sub", k)
         for l in range(cfg.n_layers):
             for t, name in enumerate(names):
                 got = pool.read_trace(l, t, 4)
                 d = max_abs(got, tr[name][l])
-                assert d <= tol * (1 + 4 * l), (k, l, name, d)
+                assert d <= tol, (k, l, name, d)
 
 
 # ---------------------------------------------------------------------------
