@@ -87,29 +87,32 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
     return v;
 }
 
-// Grid-wide barrier of a cooperative launch; false when it gave up (timeout or
+// Grid-wide barrier of a cooperative launch.  bar[0] counts the arrivals of
+// the whole launch (zeroed before it): a CTA's k-th barrier is passed once the
+// count reaches k * gridDim.x (`target` carries k * gridDim.x from call to
+// call).  Thread 0 arrives with a release add after the CTA's own barrier and
+// polls with acquire loads; false when it gave up (timeout, latched, or
 // another CTA's abort), in which case the caller returns.
-__device__ bool grid_sync(const BeamParams& d) {
+__device__ bool grid_sync(const BeamParams& d, unsigned& target) {
     __shared__ int ok_s;
     __syncthreads();
+    target += gridDim.x;
     if (threadIdx.x == 0) {
         int ok = 1;
-        const unsigned gen = ld_acquire(&d.bar[1]);
         __threadfence();
-        if (atomicAdd(&d.bar[0], 1u) == gridDim.x - 1) {
-            atomicExch(&d.bar[0], 0u);
-            __threadfence();
-            atomicAdd(&d.bar[1], 1u);
-        } else {
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(d.bar) : "memory");
+        if (ld_acquire(d.bar) < target) {
             const long long t0 = clock64();
-            for (unsigned it = 0;; ++it) {
-                if (ld_acquire(&d.bar[1]) != gen) break;
-                if (*(volatile int*)d.abort_flag) { ok = 0; break; }
-                if ((it & 63u) == 63u && clock64() - t0 > (1ll << 31)) {
-                    latch_error(d.status, CAC_E_TIMEOUT);
-                    atomicExch(d.abort_flag, 1);
-                    ok = 0;
-                    break;
+            for (unsigned it = 1;; ++it) {
+                if (ld_acquire(d.bar) >= target) break;
+                if ((it & 255u) == 0u) {
+                    if (*(volatile int*)d.abort_flag) { ok = 0; break; }
+                    if (clock64() - t0 > (1ll << 31)) {
+                        latch_error(d.status, CAC_E_TIMEOUT);
+                        atomicExch(d.abort_flag, 1);
+                        ok = 0;
+                        break;
+                    }
                 }
             }
         }
@@ -688,6 +691,7 @@ __device__ void phase_bc(const BeamParams& d, int it, float* wsm) {
 
 // The whole launch (see the top of the file).
 __global__ void __launch_bounds__(BT, 1) beam_step_kernel(BeamParams d) {
+    unsigned gt = 0;  // grid-barrier target
     extern __shared__ float smem[];
     const int Kd = d.P > d.J ? d.P : d.J;
     float* As = smem;
@@ -704,25 +708,25 @@ __global__ void __launch_bounds__(BT, 1) beam_step_kernel(BeamParams d) {
     }
     __syncthreads();
     phase_init(d);
-    if (!grid_sync(d)) return;
+    if (!grid_sync(d, gt)) return;
     if (__ldcg(d.cnt + 1) > 0) {  // predictor states of the stream starts
         phase_lstm(d, 0, As, Ws, Os, red, rt, &tbar, tphase);
-        if (!grid_sync(d)) return;
+        if (!grid_sync(d, gt)) return;
         phase_proj(d, 0, As, Ws, Os, red, rt, &tbar, tphase);
-        if (!grid_sync(d)) return;
+        if (!grid_sync(d, gt)) return;
     }
     int it = 1;
     for (; it <= d.maxit; ++it) {
         if (__ldcg(d.cnt + 2 * it) == 0) break;
         phase_joint(d, it, As, Ws, Os, Ps, red, rt, &tbar, tphase);
-        if (!grid_sync(d)) return;
+        if (!grid_sync(d, gt)) return;
         phase_bc(d, it, smem);
-        if (!grid_sync(d)) return;
+        if (!grid_sync(d, gt)) return;
         if (__ldcg(d.cnt + 2 * it + 1) > 0) {
             phase_lstm(d, it, As, Ws, Os, red, rt, &tbar, tphase);
-            if (!grid_sync(d)) return;
+            if (!grid_sync(d, gt)) return;
             phase_proj(d, it, As, Ws, Os, red, rt, &tbar, tphase);
-            if (!grid_sync(d)) return;
+            if (!grid_sync(d, gt)) return;
         }
     }
     if (it > d.maxit && blockIdx.x == 0 && threadIdx.x == 0 && __ldcg(d.cnt + 2 * it) > 0) *d.pending = 1;

@@ -7,31 +7,41 @@
 //
 // One step decodes n streams over T frames in ONE cooperative launch of a
 // persistent kernel (one 256-thread CTA per SM).  The streams advance in
-// lockstep iterations; each iteration is
-//   A  joint + argmax: logits of every still-active slot at its current frame,
-//      tiled (32 slots x 16 classes) over the CTAs, K = joint_dim, written as
-//      per-tile partial maxima;
-//   B  decisions: per active slot the first maximum over the partials; blank
-//      (or max_symbols reached) moves the slot to its next frame, anything else
-//      is emitted and queued for the predictor;
-//   C  LSTM step of the queued slots, tiled (32 slots x 4 hidden units = 16
-//      gate rows): gates = tab[token] + W_hh h, with tab = emb W_ih^T + b_ih +
-//      b_hh computed once at load (the input half of the gates depends on the
-//      token only), then the cell update in the tile;
-//   D  predictor projection p = W_pred h' + b_pred of the queued slots, tiled
-//      (32 slots x 16 outputs).
-// Every tile stages its rows (weights, and slot rows when its slot tile
-// changes) with one TMA bulk copy per row; the 8 warps split K and reduce
-// their partial tiles through shared memory.
-// h is kept twice per stream ([2][S][P]): a queued emission carries the index
-// of the stream's current copy, phase C reads it and writes the new h into
-// the other one, which becomes current (the index flips when the emission is
-// queued, so phase D reads the new copy and nothing is copied back).
-// Grid-wide barriers separate the phases: an arrival counter and a generation
-// word in global memory, every spin bounded (about a second) after which the
-// kernel latches CAC_E_TIMEOUT, raises an abort word that releases every
-// other waiter, and returns.  Everything is fp32 on the CUDA cores (the pages
-// fix fp32 for the decoder, so every argmax is decided in fp32).
+// lockstep iterations, and every iteration is a short chain of latency-bound
+// phases, so the kernel is built to keep each phase and each hand-off short:
+//
+// * Weights stay on chip.  CTA g owns a slice of the classes (joint rows of
+//   W_out), of the LSTM hidden units (their 4 gate rows of W_hh) and of the
+//   predictor-projection outputs (rows of W_pred); the slices are copied into
+//   shared memory once per launch and every iteration only moves activation
+//   rows (u = ReLU(z + p) for the joint, h for the LSTM, the new h for the
+//   projection).
+// * Rows arrive through a ring of TMA bulk copies: warp w consumes rows w, w +
+//   8, ... and refills the ring slot it just read with the row RB further on,
+//   so up to RB rows per CTA are in flight whatever the number of active slots.
+// * Decisions are replicated.  Phase A ends with one 64-bit atomicMax per
+//   (active slot, CTA): the key packs the logit (as an order-preserving
+//   unsigned) above the complemented class id, so the maximum over the CTAs
+//   is the largest logit with the lowest class on ties, independent of the
+//   order of the atomics.  Every CTA then reads the keys of all active slots
+//   and applies the same decisions to its own shared-memory copy of the slot
+//   state (frame, symbols on the frame, emissions, current h copy, active
+//   list), so no CTA has to publish decisions to the others; the owner of a
+//   slot (slot mod grid) writes its outputs.
+//
+// Iteration: A joint + per-CTA argmax keys | grid barrier | B decisions (all
+// CTAs alike) and C the LSTM step of the emitting slots (gates = tab[token] +
+// W_hh h, tab = emb W_ih^T + b_ih + b_hh computed once at load; the cell
+// update of the CTA's units, new h into the stream's other h copy) | grid
+// barrier (only when something was emitted) | D the predictor projection
+// p = W_pred h' + b_pred of the emitting slots and the next joint inputs u of
+// every slot that stays active (its frame or its p changed) | grid barrier.
+// Grid barriers: an arrival counter and a generation word in global memory,
+// every spin bounded (about a second) after which the kernel latches
+// CAC_E_TIMEOUT, raises an abort word that releases every other waiter, and
+// returns.  Everything is fp32 on the CUDA cores (the pages fix fp32 for the
+// decoder, so every argmax is decided in fp32).
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 #include <cstring>
@@ -45,26 +55,31 @@
 namespace cac {
 namespace {
 
-constexpr int DT = 256;        // threads per CTA
-constexpr int TS = 32;         // slots per tile
-constexpr int TN = 16;         // output columns per tile
-constexpr int OLD = TN + 1;    // row stride of the output tile
+constexpr int DT = 256;         // threads per CTA
+constexpr int NW = DT / 32;     // warps per CTA
+constexpr int MAXCH = 16;       // 64-float chunks per row (pred_dim, joint_dim <= 1024)
+constexpr int RB_MAX = 64;      // ring slots (rows in flight per CTA)
+constexpr int STATE_INTS = 10;  // ints of replicated slot state per stream slot
+
+// floats of the bias slices in shared memory, rounded so that the row ring
+// after them stays 256-byte aligned
+__host__ __device__ constexpr int bias_floats(int nc_max, int no_max) { return (nc_max + no_max + 63) / 64 * 64; }
 
 struct DecParams {
-    int n, T, C, P, J, max_sym, blank, nct, maxit;
+    int n, T, C, P, J, max_sym, blank, maxit, S;
+    int nc_max, nu_max, no_max;  // largest class / hidden-unit / projection-output slice of a CTA
+    int RB;                      // ring slots, a multiple of NW
     const int* ids;
     const float* z;
     long long zb;
     int *tokens, *frames, *counts;
     const float *tab, *whh, *wpp, *bpp, *wout, *bout;
     float *h, *c, *p;
+    float* u;                    // [S][J] joint inputs ReLU(z + p) of the slots
+    unsigned long long* keys;    // [2][S] packed (logit, class) maxima, one parity per iteration
     int* primed;
-    int *frame, *sym, *act, *emk, *emid, *cnt;  // emid: stream id * 2 + current h copy
-    float* pval;
-    int* pidx;
-    int* hsel;  // [S] index of the stream's current h copy
-    int S;
-    unsigned* bar;  // [0] arrivals, [1] generation
+    int* hsel;                   // [S] index of the stream's current h copy
+    unsigned* bar;               // [0] arrivals, [1] generation
     int* abort_flag;
     int* status;
 };
@@ -75,29 +90,32 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
     return v;
 }
 
-// Grid-wide barrier of a cooperative launch; false when it gave up (timeout or
+// Grid-wide barrier of a cooperative launch.  bar[0] counts the arrivals of
+// the whole launch (zeroed before it): a CTA's k-th barrier is passed once the
+// count reaches k * gridDim.x (`target` carries k * gridDim.x from call to
+// call).  Thread 0 arrives with a release add after the CTA's own barrier and
+// polls with acquire loads; false when it gave up (timeout, latched, or
 // another CTA's abort), in which case the caller returns.
-__device__ bool grid_sync(const DecParams& d) {
+__device__ bool grid_sync(const DecParams& d, unsigned& target) {
     __shared__ int ok_s;
     __syncthreads();
+    target += gridDim.x;
     if (threadIdx.x == 0) {
         int ok = 1;
-        const unsigned gen = ld_acquire(&d.bar[1]);
         __threadfence();
-        if (atomicAdd(&d.bar[0], 1u) == gridDim.x - 1) {
-            atomicExch(&d.bar[0], 0u);
-            __threadfence();
-            atomicAdd(&d.bar[1], 1u);
-        } else {
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(d.bar) : "memory");
+        if (ld_acquire(d.bar) < target) {
             const long long t0 = clock64();
-            for (unsigned it = 0;; ++it) {
-                if (ld_acquire(&d.bar[1]) != gen) break;
-                if (*(volatile int*)d.abort_flag) { ok = 0; break; }
-                if ((it & 63u) == 63u && clock64() - t0 > (1ll << 31)) {
-                    latch_error(d.status, CAC_E_TIMEOUT);
-                    atomicExch(d.abort_flag, 1);
-                    ok = 0;
-                    break;
+            for (unsigned it = 1;; ++it) {
+                if (ld_acquire(d.bar) >= target) break;
+                if ((it & 255u) == 0u) {
+                    if (*(volatile int*)d.abort_flag) { ok = 0; break; }
+                    if (clock64() - t0 > (1ll << 31)) {
+                        latch_error(d.status, CAC_E_TIMEOUT);
+                        atomicExch(d.abort_flag, 1);
+                        ok = 0;
+                        break;
+                    }
                 }
             }
         }
@@ -110,352 +128,432 @@ __device__ bool grid_sync(const DecParams& d) {
 
 __device__ __forceinline__ float sigm(float x) { return 1.f / (1.f + expf(-x)); }
 
-// Os[slot][col] = sum_k As[slot][k] * Ws[col][k] for the tile's 32 slots x
-// TN columns.  Warp w takes the K segment [w K/8, (w + 1) K/8) for all 512
-// outputs (lane = slot, 16 independent accumulators, weights broadcast to the
-// warp), so the tile's latency is one segment whatever the number of live
-// slots; the 8 partial tiles are summed through `red` (8 x 512 floats).  K a
-// multiple of 32, rows K + 4 floats apart.
-__device__ __forceinline__ void mac16(int K, const float* As, const float* Ws, float* Os, float* red) {
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, ld = K + 4;
-    const int seg = K / 8, k0 = w * seg;
-    float acc[TN];
+// First index of CTA g's share of `total` items split as evenly as possible.
+__device__ __forceinline__ int slice_lo(int total, int g, int G) { return (int)(((long long)total * g) / G); }
+
+// Dot products of a group of RG rows (shared memory, K floats) with nv <= NV
+// weight rows W + v * ldw (shared memory): lane l accumulates the products of
+// the elements 64 ch + 2 l, 64 ch + 2 l + 1 of every 64-float chunk ch, so
+// every weight element loaded serves all RG rows.
+template <int RG, int NV>
+__device__ __forceinline__ void group_dots(const float* const (&rows)[RG], const float* W, int ldw, int nv, int K,
+                                           float (&acc)[RG][NV]) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int c = 0; c < TN; ++c) acc[c] = 0.f;
-    const float* ap = As + lane * ld + k0;
-    const float* wp = Ws + k0;
+    for (int r = 0; r < RG; ++r)
+#pragma unroll
+        for (int v = 0; v < NV; ++v) acc[r][v] = 0.f;
 #pragma unroll 2
-    for (int k = 0; k < seg; k += 4) {
-        const float4 a = *reinterpret_cast<const float4*>(ap + k);
+    for (int c0 = 2 * lane; c0 < K; c0 += 64) {
+        float2 x[RG];
 #pragma unroll
-        for (int c = 0; c < TN; ++c) {
-            const float4 v = *reinterpret_cast<const float4*>(wp + c * ld + k);
-            acc[c] = fmaf(a.x, v.x, acc[c]);
-            acc[c] = fmaf(a.y, v.y, acc[c]);
-            acc[c] = fmaf(a.z, v.z, acc[c]);
-            acc[c] = fmaf(a.w, v.w, acc[c]);
-        }
-    }
-    float4* rp = reinterpret_cast<float4*>(red + w * TS * TN + lane * TN);
+        for (int r = 0; r < RG; ++r) x[r] = *reinterpret_cast<const float2*>(rows[r] + c0);
 #pragma unroll
-    for (int q = 0; q < TN / 4; ++q) rp[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
-    __syncthreads();
-    for (int o = tid; o < TS * TN; o += DT) {
-        float sum = 0.f;
+        for (int v = 0; v < NV; ++v)
+            if (v < nv) {
+                const float2 w = *reinterpret_cast<const float2*>(W + (size_t)v * ldw + c0);
 #pragma unroll
-        for (int ww = 0; ww < 8; ++ww) sum += red[ww * TS * TN + o];
-        Os[(o / TN) * OLD + (o % TN)] = sum;
+                for (int r = 0; r < RG; ++r) {
+                    acc[r][v] = fmaf(x[r].x, w.x, acc[r][v]);
+                    acc[r][v] = fmaf(x[r].y, w.y, acc[r][v]);
+                }
+            }
     }
 }
 
-// Stage one tile's rows with the TMA engine: every row is contiguous (K
-// floats), so one bulk copy per row lands it in shared memory (rows K + 4
-// floats apart) and completes on `bar`.  Sources: A rows from a0[r] into A0
-// and, if a1, from a1[r] into A1 (only when load_a), weight rows wrow(r) into
-// Ws; nullptr rows are left as they are (their outputs are never used:
-// padding slots are not stored, classes past the last are masked).  Every
-// thread calls; false when the wait gave up (CAC_E_TIMEOUT latched, abort
-// raised).
-template <class WRow>
-__device__ bool stage_tile(const DecParams& d, int K, bool load_a, float* A0, const float* const* a0, float* A1,
-                           const float* const* a1, float* Ws, WRow wrow, uint64_t* bar, uint32_t& phase) {
-    const int ld = K + 4, tid = threadIdx.x;
-    __syncthreads();  // every earlier read of these buffers is done
-    if (tid < 32) {  // warp 0: lane 0 posts the byte count, the lanes issue one row each
-        const uint32_t rb = (uint32_t)K * 4;
-        if (tid == 0) {
-            fence_proxy_async_smem();
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            uint32_t bytes = 0;
-            for (int r = 0; r < TN; ++r) bytes += wrow(r) ? rb : 0;
-            if (load_a)
-                for (int r = 0; r < TS; ++r) bytes += (a0[r] ? rb : 0) + (a1 && a1[r] ? rb : 0);
-            mbar_expect_tx(bar, bytes);
-        }
-        __syncwarp();
-        if (tid < TN)
-            if (const float* w = wrow(tid)) bulk_g2s(Ws + tid * ld, w, rb, bar);
-        if (load_a) {
-            if (a0[tid]) bulk_g2s(A0 + tid * ld, a0[tid], rb, bar);
-            if (a1 && a1[tid]) bulk_g2s(A1 + tid * ld, a1[tid], rb, bar);
+// Transposed warp reduction of 32 per-lane values: afterwards lane l holds the
+// sum over the warp of value l (31 shuffles: each round a lane keeps half of
+// its values and receives its partner's partial of that half).
+__device__ __forceinline__ float transpose_sum32(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+            const float send = up ? v[i] : v[i + o];
+            const float keep = up ? v[i + o] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
         }
     }
-    const bool ok = __syncthreads_and(mbar_wait(bar, phase));
-    phase ^= 1u;
-    if (!ok && tid == 0) {
-        latch_error(d.status, CAC_E_TIMEOUT);
-        atomicExch(d.abort_flag, 1);
-    }
-    return ok;
+    return v[0];
 }
 
-// Per-tile row table in shared memory: the slot b, stream id and (phase A)
-// token-independent row pointers of the tile's 32 rows, resolved once by 32
-// threads so that the bulk row loads that follow are independent.
-struct RowTab {
-    int b[TS], id[TS], k[TS];
-    const float* src[TS];  // A row source (nullptr: padding row)
-    const float* aux[TS];  // phase A: the stream's predictor projection p
+// Argmax key: the logit's bits made order-preserving as an unsigned (negative
+// values flipped, positive ones offset), above the complemented class id, so
+// that the unsigned maximum is the largest logit and, among equal logits, the
+// lowest class.  Zero is below every key.
+__device__ __forceinline__ unsigned long long pack_key(float v, int cls) {
+    uint32_t b = __float_as_uint(v);
+    b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((unsigned long long)b << 32) | (unsigned long long)(~(uint32_t)cls);
+}
+__device__ __forceinline__ int key_class(unsigned long long k) { return (int)~(uint32_t)(k & 0xffffffffull); }
+
+// Ring of RB row buffers (K floats each) filled by TMA bulk copies.  Row i of
+// a pass lands in slot i mod RB and is consumed by warp i mod NW (RB is a
+// multiple of NW, so a slot always belongs to the same warp); after consuming
+// row i the warp refills the slot with row i + RB.  `par` holds the warp's
+// slot parities (bit j: slot warp + NW j) across passes.
+struct Ring {
+    float* buf;
+    uint64_t* full;
+    int RB, K;
 };
 
-// Phase C: LSTM step of the queued emissions 0 .. ne (token emk[.], stream and h copy emid[.]):
-// tile = (32 slots, 4 hidden units = the 4 x 4 gate rows of those units).
-__device__ void phase_lstm(const DecParams& d, const int* emk, const int* emid, int ne, float* As, float* Ws,
-                           float* Os, float* red, RowTab& rt, uint64_t* bar, uint32_t& phase) {
-    const int P = d.P, tid = threadIdx.x;
-    const int ut = P / 4, tiles = ((ne + TS - 1) / TS) * ut;
-    int loaded = -1;  // slot tile whose h rows sit in As
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
-        const int st = t / ut, j0 = (t % ut) * 4;
-        const bool load_a = st != loaded;
-        if (load_a) {
-            __syncthreads();
-            if (tid < TS) {
-                const int i = st * TS + tid;
-                rt.src[tid] = nullptr;
-                if (i < ne) {
-                    const int e2 = __ldcg(emid + i), id = e2 >> 1, cur = e2 & 1;
-                    rt.id[tid] = id;
-                    rt.k[tid] = __ldcg(emk + i);
-                    rt.src[tid] = d.h + ((long long)cur * d.S + id) * P;
-                    rt.aux[tid] = d.h + ((long long)(cur ^ 1) * d.S + id) * P;  // the new h goes to the other copy
+// One pass over rows 0 .. m-1 of rowK <= K floats (src(i): global address of
+// row i, 16-byte aligned).  The warp takes its rows in groups of RG (RG <=
+// RB / NW, so the rows of a group sit in distinct slots): use(rows, idx) gets
+// the group's shared-memory rows and row indices (idx -1 and a repeat of the
+// first row past the end).  False when a wait gave up (the caller latches and
+// aborts).
+template <int RG, class Src, class Use>
+__device__ bool ring_pass(const Ring& R, uint32_t& par, int m, int rowK, Src src, Use use) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t bytes = (uint32_t)rowK * 4u;
+    if (lane == 0) {
+        // rows were written by other CTAs (generic stores, released by the grid
+        // barrier) and this warp's earlier reads of its slots are done: order
+        // both before the bulk copies
+        fence_proxy_async_smem();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        for (int i = warp; i < m && i < R.RB; i += NW) {
+            mbar_expect_tx(&R.full[i], bytes);
+            bulk_g2s(R.buf + (size_t)i * R.K, src(i), bytes, &R.full[i]);
+        }
+    }
+    __syncwarp();
+    for (int i0 = warp; i0 < m; i0 += NW * RG) {
+        const float* rows[RG];
+        int idx[RG];
+#pragma unroll
+        for (int r = 0; r < RG; ++r) {
+            const int i = i0 + NW * r;
+            if (i < m) {
+                const int s = i % R.RB, j = s / NW;
+                if (!mbar_wait(&R.full[s], (par >> j) & 1u)) return false;
+                par ^= 1u << j;
+                rows[r] = R.buf + (size_t)s * R.K;
+                idx[r] = i;
+            } else {
+                rows[r] = rows[0];
+                idx[r] = -1;
+            }
+        }
+        use(rows, idx);
+        __syncwarp();
+        if (lane == 0) {
+            fence_proxy_async_smem();
+#pragma unroll
+            for (int r = 0; r < RG; ++r) {
+                const int i = i0 + NW * r;
+                if (i + R.RB < m) {
+                    const int s = i % R.RB;
+                    mbar_expect_tx(&R.full[s], bytes);
+                    bulk_g2s(R.buf + (size_t)s * R.K, src(i + R.RB), bytes, &R.full[s]);
                 }
             }
-            __syncthreads();
-            loaded = st;
         }
-        if (!stage_tile(d, P, load_a, As, rt.src, nullptr, nullptr, Ws,
-                        [&](int r) -> const float* { return d.whh + (long long)((r >> 2) * P + j0 + (r & 3)) * P; },
-                        bar, phase))
-            return;
-        mac16(P, As, Ws, Os, red);
-        __syncthreads();
-        if (tid < TS * 4) {  // cell update of (slot r, unit jj)
-            const int r = tid >> 2, jj = tid & 3;
-            if (rt.src[r]) {
-                const int id = rt.id[r], j = j0 + jj;
-                const float* tb = d.tab + (long long)rt.k[r] * 4 * P;
-                const float gi = Os[r * OLD + jj] + __ldg(tb + j);
-                const float gf = Os[r * OLD + 4 + jj] + __ldg(tb + P + j);
-                const float gg = Os[r * OLD + 8 + jj] + __ldg(tb + 2 * P + j);
-                const float go = Os[r * OLD + 12 + jj] + __ldg(tb + 3 * P + j);
-                float* cp = d.c + (long long)id * P + j;
-                const float c2 = sigm(gf) * __ldcg(cp) + sigm(gi) * tanhf(gg);
-                *cp = c2;
-                const_cast<float*>(rt.aux[r])[j] = sigm(go) * tanhf(c2);
-            }
-        }
-        __syncthreads();  // Ws, Os and the row table are reused by the next tile
     }
+    return true;
 }
 
-// Phase D: p = W_pred h' + b_pred for the queued slots.
-__device__ void phase_proj(const DecParams& d, const int* emid, int ne, float* As, float* Ws, float* Os,
-                           float* red, RowTab& rt, uint64_t* bar, uint32_t& phase) {
-    const int P = d.P, J = d.J, tid = threadIdx.x;
-    const int jt = J / TN, tiles = ((ne + TS - 1) / TS) * jt;
-    int loaded = -1;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
-        const int st = t / jt, c0 = (t % jt) * TN;
-        const bool load_a = st != loaded;
-        if (load_a) {
-            __syncthreads();
-            if (tid < TS) {
-                const int i = st * TS + tid;
-                rt.src[tid] = nullptr;
-                if (i < ne) {
-                    const int e2 = __ldcg(emid + i), id = e2 >> 1;
-                    rt.id[tid] = id;
-                    rt.src[tid] = d.h + ((long long)((e2 & 1) ^ 1) * d.S + id) * P;  // the new h
-                }
-            }
-            __syncthreads();
-            loaded = st;
-        }
-        if (!stage_tile(d, P, load_a, As, rt.src, nullptr, nullptr, Ws,
-                        [&](int r) -> const float* { return d.wpp + (long long)(c0 + r) * P; }, bar, phase))
-            return;
-        mac16(P, As, Ws, Os, red);
-        __syncthreads();
-        for (int e = tid; e < TS * TN; e += DT) {
-            const int r = e / TN, cc = e % TN;
-            if (rt.src[r]) d.p[(long long)rt.id[r] * J + c0 + cc] = Os[r * OLD + cc] + __ldg(d.bpp + c0 + cc);
-        }
-        __syncthreads();
-    }
+__device__ __forceinline__ void fail_abort(const DecParams& d) {
+    latch_error(d.status, CAC_E_TIMEOUT);
+    atomicExch(d.abort_flag, 1);
 }
 
-// Phase A: logits of the active slots act[0 .. na) at their current frame,
-// partial first-maximum per TN-class tile into pval / pidx [slot][nct].
-__device__ void phase_joint(const DecParams& d, const int* act, int na, float* As, float* Ws, float* Os,
-                            float* Ps, float* red, RowTab& rt, uint64_t* bar, uint32_t& phase) {
-    const int J = d.J, C = d.C, tid = threadIdx.x;
-    const int tiles = ((na + TS - 1) / TS) * d.nct;
-    int loaded = -1;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
-        const int st = t / d.nct, ct = t % d.nct, c0 = ct * TN;
-        const bool load_a = st != loaded;
-        if (load_a) {
-            __syncthreads();
-            if (tid < TS) {
-                const int i = st * TS + tid;
-                rt.src[tid] = nullptr;
-                rt.aux[tid] = nullptr;
-                if (i < na) {
-                    const int b = __ldcg(act + i), id = d.ids[b], f = __ldcg(d.frame + b);
-                    rt.b[tid] = b;
-                    rt.src[tid] = d.z + b * d.zb + (long long)f * J;
-                    rt.aux[tid] = d.p + (long long)id * J;
-                }
-            }
-            __syncthreads();
-        }
-        if (!stage_tile(d, J, load_a, As, rt.src, Ps, rt.aux, Ws,
-                        [&](int r) -> const float* { return c0 + r < C ? d.wout + (long long)(c0 + r) * J : nullptr; },
-                        bar, phase))
-            return;
-        if (load_a) {
-            for (int e = tid; e < TS * J / 4; e += DT) {  // As <- ReLU(z + p)
-                const int r = e / (J / 4), q = e % (J / 4);
-                float4* a = reinterpret_cast<float4*>(As + r * (J + 4) + 4 * q);
-                const float4 pp = *reinterpret_cast<const float4*>(Ps + r * (J + 4) + 4 * q);
-                const float4 zz = *a;
-                *a = make_float4(fmaxf(zz.x + pp.x, 0.f), fmaxf(zz.y + pp.y, 0.f), fmaxf(zz.z + pp.z, 0.f),
-                                 fmaxf(zz.w + pp.w, 0.f));
-            }
-            __syncthreads();
-            loaded = st;
-        }
-        mac16(J, As, Ws, Os, red);
-        __syncthreads();
-        if (tid < TS && rt.src[tid]) {
-            float best = -FLT_MAX;
-            int bi = c0;
-            for (int q = 0; q < TN && c0 + q < C; ++q) {
-                const float v = Os[tid * OLD + q] + __ldg(d.bout + c0 + q);
-                if (v > best) { best = v; bi = c0 + q; }
-            }
-            const int b = rt.b[tid];
-            d.pval[(long long)b * d.nct + ct] = best;
-            d.pidx[(long long)b * d.nct + ct] = bi;
-        }
-        __syncthreads();
-    }
-}
-
-// The whole step (see the top of the file).  Iteration it reads the active
-// list act[it & 1] (length cnt[2 it]) and writes the next one act[(it + 1) & 1]
-// (length cnt[2 it + 2]) and its emissions emk/emid[it & 1] (length cnt[2 it +
-// 1]); iteration 0 only builds the first active list and primes reset streams.
+// The whole step (see the top of the file).
 __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
-    extern __shared__ float smem[];
-    const int K = d.P > d.J ? d.P : d.J;
-    float* As = smem;
-    float* Ws = As + TS * (K + 4);
-    float* Os = Ws + TN * (K + 4);
-    float* Ps = Os + TS * OLD;  // phase A: the p rows (TS x (J + 4))
-    float* red = Ps + TS * (d.J + 4);  // partial tiles of mac16 (8 x TS x TN)
-    __shared__ RowTab rt;
-    __shared__ __align__(8) uint64_t tbar;
-    uint32_t tphase = 0;
-    if (threadIdx.x == 0) {
-        mbar_init(&tbar, 1);
+    extern __shared__ __align__(16) float sm[];
+    __shared__ __align__(8) uint64_t ring_full[RB_MAX];
+    __shared__ __align__(8) uint64_t wbar;
+    __shared__ int s_cnt[2];  // emitted, next active
+    const int G = gridDim.x, g = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = d.P, J = d.J, n = d.n, S = d.S;
+    const int c_lo = slice_lo(d.C, g, G), nc = slice_lo(d.C, g + 1, G) - c_lo;
+    const int u_lo = slice_lo(P, g, G), nu = slice_lo(P, g + 1, G) - u_lo;
+    const int o_lo = slice_lo(J, g, G), no = slice_lo(J, g + 1, G) - o_lo;
+    const int K = P > J ? P : J;
+    float* Wo = sm;                                   // [nc_max][J]
+    float* Wh = Wo + (size_t)d.nc_max * J;            // [4 nu][P]: row q nu + i = gate q of unit u_lo + i
+    float* Wp = Wh + (size_t)4 * d.nu_max * P;        // [no_max][P]
+    float* bo_s = Wp + (size_t)d.no_max * P;          // [nc_max] joint biases of the CTA's classes
+    float* bp_s = bo_s + d.nc_max;                    // [no_max] projection biases
+    float* rbuf = Wp + (size_t)d.no_max * P + bias_floats(d.nc_max, d.no_max);  // [RB][K]
+    int* frame = reinterpret_cast<int*>(rbuf + (size_t)d.RB * K);  // replicated slot state
+    int* sym = frame + S;                             // emissions on the current frame
+    int* ecount = sym + S;                            // emissions of the step
+    int* cur = ecount + S;                            // current h copy of the slot's stream
+    int* act = cur + S;                               // [2][S] active lists
+    int* dec = act + 2 * S;                           // decided class per active index
+    int* eb = dec + S;                                // emitting slots, in active order
+    int* ek = eb + S;                                 // their classes
+    int* eh = ek + S;                                 // their h copy before the step
+    const Ring R{rbuf, ring_full, d.RB, K};
+    uint32_t par = 0;
+    unsigned gt = 0;  // grid-barrier target
+    const long long tsym = (long long)d.T * d.max_sym;
+
+    // ---- weights of this CTA's slices into shared memory (TMA bulk copies)
+    if (tid == 0) {
+        mbar_init(&wbar, 1);
+        for (int s = 0; s < d.RB; ++s) mbar_init(&ring_full[s], 1);
         fence_mbar_init();
     }
     __syncthreads();
-    const int gtid = blockIdx.x * DT + threadIdx.x, gstride = gridDim.x * DT;
-    const long long tsym = (long long)d.T * d.max_sym;
+    if (tid == 0) {
+        mbar_expect_tx(&wbar, (uint32_t)(nc * J + 4 * nu * P + no * P) * 4u);
+        for (int i = 0; i < nc; ++i) bulk_g2s(Wo + (size_t)i * J, d.wout + (size_t)(c_lo + i) * J, J * 4, &wbar);
+        for (int q = 0; q < 4; ++q)
+            for (int i = 0; i < nu; ++i)
+                bulk_g2s(Wh + (size_t)(q * nu + i) * P, d.whh + ((size_t)q * P + u_lo + i) * P, P * 4, &wbar);
+        for (int i = 0; i < no; ++i) bulk_g2s(Wp + (size_t)i * P, d.wpp + (size_t)(o_lo + i) * P, P * 4, &wbar);
+    }
+    for (int i = tid; i < nc; i += DT) bo_s[i] = __ldg(d.bout + c_lo + i);
+    for (int i = tid; i < no; i += DT) bp_s[i] = __ldg(d.bpp + o_lo + i);
+    // ---- replicated slot state; keys of both parities start at zero
+    for (int b = tid; b < n; b += DT) {
+        frame[b] = 0;
+        sym[b] = 0;
+        ecount[b] = 0;
+        cur[b] = __ldcg(d.hsel + d.ids[b]);
+        act[b] = b;
+    }
+    for (int b = g * DT + tid; b < 2 * n; b += G * DT) d.keys[(b >= n) * S + b % n] = 0ull;
+    __syncthreads();
+    // streams after a reset start from h = c = 0 with one predictor step on the
+    // blank token: listed like emissions (slot order, every CTA alike)
+    if (warp == 0) {
+        int m = 0;
+        for (int base = 0; base < n; base += 32) {
+            const int b = base + lane;
+            const bool pr = b < n && __ldcg(d.primed + d.ids[b]) == 0;
+            const unsigned mk = __ballot_sync(0xffffffffu, pr);
+            if (pr) {
+                const int q = m + __popc(mk & ((1u << lane) - 1u));
+                eb[q] = b;
+                ek[q] = d.blank;
+                eh[q] = cur[b];
+                cur[b] ^= 1;
+            }
+            m += __popc(mk);
+        }
+        if (lane == 0) s_cnt[0] = m;
+    }
+    const bool wok = __syncthreads_and(mbar_wait(&wbar, 0));
+    if (!wok) {
+        if (tid == 0) fail_abort(d);
+        return;
+    }
+    int ne = s_cnt[0];
+    // priming LSTM step of this CTA's units: W_hh h = 0 and c = 0, so the gates are the blank's table row
+    for (int x = tid; x < ne * nu; x += DT) {
+        const int e = x / nu, j = u_lo + x % nu, id = d.ids[eb[e]];
+        const float* tb = d.tab + (size_t)d.blank * 4 * P;
+        const float gi = __ldg(tb + j), gg = __ldg(tb + 2 * P + j), go = __ldg(tb + 3 * P + j);
+        const float c2 = sigm(gi) * tanhf(gg);  // the forget gate multiplies c = 0
+        __stcg(d.c + (size_t)id * P + j, c2);
+        __stcg(d.h + ((size_t)(eh[e] ^ 1) * S + id) * P + j, sigm(go) * tanhf(c2));
+    }
 
-    for (int b = gtid; b < d.n; b += gstride) {
-        const int id = d.ids[b];
-        d.frame[b] = 0;
-        d.sym[b] = 0;
-        d.counts[b] = 0;
-        if (d.T > 0) d.act[d.n + atomicAdd(&d.cnt[2], 1)] = b;
-        if (__ldcg(d.primed + id) == 0) {  // stream start: zero state, one predictor step on blank
-            const int cur = __ldcg(d.hsel + id);
-            for (int j = 0; j < d.P; ++j) {
-                d.h[((long long)cur * d.S + id) * d.P + j] = 0.f;
-                d.c[(long long)id * d.P + j] = 0.f;
-            }
-            d.primed[id] = 1;
-            d.hsel[id] = cur ^ 1;
-            const int q = atomicAdd(&d.cnt[1], 1);
-            d.emk[q] = d.blank;
-            d.emid[q] = id * 2 + cur;
+    // ---- D: projection of the emitting slots (their new h), then the joint
+    // inputs of the listed slots; shared by the priming and every iteration
+    auto phase_d = [&](int ne_, const int* L, int m) -> bool {
+        if (ne_ > 0 && no > 0) {
+            const bool ok = ring_pass<4>(
+                R, par, ne_, P,
+                [&](int e) { return d.h + ((size_t)(eh[e] ^ 1) * S + d.ids[eb[e]]) * P; },
+                [&](const float* const (&rows)[4], const int (&idx)[4]) {
+                    float acc[4][8];
+                    group_dots<4, 8>(rows, Wp, P, no, P, acc);
+                    // lane 8 r + o: output o_lo + o of row r
+                    const float v = transpose_sum32(reinterpret_cast<float (&)[32]>(acc));
+                    const int r = lane >> 3, o = lane & 7;
+                    if (o < no && idx[r] >= 0)
+                        __stcg(d.p + (size_t)d.ids[eb[idx[r]]] * J + o_lo + o, v + bp_s[o]);
+                });
+            if (!__syncthreads_and(ok)) return false;  // also orders the p stores before the reads below
         }
+        for (int x = tid; x < m * no; x += DT) {
+            const int b = L[x / no], j = o_lo + x % no;
+            const float zz = __ldg(d.z + b * d.zb + (long long)frame[b] * J + j);
+            const float pp = __ldcg(d.p + (size_t)d.ids[b] * J + j);
+            __stcg(d.u + (size_t)b * J + j, fmaxf(zz + pp, 0.f));
+        }
+        return true;
+    };
+
+    int na = d.T > 0 ? n : 0;
+    if (ne > 0 && !grid_sync(d, gt)) return;
+    if (!phase_d(ne, act, na)) {
+        if (tid == 0) fail_abort(d);
+        return;
     }
-    if (!grid_sync(d)) return;
-    int ne = __ldcg(d.cnt + 1);
-    if (ne > 0) {
-        phase_lstm(d, d.emk, d.emid, ne, As, Ws, Os, red, rt, &tbar, tphase);
-        if (!grid_sync(d)) return;
-        phase_proj(d, d.emid, ne, As, Ws, Os, red, rt, &tbar, tphase);
-        if (!grid_sync(d)) return;
-    }
-    for (int it = 1; it <= d.maxit; ++it) {
-        const int na = __ldcg(d.cnt + 2 * it);
-        if (na == 0) break;
-        const int* act = d.act + (it & 1) * d.n;
-        phase_joint(d, act, na, As, Ws, Os, Ps, red, rt, &tbar, tphase);
-        if (!grid_sync(d)) return;
-        int* nact = d.act + ((it + 1) & 1) * d.n;
-        int* emk = d.emk + (it & 1) * d.n;
-        int* emid = d.emid + (it & 1) * d.n;
-        // one warp per active slot: first maximum over the slot's partials
-        const int lane = threadIdx.x & 31;
-        for (int i = gtid >> 5; i < na; i += gstride >> 5) {
-            const int b = __ldcg(act + i);
-            const long long pb = (long long)b * d.nct;
-            float best = -FLT_MAX;
-            int k = INT_MAX;
-            for (int q = lane; q < d.nct; q += 32) {  // tiles in class order: strict > keeps the lowest index
-                const float v = __ldcg(d.pval + pb + q);
-                if (v > best) {
-                    best = v;
-                    k = __ldcg(d.pidx + pb + q);
-                }
-            }
+    if (!grid_sync(d, gt)) return;
+
+    int cb = 0;
+    for (int it = 0; it < d.maxit && na > 0; ++it) {
+        const int* A = act + cb * S;
+        int* N = act + (cb ^ 1) * S;
+        unsigned long long* keys = d.keys + (size_t)(it & 1) * S;
+        // ---- A: logits of this CTA's classes for every active slot, argmax key
+        bool ok = true;
+        if (nc > 0)
+            ok = ring_pass<4>(
+                R, par, na, J, [&](int i) { return d.u + (size_t)A[i] * J; },
+                [&](const float* const (&rows)[4], const int (&idx)[4]) {
+                    // lane 8 r + v: class c0 + v of row r; the running best of row r
+                    // (largest logit, lowest class on ties) ends in lane 8 r
+                    const int r = lane >> 3, v = lane & 7;
+                    float best = -FLT_MAX;
+                    int bi = INT_MAX;
+                    for (int c0 = 0; c0 < nc; c0 += 8) {
+                        const int nv = min(8, nc - c0);
+                        float acc[4][8];
+                        group_dots<4, 8>(rows, Wo + (size_t)c0 * J, J, nv, J, acc);
+                        float x = transpose_sum32(reinterpret_cast<float (&)[32]>(acc));
+                        int k = c0 + v;
+                        if (v < nv) x += bo_s[c0 + v];
+                        else x = -FLT_MAX, k = INT_MAX;
 #pragma unroll
-            for (int o = 16; o; o >>= 1) {  // larger value wins, equal values: the lower class
-                const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-                const int ok = __shfl_xor_sync(0xffffffffu, k, o);
-                if (ov > best || (ov == best && ok < k)) {
-                    best = ov;
-                    k = ok;
+                        for (int o = 4; o >= 1; o >>= 1) {
+                            const float ox = __shfl_xor_sync(0xffffffffu, x, o);
+                            const int ok_ = __shfl_xor_sync(0xffffffffu, k, o);
+                            if (ox > x || (ox == x && ok_ < k)) {
+                                x = ox;
+                                k = ok_;
+                            }
+                        }
+                        if (x > best || (x == best && k < bi)) {
+                            best = x;
+                            bi = k;
+                        }
+                    }
+                    if (v == 0 && idx[r] >= 0) atomicMax(keys + A[idx[r]], pack_key(best, c_lo + bi));
+                });
+        if (!__syncthreads_and(ok)) {
+            if (tid == 0) fail_abort(d);
+            return;
+        }
+        if (!grid_sync(d, gt)) return;
+        // ---- B: the decisions of every active slot, in every CTA alike
+        for (int i = tid; i < na; i += DT) dec[i] = key_class(__ldcg(keys + A[i]));
+        // the other parity's keys serve the next iteration (all its readers passed a barrier)
+        for (int b = g * DT + tid; b < n; b += G * DT) d.keys[(size_t)((it + 1) & 1) * S + b] = 0ull;
+        __syncthreads();
+        if (warp == 0) {
+            int ne_ = 0, nn = 0;
+            for (int base = 0; base < na; base += 32) {
+                const int i = base + lane;
+                bool em = false, keep = false;
+                int b = 0, k = 0;
+                if (i < na) {
+                    b = A[i];
+                    k = dec[i];
+                    int f = frame[b], sy = sym[b];
+                    bool next = k == d.blank;
+                    if (!next) {
+                        em = true;
+                        if (b % G == g) {
+                            d.tokens[b * tsym + ecount[b]] = k;
+                            d.frames[b * tsym + ecount[b]] = f;
+                        }
+                        ++ecount[b];
+                        next = ++sy == d.max_sym;
+                    }
+                    if (next) {
+                        ++f;
+                        sy = 0;
+                    }
+                    frame[b] = f;
+                    sym[b] = sy;
+                    keep = f < d.T;
                 }
+                const unsigned lt = (1u << lane) - 1u;
+                const unsigned me = __ballot_sync(0xffffffffu, em), mk = __ballot_sync(0xffffffffu, keep);
+                if (em) {
+                    const int q = ne_ + __popc(me & lt);
+                    eb[q] = b;
+                    ek[q] = k;
+                    eh[q] = cur[b];
+                    cur[b] ^= 1;
+                }
+                if (keep) N[nn + __popc(mk & lt)] = b;
+                ne_ += __popc(me);
+                nn += __popc(mk);
             }
-            if (lane != 0) continue;
-            int f = __ldcg(d.frame + b), sy = __ldcg(d.sym + b);
-            bool next = k == d.blank;
-            if (!next) {
-                const int cn = __ldcg(d.counts + b);
-                d.tokens[b * tsym + cn] = k;
-                d.frames[b * tsym + cn] = f;
-                d.counts[b] = cn + 1;
-                const int q = atomicAdd(&d.cnt[2 * it + 1], 1);
-                const int id = d.ids[b], cur = __ldcg(d.hsel + id);
-                d.hsel[id] = cur ^ 1;
-                emk[q] = k;
-                emid[q] = id * 2 + cur;
-                next = ++sy == d.max_sym;
+            if (lane == 0) {
+                s_cnt[0] = ne_;
+                s_cnt[1] = nn;
             }
-            if (next) {
-                ++f;
-                sy = 0;
-            }
-            d.frame[b] = f;
-            d.sym[b] = sy;
-            if (f < d.T) nact[atomicAdd(&d.cnt[2 * it + 2], 1)] = b;
         }
-        if (!grid_sync(d)) return;
-        ne = __ldcg(d.cnt + 2 * it + 1);
+        __syncthreads();
+        ne = s_cnt[0];
+        const int nn = s_cnt[1];
+        // ---- C: LSTM step of this CTA's units for the emitting slots
         if (ne > 0) {
-            phase_lstm(d, emk, emid, ne, As, Ws, Os, red, rt, &tbar, tphase);
-            if (!grid_sync(d)) return;
-            phase_proj(d, emid, ne, As, Ws, Os, red, rt, &tbar, tphase);
-            if (!grid_sync(d)) return;
+            ok = true;
+            if (nu > 0)
+                ok = ring_pass<2>(
+                    R, par, ne, P, [&](int e) { return d.h + ((size_t)eh[e] * S + d.ids[eb[e]]) * P; },
+                    [&](const float* const (&rows)[2], const int (&idx)[2]) {
+                        // lane uu < nu: its unit's table entries and cell state, loaded
+                        // ahead of the dot products
+                        float t4[2][4], cold[2];
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            t4[r][0] = t4[r][1] = t4[r][2] = t4[r][3] = cold[r] = 0.f;
+                            if (lane < nu && idx[r] >= 0) {
+                                const int e = idx[r];
+                                const float* tb = d.tab + (size_t)ek[e] * 4 * P + u_lo + lane;
+                                t4[r][0] = __ldg(tb);
+                                t4[r][1] = __ldg(tb + P);
+                                t4[r][2] = __ldg(tb + 2 * P);
+                                t4[r][3] = __ldg(tb + 3 * P);
+                                cold[r] = __ldcg(d.c + (size_t)d.ids[eb[e]] * P + u_lo + lane);
+                            }
+                        }
+                        float acc[2][32];
+                        group_dots<2, 32>(rows, Wh, P, 4 * nu, P, acc);
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            // lane q nu + uu: gate q of unit uu; gather a unit's 4 gates in lane uu
+                            const float gsum = transpose_sum32(acc[r]);
+                            float gm[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) gm[q] = __shfl_sync(0xffffffffu, gsum, min(q * nu + lane, 31));
+                            if (lane < nu && idx[r] >= 0) {
+                                const int e = idx[r], id = d.ids[eb[e]], j = u_lo + lane;
+                                const float gi = gm[0] + t4[r][0], gf = gm[1] + t4[r][1];
+                                const float gg = gm[2] + t4[r][2], go = gm[3] + t4[r][3];
+                                const float c2 = sigm(gf) * cold[r] + sigm(gi) * tanhf(gg);
+                                __stcg(d.c + (size_t)id * P + j, c2);
+                                __stcg(d.h + ((size_t)(eh[e] ^ 1) * S + id) * P + j, sigm(go) * tanhf(c2));
+                            }
+                        }
+                    });
+            if (!__syncthreads_and(ok)) {
+                if (tid == 0) fail_abort(d);
+                return;
+            }
+            if (!grid_sync(d, gt)) return;
         }
+        // ---- D
+        if (!phase_d(ne, N, nn)) {
+            if (tid == 0) fail_abort(d);
+            return;
+        }
+        if (!grid_sync(d, gt)) return;
+        cb ^= 1;
+        na = nn;
+    }
+    // ---- the owners write the per-slot results back (every CTA read hsel and
+    // primed before the first barrier)
+    for (int b = g + G * tid; b < n; b += G * DT) {
+        d.counts[b] = ecount[b];
+        d.hsel[d.ids[b]] = cur[b];
+        d.primed[d.ids[b]] = 1;
     }
 }
 
@@ -488,7 +586,8 @@ __global__ void wait_selftest_mbar_kernel(int* status) {
 
 __global__ void wait_selftest_grid_kernel(DecParams d) {
     if (blockIdx.x == 0) return;  // the first block never reaches the barrier
-    grid_sync(d);
+    unsigned gt = 0;
+    grid_sync(d, gt);
 }
 
 constexpr int ID_SLOTS = 4;
@@ -501,18 +600,18 @@ using namespace cac;
 
 struct cac_decoder {
     cac_dec_config cfg{};
-    int C = 0, S = 0, nct = 0, grid = 0;
+    int C = 0, S = 0, grid = 0;
+    int nc_max = 0, nu_max = 0, no_max = 0, RB = 0;
     size_t smem = 0;
     std::vector<void*> allocs;
     float *tab = nullptr, *whh = nullptr, *wpp = nullptr, *bpp = nullptr, *wout = nullptr, *bout = nullptr;
     float *h = nullptr, *c = nullptr, *p = nullptr;
     int* primed = nullptr;
     // step scratch for up to S slots
-    int *ids = nullptr, *frame = nullptr, *sym = nullptr, *act = nullptr, *emk = nullptr, *emid = nullptr;
-    int* cnt = nullptr;  // [2 (maxit + 2)] iteration counters, then arrivals / generation / abort
-    int cnt_ints = 0;
-    float* pval = nullptr;
-    int* pidx = nullptr;
+    int* ids = nullptr;
+    float* u = nullptr;                 // [S][J] joint inputs of the slots
+    unsigned long long* keys = nullptr; // [2][S] argmax keys
+    int* bar = nullptr;                 // arrivals, generation, abort word
     int* hsel = nullptr;  // [S]
     int* status = nullptr;
     int* pinned = nullptr;  // ID_SLOTS x S host ids
@@ -565,7 +664,8 @@ extern "C" int cac_decoder_create(const cac_dec_config* cfg, const float* weight
     if (!cfg || !weights || !out || max_streams < 1 || cfg->vocab < 1 || cfg->max_symbols < 1 ||
         cfg->pred_dim < 64 || cfg->joint_dim < 64)
         return CAC_E_INVAL;
-    if (cfg->pred_dim % 64 || cfg->joint_dim % 64) return CAC_E_UNSUPPORTED;
+    if (cfg->pred_dim % 64 || cfg->joint_dim % 64 || cfg->pred_dim > 64 * MAXCH || cfg->joint_dim > 64 * MAXCH)
+        return CAC_E_UNSUPPORTED;
     const size_t C = (size_t)cfg->vocab + 2, P = cfg->pred_dim, J = cfg->joint_dim;
     const size_t need = C * P + 2 * 4 * P * P + 2 * 4 * P + J * P + J + C * J + C;
     if (n_floats != need) return CAC_E_INVAL;
@@ -574,7 +674,6 @@ extern "C" int cac_decoder_create(const cac_dec_config* cfg, const float* weight
     d->cfg = *cfg;
     d->C = (int)C;
     d->S = max_streams;
-    d->nct = (int)((C + TN - 1) / TN);
     auto fail = [&](int code) {
         cac_decoder_destroy(d);
         return code;
@@ -606,14 +705,9 @@ extern "C" int cac_decoder_create(const cac_dec_config* cfg, const float* weight
     const size_t S = max_streams;
     if ((r = dalloc_t(d, 2 * S * P, &d->h)) || (r = dalloc_t(d, S, &d->hsel)) || (r = dalloc_t(d, S * P, &d->c)) ||
         (r = dalloc_t(d, S * J, &d->p)) ||
-        (r = dalloc_t(d, S, &d->primed)) || (r = dalloc_t(d, S, &d->ids)) || (r = dalloc_t(d, S, &d->frame)) ||
-        (r = dalloc_t(d, S, &d->sym)) || (r = dalloc_t(d, 2 * S, &d->act)) || (r = dalloc_t(d, 2 * S, &d->emid)) ||
-        (r = dalloc_t(d, 2 * S, &d->emk)) || (r = dalloc_t(d, S * d->nct, &d->pval)) ||
-        (r = dalloc_t(d, S * d->nct, &d->pidx)) ||
-        (r = dalloc_t(d, 1, &d->status)))
+        (r = dalloc_t(d, S, &d->primed)) || (r = dalloc_t(d, S, &d->ids)) || (r = dalloc_t(d, S * J, &d->u)) ||
+        (r = dalloc_t(d, 2 * S, &d->keys)) || (r = dalloc_t(d, 4, &d->bar)) || (r = dalloc_t(d, 1, &d->status)))
         return fail(r);
-    d->cnt_ints = 2 * (maxit_for(*cfg, MAX_T) + 2) + 4;
-    if ((r = dalloc_t(d, d->cnt_ints, &d->cnt))) return fail(r);
     if (cudaMemset(d->primed, 0, S * 4) != cudaSuccess || cudaMemset(d->status, 0, 4) != cudaSuccess ||
         cudaMemset(d->h, 0, 2 * S * P * 4) != cudaSuccess || cudaMemset(d->hsel, 0, S * 4) != cudaSuccess || cudaMemset(d->c, 0, S * P * 4) != cudaSuccess ||
         cudaMemset(d->p, 0, S * J * 4) != cudaSuccess)
@@ -622,14 +716,27 @@ extern "C" int cac_decoder_create(const cac_dec_config* cfg, const float* weight
         return fail(CAC_E_NOMEM);
     for (auto& e : d->slot_ev)
         if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return fail(CAC_E_CUDA);
-    // one CTA per SM, all co-resident (cooperative launch)
-    const int K = (int)(P > J ? P : J);
-    d->smem = sizeof(float) * ((size_t)(TS + TN) * (K + 4) + (size_t)TS * OLD + (size_t)TS * (J + 4) + 8 * TS * TN);
-    if (d->smem > 227 * 1024) return fail(CAC_E_UNSUPPORTED);
+    // one CTA per SM, all co-resident (cooperative launch).  Shared memory:
+    // the CTA's weight slices, the row ring (as many slots as fit, up to
+    // RB_MAX, a multiple of the warp count) and the replicated slot state.
+    const size_t K = P > J ? P : J;
     int dev = 0, sms = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaFuncSetAttribute(dec_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)d->smem) !=
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        return fail(CAC_E_CUDA);
+    d->nc_max = (int)((C + sms - 1) / sms);
+    d->nu_max = (int)((P + sms - 1) / sms);
+    d->no_max = (int)((J + sms - 1) / sms);
+    // a CTA's gate rows (4 per unit) fill at most one warp, its projection outputs at most 8 lanes per row
+    if (d->nu_max > 8 || d->no_max > 8) return fail(CAC_E_UNSUPPORTED);
+    const size_t fixed = sizeof(float) * ((size_t)d->nc_max * J + (size_t)4 * d->nu_max * P + (size_t)d->no_max * P +
+                                          bias_floats(d->nc_max, d->no_max)) +
+                         sizeof(int) * STATE_INTS * S;
+    const size_t budget = 227 * 1024 - 1024;  // less the kernel's static shared memory
+    if (fixed + sizeof(float) * K * 4 * NW > budget) return fail(CAC_E_UNSUPPORTED);  // groups of 4 rows per warp
+    d->RB = (int)std::min<size_t>(RB_MAX, (budget - fixed) / (sizeof(float) * K) / NW * NW);
+    d->smem = fixed + sizeof(float) * K * d->RB;
+    if (cudaFuncSetAttribute(dec_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)d->smem) !=
             cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dec_step_kernel, DT, d->smem) != cudaSuccess)
         return fail(CAC_E_CUDA);
@@ -689,18 +796,16 @@ extern "C" int cac_decoder_step(cac_decoder* d, int n, const int* ids, const flo
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((r = dec_upload_ids(d, ids, n, d->ids, s)) != CAC_OK) return r;
     const int maxit = maxit_for(d->cfg, T);
-    const int nc = 2 * (maxit + 2);
-    if (cudaMemsetAsync(d->cnt, 0, sizeof(int) * (nc + 4), s) != cudaSuccess) return CAC_E_CUDA;
+    if (cudaMemsetAsync(d->bar, 0, sizeof(int) * 4, s) != cudaSuccess) return CAC_E_CUDA;
     DecParams p{};
     p.n = n; p.T = T; p.C = d->C; p.P = d->cfg.pred_dim; p.J = d->cfg.joint_dim; p.max_sym = d->cfg.max_symbols;
-    p.blank = d->cfg.vocab; p.nct = d->nct; p.maxit = maxit;
+    p.blank = d->cfg.vocab; p.maxit = maxit; p.S = d->S;
+    p.nc_max = d->nc_max; p.nu_max = d->nu_max; p.no_max = d->no_max; p.RB = d->RB;
     p.ids = d->ids; p.z = z; p.zb = z_bstride; p.tokens = tokens; p.frames = frames; p.counts = counts;
     p.tab = d->tab; p.whh = d->whh; p.wpp = d->wpp; p.bpp = d->bpp; p.wout = d->wout; p.bout = d->bout;
-    p.h = d->h; p.c = d->c; p.p = d->p; p.primed = d->primed; p.hsel = d->hsel; p.S = d->S;
-    p.frame = d->frame; p.sym = d->sym; p.act = d->act; p.emk = d->emk; p.emid = d->emid; p.cnt = d->cnt;
-    p.pval = d->pval; p.pidx = d->pidx;
-    p.bar = reinterpret_cast<unsigned*>(d->cnt + nc);
-    p.abort_flag = d->cnt + nc + 2;
+    p.h = d->h; p.c = d->c; p.p = d->p; p.u = d->u; p.keys = d->keys; p.primed = d->primed; p.hsel = d->hsel;
+    p.bar = reinterpret_cast<unsigned*>(d->bar);
+    p.abort_flag = d->bar + 2;
     p.status = d->status;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(d->grid);

@@ -44,7 +44,11 @@ typedef struct cac_decoder cac_decoder;
  * with C = vocab + 2, P = pred_dim, J = joint_dim; LSTM gate rows in the order
  * input, forget, cell, output.  The library copies what it needs to the current
  * device; the caller keeps the blob.  max_streams: stream ids 0 .. max_streams-1
- * each own one predictor state (h, c and its projection), all starting reset. */
+ * each own one predictor state (h, c and its projection), all starting reset.
+ * Every CTA of the step kernel keeps a copy of the per-slot decoding state in
+ * shared memory beside its weight slices, which bounds max_streams (about
+ * 1,600 for the 1024-token, 640-wide decoder on a 152-SM GPU); beyond that,
+ * or for pred_dim / joint_dim above 1024, the call returns CAC_E_UNSUPPORTED. */
 int cac_decoder_create(const cac_dec_config* cfg, const float* weights, size_t n_floats, int max_streams,
                        cac_decoder** out);
 void cac_decoder_destroy(cac_decoder* d);
