@@ -179,6 +179,25 @@ __device__ __forceinline__ float transpose_sum32(float (&v)[32]) {
     return v[0];
 }
 
+// The same for 16 values: lanes l and l + 16 both end with the sum of value
+// l mod 16 (a plain exchange across the half-warps, then four transposed rounds).
+__device__ __forceinline__ float transpose_sum16(float (&v)[16]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], 16);
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+            const float send = up ? v[i] : v[i + o];
+            const float keep = up ? v[i + o] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0];
+}
+
 // Argmax key: the logit's bits made order-preserving as an unsigned (negative
 // values flipped, positive ones offset), above the complemented class id, so
 // that the unsigned maximum is the largest logit and, among equal logits, the
@@ -361,16 +380,16 @@ __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
     // inputs of the listed slots; shared by the priming and every iteration
     auto phase_d = [&](int ne_, const int* L, int m) -> bool {
         if (ne_ > 0 && no > 0) {
-            const bool ok = ring_pass<4>(
+            const bool ok = ring_pass<2>(
                 R, par, ne_, P,
                 [&](int e) { return d.h + ((size_t)(eh[e] ^ 1) * S + d.ids[eb[e]]) * P; },
-                [&](const float* const (&rows)[4], const int (&idx)[4]) {
-                    float acc[4][8];
-                    group_dots<4, 8>(rows, Wp, P, no, P, acc);
-                    // lane 8 r + o: output o_lo + o of row r
-                    const float v = transpose_sum32(reinterpret_cast<float (&)[32]>(acc));
-                    const int r = lane >> 3, o = lane & 7;
-                    if (o < no && idx[r] >= 0)
+                [&](const float* const (&rows)[2], const int (&idx)[2]) {
+                    float acc[2][8];
+                    group_dots<2, 8>(rows, Wp, P, no, P, acc);
+                    // lane 8 r + o (< 16): output o_lo + o of row r
+                    const float v = transpose_sum16(reinterpret_cast<float (&)[16]>(acc));
+                    const int r = (lane >> 3) & 1, o = lane & 7;
+                    if (lane < 16 && o < no && idx[r] >= 0)
                         __stcg(d.p + (size_t)d.ids[eb[idx[r]]] * J + o_lo + o, v + bp_s[o]);
                 });
             if (!__syncthreads_and(ok)) return false;  // also orders the p stores before the reads below
@@ -400,19 +419,21 @@ __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
         // ---- A: logits of this CTA's classes for every active slot, argmax key
         bool ok = true;
         if (nc > 0)
-            ok = ring_pass<4>(
+            ok = ring_pass<2>(
                 R, par, na, J, [&](int i) { return d.u + (size_t)A[i] * J; },
-                [&](const float* const (&rows)[4], const int (&idx)[4]) {
-                    // lane 8 r + v: class c0 + v of row r; the running best of row r
-                    // (largest logit, lowest class on ties) ends in lane 8 r
-                    const int r = lane >> 3, v = lane & 7;
+                [&](const float* const (&rows)[2], const int (&idx)[2]) {
+                    // lane 8 r + v (and 8 r + v + 16): class c0 + v of row r; the
+                    // running best of row r (largest logit, lowest class on ties)
+                    // ends in lane 8 r.  Groups of two rows keep two groups of rows
+                    // in flight in each warp's ring slots while one is computed.
+                    const int r = (lane >> 3) & 1, v = lane & 7;
                     float best = -FLT_MAX;
                     int bi = INT_MAX;
                     for (int c0 = 0; c0 < nc; c0 += 8) {
                         const int nv = min(8, nc - c0);
-                        float acc[4][8];
-                        group_dots<4, 8>(rows, Wo + (size_t)c0 * J, J, nv, J, acc);
-                        float x = transpose_sum32(reinterpret_cast<float (&)[32]>(acc));
+                        float acc[2][8];
+                        group_dots<2, 8>(rows, Wo + (size_t)c0 * J, J, nv, J, acc);
+                        float x = transpose_sum16(reinterpret_cast<float (&)[16]>(acc));
                         int k = c0 + v;
                         if (v < nv) x += bo_s[c0 + v];
                         else x = -FLT_MAX, k = INT_MAX;
@@ -430,7 +451,7 @@ __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
                             bi = k;
                         }
                     }
-                    if (v == 0 && idx[r] >= 0) atomicMax(keys + A[idx[r]], pack_key(best, c_lo + bi));
+                    if (lane < 16 && v == 0 && idx[r] >= 0) atomicMax(keys + A[idx[r]], pack_key(best, c_lo + bi));
                 });
         if (!__syncthreads_and(ok)) {
             if (tid == 0) fail_abort(d);
