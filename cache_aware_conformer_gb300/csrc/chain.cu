@@ -222,7 +222,7 @@ __device__ __forceinline__ void run_epilogue(const EpiParams& ep, int row, int M
             break;
         case EPI_GLUDW:
             epi_prefetch<EPI_GLUDW>(ep, row, col, pre);
-            epilogue_gludw(ep, row, live, col, v, pre);
+            epilogue_gludw(ep, row, live, col, v, pre, nullptr, nullptr, nullptr);
             break;
         default: break;
     }

@@ -486,12 +486,40 @@ __device__ __forceinline__ void epilogue32(const EpiParams& e, int row, int col0
 
 // EPI_GLUDW for one 32-column accumulator segment (16 output channels); every
 // lane of the warp calls it (shuffles), `live` marks rows < M.
+// win: the lane's stream in the GEMM's shared-memory copy of the conv ring
+// ([slot][32 channels], offset to this chunk's 16 channels), or nullptr to
+// read the ring in global memory.  prm: the GEMM's shared-memory copy of the
+// per-channel constants offset to this chunk's channels (rows of 32 floats:
+// 0-8 the taps, 9 the conv bias, 10 gamma, 11 beta), csum: its copy of
+// ln_colsum offset to this chunk's columns; both nullptr to read them in
+// global memory.
 __device__ __forceinline__ void epilogue_gludw(const EpiParams& e, int row, bool live, int col0, float (&v)[32],
-                                               const EpiPre& pre) {
+                                               const EpiPre& pre, const bf16* win, const float* prm,
+                                               const float* csum) {
     const int lane = threadIdx.x & 31;
     const int D = e.D, C = col0 >> 1, nq = e.nq;
     if (kChecked && pre.dw_id < 0) live = false;  // an id or position out of range (latched)
-    if (e.ln_stats) ln_fold32(e, col0, pre, v);
+    if (e.ln_stats) {
+        if (csum) {
+            const float4* c4 = reinterpret_cast<const float4*>(csum);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 c = c4[i];
+                v[4 * i] = pre.ln_rstd * fmaf(-pre.ln_mean, c.x, v[4 * i]);
+                v[4 * i + 1] = pre.ln_rstd * fmaf(-pre.ln_mean, c.y, v[4 * i + 1]);
+                v[4 * i + 2] = pre.ln_rstd * fmaf(-pre.ln_mean, c.z, v[4 * i + 2]);
+                v[4 * i + 3] = pre.ln_rstd * fmaf(-pre.ln_mean, c.w, v[4 * i + 3]);
+            }
+        } else {
+            ln_fold32(e, col0, pre, v);
+        }
+    }
+    // per-channel constant rows: shared memory (row stride 32) or global (row stride D)
+    auto cvec = [&](int r, int q) -> float4 {
+        if (prm) return reinterpret_cast<const float4*>(prm + r * 32)[q];
+        const float* g = r < 9 ? e.dw_wT + (long long)r * D : (r == 9 ? e.dw_bias : (r == 10 ? e.dw_gamma : e.dw_beta));
+        return __ldg(reinterpret_cast<const float4*>(g + C) + q);
+    };
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const float4 b = pre.b[i];
@@ -504,13 +532,10 @@ __device__ __forceinline__ void epilogue_gludw(const EpiParams& e, int row, bool
     const int id = live ? pre.dw_id : 0, p0 = live ? pre.dw_p0 : 0;  // loaded ahead (epi_prefetch)
     bf16* ring = static_cast<bf16*>(e.dw_ring) + (long long)id * e.dw_sstride;
     float acc[16];
-    {
-        const float4* b4 = reinterpret_cast<const float4*>(e.dw_bias + C);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 t = __ldg(b4 + q);
-            acc[4 * q] = t.x; acc[4 * q + 1] = t.y; acc[4 * q + 2] = t.z; acc[4 * q + 3] = t.w;
-        }
+    for (int q = 0; q < 4; ++q) {
+        const float4 t = cvec(9, q);
+        acc[4 * q] = t.x; acc[4 * q + 1] = t.y; acc[4 * q + 2] = t.z; acc[4 * q + 3] = t.w;
     }
     // taps k = 0 .. 7 (d = 8 - k frames back): this step's earlier rows by
     // shuffle, older frames from the conv ring (slot = frame mod 8, zero before
@@ -523,7 +548,8 @@ __device__ __forceinline__ void epilogue_gludw(const EpiParams& e, int row, bool
         for (int j = 0; j < TB; ++j) {
             const int d = 8 - (k0 + j), pabs = p0 + fi - d;
             if (d > fi && live && pabs >= 0) {
-                const uint4* src = reinterpret_cast<const uint4*>(ring + (long long)(pabs & 7) * D + C);
+                const uint4* src = win ? reinterpret_cast<const uint4*>(win + (pabs & 7) * 32)
+                                       : reinterpret_cast<const uint4*>(ring + (long long)(pabs & 7) * D + C);
                 r[j][0] = src[0];
                 r[j][1] = src[1];
             } else {
@@ -549,10 +575,9 @@ __device__ __forceinline__ void epilogue_gludw(const EpiParams& e, int row, bool
                     win[2 * i] = a0.x; win[2 * i + 1] = a0.y; win[8 + 2 * i] = a1.x; win[8 + 2 * i + 1] = a1.y;
                 }
             }
-            const float4* w4 = reinterpret_cast<const float4*>(e.dw_wT + (long long)k * D + C);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float4 w = __ldg(w4 + q);
+                const float4 w = cvec(k, q);
                 acc[4 * q] = fmaf(w.x, win[4 * q], acc[4 * q]);
                 acc[4 * q + 1] = fmaf(w.y, win[4 * q + 1], acc[4 * q + 1]);
                 acc[4 * q + 2] = fmaf(w.z, win[4 * q + 2], acc[4 * q + 2]);
@@ -561,10 +586,9 @@ __device__ __forceinline__ void epilogue_gludw(const EpiParams& e, int row, bool
         }
     }
     {   // tap 8 (d = 0): this row's own GLU value
-        const float4* w4 = reinterpret_cast<const float4*>(e.dw_wT + 8LL * D + C);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float4 w = __ldg(w4 + q);
+            const float4 w = cvec(8, q);
             acc[4 * q] = fmaf(w.x, g[4 * q], acc[4 * q]);
             acc[4 * q + 1] = fmaf(w.y, g[4 * q + 1], acc[4 * q + 1]);
             acc[4 * q + 2] = fmaf(w.z, g[4 * q + 2], acc[4 * q + 2]);
@@ -573,12 +597,10 @@ __device__ __forceinline__ void epilogue_gludw(const EpiParams& e, int row, bool
     }
     __syncwarp();  // every lane has read the ring before this step's rows are committed
     if (!live) return;
-    const float4* g4 = reinterpret_cast<const float4*>(e.dw_gamma + C);
-    const float4* be4 = reinterpret_cast<const float4*>(e.dw_beta + C);
     float y[16];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const float4 gg = __ldg(g4 + q), bb = __ldg(be4 + q);
+        const float4 gg = cvec(10, q), bb = cvec(11, q);
         y[4 * q] = siluf_(fmaf(gg.x, acc[4 * q], bb.x));
         y[4 * q + 1] = siluf_(fmaf(gg.y, acc[4 * q + 1], bb.y));
         y[4 * q + 2] = siluf_(fmaf(gg.z, acc[4 * q + 2], bb.z));

@@ -41,13 +41,22 @@ constexpr int A_TILE = BM * BK * 2;  // bytes
 // SPLIT: the A operand is a split pair (hi, lo) of bf16 tiles per K slice (hi
 // at column k, lo at column K + k of the A tensor map); both are multiplied by
 // the same B tile into the same accumulator.
-template <int BN, int SPLIT>
+// WIN (the fused GLU + depthwise-conv epilogue at BN = 64): a shared-memory copy
+// of the conv-ring rows of the tile's streams, [stream][slot][32 channels]
+// bf16 for up to 64 streams (two or more frames per stream), loaded by the
+// idle warps before the wait on the previous kernel (the rows were written a
+// step earlier); one ring stage fewer makes room for it.
+template <int BN, int SPLIT, int KIND>
 struct TcCfg {
+    static constexpr bool HAS_WIN = KIND == EPI_GLUDW && BN == 64;
+    static constexpr int WIN = HAS_WIN ? 64 * 8 * 32 * 2 : 0;
+    static constexpr int PRM = HAS_WIN ? (12 * 32 + 64) * 4 : 0;  // conv constants and LayerNorm column sums
     static constexpr int B_TILE = BN * BK * 2;
     static constexpr int A_TILES = A_TILE * (1 + SPLIT);
     static constexpr int STAGE = A_TILES + B_TILE;
-    static constexpr int STAGES = SPLIT ? ((BN == 256) ? 3 : (BN == 128 ? 4 : 5)) : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
-    static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/ + BM * 8 /*row stats*/;
+    static constexpr int STAGES = SPLIT ? ((BN == 256) ? 3 : (BN == 128 ? 4 : (HAS_WIN ? 4 : 5)))
+                                        : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
+    static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/ + BM * 8 /*row stats*/ + WIN + PRM;
     static_assert(STAGES * STAGE >= BN * BM * 4, "split-K partial tile must fit the pipeline buffers");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
@@ -59,7 +68,7 @@ template <int BN, int KIND, class TAct, int SPLIT>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
                    int K, int conv_C, EpiParams ep, int* status) {
-    using C = TcCfg<BN, SPLIT>;
+    using C = TcCfg<BN, SPLIT, KIND>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
@@ -71,6 +80,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // LayerNorm statistics of the tile's rows, computed once per row by warps
     // 2-5 while the main loop runs (warps 0 and 1 are busy in it)
     float2* rowstat = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(full) + 256);
+    bf16* win = reinterpret_cast<bf16*>(rowstat + BM);  // C::WIN bytes
+    float* prm = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(win) + C::WIN);  // C::PRM bytes
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
@@ -149,6 +160,57 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         tc_commit(accb);
     }
+    // conv-ring window of the tile's streams (GLU + depthwise epilogue): the
+    // slots hold frames of earlier steps, final before this kernel started, so
+    // the idle warps copy them while the previous kernel finishes, with the
+    // per-channel constants of the tile's 32 channels and the LayerNorm
+    // column sums of its 64 columns
+    const bool use_win = C::HAS_WIN && ep.nq >= 2;
+    if constexpr (C::HAS_WIN) {
+        if (warp >= 2) {
+            const int C0 = n0 >> 1;
+            for (int i = threadIdx.x - 64; i < 12 * 32 + 64; i += TC_THREADS - 64) {
+                float v;
+                if (i < 9 * 32) v = __ldg(ep.dw_wT + (long long)(i >> 5) * ep.D + C0 + (i & 31));
+                else if (i < 10 * 32) v = __ldg(ep.dw_bias + C0 + i - 9 * 32);
+                else if (i < 11 * 32) v = __ldg(ep.dw_gamma + C0 + i - 10 * 32);
+                else if (i < 12 * 32) v = __ldg(ep.dw_beta + C0 + i - 11 * 32);
+                else v = ep.ln_colsum ? __ldg(ep.ln_colsum + n0 + i - 12 * 32) : 0.f;
+                prm[i] = v;
+            }
+        }
+        if (use_win && warp >= 2) {
+            // 16-byte pieces idx = (stream, slot, quarter of 8 channels), in batches
+            // whose stream ids and then ring rows are all requested before any
+            // is used (one dependent round trip each per batch)
+            constexpr int LT = TC_THREADS - 64, PER = 6;
+            const int nS = BM / ep.nq, sb0 = m0 / ep.nq, C0 = n0 >> 1, t = threadIdx.x - 64;
+            const bf16* ring = static_cast<const bf16*>(ep.dw_ring);
+            uint4* w4 = reinterpret_cast<uint4*>(win);
+            for (int j0 = 0; j0 * LT < nS * 32; j0 += PER) {
+                int id[PER];
+#pragma unroll
+                for (int j = 0; j < PER; ++j) {
+                    const int idx = t + (j0 + j) * LT, b = sb0 + (idx >> 5);
+                    id[j] = (idx < nS * 32 && b * ep.nq < ep.dw_rows) ? ep.ids[b] : -1;
+                }
+                uint4 v[PER];
+#pragma unroll
+                for (int j = 0; j < PER; ++j) {
+                    const int idx = t + (j0 + j) * LT, slot = (idx >> 2) & 7, q = idx & 3;
+                    v[j] = make_uint4(0u, 0u, 0u, 0u);
+                    if (id[j] >= 0 && id[j] < ep.n_streams)  // an id out of range is latched by epi_prefetch
+                        v[j] = *reinterpret_cast<const uint4*>(ring + (long long)id[j] * ep.dw_sstride +
+                                                               (long long)slot * ep.D + C0 + 8 * q);
+                }
+#pragma unroll
+                for (int j = 0; j < PER; ++j) {
+                    const int idx = t + (j0 + j) * LT;
+                    if (idx < nS * 32) w4[idx] = v[j];
+                }
+            }
+        }
+    }
     __syncwarp();
     pdl_wait();  // the epilogue reads/writes buffers of earlier kernels
     const int quarter = warp & 3, half = warp >> 2;
@@ -161,6 +223,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (row_stats && warp >= 2 && warp < 6) rowstat[(warp - 2) * 32 + lane] = epi_row_stats(ep, m0 + (warp - 2) * 32 + lane);
 
     if (!mbar_wait(accb, 0)) ok = false;
+    if constexpr (C::HAS_WIN) {
+        if (!row_stats) __syncthreads();  // the conv-ring window and constants are in shared memory
+    }
     if (row_stats) {
         __syncthreads();  // the row statistics are in shared memory
         if (row < M || KIND == EPI_GLUDW) epi_apply_stats(rowstat[rloc], pre);
@@ -169,7 +234,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_fence_after();
     // partial tile [BN columns][128 rows] fp32 in the pipeline buffers (idle now)
     float* part = reinterpret_cast<float*>(sA);
-    static_assert(C::STAGES * C::B_TILE >= 8 * EPI_STAGE_FLOATS * 4, "epilogue staging");
+    static_assert(KIND == EPI_GLUDW || C::STAGES * C::B_TILE >= 8 * EPI_STAGE_FLOATS * 4, "epilogue staging");
     float* stage = reinterpret_cast<float*>(sB) + warp * EPI_STAGE_FLOATS;
     if (splits > 1 && crank != 0) {
 #pragma unroll 1
@@ -195,7 +260,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     epi_prefetch<KIND>(ep, row, n0 + c, pre, !row_stats);
                     if (row_stats) epi_apply_stats(rowstat[rloc], pre);
                 }
-                epilogue_gludw(ep, row, ok && row < M, n0 + c, v, pre);
+                epilogue_gludw(ep, row, ok && row < M, n0 + c, v, pre,
+                               use_win ? win + (rloc / ep.nq) * 256 + (c >> 1) : nullptr,
+                               C::HAS_WIN ? prm + (c >> 1) : nullptr, C::HAS_WIN ? prm + 12 * 32 + c : nullptr);
             } else {
                 // every lane: the row stores go through this warp's slice of the
                 // (idle) B ring
@@ -281,7 +348,7 @@ bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t 
 template <int BN, int KIND, int SPLIT>
 static cudaError_t launch_bn_kind(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int conv_C,
                                   int splits, const EpiParams& ep, int* status, cudaStream_t s) {
-    using C = TcCfg<BN, SPLIT>;
+    using C = TcCfg<BN, SPLIT, KIND>;
     auto kern = gemm_tc_kernel<BN, KIND, bf16, SPLIT>;
     static bool attr_set = false;  // per instantiation, per process
     if (!attr_set) {
