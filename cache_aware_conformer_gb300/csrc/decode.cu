@@ -68,7 +68,7 @@ __host__ __device__ constexpr int bias_floats(int nc_max, int no_max) { return (
 struct DecParams {
     int n, T, C, P, J, max_sym, blank, maxit, S;
     int nc_max, nu_max, no_max;  // largest class / hidden-unit / projection-output slice of a CTA
-    int RB;                      // ring slots, a multiple of NW
+    int RB;                      // ring slots, a multiple of 2 NW (pairs of slots for the joint)
     const int* ids;
     const float* z;
     long long zb;
@@ -102,7 +102,6 @@ __device__ bool grid_sync(const DecParams& d, unsigned& target) {
     target += gridDim.x;
     if (threadIdx.x == 0) {
         int ok = 1;
-        __threadfence();
         asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(d.bar) : "memory");
         if (ld_acquire(d.bar) < target) {
             const long long t0 = clock64();
@@ -119,7 +118,6 @@ __device__ bool grid_sync(const DecParams& d, unsigned& target) {
                 }
             }
         }
-        __threadfence();
         ok_s = ok;
     }
     __syncthreads();
@@ -277,6 +275,53 @@ __device__ bool ring_pass(const Ring& R, uint32_t& par, int m, int rowK, Src src
     return true;
 }
 
+// The same ring with slots of two rows (RB / 2 pair slots, a multiple of NW):
+// pair p holds rows 2p and 2p + 1 of the pass (src(i) as above) and comes in
+// one bulk copy when the two rows are adjacent in global memory (consecutive
+// slots), in two otherwise, so that a pass over consecutive rows issues half
+// as many copies.  use(rows, idx) as for RG = 2.
+template <class Src, class Use>
+__device__ bool ring_pass_pairs(const Ring& R, uint32_t& par, int m, int rowK, Src src, Use use) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int RBP = R.RB / 2, np = (m + 1) / 2;
+    auto issue = [&](int p, int s) {
+        const int i0 = 2 * p, cnt = i0 + 1 < m ? 2 : 1;
+        const float* a = src(i0);
+        float* dst = R.buf + (size_t)s * 2 * R.K;
+        mbar_expect_tx(&R.full[s], (uint32_t)(cnt * rowK) * 4u);
+        if (cnt == 2) {
+            const float* b = src(i0 + 1);
+            if (b == a + rowK && rowK == R.K) {
+                bulk_g2s(dst, a, (uint32_t)(2 * rowK) * 4u, &R.full[s]);
+                return;
+            }
+            bulk_g2s(dst + R.K, b, (uint32_t)rowK * 4u, &R.full[s]);
+        }
+        bulk_g2s(dst, a, (uint32_t)rowK * 4u, &R.full[s]);
+    };
+    if (lane == 0) {
+        fence_proxy_async_smem();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        for (int p = warp; p < np && p < RBP; p += NW) issue(p, p);
+    }
+    __syncwarp();
+    for (int p = warp; p < np; p += NW) {
+        const int s = p % RBP, j = s / NW;
+        if (!mbar_wait(&R.full[s], (par >> j) & 1u)) return false;
+        par ^= 1u << j;
+        const float* rows[2] = {R.buf + (size_t)s * 2 * R.K, R.buf + (size_t)s * 2 * R.K + R.K};
+        const int idx[2] = {2 * p, 2 * p + 1 < m ? 2 * p + 1 : -1};
+        if (idx[1] < 0) rows[1] = rows[0];
+        use(rows, idx);
+        __syncwarp();
+        if (lane == 0 && p + RBP < np) {
+            fence_proxy_async_smem();
+            issue(p + RBP, s);
+        }
+    }
+    return true;
+}
+
 __device__ __forceinline__ void fail_abort(const DecParams& d) {
     latch_error(d.status, CAC_E_TIMEOUT);
     atomicExch(d.abort_flag, 1);
@@ -310,6 +355,13 @@ __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
     int* ek = eb + S;                                 // their classes
     int* eh = ek + S;                                 // their h copy before the step
     const Ring R{rbuf, ring_full, d.RB, K};
+    // every CTA reads the same rows (all active slots, all emitting slots): CTA
+    // g starts its pass at row g m / G, so that the CTAs do not all request the
+    // same lines of L2 at the same moment
+    auto rot = [&](int i, int m) {
+        const int j = i + (int)(((long long)g * m) / G);
+        return j >= m ? j - m : j;
+    };
     uint32_t par = 0;
     unsigned gt = 0;  // grid-barrier target
     const long long tsym = (long long)d.T * d.max_sym;
@@ -382,7 +434,10 @@ __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
         if (ne_ > 0 && no > 0) {
             const bool ok = ring_pass<2>(
                 R, par, ne_, P,
-                [&](int e) { return d.h + ((size_t)(eh[e] ^ 1) * S + d.ids[eb[e]]) * P; },
+                [&](int e) {
+                    const int q = rot(e, ne_);
+                    return d.h + ((size_t)(eh[q] ^ 1) * S + d.ids[eb[q]]) * P;
+                },
                 [&](const float* const (&rows)[2], const int (&idx)[2]) {
                     float acc[2][8];
                     group_dots<2, 8>(rows, Wp, P, no, P, acc);
@@ -390,7 +445,7 @@ __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
                     const float v = transpose_sum16(reinterpret_cast<float (&)[16]>(acc));
                     const int r = (lane >> 3) & 1, o = lane & 7;
                     if (lane < 16 && o < no && idx[r] >= 0)
-                        __stcg(d.p + (size_t)d.ids[eb[idx[r]]] * J + o_lo + o, v + bp_s[o]);
+                        __stcg(d.p + (size_t)d.ids[eb[rot(idx[r], ne_)]] * J + o_lo + o, v + bp_s[o]);
                 });
             if (!__syncthreads_and(ok)) return false;  // also orders the p stores before the reads below
         }
@@ -419,8 +474,8 @@ __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
         // ---- A: logits of this CTA's classes for every active slot, argmax key
         bool ok = true;
         if (nc > 0)
-            ok = ring_pass<2>(
-                R, par, na, J, [&](int i) { return d.u + (size_t)A[i] * J; },
+            ok = ring_pass_pairs(
+                R, par, na, J, [&](int i) { return d.u + (size_t)A[rot(i, na)] * J; },
                 [&](const float* const (&rows)[2], const int (&idx)[2]) {
                     // lane 8 r + v (and 8 r + v + 16): class c0 + v of row r; the
                     // running best of row r (largest logit, lowest class on ties)
@@ -451,14 +506,29 @@ __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
                             bi = k;
                         }
                     }
-                    if (lane < 16 && v == 0 && idx[r] >= 0) atomicMax(keys + A[idx[r]], pack_key(best, c_lo + bi));
+                    if (lane < 16 && v == 0 && idx[r] >= 0)
+                        atomicMax(keys + A[rot(idx[r], na)], pack_key(best, c_lo + bi));
                 });
         if (!__syncthreads_and(ok)) {
             if (tid == 0) fail_abort(d);
             return;
         }
         if (!grid_sync(d, gt)) return;
-        // ---- B: the decisions of every active slot, in every CTA alike
+        // ---- B: the decisions of every active slot, in every CTA alike.  When
+        // the active list fits the ring, the LSTM's h rows of all active slots
+        // are requested first (any of them may emit), so that they arrive while
+        // the keys are read and the decisions taken.
+        const bool pre_h = nu > 0 && na <= d.RB;
+        if (pre_h && lane == 0) {
+            fence_proxy_async_smem();
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            for (int i = warp; i < na; i += NW) {
+                const int b = A[i];
+                mbar_expect_tx(&R.full[i], (uint32_t)P * 4u);
+                bulk_g2s(R.buf + (size_t)i * K, d.h + ((size_t)cur[b] * S + d.ids[b]) * P, (uint32_t)P * 4u,
+                         &R.full[i]);
+            }
+        }
         for (int i = tid; i < na; i += DT) dec[i] = key_class(__ldcg(keys + A[i]));
         // the other parity's keys serve the next iteration (all its readers passed a barrier)
         for (int b = g * DT + tid; b < n; b += G * DT) d.keys[(size_t)((it + 1) & 1) * S + b] = 0ull;
@@ -512,54 +582,88 @@ __global__ void __launch_bounds__(DT, 1) dec_step_kernel(DecParams d) {
         __syncthreads();
         ne = s_cnt[0];
         const int nn = s_cnt[1];
-        // ---- C: LSTM step of this CTA's units for the emitting slots
-        if (ne > 0) {
-            ok = true;
-            if (nu > 0)
-                ok = ring_pass<2>(
-                    R, par, ne, P, [&](int e) { return d.h + ((size_t)eh[e] * S + d.ids[eb[e]]) * P; },
-                    [&](const float* const (&rows)[2], const int (&idx)[2]) {
-                        // lane uu < nu: its unit's table entries and cell state, loaded
-                        // ahead of the dot products
-                        float t4[2][4], cold[2];
+        // ---- C: LSTM step of this CTA's units for the emitting slots.  A group
+        // of up to two rows: row r is stream id[r], class k[r], h copy hc[r] (its
+        // new h goes to the other copy), live when id[r] >= 0.
+        auto lstm_group = [&](const float* const (&rows)[2], const int (&idv)[2], const int (&kv)[2],
+                              const int (&hcv)[2]) {
+            // lane uu < nu: its unit's table entries and cell state, loaded ahead of the dot products
+            float t4[2][4], cold[2];
 #pragma unroll
-                        for (int r = 0; r < 2; ++r) {
-                            t4[r][0] = t4[r][1] = t4[r][2] = t4[r][3] = cold[r] = 0.f;
-                            if (lane < nu && idx[r] >= 0) {
-                                const int e = idx[r];
-                                const float* tb = d.tab + (size_t)ek[e] * 4 * P + u_lo + lane;
-                                t4[r][0] = __ldg(tb);
-                                t4[r][1] = __ldg(tb + P);
-                                t4[r][2] = __ldg(tb + 2 * P);
-                                t4[r][3] = __ldg(tb + 3 * P);
-                                cold[r] = __ldcg(d.c + (size_t)d.ids[eb[e]] * P + u_lo + lane);
-                            }
-                        }
-                        float acc[2][32];
-                        group_dots<2, 32>(rows, Wh, P, 4 * nu, P, acc);
-#pragma unroll
-                        for (int r = 0; r < 2; ++r) {
-                            // lane q nu + uu: gate q of unit uu; gather a unit's 4 gates in lane uu
-                            const float gsum = transpose_sum32(acc[r]);
-                            float gm[4];
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) gm[q] = __shfl_sync(0xffffffffu, gsum, min(q * nu + lane, 31));
-                            if (lane < nu && idx[r] >= 0) {
-                                const int e = idx[r], id = d.ids[eb[e]], j = u_lo + lane;
-                                const float gi = gm[0] + t4[r][0], gf = gm[1] + t4[r][1];
-                                const float gg = gm[2] + t4[r][2], go = gm[3] + t4[r][3];
-                                const float c2 = sigm(gf) * cold[r] + sigm(gi) * tanhf(gg);
-                                __stcg(d.c + (size_t)id * P + j, c2);
-                                __stcg(d.h + ((size_t)(eh[e] ^ 1) * S + id) * P + j, sigm(go) * tanhf(c2));
-                            }
-                        }
-                    });
-            if (!__syncthreads_and(ok)) {
-                if (tid == 0) fail_abort(d);
-                return;
+            for (int r = 0; r < 2; ++r) {
+                t4[r][0] = t4[r][1] = t4[r][2] = t4[r][3] = cold[r] = 0.f;
+                if (lane < nu && idv[r] >= 0) {
+                    const float* tb = d.tab + (size_t)kv[r] * 4 * P + u_lo + lane;
+                    t4[r][0] = __ldg(tb);
+                    t4[r][1] = __ldg(tb + P);
+                    t4[r][2] = __ldg(tb + 2 * P);
+                    t4[r][3] = __ldg(tb + 3 * P);
+                    cold[r] = __ldcg(d.c + (size_t)idv[r] * P + u_lo + lane);
+                }
             }
-            if (!grid_sync(d, gt)) return;
+            float acc[2][32];
+            group_dots<2, 32>(rows, Wh, P, 4 * nu, P, acc);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                // lane q nu + uu: gate q of unit uu; gather a unit's 4 gates in lane uu
+                const float gsum = transpose_sum32(acc[r]);
+                float gm[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) gm[q] = __shfl_sync(0xffffffffu, gsum, min(q * nu + lane, 31));
+                if (lane < nu && idv[r] >= 0) {
+                    const int id = idv[r], j = u_lo + lane;
+                    const float gi = gm[0] + t4[r][0], gf = gm[1] + t4[r][1];
+                    const float gg = gm[2] + t4[r][2], go = gm[3] + t4[r][3];
+                    const float c2 = sigm(gf) * cold[r] + sigm(gi) * tanhf(gg);
+                    __stcg(d.c + (size_t)id * P + j, c2);
+                    __stcg(d.h + ((size_t)(hcv[r] ^ 1) * S + id) * P + j, sigm(go) * tanhf(c2));
+                }
+            }
+        };
+        ok = true;
+        if (pre_h) {
+            // the active slots' h rows were requested before the decisions (row i
+            // of the active list in ring slot i): wait for every one, so that no
+            // copy is left in flight, and step the emitting slots
+            for (int i = warp; i < na; i += NW) {
+                const int j = i / NW;
+                if (!mbar_wait(&R.full[i], (par >> j) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                par ^= 1u << j;
+                if (dec[i] != d.blank) {
+                    const int b = A[i];
+                    const float* rows[2] = {R.buf + (size_t)i * K, R.buf + (size_t)i * K};
+                    const int idv[2] = {d.ids[b], -1}, kv[2] = {dec[i], 0}, hcv[2] = {cur[b] ^ 1, 0};
+                    lstm_group(rows, idv, kv, hcv);
+                }
+                __syncwarp();
+            }
+        } else if (ne > 0 && nu > 0) {
+            ok = ring_pass<2>(
+                R, par, ne, P,
+                [&](int e) {
+                    const int q = rot(e, ne);
+                    return d.h + ((size_t)eh[q] * S + d.ids[eb[q]]) * P;
+                },
+                [&](const float* const (&rows)[2], const int (&idx)[2]) {
+                    int idv[2], kv[2], hcv[2];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int q = idx[r] >= 0 ? rot(idx[r], ne) : 0;
+                        idv[r] = idx[r] >= 0 ? d.ids[eb[q]] : -1;
+                        kv[r] = idx[r] >= 0 ? ek[q] : 0;
+                        hcv[r] = idx[r] >= 0 ? eh[q] : 0;
+                    }
+                    lstm_group(rows, idv, kv, hcv);
+                });
         }
+        if (!__syncthreads_and(ok)) {
+            if (tid == 0) fail_abort(d);
+            return;
+        }
+        if (ne > 0 && !grid_sync(d, gt)) return;
         // ---- D
         if (!phase_d(ne, N, nn)) {
             if (tid == 0) fail_abort(d);
@@ -755,7 +859,7 @@ extern "C" int cac_decoder_create(const cac_dec_config* cfg, const float* weight
                          sizeof(int) * STATE_INTS * S;
     const size_t budget = 227 * 1024 - 1024;  // less the kernel's static shared memory
     if (fixed + sizeof(float) * K * 4 * NW > budget) return fail(CAC_E_UNSUPPORTED);  // groups of 4 rows per warp
-    d->RB = (int)std::min<size_t>(RB_MAX, (budget - fixed) / (sizeof(float) * K) / NW * NW);
+    d->RB = (int)std::min<size_t>(RB_MAX, (budget - fixed) / (sizeof(float) * K) / (2 * NW) * (2 * NW));
     d->smem = fixed + sizeof(float) * K * d->RB;
     if (cudaFuncSetAttribute(dec_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)d->smem) !=
             cudaSuccess ||
