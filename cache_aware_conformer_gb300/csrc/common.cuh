@@ -204,6 +204,17 @@ __device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
     return v;
 }
 
+// shared::cluster address of the byte at `local`'s offset in CTA `rank`'s
+// shared memory, and a 4-byte store there
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    return remote;
+}
+__device__ __forceinline__ void st_dsmem_f32(uint32_t remote, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05 (5th-gen tensor core) wrappers
 // ---------------------------------------------------------------------------

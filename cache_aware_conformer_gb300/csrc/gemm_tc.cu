@@ -19,10 +19,11 @@
 // activation enters the product with ~16 significant bits while the
 // contraction stays bf16 x bf16 with fp32 accumulation.
 // Split-K: the `splits` CTAs of one output tile form a thread-block cluster
-// along z, each accumulating a contiguous range of K slices.  Ranks > 0 park
-// their fp32 partial tile in their (now idle) pipeline shared memory; rank 0
-// adds them over distributed shared memory in rank order (deterministic) and
-// runs the fused epilogue once.
+// along z, each accumulating a contiguous range of K slices.  Once every
+// rank's main loop is done (a cluster barrier), ranks > 0 store their fp32
+// partial tiles into rank 0's (now idle) pipeline shared memory over
+// distributed shared memory; after a second barrier rank 0 adds them in rank
+// order (deterministic) and runs the fused epilogue once.
 // Every mbarrier wait is bounded; a wait that gives up latches
 // CAC_E_TIMEOUT in the status word and the CTA unwinds without hanging.
 #include <cudaTypedefs.h>
@@ -57,7 +58,7 @@ struct TcCfg {
     static constexpr int STAGES = SPLIT ? ((BN == 256) ? 3 : (BN == 128 ? 4 : (HAS_WIN ? 4 : 5)))
                                         : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
     static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/ + BM * 8 /*row stats*/ + WIN + PRM;
-    static_assert(STAGES * STAGE >= BN * BM * 4, "split-K partial tile must fit the pipeline buffers");
+    static_assert(BN != 64 || STAGES * A_TILES >= 3 * BN * BM * 4, "split-K partial tiles must fit the A ring");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 }  // namespace
@@ -232,28 +233,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     pdl_trigger();  // main loop done: let the next kernel launch while the epilogue runs
     tc_fence_after();
-    // partial tile [BN columns][128 rows] fp32 in the pipeline buffers (idle now)
+    // split-K: the partial tiles of ranks 1 .. splits-1, [rank - 1][BN columns][128
+    // rows] fp32, land in rank 0's pipeline buffers (idle once every rank's main
+    // loop is done)
     float* part = reinterpret_cast<float*>(sA);
     static_assert(KIND == EPI_GLUDW || C::STAGES * C::B_TILE >= 8 * EPI_STAGE_FLOATS * 4, "epilogue staging");
     float* stage = reinterpret_cast<float*>(sB) + warp * EPI_STAGE_FLOATS;
-    if (splits > 1 && crank != 0) {
+    if (splits > 1) {
+        cluster_sync();  // every rank's main loop is done: rank 0's ring takes the partials
+        if (crank != 0) {
+            // pushed with remote stores (a warp writes one 128-byte column
+            // segment per store), so that rank 0 adds them from its own memory
+            const uint32_t dst = dsmem_addr(part + (size_t)(crank - 1) * BN * BM + rloc, 0);
 #pragma unroll 1
-        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
-            float v[32];
-            tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
+            for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
+                float v[32];
+                tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) part[(c + k) * BM + rloc] = v[k];
+                for (int k = 0; k < 32; ++k) st_dsmem_f32(dst + (uint32_t)((c + k) * BM) * 4u, v[k]);
+            }
         }
+        cluster_sync();  // the partials are in rank 0's shared memory
     }
-    if (splits > 1) cluster_sync();
     if (crank == 0) {
 #pragma unroll 1
         for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
             float v[32];
             tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
-            for (int rr = 1; rr < splits; ++rr) {
+            for (int rr = 1; rr < splits; ++rr) {  // in rank order (deterministic)
+                const float* pr = part + (size_t)(rr - 1) * BN * BM + rloc;
 #pragma unroll
-                for (int k = 0; k < 32; ++k) v[k] += ld_dsmem(&part[(c + k) * BM + rloc], (uint32_t)rr);
+                for (int k = 0; k < 32; ++k) v[k] += pr[(c + k) * BM];
             }
             if constexpr (KIND == EPI_GLUDW) {
                 if (c != c_first) {  // bias only: any row
@@ -275,7 +285,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
         }
     }
-    if (splits > 1) cluster_sync();  // keep every rank's partial alive until rank 0 has read it
     if (!ok) latch_error(status, CAC_E_TIMEOUT);
     tc_fence_before();
     __syncthreads();
@@ -391,6 +400,7 @@ cudaError_t launch_gemm_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, int M
     if (K % BK || K <= 0 || N % BN || !ep.act_bf16) return cudaErrorInvalidValue;
     if (conv_C && (conv_C % BK || K != 3 * conv_C)) return cudaErrorInvalidValue;
     if (splits < 1 || splits > 4 || splits > K / BK) return cudaErrorInvalidValue;
+    if (splits > 1 && BN != 64) return cudaErrorInvalidValue;  // rank 0's ring holds three 128 x 64 partials
     if (ep.kind == EPI_GLUDW && (splits != 1 || !a_split || ep.nq < 1 || 32 % ep.nq || 2 * ep.D != N || ep.D % 16))
         return cudaErrorInvalidValue;
     switch (BN) {
