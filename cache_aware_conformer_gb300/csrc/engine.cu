@@ -745,6 +745,14 @@ struct cac_pool {
     int* pinned = nullptr;
     cudaEvent_t slot_ev[ID_SLOTS] = {};
     int slot = 0;
+    // host buffers of a cac_stream_push_host call whose step runs as concurrent
+    // sub-batches: each sub-batch copies its slice in and out on its own stream
+    struct HostIO {
+        const float* mel = nullptr;  // page-locked source of the mel rows
+        float* enc = nullptr;        // page-locked destinations (nullptr: not wanted)
+        float* joint = nullptr;
+    } hio;
+    bool hio_on = false;
     // staging for cac_stream_push_host
     float* h_mel = nullptr;
     float* d_mel = nullptr;
@@ -1284,10 +1292,22 @@ int step(cac_pool* p, int nb, int n, const float* mel, long long mel_bstride, co
         const int b0 = g * per, nbg = std::min(per, nb - b0);
         if (nbg <= 0) break;
         CK(cudaStreamWaitEvent(p->gs[g], p->fork_ev, 0));
+        if (p->hio_on)  // this sub-batch's mel rows, from the caller's host buffer
+            CK(cudaMemcpyAsync(const_cast<float*>(mel) + (size_t)b0 * mel_bstride, p->hio.mel + (size_t)b0 * mel_bstride,
+                               (size_t)nbg * mel_bstride * sizeof(float), cudaMemcpyHostToDevice, p->gs[g]));
         RET(step_one(p, g, nbg, n, mel + (size_t)b0 * mel_bstride, mel_bstride, nullptr,
                      enc ? enc + (size_t)b0 * out_bstride * D : nullptr,
                      joint ? joint + (size_t)b0 * out_bstride * J : nullptr, out_bstride, out_off, p->ids_dev + b0,
                      p->gs[g]));
+        if (p->hio_on) {  // and its frames back, while the other sub-batches still run
+            const size_t eo = (size_t)b0 * out_bstride * D, jo = (size_t)b0 * out_bstride * J;
+            if (enc && p->hio.enc)
+                CK(cudaMemcpyAsync(p->hio.enc + eo, enc + eo, (size_t)nbg * out_bstride * D * sizeof(float),
+                                   cudaMemcpyDeviceToHost, p->gs[g]));
+            if (joint && p->hio.joint)
+                CK(cudaMemcpyAsync(p->hio.joint + jo, joint + jo, (size_t)nbg * out_bstride * J * sizeof(float),
+                                   cudaMemcpyDeviceToHost, p->gs[g]));
+        }
         CK(cudaEventRecord(p->join_ev[g], p->gs[g]));
         CK(cudaStreamWaitEvent(s, p->join_ev[g], 0));
     }
@@ -1696,13 +1716,30 @@ extern "C" int cac_stream_push_host(cac_pool* p, int n, const int* ids, const fl
     const bool mel_locked = locked(mel);
     const bool enc_locked = enc && locked(enc), joint_locked = joint && locked(joint);
     if (!mel_locked) std::memcpy(p->h_mel, mel, mel_n * 4);
-    CK(cudaMemcpyAsync(p->d_mel, mel_locked ? mel : p->h_mel, mel_n * 4, cudaMemcpyHostToDevice, s));
+    const float* src = mel_locked ? mel : p->h_mel;
+    float* he = enc ? (enc_locked ? enc : p->h_out) : nullptr;
+    float* hj = joint ? (joint_locked ? joint : p->h_out + enc_n) : nullptr;
     float* de = enc ? p->d_out : nullptr;
     float* dj = joint ? p->d_out + enc_n : nullptr;
-    RET(cac_stream_push(p, n, ids, p->d_mel, n_mel, de, dj, n_out, stream));
-    if (enc) CK(cudaMemcpyAsync(enc_locked ? enc : p->h_out, de, enc_n * 4, cudaMemcpyDeviceToHost, s));
-    if (joint)
-        CK(cudaMemcpyAsync(joint_locked ? joint : p->h_out + enc_n, dj, joint_n * 4, cudaMemcpyDeviceToHost, s));
+    // one chunked step that runs as concurrent sub-batches: the copies go with
+    // the sub-batches (each its own slice, on its own stream); otherwise one
+    // copy in before the push and the frames out after it
+    const int A = m->cfg.att_chunk;
+    const bool piped = m->cfg.right_context == 0 && frames <= (p->nmax / A) * A && step_groups(p, n, frames, false) > 1;
+    if (piped) {
+        p->hio.mel = src;
+        p->hio.enc = he;
+        p->hio.joint = hj;
+        p->hio_on = true;
+        const int r = cac_stream_push(p, n, ids, p->d_mel, n_mel, de, dj, n_out, stream);
+        p->hio_on = false;
+        RET(r);
+    } else {
+        CK(cudaMemcpyAsync(p->d_mel, src, mel_n * 4, cudaMemcpyHostToDevice, s));
+        RET(cac_stream_push(p, n, ids, p->d_mel, n_mel, de, dj, n_out, stream));
+        if (enc) CK(cudaMemcpyAsync(he, de, enc_n * 4, cudaMemcpyDeviceToHost, s));
+        if (joint) CK(cudaMemcpyAsync(hj, dj, joint_n * 4, cudaMemcpyDeviceToHost, s));
+    }
     CK(cudaStreamSynchronize(s));
     if (enc && !enc_locked) std::memcpy(enc, p->h_out, enc_n * 4);
     if (joint && !joint_locked) std::memcpy(joint, p->h_out + enc_n, joint_n * 4);

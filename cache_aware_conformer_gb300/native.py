@@ -162,9 +162,22 @@ def weights_size(cfg: ModelConfig) -> int:
     return int(_lib().cac_weights_size(ctypes.byref(c)))
 
 
+_IDS_CACHE: dict = {}
+
+
 def _ids(ids) -> ctypes.Array:
-    ids = [int(i) for i in ids]
-    return (c_int * len(ids))(*ids)
+    """ids as a C int array.  The same id list pushed again (a pool's streams,
+    every step) reuses its array: the library only reads it, and building a
+    256-entry ctypes array costs more than the lookup."""
+    key = tuple(ids)
+    arr = _IDS_CACHE.get(key)
+    if arr is None:
+        vals = [int(i) for i in key]
+        arr = (c_int * len(vals))(*vals)
+        if len(_IDS_CACHE) >= 64:
+            _IDS_CACHE.clear()
+        _IDS_CACHE[key] = arr
+    return arr
 
 
 def _ptr(t) -> int | None:

@@ -249,6 +249,32 @@ def test_push_host_matches_device_push():
     assert n2 == [8] and np.array_equal(e0, e2.numpy()) and np.array_equal(j0, j2.numpy())
 
 
+def test_push_host_sub_batches_match_device_push():
+    """A host-buffer push over 256 streams runs as concurrent 64-stream
+    sub-batches that copy their own mel slices in and frames out: equal to the
+    device push of the same mel bit for bit, over several 160 ms steps (graph
+    replay on both pools), with page-locked and with pageable buffers."""
+    from cache_aware_conformer_gb300 import native
+    cfg = EOU2
+    _, model = make_model(cfg)
+    S = 256
+    pools = [native.Pool(model, S, 2) for _ in range(3)]
+    for p in pools:
+        p.set_graphs(True)
+    ids = [[p.create_stream() for _ in range(S)] for p in pools]
+    out = (torch.empty(S, 2, cfg.d_model).pin_memory(), torch.empty(S, 2, cfg.joint_dim).pin_memory())
+    for step in range(4):
+        mel = np.stack([synth.make_mel(16, 100 * step + s) for s in range(S)])
+        e0, j0, _ = _push(pools[0], ids[0], list(mel))
+        e1, j1, n1 = pools[1].push_host(ids[1], torch.from_numpy(mel).pin_memory(), out=out)
+        e2, j2, n2 = pools[2].push_host(ids[2], mel)
+        assert n1 == [2] * S and n2 == [2] * S
+        assert np.array_equal(e0, e1.numpy()) and np.array_equal(j0, j1.numpy()), step
+        assert np.array_equal(e0, e2) and np.array_equal(j0, j2), step
+    for p in pools:
+        p.check()
+
+
 def test_c600m_shape_multistream():
     """The 600M encoder's layer shapes (d_model 1024, 16 heads, ff 4096), two
     layers, three streams with 160 / 320 / 640 ms pushes and a ragged flush."""
