@@ -435,6 +435,15 @@ int gemm(cac_model* m, const void* A, long long lda, int M, int K, const Lin& W,
             ++*launches;
             return CAC_OK;
         }
+        // long K (the FF down-projections): 128-column tiles split 4 ways over K,
+        // each rank finishing one 32-column chunk (owner mode; CAC_SPLIT_OWNER=0
+        // keeps 64-column tiles finished by rank 0)
+        static const bool owner_on = env_int("CAC_SPLIT_OWNER", 1, 0, 1) != 0;
+        if (owner_on && W.has128 && !conv_C && ep.kind != EPI_GLUDW && K / 64 >= 32) {
+            CK(launch_gemm_tc(&tmA, &W.tm128, M, W.N, K, 128, conv_C, 4, a_split, ep, m->status, s));
+            ++*launches;
+            return CAC_OK;
+        }
         // the fused depthwise conv reads its stream's rows within one CTA: no split-K
         const int splits = ep.kind == EPI_GLUDW ? 1 : choose_splits((W.N / W.BN) * ((M + 127) / 128), K / 64);
         CK(launch_gemm_tc(&tmA, &W.tm, M, W.N, K, W.BN, conv_C, splits, a_split, ep, m->status, s));

@@ -59,6 +59,7 @@ struct TcCfg {
                                         : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
     static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/ + BM * 8 /*row stats*/ + WIN + PRM;
     static_assert(BN != 64 || STAGES * A_TILES >= 3 * BN * BM * 4, "split-K partial tiles must fit the A ring");
+    static_assert(BN != 128 || STAGES * A_TILES >= 3 * 32 * BM * 4, "owner-mode partial chunks must fit the A ring");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 }  // namespace
@@ -217,10 +218,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int quarter = warp & 3, half = warp >> 2;
     const int rloc = quarter * 32 + lane;
     const int row = m0 + rloc;
-    const int c_first = half * (BN / 2);
+    // owner mode (BN = 128, 4-way split-K): rank r reduces and finishes the
+    // tile's 32-column chunk r; otherwise rank 0 finishes the whole tile
+    const bool owner = BN == 128 && splits == 4;
+    const bool finisher = owner ? half == 0 : crank == 0;
+    const int c_first = owner ? 32 * (int)crank : half * (BN / 2);
     EpiPre pre;
-    const bool row_stats = ep.ln_stats != nullptr && crank == 0;
-    if (crank == 0 && (row < M || KIND == EPI_GLUDW)) epi_prefetch<KIND>(ep, row, n0 + c_first, pre, !row_stats);
+    const bool row_stats = ep.ln_stats != nullptr && (owner || crank == 0);
+    if (finisher && (row < M || KIND == EPI_GLUDW)) epi_prefetch<KIND>(ep, row, n0 + c_first, pre, !row_stats);
     if (row_stats && warp >= 2 && warp < 6) rowstat[(warp - 2) * 32 + lane] = epi_row_stats(ep, m0 + (warp - 2) * 32 + lane);
 
     if (!mbar_wait(accb, 0)) ok = false;
@@ -240,8 +245,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     static_assert(KIND == EPI_GLUDW || C::STAGES * C::B_TILE >= 8 * EPI_STAGE_FLOATS * 4, "epilogue staging");
     float* stage = reinterpret_cast<float*>(sB) + warp * EPI_STAGE_FLOATS;
     if (splits > 1) {
-        cluster_sync();  // every rank's main loop is done: rank 0's ring takes the partials
-        if (crank != 0) {
+        cluster_sync();  // every rank's main loop is done: the finishers' rings take the partials
+        if (owner) {
+            // this rank's partial of chunk q goes to rank q, into slot (its rank
+            // among q's three peers); half 0 pushes the first and third other
+            // chunk, half 1 the second
+#pragma unroll 1
+            for (int i = half; i < 3; i += 2) {
+                const int q = i + (i >= (int)crank ? 1 : 0);
+                const int slot = (int)crank < q ? (int)crank : (int)crank - 1;
+                const uint32_t dst = dsmem_addr(part + (size_t)slot * 32 * BM + rloc, (uint32_t)q);
+                float v[32];
+                tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(32 * q), v);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) st_dsmem_f32(dst + (uint32_t)(k * BM) * 4u, v[k]);
+            }
+        } else if (crank != 0) {
             // pushed with remote stores (a warp writes one 128-byte column
             // segment per store), so that rank 0 adds them from its own memory
             const uint32_t dst = dsmem_addr(part + (size_t)(crank - 1) * BN * BM + rloc, 0);
@@ -253,9 +272,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 for (int k = 0; k < 32; ++k) st_dsmem_f32(dst + (uint32_t)((c + k) * BM) * 4u, v[k]);
             }
         }
-        cluster_sync();  // the partials are in rank 0's shared memory
+        cluster_sync();  // the partials are in the finishers' shared memory
     }
-    if (crank == 0) {
+    if (owner) {
+        if (half == 0) {
+            // the chunk's four partials added in rank order (the same order as
+            // rank 0 finishing the whole tile: bit-identical results)
+            float own[32], v[32];
+            tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c_first, own);
+#pragma unroll 1
+            for (int rr = 0; rr < 4; ++rr) {
+                const float* pr = part + (size_t)(rr < (int)crank ? rr : rr - 1) * 32 * BM + rloc;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const float t = rr == (int)crank ? own[k] : pr[k * BM];
+                    v[k] = rr == 0 ? t : v[k] + t;
+                }
+            }
+            const bool live = ok && row < M;
+            if constexpr (KIND != EPI_GLUDW) epilogue32<KIND, TAct>(ep, row, n0 + c_first, v, pre, stage, live);
+        }
+    } else if (crank == 0) {
 #pragma unroll 1
         for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
             float v[32];
@@ -400,7 +437,9 @@ cudaError_t launch_gemm_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, int M
     if (K % BK || K <= 0 || N % BN || !ep.act_bf16) return cudaErrorInvalidValue;
     if (conv_C && (conv_C % BK || K != 3 * conv_C)) return cudaErrorInvalidValue;
     if (splits < 1 || splits > 4 || splits > K / BK) return cudaErrorInvalidValue;
-    if (splits > 1 && BN != 64) return cudaErrorInvalidValue;  // rank 0's ring holds three 128 x 64 partials
+    // rank 0's ring holds three 128 x 64 partials; at BN = 128 the four ranks
+    // each finish a 32-column chunk (owner mode)
+    if (splits > 1 && !(BN == 64 || (BN == 128 && splits == 4))) return cudaErrorInvalidValue;
     if (ep.kind == EPI_GLUDW && (splits != 1 || !a_split || ep.nq < 1 || 32 % ep.nq || 2 * ep.D != N || ep.D % 16))
         return cudaErrorInvalidValue;
     switch (BN) {
