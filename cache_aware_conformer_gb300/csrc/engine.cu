@@ -439,7 +439,8 @@ int gemm(cac_model* m, const void* A, long long lda, int M, int K, const Lin& W,
         // each rank finishing one 32-column chunk (owner mode; CAC_SPLIT_OWNER=0
         // keeps 64-column tiles finished by rank 0)
         static const bool owner_on = env_int("CAC_SPLIT_OWNER", 1, 0, 1) != 0;
-        if (owner_on && W.has128 && !conv_C && ep.kind != EPI_GLUDW && K / 64 >= 32) {
+        static const int owner_min = env_int("CAC_SPLIT_OWNER_MIN_SLICES", 32, 4, 1 << 20);
+        if (owner_on && W.has128 && !conv_C && ep.kind != EPI_GLUDW && K / 64 >= owner_min) {
             CK(launch_gemm_tc(&tmA, &W.tm128, M, W.N, K, 128, conv_C, 4, a_split, ep, m->status, s));
             ++*launches;
             return CAC_OK;
