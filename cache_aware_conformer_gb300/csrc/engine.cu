@@ -12,6 +12,7 @@
 #include <mutex>
 #include <new>
 #include <tuple>
+#include <unordered_map>
 #include <vector>
 
 #include "../../include/cac_ops.h"
@@ -65,6 +66,12 @@ struct Lin {
     CUtensorMap tm;      // bf16 weights on the tcgen05 path (BN-row boxes)
     CUtensorMap tm128;   // the same with 128-row boxes (persistent GEMM), when N % 128 == 0
     bool has128 = false;
+    // palette form (cac_model_create_palette): 6-bit indices [N][3K/4] bytes and
+    // one 64-entry bf16 table per 64-row block of the outputs
+    bool pal = false;
+    void* packed = nullptr;
+    uint16_t* ptab = nullptr;
+    CUtensorMap tmp;     // packed indices, 48-byte x 64-row boxes
 };
 
 struct LayerW {
@@ -162,6 +169,64 @@ int upload_lin(cac_model* m, const float* w, const float* b, int N, int K, Lin* 
         lin->has128 = N % 128 == 0;
         if (lin->has128 && !make_tmap_bf16(&lin->tm128, p, K, N, (uint64_t)K * 2, 128)) return CAC_E_CUDA;
     }
+    return CAC_OK;
+}
+
+// Palette form of a projection for cac_model_create_palette: each weight's index
+// in its matrix's 64-entry table (exact value match; the lowest index among
+// equal entries; -0 and +0 alike), packed 6 bits per weight along K in the
+// GEMM's row order (`perm` as in upload_lin), and one bf16 table per 64-row
+// block of the outputs.  tab_of(src) is the table of source row src; the rows
+// of a block must share one.  A weight absent from its table, or a table entry
+// that is not a bf16 value, is CAC_E_INVAL.
+template <class TabOf>
+int pal_attach(cac_model* m, Lin* lin, const float* w, int N, int K, const std::vector<int>* perm, TabOf tab_of) {
+    if (N % 64 || K % 64) return CAC_E_UNSUPPORTED;
+    auto key = [](float v) {
+        uint32_t b;
+        std::memcpy(&b, &v, 4);
+        return b == 0x80000000u ? 0u : b;
+    };
+    const size_t rb = (size_t)K * 6 / 8;
+    std::vector<uint8_t> packed((size_t)N * rb, 0);
+    std::vector<uint16_t> tabs((size_t)N);
+    for (int blk = 0; blk < N / 64; ++blk) {
+        const float* T = nullptr;
+        for (int r = blk * 64; r < blk * 64 + 64; ++r) {
+            const float* t = tab_of(perm ? (*perm)[r] : r);
+            if (!t) return CAC_E_INVAL;
+            if (T && t != T) return CAC_E_UNSUPPORTED;
+            T = t;
+        }
+        std::unordered_map<uint32_t, int> idx_of;
+        for (int i = 63; i >= 0; --i) {  // descending: the lowest index of equal entries wins
+            if (bf2f(f2bf(T[i])) != T[i]) return CAC_E_INVAL;
+            idx_of[key(T[i])] = i;
+            tabs[(size_t)blk * 64 + i] = f2bf(T[i]);
+        }
+        for (int r = blk * 64; r < blk * 64 + 64; ++r) {
+            const float* src = w + (size_t)(perm ? (*perm)[r] : r) * K;
+            uint8_t* row = &packed[(size_t)r * rb];
+            for (int k = 0; k < K; ++k) {
+                const auto it = idx_of.find(key(src[k]));
+                if (it == idx_of.end()) return CAC_E_INVAL;
+                const uint32_t ix = (uint32_t)it->second;
+                const int bit = 6 * k, off = bit & 7;
+                row[bit >> 3] |= (uint8_t)(ix << off);
+                if (off > 2) row[(bit >> 3) + 1] |= (uint8_t)(ix >> (8 - off));
+            }
+        }
+    }
+    void* pk;
+    void* pt;
+    RET(dalloc(m, packed.size(), &pk));
+    RET(dalloc(m, tabs.size() * 2, &pt));
+    CK(cudaMemcpy(pk, packed.data(), packed.size(), cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(pt, tabs.data(), tabs.size() * 2, cudaMemcpyHostToDevice));
+    if (!make_tmap_packed(&lin->tmp, pk, rb, (uint64_t)N)) return CAC_E_CUDA;
+    lin->packed = pk;
+    lin->ptab = static_cast<uint16_t*>(pt);
+    lin->pal = true;
     return CAC_OK;
 }
 
@@ -397,7 +462,7 @@ int gemm(cac_model* m, const void* A, long long lda, int M, int K, const Lin& W,
     ep.act_bf16 = m->bf16;
     if (m->tc && m->rec && m->rec->on) {
         ChainRec* r = m->rec;
-        const bool chainable = !conv_C && W.BN == 64 && W.N % 64 == 0 &&
+        const bool chainable = !conv_C && !W.pal && W.BN == 64 && W.N % 64 == 0 &&
                                (ep.kind == EPI_STORE || ep.kind == EPI_RESID || ep.kind == EPI_QKV ||
                                 ep.kind == EPI_GLUDW) &&
                                (r->ph.empty() || r->M == M) && (int)r->ph.size() < CH_MAX_PHASES &&
@@ -430,7 +495,7 @@ int gemm(cac_model* m, const void* A, long long lda, int M, int K, const Lin& W,
         if (!ok) return CAC_E_CUDA;
         // many output tiles (the offline encode): the persistent kernel, whose
         // epilogue of one tile overlaps the main loop of the next
-        if (W.has128 && ep.kind != EPI_GLUDW && (long long)((M + 127) / 128) * (W.N / 128) >= 2 * m->sms) {
+        if (W.has128 && !W.pal && ep.kind != EPI_GLUDW && (long long)((M + 127) / 128) * (W.N / 128) >= 2 * m->sms) {
             CK(launch_gemm_tc_persistent(&tmA, &W.tm128, M, W.N, K, conv_C, a_split, ep, m->status, s));
             ++*launches;
             return CAC_OK;
@@ -440,14 +505,17 @@ int gemm(cac_model* m, const void* A, long long lda, int M, int K, const Lin& W,
         // keeps 64-column tiles finished by rank 0)
         static const bool owner_on = env_int("CAC_SPLIT_OWNER", 1, 0, 1) != 0;
         static const int owner_min = env_int("CAC_SPLIT_OWNER_MIN_SLICES", 32, 4, 1 << 20);
-        if (owner_on && W.has128 && !conv_C && ep.kind != EPI_GLUDW && K / 64 >= owner_min) {
+        if (owner_on && W.has128 && !W.pal && !conv_C && ep.kind != EPI_GLUDW && K / 64 >= owner_min) {
             CK(launch_gemm_tc(&tmA, &W.tm128, M, W.N, K, 128, conv_C, 4, a_split, ep, m->status, s));
             ++*launches;
             return CAC_OK;
         }
         // the fused depthwise conv reads its stream's rows within one CTA: no split-K
         const int splits = ep.kind == EPI_GLUDW ? 1 : choose_splits((W.N / W.BN) * ((M + 127) / 128), K / 64);
-        CK(launch_gemm_tc(&tmA, &W.tm, M, W.N, K, W.BN, conv_C, splits, a_split, ep, m->status, s));
+        if (W.pal)  // palette weights: 64-row tiles decoded in the kernel
+            CK(launch_gemm_tc(&tmA, &W.tmp, M, W.N, K, 64, conv_C, splits, a_split, ep, m->status, s, W.ptab));
+        else
+            CK(launch_gemm_tc(&tmA, &W.tm, M, W.N, K, W.BN, conv_C, splits, a_split, ep, m->status, s));
     } else {
         CK(launch_gemm_simt(m->bf16, A, lda, W.w, K, M, W.N, K, conv_C, a_split, ep, s));
     }
@@ -475,7 +543,10 @@ extern "C" size_t cac_weights_size(const cac_config* c) {
     return n;
 }
 
-extern "C" int cac_model_create(const cac_config* cfg, const float* weights, size_t n_floats, cac_model** out) {
+namespace {
+// The model from a dense weight blob; with `tables` (palette form, see
+// cac_model_create_palette) the projections also take their palette form.
+int model_create(const cac_config* cfg, const float* weights, size_t n_floats, const float* tables, cac_model** out) {
     if (!out || !weights) return CAC_E_INVAL;
     *out = nullptr;
     RET(validate(cfg));
@@ -518,14 +589,29 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
     if (cudaMemset(m->status, 0, sizeof(int)) != cudaSuccess) return fail(CAC_E_CUDA);
 
     const float *w, *b;
+    // palette tables in their documented order (see cac_model_create_palette)
+    auto table = [&](int i) -> const float* { return tables ? tables + (size_t)64 * i : nullptr; };
+    auto palette = [&](Lin* dst, const float* ww, int N, int K, const std::vector<int>* perm, int ti) {
+        if (!tables) return (int)CAC_OK;
+        const float* t = table(ti);
+        return pal_attach(m, dst, ww, N, K, perm, [t](int) { return t; });
+    };
     w = c.take((size_t)D * 3 * MEL); b = c.take(D);
-    if ((r = upload_lin(m, w, b, D, 3 * MEL, &m->sub1, nullptr)) != CAC_OK) return fail(r);
+    if ((r = upload_lin(m, w, b, D, 3 * MEL, &m->sub1, nullptr)) != CAC_OK ||
+        (r = palette(&m->sub1, w, D, 3 * MEL, nullptr, 0)) != CAC_OK)
+        return fail(r);
     w = c.take((size_t)D * 3 * D); b = c.take(D);
-    if ((r = upload_lin(m, w, b, D, 3 * D, &m->sub2, nullptr)) != CAC_OK) return fail(r);
+    if ((r = upload_lin(m, w, b, D, 3 * D, &m->sub2, nullptr)) != CAC_OK ||
+        (r = palette(&m->sub2, w, D, 3 * D, nullptr, 1)) != CAC_OK)
+        return fail(r);
     w = c.take((size_t)D * 3 * D); b = c.take(D);
-    if ((r = upload_lin(m, w, b, D, 3 * D, &m->sub3, nullptr)) != CAC_OK) return fail(r);
+    if ((r = upload_lin(m, w, b, D, 3 * D, &m->sub3, nullptr)) != CAC_OK ||
+        (r = palette(&m->sub3, w, D, 3 * D, nullptr, 2)) != CAC_OK)
+        return fail(r);
     w = c.take((size_t)D * D); b = c.take(D);
-    if ((r = upload_lin(m, w, b, D, D, &m->subo, nullptr)) != CAC_OK) return fail(r);
+    if ((r = upload_lin(m, w, b, D, D, &m->subo, nullptr)) != CAC_OK ||
+        (r = palette(&m->subo, w, D, D, nullptr, 3)) != CAC_OK)
+        return fail(r);
 
     // GLU interleave: every 32 output columns of pw1 = 16 value rows then their 16 gate rows
     std::vector<int> glu_perm(2 * D);
@@ -562,18 +648,20 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
             return e ? e : upload_f32(m, host_b, D, be);
         };
         // a projection that consumes the last vec_ln() LayerNorm; also stored folded (fold_ln)
-        auto lin = [&](Lin* dst, int N, int K, const std::vector<int>* perm, float** fold_b = nullptr,
+        const int tl = 5 + 11 * l;  // this layer's first palette table
+        auto lin = [&](Lin* dst, int N, int K, const std::vector<int>* perm, int ti, float** fold_b = nullptr,
                        float** colsum = nullptr) {
             const float* ww = c.take((size_t)N * K);
             const float* bb = c.take(N);
-            if (!ww || !bb) return CAC_E_INVAL;
+            if (!ww || !bb) return (int)CAC_E_INVAL;
             int e = upload_lin(m, ww, bb, N, K, dst, perm);
             if (e == CAC_OK && fold_b && m->fold_ln)
                 e = upload_ln_fold(m, ww, bb, host_g, host_b, N, K, perm, fold_b, colsum);
+            if (e == CAC_OK) e = palette(dst, ww, N, K, perm, tl + ti);
             return e;
         };
-        if ((r = vec(&Lw.ff1_g, D)) || (r = vec(&Lw.ff1_b, D)) || (r = lin(&Lw.ff1_w1, F, D, nullptr)) ||
-            (r = lin(&Lw.ff1_w2, D, F, nullptr)))
+        if ((r = vec(&Lw.ff1_g, D)) || (r = vec(&Lw.ff1_b, D)) || (r = lin(&Lw.ff1_w1, F, D, nullptr, 0)) ||
+            (r = lin(&Lw.ff1_w2, D, F, nullptr, 1)))
             return fail(r);
         if ((r = vec_ln(&Lw.att_g, &Lw.att_b))) return fail(r);
         {   // q, k, v concatenated into one [3D][D] projection
@@ -588,11 +676,14 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
             std::memcpy(&bqkv[D], bk, sizeof(float) * D);
             std::memcpy(&bqkv[2 * D], bv, sizeof(float) * D);
             if ((r = upload_lin(m, wqkv.data(), bqkv.data(), 3 * D, D, &Lw.qkv, nullptr)) != CAC_OK) return fail(r);
+            if (tables && (r = pal_attach(m, &Lw.qkv, wqkv.data(), 3 * D, D, nullptr,
+                                          [&](int src) { return table(tl + 2 + src / D); })) != CAC_OK)
+                return fail(r);
             if (m->fold_ln && (r = upload_ln_fold(m, wqkv.data(), bqkv.data(), host_g, host_b, 3 * D, D, nullptr,
                                                   &Lw.qkv_fb, &Lw.qkv_cs)) != CAC_OK)
                 return fail(r);
         }
-        if ((r = lin(&Lw.wo, D, D, nullptr))) return fail(r);
+        if ((r = lin(&Lw.wo, D, D, nullptr, 5))) return fail(r);
         {   // P = pe @ wpos^T, computed once per layer in fp32
             const float* wpos = c.take((size_t)D * D);
             if (!wpos) return fail(CAC_E_INVAL);
@@ -636,7 +727,7 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
             }
         }
         if ((r = vec(&Lw.pbu, (size_t)H * HD)) || (r = vec(&Lw.pbv, (size_t)H * HD))) return fail(r);
-        if ((r = vec_ln(&Lw.conv_g, &Lw.conv_b)) || (r = lin(&Lw.pw1, 2 * D, D, &glu_perm, &Lw.pw1_fb, &Lw.pw1_cs)))
+        if ((r = vec_ln(&Lw.conv_g, &Lw.conv_b)) || (r = lin(&Lw.pw1, 2 * D, D, &glu_perm, 7, &Lw.pw1_fb, &Lw.pw1_cs)))
             return fail(r);
         {   // depthwise [D][9] -> [9][D]
             const float* wdw = c.take((size_t)D * 9);
@@ -647,10 +738,10 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
             if ((r = upload_f32(m, tmp.data(), tmp.size(), &Lw.dwT)) != CAC_OK) return fail(r);
         }
         if ((r = vec(&Lw.bdw, D)) || (r = vec(&Lw.bng, D)) || (r = vec(&Lw.bnb, D)) ||
-            (r = lin(&Lw.pw2, D, D, nullptr)))
+            (r = lin(&Lw.pw2, D, D, nullptr, 8)))
             return fail(r);
-        if ((r = vec_ln(&Lw.ff2_g, &Lw.ff2_b)) || (r = lin(&Lw.ff2_w1, F, D, nullptr, &Lw.ff2_fb, &Lw.ff2_cs)) ||
-            (r = lin(&Lw.ff2_w2, D, F, nullptr)))
+        if ((r = vec_ln(&Lw.ff2_g, &Lw.ff2_b)) || (r = lin(&Lw.ff2_w1, F, D, nullptr, 9, &Lw.ff2_fb, &Lw.ff2_cs)) ||
+            (r = lin(&Lw.ff2_w2, D, F, nullptr, 10)))
             return fail(r);
         if ((r = vec(&Lw.out_g, D)) || (r = vec(&Lw.out_b, D))) return fail(r);
     }
@@ -658,12 +749,27 @@ extern "C" int cac_model_create(const cac_config* cfg, const float* weights, siz
         const float* wj = c.take((size_t)m->J * D);
         const float* bj = c.take(m->J);
         if (!wj || !bj) return fail(CAC_E_INVAL);
-        if ((r = upload_lin(m, wj, bj, m->J, D, &m->joint, nullptr)) != CAC_OK) return fail(r);
+        if ((r = upload_lin(m, wj, bj, m->J, D, &m->joint, nullptr)) != CAC_OK ||
+            (r = palette(&m->joint, wj, m->J, D, nullptr, 4)) != CAC_OK)
+            return fail(r);
     }
     if (c.left != 0) return fail(CAC_E_INVAL);
     if (cudaDeviceSynchronize() != cudaSuccess) return fail(CAC_E_CUDA);
     *out = m;
     return CAC_OK;
+}
+}  // namespace
+
+extern "C" int cac_model_create(const cac_config* cfg, const float* weights, size_t n_floats, cac_model** out) {
+    return model_create(cfg, weights, n_floats, nullptr, out);
+}
+
+extern "C" int cac_model_create_palette(const cac_config* cfg, const float* weights, size_t n_floats,
+                                        const float* tables, size_t n_tables, cac_model** out) {
+    if (!cfg || !tables || !out) return CAC_E_INVAL;
+    if (cfg->dtype != CAC_DTYPE_BF16 || cfg->gemm_simt) return CAC_E_UNSUPPORTED;
+    if (n_tables != (size_t)64 * (5 + 11 * (size_t)cfg->n_layers)) return CAC_E_INVAL;
+    return model_create(cfg, weights, n_floats, tables, out);
 }
 
 extern "C" void cac_model_destroy(cac_model* m) {

@@ -124,8 +124,16 @@ bool make_tmap_bf16_conv(CUtensorMap* tm, const void* base, uint64_t C, uint64_t
 // reduced deterministically through distributed shared memory.
 // a_split: A is a split operand [M][2K] (hi in columns [0, K), lo = residual of
 // the bf16 rounding in [K, 2K)); the product is (hi + lo) * B^T.
+// pal_tab (palette weights, BN = 64): tmB is a make_tmap_packed map over the
+// 6-bit indices [N][3K/4] bytes and pal_tab holds N/64 tables of 64 bf16 values,
+// one per 64-row block of the output columns.
 cudaError_t launch_gemm_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int BN, int conv_C,
-                           int splits, int a_split, const EpiParams& ep, int* status, cudaStream_t s);
+                           int splits, int a_split, const EpiParams& ep, int* status, cudaStream_t s,
+                           const uint16_t* pal_tab = nullptr);
+
+// Packed 6-bit indices [rows][row_bytes] (a row's indices as a little-endian bit
+// stream, row_bytes = 3K/4 a multiple of 16), box 48 bytes x 64 rows.
+bool make_tmap_packed(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows);
 
 // Persistent tcgen05 GEMM for many output tiles (128 x 128 tiles, one CTA per
 // SM, two TMEM accumulators so epilogue and main loop overlap).  tmB128: the

@@ -146,32 +146,6 @@ __global__ void __launch_bounds__(PTHREADS, 1)
     if (warp == 1) tmem_dealloc(tmem, PBN);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 p_encode = nullptr;
-std::once_flag p_encode_once;
-
-void p_load_encode() {
-    cudaDriverEntryPointQueryResult q;
-    void* fn = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-        p_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-}
-
-// packed indices [N][3K/4] bytes, box of 48 bytes x 64 rows, no swizzle
-bool make_tmap_packed(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows) {
-    std::call_once(p_encode_once, p_load_encode);
-    if (!p_encode) return false;
-    if ((reinterpret_cast<uintptr_t>(base) & 15) || (row_bytes % 16) || rows == 0) return false;
-    cuuint64_t dims[2] = {row_bytes, rows};
-    cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {PP_ROW, PBN};
-    cuuint32_t estr[2] = {1, 1};
-    return p_encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 }  // namespace cac
 

@@ -47,17 +47,24 @@ constexpr int A_TILE = BM * BK * 2;  // bytes
 // bf16 for up to 64 streams (two or more frames per stream), loaded by the
 // idle warps before the wait on the previous kernel (the rows were written a
 // step earlier); one ring stage fewer makes room for it.
-template <int BN, int SPLIT, int KIND>
+// PAL (BN = 64): the weights are 6-bit palette indices (64 rows x 48 bytes per
+// K slice, loaded by TMA) that warps 2-3 decode into the bf16 B tile through
+// the 64-entry table of the tile's rows.
+template <int BN, int SPLIT, int KIND, int PAL = 0>
 struct TcCfg {
+    static_assert(!PAL || BN == 64, "palette tiles are 64 rows");
     static constexpr bool HAS_WIN = KIND == EPI_GLUDW && BN == 64;
+    static constexpr int P_TILE = PAL ? 64 * 48 : 0;
     static constexpr int WIN = HAS_WIN ? 64 * 8 * 32 * 2 : 0;
     static constexpr int PRM = HAS_WIN ? (12 * 32 + 64) * 4 : 0;  // conv constants and LayerNorm column sums
     static constexpr int B_TILE = BN * BK * 2;
     static constexpr int A_TILES = A_TILE * (1 + SPLIT);
-    static constexpr int STAGE = A_TILES + B_TILE;
+    static constexpr int STAGE = A_TILES + B_TILE + P_TILE;
+    static constexpr int TX = A_TILES + (PAL ? P_TILE : B_TILE);  // bytes the TMA brings per stage
     static constexpr int STAGES = SPLIT ? ((BN == 256) ? 3 : (BN == 128 ? 4 : (HAS_WIN ? 4 : 5)))
                                         : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
-    static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/ + BM * 8 /*row stats*/ + WIN + PRM;
+    static constexpr int SMEM = STAGES * STAGE + 1024 /*align slack*/ + 256 /*barriers*/ + BM * 8 /*row stats*/ + WIN + PRM +
+                                (PAL ? 128 : 0) /*table*/;
     static_assert(BN != 64 || STAGES * A_TILES >= 3 * BN * BM * 4, "split-K partial tiles must fit the A ring");
     static_assert(BN != 128 || STAGES * A_TILES >= 3 * 32 * BM * 4, "owner-mode partial chunks must fit the A ring");
     static_assert(SMEM <= 227 * 1024, "shared memory");
@@ -66,24 +73,29 @@ struct TcCfg {
 
 constexpr int TC_THREADS = 256;
 
-template <int BN, int KIND, class TAct, int SPLIT>
+template <int BN, int KIND, class TAct, int SPLIT, int PAL>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
-                   int K, int conv_C, EpiParams ep, int* status) {
-    using C = TcCfg<BN, SPLIT, KIND>;
+                   int K, int conv_C, EpiParams ep, const uint16_t* pal_tab, int* status) {
+    using C = TcCfg<BN, SPLIT, KIND, PAL>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + C::STAGES * C::A_TILES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_TILE);
+    uint8_t* sP = sB + C::STAGES * C::B_TILE;  // PAL: packed index tiles
+    uint64_t* full = reinterpret_cast<uint64_t*>(sP + C::STAGES * C::P_TILE);
     uint64_t* empty = full + C::STAGES;
     uint64_t* accb = empty + C::STAGES;
+    uint64_t* ready = accb + 2;  // PAL: [STAGES] decoded B tiles (64 arrivals)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accb + 1);
     // LayerNorm statistics of the tile's rows, computed once per row by warps
     // 2-5 while the main loop runs (warps 0 and 1 are busy in it)
     float2* rowstat = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(full) + 256);
     bf16* win = reinterpret_cast<bf16*>(rowstat + BM);  // C::WIN bytes
     float* prm = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(win) + C::WIN);  // C::PRM bytes
+    uint16_t* ptab = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(prm) + C::PRM);  // PAL: 64 entries
+    // warps free during the main loop: 2-7, or 4-7 when 2-3 decode palette tiles
+    constexpr int FREE0 = PAL ? 4 : 2;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
@@ -99,10 +111,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(&empty[s], 1);
         }
         mbar_init(accb, 1);
+        if (PAL)
+            for (int s = 0; s < C::STAGES; ++s) mbar_init(&ready[s], 64);
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
+    if (PAL && threadIdx.x < 64) ptab[threadIdx.x] = pal_tab[(size_t)(n0 / 64) * 64 + threadIdx.x];
     if (warp == 1) tmem_alloc(tmem_slot, BN);
     tc_fence_before();
     __syncthreads();
@@ -115,8 +130,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // tiles before waiting for it, then the activations
         const int pre = nk < C::STAGES ? nk : C::STAGES;
         for (int kb = 0; kb < pre; ++kb) {
-            mbar_expect_tx(&full[kb], C::STAGE);
-            tma_load_2d(sB + kb * C::B_TILE, &tmB, (kb0 + kb) * BK, n0, &full[kb]);
+            mbar_expect_tx(&full[kb], C::TX);
+            if (PAL) tma_load_2d(sP + kb * C::P_TILE, &tmB, (kb0 + kb) * 48, n0, &full[kb]);
+            else tma_load_2d(sB + kb * C::B_TILE, &tmB, (kb0 + kb) * BK, n0, &full[kb]);
         }
         pdl_wait();
         for (int kb = 0; kb < nk; ++kb) {
@@ -125,8 +141,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int k0 = (kb0 + kb) * BK;
             if (kb >= pre) {
                 if (!mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }
-                mbar_expect_tx(&full[s], C::STAGE);
-                tma_load_2d(sB + s * C::B_TILE, &tmB, k0, n0, &full[s]);
+                mbar_expect_tx(&full[s], C::TX);
+                if (PAL) tma_load_2d(sP + s * C::P_TILE, &tmB, (kb0 + kb) * 48, n0, &full[s]);
+                else tma_load_2d(sB + s * C::B_TILE, &tmB, k0, n0, &full[s]);
             }
             if (conv_C) {
                 const int tap = k0 / conv_C;
@@ -144,7 +161,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % C::STAGES;
             const uint32_t ph = (kb / C::STAGES) & 1;
-            if (!mbar_wait(&full[s], ph)) { ok = false; break; }
+            if (!mbar_wait(&full[s], ph) || (PAL && !mbar_wait(&ready[s], ph))) { ok = false; break; }
             tc_fence_after();
             const uint64_t ad = sdesc_k_sw128(sA + s * C::A_TILES);
             const uint64_t bd = sdesc_k_sw128(sB + s * C::B_TILE);
@@ -161,6 +178,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tc_commit(&empty[s]);
         }
         tc_commit(accb);
+    } else if (PAL && (warp == 2 || warp == 3)) {
+        // decoders: thread r turns weight row r's 48 packed bytes of each K slice
+        // (index k at bits [6k, 6k + 6)) into 64 table values, written in the
+        // 128-byte-swizzled K-major layout the tensor core reads (16-byte chunk c
+        // of row r at byte r * 128 + ((c ^ (r & 7)) << 4), as the TMA writes the
+        // A tiles)
+        const int r = threadIdx.x - 64;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % C::STAGES;
+            const uint32_t ph = (kb / C::STAGES) & 1;
+            if (!mbar_wait(&full[s], ph)) { ok = false; break; }
+            const uint8_t* pk = sP + s * C::P_TILE + r * 48;
+            uint8_t* out = sB + s * C::B_TILE + r * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {  // 8 indices = 6 bytes -> one 16-byte chunk of 8 bf16
+                uint64_t v = 0;
+#pragma unroll
+                for (int q = 0; q < 6; ++q) v |= (uint64_t)pk[c * 6 + q] << (8 * q);
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w[e] = (uint32_t)ptab[(v >> (12 * e)) & 63] | ((uint32_t)ptab[(v >> (12 * e + 6)) & 63] << 16);
+                *reinterpret_cast<uint4*>(out + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&ready[s]);
+        }
     }
     // conv-ring window of the tile's streams (GLU + depthwise epilogue): the
     // slots hold frames of earlier steps, final before this kernel started, so
@@ -169,9 +213,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // column sums of its 64 columns
     const bool use_win = C::HAS_WIN && ep.nq >= 2;
     if constexpr (C::HAS_WIN) {
-        if (warp >= 2) {
+        if (warp >= FREE0) {
             const int C0 = n0 >> 1;
-            for (int i = threadIdx.x - 64; i < 12 * 32 + 64; i += TC_THREADS - 64) {
+            for (int i = threadIdx.x - 32 * FREE0; i < 12 * 32 + 64; i += TC_THREADS - 32 * FREE0) {
                 float v;
                 if (i < 9 * 32) v = __ldg(ep.dw_wT + (long long)(i >> 5) * ep.D + C0 + (i & 31));
                 else if (i < 10 * 32) v = __ldg(ep.dw_bias + C0 + i - 9 * 32);
@@ -181,12 +225,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 prm[i] = v;
             }
         }
-        if (use_win && warp >= 2) {
+        if (use_win && warp >= FREE0) {
             // 16-byte pieces idx = (stream, slot, quarter of 8 channels), in batches
             // whose stream ids and then ring rows are all requested before any
             // is used (one dependent round trip each per batch)
-            constexpr int LT = TC_THREADS - 64, PER = 6;
-            const int nS = BM / ep.nq, sb0 = m0 / ep.nq, C0 = n0 >> 1, t = threadIdx.x - 64;
+            constexpr int LT = TC_THREADS - 32 * FREE0, PER = PAL ? 8 : 6;
+            const int nS = BM / ep.nq, sb0 = m0 / ep.nq, C0 = n0 >> 1, t = threadIdx.x - 32 * FREE0;
             const bf16* ring = static_cast<const bf16*>(ep.dw_ring);
             uint4* w4 = reinterpret_cast<uint4*>(win);
             for (int j0 = 0; j0 * LT < nS * 32; j0 += PER) {
@@ -226,7 +270,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     EpiPre pre;
     const bool row_stats = ep.ln_stats != nullptr && (owner || crank == 0);
     if (finisher && (row < M || KIND == EPI_GLUDW)) epi_prefetch<KIND>(ep, row, n0 + c_first, pre, !row_stats);
-    if (row_stats && warp >= 2 && warp < 6) rowstat[(warp - 2) * 32 + lane] = epi_row_stats(ep, m0 + (warp - 2) * 32 + lane);
+    if (row_stats && warp >= FREE0 && warp < FREE0 + 4)
+        rowstat[(warp - FREE0) * 32 + lane] = epi_row_stats(ep, m0 + (warp - FREE0) * 32 + lane);
 
     if (!mbar_wait(accb, 0)) ok = false;
     if constexpr (C::HAS_WIN) {
@@ -391,11 +436,12 @@ bool make_tmap_bf16(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t 
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, int KIND, int SPLIT>
+template <int BN, int KIND, int SPLIT, int PAL>
 static cudaError_t launch_bn_kind(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int conv_C,
-                                  int splits, const EpiParams& ep, int* status, cudaStream_t s) {
-    using C = TcCfg<BN, SPLIT, KIND>;
-    auto kern = gemm_tc_kernel<BN, KIND, bf16, SPLIT>;
+                                  int splits, const EpiParams& ep, const uint16_t* pal_tab, int* status,
+                                  cudaStream_t s) {
+    using C = TcCfg<BN, SPLIT, KIND, PAL>;
+    auto kern = gemm_tc_kernel<BN, KIND, bf16, SPLIT, PAL>;
     static bool attr_set = false;  // per instantiation, per process
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -403,36 +449,37 @@ static cudaError_t launch_bn_kind(const CUtensorMap* tmA, const CUtensorMap* tmB
         attr_set = true;
     }
     return launch_k(kern, dim3(N / BN, (M + BM - 1) / BM, splits), dim3(TC_THREADS), C::SMEM, s, splits, *tmA, *tmB,
-                    M, N, K, conv_C, ep, status);
+                    M, N, K, conv_C, ep, pal_tab, status);
 }
 
-template <int BN>
+template <int BN, int PAL>
 static cudaError_t launch_bn(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int cc, int sp,
-                             int a_split, const EpiParams& ep, int* status, cudaStream_t s) {
+                             int a_split, const EpiParams& ep, const uint16_t* pt, int* status, cudaStream_t s) {
     if (a_split) {
         // split operands: LayerNorm outputs, the attention output, the subsampling windows
         switch (ep.kind) {
-            case EPI_STORE: return launch_bn_kind<BN, EPI_STORE, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
-            case EPI_RESID: return launch_bn_kind<BN, EPI_RESID, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
-            case EPI_GLU: return launch_bn_kind<BN, EPI_GLU, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
-            case EPI_QKV: return launch_bn_kind<BN, EPI_QKV, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
-            case EPI_SUB: return launch_bn_kind<BN, EPI_SUB, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
-            case EPI_GLUDW: return launch_bn_kind<BN, EPI_GLUDW, 1>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+            case EPI_STORE: return launch_bn_kind<BN, EPI_STORE, 1, PAL>(tmA, tmB, M, N, K, cc, sp, ep, pt, status, s);
+            case EPI_RESID: return launch_bn_kind<BN, EPI_RESID, 1, PAL>(tmA, tmB, M, N, K, cc, sp, ep, pt, status, s);
+            case EPI_GLU: return launch_bn_kind<BN, EPI_GLU, 1, PAL>(tmA, tmB, M, N, K, cc, sp, ep, pt, status, s);
+            case EPI_QKV: return launch_bn_kind<BN, EPI_QKV, 1, PAL>(tmA, tmB, M, N, K, cc, sp, ep, pt, status, s);
+            case EPI_SUB: return launch_bn_kind<BN, EPI_SUB, 1, PAL>(tmA, tmB, M, N, K, cc, sp, ep, pt, status, s);
+            case EPI_GLUDW: return launch_bn_kind<BN, EPI_GLUDW, 1, PAL>(tmA, tmB, M, N, K, cc, sp, ep, pt, status, s);
         }
         return cudaErrorInvalidValue;
     }
     switch (ep.kind) {
-        case EPI_STORE: return launch_bn_kind<BN, EPI_STORE, 0>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
-        case EPI_RESID: return launch_bn_kind<BN, EPI_RESID, 0>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
-        case EPI_GLU: return launch_bn_kind<BN, EPI_GLU, 0>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
-        case EPI_QKV: return launch_bn_kind<BN, EPI_QKV, 0>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
-        case EPI_SUB: return launch_bn_kind<BN, EPI_SUB, 0>(tmA, tmB, M, N, K, cc, sp, ep, status, s);
+        case EPI_STORE: return launch_bn_kind<BN, EPI_STORE, 0, PAL>(tmA, tmB, M, N, K, cc, sp, ep, pt, status, s);
+        case EPI_RESID: return launch_bn_kind<BN, EPI_RESID, 0, PAL>(tmA, tmB, M, N, K, cc, sp, ep, pt, status, s);
+        case EPI_GLU: return launch_bn_kind<BN, EPI_GLU, 0, PAL>(tmA, tmB, M, N, K, cc, sp, ep, pt, status, s);
+        case EPI_QKV: return launch_bn_kind<BN, EPI_QKV, 0, PAL>(tmA, tmB, M, N, K, cc, sp, ep, pt, status, s);
+        case EPI_SUB: return launch_bn_kind<BN, EPI_SUB, 0, PAL>(tmA, tmB, M, N, K, cc, sp, ep, pt, status, s);
     }
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, int M, int N, int K, int BN, int conv_C,
-                           int splits, int a_split, const EpiParams& ep, int* status, cudaStream_t s) {
+                           int splits, int a_split, const EpiParams& ep, int* status, cudaStream_t s,
+                           const uint16_t* pal_tab) {
     if (M <= 0) return cudaSuccess;
     if (K % BK || K <= 0 || N % BN || !ep.act_bf16) return cudaErrorInvalidValue;
     if (conv_C && (conv_C % BK || K != 3 * conv_C)) return cudaErrorInvalidValue;
@@ -442,12 +489,30 @@ cudaError_t launch_gemm_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, int M
     if (splits > 1 && !(BN == 64 || (BN == 128 && splits == 4))) return cudaErrorInvalidValue;
     if (ep.kind == EPI_GLUDW && (splits != 1 || !a_split || ep.nq < 1 || 32 % ep.nq || 2 * ep.D != N || ep.D % 16))
         return cudaErrorInvalidValue;
+    if (pal_tab) {  // palette weights: 64-row tiles, tmB over the packed indices
+        if (BN != 64) return cudaErrorInvalidValue;
+        return launch_bn<64, 1>(tmA, tmB, M, N, K, conv_C, splits, a_split, ep, pal_tab, status, s);
+    }
     switch (BN) {
-        case 64: return launch_bn<64>(tmA, tmB, M, N, K, conv_C, splits, a_split, ep, status, s);
-        case 128: return launch_bn<128>(tmA, tmB, M, N, K, conv_C, splits, a_split, ep, status, s);
-        case 256: return launch_bn<256>(tmA, tmB, M, N, K, conv_C, splits, a_split, ep, status, s);
+        case 64: return launch_bn<64, 0>(tmA, tmB, M, N, K, conv_C, splits, a_split, ep, nullptr, status, s);
+        case 128: return launch_bn<128, 0>(tmA, tmB, M, N, K, conv_C, splits, a_split, ep, nullptr, status, s);
+        case 256: return launch_bn<256, 0>(tmA, tmB, M, N, K, conv_C, splits, a_split, ep, nullptr, status, s);
     }
     return cudaErrorInvalidValue;
+}
+
+// packed 6-bit indices [rows][row_bytes] (row_bytes = 3K/4), box of 48 bytes x 64 rows, no swizzle
+bool make_tmap_packed(CUtensorMap* tm, const void* base, uint64_t row_bytes, uint64_t rows) {
+    std::call_once(g_encode_once, load_encode);
+    if (!g_encode) return false;
+    if ((reinterpret_cast<uintptr_t>(base) & 15) || (row_bytes % 16) || rows == 0) return false;
+    cuuint64_t dims[2] = {row_bytes, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {48, 64};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace cac

@@ -26,7 +26,7 @@ ERRORS = {-1: "CAC_E_INVAL", -2: "CAC_E_ALIGN", -3: "CAC_E_STATE", -4: "CAC_E_NO
           -10: "CAC_E_LIMIT"}
 
 # every symbol include/cac.h declares
-SYMBOLS = ["cac_weights_size", "cac_model_create", "cac_model_destroy", "cac_pool_create", "cac_pool_destroy",
+SYMBOLS = ["cac_weights_size", "cac_model_create", "cac_model_create_palette", "cac_model_destroy", "cac_pool_create", "cac_pool_destroy",
            "cac_stream_create", "cac_stream_destroy", "cac_stream_reset", "cac_stream_push", "cac_stream_push_host",
            "cac_stream_flush", "cac_stream_flush_frames", "cac_encode_offline", "cac_stream_get_state",
            "cac_stream_set_state", "cac_pool_check", "cac_model_check", "cac_pool_set_graphs",
@@ -81,6 +81,7 @@ def _lib():
         sig = {
             "cac_weights_size": (c_size_t, [POINTER(CacConfig)]),
             "cac_model_create": (c_int, [POINTER(CacConfig), fp, c_size_t, POINTER(vp)]),
+            "cac_model_create_palette": (c_int, [POINTER(CacConfig), fp, c_size_t, fp, c_size_t, POINTER(vp)]),
             "cac_model_destroy": (None, [vp]),
             "cac_pool_create": (c_int, [vp, c_int, c_int, POINTER(vp)]),
             "cac_pool_destroy": (None, [vp]),
@@ -207,13 +208,20 @@ def gemm_bf16(A, B, bias=None, splits: int = 0, out=None, stream=None, split: bo
 class Model:
     """A model on the current CUDA device (cac_model_create)."""
 
-    def __init__(self, cfg: ModelConfig, blob: np.ndarray, gemm_simt: bool = False):
+    def __init__(self, cfg: ModelConfig, blob: np.ndarray, gemm_simt: bool = False, tables=None):
+        """tables: optional [5 + 11 L][64] palette tables (cac_model_create_palette)."""
         self.cfg = cfg
         blob = np.ascontiguousarray(blob, dtype=np.float32)
         self._c = make_config(cfg, gemm_simt)
         h = c_void_p()
-        _check(_lib().cac_model_create(ctypes.byref(self._c), blob.ctypes.data_as(POINTER(c_float)), blob.size,
-                                       ctypes.byref(h)), "cac_model_create")
+        if tables is None:
+            _check(_lib().cac_model_create(ctypes.byref(self._c), blob.ctypes.data_as(POINTER(c_float)), blob.size,
+                                           ctypes.byref(h)), "cac_model_create")
+        else:
+            t = np.ascontiguousarray(tables, dtype=np.float32)
+            _check(_lib().cac_model_create_palette(ctypes.byref(self._c), blob.ctypes.data_as(POINTER(c_float)),
+                                                   blob.size, t.ctypes.data_as(POINTER(c_float)), t.size,
+                                                   ctypes.byref(h)), "cac_model_create_palette")
         self.h = h
 
     def close(self):

@@ -111,6 +111,27 @@ size_t cac_weights_size(const cac_config* cfg);
  * `n_floats` values (layout above).  In bf16 mode the values are rounded to
  * bf16 on upload.  The caller keeps ownership of `weights`. */
 int  cac_model_create(const cac_config* cfg, const float* weights, size_t n_floats, cac_model** out);
+
+/* The same model with its weight matrices stored as 6-bit palettes ("Fast
+ * Accuracy-Preserving RNNT Beam Search on Apple Silicon", §1.3: the encoder
+ * keeps every matrix as a 64-entry lookup table and 6-bit indices; vectors
+ * and the depthwise taps stay dense).  bf16 mode on the tcgen05 path only
+ * (else CAC_E_UNSUPPORTED).
+ *   weights  the dense blob of cac_model_create, every palettised matrix
+ *            holding its decoded values (table entries);
+ *   tables   host fp32 [n_tables / 64][64], one table per matrix in this order:
+ *            sub.w1, sub.w2, sub.w3, sub.wo, joint.w, then for each layer
+ *            ff1.w1, ff1.w2, att.wq, att.wk, att.wv, att.wo, att.wpos,
+ *            conv.w_pw1, conv.w_pw2, ff2.w1, ff2.w2 (n_tables = 64 (5 + 11 L));
+ *            every entry a bf16 value.
+ * The library finds each weight's index in its matrix's table (exact match,
+ * the lowest index among equal entries), packs the indices 6 bits per weight
+ * (0.75 bytes instead of 2) and the projections' GEMMs decode them into bf16
+ * tiles on the device; att.wpos only enters the position table computed at
+ * load.  A weight absent from its table, or a table entry that is not a bf16
+ * value, returns CAC_E_INVAL.  The caller keeps ownership of both arrays. */
+int  cac_model_create_palette(const cac_config* cfg, const float* weights, size_t n_floats, const float* tables,
+                              size_t n_tables, cac_model** out);
 void cac_model_destroy(cac_model* m);
 
 /* Per-stream state pool for up to `max_streams` concurrent streams and at

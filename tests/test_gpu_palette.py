@@ -79,3 +79,75 @@ def test_palette_gemm_rejects_bad_arguments():
     tab = torch.zeros(64, device="cuda", dtype=torch.bfloat16)
     with pytest.raises(native.CacError):
         native.gemm_palette(A, packed, tab)                 # K % 64
+
+
+# ---------------------------------------------------------------------------
+# the encoder with palette weights (cac_model_create_palette)
+# ---------------------------------------------------------------------------
+def _palette_model_inputs(cfg, seed=0):
+    """Weights of cfg palettized by the compression oracle (bf16 tables): the
+    decoded weight dict and the tables in the library's order."""
+    from cache_aware_conformer_gb300 import synth
+    W = synth.make_weights(cfg, seed)
+    Wd = dict(W)
+    tables = []
+    for name in OC.compressed_names(cfg.n_layers):
+        table, idx = OC.palettize(W[name], table_dtype="bf16")
+        Wd[name] = OC.depalettize(table, idx)
+        tables.append(table)
+    return Wd, np.stack(tables).astype(np.float32)
+
+
+def test_palette_encoder_matches_dense_and_oracle():
+    """A two-layer bf16 encoder whose projections run on 6-bit palettes, pushed
+    160 ms at a time: bit-identical to the dense model on the decoded weights
+    (the kernel must decode exactly their bf16 values), and within the bf16
+    bars of the fp64 oracle on the decoded weights (the compressed encoder)."""
+    from dataclasses import replace
+    from cache_aware_conformer_gb300 import native, synth
+    from cache_aware_conformer_gb300.config import EOU_120M
+    from oracle import conformer as O
+    from _util import assert_close
+    cfg = replace(EOU_120M, n_layers=2, d_model=128, n_heads=2, ff_dim=512)
+    Wd, tables = _palette_model_inputs(cfg)
+    blob = synth.pack_weights(cfg, Wd)
+    pal = native.Model(cfg, blob, tables=tables)
+    dense = native.Model(cfg, blob)
+    S = 8
+    pools = [native.Pool(m, S, 2) for m in (pal, dense)]
+    ids = [[p.create_stream() for _ in range(S)] for p in pools]
+    refs = [O.StreamingEncoder(Wd, cfg) for _ in range(2)]  # streams 0 and S - 1
+    mels = [synth.make_mel(96, 40 + s) for s in range(S)]
+    for k in range(6):
+        chunk = np.stack([m[16 * k: 16 * (k + 1)] for m in mels])
+        outs = [p.push(i, torch.from_numpy(chunk).cuda()) for p, i in zip(pools, ids)]
+        e_pal, j_pal = outs[0][0].cpu().numpy(), outs[0][1].cpu().numpy()
+        e_den, j_den = outs[1][0].cpu().numpy(), outs[1][1].cpu().numpy()
+        assert np.array_equal(e_pal, e_den) and np.array_equal(j_pal, j_den), k
+        for r, s in zip(refs, (0, S - 1)):
+            e_ref, j_ref = r.push(mels[s][16 * k: 16 * (k + 1)])
+            assert_close(e_pal[s], e_ref, cfg, f"palette enc step {k} stream {s}")
+            assert_close(j_pal[s], j_ref, cfg, f"palette joint step {k} stream {s}")
+    for p in pools:
+        p.check()
+    pal.check()
+
+
+def test_palette_model_rejects_a_weight_missing_from_its_table():
+    from dataclasses import replace
+    from cache_aware_conformer_gb300 import native, synth
+    from cache_aware_conformer_gb300.config import EOU_120M
+    cfg = replace(EOU_120M, n_layers=1, d_model=128, n_heads=2, ff_dim=512)
+    Wd, tables = _palette_model_inputs(cfg)
+    blob = synth.pack_weights(cfg, Wd)
+    bad = tables.copy()
+    # an entry of the pw2 table (layer 0: 5 + 8) that some weight uses, moved off its value
+    t = 5 + 8
+    used = np.unique(Wd["l0.conv.w_pw2"])
+    i = int(np.flatnonzero(np.isin(bad[t], used))[0])
+    bad[t, i] = np.float32(bad[t, i] * 1.5 + 0.25)
+    with pytest.raises(native.CacError) as e:
+        native.Model(cfg, blob, tables=bad)
+    assert e.value.code == -1  # CAC_E_INVAL
+    with pytest.raises(native.CacError):
+        native.Model(cfg, blob, tables=tables[:-1])  # one table short
