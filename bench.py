@@ -581,7 +581,9 @@ def run_ours(args, wl):
     legs = {}
     for name, steps, fn in (("frontend", args.frontend_steps,
                              lambda: measure_frontend(w.S, args.frontend_steps, dev, load_peaks()[0])),
-                            ("beam", args.beam_steps, lambda: measure_beam(w.S, args.beam_steps, dev))):
+                            ("beam", args.beam_steps, lambda: measure_beam(w.S, args.beam_steps, dev)),
+                            ("palette", args.palette_steps if w.cfg.dtype == "bf16" and not w.cfg.provisional else 0,
+                             lambda: measure_palette(w, args.palette_steps, dev))):
         if steps > 0:
             try:
                 legs[name] = fn()
@@ -674,6 +676,49 @@ def measure_decode(w, Kd: int, dev, clk):
             "roofline": {"bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
                          "traffic": None,
                          "peak_source": "derived: SMs x 128 FP32 lanes x 2 FLOP x max SM clock"}}
+
+
+def measure_palette(w, Kp: int, dev):
+    """The encoder with its weight matrices as 6-bit palettes
+    (cac_model_create_palette; tables by cache_aware_conformer_gb300.palette)
+    against the dense encoder on the same decoded weights: the workload's
+    streams, one 160 ms push per step, graphs on, device-timed with CUDA
+    events; weight bytes per step read by the projections (dense bf16: 2 B
+    a weight, palette: 0.75 B)."""
+    import torch
+    from cache_aware_conformer_gb300 import native, palette
+    cfg = w.cfg
+    Wd, tables = palette.palettize_model(cfg, synth.make_weights(cfg, 0))
+    blob = synth.pack_weights(cfg, Wd)
+    mel = torch.from_numpy(np.stack([synth.make_mel(w.push_mel, s) for s in range(w.S)])).to(dev)
+    F = w.push_mel // 8
+    enc = torch.empty(w.S, F, cfg.d_model, device=dev)
+    jt = torch.empty(w.S, F, cfg.joint_dim, device=dev)
+    n_w = sum(np.asarray(Wd[n]).size for n in palette.matrix_names(cfg.n_layers) if not n.endswith("att.wpos"))
+    out = {"what": "encoder step with 6-bit palette weights vs dense on the same decoded weights "
+                   f"({w.S} streams, one {w.push_mel * 10} ms push per step, graphs)",
+           "matrix_weights": int(n_w),
+           "weight_bytes_per_step": {"dense_bf16": 2 * n_w, "palette": int(0.75 * n_w)}}
+    for name, tab in (("palette", tables), ("dense", None)):
+        model = native.Model(cfg, blob, tables=tab)
+        pool = native.Pool(model, w.S, max(2, F))
+        pool.set_graphs(True)
+        ids = [pool.create_stream() for _ in range(w.S)]
+        for _ in range(3):
+            pool.push_into(ids, mel, enc, jt)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(Kp):
+            pool.push_into(ids, mel, enc, jt)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / Kp
+        pool.check()
+        out[name] = {"ms_per_step": ms, "value": w.S * F * FRAME_SEC / (ms * 1e-3), "unit": UNIT}
+        pool.close()
+        model.close()
+    return out
 
 
 def measure_frontend(S: int, Kf: int, dev, peak_gbs: float):
@@ -818,6 +863,8 @@ def main(argv=None):
     ap.add_argument("--decode-steps", type=int, default=40)
     ap.add_argument("--frontend-steps", type=int, default=20, help="log-mel front-end pushes to time (0: skip)")
     ap.add_argument("--beam-steps", type=int, default=10, help="beam-search steps to time (0: skip)")
+    ap.add_argument("--palette-steps", type=int, default=20,
+                    help="steps of the palette-weight encoder and its dense twin to time (0: skip)")
     ap.add_argument("--streams", type=int, default=0,
                     help="override the workload's stream count (small cases for profiler captures; 0: the workload's)")
     args = ap.parse_args(argv)

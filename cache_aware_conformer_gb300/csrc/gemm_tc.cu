@@ -189,13 +189,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int s = kb % C::STAGES;
             const uint32_t ph = (kb / C::STAGES) & 1;
             if (!mbar_wait(&full[s], ph)) { ok = false; break; }
-            const uint8_t* pk = sP + s * C::P_TILE + r * 48;
+            // the row's 48 bytes as three 16-byte loads (rows 48 bytes apart, the
+            // tile 1024-aligned), then 6 bytes = 8 indices per 16-byte output chunk
+            const uint4* pk4 = reinterpret_cast<const uint4*>(sP + s * C::P_TILE + r * 48);
+            uint32_t wd[12];
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+                const uint4 t = pk4[q];
+                wd[4 * q] = t.x; wd[4 * q + 1] = t.y; wd[4 * q + 2] = t.z; wd[4 * q + 3] = t.w;
+            }
             uint8_t* out = sB + s * C::B_TILE + r * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {  // 8 indices = 6 bytes -> one 16-byte chunk of 8 bf16
-                uint64_t v = 0;
-#pragma unroll
-                for (int q = 0; q < 6; ++q) v |= (uint64_t)pk[c * 6 + q] << (8 * q);
+                // bytes 6c .. 6c + 5 of the row, little-endian
+                const int b0 = 6 * c, w0 = b0 >> 2, sh = 8 * (b0 & 3);
+                const uint64_t lo = (uint64_t)wd[w0] | ((uint64_t)wd[w0 + 1] << 32);
+                const uint64_t hi = w0 + 2 < 12 ? (uint64_t)wd[w0 + 2] : 0ull;
+                const uint64_t v = ((lo >> sh) | (sh ? hi << (64 - sh) : 0ull)) & 0xFFFFFFFFFFFFull;
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e)

@@ -51,3 +51,35 @@ def test_kernel_decode_order_matches_oracle_packing():
         got = (_unswizzle(tile).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
         np.testing.assert_array_equal(got, dec[:, kb * 64:(kb + 1) * 64])
         np.testing.assert_array_equal(OC.unpack6(packed, K)[:, kb * 64:(kb + 1) * 64], idx[:, kb * 64:(kb + 1) * 64])
+
+
+def test_library_palettiser_tables_and_nearest_entries():
+    """cache_aware_conformer_gb300.palette (the users' compression tool): 64
+    sorted bf16 table values per matrix, every decoded weight its entry's
+    nearest table value (ties to the lower entry), one table per matrix in the
+    order cac_model_create_palette documents."""
+    from dataclasses import replace
+    import torch
+    from cache_aware_conformer_gb300 import palette, synth
+    from cache_aware_conformer_gb300.config import EOU_120M
+    r = np.random.default_rng(3)
+    w = (r.normal(size=(96, 128)) * 0.05).astype(np.float32)
+    table, dec = palette.palettize(w)
+    assert table.shape == (64,) and np.all(np.diff(table) >= 0)
+    assert np.array_equal(torch.from_numpy(table).to(torch.bfloat16).float().numpy(), table)
+    d = np.abs(w.astype(np.float64)[..., None] - table.astype(np.float64)[None, None, :])
+    best = np.argmin(d, axis=-1)                      # first (lowest) index among the nearest
+    assert np.array_equal(dec, table[best])
+    # bf16 rounding: ties to even, as torch rounds
+    x = np.float32([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5e-3, 123.456])
+    assert np.array_equal(palette.to_bf16(x), torch.from_numpy(x).to(torch.bfloat16).float().numpy())
+    cfg = replace(EOU_120M, n_layers=2, d_model=128, n_heads=2, ff_dim=512)
+    W = synth.make_weights(cfg, 0)
+    Wd, tables = palette.palettize_model(cfg, W)
+    names = palette.matrix_names(cfg.n_layers)
+    assert tables.shape == (5 + 11 * cfg.n_layers, 64) and len(names) == tables.shape[0]
+    for t, n in zip(tables, names):
+        assert np.all(np.isin(np.asarray(Wd[n], dtype=np.float32), t)), n
+    assert all(np.array_equal(Wd[k], W[k]) for k in W if k not in names)
+    from oracle import compress as OC
+    assert names == OC.compressed_names(cfg.n_layers)  # the oracle's order, the library's table order
