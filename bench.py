@@ -8,8 +8,10 @@ resident on the GPU, random per-stream resets at 1 % per step, and stream start
 offsets drawn on 0..499 frames (even) and reached by an untimed pre-roll.
 
 One JSON line on rank 0:  value = streamed audio-seconds per second over all
-ranks (max time over ranks), e2e = the same through cac_stream_push_host with
-host buffers, roofline of the dominant kernel class (CUDA events on the
+ranks (max time over ranks), e2e = the same from page-locked host buffers
+(cac_stream_push_host_async: each push queued before the host reads the
+previous push's frames; the one-call-at-a-time cac_stream_push_host beside it),
+roofline of the dominant kernel class (CUDA events on the
 launching stream, in a profiled pass of the same steps), the fp64 oracle timed
 on the host cores as cpu_baseline, and the SM clocks sampled during the timed
 region.  `--impl reference` times the oracle itself as the reference arm.
@@ -359,6 +361,18 @@ class StreamWorkload:
         self.t += 1
         return enc, joint
 
+    def step_host_async(self, mel_host, out):
+        """Queue one host-buffer push into `out` (frames there once the
+        default stream has passed it)."""
+        t = self.t
+        r = self.resets[t]
+        if len(r):
+            self.pool.reset([self.ids[i] for i in r])
+            self.subT[r] = 0
+        self.pool.push_host_async(self.ids, mel_host, out)
+        self.subT += self.n
+        self.t += 1
+
 
 class OfflineWorkload:
     """B windows of offline_mel mel frames encoded in one cac_encode_offline call per step."""
@@ -454,7 +468,7 @@ def run_ours(args, wl):
     Ke = min(K, args.e2e_steps)
     Kd = min(K, args.decode_steps) if wl.model.joint_dim == EOU_DECODER.joint_dim and not wl.model.provisional else 0
     E_WARM = 3 if Ke else 0  # untimed host-buffer pushes before the e2e leg (its staging buffers and graph)
-    total_steps = Wm + K + 2 * Kp + E_WARM + Ke + (Kd + 3 if Kd else 0)
+    total_steps = Wm + K + 2 * Kp + E_WARM + 2 * Ke + (Kd + 3 if Kd else 0)
     workers = max(1, min(cpu_cores(), 16))
     w = StreamWorkload(wl, rank, dev, total_steps, workers)
     w.pool.set_graphs(True)
@@ -551,24 +565,50 @@ def run_ours(args, wl):
     # inputs and results in page-locked host memory (copied directly by the library).
     # The first host-buffer pushes allocate the library's staging buffers and
     # capture the step's graph for them, so a few run untimed first, as the
-    # device-timed leg's warm-up steps do.
-    host_mels = [w.step_mel[w.t + i].cpu().pin_memory() for i in range(E_WARM + Ke)]
-    w.host_out = (torch.empty(w.S, w.n, w.cfg.d_model).pin_memory(),
-                  torch.empty(w.S, w.n, w.cfg.joint_dim).pin_memory())
+    # device-timed leg's warm-up steps do.  Timed: each step's push is queued
+    # (cac_stream_push_host_async) before the host waits for the previous
+    # step's frames and reads them from the other of two output buffers; the
+    # last step's frames are waited for and read inside the timed region.
+    # Beside it, the same steps one synchronous cac_stream_push_host at a time.
+    host_mels = [w.step_mel[w.t + i].cpu().pin_memory() for i in range(E_WARM + 2 * Ke)]
+    outs = [(torch.empty(w.S, w.n, w.cfg.d_model).pin_memory(),
+             torch.empty(w.S, w.n, w.cfg.joint_dim).pin_memory()) for _ in range(2)]
+    w.host_out = outs[0]
     for i in range(E_WARM):
         w.step_host(host_mels[i])
     host_mels = host_mels[E_WARM:]
+    evs = [torch.cuda.Event(), torch.cuda.Event()]
+    out_np = [(e.numpy(), j.numpy()) for e, j in outs]  # host reads through numpy views of the pinned buffers
+    seen = float(out_np[0][1][:, -1, 0].sum())
     torch.cuda.synchronize()
     barrier()
     t0 = time.perf_counter()
     for i in range(Ke):
-        w.step_host(host_mels[i])
+        w.step_host_async(host_mels[i], outs[i % 2])
+        evs[i % 2].record()
+        if i:
+            evs[(i - 1) % 2].synchronize()
+            seen += float(out_np[(i - 1) % 2][1][:, -1, 0].sum())  # the host reads the step's joint frames
+    if Ke:
+        evs[(Ke - 1) % 2].synchronize()
+        seen += float(out_np[(Ke - 1) % 2][1][:, -1, 0].sum())
     e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(Ke):
+        w.step_host(host_mels[Ke + i])
+    e2e_sync_s = max_over_ranks(time.perf_counter() - t0, dev)
     e2e = None  # not measured with --e2e-steps 0
     if Ke:
         e2e = {"value": world * w.S * w.n * FRAME_SEC * Ke / e2e_s, "unit": UNIT,
                "h2d_bytes_per_step": w.S * w.push_mel * 128 * 4,
-               "d2h_bytes_per_step": w.S * w.n * (w.cfg.d_model + w.cfg.joint_dim) * 4}
+               "d2h_bytes_per_step": w.S * w.n * (w.cfg.d_model + w.cfg.joint_dim) * 4,
+               "mode": ("cac_stream_push_host_async: step k+1 queued before the host waits for and reads "
+                        "step k's frames (two page-locked output buffers); host wall time"),
+               "one_call_at_a_time": {"value": world * w.S * w.n * FRAME_SEC * Ke / e2e_sync_s, "unit": UNIT,
+                                      "what": "cac_stream_push_host, synchronous, the same number of steps"},
+               "finite": bool(np.isfinite(seen))}
     w.pool.check()
 
     decode = None

@@ -28,6 +28,7 @@ ERRORS = {-1: "CAC_E_INVAL", -2: "CAC_E_ALIGN", -3: "CAC_E_STATE", -4: "CAC_E_NO
 # every symbol include/cac.h declares
 SYMBOLS = ["cac_weights_size", "cac_model_create", "cac_model_create_palette", "cac_model_destroy", "cac_pool_create", "cac_pool_destroy",
            "cac_stream_create", "cac_stream_destroy", "cac_stream_reset", "cac_stream_push", "cac_stream_push_host",
+           "cac_stream_push_host_async",
            "cac_stream_flush", "cac_stream_flush_frames", "cac_encode_offline", "cac_stream_get_state",
            "cac_stream_set_state", "cac_pool_check", "cac_model_check", "cac_pool_set_graphs",
            "cac_pool_launch_count", "cac_pool_set_chains", "cac_pool_sub_batches", "cac_pool_check_guards",
@@ -90,6 +91,7 @@ def _lib():
             "cac_stream_reset": (c_int, [vp, c_int, ip, vp]),
             "cac_stream_push": (c_int, [vp, c_int, ip, vp, c_int, vp, vp, ip, vp]),
             "cac_stream_push_host": (c_int, [vp, c_int, ip, vp, c_int, vp, vp, ip, vp]),
+            "cac_stream_push_host_async": (c_int, [vp, c_int, ip, vp, c_int, vp, vp, ip, vp]),
             "cac_stream_flush": (c_int, [vp, c_int, ip, vp, c_int, ip, vp, vp, c_int, ip, vp]),
             "cac_stream_flush_frames": (c_int, [vp, c_int, c_int, ip]),
             "cac_encode_offline": (c_int, [vp, c_int, vp, ip, c_int, vp, vp, ip, vp]),
@@ -343,6 +345,24 @@ class Pool:
         _check(_lib().cac_stream_push_host(self.h, n, _ids(ids), mel_ptr, n_mel, addr(enc), addr(jt), n_out,
                                            _stream(stream)), "cac_stream_push_host")
         return enc, jt, list(n_out)
+
+    def push_host_async(self, ids, mel, out, stream=None):
+        """Queued host-buffer push (cac_stream_push_host_async).  mel: pinned CPU
+        torch tensor [n, n_mel, 128] float32; out: (enc, joint) pinned CPU
+        tensors to receive the frames (joint may be None).  Returns n_out; the
+        frames are in `out` once `stream` has passed this call's work, and
+        until then mel must not change nor `out` be read."""
+        ids = list(ids)
+        enc, jt = out
+        for t in (mel, enc, jt):
+            assert t is None or (t.dtype.is_floating_point and t.is_contiguous() and not t.is_cuda)
+        n, n_mel, _ = mel.shape
+        n_out = (c_int * n)()
+        _check(_lib().cac_stream_push_host_async(self.h, n, _ids(ids), c_void_p(mel.data_ptr()), n_mel,
+                                                 c_void_p(enc.data_ptr()) if enc is not None else None,
+                                                 c_void_p(jt.data_ptr()) if jt is not None else None, n_out,
+                                                 _stream(stream)), "cac_stream_push_host_async")
+        return list(n_out)
 
     def flush_frames(self, sid: int, n_mel: int) -> int:
         """Frames a flush of `n_mel` remaining mel frames emits for stream `sid`

@@ -174,6 +174,21 @@ int  cac_stream_push(cac_pool* p, int n, const int* ids, const float* mel, int n
 int  cac_stream_push_host(cac_pool* p, int n, const int* ids, const float* mel, int n_mel,
                           float* enc, float* joint, int* n_out, void* stream);
 
+/* Asynchronous form of cac_stream_push_host: queues the copy of mel in, the
+ * push and the copies of enc/joint out on `stream`, and returns without
+ * waiting for them.  mel, enc and joint (enc/joint may be NULL) must be
+ * page-locked host memory (cudaHostAlloc / cudaHostRegister); a pageable
+ * buffer returns CAC_E_INVAL before anything is queued.  Until `stream` has
+ * passed this call's work (cudaStreamSynchronize, or an event recorded on
+ * `stream` after the call), the caller must not modify mel nor read or reuse
+ * enc/joint.  n_out is written before the call returns.  A caller can thus
+ * queue push k+1 while push k runs and read push k's frames meanwhile, so the
+ * GPU does not idle while the host prepares the next chunk.  The first call
+ * (and one needing larger buffers than any before it) grows the pool's
+ * device staging and synchronizes `stream` to do so. */
+int  cac_stream_push_host_async(cac_pool* p, int n, const int* ids, const float* mel, int n_mel,
+                                float* enc, float* joint, int* n_out, void* stream);
+
 /* flush(): final partial chunk of each listed stream; afterwards the stream
  * needs cac_stream_reset before it can push again.
  *   mel        device [n][mel_stride][mel_bins]; stream b uses its first

@@ -275,6 +275,55 @@ def test_push_host_sub_batches_match_device_push():
         p.check()
 
 
+@pytest.mark.parametrize("S", [256, 16], ids=["sub_batches", "one_batch"])
+def test_push_host_async_pipelined_matches_device_push(S):
+    """Queued host-buffer pushes (cac_stream_push_host_async), each queued
+    before the host reads the previous one's frames from a second pair of
+    page-locked buffers, with resets queued between them: equal bit for bit
+    to device pushes of the same mel (graph replay on both pools), for a push
+    that runs as concurrent sub-batches (256 streams) and one that runs as one
+    batch (16).  Pageable buffers are refused before anything is queued."""
+    from cache_aware_conformer_gb300 import native
+    cfg = EOU2
+    _, model = make_model(cfg)
+    pools = [native.Pool(model, S, 2) for _ in range(2)]
+    for p in pools:
+        p.set_graphs(True)
+    ids = [[p.create_stream() for _ in range(S)] for p in pools]
+    steps = 6
+    mels = [np.stack([synth.make_mel(16, 7000 + 100 * step + s) for s in range(S)]) for step in range(steps)]
+    resets = {2: [0, S // 2, S - 1], 4: [1, 5]}
+    want = []
+    for step in range(steps):
+        pools[0].reset([ids[0][i] for i in resets.get(step, [])])
+        e0, j0, _ = _push(pools[0], ids[0], list(mels[step]))
+        want.append((e0, j0))
+    host_mel = [torch.from_numpy(m).pin_memory() for m in mels]
+    outs = [(torch.empty(S, 2, cfg.d_model).pin_memory(), torch.empty(S, 2, cfg.joint_dim).pin_memory())
+            for _ in range(2)]
+    evs = [torch.cuda.Event() for _ in range(2)]
+    for step in range(steps):
+        pools[1].reset([ids[1][i] for i in resets.get(step, [])])
+        n_out = pools[1].push_host_async(ids[1], host_mel[step], outs[step % 2])
+        assert n_out == [2] * S
+        evs[step % 2].record()
+        if step > 0:  # the previous push's frames, read while this one runs
+            evs[(step - 1) % 2].synchronize()
+            e, j = outs[(step - 1) % 2]
+            assert np.array_equal(e.numpy(), want[step - 1][0]), step - 1
+            assert np.array_equal(j.numpy(), want[step - 1][1]), step - 1
+    evs[(steps - 1) % 2].synchronize()
+    e, j = outs[(steps - 1) % 2]
+    assert np.array_equal(e.numpy(), want[-1][0]) and np.array_equal(j.numpy(), want[-1][1])
+    for bad in ((torch.from_numpy(mels[0]), outs[0]),
+                (host_mel[0], (torch.empty(S, 2, cfg.d_model), outs[0][1]))):
+        with pytest.raises(native.CacError) as err:
+            pools[1].push_host_async(ids[1], *bad)
+        assert err.value.code == -1
+    for p in pools:
+        p.check()
+
+
 def test_c600m_shape_multistream():
     """The 600M encoder's layer shapes (d_model 1024, 16 heads, ff 4096), two
     layers, three streams with 160 / 320 / 640 ms pushes and a ragged flush."""
