@@ -46,9 +46,9 @@ nearest-entry assignment by brute force; the k-means objective never
 increasing; the uniform distribution's optimal 64-level quantiser (centres
 (i + 1/2)/64, error 1/(12 * 64^2)); scikit-learn's KMeans objective on
 bell-shaped data; int8 bounds, extremes and half-even ties; which tensors change).
-Parity unpinned by the pages: table granularity, the k-means initialisation,
-the packing order and the int8 scheme are readings; only the 64-entry tables
-are the pages'.
+Readings that no page fixes (every function is still pinned above): table
+granularity, the k-means initialisation, the packing order and the int8
+scheme; only the 64-entry tables are the pages'.
 """
 from __future__ import annotations
 

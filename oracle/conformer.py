@@ -36,10 +36,10 @@ Readings where the pages are silent (each is listed in the design notes):
 Parity pins: every function here is checked by tests/test_oracle_pins.py against
 library routines (torch layer_norm / conv1d / glu / scaled-dot-product attention),
 closed forms, the relShift cross-check and the streaming == offline invariant.
-Parity unpinned by the pages: the readings above (subsampling form, block
-internals, score scale, positional encoding) and the synthetic initialisation
-are fixed by no page; the pins show that this module states them correctly,
-not that the pages' model used them.
+Readings that no page fixes (every function is still pinned above): the
+subsampling form, block internals, score scale, positional encoding and the
+synthetic initialisation; the pins show that this module states them
+correctly, not that the pages' model used them.
 """
 from __future__ import annotations
 

@@ -32,9 +32,9 @@ usual NeMo-style filterbank front end —
 Parity pins: tests/test_oracle_frontend_pins.py (torch.stft and scipy's lfilter
 as library references, the Slaney scale's closed forms, the triangles'
 partition of unity, pure tones, silence, the pages' 240,000 -> 1,501 frame
-count, and streamed == one-shot output).  Parity unpinned by the pages: the
-window, transform size, filter shape, log guard and pre-emphasis readings
-above are fixed by no page; the pins show they are stated correctly.
+count, and streamed == one-shot output).  Readings that no page fixes (every
+function is still pinned): the window, transform size, filter shape, log
+guard and pre-emphasis above; the pins show they are stated correctly.
 """
 from __future__ import annotations
 
