@@ -133,11 +133,17 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU baseline: the fp64 oracle on the host cores (spawned workers)
 # ---------------------------------------------------------------------------
-def _oracle_worker(conn, blob_path, cfg, sid, mel):
+def _oracle_worker(conn, blob_path, cfg, mel, push_mel):
+    """One oracle instance stepped on command: a stream pushing `push_mel` mel
+    frames per step (the provisional-tail encoder when the model has right
+    context), or, with push_mel 0, one offline window encoded per step."""
     os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
     from oracle import conformer as O
     blob = np.load(blob_path, mmap_mode="r")
-    enc = O.StreamingEncoder(synth.unpack_weights(cfg, blob), cfg)
+    W = O.weights_f64(synth.unpack_weights(cfg, blob))
+    enc = None
+    if push_mel:
+        enc = O.ProvisionalTailEncoder(W, cfg) if cfg.right_context > 0 else O.StreamingEncoder(W, cfg)
     k = 0
     conn.send("ready")
     while True:
@@ -145,15 +151,38 @@ def _oracle_worker(conn, blob_path, cfg, sid, mel):
         if cmd is None:
             break
         for _ in range(cmd):
-            enc.push(mel[16 * k: 16 * (k + 1)])
-            k += 1
+            if push_mel:
+                r = k % (mel.shape[0] // push_mel)  # an utterance shorter than the sample repeats
+                enc.push(mel[push_mel * r: push_mel * (r + 1)])
+                k += 1
+            else:
+                O.encode_offline(mel, W, cfg)
         conn.send("done")
 
 
-class OracleFarm:
-    """`cores` worker processes, one stream each, stepping 160 ms chunks on command."""
+def oracle_workers(blob, units: int) -> int:
+    """Workers of a bounded oracle sample: one per host core, at most one per
+    stream (or window) of the workload, and at most what half the host memory
+    holds (a worker keeps the weights in fp32 and in fp64)."""
+    n = max(1, min(cpu_cores(), units))
+    try:
+        mem = os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
+    except (ValueError, OSError, AttributeError):
+        return n
+    return max(1, min(n, int(mem // 2 // (12 * blob.size + (1 << 28)))))
 
-    def __init__(self, cfg, blob, cores: int, n_chunks: int):
+
+def workload_mel(wl, sid: int) -> np.ndarray:
+    """Stream (or window) `sid`'s mel as the GPU legs generate it."""
+    n = wl.offline_mel if wl.offline_batch else (int(round(wl.seconds * 100)) // wl.push_mel) * wl.push_mel
+    return synth.make_mel(n, sid, silence_frac=wl.silence_frac)
+
+
+class OracleFarm:
+    """One worker process per stream (or offline window) of a sample, each
+    stepping its own oracle instance on command."""
+
+    def __init__(self, cfg, blob, mels, push_mel: int):
         import multiprocessing as mp
         for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
             os.environ[v] = "1"
@@ -161,12 +190,11 @@ class OracleFarm:
         self.tmp = tempfile.mkdtemp(prefix="cac_oracle_")
         self.blob_path = os.path.join(self.tmp, "w.npy")
         np.save(self.blob_path, blob)
-        self.cores = cores
+        self.cores = len(mels)
         self.procs, self.conns = [], []
-        for c in range(cores):
+        for mel in mels:
             a, b = ctx.Pipe()
-            mel = synth.make_mel(16 * n_chunks, 100000 + c)
-            p = ctx.Process(target=_oracle_worker, args=(b, self.blob_path, cfg, c, mel), daemon=True)
+            p = ctx.Process(target=_oracle_worker, args=(b, self.blob_path, cfg, mel, push_mel), daemon=True)
             p.start()
             self.procs.append(p)
             self.conns.append(a)
@@ -449,12 +477,13 @@ def run_offline(args, wl):
                 "peak": tf_peak, "unit": "TFLOP/s", "frac": ach / tf_peak, "traffic": None,
                 "peak_source": f"{peak_src} (bf16 sustained)"}
     if rank == 0:
-        print(json.dumps({"metric": "offline encode audio-sec/sec (" + wl.name + ")", "value": value, "unit": UNIT,
+        cpu = cpu_baseline(wl, w.blob, 1) if world == 1 and not args.no_cpu_baseline else None
+        print(json.dumps({"metric": workload_metric(wl), "value": value, "unit": UNIT,
                           "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": ms / K, "higher_is_better": True,
                           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                           "config": {"workload": wl.name, "windows": w.B, "mel_frames": w.T, "frames": w.T3,
                                      "layers": L, "d_model": D, "parallelism": f"replicas x{world}"},
-                          "roofline": roofline, "cpu_baseline": None, "e2e": e2e, "gpu_launches": None,
+                          "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": None,
                           "clocks": clk}), flush=True)
 
 
@@ -632,7 +661,7 @@ def run_ours(args, wl):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w.cfg, w.blob, args.cpu_chunks)
+        cpu = cpu_baseline(wl, w.blob, args.cpu_chunks)
     if rank == 0:
         line = {"metric": workload_metric(wl),
                 "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": Wm,
@@ -825,24 +854,39 @@ def measure_beam(S: int, Kb: int, dev, beam: int = 8):
                              "search and are not counted on the device"}
 
 
-def cpu_baseline(cfg, blob, chunks: int):
-    """The oracle as it stands, one stream per host core, `chunks` pushes each."""
-    cores = cpu_cores()
-    farm = OracleFarm(cfg, blob, cores, 2 * chunks + 1)
+def cpu_baseline(wl, blob, chunks: int):
+    """The oracle as it stands on a bounded sample of the workload: streams
+    0 .. C-1 (one per host core), `chunks` pushes each after an untimed first
+    one; offline workloads: windows 0 .. C-1, `chunks` encodes each."""
+    cfg = wl.model
+    units = wl.offline_batch or wl.streams
+    n = oracle_workers(blob, units)
+    farm = OracleFarm(cfg, blob, [workload_mel(wl, sid) for sid in range(n)], 0 if wl.offline_batch else wl.push_mel)
     try:
-        farm.step(1)                      # first push (stream start) untimed
+        if not wl.offline_batch:
+            farm.step(1)                  # first push (stream start) untimed
         secs = farm.step(chunks)
-        one = farm.step_one(chunks)       # the same stream length on one core, the others idle
+        one = farm.step_one(chunks)       # the same work on one core, the others idle
     finally:
         farm.close()
-    return {"value": cores * chunks * 0.16 / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{cores} streams x {chunks} pushes of 160 ms (one stream per core, fp64 numpy, "
-                      f"17-layer model); {secs:.1f} s wall",
-            "single_core": {"value": chunks * 0.16 / one, "unit": UNIT, "cores": 1,
-                            "sample": f"1 stream x {chunks} pushes of 160 ms; {one:.1f} s wall"}}
+    what = f"{cfg.n_layers}-layer d_model-{cfg.d_model} model, fp64 numpy"
+    if wl.offline_batch:
+        sec = wl.offline_mel * 0.01
+        sample = f"windows 0..{n - 1} of {units} x {chunks} offline encodes of {wl.offline_mel} mel frames"
+        sample1 = f"1 window x {chunks} offline encodes"
+    else:
+        sec = wl.push_mel * 0.01
+        sample = f"streams 0..{n - 1} of {units} x {chunks} pushes of {10 * wl.push_mel} ms"
+        sample1 = f"1 stream x {chunks} pushes of {10 * wl.push_mel} ms"
+    return {"value": n * chunks * sec / secs, "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": f"{sample} (one per core, {what}); {secs:.1f} s wall",
+            "single_core": {"value": chunks * sec / one, "unit": UNIT, "cores": 1,
+                            "sample": f"{sample1}; {one:.1f} s wall"}}
 
 
 def workload_metric(wl) -> str:
+    if wl.offline_batch:
+        return f"offline encode audio-sec/sec ({wl.name})"
     return METRIC if wl.name == "eou120m_256streams_60s" else f"streamed audio-sec/sec ({wl.name})"
 
 
@@ -860,8 +904,9 @@ def workload_config(wl, world: int) -> dict:
 
 
 def run_reference(args, wl):
-    """Reference arm: the fp64 oracle itself on the host cores, same metric and config.
-    Each step = one 160 ms push of a sample of streams (one per core)."""
+    """Reference arm: the fp64 oracle itself on the host cores, same metric and
+    config.  Each step = one push of a sample of the workload's streams (one per
+    core); offline workloads: one encode of a sample of its windows."""
     rank, _, world = dist_env()
     if rank != 0:
         return
@@ -869,21 +914,31 @@ def run_reference(args, wl):
     W = synth.make_weights_parallel(cfg, seed=0, workers=cpu_cores())
     blob = synth.pack_weights(cfg, W)
     del W
-    cores = cpu_cores()
-    K, Wm = min(args.steps, args.ref_steps), min(args.warmup, 3)
-    farm = OracleFarm(cfg, blob, cores, Wm + K + 1)
+    units = wl.offline_batch or wl.streams
+    n = oracle_workers(blob, units)
+    if wl.offline_batch:  # a window is seconds of fp64 work: fewer steps
+        K, Wm = min(args.steps, args.ref_steps, 2), 1
+    else:
+        K, Wm = min(args.steps, args.ref_steps), min(args.warmup, 3)
+    farm = OracleFarm(cfg, blob, [workload_mel(wl, sid) for sid in range(n)], 0 if wl.offline_batch else wl.push_mel)
     try:
-        farm.step(1 + Wm)
+        farm.step(Wm if wl.offline_batch else 1 + Wm)
         secs = farm.step(K)
     finally:
         farm.close()
-    value = cores * K * 0.16 / secs
+    sec = (wl.offline_mel if wl.offline_batch else wl.push_mel) * 0.01
+    value = n * K * sec / secs
+    unit_name = "windows" if wl.offline_batch else "streams"
+    step_name = "offline encodes" if wl.offline_batch else f"pushes of {10 * wl.push_mel} ms"
+    config = (dict(workload=wl.name, windows=wl.offline_batch, mel_frames=wl.offline_mel, layers=cfg.n_layers,
+                   d_model=cfg.d_model, parallelism=f"replicas x{world}") if wl.offline_batch
+              else workload_config(wl, world))
     line = {"impl": "reference", "metric": workload_metric(wl), "value": value, "unit": UNIT, "n_gpus": world,
             "steps": K, "warmup": Wm, "ms_per_step": 1e3 * secs / K, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": dict(workload_config(wl, world), streams_sampled=cores),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{cores} of {wl.streams} streams, {K} pushes of 160 ms each"},
+            "config": dict(config, **{f"{unit_name}_sampled": n}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": n, "kind": "oracle",
+                             "sample": f"{unit_name} 0..{n - 1} of {units}, {K} {step_name} each"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
