@@ -203,6 +203,56 @@ def test_rel_pos_attention_matches_relshift_plus_sdpa():
 # lengths and receptive field
 # ---------------------------------------------------------------------------
 
+def test_offline_encoder_matches_torch_composition():
+    """The whole offline encode against the same network written with torch
+    primitives: subsampling (three causal stride-2 conv1d + ReLU, then the
+    linear), every layer as FF1 (half residual) -> attention -> conv module ->
+    FF2 (half residual) -> ln_out, then the joint projection.  Attention is
+    textbook multi-head softmax attention here (position terms zero, a context
+    and chunk covering the sequence), so any slip in module order, residual
+    weight, LayerNorm placement or a weight's role fails."""
+    cfg = tiny(att_left=1000, att_chunk=64)
+    W = weights(cfg, 3)
+    for l in range(cfg.n_layers):
+        for n in ("wpos", "pbu", "pbv"):
+            W[f"l{l}.att.{n}"] = np.zeros_like(W[f"l{l}.att.{n}"])
+    mel = synth.make_mel(200, 5)                                   # 25 frames, all in one chunk
+    enc, joint = O.encode_offline(mel, W, cfg)
+    t = {k: torch.tensor(v) for k, v in W.items()}
+    D, H, kk = cfg.d_model, cfg.n_heads, cfg.dw_kernel
+    hd = D // H
+    y = torch.tensor(mel, dtype=T64)
+    for st in (1, 2, 3):                                            # weights stored [out][tap][in]
+        y = F.relu(F.conv1d(F.pad(y.T[None], (2, 0)), t[f"sub.w{st}"].permute(0, 2, 1), t[f"sub.b{st}"],
+                            stride=2)[0].T)
+    x = F.linear(y, t["sub.wo"], t["sub.bo"])
+
+    def ln(v, p):
+        return F.layer_norm(v, (D,), t[p + "ln_g"], t[p + "ln_b"], eps=1e-5)
+
+    def ff(v, p):
+        return v + 0.5 * F.linear(F.silu(F.linear(ln(v, p), t[p + "w1"], t[p + "b1"])), t[p + "w2"], t[p + "b2"])
+
+    for l in range(cfg.n_layers):
+        p = f"l{l}."
+        x = ff(x, p + "ff1.")
+        a = ln(x, p + "att.")
+        q, k, v = (F.linear(a, t[p + f"att.w{c}"], t[p + f"att.b{c}"]).view(-1, H, hd).transpose(0, 1)
+                   for c in "qkv")
+        o = F.scaled_dot_product_attention(q[None], k[None], v[None])[0].transpose(0, 1).reshape(-1, D)
+        x = x + F.linear(o, t[p + "att.wo"], t[p + "att.bo"])
+        g = F.glu(F.linear(ln(x, p + "conv."), t[p + "conv.w_pw1"], t[p + "conv.b_pw1"]), dim=-1)
+        dw = F.conv1d(F.pad(g.T[None], (kk - 1, 0)), t[p + "conv.w_dw"][:, None, :], t[p + "conv.b_dw"],
+                      groups=D)[0].T
+        x = x + F.linear(F.silu(t[p + "conv.bn_g"] * dw + t[p + "conv.bn_b"]), t[p + "conv.w_pw2"],
+                         t[p + "conv.b_pw2"])
+        x = ff(x, p + "ff2.")
+        x = ln(x, p + "out.")
+    assert enc.shape == (25, D)
+    np.testing.assert_allclose(enc, x.numpy(), rtol=0, atol=1e-10)
+    np.testing.assert_allclose(joint, F.linear(x, t["joint.w"], t["joint.b"]).numpy(), rtol=0, atol=1e-10)
+
+
 def test_length_arithmetic():
     fw = GOLDEN["offline_window"]
     assert O.subsampled_len(fw["mel"]) == fw["frames"]
