@@ -41,6 +41,55 @@ def test_lstm_cell_matches_torch_lstmcell():
     np.testing.assert_allclose(c2, tc[0].numpy(), rtol=0, atol=2e-6)
 
 
+class TorchScorer:
+    """The predictor + joint as torch modules in fp64: embedding, LSTM cell,
+    predictor projection, ReLU joint, primed by one step on the blank token from
+    zero state; the oracle's greedy loop drives it."""
+
+    def __init__(self, z, W, dc):
+        P, J, C = dc.pred_dim, dc.joint_dim, W["out.w"].shape[0]
+        t = {k: torch.from_numpy(np.asarray(v, np.float64)) for k, v in W.items()}
+        self.emb = torch.nn.Embedding.from_pretrained(t["emb"])
+        self.cell = torch.nn.LSTMCell(P, P, dtype=torch.float64)
+        self.pred = torch.nn.Linear(P, J, dtype=torch.float64)
+        self.out = torch.nn.Linear(J, C, dtype=torch.float64)
+        with torch.no_grad():
+            for mod, pairs in ((self.cell, (("weight_ih", "lstm.w_ih"), ("weight_hh", "lstm.w_hh"),
+                                            ("bias_ih", "lstm.b_ih"), ("bias_hh", "lstm.b_hh"))),
+                               (self.pred, (("weight", "pred.w"), ("bias", "pred.b"))),
+                               (self.out, (("weight", "out.w"), ("bias", "out.b")))):
+                for attr, name in pairs:
+                    getattr(mod, attr).copy_(t[name])
+        self.z = torch.from_numpy(np.asarray(z, np.float64))
+        zero = torch.zeros(1, P, dtype=torch.float64)
+        self.hc = (zero, zero)
+        self.advance(dc.blank)
+
+    @torch.no_grad()
+    def logits(self, t):
+        return self.out(torch.relu(self.z[t] + self.p[0])).numpy()
+
+    @torch.no_grad()
+    def advance(self, k):
+        self.hc = self.cell(self.emb(torch.tensor([k])), self.hc)
+        self.p = self.pred(self.hc[0])
+
+
+def test_predictor_and_joint_match_torch_modules():
+    """The oracle's scorer (primed state, token embedding, LSTM step, predictor
+    projection, joint) decides like the same network built from torch modules
+    in fp64, emission for emission, and ends in the same LSTM state."""
+    dc = replace(TINY_DECODER, blank_bias=2.0)  # a few dozen emissions over 24 frames
+    W = _weights(dc, seed=4)
+    z = synth.make_joint_frames(24, 7, dc.joint_dim)
+    em, st = O.decode_chunk(z, O.DecoderState.fresh(W, dc), W, dc)
+    ref = TorchScorer(z, W, dc)
+    em_ref = O.greedy_rnnt(24, ref, dc.blank, dc.max_symbols)
+    assert len(em) > 20 and len({k for _, k in em}) > 2 and em == em_ref
+    np.testing.assert_allclose(st.h, ref.hc[0][0].numpy(), rtol=0, atol=1e-5)
+    np.testing.assert_allclose(st.c, ref.hc[1][0].numpy(), rtol=0, atol=1e-5)
+
+
 def test_lstm_cell_closed_form_with_zero_weights():
     """With zero matrices the gates are the biases: c' = s(b_f) c + s(b_i) tanh(b_g),
     h' = s(b_o) tanh(c'), s the logistic function (written out in float64 here)."""
