@@ -172,3 +172,25 @@ def test_streamed_beam_equals_the_whole_utterance(chunks):
         got_best, got_finals = st.flush()
         assert got_best == best
         assert [f and (f[0], float(f[1])) for f in got_finals] == [f and (f[0], float(f[1])) for f in finals]
+
+
+def test_logsumexp_and_log_softmax_match_library_routines():
+    """The fp32 log-sum-exp used by recombination against numpy's logaddexp
+    (with -inf members and an all -inf set), and the scorer's log-softmax
+    against torch.log_softmax of the same joint logits."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(11)
+    for xs in (rng.normal(size=7) * 5, np.array([0.3, NEG, -2.0, NEG]), np.array([80.0, 79.5, -300.0])):
+        ref = np.logaddexp.reduce(xs.astype(np.float32).astype(np.float64))
+        assert abs(float(B.logsumexp32(xs)) - ref) < 1e-5 * max(1.0, abs(ref))
+    assert B.logsumexp32([NEG, NEG]) == NEG
+    dc = TINY_DECODER
+    W = synth.make_decoder_weights(dc, 2)
+    z = synth.make_joint_frames(3, 5, dc.joint_dim)
+    sc = B.PredictorScorer(z, W, dc)
+    st = sc.advance(sc.init_state(), 4)
+    for t in range(3):
+        lp = sc.log_probs(t, st)
+        ref = torch.log_softmax(torch.from_numpy(D.joint_logits(z[t], st.p, W).astype(np.float64)), 0).numpy()
+        np.testing.assert_allclose(lp, ref, rtol=0, atol=2e-5)
+        assert abs(float(np.exp(lp.astype(np.float64)).sum()) - 1.0) < 1e-5
