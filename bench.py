@@ -477,7 +477,12 @@ def run_offline(args, wl):
                 "peak": tf_peak, "unit": "TFLOP/s", "frac": ach / tf_peak, "traffic": None,
                 "peak_source": f"{peak_src} (bf16 sustained)"}
     if rank == 0:
-        cpu = cpu_baseline(wl, w.blob, 1) if world == 1 and not args.no_cpu_baseline else None
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            try:
+                cpu = cpu_baseline(wl, w.blob, 1)
+            except Exception as exc:  # reported beside the GPU figures, never instead of them
+                cpu = {"error": f"{type(exc).__name__}: {exc}"[:300], "kind": "oracle"}
         print(json.dumps({"metric": workload_metric(wl), "value": value, "unit": UNIT,
                           "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": ms / K, "higher_is_better": True,
                           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -661,7 +666,10 @@ def run_ours(args, wl):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, w.blob, args.cpu_chunks)
+        try:
+            cpu = cpu_baseline(wl, w.blob, args.cpu_chunks)
+        except Exception as exc:  # reported beside the GPU figures, never instead of them
+            cpu = {"error": f"{type(exc).__name__}: {exc}"[:300], "kind": "oracle"}
     if rank == 0:
         line = {"metric": workload_metric(wl),
                 "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": Wm,
