@@ -38,6 +38,7 @@
 #include "cac.h"
 #include "cac_beam.h"
 #include "common.cuh"
+#include "status.cuh"
 
 namespace cac {
 namespace {
@@ -771,7 +772,7 @@ struct cac_beam {
 namespace {
 
 int balloc(cac_beam* d, size_t bytes, void** out) {
-    if (cudaMalloc(out, bytes < 16 ? 16 : bytes) != cudaSuccess) return CAC_E_NOMEM;
+    if (cudaMalloc(out, bytes < 16 ? 16 : bytes) != cudaSuccess) return cac::nomem();
     d->allocs.push_back(*out);
     return CAC_OK;
 }
@@ -924,7 +925,7 @@ extern "C" int cac_beam_create(const cac_dec_config* cfg, const float* weights, 
         return fail(CAC_E_CUDA);
     if (cudaMallocHost(reinterpret_cast<void**>(&d->pinned), sizeof(int) * 3 * S * BEAM_ID_SLOTS) != cudaSuccess ||
         cudaMallocHost(reinterpret_cast<void**>(&d->h_pending), sizeof(int)) != cudaSuccess)
-        return fail(CAC_E_NOMEM);
+        return fail(cac::nomem());
     for (auto& e : d->ev)
         if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return fail(CAC_E_CUDA);
     const size_t Kd = P > J ? P : J;

@@ -51,6 +51,7 @@
 #include "cac.h"
 #include "cac_decode.h"
 #include "common.cuh"
+#include "status.cuh"
 
 namespace cac {
 namespace {
@@ -747,7 +748,7 @@ struct cac_decoder {
 namespace {
 
 int dalloc(cac_decoder* d, size_t bytes, void** out) {
-    if (cudaMalloc(out, bytes) != cudaSuccess) return CAC_E_NOMEM;
+    if (cudaMalloc(out, bytes) != cudaSuccess) return cac::nomem();
     d->allocs.push_back(*out);
     return CAC_OK;
 }
@@ -838,7 +839,7 @@ extern "C" int cac_decoder_create(const cac_dec_config* cfg, const float* weight
         cudaMemset(d->p, 0, S * J * 4) != cudaSuccess)
         return fail(CAC_E_CUDA);
     if (cudaMallocHost(reinterpret_cast<void**>(&d->pinned), sizeof(int) * S * ID_SLOTS) != cudaSuccess)
-        return fail(CAC_E_NOMEM);
+        return fail(cac::nomem());
     for (auto& e : d->slot_ev)
         if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return fail(CAC_E_CUDA);
     // one CTA per SM, all co-resident (cooperative launch).  Shared memory:
@@ -972,7 +973,7 @@ extern "C" int cac_op_wait_selftest(int which, void* stream) {
     if (which != 0 && which != 1) return CAC_E_INVAL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int* buf = nullptr;  // [0] status, [1] abort, [2..3] barrier words
-    if (cudaMalloc(&buf, 4 * sizeof(int)) != cudaSuccess) return CAC_E_NOMEM;
+    if (cudaMalloc(&buf, 4 * sizeof(int)) != cudaSuccess) return cac::nomem();
     int rc = CAC_E_CUDA;
     if (cudaMemsetAsync(buf, 0, 4 * sizeof(int), s) == cudaSuccess) {
         cudaError_t e;

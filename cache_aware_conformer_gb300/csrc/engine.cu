@@ -19,6 +19,7 @@
 #include "chain.cuh"
 #include "gemm.cuh"
 #include "kernels.cuh"
+#include "status.cuh"
 
 using namespace cac;
 
@@ -119,7 +120,7 @@ namespace {
 
 int dalloc(cac_model* m, size_t bytes, void** out) {
     void* p = nullptr;
-    if (cudaMalloc(&p, std::max<size_t>(bytes, 16)) != cudaSuccess) return CAC_E_NOMEM;
+    if (cudaMalloc(&p, std::max<size_t>(bytes, 16)) != cudaSuccess) return nomem();
     m->allocs.push_back(p);
     *out = p;
     return CAC_OK;
@@ -394,7 +395,7 @@ int chain_flush(ChainRec* r, cudaStream_t s) {
             if (r->ctl.ws) cudaFree(r->ctl.ws);
             r->ctl.ws = nullptr;
             r->ws_floats = 0;
-            if (cudaMalloc(&r->ctl.ws, sizeof(float) * ws) != cudaSuccess) return CAC_E_NOMEM;
+            if (cudaMalloc(&r->ctl.ws, sizeof(float) * ws) != cudaSuccess) return nomem();
             r->ws_floats = ws;
         }
         if (tc > r->tcnt_n) {
@@ -402,14 +403,14 @@ int chain_flush(ChainRec* r, cudaStream_t s) {
             if (r->ctl.tcnt) cudaFree(r->ctl.tcnt);
             r->ctl.tcnt = nullptr;
             r->tcnt_n = 0;
-            if (cudaMalloc(&r->ctl.tcnt, sizeof(int) * tc) != cudaSuccess) return CAC_E_NOMEM;
+            if (cudaMalloc(&r->ctl.tcnt, sizeof(int) * tc) != cudaSuccess) return nomem();
             CK(cudaMemset(r->ctl.tcnt, 0, sizeof(int) * tc));
             r->tcnt_n = tc;
         }
         ChainProg prog;
         prog.n = (int)r->ph.size();
         prog.M = r->M;
-        if (cudaMalloc(&prog.d, sizeof(ChainPhase) * prog.n) != cudaSuccess) return CAC_E_NOMEM;
+        if (cudaMalloc(&prog.d, sizeof(ChainPhase) * prog.n) != cudaSuccess) return nomem();
         CK(cudaMemcpy(prog.d, r->ph.data(), sizeof(ChainPhase) * prog.n, cudaMemcpyHostToDevice));
         if (it != r->cache.end() && it->second.d) {
             CK(cudaStreamSynchronize(s));
@@ -911,7 +912,7 @@ constexpr size_t GUARD_BYTES = 4096;
 int palloc_guarded(cac_pool* p, size_t bytes, void** out) {
     char* d = nullptr;
     const size_t total = bytes + 2 * GUARD_BYTES;
-    if (cudaMalloc(&d, total) != cudaSuccess) return CAC_E_NOMEM;
+    if (cudaMalloc(&d, total) != cudaSuccess) return nomem();
     p->allocs.push_back(d);
     if (cudaMemset(d, 0, total) != cudaSuccess || cudaMemset(d, 0xFF, GUARD_BYTES) != cudaSuccess ||
         cudaMemset(d + GUARD_BYTES + bytes, 0xFF, GUARD_BYTES) != cudaSuccess)
@@ -924,7 +925,7 @@ int palloc_guarded(cac_pool* p, size_t bytes, void** out) {
 
 int palloc(cac_pool* p, size_t bytes, void** out, bool zero = true) {
     void* d = nullptr;
-    if (cudaMalloc(&d, std::max<size_t>(bytes, 16)) != cudaSuccess) return CAC_E_NOMEM;
+    if (cudaMalloc(&d, std::max<size_t>(bytes, 16)) != cudaSuccess) return nomem();
     p->allocs.push_back(d);
     if (zero && cudaMemset(d, 0, std::max<size_t>(bytes, 16)) != cudaSuccess) return CAC_E_CUDA;
     *out = d;
@@ -1552,7 +1553,7 @@ extern "C" int cac_pool_create(cac_model* m, int max_streams, int max_frames_per
     }
     if (cudaHostAlloc(reinterpret_cast<void**>(&p->pinned), sizeof(int) * S * ID_SLOTS, cudaHostAllocDefault) !=
         cudaSuccess)
-        return fail(CAC_E_NOMEM);
+        return fail(nomem());
     for (int k = 0; k < ID_SLOTS; ++k)
         if (cudaEventCreateWithFlags(&p->slot_ev[k], cudaEventDisableTiming) != cudaSuccess) return fail(CAC_E_CUDA);
     p->alive.assign(S, 0);
@@ -1823,7 +1824,7 @@ int push_host_impl(cac_pool* p, int n, const int* ids, const float* mel, int n_m
         p->h_mel_cap = 0;
         if (cudaHostAlloc(reinterpret_cast<void**>(&p->h_mel), mel_n * 4, cudaHostAllocDefault) != cudaSuccess ||
             cudaMalloc(&p->d_mel, mel_n * 4) != cudaSuccess)
-            return CAC_E_NOMEM;
+            return nomem();
         p->h_mel_cap = mel_n;
     }
     if (enc_n + joint_n > p->h_out_cap) {
@@ -1836,7 +1837,7 @@ int push_host_impl(cac_pool* p, int n, const int* ids, const float* mel, int n_m
         if (cudaHostAlloc(reinterpret_cast<void**>(&p->h_out), (enc_n + joint_n) * 4, cudaHostAllocDefault) !=
                 cudaSuccess ||
             cudaMalloc(&p->d_out, (enc_n + joint_n) * 4) != cudaSuccess)
-            return CAC_E_NOMEM;
+            return nomem();
         p->h_out_cap = enc_n + joint_n;
     }
     // page-locked caller buffers are copied directly, pageable ones staged
@@ -2141,7 +2142,7 @@ extern "C" int cac_encode_offline(cac_model* m, int B, const float* mel, const i
         if (m->ws.base) cudaFree(m->ws.base);
         m->ws.base = nullptr;
         m->ws.bytes = 0;
-        if (cudaMalloc(&m->ws.base, lay.bytes) != cudaSuccess) return CAC_E_NOMEM;
+        if (cudaMalloc(&m->ws.base, lay.bytes) != cudaSuccess) return nomem();
         CK(cudaMemset(m->ws.base, 0, lay.bytes));
         m->ws.bytes = lay.bytes;
     }
@@ -2392,7 +2393,7 @@ extern "C" int cac_pool_set_trace(cac_pool* p, int enable) {
     if (!p) return CAC_E_INVAL;
     if (enable && !p->trace_buf) {
         const size_t n = ((size_t)p->m->L * N_TAPS + 1) * p->trace_rows * p->m->D;
-        if (cudaMalloc(reinterpret_cast<void**>(&p->trace_buf), n * 4) != cudaSuccess) return CAC_E_NOMEM;
+        if (cudaMalloc(reinterpret_cast<void**>(&p->trace_buf), n * 4) != cudaSuccess) return nomem();
         CK(cudaMemset(p->trace_buf, 0, n * 4));
     }
     p->trace = enable != 0;

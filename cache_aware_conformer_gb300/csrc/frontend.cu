@@ -26,6 +26,7 @@
 
 #include "cac.h"
 #include "cac_frontend.h"
+#include "status.cuh"
 
 namespace {
 
@@ -281,7 +282,7 @@ extern "C" int cac_frontend_create(int max_streams, cac_frontend** out) {
                             cudaHostAllocDefault) == cudaSuccess;
     if (!ok) {
         cac_frontend_destroy(fe);
-        return CAC_E_NOMEM;
+        return cac::nomem();
     }
     ok = cudaMemcpy(fe->win, T.win.data(), sizeof(float) * NFFT, cudaMemcpyHostToDevice) == cudaSuccess &&
          cudaMemcpy(fe->tw, T.tw.data(), sizeof(float2) * NFFT / 2, cudaMemcpyHostToDevice) == cudaSuccess &&

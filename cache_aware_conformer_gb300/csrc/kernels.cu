@@ -5,6 +5,7 @@
 #include <cfloat>
 
 #include "kernels.cuh"
+#include "status.cuh"
 
 namespace cac {
 
@@ -997,10 +998,10 @@ extern "C" int cac_op_bounds_selftest(void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float* buf = nullptr;
     int* st = nullptr;
-    if (cudaMalloc(&buf, 32 * sizeof(float)) != cudaSuccess) return CAC_E_NOMEM;
+    if (cudaMalloc(&buf, 32 * sizeof(float)) != cudaSuccess) return cac::nomem();
     if (cudaMalloc(&st, sizeof(int)) != cudaSuccess) {
         cudaFree(buf);
-        return CAC_E_NOMEM;
+        return cac::nomem();
     }
     int h = CAC_E_CUDA;
     if (cudaMemsetAsync(st, 0, sizeof(int), s) == cudaSuccess) {

@@ -230,6 +230,36 @@ def test_errors_are_reported():
     pool.check()
 
 
+def test_pool_exhaustion_and_a_refused_allocation_leave_the_library_usable():
+    """Faults injected on the host: a pool hands out at most max_streams ids
+    (CAC_E_NOMEM after that, a destroyed id is handed out again), and a pool
+    larger than the device's memory is refused with CAC_E_NOMEM; afterwards
+    pushes on the existing pool run and report no error (the refused
+    allocation leaves no error behind for the next launch check)."""
+    from cache_aware_conformer_gb300 import native
+    cfg = EOU2
+    W, model = make_model(cfg)
+    pool = native.Pool(model, 2, 8)
+    a, b = pool.create_stream(), pool.create_stream()
+    with pytest.raises(native.CacError) as e:
+        pool.create_stream()
+    assert e.value.code == -4
+    pool.destroy_stream(b)
+    assert pool.create_stream() == b
+    # 2,000,000 streams of this model: 328 GB for each of the K and V rings
+    with pytest.raises(native.CacError) as e:
+        native.Pool(model, 2_000_000, 8)
+    assert e.value.code == -4
+    mel = synth.make_mel(32, 4)
+    enc, _, n_out = _push(pool, [a, b], [mel, mel])
+    pool.check()
+    model.check()
+    ref = O.StreamingEncoder(W, cfg)
+    e_ref, _ = ref.push(mel)
+    assert n_out == [4, 4] and np.array_equal(enc[0], enc[1])
+    assert_close(enc[0], e_ref, cfg, "after a refused pool")
+
+
 def test_push_host_matches_device_push():
     from cache_aware_conformer_gb300 import native
     cfg = EOU2
